@@ -1,0 +1,198 @@
+/*
+ * fw_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, sequential fp64 CPU statement of the delta-rule fast-weight
+ * layer core with the DPFP feature map.  Only the tests, the smoke check and
+ * the benchmark's CPU-baseline leg may load this code; the product path never
+ * does.  It shares no code, header or table with the CUDA library.
+ *
+ * Sources (all on the Fast Weights Transformer guide, xdnf.cn/news/308600,
+ * a walk-through of "Linear Transformers Are Secretly Fast Weight Memory
+ * Systems", arXiv:2102.11174):
+ *   - section "DPFP: projection formula and hyper-parameters": the feature
+ *     map phi over ReLU([k,-k]) and its cyclic shifts, output size
+ *     2*d_key*nu, nu in 1..2*d_key-1;
+ *   - section "normalisation" and the DPFP source listed with it: phi is
+ *     divided by (sum of its entries + eps), eps = 1e-6 by default, and the
+ *     shift is torch.roll(shifts=i), i.e. the rolled vector at position j
+ *     holds x[(j - i) mod 2*d_key];
+ *   - section "FastWeightsAttention: the new update rule": retrieve
+ *     vbar = W_{i-1} phi(k_i), write W_i = W_{i-1} + beta_i (v_i - vbar)
+ *     outer phi(k_i), read y_i = W_i phi(q_i) with the updated W;
+ *   - section "forward pass", the loop over steps: W starts at zero with
+ *     shape [batch, heads, d_value, d_dot] and phi is applied to query and
+ *     key, not to value;
+ *   - section "token_wise variant": one token at a time against a W that
+ *     persists across calls (the decode step).
+ *
+ * Every routine below follows those steps in that order, one token at a time,
+ * with no blocking, fusion or reordering.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define FWO_OK 0
+#define FWO_BAD_ARG 1
+
+/* DPFP of one vector k (length d_key) into phi (length 2*d_key*nu).
+ * x = ReLU([k, -k]); phi[(i-1)*2*d_key + j] = x[j] * x[(j - i) mod 2*d_key]
+ * for i = 1..nu and j = 0..2*d_key-1; then phi /= (sum(phi) + eps).
+ * x is a caller-provided scratch of length 2*d_key. */
+static void dpfp_one(const double *k, double *phi, double *x, int d_key, int nu, double eps)
+{
+    const int n = 2 * d_key;
+    for (int j = 0; j < d_key; ++j) {
+        x[j] = k[j] > 0.0 ? k[j] : 0.0;
+        x[d_key + j] = -k[j] > 0.0 ? -k[j] : 0.0;
+    }
+    double s = 0.0;
+    for (int i = 1; i <= nu; ++i) {
+        for (int j = 0; j < n; ++j) {
+            int src = ((j - i) % n + n) % n;
+            double p = x[j] * x[src];
+            phi[(size_t)(i - 1) * n + j] = p;
+            s += p;
+        }
+    }
+    const int d_dot = n * nu;
+    for (int m = 0; m < d_dot; ++m)
+        phi[m] = phi[m] / (s + eps);
+}
+
+int fwo_dpfp(const double *x, double *phi, int64_t rows, int d_key, int nu, double eps)
+{
+    if (!x || !phi || rows < 0 || d_key <= 0 || nu < 1 || nu > 2 * d_key - 1)
+        return FWO_BAD_ARG;
+    const int d_dot = 2 * d_key * nu;
+    double *scratch = (double *)malloc(sizeof(double) * 2 * (size_t)d_key);
+    if (!scratch)
+        return FWO_BAD_ARG;
+    for (int64_t r = 0; r < rows; ++r)
+        dpfp_one(x + r * d_key, phi + r * d_dot, scratch, d_key, nu, eps);
+    free(scratch);
+    return FWO_OK;
+}
+
+/* ---------------------------------------------------------------------- */
+/* The recurrence for one (batch, head) pair over L tokens.               */
+/*   q, k: [L, d_key]; v, y: [L, d_v]; beta: [L]; W: [d_v, d_dot] in/out.  */
+/* ---------------------------------------------------------------------- */
+static void recurrence_one(const double *q, const double *k, const double *v, const double *beta,
+                           double *W, double *y, int64_t L, int d_key, int nu, int d_v, double eps)
+{
+    const int d_dot = 2 * d_key * nu;
+    double *pk = (double *)malloc(sizeof(double) * d_dot);
+    double *pq = (double *)malloc(sizeof(double) * d_dot);
+    double *x = (double *)malloc(sizeof(double) * 2 * d_key);
+    double *vbar = (double *)malloc(sizeof(double) * d_v);
+    for (int64_t t = 0; t < L; ++t) {
+        /* phi is applied to the key and the query of this step */
+        dpfp_one(k + t * d_key, pk, x, d_key, nu, eps);
+        dpfp_one(q + t * d_key, pq, x, d_key, nu, eps);
+        /* retrieve: vbar = W_{t-1} phi(k_t) */
+        for (int r = 0; r < d_v; ++r) {
+            double acc = 0.0;
+            for (int m = 0; m < d_dot; ++m)
+                acc += W[(size_t)r * d_dot + m] * pk[m];
+            vbar[r] = acc;
+        }
+        /* write: W_t = W_{t-1} + beta_t (v_t - vbar) outer phi(k_t) */
+        for (int r = 0; r < d_v; ++r) {
+            double u = beta[t] * (v[t * d_v + r] - vbar[r]);
+            for (int m = 0; m < d_dot; ++m)
+                W[(size_t)r * d_dot + m] += u * pk[m];
+        }
+        /* read with the updated weights: y_t = W_t phi(q_t) */
+        for (int r = 0; r < d_v; ++r) {
+            double acc = 0.0;
+            for (int m = 0; m < d_dot; ++m)
+                acc += W[(size_t)r * d_dot + m] * pq[m];
+            y[t * d_v + r] = acc;
+        }
+    }
+    free(pk);
+    free(pq);
+    free(x);
+    free(vbar);
+}
+
+typedef struct {
+    const double *q, *k, *v, *beta, *W0;
+    double *W_final, *y;
+    int64_t BH, L;
+    int d_key, nu, d_v;
+    double eps;
+    int64_t first, last; /* half-open range of (b,h) indices */
+} job_t;
+
+static void *run_job(void *arg)
+{
+    job_t *j = (job_t *)arg;
+    const int d_dot = 2 * j->d_key * j->nu;
+    const size_t wsz = (size_t)j->d_v * d_dot;
+    for (int64_t bh = j->first; bh < j->last; ++bh) {
+        double *W = j->W_final + bh * wsz;
+        if (j->W0 && j->W0 + bh * wsz != W)
+            memcpy(W, j->W0 + bh * wsz, sizeof(double) * wsz);
+        else if (j->W0)
+            ; /* in place: W already holds W_0 */
+        else
+            memset(W, 0, sizeof(double) * wsz); /* W_0 = 0 */
+        recurrence_one(j->q + bh * j->L * j->d_key, j->k + bh * j->L * j->d_key,
+                       j->v + bh * j->L * j->d_v, j->beta + bh * j->L, W,
+                       j->y + bh * j->L * j->d_v, j->L, j->d_key, j->nu, j->d_v, j->eps);
+    }
+    return NULL;
+}
+
+/* The sequential forward: inputs q, k [B,H,L,d_key]; v [B,H,L,d_v];
+ * beta [B,H,L]; W0 [B,H,d_v,d_dot] or NULL (zeros).  Outputs y [B,H,L,d_v]
+ * and W_final [B,H,d_v,d_dot] (both required; W_final may equal W0).
+ * nthreads > 1 splits the independent (b,h) pairs over POSIX threads. */
+int fwo_delta_forward(const double *q, const double *k, const double *v, const double *beta,
+                      const double *W0, double *W_final, double *y, int64_t B, int64_t H, int64_t L,
+                      int d_key, int nu, int d_v, double eps, int nthreads)
+{
+    if (!q || !k || !v || !beta || !W_final || !y || B < 0 || H < 0 || L < 0 || d_key <= 0 ||
+        d_v <= 0 || nu < 1 || nu > 2 * d_key - 1)
+        return FWO_BAD_ARG;
+    const int64_t BH = B * H;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > BH)
+        nthreads = BH > 0 ? (int)BH : 1;
+    job_t *jobs = (job_t *)calloc((size_t)nthreads, sizeof(job_t));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    for (int i = 0; i < nthreads; ++i) {
+        job_t *j = &jobs[i];
+        j->q = q; j->k = k; j->v = v; j->beta = beta; j->W0 = W0;
+        j->W_final = W_final; j->y = y; j->BH = BH; j->L = L;
+        j->d_key = d_key; j->nu = nu; j->d_v = d_v; j->eps = eps;
+        j->first = BH * i / nthreads;
+        j->last = BH * (i + 1) / nthreads;
+    }
+    if (nthreads == 1) {
+        run_job(&jobs[0]);
+    } else {
+        for (int i = 0; i < nthreads; ++i)
+            pthread_create(&tids[i], NULL, run_job, &jobs[i]);
+        for (int i = 0; i < nthreads; ++i)
+            pthread_join(tids[i], NULL);
+    }
+    free(jobs);
+    free(tids);
+    return FWO_OK;
+}
+
+/* One decode step of the token-wise variant: q, k [B,H,d_key]; v, y
+ * [B,H,d_v]; beta [B,H]; W [B,H,d_v,d_dot] updated in place.  It is the
+ * recurrence above over a single token with W carried in from the caller. */
+int fwo_delta_decode_step(const double *q, const double *k, const double *v, const double *beta,
+                          double *W, double *y, int64_t B, int64_t H, int d_key, int nu, int d_v,
+                          double eps, int nthreads)
+{
+    return fwo_delta_forward(q, k, v, beta, W, W, y, B, H, 1, d_key, nu, d_v, eps, nthreads);
+}

@@ -1,0 +1,259 @@
+"""Pins for the fp64 oracle: checks against what the pages and the mathematics
+fix, written so that each takes an oracle object (oracle.OracleLib) and raises
+AssertionError on a mismatch.  tests/test_oracle_pins.py runs them against the
+oracle as built; tests/test_oracle_mutants.py runs them against copies of the
+oracle with a planted mistake and expects at least one to fail.
+
+None of these re-types the oracle's own loop: they compare it with
+hand-worked fractions (tests/golden/), with an FFT identity for the DPFP block
+sums, with closed forms and invariants of the recurrence, and with the
+independent chunked form O2 (oracle/chunked.py).
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _frac(s):
+    return float(Fraction(s))
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ----------------------------------------------------------------- DPFP pins
+def pin_dpfp_hand(o):
+    """Hand-worked DPFP values (exact with eps = 0; scaled by s/(s+eps) otherwise)."""
+    for case in _load("dpfp_hand.json")["cases"]:
+        k = np.array(case["k"], dtype=np.float64)
+        want = np.array([_frac(x) for x in case["phi"]])
+        got = o.dpfp(k, case["nu"], 0.0)
+        assert got.shape == want.shape, (got.shape, want.shape)
+        assert np.allclose(got, want, rtol=0, atol=1e-15), (case["k"], got, want)
+        s = _frac(case["s"])
+        got_eps = o.dpfp(k, case["nu"], 1e-6)
+        assert np.allclose(got_eps, want * s / (s + 1e-6), rtol=1e-14, atol=1e-16)
+
+
+def _autocorr_fft(x):
+    """Circular autocorrelation r[i] = sum_j x[j] x[(j - i) mod n] via the FFT."""
+    X = np.fft.fft(x)
+    return np.real(np.fft.ifft(X * np.conj(X)))
+
+
+def pin_dpfp_block_sums_fft(o):
+    """Block i of the unnormalised phi sums to the circular autocorrelation of
+    x = ReLU([k,-k]) at lag i; after normalisation the total is s/(s+eps)."""
+    rng = _rng(1)
+    for d_key, nu in [(2, 1), (3, 2), (8, 1), (8, 5), (16, 3), (16, 31), (64, 3)]:
+        k = rng.standard_normal((5, d_key))
+        for eps in (0.0, 1e-6, 0.5):
+            phi = o.dpfp(k, nu, eps)
+            n = 2 * d_key
+            assert phi.shape == (5, n * nu)
+            for r in range(5):
+                x = np.concatenate([np.maximum(k[r], 0), np.maximum(-k[r], 0)])
+                ac = _autocorr_fft(x)
+                blocks = np.array([ac[i] for i in range(1, nu + 1)])
+                s = blocks.sum()
+                got_blocks = phi[r].reshape(nu, n).sum(axis=1)
+                assert np.allclose(got_blocks, blocks / (s + eps), rtol=1e-10, atol=1e-13), \
+                    (d_key, nu, eps, got_blocks, blocks / (s + eps))
+
+
+def pin_dpfp_invariants(o):
+    """phi >= 0; scale invariance phi(c k) = phi(k) for c > 0 (eps = 0); the
+    sign flip k -> -k swaps the halves of x, which rolls every block of phi by
+    d_key; block i = d_key (reachable when nu >= d_key) is identically zero;
+    zero input gives zero output without NaN."""
+    rng = _rng(2)
+    for d_key, nu in [(2, 3), (4, 4), (8, 2), (16, 1), (5, 9)]:
+        n = 2 * d_key
+        k = rng.standard_normal((7, d_key))
+        phi = o.dpfp(k, nu, 0.0)
+        assert np.all(phi >= 0)
+        assert np.allclose(o.dpfp(3.7 * k, nu, 0.0), phi, rtol=1e-12, atol=1e-15)
+        flipped = o.dpfp(-k, nu, 0.0).reshape(7, nu, n)
+        rolled = np.roll(phi.reshape(7, nu, n), -d_key, axis=2)
+        assert np.allclose(flipped, rolled, rtol=1e-12, atol=1e-15)
+        if nu >= d_key:
+            assert np.all(phi.reshape(7, nu, n)[:, d_key - 1, :] == 0.0)
+    z = o.dpfp(np.zeros((3, 8)), 2, 1e-6)
+    assert np.all(z == 0.0) and not np.any(np.isnan(z))
+
+
+def pin_dpfp_sparsity_and_gram(o):
+    """Each phi entry is a product of two ReLU outputs, so for nu = 1 and a
+    random k roughly a quarter of the 2*d_key entries are non-zero (adjacent
+    pairs of x of the same sign); and ||phi||^2 <= (sum phi)^2 = 1 for eps = 0.
+    The sparsity statistic is loose: it catches a dropped ReLU, not rounding."""
+    rng = _rng(3)
+    k = rng.standard_normal((4000, 64))
+    phi = o.dpfp(k, 1, 0.0)
+    nnz = np.count_nonzero(phi) / phi.size
+    assert 0.20 < nnz < 0.30, nnz
+    assert np.all(np.sum(phi * phi, axis=1) <= 1.0 + 1e-12)
+
+
+# ------------------------------------------------------- recurrence pins
+def pin_recurrence_hand(o):
+    """Hand-worked two-step and exact-overwrite examples."""
+    for case in _load("recurrence_hand.json")["cases"]:
+        k = np.array(case["k"], dtype=np.float64)[None, None]
+        q = np.array(case["q"], dtype=np.float64)[None, None]
+        v = np.array(case["v"], dtype=np.float64)[None, None]
+        beta = np.array([_frac(b) for b in case["beta"]])[None, None]
+        y_want = np.array([[_frac(x) for x in row] for row in case["y"]])
+        W_want = np.array([[_frac(x) for x in row] for row in case["W_final"]])
+        y, W = o.delta_forward(q, k, v, beta, None, case["nu"], 0.0)
+        assert np.allclose(y[0, 0], y_want, rtol=0, atol=1e-14), (case["name"], y[0, 0], y_want)
+        assert np.allclose(W[0, 0], W_want, rtol=0, atol=1e-14), (case["name"], W[0, 0], W_want)
+        y6, W6 = o.delta_forward(q, k, v, beta, None, case["nu"], 1e-6)
+        assert np.allclose(y6[0, 0], y_want, rtol=1e-5, atol=1e-6)
+        assert np.allclose(W6[0, 0], W_want, rtol=1e-5, atol=1e-6)
+
+
+def _rand_inputs(rng, B, H, L, d_key, nu, d_v, with_w0=True):
+    q = rng.standard_normal((B, H, L, d_key))
+    k = rng.standard_normal((B, H, L, d_key))
+    v = rng.standard_normal((B, H, L, d_v))
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((B, H, L))))
+    W0 = 0.1 * rng.standard_normal((B, H, d_v, 2 * d_key * nu)) if with_w0 else None
+    return q, k, v, beta, W0
+
+
+def pin_beta_zero(o):
+    """beta = 0 never writes: W_final = W0 and y_t = W0 phi(q_t)."""
+    rng = _rng(4)
+    q, k, v, beta, W0 = _rand_inputs(rng, 2, 2, 9, 4, 2, 3)
+    y, W = o.delta_forward(q, k, v, np.zeros_like(beta), W0, 2, 1e-6)
+    assert np.array_equal(W, W0)
+    pq = o.dpfp(q, 2, 1e-6)
+    assert np.allclose(y, np.einsum("bhvd,bhtd->bhtv", W0, pq), rtol=1e-12, atol=1e-14)
+
+
+def pin_one_step_closed_form(o):
+    """From W0 = 0 one step gives W1 = beta v phi(k)^T and
+    y1 = beta v (phi(k) . phi(q))."""
+    rng = _rng(5)
+    q, k, v, beta, _ = _rand_inputs(rng, 3, 2, 1, 8, 3, 5, with_w0=False)
+    y, W = o.delta_forward(q, k, v, beta, None, 3, 1e-6)
+    pk = o.dpfp(k, 3, 1e-6)[:, :, 0]
+    pq = o.dpfp(q, 3, 1e-6)[:, :, 0]
+    bv = beta[:, :, 0, None] * v[:, :, 0]
+    assert np.allclose(W, bv[..., None] * pk[:, :, None, :], rtol=1e-12, atol=1e-15)
+    dot = np.sum(pk * pq, axis=-1)
+    assert np.allclose(y[:, :, 0], bv * dot[..., None], rtol=1e-12, atol=1e-15)
+
+
+def pin_linearity(o):
+    """For fixed k, q, beta the outputs are jointly linear in (V, W0)."""
+    rng = _rng(6)
+    q, k, v1, beta, W01 = _rand_inputs(rng, 1, 2, 11, 4, 1, 3)
+    _, _, v2, _, W02 = _rand_inputs(rng, 1, 2, 11, 4, 1, 3)
+    a, b = 0.7, -1.3
+    y1, Wf1 = o.delta_forward(q, k, v1, beta, W01, 1, 1e-6)
+    y2, Wf2 = o.delta_forward(q, k, v2, beta, W02, 1, 1e-6)
+    y3, Wf3 = o.delta_forward(q, k, a * v1 + b * v2, beta, a * W01 + b * W02, 1, 1e-6)
+    assert np.allclose(y3, a * y1 + b * y2, rtol=1e-10, atol=1e-12)
+    assert np.allclose(Wf3, a * Wf1 + b * Wf2, rtol=1e-10, atol=1e-12)
+
+
+def pin_value_channel_permutation(o):
+    """Rows of W evolve independently: permuting the d_v channels of V and W0
+    permutes y and W_final the same way."""
+    rng = _rng(7)
+    q, k, v, beta, W0 = _rand_inputs(rng, 2, 1, 10, 3, 2, 6)
+    perm = rng.permutation(6)
+    y, W = o.delta_forward(q, k, v, beta, W0, 2, 1e-6)
+    yp, Wp = o.delta_forward(q, k, v[..., perm], beta, W0[:, :, perm], 2, 1e-6)
+    assert np.allclose(yp, y[..., perm], rtol=1e-13, atol=1e-15)
+    assert np.allclose(Wp, W[:, :, perm], rtol=1e-13, atol=1e-15)
+
+
+def pin_contraction_bound(o):
+    """Each step maps W to W (I - beta phi phi^T) + beta v phi^T and
+    ||I - beta phi phi^T||_2 <= 1 (0 <= beta <= 1, ||phi||_2 <= 1), so
+    ||W_t||_F <= ||W_{t-1}||_F + beta_t ||v_t|| ||phi(k_t)||."""
+    rng = _rng(8)
+    q, k, v, beta, W0 = _rand_inputs(rng, 1, 1, 40, 4, 1, 3)
+    bound = np.linalg.norm(W0[0, 0])
+    pk = o.dpfp(k, 1, 1e-6)[0, 0]
+    for t in range(40):
+        bound += beta[0, 0, t] * np.linalg.norm(v[0, 0, t]) * np.linalg.norm(pk[t])
+    _, W = o.delta_forward(q, k, v, beta, W0, 1, 1e-6)
+    assert np.linalg.norm(W[0, 0]) <= bound * (1 + 1e-12)
+
+
+def pin_one_hot_recall(o):
+    """d_key = 64: a key whose only non-zero entries are two adjacent positive
+    values has a one-hot phi (nu = 1).  Keys on disjoint positions are
+    orthogonal, so with beta = 1 every stored value is recalled exactly and a
+    second write to the same key replaces the first."""
+    d_key, d_v = 64, 5
+    rng = _rng(9)
+    pos = [3, 10, 20, 40, 3]
+    L = len(pos)
+    k = np.zeros((1, 1, L, d_key))
+    for t, a in enumerate(pos):
+        k[0, 0, t, a] = 1.0 + rng.random()
+        k[0, 0, t, a + 1] = 1.0 + rng.random()
+    q = k.copy()
+    v = rng.standard_normal((1, 1, L, d_v))
+    beta = np.ones((1, 1, L))
+    y, W = o.delta_forward(q, k, v, beta, None, 1, 0.0)
+    assert np.allclose(y[0, 0], v[0, 0], rtol=0, atol=1e-14)
+    # query all keys against the final state: the repeated key holds its last value
+    qs = k[:, :, :4].copy()
+    pq = o.dpfp(qs, 1, 0.0)[0, 0]
+    recalled = pq @ W[0, 0].T
+    want = v[0, 0, [4, 1, 2, 3]]
+    assert np.allclose(recalled, want, rtol=0, atol=1e-14)
+
+
+def pin_chunked_equals_sequential(o, chunked):
+    """O1 (one token at a time) equals O2 (chunked WY form) to rounding for
+    every chunk length and every L in 1..9, with and without W0."""
+    rng = _rng(10)
+    for L in range(1, 10):
+        for d_key, nu, d_v in [(2, 1, 1), (3, 2, 2), (4, 3, 5)]:
+            for with_w0 in (False, True):
+                q, k, v, beta, W0 = _rand_inputs(rng, 2, 1, L, d_key, nu, d_v, with_w0)
+                y1, W1 = o.delta_forward(q, k, v, beta, W0, nu, 1e-6)
+                for C in sorted({1, 2, 3, L}):
+                    y2, W2 = chunked(q, k, v, beta, W0, nu, 1e-6, C)
+                    sy = max(1.0, np.abs(y1).max())
+                    sw = max(1.0, np.abs(W1).max())
+                    assert np.abs(y2 - y1).max() <= 1e-12 * sy, (L, C, np.abs(y2 - y1).max())
+                    assert np.abs(W2 - W1).max() <= 1e-12 * sw, (L, C)
+
+
+def pin_decode_stepped_equals_forward(o):
+    """The token-wise variant stepped over L tokens equals the forward over
+    the same tokens, in y and in the final state."""
+    rng = _rng(11)
+    q, k, v, beta, W0 = _rand_inputs(rng, 2, 3, 7, 4, 2, 3)
+    y, W = o.delta_forward(q, k, v, beta, W0, 2, 1e-6)
+    Ws = W0.copy()
+    for t in range(7):
+        yt, Ws = o.delta_decode_step(q[:, :, t], k[:, :, t], v[:, :, t], beta[:, :, t], Ws, 2, 1e-6)
+        assert np.allclose(yt, y[:, :, t], rtol=1e-13, atol=1e-15)
+    assert np.allclose(Ws, W, rtol=1e-13, atol=1e-15)
+
+
+ALL_PINS = [
+    pin_dpfp_hand, pin_dpfp_block_sums_fft, pin_dpfp_invariants, pin_dpfp_sparsity_and_gram,
+    pin_recurrence_hand, pin_beta_zero, pin_one_step_closed_form, pin_linearity,
+    pin_value_channel_permutation, pin_contraction_bound, pin_one_hot_recall,
+    pin_decode_stepped_equals_forward,
+]

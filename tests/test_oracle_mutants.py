@@ -1,0 +1,66 @@
+"""Planted mistakes in the oracle must fail its pins (CPU only).
+
+Each case copies oracle/fw_oracle.c to a temporary folder, applies one textual
+mutation of the kind a plausible slip would make (a wrong roll direction, a
+dropped term, a wrong sign, a swapped operand, the read taken before the
+write, ...), compiles it, and runs every pin from tests/oracle_pins.py against
+it.  At least one pin has to fail, otherwise the pins would not notice that
+mistake in the oracle.
+"""
+import os
+import subprocess
+
+import pytest
+
+from oracle import OracleLib
+from oracle.build import SRC
+from oracle.chunked import delta_forward_chunked
+from tests import oracle_pins
+
+MUTANTS = {
+    "roll_direction": ("int src = ((j - i) % n + n) % n;", "int src = ((j + i) % n + n) % n;"),
+    "relu_of_minus_k_dropped": ("x[d_key + j] = -k[j] > 0.0 ? -k[j] : 0.0;",
+                                "x[d_key + j] = k[j] > 0.0 ? k[j] : 0.0;"),
+    "eps_dropped": ("phi[m] = phi[m] / (s + eps);", "phi[m] = phi[m] / (s);"),
+    "not_normalised": ("phi[m] = phi[m] / (s + eps);", "phi[m] = phi[m] + 0.0 * eps;"),
+    "retrieve_with_query": ("acc += W[(size_t)r * d_dot + m] * pk[m];\n            vbar[r] = acc;",
+                            "acc += W[(size_t)r * d_dot + m] * pq[m];\n            vbar[r] = acc;"),
+    "update_sign": ("W[(size_t)r * d_dot + m] += u * pk[m];", "W[(size_t)r * d_dot + m] -= u * pk[m];"),
+    "beta_on_value_only": ("double u = beta[t] * (v[t * d_v + r] - vbar[r]);",
+                           "double u = beta[t] * v[t * d_v + r] - vbar[r];"),
+    "write_with_query": ("W[(size_t)r * d_dot + m] += u * pk[m];", "W[(size_t)r * d_dot + m] += u * pq[m];"),
+    "read_before_write": ("acc += W[(size_t)r * d_dot + m] * pq[m];\n            y[t * d_v + r] = acc;",
+                          "acc += (W[(size_t)r * d_dot + m] - beta[t] * (v[t * d_v + r] - vbar[r]) * pk[m])"
+                          " * pq[m];\n            y[t * d_v + r] = acc;"),
+    "initial_state_ignored": ("memcpy(W, j->W0 + bh * wsz, sizeof(double) * wsz);",
+                              "memset(W, 0, sizeof(double) * wsz);"),
+    "state_transposed": ("W[(size_t)r * d_dot + m] += u * pk[m];",
+                         "W[(size_t)m * d_v + r] += u * pk[m];"),
+}
+
+
+def _build_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found in the oracle"
+    mutated = src.replace(old, new, 1)
+    c = tmp_path / f"{name}.c"
+    so = tmp_path / f"{name}.so"
+    c.write_text(mutated)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-o",
+                    str(so), str(c), "-lpthread", "-lm"], check=True)
+    return OracleLib(str(so))
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    old, new = MUTANTS[name]
+    o = _build_mutant(tmp_path, name, old, new)
+    failed = []
+    pins = list(oracle_pins.ALL_PINS) + [
+        lambda ob: oracle_pins.pin_chunked_equals_sequential(ob, delta_forward_chunked)]
+    for pin in pins:
+        try:
+            pin(o)
+        except (AssertionError, ValueError, FloatingPointError):
+            failed.append(getattr(pin, "__name__", "chunked"))
+    assert failed, f"no pin caught the planted mistake '{name}'"
