@@ -1,0 +1,482 @@
+"""Benchmark of the delta-rule fast-weight layer core on GB300.
+
+One step = one fw_delta_forward call (DPFP of q and k fused, the chunked
+delta rule, y and the final state written) over the B4 H8 L512 d_key 64
+nu 1 d_v 64 bf16 workload (chunk 64), with inputs resident in HBM.  Every
+rank runs its own replica of that workload (weak scaling, no data-path
+collective); the timing is bracketed by a barrier and a device
+synchronisation on both sides and the slowest rank's time is reported.
+
+Between steps the inputs rotate over enough distinct sets that their total
+exceeds 3x the 129 MB L2, so no step finds its inputs in L2.
+
+The JSON line also carries the other rows of the hot path measured on their
+own (the standalone DPFP kernel, the decode step on its 512 MiB state, and
+the long nu = 3 forward), the roofline of the dominant kernel, an end-to-end
+number with host buffers, clocks sampled during the timed region, and the
+CPU oracle's throughput on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "delta-rule fast-weight forward tokens/s (1 GB300) + % tensor/HBM roofline"
+WORKLOAD = "b4h8_l512"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-rows", action="store_true", help="skip the per-row extra measurements")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+def forward_flops_per_head_token(C, d_dot, d_v):
+    """Algorithmic FLOPs of the chunked form per (b,h,token): the C x C
+    triangular products counted at half."""
+    return 2.0 * (1.5 * C * d_dot + C * d_v + 3.0 * d_dot * d_v) + (2.0 / 3.0) * C * C
+
+
+def forward_bytes_per_head_token(d_key, d_v, io_bytes):
+    """Algorithmic HBM bytes per (b,h,token): read q, k, v, beta, write y."""
+    return io_bytes * (2 * d_key + 2 * d_v + 1)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key, sources):
+    """dram bytes per launch recorded from an ncu capture (profiles/traffic.json),
+    or None when absent or when the kernel's source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel_key)
+    if not rec or rec.get("source_hash") != source_hash(sources):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    from delta_rule_linear_dpfp_gb300 import binding as fw
+    from delta_rule_linear_dpfp_gb300 import build, inputs
+
+    build.build()
+    fw.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    cfg = inputs.FORWARD_CONFIGS[WORKLOAD]
+    B, H, L, d_key, nu, d_v, C = (cfg[n] for n in ("B", "H", "L", "d_key", "nu", "d_v", "chunk"))
+    d_dot = 2 * d_key * nu
+    dt = inputs.torch_dtype(cfg["io"])
+    io_bytes = 2 if dt == torch.bfloat16 else 4
+
+    host = inputs.forward_inputs(WORKLOAD, seed=rank)
+    set_bytes = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    nsets = max(2, math.ceil(3 * L2_BYTES / set_bytes))
+    sets = []
+    for s in range(nsets):
+        d = inputs.forward_inputs(WORKLOAD, seed=1000 * rank + s) if s else host
+        sets.append({k: (None if v is None else v.to(dev)) for k, v in d.items()})
+    y = torch.empty(B, H, L, d_v, dtype=dt, device=dev)
+    Wf = torch.empty(B, H, d_v, d_dot, dtype=torch.float32, device=dev)
+    ws_bytes = fw.fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, C, dt)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+
+    def step(i):
+        d = sets[i % nsets]
+        fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=None, nu=nu, chunk=C,
+                            y=y, W_final=Wf, workspace=ws, stream=stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert fw.fw_device_status() == fw.FW_OK
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    tokens_per_step = B * L
+    value = tokens_per_step * world / (ms_step * 1e-3)
+
+    # ---------------------------------------------------------------- e2e
+    pinned = {k: (None if v is None else v.pin_memory()) for k, v in host.items()}
+    y_host = torch.empty(y.shape, dtype=dt).pin_memory()
+    W_host = torch.empty(Wf.shape, dtype=torch.float32).pin_memory()
+    dq = {k: torch.empty_like(v, device=dev) for k, v in pinned.items() if v is not None}
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
+    d2h = y_host.numel() * y_host.element_size() + W_host.numel() * 4
+
+    def e2e_step():
+        for k, v in dq.items():
+            v.copy_(pinned[k], non_blocking=True)
+        fw.fw_delta_forward(dq["q"], dq["k"], dq["v"], dq["beta"], W0=None, nu=nu, chunk=C,
+                            y=y, W_final=Wf, workspace=ws, stream=stream)
+        y_host.copy_(y, non_blocking=True)
+        W_host.copy_(Wf, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 2000))
+    for _ in range(max(3, min(args.warmup, 20))):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ----------------------------------------------------------- roofline
+    pk = peaks()
+    flops = forward_flops_per_head_token(C, d_dot, d_v) * B * H * L
+    nbytes = forward_bytes_per_head_token(d_key, d_v, io_bytes) * B * H * L
+    # the bound is the resource whose time at peak is longer
+    t_hbm = nbytes / (pk["hbm"] * 1e9)
+    t_tc = flops / (pk["bf16"] * 1e12)
+    launches_per_step = FORWARD_LAUNCHES
+    kernel_ms = forward_kernel_ms(fw, sets, y, Wf, ws, nu, C, stream)
+    if t_hbm >= t_tc:
+        achieved = nbytes / (kernel_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": achieved / pk["hbm"]}
+    else:
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16"]}
+    roof.update({"traffic": recorded_traffic(FORWARD_KERNEL_KEY, FORWARD_SOURCES),
+                 "kernel": FORWARD_KERNEL_KEY, "peak_source": pk["source"],
+                 "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                 "kernel_ms": kernel_ms,
+                 "tensor_frac": flops / (kernel_ms * 1e-3) / 1e12 / pk["bf16"],
+                 "hbm_frac": nbytes / (kernel_ms * 1e-3) / 1e9 / pk["hbm"]})
+
+    rows = None
+    if rank == 0 and not args.no_rows:
+        rows = measure_rows(fw, inputs, dev, stream, pk)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: B{B} H{H} L{L} d_key{d_key} nu{nu} d_v{d_v} "
+                               f"bf16 I/O, fp32 state, chunk {C}, W0 = 0, y and W_final out",
+                   "global_batch": B * world, "seq_len": L,
+                   "parallelism": "replicas" if world == 1 else f"replicas x{world}",
+                   "l2": f"inputs rotate over {nsets} sets ({nsets * set_bytes / 2**20:.0f} MiB "
+                         f"> 3x L2), no flush"},
+        "clocks": clk,
+        "e2e": {"value": tokens_per_step * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roof,
+    }
+    if rows is not None:
+        result["rows"] = rows
+    return result
+
+
+# the forward's launches per call and the kernel the roofline is taken on
+FORWARD_LAUNCHES = 1
+FORWARD_KERNEL_KEY = "rowscan_kernel<bf16>"
+FORWARD_SOURCES = ["delta_rule_linear_dpfp_gb300/csrc/fw_rowscan.cu"]
+
+
+def forward_kernel_ms(fw, sets, y, Wf, ws, nu, C, stream, reps=200):
+    """Average duration of one forward call, CUDA events on its stream."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(reps):
+        d = sets[i % len(sets)]
+        fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=None, nu=nu, chunk=C, y=y,
+                            W_final=Wf, workspace=ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def _time(fn, reps, stream):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        fn(0)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(reps):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def measure_rows(fw, inputs, dev, stream, pk):
+    rows = {}
+    # a1 standalone: DPFP of the nu = 3 workload's q and k rows (65536 rows)
+    g = torch.Generator().manual_seed(0)
+    nrows = 2 * 8 * 2048 * 2
+    xs = [torch.randn(nrows, 64, generator=g).to(torch.bfloat16).to(dev) for _ in range(4)]
+    outs = [torch.empty(nrows, 384, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    ms = _time(lambda i: fw.fw_dpfp(xs[i % 4], nu=3, out=outs[i % 4], stream=stream), 200, stream)
+    nb = nrows * (64 + 384) * 2
+    rows["dpfp_65536x64_nu3_bf16"] = {"ms": ms, "GB/s": nb / ms / 1e6,
+                                      "hbm_frac": nb / ms / 1e6 / pk["hbm"],
+                                      "bytes": nb}
+    # a6: decode step, B256 H16 d_key64 nu2 d_v128, W 512 MiB fp32
+    cfg = inputs.DECODE_CONFIGS["decode_b256"]
+    B, H, d_key, nu, d_v = (cfg[n] for n in ("B", "H", "d_key", "nu", "d_v"))
+    d = inputs.decode_inputs(B, H, d_key, nu, d_v, 8, "bf16", seed=0)
+    dd = {k: v.to(dev) for k, v in d.items()}
+    W = dd["W0"]
+    yd = torch.empty(B, H, d_v, dtype=torch.bfloat16, device=dev)
+
+    def dec(i):
+        t = i % 8
+        fw.fw_delta_decode_step(dd["q"][t], dd["k"][t], dd["v"][t], dd["beta"][t], W, nu=nu, y=yd,
+                                stream=stream)
+    ms = _time(dec, 100, stream)
+    d_dot = 2 * d_key * nu
+    nb = B * H * d_v * d_dot * 4 * 2 + B * H * (2 * d_key + 2 * d_v + 1) * 2
+    rows["decode_b256h16_nu2_dv128"] = {"ms": ms, "tokens/s": B / (ms * 1e-3), "GB/s": nb / ms / 1e6,
+                                        "hbm_frac": nb / ms / 1e6 / pk["hbm"], "bytes": nb}
+    # a1-a5 on the long nu = 3 workload with W0 in, W_final out
+    name = "b2h8_l2048_nu3"
+    c = inputs.FORWARD_CONFIGS[name]
+    d = {k: (None if v is None else v.to(dev)) for k, v in inputs.forward_inputs(name).items()}
+    B, H, L, d_key, nu, d_v, C = (c[n] for n in ("B", "H", "L", "d_key", "nu", "d_v", "chunk"))
+    d_dot = 2 * d_key * nu
+    y = torch.empty(B, H, L, d_v, dtype=torch.bfloat16, device=dev)
+    Wf = torch.empty(B, H, d_v, d_dot, dtype=torch.float32, device=dev)
+    nws = fw.fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, C, torch.bfloat16)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    ms = _time(lambda i: fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=d["W0"], nu=nu,
+                                             chunk=C, y=y, W_final=Wf, workspace=ws, stream=stream),
+               50, stream)
+    flops = forward_flops_per_head_token(C, d_dot, d_v) * B * H * L
+    rows[name] = {"ms": ms, "tokens/s": B * L / (ms * 1e-3), "TFLOP/s": flops / ms / 1e9,
+                  "tensor_frac": flops / ms / 1e9 / pk["bf16"], "flops": flops}
+    return rows
+
+
+# ------------------------------------------------------------ the oracle
+class OracleSample:
+    """The fp64 CPU oracle on the host cores over a bounded sample of the
+    workload: whole (b,h) sequences when the time budget allows several, else
+    the first tokens of one sequence.  Inputs are drawn and widened once."""
+
+    def __init__(self, B, H, L, d_key, nu, d_v, io, seed=0):
+        import numpy as np
+
+        import oracle
+        from delta_rule_linear_dpfp_gb300 import inputs
+        self.oracle, self.np = oracle, np
+        d = inputs.random_forward_inputs(B, H, L, d_key, nu, d_v, io, None, seed)
+        flat = lambda t: np.ascontiguousarray(
+            t.float().double().numpy().reshape((1, B * H) + tuple(t.shape[2:])))
+        self.f = {k: flat(v) for k, v in d.items() if v is not None}
+        self.B, self.H, self.L, self.nu = B, H, L, nu
+        self.threads = oracle.default_threads()
+        t0 = time.perf_counter()
+        self._run(1, L, 1)
+        self.t_pair = max(time.perf_counter() - t0, 1e-6)
+
+    def _run(self, pairs, tokens, threads):
+        f = self.f
+        sl = lambda a: self.np.ascontiguousarray(a[:, :pairs, :tokens])
+        self.oracle.delta_forward(sl(f["q"]), sl(f["k"]), sl(f["v"]), sl(f["beta"]), None, self.nu,
+                                  1e-6, threads)
+
+    def plan(self, budget_s):
+        pairs = int(max(1, min(self.B * self.H, budget_s * self.threads / self.t_pair)))
+        tokens = self.L
+        if pairs == 1 and budget_s < self.t_pair:
+            tokens = int(max(1, self.L * budget_s / self.t_pair))
+        return pairs, tokens
+
+    def measure(self, budget_s):
+        """Returns (tokens/s, threads used, sample description, seconds)."""
+        pairs, tokens = self.plan(budget_s)
+        threads = min(self.threads, pairs)
+        t0 = time.perf_counter()
+        self._run(pairs, tokens, threads)
+        dt = time.perf_counter() - t0
+        sample = (f"{pairs} of {self.B * self.H} (b,h) sequences x {tokens} of {self.L} tokens, "
+                  f"fp64, {threads} threads")
+        return pairs * tokens / self.H / dt, threads, sample, dt
+
+
+def run_reference(args, rank, world):
+    from delta_rule_linear_dpfp_gb300 import inputs
+    cfg = inputs.FORWARD_CONFIGS[WORKLOAD]
+    B, H, L, d_key, nu, d_v = (cfg[n] for n in ("B", "H", "L", "d_key", "nu", "d_v"))
+    budget = max(0.002, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    orc = OracleSample(B, H, L, d_key, nu, d_v, cfg["io"])
+    for _ in range(args.warmup):
+        orc.measure(budget)
+    tok, secs = 0.0, 0.0
+    for _ in range(args.steps):
+        v, cores, sample, dt = orc.measure(budget)
+        tok += v * dt
+        secs += dt
+    value = tok / secs
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: B{B} H{H} L{L} d_key{d_key} nu{nu} d_v{d_v}",
+                   "global_batch": B, "seq_len": L, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu:
+            from delta_rule_linear_dpfp_gb300 import inputs
+            cfg = inputs.FORWARD_CONFIGS[WORKLOAD]
+            orc = OracleSample(cfg["B"], cfg["H"], cfg["L"], cfg["d_key"], cfg["nu"], cfg["d_v"],
+                               cfg["io"])
+            v, cores, sample, _ = orc.measure(12.0)
+            res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                   "sample": sample}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,173 @@
+"""Thin Python binding of the C ABI in include/fastweight.h.
+
+Argument marshalling only: every function here checks tensor shapes/dtypes,
+allocates missing outputs with PyTorch (device memory is PyTorch's job) and
+calls the entry point of the same name in libfastweight.so through ctypes on
+the current CUDA stream.  All arithmetic runs in the library's sm_103a
+kernels.  There is no fallback: if the library is missing the import of a
+function raises, and a non-zero status raises FwError.
+"""
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+FW_OK = 0
+FW_ERR_INVALID_ARG = 1
+FW_ERR_UNSUPPORTED = 2
+FW_ERR_CUDA = 3
+FW_ERR_TIMEOUT = 4
+FW_DTYPE_F32 = 0
+FW_DTYPE_BF16 = 1
+
+#: every entry point include/fastweight.h declares
+EXPORTS = ("fw_status_string", "fw_dpfp", "fw_delta_forward_workspace_size", "fw_delta_forward",
+           "fw_delta_decode_step", "fw_device_status")
+
+_lib = None
+
+
+class FwError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)}")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(path: str = None) -> ctypes.CDLL:
+    """Load libfastweight.so (built by delta_rule_linear_dpfp_gb300.build)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB
+    if not os.path.exists(p):
+        raise RuntimeError(f"libfastweight.so is not built ({p}); run "
+                           "delta_rule_linear_dpfp_gb300.build.build() first")
+    lib = ctypes.CDLL(p)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.fw_status_string.restype = ctypes.c_char_p
+    lib.fw_status_string.argtypes = [i32]
+    lib.fw_dpfp.restype = i32
+    lib.fw_dpfp.argtypes = [vp, vp, i64, i32, i32, i32, i32, f32, vp]
+    lib.fw_delta_forward_workspace_size.restype = sz
+    lib.fw_delta_forward_workspace_size.argtypes = [i32] * 8
+    lib.fw_delta_forward.restype = i32
+    lib.fw_delta_forward.argtypes = [vp] * 8 + [sz] + [i32] * 8 + [f32, vp]
+    lib.fw_delta_decode_step.restype = i32
+    lib.fw_delta_decode_step.argtypes = [vp] * 6 + [i32] * 6 + [f32, vp]
+    lib.fw_device_status.restype = i32
+    lib.fw_device_status.argtypes = [vp]
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().fw_status_string(int(code)).decode()
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return FW_DTYPE_F32
+    if t == torch.bfloat16:
+        return FW_DTYPE_BF16
+    raise TypeError(f"unsupported dtype {t}; use torch.float32 or torch.bfloat16")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(code, where):
+    if code != FW_OK:
+        raise FwError(code, where)
+
+
+def _dev(t, name):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def fw_dpfp(x, nu: int = 1, eps: float = 1e-6, out_dtype=None, out=None, stream=None):
+    """phi = DPFP(x) over the last axis: [..., d_key] -> [..., 2*d_key*nu]."""
+    _dev(x, "x")
+    d_key = x.shape[-1]
+    out_dtype = out_dtype or x.dtype
+    if out is None:
+        out = torch.empty(*x.shape[:-1], 2 * d_key * nu, dtype=out_dtype, device=x.device)
+    _dev(out, "out")
+    rows = x.numel() // d_key if d_key else 0
+    rc = load().fw_dpfp(_ptr(x), _ptr(out), rows, d_key, nu, _dtype_code(x.dtype),
+                        _dtype_code(out.dtype), eps, _stream(stream))
+    _check(rc, "fw_dpfp")
+    return out
+
+
+def fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk, io_dtype) -> int:
+    code = io_dtype if isinstance(io_dtype, int) else _dtype_code(io_dtype)
+    return int(load().fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk, code))
+
+
+def fw_delta_forward(q, k, v, beta, W0=None, nu: int = 1, chunk: int = 64, eps: float = 1e-6,
+                     return_state: bool = True, y=None, W_final=None, workspace=None, stream=None):
+    """Delta-rule forward over [B,H,L,*] inputs.  Returns (y, W_final or None)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
+        _dev(t, name)
+    B, H, L, d_key = q.shape
+    d_v = v.shape[-1]
+    d_dot = 2 * d_key * nu
+    if k.shape != q.shape or v.shape != (B, H, L, d_v) or beta.shape != (B, H, L):
+        raise ValueError("shape mismatch among q, k, v, beta")
+    if not (q.dtype == k.dtype == v.dtype == beta.dtype):
+        raise ValueError("q, k, v, beta must share the I/O dtype")
+    if W0 is not None:
+        _dev(W0, "W0")
+        if W0.dtype != torch.float32 or W0.shape != (B, H, d_v, d_dot):
+            raise ValueError("W0 must be fp32 [B,H,d_v,d_dot]")
+    if y is None:
+        y = torch.empty(B, H, L, d_v, dtype=q.dtype, device=q.device)
+    if W_final is None and return_state:
+        W_final = torch.empty(B, H, d_v, d_dot, dtype=torch.float32, device=q.device)
+    code = _dtype_code(q.dtype)
+    need = fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk, code)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().fw_delta_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(W0), _ptr(W_final),
+                                 _ptr(y), _ptr(workspace), ws_bytes, B, H, L, d_key, nu, d_v, chunk,
+                                 code, eps, _stream(stream))
+    _check(rc, "fw_delta_forward")
+    return y, W_final
+
+
+def fw_delta_decode_step(q, k, v, beta, W, nu: int = 1, eps: float = 1e-6, y=None, stream=None):
+    """One token per (b,h): q, k [B,H,d_key]; v [B,H,d_v]; beta [B,H]; W fp32
+    [B,H,d_v,d_dot] updated in place.  Returns y [B,H,d_v]."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("W", W)):
+        _dev(t, name)
+    B, H, d_key = q.shape
+    d_v = v.shape[-1]
+    if W.dtype != torch.float32 or W.shape != (B, H, d_v, 2 * d_key * nu):
+        raise ValueError("W must be fp32 [B,H,d_v,d_dot]")
+    if y is None:
+        y = torch.empty(B, H, d_v, dtype=q.dtype, device=q.device)
+    rc = load().fw_delta_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(W), _ptr(y), B, H,
+                                     d_key, nu, d_v, _dtype_code(q.dtype), eps, _stream(stream))
+    _check(rc, "fw_delta_decode_step")
+    return y
+
+
+def fw_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return int(load().fw_device_status(_stream(stream)))

@@ -1,0 +1,215 @@
+// fw_api.cu -- the C ABI (include/fastweight.h): argument checks on the host,
+// then dispatch to the sm_103a kernels.  Nothing is enqueued unless every
+// check passes; the library never allocates device memory.
+#include "fastweight.h"
+#include "fw_common.cuh"
+#include "fw_forward_tc.h"
+
+#include <cmath>
+#include <mutex>
+
+namespace fw {
+cudaError_t launch_dpfp(const void *x, void *phi, int64_t rows, int d_key, int nu, int in_bf16,
+                        int out_bf16, float eps, int num_sms, cudaStream_t st);
+cudaError_t launch_rowscan(const void *q, const void *k, const void *v, const void *beta,
+                           const float *W0, float *Wout, void *y, int BH, int L, int d_key, int nu,
+                           int d_v, int bf16, float eps, cudaStream_t st);
+} // namespace fw
+
+// Device-side status word (bit fw::kStatusTimeout: a bounded wait gave up).
+static __device__ unsigned g_fw_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_status_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+
+struct DeviceInfo {
+    int num_sms;
+    unsigned *status;
+};
+
+// Per-device facts, looked up once per device with that device current.
+cudaError_t device_info(DeviceInfo *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_status_ptr[dev]) {
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fw_device_status);
+        if (e != cudaSuccess)
+            return e;
+        g_num_sms[dev] = sms;
+        g_status_ptr[dev] = static_cast<unsigned *>(p);
+    }
+    out->num_sms = g_num_sms[dev];
+    out->status = g_status_ptr[dev];
+    return cudaSuccess;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dtype_ok(int d) { return d == FW_DTYPE_F32 || d == FW_DTYPE_BF16; }
+bool dkey_supported(int d_key) {
+    return d_key == 8 || d_key == 16 || d_key == 32 || d_key == 64 || d_key == 128;
+}
+bool eps_ok(float eps) { return std::isfinite(eps) && eps >= 0.f; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? FW_OK : FW_ERR_CUDA; }
+
+} // namespace
+
+extern "C" {
+
+FW_API const char *fw_status_string(int status) {
+    switch (status) {
+    case FW_OK: return "FW_OK";
+    case FW_ERR_INVALID_ARG: return "FW_ERR_INVALID_ARG: invalid argument";
+    case FW_ERR_UNSUPPORTED: return "FW_ERR_UNSUPPORTED: shape or dtype outside the compiled set";
+    case FW_ERR_CUDA: return "FW_ERR_CUDA: a CUDA call failed";
+    case FW_ERR_TIMEOUT: return "FW_ERR_TIMEOUT: a bounded device wait gave up";
+    default: return "unknown fw_status";
+    }
+}
+
+FW_API int fw_dpfp(const void *x, void *phi, int64_t rows, int d_key, int nu, int in_dtype,
+                   int out_dtype, float eps, void *stream) {
+    if (!x || !phi || !aligned16(x) || !aligned16(phi) || rows < 0 || d_key <= 0 || nu < 1 ||
+        nu > 2 * d_key - 1 || !dtype_ok(in_dtype) || !dtype_ok(out_dtype) || !eps_ok(eps))
+        return FW_ERR_INVALID_ARG;
+    if (!dkey_supported(d_key))
+        return FW_ERR_UNSUPPORTED;
+    if (rows == 0)
+        return FW_OK;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess)
+        return FW_ERR_CUDA;
+    e = fw::launch_dpfp(x, phi, rows, d_key, nu, in_dtype == FW_DTYPE_BF16, out_dtype == FW_DTYPE_BF16,
+                        eps, di.num_sms, static_cast<cudaStream_t>(stream));
+    return cuda_status(e);
+}
+
+namespace {
+
+// Shape checks shared by the forward and its workspace query.
+// Returns FW_OK, FW_ERR_INVALID_ARG or FW_ERR_UNSUPPORTED.
+int check_forward_shape(int B, int H, int L, int d_key, int nu, int d_v, int chunk, int io_dtype) {
+    if (B < 0 || H < 0 || L < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 ||
+        !dtype_ok(io_dtype) || !(chunk == 16 || chunk == 32 || chunk == 64))
+        return FW_ERR_INVALID_ARG;
+    if (!dkey_supported(d_key))
+        return FW_ERR_UNSUPPORTED;
+    const int d_dot = 2 * d_key * nu;
+    if (io_dtype == FW_DTYPE_F32)
+        return d_dot <= 1024 ? FW_OK : FW_ERR_UNSUPPORTED;
+    return fw::tc_forward_supported(d_key, nu, d_v, chunk) ? FW_OK : FW_ERR_UNSUPPORTED;
+}
+
+} // namespace
+
+FW_API size_t fw_delta_forward_workspace_size(int B, int H, int L, int d_key, int nu, int d_v,
+                                              int chunk, int io_dtype) {
+    if (check_forward_shape(B, H, L, d_key, nu, d_v, chunk, io_dtype) != FW_OK)
+        return 0;
+    if (io_dtype == FW_DTYPE_F32)
+        return 0;
+    return fw::tc_forward_workspace_bytes(B, H, L, d_key, nu, d_v, chunk);
+}
+
+FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const void *beta,
+                            const float *W0, float *W_final, void *y, void *workspace,
+                            size_t workspace_bytes, int B, int H, int L, int d_key, int nu,
+                            int d_v, int chunk, int io_dtype, float eps, void *stream) {
+    if (!q || !k || !v || !beta || !y || !eps_ok(eps))
+        return FW_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) || !aligned16(y) ||
+        (W0 && !aligned16(W0)) || (W_final && !aligned16(W_final)) ||
+        (workspace && !aligned16(workspace)))
+        return FW_ERR_INVALID_ARG;
+    const int rc = check_forward_shape(B, H, L, d_key, nu, d_v, chunk, io_dtype);
+    if (rc != FW_OK)
+        return rc;
+    const size_t need = fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk, io_dtype);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return FW_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t BH = (int64_t)B * H;
+    if (BH == 0)
+        return FW_OK;
+    if (BH > (int64_t)1 << 30)
+        return FW_ERR_UNSUPPORTED;
+    const int d_dot = 2 * d_key * nu;
+    if (L == 0) {
+        // no token: the final state is the initial one
+        if (!W_final)
+            return FW_OK;
+        const size_t bytes = sizeof(float) * (size_t)BH * d_v * d_dot;
+        if (W0 == W_final)
+            return FW_OK;
+        cudaError_t e = W0 ? cudaMemcpyAsync(W_final, W0, bytes, cudaMemcpyDeviceToDevice, st)
+                           : cudaMemsetAsync(W_final, 0, bytes, st);
+        return cuda_status(e);
+    }
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess)
+        return FW_ERR_CUDA;
+    if (io_dtype == FW_DTYPE_F32) {
+        e = fw::launch_rowscan(q, k, v, beta, W0, W_final, y, (int)BH, L, d_key, nu, d_v, 0, eps, st);
+        return cuda_status(e);
+    }
+    e = fw::tc_forward_launch(q, k, v, beta, W0, W_final, y, workspace, B, H, L, d_key, nu, d_v,
+                              chunk, eps, di.num_sms, di.status, st);
+    return cuda_status(e);
+}
+
+FW_API int fw_delta_decode_step(const void *q, const void *k, const void *v, const void *beta,
+                                float *W, void *y, int B, int H, int d_key, int nu, int d_v,
+                                int io_dtype, float eps, void *stream) {
+    if (!q || !k || !v || !beta || !W || !y || !eps_ok(eps) || B < 0 || H < 0 || d_key <= 0 ||
+        d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 || !dtype_ok(io_dtype))
+        return FW_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) || !aligned16(W) ||
+        !aligned16(y))
+        return FW_ERR_INVALID_ARG;
+    if (!dkey_supported(d_key) || 2 * d_key * nu > 1024)
+        return FW_ERR_UNSUPPORTED;
+    const int64_t BH = (int64_t)B * H;
+    if (BH == 0)
+        return FW_OK;
+    if (BH > (int64_t)1 << 30)
+        return FW_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess)
+        return FW_ERR_CUDA;
+    e = fw::launch_decode(q, k, v, beta, W, y, (int)BH, d_key, nu, d_v, io_dtype == FW_DTYPE_BF16,
+                          eps, di.num_sms, static_cast<cudaStream_t>(stream));
+    return cuda_status(e);
+}
+
+FW_API int fw_device_status(void *stream) {
+    DeviceInfo di;
+    if (device_info(&di) != cudaSuccess)
+        return FW_ERR_CUDA;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return FW_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, di.status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FW_ERR_CUDA;
+    if (word != 0 && cudaMemset(di.status, 0, sizeof(word)) != cudaSuccess)
+        return FW_ERR_CUDA;
+    return (word & fw::kStatusTimeout) ? FW_ERR_TIMEOUT : FW_OK;
+}
+
+} // extern "C"

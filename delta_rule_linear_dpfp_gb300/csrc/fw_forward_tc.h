@@ -1,0 +1,25 @@
+// fw_forward_tc.h -- host interface of the bf16 chunked forward (tcgen05).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fw {
+
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *beta, float *W,
+                          void *y, int BH, int d_key, int nu, int d_v, int bf16, float eps,
+                          int num_sms, cudaStream_t st);
+
+// True if the bf16 tensor-core forward is compiled for this shape.
+bool tc_forward_supported(int d_key, int nu, int d_v, int chunk);
+
+// Device workspace bytes the bf16 forward needs for this shape.
+size_t tc_forward_workspace_bytes(int B, int H, int L, int d_key, int nu, int d_v, int chunk);
+
+// Enqueue the bf16 forward (arguments validated by the caller).
+cudaError_t tc_forward_launch(const void *q, const void *k, const void *v, const void *beta,
+                              const float *W0, float *W_final, void *y, void *workspace, int B,
+                              int H, int L, int d_key, int nu, int d_v, int chunk, float eps,
+                              int num_sms, unsigned *status, cudaStream_t st);
+
+} // namespace fw

@@ -1,0 +1,169 @@
+/*
+ * fastweight.h -- C ABI of the GB300 (sm_103a) delta-rule fast-weight layer
+ * core with the DPFP feature map.
+ *
+ * The method is the one the Fast Weights Transformer guide (xdnf.cn/news/308600,
+ * a walk-through of "Linear Transformers Are Secretly Fast Weight Memory
+ * Systems", arXiv:2102.11174) describes:
+ *
+ *   phi(k)   = DPFP(k): x = ReLU([k, -k]) (length 2*d_key); for i = 1..nu the
+ *              block i of phi is x * roll(x, i), where roll follows
+ *              torch.roll(shifts=i) (position j holds x[(j - i) mod 2*d_key]);
+ *              phi is then divided by (sum(phi) + eps).  d_dot = 2*d_key*nu.
+ *              [section "DPFP: projection formula and hyper-parameters", the
+ *              normalisation formula and the DPFP source shown with it]
+ *   vbar_t   = W_{t-1} phi(k_t)
+ *   W_t      = W_{t-1} + beta_t (v_t - vbar_t) outer phi(k_t)
+ *   y_t      = W_t phi(q_t)         (the read uses the updated W)
+ *              [section "FastWeightsAttention: the new update rule" and its
+ *              forward-pass loop; W starts from zero per (batch, head) unless
+ *              an initial state is given]
+ *
+ * There is no normaliser z and no 1/sqrt(d) scale: phi is already normalised
+ * (same section).
+ *
+ * Conventions shared by every call
+ *   - All tensor arguments are CALLER-OWNED DEVICE pointers to contiguous,
+ *     row-major memory (the last dimension is fastest).  The library never
+ *     allocates or frees device memory and keeps no pointer after a call
+ *     returns.
+ *   - Activations use the [B, H, L, d] layout (batch, head, token, feature).
+ *     The fast-weight state W is fp32 [B, H, d_v, d_dot], the layout of the
+ *     guide's forward pass (weights of shape [batch, heads, d_value, d_key]).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call only enqueues work on it and returns; results are
+ *     ready once the stream has reached that point.
+ *   - Every argument is checked on the host BEFORE anything is enqueued: a
+ *     call that returns an error has launched nothing and touched no memory.
+ *   - Pointers must be 16-byte aligned (FW_ERR_INVALID_ARG otherwise).
+ *   - No call has a CPU fallback: shapes outside the compiled tile set give
+ *     FW_ERR_UNSUPPORTED.
+ *   - Return values are fw_status codes; fw_status_string() names them.
+ */
+#ifndef FASTWEIGHT_H
+#define FASTWEIGHT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FW_API __attribute__((visibility("default")))
+#else
+#define FW_API
+#endif
+
+typedef enum fw_status {
+    FW_OK = 0,
+    FW_ERR_INVALID_ARG = 1, /* null or misaligned pointer, non-positive size, nu out of range */
+    FW_ERR_UNSUPPORTED = 2, /* valid arguments outside the compiled shapes / dtypes */
+    FW_ERR_CUDA = 3,        /* a CUDA launch or runtime call failed */
+    FW_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (see fw_device_status) */
+} fw_status;
+
+typedef enum fw_dtype {
+    FW_DTYPE_F32 = 0, /* IEEE binary32 */
+    FW_DTYPE_BF16 = 1 /* bfloat16 */
+} fw_dtype;
+
+/* Name of a status code (static string, never NULL). */
+FW_API const char *fw_status_string(int status);
+
+/*
+ * fw_dpfp -- the DPFP feature map with its sum-normalisation, one fused pass.
+ * [Fast Weights Transformer guide, section "DPFP: projection formula and
+ * hyper-parameters" and the normalisation formula with its source]
+ *
+ *   x    : [rows, d_key] in in_dtype          (read)
+ *   phi  : [rows, 2*d_key*nu] in out_dtype    (written)
+ *   rows : >= 0 (0 enqueues nothing);  d_key in {8, 16, 32, 64, 128};
+ *   nu   : 1 .. 2*d_key-1;  eps >= 0 (the guide's default is 1e-6).
+ *   A row whose phi sums to zero gives phi = 0 (0 / (0 + eps)).
+ * Errors: FW_ERR_INVALID_ARG for null/misaligned pointers, rows < 0,
+ * d_key <= 0, nu out of range, eps < 0 or an unknown dtype;
+ * FW_ERR_UNSUPPORTED for other d_key; FW_ERR_CUDA if the launch fails.
+ */
+FW_API int fw_dpfp(const void *x, void *phi, int64_t rows, int d_key, int nu, int in_dtype,
+                   int out_dtype, float eps, void *stream);
+
+/*
+ * Bytes of device workspace fw_delta_forward needs for this shape (0 when it
+ * needs none; also 0 for arguments it would reject).  The caller allocates it.
+ */
+FW_API size_t fw_delta_forward_workspace_size(int B, int H, int L, int d_key, int nu, int d_v,
+                                              int chunk, int io_dtype);
+
+/*
+ * fw_delta_forward -- the delta-rule recurrence over a whole sequence, for
+ * every (batch, head) pair, with the DPFP map of q and k fused in.
+ * [Fast Weights Transformer guide, section "FastWeightsAttention: the new
+ * update rule" and its forward-pass loop; the chunked evaluation with the
+ * memory passed from chunk to chunk follows the lucidrains
+ * fast-weight-attention write-up, section 4.2, which gives the interface
+ * (tokens in, output and next memory out) but no algorithm.]
+ *
+ *   q, k     : [B, H, L, d_key]  io_dtype             (read)
+ *   v        : [B, H, L, d_v]    io_dtype             (read)
+ *   beta     : [B, H, L]         io_dtype, in [0, 1]  (read)
+ *   W0       : [B, H, d_v, d_dot] fp32 initial state, or NULL for zeros
+ *   W_final  : [B, H, d_v, d_dot] fp32 final state, or NULL to skip it;
+ *              W_final == W0 (in place) is allowed
+ *   y        : [B, H, L, d_v]    io_dtype             (written)
+ *   workspace: device scratch of at least fw_delta_forward_workspace_size()
+ *              bytes (may be NULL when that size is 0); its contents on entry
+ *              do not matter and are garbage on return
+ *   chunk    : tokens per chunk of the chunked evaluation, in {16, 32, 64};
+ *              L need not be a multiple of it (the last chunk is partial).
+ *              The result does not depend on it beyond rounding.
+ *   io_dtype : FW_DTYPE_F32 -- fp32 arithmetic on CUDA cores, token by token
+ *              (chunk is validated but only tiles the work);
+ *              FW_DTYPE_BF16 -- bf16 operands on the tcgen05 tensor cores
+ *              with fp32 accumulation and an fp32 state.
+ *   eps      : DPFP normaliser (1e-6 in the guide).
+ * Other pointers must not alias each other.
+ * Errors: FW_ERR_INVALID_ARG (null required pointer, misaligned pointer,
+ * non-positive size, nu out of range, workspace too small);
+ * FW_ERR_UNSUPPORTED (shapes outside the compiled set: d_key in {8, 16, 32,
+ * 64, 128}; for bf16 also d_v in {16, 32, 64, 128} and the state must fit
+ * the tensor memory); FW_ERR_CUDA (launch failure).  A device-side bounded
+ * wait that gives up is reported by fw_device_status().
+ */
+FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const void *beta,
+                            const float *W0, float *W_final, void *y, void *workspace,
+                            size_t workspace_bytes, int B, int H, int L, int d_key, int nu,
+                            int d_v, int chunk, int io_dtype, float eps, void *stream);
+
+/*
+ * fw_delta_decode_step -- one new token per (batch, head) against a
+ * persistent fast-weight state, updated in place.  Every element of W is read
+ * once and written once.
+ * [Fast Weights Transformer guide, section "token_wise variant" (one token at
+ * a time, the weights kept from step to step) and section "inference and
+ * sampling"; the arithmetic is the update rule above for one token]
+ *
+ *   q, k : [B, H, d_key] io_dtype;  v, y : [B, H, d_v] io_dtype;
+ *   beta : [B, H] io_dtype;  W : [B, H, d_v, d_dot] fp32, read and written.
+ * Errors: as fw_delta_forward (d_key in {8, 16, 32, 64, 128}, d_dot <= 1024).
+ */
+FW_API int fw_delta_decode_step(const void *q, const void *k, const void *v, const void *beta,
+                                float *W, void *y, int B, int H, int d_key, int nu, int d_v,
+                                int io_dtype, float eps, void *stream);
+
+/*
+ * fw_device_status -- waits for `stream`, then reports and clears the
+ * device-side status word of the current device: FW_ERR_TIMEOUT if any
+ * kernel of this library gave up a bounded wait (its outputs are then
+ * undefined) since the last call, FW_OK otherwise, FW_ERR_CUDA if the
+ * synchronisation itself failed.  Not an error path of the math: with valid
+ * inputs the waits always complete.
+ */
+FW_API int fw_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FASTWEIGHT_H */

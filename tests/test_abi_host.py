@@ -1,0 +1,122 @@
+"""The C-ABI library on the host (no GPU needed): it builds, loads, exports
+every symbol include/fastweight.h declares, and rejects bad arguments before
+touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from delta_rule_linear_dpfp_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fastweight.h")
+
+# a non-null, 16-byte aligned address that is never dereferenced: every call
+# below fails its host-side checks before any CUDA call
+FAKE = ctypes.c_void_p(0x10000)
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"FW_API[^;(]*?\b(fw_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_symbols() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert binding.status_string(code).startswith("FW_")
+    assert binding.status_string(99) == "unknown fw_status"
+
+
+def test_dpfp_argument_checks(lib):
+    E, U, OK = binding.FW_ERR_INVALID_ARG, binding.FW_ERR_UNSUPPORTED, binding.FW_OK
+    call = lib.fw_dpfp
+    assert call(None, FAKE, 4, 64, 1, 0, 0, 1e-6, None) == E
+    assert call(FAKE, None, 4, 64, 1, 0, 0, 1e-6, None) == E
+    assert call(MISALIGNED, FAKE, 4, 64, 1, 0, 0, 1e-6, None) == E
+    assert call(FAKE, FAKE, -1, 64, 1, 0, 0, 1e-6, None) == E
+    assert call(FAKE, FAKE, 4, 64, 0, 0, 0, 1e-6, None) == E
+    assert call(FAKE, FAKE, 4, 64, 128, 0, 0, 1e-6, None) == E      # nu > 2*d_key-1
+    assert call(FAKE, FAKE, 4, 64, 1, 7, 0, 1e-6, None) == E        # unknown dtype
+    assert call(FAKE, FAKE, 4, 64, 1, 0, 0, -1.0, None) == E        # eps < 0
+    assert call(FAKE, FAKE, 4, 64, 1, 0, 0, float("nan"), None) == E
+    assert call(FAKE, FAKE, 4, 12, 1, 0, 0, 1e-6, None) == U        # d_key not compiled
+    assert call(FAKE, FAKE, 0, 64, 1, 0, 0, 1e-6, None) == OK       # empty: nothing enqueued
+
+
+def _fwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, beta=FAKE, W0=None, Wf=None, y=FAKE, ws=None, wsb=0, B=2, H=2,
+             L=8, d_key=64, nu=1, d_v=64, chunk=64, io=1, eps=1e-6)
+    a.update(kw)
+    return lib.fw_delta_forward(a["q"], a["k"], a["v"], a["beta"], a["W0"], a["Wf"], a["y"],
+                                a["ws"], a["wsb"], a["B"], a["H"], a["L"], a["d_key"], a["nu"],
+                                a["d_v"], a["chunk"], a["io"], a["eps"], None)
+
+
+def test_forward_argument_checks(lib):
+    E, U, OK = binding.FW_ERR_INVALID_ARG, binding.FW_ERR_UNSUPPORTED, binding.FW_OK
+    for name in ("q", "k", "v", "beta", "y"):
+        assert _fwd(lib, **{name: None}) == E, name
+        assert _fwd(lib, **{name: MISALIGNED}) == E, name
+    assert _fwd(lib, W0=MISALIGNED) == E
+    assert _fwd(lib, Wf=MISALIGNED) == E
+    assert _fwd(lib, B=-1) == E
+    assert _fwd(lib, d_v=0) == E
+    assert _fwd(lib, nu=0) == E
+    assert _fwd(lib, chunk=48) == E
+    assert _fwd(lib, io=3) == E
+    assert _fwd(lib, eps=-1e-6) == E
+    assert _fwd(lib, d_key=24) == U
+    need = lib.fw_delta_forward_workspace_size(2, 2, 8, 64, 1, 64, 64, 1)
+    if need > 0:
+        assert _fwd(lib, ws=None, wsb=0) == E
+        assert _fwd(lib, ws=FAKE, wsb=need - 1) == E
+    # empty batch: nothing to do, nothing enqueued
+    assert _fwd(lib, B=0, ws=FAKE, wsb=1 << 40) == OK
+
+
+def test_forward_workspace_query(lib):
+    ws = lib.fw_delta_forward_workspace_size
+    assert ws(2, 2, 8, 64, 1, 64, 64, 0) == 0          # fp32 path needs none
+    assert ws(2, 2, 8, 64, 1, 64, 48, 1) == 0          # rejected chunk -> 0
+    assert ws(2, 2, 8, 24, 1, 64, 64, 1) == 0          # unsupported d_key -> 0
+    a = ws(2, 8, 2048, 64, 3, 64, 64, 1)
+    b = ws(4, 8, 2048, 64, 3, 64, 64, 1)
+    assert b >= a
+
+
+def test_decode_argument_checks(lib):
+    E, U = binding.FW_ERR_INVALID_ARG, binding.FW_ERR_UNSUPPORTED
+    call = lib.fw_delta_decode_step
+    base = [FAKE] * 6 + [4, 2, 64, 2, 128, 1, 1e-6, None]
+    for i in range(6):
+        args = list(base)
+        args[i] = None
+        assert call(*args) == E
+        args[i] = MISALIGNED
+        assert call(*args) == E
+    args = list(base)
+    args[9] = 0                                        # nu = 0
+    assert call(*args) == E
+    args = list(base)
+    args[8] = 20                                       # d_key not compiled
+    assert call(*args) == U
+    args = list(base)
+    args[8], args[9] = 128, 5                          # d_dot = 1280 > 1024
+    assert call(*args) == U

@@ -1,0 +1,233 @@
+"""GPU parity: the sm_103a kernels, called through the C ABI, against the fp64
+oracle on the same seeded inputs.  Tolerances: max normwise relative error
+1e-4 for fp32 I/O and 2e-2 for bf16 I/O with fp32 state (tests/parity_util.py);
+the final-state shape and layout must match exactly."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from delta_rule_linear_dpfp_gb300 import binding as fw
+from delta_rule_linear_dpfp_gb300 import build, inputs
+from tests.parity_util import f64, maxrel, to_dev, tol_for
+
+pytestmark = pytest.mark.gpu
+
+NT = oracle.default_threads()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    build.build()
+    fw.load()
+    yield
+    assert fw.fw_device_status() == fw.FW_OK
+
+
+# ------------------------------------------------------------------ K1 DPFP
+@pytest.mark.parametrize("d_key", [8, 16, 32, 64, 128])
+@pytest.mark.parametrize("nu", [1, 2, 3])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_dpfp_parity(d_key, nu, io):
+    dt = inputs.torch_dtype(io)
+    g = torch.Generator().manual_seed(d_key * 10 + nu)
+    rows = 1000 + d_key  # several warps, ragged tail
+    x = torch.randn(rows, d_key, generator=g).to(dt)
+    phi = fw.fw_dpfp(x.cuda(), nu=nu, eps=1e-6)
+    torch.cuda.synchronize()
+    ref = oracle.dpfp(f64(x), nu, 1e-6)
+    assert tuple(phi.shape) == ref.shape
+    err = maxrel(f64(phi), ref)
+    assert err <= tol_for(dt), err
+    # elementwise: fp32 arithmetic, then one rounding to the output type
+    bound = (2.0 ** -8 if io == "bf16" else 1e-5) * np.abs(ref) + 1e-7 * np.abs(ref).max()
+    assert np.all(np.abs(f64(phi) - ref) <= bound)
+
+
+@pytest.mark.parametrize("in_io,out_io", [("bf16", "f32"), ("f32", "bf16")])
+def test_dpfp_mixed_dtypes(in_io, out_io):
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(333, 64, generator=g).to(inputs.torch_dtype(in_io))
+    phi = fw.fw_dpfp(x.cuda(), nu=2, out_dtype=inputs.torch_dtype(out_io))
+    ref = oracle.dpfp(f64(x), 2, 1e-6)
+    assert maxrel(f64(phi), ref) <= tol_for(inputs.torch_dtype(out_io))
+
+
+def test_dpfp_edge_cases():
+    # zero rows, all-zero keys (phi = 0, no NaN), the largest nu
+    x = torch.zeros(0, 64, device="cuda")
+    assert fw.fw_dpfp(x, nu=1).shape == (0, 128)
+    z = fw.fw_dpfp(torch.zeros(5, 16, device="cuda"), nu=3)
+    assert torch.all(z == 0)
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(37, 16, generator=g)
+    phi = fw.fw_dpfp(x.cuda(), nu=31)
+    assert maxrel(f64(phi), oracle.dpfp(f64(x), 31, 1e-6)) <= 1e-4
+
+
+# --------------------------------------------------------------- K2 forward
+def _forward_case(d, nu, chunk, W0=None, return_state=True):
+    dd = to_dev(d)
+    y, Wf = fw.fw_delta_forward(dd["q"], dd["k"], dd["v"], dd["beta"], W0=dd["W0"] if W0 is None else W0,
+                                nu=nu, chunk=chunk, return_state=return_state)
+    torch.cuda.synchronize()
+    assert fw.fw_device_status() == fw.FW_OK
+    y_ref, W_ref = oracle.delta_forward(f64(d["q"]), f64(d["k"]), f64(d["v"]), f64(d["beta"]),
+                                        None if d["W0"] is None else f64(d["W0"]), nu, 1e-6, NT)
+    return y, Wf, y_ref, W_ref
+
+
+@pytest.mark.parametrize("name", list(inputs.FORWARD_CONFIGS))
+def test_forward_configs(name):
+    cfg = inputs.FORWARD_CONFIGS[name]
+    d = inputs.forward_inputs(name, seed=0)
+    y, Wf, y_ref, W_ref = _forward_case(d, cfg["nu"], cfg["chunk"])
+    tol = tol_for(inputs.torch_dtype(cfg["io"]))
+    assert Wf.dtype == torch.float32 and tuple(Wf.shape) == W_ref.shape
+    assert Wf.is_contiguous() and Wf.stride() == torch.empty(W_ref.shape).stride()
+    ey, ew = maxrel(f64(y), y_ref), maxrel(f64(Wf), W_ref)
+    print(f"{name}: y maxrel {ey:.3e}  W_final maxrel {ew:.3e}")
+    assert ey <= tol and ew <= tol
+
+
+EDGE = [
+    # (B, H, L, d_key, nu, d_v, chunk, io, w0)
+    (1, 1, 1, 64, 1, 64, 64, "bf16", False),      # one token
+    (2, 3, 130, 64, 1, 64, 64, "bf16", True),     # ragged tail: 2 full chunks + 2
+    (1, 2, 100, 64, 2, 64, 32, "bf16", True),     # nu = 2, chunk 32, ragged
+    (1, 2, 77, 32, 2, 64, 16, "bf16", False),     # d_key 32, chunk 16
+    (2, 1, 65, 64, 1, 128, 64, "bf16", True),     # d_v != d_key
+    (1, 1, 200, 16, 3, 16, 64, "f32", True),      # fp32, several tiles
+    (2, 2, 33, 8, 1, 24, 16, "f32", False),       # fp32, odd d_v
+    (1, 1, 70, 128, 2, 32, 64, "f32", True),      # d_dot 512
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: "B{}H{}L{}dk{}nu{}dv{}C{}{}{}".format(
+    *c[:8], "w0" if c[8] else ""))
+def test_forward_edge_shapes(case):
+    B, H, L, d_key, nu, d_v, chunk, io, w0 = case
+    if fw.fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk,
+                                          inputs.torch_dtype(io)) == 0 and io == "bf16":
+        pass
+    d = inputs.random_forward_inputs(B, H, L, d_key, nu, d_v, io, 0.01 if w0 else None, seed=L)
+    y, Wf, y_ref, W_ref = _forward_case(d, nu, chunk)
+    tol = tol_for(inputs.torch_dtype(io))
+    assert maxrel(f64(y), y_ref) <= tol
+    assert maxrel(f64(Wf), W_ref) <= tol
+
+
+def test_forward_zero_keys_and_beta_zero():
+    d = inputs.random_forward_inputs(1, 2, 70, 64, 1, 64, "bf16", 0.01, seed=5)
+    d["k"][:, :, 10:20] = 0           # phi(k) = 0: no write, no NaN
+    d["beta"][:, 1] = 0               # head 1 never writes
+    y, Wf, y_ref, W_ref = _forward_case(d, 1, 64)
+    assert maxrel(f64(y), y_ref) <= 2e-2 and maxrel(f64(Wf), W_ref) <= 2e-2
+    assert maxrel(f64(Wf[:, 1]), f64(d["W0"][:, 1])) <= 1e-2
+
+
+def test_forward_in_place_state_and_no_state():
+    d = inputs.random_forward_inputs(2, 2, 90, 64, 1, 64, "bf16", 0.01, seed=6)
+    dd = to_dev(d)
+    W = dd["W0"].clone()
+    y1, W1 = fw.fw_delta_forward(dd["q"], dd["k"], dd["v"], dd["beta"], W0=W, W_final=W)
+    y2, none = fw.fw_delta_forward(dd["q"], dd["k"], dd["v"], dd["beta"], W0=dd["W0"],
+                                   return_state=False)
+    torch.cuda.synchronize()
+    assert none is None and W1.data_ptr() == W.data_ptr()
+    y_ref, W_ref = oracle.delta_forward(f64(d["q"]), f64(d["k"]), f64(d["v"]), f64(d["beta"]),
+                                        f64(d["W0"]), 1, 1e-6, NT)
+    assert maxrel(f64(W), W_ref) <= 2e-2
+    assert maxrel(f64(y1), y_ref) <= 2e-2 and maxrel(f64(y2), y_ref) <= 2e-2
+
+
+def test_forward_empty_sequence():
+    d = inputs.random_forward_inputs(2, 2, 1, 64, 1, 64, "bf16", 0.01, seed=1)
+    dd = to_dev(d)
+    e = lambda t: t[:, :, :0].contiguous()
+    y, Wf = fw.fw_delta_forward(e(dd["q"]), e(dd["k"]), e(dd["v"]), e(dd["beta"]), W0=dd["W0"])
+    torch.cuda.synchronize()
+    assert y.shape == (2, 2, 0, 64) and torch.equal(Wf, dd["W0"])
+
+
+def test_forward_resume_equals_whole():
+    """forward(first part) then forward(rest, W0 = W_final) = forward(all)."""
+    d = inputs.random_forward_inputs(1, 4, 256, 64, 1, 64, "bf16", 0.01, seed=9)
+    dd = to_dev(d)
+    y, W = fw.fw_delta_forward(dd["q"], dd["k"], dd["v"], dd["beta"], W0=dd["W0"])
+    sl = lambda t, a, b: t[:, :, a:b].contiguous()
+    ya, Wa = fw.fw_delta_forward(*(sl(dd[n], 0, 100) for n in ("q", "k", "v", "beta")), W0=dd["W0"])
+    yb, Wb = fw.fw_delta_forward(*(sl(dd[n], 100, 256) for n in ("q", "k", "v", "beta")), W0=Wa)
+    torch.cuda.synchronize()
+    assert maxrel(f64(torch.cat([ya, yb], 2)), f64(y)) <= 2e-2
+    assert maxrel(f64(Wb), f64(W)) <= 2e-2
+
+
+# ---------------------------------------------------------------- K3 decode
+def test_decode_small_stepped():
+    B, H, d_key, nu, d_v, steps = 3, 2, 64, 2, 128, 6
+    d = inputs.decode_inputs(B, H, d_key, nu, d_v, steps, "bf16", w0_var=0.01, seed=2)
+    W = d["W0"].cuda()
+    Wr = f64(d["W0"])
+    for t in range(steps):
+        y = fw.fw_delta_decode_step(d["q"][t].cuda(), d["k"][t].cuda(), d["v"][t].cuda(),
+                                    d["beta"][t].cuda(), W, nu=nu)
+        y_ref, Wr = oracle.delta_decode_step(f64(d["q"][t]), f64(d["k"][t]), f64(d["v"][t]),
+                                             f64(d["beta"][t]), Wr, nu, 1e-6, NT)
+        assert maxrel(f64(y), y_ref) <= 2e-2
+    assert maxrel(f64(W), Wr) <= 2e-2
+
+
+def test_decode_f32():
+    d = inputs.decode_inputs(2, 3, 16, 3, 20, 4, "f32", w0_var=0.01, seed=4)
+    W = d["W0"].cuda()
+    Wr = f64(d["W0"])
+    for t in range(4):
+        y = fw.fw_delta_decode_step(d["q"][t].cuda(), d["k"][t].cuda(), d["v"][t].cuda(),
+                                    d["beta"][t].cuda(), W, nu=3)
+        y_ref, Wr = oracle.delta_decode_step(f64(d["q"][t]), f64(d["k"][t]), f64(d["v"][t]),
+                                             f64(d["beta"][t]), Wr, 3, 1e-6, NT)
+        assert maxrel(f64(y), y_ref) <= 1e-4
+    assert maxrel(f64(W), Wr) <= 1e-4
+
+
+def test_decode_full_size_sampled():
+    """The 256 x 16 x 128 x 256 fp32 state over 128 tokens, checked on a
+    sample of (b, h) pairs the oracle recomputes one by one."""
+    cfg = inputs.DECODE_CONFIGS["decode_b256"]
+    B, H, d_key, nu, d_v, steps = (cfg[n] for n in ("B", "H", "d_key", "nu", "d_v", "steps"))
+    d = inputs.decode_inputs(B, H, d_key, nu, d_v, steps, cfg["io"], seed=0)
+    dd = to_dev(d)
+    W = dd["W0"].clone()
+    ys = []
+    for t in range(steps):
+        ys.append(fw.fw_delta_decode_step(dd["q"][t], dd["k"][t], dd["v"][t], dd["beta"][t], W, nu=nu))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    pairs = [(int(b), int(h)) for b, h in zip(rng.integers(0, B, 12), rng.integers(0, H, 12))]
+    pairs += [(0, 0), (B - 1, H - 1)]
+    for b, h in pairs:
+        sel = lambda t: f64(t[:, b:b + 1, h:h + 1])
+        Wr = f64(d["W0"][b:b + 1, h:h + 1])
+        for t in range(steps):
+            y_ref, Wr = oracle.delta_decode_step(sel(d["q"])[t], sel(d["k"])[t], sel(d["v"])[t],
+                                                 sel(d["beta"])[t], Wr, nu, 1e-6)
+            assert maxrel(f64(ys[t][b:b + 1, h:h + 1]), y_ref) <= 2e-2, (b, h, t)
+        assert maxrel(f64(W[b:b + 1, h:h + 1]), Wr) <= 2e-2, (b, h)
+
+
+def test_decode_stepped_equals_forward():
+    """Training and inference kernels agree: the decode step over L tokens
+    equals the chunked forward over the same tokens."""
+    d = inputs.random_forward_inputs(2, 4, 96, 64, 1, 64, "bf16", 0.01, seed=12)
+    dd = to_dev(d)
+    y, Wf = fw.fw_delta_forward(dd["q"], dd["k"], dd["v"], dd["beta"], W0=dd["W0"])
+    W = dd["W0"].clone()
+    ys = [fw.fw_delta_decode_step(dd["q"][:, :, t].contiguous(), dd["k"][:, :, t].contiguous(),
+                                  dd["v"][:, :, t].contiguous(), dd["beta"][:, :, t].contiguous(), W)
+          for t in range(96)]
+    torch.cuda.synchronize()
+    assert maxrel(f64(torch.stack(ys, 2)), f64(y)) <= 2e-2
+    assert maxrel(f64(W), f64(Wf)) <= 2e-2
