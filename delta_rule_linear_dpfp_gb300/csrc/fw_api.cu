@@ -83,13 +83,15 @@ FW_API const char *fw_status_string(int status) {
 
 FW_API int fw_dpfp(const void *x, void *phi, int64_t rows, int d_key, int nu, int in_dtype,
                    int out_dtype, float eps, void *stream) {
-    if (!x || !phi || !aligned16(x) || !aligned16(phi) || rows < 0 || d_key <= 0 || nu < 1 ||
-        nu > 2 * d_key - 1 || !dtype_ok(in_dtype) || !dtype_ok(out_dtype) || !eps_ok(eps))
+    if (rows < 0 || d_key <= 0 || nu < 1 || nu > 2 * d_key - 1 || !dtype_ok(in_dtype) ||
+        !dtype_ok(out_dtype) || !eps_ok(eps))
         return FW_ERR_INVALID_ARG;
     if (!dkey_supported(d_key))
         return FW_ERR_UNSUPPORTED;
     if (rows == 0)
-        return FW_OK;
+        return FW_OK; // empty: the pointers are not used and may be NULL
+    if (!x || !phi || !aligned16(x) || !aligned16(phi))
+        return FW_ERR_INVALID_ARG;
     DeviceInfo di;
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess)
@@ -130,22 +132,27 @@ FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const v
                             const float *W0, float *W_final, void *y, void *workspace,
                             size_t workspace_bytes, int B, int H, int L, int d_key, int nu,
                             int d_v, int chunk, int io_dtype, float eps, void *stream) {
-    if (!q || !k || !v || !beta || !y || !eps_ok(eps))
-        return FW_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) || !aligned16(y) ||
-        (W0 && !aligned16(W0)) || (W_final && !aligned16(W_final)) ||
-        (workspace && !aligned16(workspace)))
+    if (!eps_ok(eps))
         return FW_ERR_INVALID_ARG;
     const int rc = check_forward_shape(B, H, L, d_key, nu, d_v, chunk, io_dtype);
     if (rc != FW_OK)
         return rc;
-    const size_t need = fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk, io_dtype);
-    if (need > 0 && (!workspace || workspace_bytes < need))
-        return FW_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t BH = (int64_t)B * H;
     if (BH == 0)
-        return FW_OK;
+        return FW_OK; // empty: no pointer is used and any may be NULL
+    if ((W0 && !aligned16(W0)) || (W_final && !aligned16(W_final)))
+        return FW_ERR_INVALID_ARG;
+    if (L > 0) {
+        if (!q || !k || !v || !beta || !y)
+            return FW_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) || !aligned16(y) ||
+            (workspace && !aligned16(workspace)))
+            return FW_ERR_INVALID_ARG;
+        const size_t need = fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk, io_dtype);
+        if (need > 0 && (!workspace || workspace_bytes < need))
+            return FW_ERR_INVALID_ARG;
+    }
     if (BH > (int64_t)1 << 30)
         return FW_ERR_UNSUPPORTED;
     const int d_dot = 2 * d_key * nu;
@@ -176,17 +183,19 @@ FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const v
 FW_API int fw_delta_decode_step(const void *q, const void *k, const void *v, const void *beta,
                                 float *W, void *y, int B, int H, int d_key, int nu, int d_v,
                                 int io_dtype, float eps, void *stream) {
-    if (!q || !k || !v || !beta || !W || !y || !eps_ok(eps) || B < 0 || H < 0 || d_key <= 0 ||
-        d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 || !dtype_ok(io_dtype))
-        return FW_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) || !aligned16(W) ||
-        !aligned16(y))
+    if (!eps_ok(eps) || B < 0 || H < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 ||
+        !dtype_ok(io_dtype))
         return FW_ERR_INVALID_ARG;
     if (!dkey_supported(d_key) || 2 * d_key * nu > 1024)
         return FW_ERR_UNSUPPORTED;
     const int64_t BH = (int64_t)B * H;
     if (BH == 0)
-        return FW_OK;
+        return FW_OK; // empty: no pointer is used and any may be NULL
+    if (!q || !k || !v || !beta || !W || !y)
+        return FW_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) || !aligned16(W) ||
+        !aligned16(y))
+        return FW_ERR_INVALID_ARG;
     if (BH > (int64_t)1 << 30)
         return FW_ERR_UNSUPPORTED;
     DeviceInfo di;

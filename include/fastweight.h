@@ -36,6 +36,9 @@
  *   - Every argument is checked on the host BEFORE anything is enqueued: a
  *     call that returns an error has launched nothing and touched no memory.
  *   - Pointers must be 16-byte aligned (FW_ERR_INVALID_ARG otherwise).
+ *     When an operation is empty (rows == 0, B*H == 0, or L == 0 for the
+ *     activations of fw_delta_forward) the pointers of the empty tensors are
+ *     not used and may be NULL.
  *   - No call has a CPU fallback: shapes outside the compiled tile set give
  *     FW_ERR_UNSUPPORTED.
  *   - Return values are fw_status codes; fw_status_string() names them.

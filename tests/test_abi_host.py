@@ -58,6 +58,7 @@ def test_dpfp_argument_checks(lib):
     assert call(FAKE, FAKE, 4, 64, 1, 0, 0, float("nan"), None) == E
     assert call(FAKE, FAKE, 4, 12, 1, 0, 0, 1e-6, None) == U        # d_key not compiled
     assert call(FAKE, FAKE, 0, 64, 1, 0, 0, 1e-6, None) == OK       # empty: nothing enqueued
+    assert call(None, None, 0, 64, 1, 0, 0, 1e-6, None) == OK       # empty tensors may be NULL
 
 
 def _fwd(lib, **kw):
@@ -87,8 +88,9 @@ def test_forward_argument_checks(lib):
     if need > 0:
         assert _fwd(lib, ws=None, wsb=0) == E
         assert _fwd(lib, ws=FAKE, wsb=need - 1) == E
-    # empty batch: nothing to do, nothing enqueued
+    # empty batch: nothing to do, nothing enqueued, NULL pointers allowed
     assert _fwd(lib, B=0, ws=FAKE, wsb=1 << 40) == OK
+    assert _fwd(lib, B=0, q=None, k=None, v=None, beta=None, y=None) == OK
 
 
 def test_forward_workspace_query(lib):
