@@ -22,9 +22,9 @@ FW_ERR_TIMEOUT = 4
 FW_DTYPE_F32 = 0
 FW_DTYPE_BF16 = 1
 
-#: every entry point include/fastweight.h declares
+#: every entry point include/*.h declares
 EXPORTS = ("fw_status_string", "fw_dpfp", "fw_delta_forward_workspace_size", "fw_delta_forward",
-           "fw_delta_decode_step", "fw_device_status")
+           "fw_delta_decode_step", "fw_device_status", "fw_selftest_umma")
 
 _lib = None
 
@@ -62,6 +62,8 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.fw_delta_decode_step.argtypes = [vp] * 6 + [i32] * 6 + [f32, vp]
     lib.fw_device_status.restype = i32
     lib.fw_device_status.argtypes = [vp]
+    lib.fw_selftest_umma.restype = i32
+    lib.fw_selftest_umma.argtypes = [vp, vp, vp] + [i32] * 5 + [vp]
     if path is None:
         _lib = lib
     return lib
@@ -171,3 +173,16 @@ def fw_delta_decode_step(q, k, v, beta, W, nu: int = 1, eps: float = 1e-6, y=Non
 def fw_device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status code."""
     return int(load().fw_device_status(_stream(stream)))
+
+
+def fw_selftest_umma(A, B, a_mn: int = 0, b_mn: int = 0, swap_mn: int = 0, stream=None):
+    """D = A B^T through one tcgen05 MMA chain (A [128,K], B [N,K] fp32 CUDA
+    tensors holding bf16-representable values).  Returns D [128,N] fp32."""
+    _dev(A, "A")
+    _dev(B, "B")
+    K = A.shape[1]
+    N = B.shape[0]
+    D = torch.empty(128, N, dtype=torch.float32, device=A.device)
+    rc = load().fw_selftest_umma(_ptr(A), _ptr(B), _ptr(D), N, K, a_mn, b_mn, swap_mn, _stream(stream))
+    _check(rc, "fw_selftest_umma")
+    return D

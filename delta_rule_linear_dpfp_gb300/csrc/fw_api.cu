@@ -68,6 +68,17 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? FW_OK : FW_ERR_CUDA; 
 
 } // namespace
 
+namespace fw {
+// Address of the current device's status word (for the self-test entry points).
+cudaError_t status_word(unsigned **out) {
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e == cudaSuccess)
+        *out = di.status;
+    return e;
+}
+} // namespace fw
+
 extern "C" {
 
 FW_API const char *fw_status_string(int status) {

@@ -2,6 +2,7 @@
 every symbol include/fastweight.h declares, and rejects bad arguments before
 touching CUDA."""
 import ctypes
+import glob
 import os
 import re
 
@@ -10,7 +11,7 @@ import pytest
 from delta_rule_linear_dpfp_gb300 import binding, build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "fastweight.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 # a non-null, 16-byte aligned address that is never dereferenced: every call
 # below fails its host-side checks before any CUDA call
@@ -25,8 +26,10 @@ def lib():
 
 
 def declared_symbols():
-    text = open(HEADER).read()
-    return sorted(set(re.findall(r"FW_API[^;(]*?\b(fw_\w+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        names |= set(re.findall(r"FW_API[^;(]*?\b(fw_\w+)\s*\(", open(h).read()))
+    return sorted(names)
 
 
 def test_header_declares_the_binding_exports():
@@ -36,6 +39,22 @@ def test_header_declares_the_binding_exports():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_symbols():
         assert hasattr(lib, name), name
+
+
+def _prototypes():
+    """name -> parameter count of every FW_API function in include/*.h."""
+    protos = {}
+    for h in HEADERS:
+        text = open(h).read()
+        for m in re.finditer(r"FW_API[^;(]*?\b(fw_\w+)\s*\(([^)]*)\)", text):
+            params = [p for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+            protos[m.group(1)] = len(params)
+    return protos
+
+
+def test_binding_signatures_match_the_headers(lib):
+    for name, n in _prototypes().items():
+        assert len(getattr(lib, name).argtypes) == n, name
 
 
 def test_status_strings(lib):
