@@ -296,9 +296,11 @@ def run_ours(args, rank, world, local_rank):
 
 
 # the forward's launches per call and the kernel the roofline is taken on
-FORWARD_LAUNCHES = 1
-FORWARD_KERNEL_KEY = "rowscan_kernel<bf16>"
-FORWARD_SOURCES = ["delta_rule_linear_dpfp_gb300/csrc/fw_rowscan.cu"]
+FORWARD_LAUNCHES = 2
+FORWARD_KERNEL_KEY = "fw_delta_forward (chunk_prep_kernel + chunk_scan_kernel)"
+FORWARD_SOURCES = ["delta_rule_linear_dpfp_gb300/csrc/fw_forward_tc.cu",
+                   "delta_rule_linear_dpfp_gb300/csrc/fw_tc.cuh",
+                   "delta_rule_linear_dpfp_gb300/csrc/fw_dpfp.cuh"]
 
 
 def forward_kernel_ms(fw, sets, y, Wf, ws, nu, C, stream, reps=200):

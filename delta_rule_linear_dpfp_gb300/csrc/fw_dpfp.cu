@@ -16,42 +16,11 @@
 // static and the roll costs 8 warp shuffles per block.  The first pass sums
 // the products (reduced over the G lanes with xor shuffles), the second
 // recomputes them, divides and writes 8 outputs per lane with 16-byte stores.
-#include "fw_common.cuh"
+#include "fw_dpfp.cuh"
 
 namespace fw {
 
 namespace {
-
-// Products x[8g+c] * x[(8g+c-i) mod n] for c = 0..7 with i = 8*qs + R.
-template <int G, int R>
-FW_DEV void dpfp_block(const float (&x)[8], float (&p)[8], int g, int base_lane, int qs) {
-    const int src0 = base_lane + ((g - qs) % G + G) % G;     // holds x[8(g-qs) + .]
-    const int src1 = base_lane + ((g - qs - 1) % G + G) % G; // holds x[8(g-qs-1) + .]
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        float rolled;
-        if (c >= R)
-            rolled = __shfl_sync(0xffffffffu, x[c - R], src0);
-        else
-            rolled = __shfl_sync(0xffffffffu, x[c - R + 8], src1);
-        p[c] = x[c] * rolled;
-    }
-}
-
-template <int G>
-FW_DEV void dpfp_block_dispatch(const float (&x)[8], float (&p)[8], int g, int base_lane, int i) {
-    const int qs = i >> 3;
-    switch (i & 7) {
-    case 0: dpfp_block<G, 0>(x, p, g, base_lane, qs); break;
-    case 1: dpfp_block<G, 1>(x, p, g, base_lane, qs); break;
-    case 2: dpfp_block<G, 2>(x, p, g, base_lane, qs); break;
-    case 3: dpfp_block<G, 3>(x, p, g, base_lane, qs); break;
-    case 4: dpfp_block<G, 4>(x, p, g, base_lane, qs); break;
-    case 5: dpfp_block<G, 5>(x, p, g, base_lane, qs); break;
-    case 6: dpfp_block<G, 6>(x, p, g, base_lane, qs); break;
-    default: dpfp_block<G, 7>(x, p, g, base_lane, qs); break;
-    }
-}
 
 template <int DK, typename Tin, typename Tout>
 __global__ void __launch_bounds__(256) dpfp_kernel(const Tin *__restrict__ xin, Tout *__restrict__ out,
@@ -69,33 +38,9 @@ __global__ void __launch_bounds__(256) dpfp_kernel(const Tin *__restrict__ xin, 
         const int64_t row = wid * RPW + lane / G;
         const bool valid = row < rows;
         float x[8];
-        {
-            float kv[8];
-            const int kofs = 8 * (g % (G / 2));
-            if (valid) {
-                load8(xin + row * DK + kofs, kv);
-            } else {
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    kv[c] = 0.f;
-            }
-            const bool neg = g >= G / 2;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                x[c] = fmaxf(neg ? -kv[c] : kv[c], 0.f);
-        }
+        dpfp_load_x<G>(xin + row * DK, g, valid, x);
         // pass 1: the sum of all products
-        float s = 0.f;
-        for (int i = 1; i <= nu; ++i) {
-            float p[8];
-            dpfp_block_dispatch<G>(x, p, g, base_lane, i);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                s += p[c];
-        }
-#pragma unroll
-        for (int o = G / 2; o > 0; o >>= 1)
-            s += __shfl_xor_sync(0xffffffffu, s, o);
+        const float s = dpfp_row_sum<G>(x, g, base_lane, nu);
         const float denom = s + eps;
         // pass 2: recompute, normalise, store
         Tout *orow = out + row * d_dot + 8 * g;

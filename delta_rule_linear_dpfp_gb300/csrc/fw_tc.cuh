@@ -93,8 +93,8 @@ FW_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;
 FW_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // 32 lanes x 32 bit, 16 consecutive columns: this thread gets lane
-// (taddr.lane + laneid), columns taddr.col .. +15.
-FW_DEV void tmem_ld16(uint32_t taddr, float (&r)[16]) {
+// (taddr.lane + laneid), columns taddr.col .. +15, into r[0..15].
+FW_DEV void tmem_ld16(uint32_t taddr, float *r) {
     uint32_t u[16];
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
                  "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -108,7 +108,8 @@ FW_DEV void tmem_ld16(uint32_t taddr, float (&r)[16]) {
 }
 FW_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-FW_DEV void tmem_st16(uint32_t taddr, const float (&r)[16]) {
+// Store r[0..15] to lane (taddr.lane + laneid), columns taddr.col .. +15.
+FW_DEV void tmem_st16(uint32_t taddr, const float *r) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
                  "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
                  "r"(__float_as_uint(r[0])), "r"(__float_as_uint(r[1])), "r"(__float_as_uint(r[2])),
