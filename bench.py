@@ -147,6 +147,21 @@ def recorded_traffic(kernel_key, sources):
     return rec.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(x, world, device):
+    """The slowest rank's value (the job finishes when the last rank does)."""
+    if world <= 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(rank, s):
+    """Seed of input set s of rank `rank`: every rank runs its own replica
+    (weak scaling), so the ranks' batches are independent draws."""
+    return 1000 * rank + s
+
+
 # ----------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     from delta_rule_linear_dpfp_gb300 import binding as fw
@@ -163,12 +178,12 @@ def run_ours(args, rank, world, local_rank):
     dt = inputs.torch_dtype(cfg["io"])
     io_bytes = 2 if dt == torch.bfloat16 else 4
 
-    host = inputs.forward_inputs(WORKLOAD, seed=rank)
+    host = inputs.forward_inputs(WORKLOAD, seed=replica_seed(rank, 0))
     set_bytes = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     nsets = max(2, math.ceil(3 * L2_BYTES / set_bytes))
     sets = []
     for s in range(nsets):
-        d = inputs.forward_inputs(WORKLOAD, seed=1000 * rank + s) if s else host
+        d = inputs.forward_inputs(WORKLOAD, seed=replica_seed(rank, s)) if s else host
         sets.append({k: (None if v is None else v.to(dev)) for k, v in d.items()})
     y = torch.empty(B, H, L, d_v, dtype=dt, device=dev)
     Wf = torch.empty(B, H, d_v, d_dot, dtype=torch.float32, device=dev)
@@ -203,11 +218,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_step = ms_total / args.steps
     tokens_per_step = B * L
     value = tokens_per_step * world / (ms_step * 1e-3)
@@ -239,11 +250,7 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
 
     # ----------------------------------------------------------- roofline
     pk = peaks()
