@@ -24,7 +24,11 @@ FW_DTYPE_BF16 = 1
 
 #: every entry point include/*.h declares
 EXPORTS = ("fw_status_string", "fw_dpfp", "fw_delta_forward_workspace_size", "fw_delta_forward",
-           "fw_delta_decode_step", "fw_device_status", "fw_selftest_umma")
+           "fw_delta_decode_step", "fw_device_status", "fw_selftest_umma",
+           "fw_delta_forward_noalloc")
+
+#: bytes of the library's own scratch array behind fw_delta_forward_noalloc
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
 
@@ -62,6 +66,8 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.fw_delta_decode_step.argtypes = [vp] * 6 + [i32] * 6 + [f32, vp]
     lib.fw_device_status.restype = i32
     lib.fw_device_status.argtypes = [vp]
+    lib.fw_delta_forward_noalloc.restype = i32
+    lib.fw_delta_forward_noalloc.argtypes = [vp] * 7 + [i32] * 8 + [f32, vp]
     lib.fw_selftest_umma.restype = i32
     lib.fw_selftest_umma.argtypes = [vp, vp, vp] + [i32] * 5 + [vp]
     if path is None:
@@ -150,6 +156,36 @@ def fw_delta_forward(q, k, v, beta, W0=None, nu: int = 1, chunk: int = 64, eps: 
                                  _ptr(y), _ptr(workspace), ws_bytes, B, H, L, d_key, nu, d_v, chunk,
                                  code, eps, _stream(stream))
     _check(rc, "fw_delta_forward")
+    return y, W_final
+
+
+def fw_delta_forward_noalloc(q, k, v, beta, W0=None, nu: int = 1, chunk: int = 64,
+                             eps: float = 1e-6, return_state: bool = True, y=None, W_final=None,
+                             stream=None):
+    """fw_delta_forward without a caller-provided workspace: the library uses
+    its own fixed scratch array (NOALLOC_SCRATCH_BYTES per GPU) and allocates
+    nothing.  For callers that cannot allocate device memory when they call
+    the forward.  Outputs passed in as y / W_final are used as they are;
+    missing ones are created here with PyTorch before the call."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
+        _dev(t, name)
+    B, H, L, d_key = q.shape
+    d_v = v.shape[-1]
+    d_dot = 2 * d_key * nu
+    if k.shape != q.shape or v.shape != (B, H, L, d_v) or beta.shape != (B, H, L):
+        raise ValueError("shape mismatch among q, k, v, beta")
+    if W0 is not None:
+        _dev(W0, "W0")
+        if W0.dtype != torch.float32 or W0.shape != (B, H, d_v, d_dot):
+            raise ValueError("W0 must be fp32 [B,H,d_v,d_dot]")
+    if y is None:
+        y = torch.empty(B, H, L, d_v, dtype=q.dtype, device=q.device)
+    if W_final is None and return_state:
+        W_final = torch.empty(B, H, d_v, d_dot, dtype=torch.float32, device=q.device)
+    rc = load().fw_delta_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(W0),
+                                         _ptr(W_final), _ptr(y), B, H, L, d_key, nu, d_v, chunk,
+                                         _dtype_code(q.dtype), eps, _stream(stream))
+    _check(rc, "fw_delta_forward_noalloc")
     return y, W_final
 
 

@@ -139,6 +139,43 @@ FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const v
                             size_t workspace_bytes, int B, int H, int L, int d_key, int nu,
                             int d_v, int chunk, int io_dtype, float eps, void *stream);
 
+/* Size of the library's own scratch array used by fw_delta_forward_noalloc. */
+#define FW_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * fw_delta_forward_noalloc -- fw_delta_forward for callers that must not
+ * allocate device memory at call time.  The pages have no counterpart: this
+ * is an interface variant, not part of the method.
+ *
+ * Who needs it: a host program whose memory pool owns the GPU's memory and
+ * forbids further cudaMalloc, or a serving loop that cannot afford the
+ * implicit device synchronisation cudaMalloc / cudaFree may cause.  Such a
+ * caller cannot hand fw_delta_forward a workspace it would first have to
+ * allocate.
+ *
+ * What it does: the bf16 path's workspace is taken from a fixed array inside
+ * the library, FW_NOALLOC_SCRATCH_BYTES (64 MiB) on every GPU where the
+ * library's device code is loaded, held until the process exits.  Then the
+ * same checks and kernels as fw_delta_forward run, with the same arguments
+ * minus the workspace pair.  No cudaMalloc, cudaFree or other allocating call
+ * is made.
+ *   - Shapes whose workspace (fw_delta_forward_workspace_size) exceeds
+ *     FW_NOALLOC_SCRATCH_BYTES return FW_ERR_UNSUPPORTED before anything is
+ *     enqueued.  fp32 I/O needs no workspace and is never limited.
+ *   - The array's device address is looked up (cudaGetSymbolAddress) the
+ *     first time this function runs on a device, with that device current;
+ *     make that first call before any stream capture on the device.
+ *   - Every call on a device shares the one array, and its contents from the
+ *     previous call are left in place (nothing needs them to be zero).  Calls
+ *     that may run at the same time on the GPU (different streams without an
+ *     ordering between them) race on it and give undefined results: order
+ *     them, e.g. by issuing them on one stream.
+ */
+FW_API int fw_delta_forward_noalloc(const void *q, const void *k, const void *v, const void *beta,
+                                    const float *W0, float *W_final, void *y, int B, int H, int L,
+                                    int d_key, int nu, int d_v, int chunk, int io_dtype, float eps,
+                                    void *stream);
+
 /*
  * fw_delta_decode_step -- one new token per (batch, head) against a
  * persistent fast-weight state, updated in place.  Every element of W is read
