@@ -13,14 +13,21 @@
 // shift i = 8*qs + r the rolled entry needed at x[8g + c] sits in lane
 // g - qs (or g - qs - 1) of the same row group at register (c - r) mod 8;
 // r is dispatched to a compile-time case so every register index stays
-// static and the roll costs 8 warp shuffles per block.  The first pass sums
-// the products (reduced over the G lanes with xor shuffles), the second
-// recomputes them, divides and writes 8 outputs per lane with 16-byte stores.
+// static and the roll costs 8 warp shuffles per block.  The products are
+// summed (reduced over the G lanes with xor shuffles), scaled by one
+// reciprocal of (sum + eps) per row and written 8 per lane with 16-byte
+// stores; for nu <= 4 they stay in registers between the two steps, beyond
+// that they are recomputed.
 #include "fw_dpfp.cuh"
 
 namespace fw {
 
 namespace {
+
+// Products of the first NUC blocks kept in registers (one shuffle pass) when
+// nu <= NUC; otherwise a second pass recomputes them.  The normaliser is
+// applied as one reciprocal per row.
+constexpr int NUC = 4;
 
 template <int DK, typename Tin, typename Tout>
 __global__ void __launch_bounds__(256) dpfp_kernel(const Tin *__restrict__ xin, Tout *__restrict__ out,
@@ -38,20 +45,45 @@ __global__ void __launch_bounds__(256) dpfp_kernel(const Tin *__restrict__ xin, 
         const int64_t row = wid * RPW + lane / G;
         const bool valid = row < rows;
         float x[8];
-        dpfp_load_x<G>(xin + row * DK, g, valid, x);
-        // pass 1: the sum of all products
-        const float s = dpfp_row_sum<G>(x, g, base_lane, nu);
-        const float denom = s + eps;
-        // pass 2: recompute, normalise, store
+        dpfp_load_x<G>(xin + (valid ? row : 0) * DK, g, valid, x);
         Tout *orow = out + row * d_dot + 8 * g;
-        for (int i = 1; i <= nu; ++i) {
-            float p[8];
-            dpfp_block_dispatch<G>(x, p, g, base_lane, i);
+        if (nu <= NUC) {
+            float p[NUC][8];
+            float s = 0.f;
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                p[c] = __fdiv_rn(p[c], denom);
-            if (valid)
-                store8(orow + (int64_t)(i - 1) * N, p);
+            for (int i = 0; i < NUC; ++i) {
+                if (i < nu) {
+                    dpfp_block_dispatch<G>(x, p[i], g, base_lane, i + 1); // i is static once unrolled
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        s += p[i][c];
+                }
+            }
+#pragma unroll
+            for (int o = G / 2; o > 0; o >>= 1)
+                s += __shfl_xor_sync(0xffffffffu, s, o);
+            const float inv = 1.0f / (s + eps);
+#pragma unroll
+            for (int i = 0; i < NUC; ++i) {
+                if (i < nu) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        p[i][c] *= inv;
+                    if (valid)
+                        store8(orow + (int64_t)i * N, p[i]);
+                }
+            }
+        } else {
+            const float inv = 1.0f / (dpfp_row_sum<G>(x, g, base_lane, nu) + eps);
+            for (int i = 1; i <= nu; ++i) {
+                float p[8];
+                dpfp_block_dispatch<G>(x, p, g, base_lane, i);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    p[c] *= inv;
+                if (valid)
+                    store8(orow + (int64_t)(i - 1) * N, p);
+            }
         }
     }
 }

@@ -1,14 +1,10 @@
 // fw_rowscan.cu -- the token-serial delta rule on CUDA cores, fp32 throughout.
 //
-// Serves two entry points:
-//   * fw_delta_forward with fp32 I/O (the exact-arithmetic path: fp32 FMA, no
-//     tensor cores), and
-//   * fw_delta_decode_step (K3), the L = 1 case, which streams every row of
-//     the persistent state once from HBM and once back.
+// Serves fw_delta_forward with fp32 I/O: the exact-arithmetic path (fp32
+// FMA, no tensor cores), token by token.
 //
 // Method (Fast Weights Transformer guide, section "FastWeightsAttention: the
-// new update rule" and its forward-pass loop; section "token_wise variant"
-// for the decode step): per token t,
+// new update rule" and its forward-pass loop): per token t,
 //   vbar = W phi(k_t);  W += beta_t (v_t - vbar) phi(k_t)^T;  y_t = W phi(q_t).
 // Each row of W evolves on its own (row r only needs v_t[r]), so the work is
 // split over (batch, head, block of 16 rows): one warp owns two rows, each
@@ -218,15 +214,3 @@ cudaError_t launch_rowscan(const void *q, const void *k, const void *v, const vo
 
 } // namespace fw
 
-namespace fw {
-
-// K3, the decode step: the token-serial kernel over one token, with the
-// persistent state read and written in place.
-cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *beta, float *W,
-                          void *y, int BH, int d_key, int nu, int d_v, int bf16, float eps,
-                          int num_sms, cudaStream_t st) {
-    (void)num_sms;
-    return launch_rowscan(q, k, v, beta, W, W, y, BH, 1, d_key, nu, d_v, bf16, eps, st);
-}
-
-} // namespace fw
