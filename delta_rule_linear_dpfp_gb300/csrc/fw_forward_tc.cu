@@ -150,7 +150,7 @@ FW_DEV void unit_lower_inverse(const float *A, float *N, float *R, int tid) {
 
 // ---------------------------------------------------------------------------
 template <int DK>
-__global__ void __launch_bounds__(kPrepThreads, 1)
+__global__ void __launch_bounds__(kPrepThreads, 2)
     chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                       const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ beta,
                       uint8_t *__restrict__ ws, int L, int C, int nch, int nu, int Dp, int d_v, float eps,
@@ -158,16 +158,15 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     constexpr int G = DK / 4, RPW = 32 / G, N2 = 2 * DK;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    const int VB = (d_v + 63) / 64;
     uint8_t *kq = smem;                                  // [K; Q]: 128 x Dp, K-major
-    uint8_t *vt = kq + 256 * Dp;                         // V: rows t, columns v (MN-major B)
-    uint8_t *ip = vt + VB * 8192;                        // [I; P]: 128 x 64, K-major A
+    uint8_t *ip = kq + 256 * Dp;                         // [I; P]: 128 x 64, K-major A
+    uint8_t *tp = ip;                                    // [T; P T] replaces [I; P] once read
     uint8_t *tt = ip + 16384;                            // T: rows k, columns n (MN-major B)
-    uint8_t *tp = tt + 8192;                             // [T; P T]: 128 x 64, K-major A
-    float *Am = (float *)(tp + 16384);                   // A = strict_lower(beta K K^T)
+    float *Am = (float *)(tt + 8192);                    // A = strict_lower(beta K K^T)
     float *Nm = Am + 64 * LDS;                           // (I + A)^-1
     float *Rm = Nm + 64 * LDS;                           // block-solve scratch [16][LDS]
     float *bs = Rm + 16 * LDS;                           // beta (0 on padded rows)
+    uint8_t *vt = (uint8_t *)Am;                         // V (MN-major B), once A and N are done
     uint64_t *bar = (uint64_t *)(bs + 64);
     uint32_t *slot = (uint32_t *)(bar + 1);
 
@@ -192,29 +191,45 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     }
     if (tid < 64)
         bs[tid] = tid < Lc ? __bfloat162float(beta[bh * L + t0 + tid]) : 0.f;
-    // V rows of the chunk -> MN-major operand tile (zero on padded rows)
-    {
-        const int cpr = d_v / 8;
-        for (int idx = tid; idx < 64 * cpr; idx += kPrepThreads) {
-            const int t = idx / cpr, j = 8 * (idx % cpr);
-            uint4 u = make_uint4(0, 0, 0, 0);
-            if (t < Lc)
-                u = __ldg(reinterpret_cast<const uint4 *>(v + ((size_t)bh * L + t0 + t) * d_v + j));
-            const uint32_t off = (uint32_t)(j >> 6) * 8192u + (uint32_t)t * 128u +
-                                 ((uint32_t)(((j & 63) >> 3) ^ (t & 7)) << 4);
-            *reinterpret_cast<uint4 *>(vt + off) = u;
-        }
+    // V rows of the chunk, held in registers until their tile's space is free
+    // (64 rows x d_v/8 chunks of 16 bytes; zero on padded rows)
+    constexpr int kVChunks = 4; // 64 * 128 / 8 / kPrepThreads
+    uint4 vpre[kVChunks];
+    const int vcpr = d_v / 8;
+#pragma unroll
+    for (int i = 0; i < kVChunks; ++i) {
+        const int idx = tid + i * kPrepThreads, t = idx / vcpr, j = 8 * (idx % vcpr);
+        vpre[i] = make_uint4(0, 0, 0, 0);
+        if (idx < 64 * vcpr && t < Lc)
+            vpre[i] = __ldg(reinterpret_cast<const uint4 *>(v + ((size_t)bh * L + t0 + t) * d_v + j));
     }
-    // DPFP rows: r < 64 are keys, r >= 64 queries of token r & 63
+    // DPFP rows: r < 64 are keys, r >= 64 queries of token r & 63.  Every
+    // pass's 16-byte load is issued before any is used.
     {
         const int g = lane % G, base_lane = lane - g;
-        for (int r0 = 0; r0 < 128; r0 += 8 * RPW) {
-            const int r = r0 + warp * RPW + lane / G;
+        constexpr int kPasses = 128 / (8 * RPW);
+        uint4 raw[kPasses];
+#pragma unroll
+        for (int ps = 0; ps < kPasses; ++ps) {
+            const int r = ps * 8 * RPW + warp * RPW + lane / G;
             const int t = r & 63;
-            const bool valid = t < Lc;
-            const __nv_bfloat16 *src = (r < 64 ? k : q) + ((size_t)bh * L + t0 + (valid ? t : 0)) * DK;
+            raw[ps] = make_uint4(0, 0, 0, 0);
+            if (t < Lc)
+                raw[ps] = __ldg(reinterpret_cast<const uint4 *>((r < 64 ? k : q) + ((size_t)bh * L + t0 + t) * DK +
+                                                               8 * (g % (G / 2))));
+        }
+#pragma unroll
+        for (int ps = 0; ps < kPasses; ++ps) {
+            const int r = ps * 8 * RPW + warp * RPW + lane / G;
             float x[8];
-            dpfp_load_x<G>(src, g, valid, x);
+            {
+                float kv[8];
+                unpack8(raw[ps], kv);
+                const bool neg = g >= G / 2;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    x[e] = fmaxf(neg ? -kv[e] : kv[e], 0.f);
+            }
             const float inv = 1.0f / (dpfp_row_sum<G>(x, g, base_lane, nu) + eps);
             for (int i = 1; i <= nu; ++i) {
                 float p[8];
@@ -284,6 +299,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             t8[e] = Nm[kk * LDS + 8 * cc + e] * bs[8 * cc + e];
         *reinterpret_cast<uint4 *>(tt + kk * 128 + ((cc ^ (kk & 7)) << 4)) = pack8(t8);
     }
+    __syncthreads(); // A and N are done: their space takes the V tile
+#pragma unroll
+    for (int i = 0; i < kVChunks; ++i) {
+        const int idx = tid + i * kPrepThreads, t = idx / vcpr, j = 8 * (idx % vcpr);
+        if (idx < 64 * vcpr)
+            *reinterpret_cast<uint4 *>(vt + (uint32_t)(j >> 6) * 8192u + (uint32_t)t * 128u +
+                                       ((uint32_t)(((j & 63) >> 3) ^ (t & 7)) << 4)) = vpre[i];
+    }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -338,13 +361,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     {
         // [W'; Q'] image: rows < 64 take W', rows >= 64 take Q - P W'
         uint8_t *ai = rec + rc.a;
-        for (int c0 = 16 * half; c0 < Dp; c0 += 32) {
-            float w[16];
+        for (int c0 = 32 * half; c0 < Dp; c0 += 64) { // 32 columns per pass (Dp % 64 == 0)
+            float w[32];
             tmem_ld16(tm + lb + (uint32_t)c0, w);
+            tmem_ld16(tm + lb + (uint32_t)(c0 + 16), w + 16);
             tmem_ld_wait();
             if (row >= 64) {
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
+                for (int h2 = 0; h2 < 4; ++h2) {
                     float qv[8];
                     unpack8(*reinterpret_cast<const uint4 *>(kq + kmajor_chunk(row, c0 + 8 * h2, 128)), qv);
 #pragma unroll
@@ -352,8 +376,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                         w[8 * h2 + e] = qv[e] - w[8 * h2 + e];
                 }
             }
-            *reinterpret_cast<uint4 *>(ai + kmajor_chunk(row, c0, 128)) = pack8(w);
-            *reinterpret_cast<uint4 *>(ai + kmajor_chunk(row, c0 + 8, 128)) = pack8(w + 8);
+#pragma unroll
+            for (int h2 = 0; h2 < 4; ++h2)
+                *reinterpret_cast<uint4 *>(ai + kmajor_chunk(row, c0 + 8 * h2, 128)) = pack8(w + 8 * h2);
         }
         // U' (rows < 64) and Y' (rows >= 64), fp32
         float *dst = (float *)(rec + (row < 64 ? rc.up : rc.yp)) + (size_t)(row & 63) * d_v;
@@ -601,8 +626,8 @@ __global__ void __launch_bounds__(kScanThreads)
 // ---------------------------------------------------------------- host side
 size_t prep_smem(int Dp, int d_v) {
     const int VB = (d_v + 63) / 64;
-    return (size_t)256 * Dp + (size_t)VB * 8192 + 16384 + 8192 + 16384 + (2 * 64 + 16) * LDS * 4 + 64 * 4 +
-           16 + 1024;
+    (void)VB; // the V tile (<= 16 KB) reuses the fp32 work space (37 KB)
+    return (size_t)256 * Dp + 16384 + 8192 + (2 * 64 + 16) * LDS * 4 + 64 * 4 + 16 + 1024;
 }
 
 size_t scan_smem(int Dp, int dvb) {

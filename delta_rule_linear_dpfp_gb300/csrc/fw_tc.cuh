@@ -16,7 +16,7 @@
 //  * "MN-major, SW128" view of the same bytes: for an operand whose
 //    contraction index is the tile's row r and whose M/N index is the tile's
 //    column, 64-column blocks are LBO bytes apart and 8-row groups SBO apart.
-//  * Every wait is bounded: after kSpinLimit polls the caller gets `false`
+//  * Every wait is bounded: after about kWaitLimitNs the caller gets `false`
 //    and the device status word records kStatusTimeout.
 #pragma once
 
@@ -25,7 +25,7 @@
 namespace fw {
 namespace tc {
 
-constexpr uint32_t kSpinLimit = 1u << 24; // ~0.5-2 s with the back-off below
+constexpr uint64_t kWaitLimitNs = 1000000000ull; // a bounded wait gives up after ~1 s
 
 FW_DEV uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -47,14 +47,25 @@ FW_DEV bool mbar_try_wait(uint32_t addr, uint32_t parity) {
     return ok != 0;
 }
 
+FW_DEV uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
 // Wait for the phase with the given parity to complete; false on timeout.
+// try_wait itself suspends the thread for a while in hardware, so the loop
+// only re-polls; the elapsed time is checked every 64 polls.
 FW_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *status) {
     const uint32_t a = smem_u32(bar);
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(a, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(a, parity))
             return true;
-        if (i > 256)
-            __nanosleep(32);
+        if ((i & 63) == 0 && globaltimer_ns() - t0 > kWaitLimitNs)
+            break;
     }
     record_status(status, kStatusTimeout);
     return false;
