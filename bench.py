@@ -63,12 +63,41 @@ def peaks():
 def forward_flops_per_head_token(C, d_dot, d_v):
     """Algorithmic FLOPs of the chunked form per (b,h,token): the C x C
     triangular products counted at half."""
-    return 2.0 * (1.5 * C * d_dot + C * d_v + 3.0 * d_dot * d_v) + (2.0 / 3.0) * C * C
+    return prep_flops_per_head_token(C, d_dot, d_v) + scan_flops_per_head_token(d_dot, d_v)
 
 
-def forward_bytes_per_head_token(d_key, d_v, io_bytes):
-    """Algorithmic HBM bytes per (b,h,token): read q, k, v, beta, write y."""
-    return io_bytes * (2 * d_key + 2 * d_v + 1)
+def prep_flops_per_head_token(C, d_dot, d_v):
+    """The chunk-local part: Gram, solve and the products with T and P."""
+    return 2.0 * (1.5 * C * d_dot + C * d_v) + (2.0 / 3.0) * C * C
+
+
+def scan_flops_per_head_token(d_dot, d_v):
+    """The state part: W' S^T, Q' S^T and the update S += U^T K."""
+    return 2.0 * 3.0 * d_dot * d_v
+
+
+def forward_bytes(B, H, L, d_key, d_v, d_dot, io_bytes, w0=False, w_final=True):
+    """Algorithmic HBM bytes of one forward: read q, k, v, beta, write y, and
+    the fp32 state in / out when present."""
+    return (B * H * L * io_bytes * (2 * d_key + 2 * d_v + 1)
+            + (B * H * d_v * d_dot * 4) * (int(w0) + int(w_final)))
+
+
+def roofline(name, flops, nbytes, ms, pk):
+    """Achieved rate of one kernel against the resource that bounds it."""
+    t_hbm = nbytes / (pk["hbm"] * 1e9)
+    t_tc = flops / (pk["bf16"] * 1e12)
+    secs = ms * 1e-3
+    if t_hbm >= t_tc:
+        a = nbytes / secs / 1e9
+        r = {"bound": "hbm", "achieved": a, "peak": pk["hbm"], "unit": "GB/s", "frac": a / pk["hbm"]}
+    else:
+        a = flops / secs / 1e12
+        r = {"bound": "tensor", "achieved": a, "peak": pk["bf16"], "unit": "TFLOP/s", "frac": a / pk["bf16"]}
+    r.update({"kernel": name, "kernel_ms": ms, "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+              "hbm_frac": nbytes / secs / 1e9 / pk["hbm"],
+              "tensor_frac": flops / secs / 1e12 / pk["bf16"], "peak_source": pk["source"]})
+    return r
 
 
 class ClockSampler:
@@ -253,28 +282,20 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
 
     # ----------------------------------------------------------- roofline
+    # the two kernels of the forward, each timed on its own with CUDA events
+    # on the launching stream (fw_delta_forward = prepare + scan)
     pk = peaks()
-    flops = forward_flops_per_head_token(C, d_dot, d_v) * B * H * L
-    nbytes = forward_bytes_per_head_token(d_key, d_v, io_bytes) * B * H * L
-    # the bound is the resource whose time at peak is longer
-    t_hbm = nbytes / (pk["hbm"] * 1e9)
-    t_tc = flops / (pk["bf16"] * 1e12)
+    ms_prep, ms_scan = phase_ms(fw, sets, y, Wf, ws, nu, C, stream)
+    BHL = B * H * L
+    r_prep = roofline("chunk_prep_kernel", prep_flops_per_head_token(C, d_dot, d_v) * BHL,
+                      BHL * io_bytes * (2 * d_key + d_v + 1), ms_prep, pk)
+    r_scan = roofline("chunk_scan_kernel", scan_flops_per_head_token(d_dot, d_v) * BHL,
+                      BHL * io_bytes * d_v + B * H * d_v * d_dot * 4, ms_scan, pk)
+    r_fwd = roofline("fw_delta_forward (prepare + scan)", forward_flops_per_head_token(C, d_dot, d_v) * BHL,
+                     forward_bytes(B, H, L, d_key, d_v, d_dot, io_bytes), ms_step, pk)
+    roof = dict(r_prep if ms_prep >= ms_scan else r_scan)
+    roof["traffic"] = recorded_traffic(roof["kernel"], FORWARD_SOURCES)
     launches_per_step = FORWARD_LAUNCHES
-    kernel_ms = forward_kernel_ms(fw, sets, y, Wf, ws, nu, C, stream)
-    if t_hbm >= t_tc:
-        achieved = nbytes / (kernel_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                "frac": achieved / pk["hbm"]}
-    else:
-        achieved = flops / (kernel_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16"]}
-    roof.update({"traffic": recorded_traffic(FORWARD_KERNEL_KEY, FORWARD_SOURCES),
-                 "kernel": FORWARD_KERNEL_KEY, "peak_source": pk["source"],
-                 "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
-                 "kernel_ms": kernel_ms,
-                 "tensor_frac": flops / (kernel_ms * 1e-3) / 1e12 / pk["bf16"],
-                 "hbm_frac": nbytes / (kernel_ms * 1e-3) / 1e9 / pk["hbm"]})
 
     rows = None
     if rank == 0 and not args.no_rows:
@@ -296,6 +317,7 @@ def run_ours(args, rank, world, local_rank):
                 "steps": e2e_steps},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roof,
+        "kernels": {"chunk_prep_kernel": r_prep, "chunk_scan_kernel": r_scan, "forward": r_fwd},
     }
     if rows is not None:
         result["rows"] = rows
@@ -304,24 +326,30 @@ def run_ours(args, rank, world, local_rank):
 
 # the forward's launches per call and the kernel the roofline is taken on
 FORWARD_LAUNCHES = 2
-FORWARD_KERNEL_KEY = "fw_delta_forward (chunk_prep_kernel + chunk_scan_kernel)"
 FORWARD_SOURCES = ["delta_rule_linear_dpfp_gb300/csrc/fw_forward_tc.cu",
                    "delta_rule_linear_dpfp_gb300/csrc/fw_tc.cuh",
                    "delta_rule_linear_dpfp_gb300/csrc/fw_dpfp.cuh"]
 
 
-def forward_kernel_ms(fw, sets, y, Wf, ws, nu, C, stream, reps=200):
-    """Average duration of one forward call, CUDA events on its stream."""
+def phase_ms(fw, sets, y, Wf, ws, nu, C, stream, reps=200):
+    """Average duration of the prepare and of the scan kernel, each timed over
+    `reps` back-to-back launches with CUDA events on their stream."""
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     e0.record(stream)
     for i in range(reps):
         d = sets[i % len(sets)]
-        fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=None, nu=nu, chunk=C, y=y,
-                            W_final=Wf, workspace=ws, stream=stream)
+        fw.fw_delta_forward_prepare(d["q"], d["k"], d["v"], d["beta"], ws, nu=nu, chunk=C, stream=stream)
     e1.record(stream)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / reps
+    ms_prep = e0.elapsed_time(e1) / reps
+    e0.record(stream)
+    for i in range(reps):
+        fw.fw_delta_forward_scan(ws, y, W0=None, W_final=Wf, nu=nu, chunk=C, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_scan = e0.elapsed_time(e1) / reps
+    return ms_prep, ms_scan
 
 
 def _time(fn, reps, stream):
@@ -346,9 +374,7 @@ def measure_rows(fw, inputs, dev, stream, pk):
     outs = [torch.empty(nrows, 384, dtype=torch.bfloat16, device=dev) for _ in range(4)]
     ms = _time(lambda i: fw.fw_dpfp(xs[i % 4], nu=3, out=outs[i % 4], stream=stream), 200, stream)
     nb = nrows * (64 + 384) * 2
-    rows["dpfp_65536x64_nu3_bf16"] = {"ms": ms, "GB/s": nb / ms / 1e6,
-                                      "hbm_frac": nb / ms / 1e6 / pk["hbm"],
-                                      "bytes": nb}
+    rows["dpfp_65536x64_nu3_bf16"] = roofline("dpfp_kernel", nrows * 384 * 4.0, nb, ms, pk)
     # a6: decode step, B256 H16 d_key64 nu2 d_v128, W 512 MiB fp32
     cfg = inputs.DECODE_CONFIGS["decode_b256"]
     B, H, d_key, nu, d_v = (cfg[n] for n in ("B", "H", "d_key", "nu", "d_v"))
@@ -364,8 +390,9 @@ def measure_rows(fw, inputs, dev, stream, pk):
     ms = _time(dec, 100, stream)
     d_dot = 2 * d_key * nu
     nb = B * H * d_v * d_dot * 4 * 2 + B * H * (2 * d_key + 2 * d_v + 1) * 2
-    rows["decode_b256h16_nu2_dv128"] = {"ms": ms, "tokens/s": B / (ms * 1e-3), "GB/s": nb / ms / 1e6,
-                                        "hbm_frac": nb / ms / 1e6 / pk["hbm"], "bytes": nb}
+    r = roofline("decode_kernel", B * H * d_v * d_dot * 6.0, nb, ms, pk)
+    r["tokens/s"] = B / (ms * 1e-3)
+    rows["decode_b256h16_nu2_dv128"] = r
     # a1-a5 on the long nu = 3 workload with W0 in, W_final out
     name = "b2h8_l2048_nu3"
     c = inputs.FORWARD_CONFIGS[name]
@@ -380,8 +407,10 @@ def measure_rows(fw, inputs, dev, stream, pk):
                                              chunk=C, y=y, W_final=Wf, workspace=ws, stream=stream),
                50, stream)
     flops = forward_flops_per_head_token(C, d_dot, d_v) * B * H * L
-    rows[name] = {"ms": ms, "tokens/s": B * L / (ms * 1e-3), "TFLOP/s": flops / ms / 1e9,
-                  "tensor_frac": flops / ms / 1e9 / pk["bf16"], "flops": flops}
+    r = roofline("fw_delta_forward (prepare + scan)", flops,
+                 forward_bytes(B, H, L, d_key, d_v, d_dot, 2, w0=True), ms, pk)
+    r["tokens/s"] = B * L / (ms * 1e-3)
+    rows[name] = r
     return rows
 
 

@@ -25,7 +25,7 @@ FW_DTYPE_BF16 = 1
 #: every entry point include/*.h declares
 EXPORTS = ("fw_status_string", "fw_dpfp", "fw_delta_forward_workspace_size", "fw_delta_forward",
            "fw_delta_decode_step", "fw_device_status", "fw_selftest_umma",
-           "fw_delta_forward_noalloc")
+           "fw_delta_forward_noalloc", "fw_delta_forward_prepare", "fw_delta_forward_scan")
 
 #: bytes of the library's own scratch array behind fw_delta_forward_noalloc
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -66,6 +66,10 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.fw_delta_decode_step.argtypes = [vp] * 6 + [i32] * 6 + [f32, vp]
     lib.fw_device_status.restype = i32
     lib.fw_device_status.argtypes = [vp]
+    lib.fw_delta_forward_prepare.restype = i32
+    lib.fw_delta_forward_prepare.argtypes = [vp] * 5 + [sz] + [i32] * 7 + [f32, vp]
+    lib.fw_delta_forward_scan.restype = i32
+    lib.fw_delta_forward_scan.argtypes = [vp, sz, vp, vp, vp] + [i32] * 7 + [vp]
     lib.fw_delta_forward_noalloc.restype = i32
     lib.fw_delta_forward_noalloc.argtypes = [vp] * 7 + [i32] * 8 + [f32, vp]
     lib.fw_selftest_umma.restype = i32
@@ -156,6 +160,40 @@ def fw_delta_forward(q, k, v, beta, W0=None, nu: int = 1, chunk: int = 64, eps: 
                                  _ptr(y), _ptr(workspace), ws_bytes, B, H, L, d_key, nu, d_v, chunk,
                                  code, eps, _stream(stream))
     _check(rc, "fw_delta_forward")
+    return y, W_final
+
+
+def fw_delta_forward_prepare(q, k, v, beta, workspace, nu: int = 1, chunk: int = 64,
+                             eps: float = 1e-6, stream=None):
+    """Phase 1 of the bf16 forward: every chunk's preparation into `workspace`
+    (a uint8 CUDA tensor of fw_delta_forward_workspace_size bytes)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("workspace", workspace)):
+        _dev(t, name)
+    B, H, L, d_key = q.shape
+    d_v = v.shape[-1]
+    rc = load().fw_delta_forward_prepare(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), B, H, L, d_key,
+                                         nu, d_v, chunk, eps, _stream(stream))
+    _check(rc, "fw_delta_forward_prepare")
+
+
+def fw_delta_forward_scan(workspace, y, W0=None, W_final=None, nu: int = 1, chunk: int = 64,
+                          stream=None):
+    """Phase 2 of the bf16 forward: the chunk-by-chunk state scan from the
+    prepared `workspace`; writes y [B,H,L,d_v] and W_final (if given)."""
+    _dev(workspace, "workspace")
+    _dev(y, "y")
+    B, H, L, d_v = y.shape
+    if W0 is not None:
+        _dev(W0, "W0")
+    d_dot = (W0 if W0 is not None else W_final).shape[-1] if (W0 is not None or W_final is not None) else None
+    if d_dot is None:
+        raise ValueError("pass W0 or W_final so the state width is known")
+    d_key = d_dot // (2 * nu)
+    rc = load().fw_delta_forward_scan(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _ptr(W0), _ptr(W_final), _ptr(y), B, H, L, d_key, nu, d_v, chunk,
+                                      _stream(stream))
+    _check(rc, "fw_delta_forward_scan")
     return y, W_final
 
 

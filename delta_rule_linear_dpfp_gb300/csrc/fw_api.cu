@@ -191,6 +191,73 @@ FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const v
     return cuda_status(e);
 }
 
+namespace {
+
+// Checks shared by the two phases of the bf16 forward.  Returns FW_OK with
+// *empty set when nothing has to be enqueued.
+int check_phase(int B, int H, int L, int d_key, int nu, int d_v, int chunk, const void *workspace,
+                size_t workspace_bytes, bool *empty) {
+    const int rc = check_forward_shape(B, H, L, d_key, nu, d_v, chunk, FW_DTYPE_BF16);
+    if (rc != FW_OK)
+        return rc;
+    *empty = (int64_t)B * H == 0 || L == 0;
+    if (*empty)
+        return FW_OK;
+    if ((int64_t)B * H > (int64_t)1 << 30)
+        return FW_ERR_UNSUPPORTED;
+    const size_t need = fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk, FW_DTYPE_BF16);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+        return FW_ERR_INVALID_ARG;
+    return FW_OK;
+}
+
+} // namespace
+
+FW_API int fw_delta_forward_prepare(const void *q, const void *k, const void *v, const void *beta,
+                                    void *workspace, size_t workspace_bytes, int B, int H, int L,
+                                    int d_key, int nu, int d_v, int chunk, float eps, void *stream) {
+    if (!eps_ok(eps))
+        return FW_ERR_INVALID_ARG;
+    bool empty = false;
+    const int rc = check_phase(B, H, L, d_key, nu, d_v, chunk, workspace, workspace_bytes, &empty);
+    if (rc != FW_OK || empty)
+        return rc;
+    if (!q || !k || !v || !beta || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta))
+        return FW_ERR_INVALID_ARG;
+    DeviceInfo di;
+    if (device_info(&di) != cudaSuccess)
+        return FW_ERR_CUDA;
+    return cuda_status(fw::tc_prepare_launch(q, k, v, beta, workspace, B, H, L, d_key, nu, d_v, chunk, eps,
+                                             di.status, static_cast<cudaStream_t>(stream)));
+}
+
+FW_API int fw_delta_forward_scan(const void *workspace, size_t workspace_bytes, const float *W0,
+                                 float *W_final, void *y, int B, int H, int L, int d_key, int nu, int d_v,
+                                 int chunk, void *stream) {
+    bool empty = false;
+    const int rc = check_phase(B, H, L, d_key, nu, d_v, chunk, workspace, workspace_bytes, &empty);
+    if (rc != FW_OK)
+        return rc;
+    if ((W0 && !aligned16(W0)) || (W_final && !aligned16(W_final)))
+        return FW_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (empty) {
+        // no token: the final state is the initial one
+        if ((int64_t)B * H == 0 || !W_final || W0 == W_final)
+            return FW_OK;
+        const size_t bytes = sizeof(float) * (size_t)B * H * d_v * (2 * d_key * nu);
+        return cuda_status(W0 ? cudaMemcpyAsync(W_final, W0, bytes, cudaMemcpyDeviceToDevice, st)
+                              : cudaMemsetAsync(W_final, 0, bytes, st));
+    }
+    if (!y || !aligned16(y))
+        return FW_ERR_INVALID_ARG;
+    DeviceInfo di;
+    if (device_info(&di) != cudaSuccess)
+        return FW_ERR_CUDA;
+    return cuda_status(fw::tc_scan_launch(workspace, W0, W_final, y, B, H, L, d_key, nu, d_v, chunk,
+                                          di.num_sms, di.status, st));
+}
+
 FW_API int fw_delta_decode_step(const void *q, const void *k, const void *v, const void *beta,
                                 float *W, void *y, int B, int H, int d_key, int nu, int d_v,
                                 int io_dtype, float eps, void *stream) {

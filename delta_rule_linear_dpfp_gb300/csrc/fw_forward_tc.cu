@@ -695,31 +695,45 @@ size_t tc_forward_workspace_bytes(int B, int H, int L, int d_key, int nu, int d_
     return (size_t)B * H * nch * record_layout(padded_ddot(2 * d_key * nu), d_v).bytes;
 }
 
-cudaError_t tc_forward_launch(const void *q, const void *k, const void *v, const void *beta,
-                              const float *W0, float *W_final, void *y, void *workspace, int B,
-                              int H, int L, int d_key, int nu, int d_v, int chunk, float eps,
-                              int num_sms, unsigned *status, cudaStream_t st) {
+cudaError_t tc_prepare_launch(const void *q, const void *k, const void *v, const void *beta, void *workspace,
+                              int B, int H, int L, int d_key, int nu, int d_v, int chunk, float eps,
+                              unsigned *status, cudaStream_t st) {
+    const int BH = B * H;
+    const int nch = (L + chunk - 1) / chunk;
+    const int Dp = padded_ddot(2 * d_key * nu);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    switch (d_key) {
+    case 8: return launch_prep<8>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st);
+    case 16: return launch_prep<16>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st);
+    case 32: return launch_prep<32>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st);
+    case 64: return launch_prep<64>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st);
+    case 128: return launch_prep<128>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t tc_scan_launch(const void *workspace, const float *W0, float *W_final, void *y, int B, int H, int L,
+                           int d_key, int nu, int d_v, int chunk, int num_sms, unsigned *status, cudaStream_t st) {
     const int BH = B * H;
     const int nch = (L + chunk - 1) / chunk;
     const int d_dot = 2 * d_key * nu;
     const int Dp = padded_ddot(d_dot);
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    cudaError_t e;
-    switch (d_key) {
-    case 8: e = launch_prep<8>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st); break;
-    case 16: e = launch_prep<16>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st); break;
-    case 32: e = launch_prep<32>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st); break;
-    case 64: e = launch_prep<64>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st); break;
-    case 128: e = launch_prep<128>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st); break;
-    default: return cudaErrorInvalidValue;
-    }
-    if (e != cudaSuccess)
-        return e;
+    const uint8_t *ws = static_cast<const uint8_t *>(workspace);
     switch (choose_dvb(BH, d_v, Dp, num_sms)) {
     case 16: return launch_scan<16>(W0, W_final, y, ws, BH, L, chunk, nch, d_v, d_dot, Dp, status, st);
     case 32: return launch_scan<32>(W0, W_final, y, ws, BH, L, chunk, nch, d_v, d_dot, Dp, status, st);
     default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t tc_forward_launch(const void *q, const void *k, const void *v, const void *beta,
+                              const float *W0, float *W_final, void *y, void *workspace, int B,
+                              int H, int L, int d_key, int nu, int d_v, int chunk, float eps,
+                              int num_sms, unsigned *status, cudaStream_t st) {
+    const cudaError_t e = tc_prepare_launch(q, k, v, beta, workspace, B, H, L, d_key, nu, d_v, chunk, eps, status, st);
+    if (e != cudaSuccess)
+        return e;
+    return tc_scan_launch(workspace, W0, W_final, y, B, H, L, d_key, nu, d_v, chunk, num_sms, status, st);
 }
 
 } // namespace fw

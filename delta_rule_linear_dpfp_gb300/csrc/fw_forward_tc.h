@@ -16,7 +16,15 @@ bool tc_forward_supported(int d_key, int nu, int d_v, int chunk);
 // Device workspace bytes the bf16 forward needs for this shape.
 size_t tc_forward_workspace_bytes(int B, int H, int L, int d_key, int nu, int d_v, int chunk);
 
-// Enqueue the bf16 forward (arguments validated by the caller).
+// The two phases of the bf16 forward (arguments validated by the caller):
+// per-chunk preparation into the workspace, then the serial state scan.
+cudaError_t tc_prepare_launch(const void *q, const void *k, const void *v, const void *beta, void *workspace,
+                              int B, int H, int L, int d_key, int nu, int d_v, int chunk, float eps,
+                              unsigned *status, cudaStream_t st);
+cudaError_t tc_scan_launch(const void *workspace, const float *W0, float *W_final, void *y, int B, int H, int L,
+                           int d_key, int nu, int d_v, int chunk, int num_sms, unsigned *status, cudaStream_t st);
+
+// Enqueue the bf16 forward: both phases (arguments validated by the caller).
 cudaError_t tc_forward_launch(const void *q, const void *k, const void *v, const void *beta,
                               const float *W0, float *W_final, void *y, void *workspace, int B,
                               int H, int L, int d_key, int nu, int d_v, int chunk, float eps,

@@ -139,6 +139,30 @@ FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const v
                             size_t workspace_bytes, int B, int H, int L, int d_key, int nu,
                             int d_v, int chunk, int io_dtype, float eps, void *stream);
 
+/*
+ * fw_delta_forward_prepare / fw_delta_forward_scan -- the two phases of the
+ * bf16 fw_delta_forward, callable on their own (bf16 I/O only).  Enqueuing
+ * prepare then scan on one stream computes exactly what fw_delta_forward
+ * computes for the same arguments.
+ *   prepare: every chunk of every (batch, head) in parallel -- DPFP of the
+ *            chunk's q and k, the chunk's Gram matrix and the triangular
+ *            solve of the chunked form, and the products that do not involve
+ *            the state -- written to `workspace`.  Reads q, k, v, beta.
+ *   scan:    the chunks of each (batch, head) in order -- the state passes
+ *            from chunk to chunk, y and the final state are written.  Reads
+ *            the workspace written by prepare (and W0), not q, k, v, beta.
+ * [the chunked evaluation of the update rule of the Fast Weights Transformer
+ * guide; the split into a parallel and a serial phase is this library's]
+ * Arguments and errors as fw_delta_forward (io_dtype is bf16).  The
+ * workspace must stay untouched between the two calls.
+ */
+FW_API int fw_delta_forward_prepare(const void *q, const void *k, const void *v, const void *beta,
+                                    void *workspace, size_t workspace_bytes, int B, int H, int L,
+                                    int d_key, int nu, int d_v, int chunk, float eps, void *stream);
+FW_API int fw_delta_forward_scan(const void *workspace, size_t workspace_bytes, const float *W0,
+                                 float *W_final, void *y, int B, int H, int L, int d_key, int nu, int d_v,
+                                 int chunk, void *stream);
+
 /* Size of the library's own scratch array used by fw_delta_forward_noalloc. */
 #define FW_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 

@@ -141,3 +141,39 @@ def test_decode_argument_checks(lib):
     args = list(base)
     args[8], args[9] = 128, 5                          # d_dot = 1280 > 1024
     assert call(*args) == U
+
+
+def test_phase_argument_checks(lib):
+    E, U, OK = binding.FW_ERR_INVALID_ARG, binding.FW_ERR_UNSUPPORTED, binding.FW_OK
+    prep, scan = lib.fw_delta_forward_prepare, lib.fw_delta_forward_scan
+    need = lib.fw_delta_forward_workspace_size(2, 2, 8, 64, 1, 64, 64, 1)
+    assert need > 0
+    args = [FAKE] * 5 + [need, 2, 2, 8, 64, 1, 64, 64, 1e-6, None]
+    for i in range(5):                   # q, k, v, beta, workspace
+        bad = list(args)
+        bad[i] = None
+        assert prep(*bad) == E
+        bad[i] = MISALIGNED
+        assert prep(*bad) == E
+    bad = list(args)
+    bad[5] = need - 1                    # workspace too small
+    assert prep(*bad) == E
+    bad = list(args)
+    bad[9] = 24                          # d_key not compiled
+    assert prep(*bad) == U
+    bad = list(args)
+    bad[12] = 48                         # chunk
+    assert prep(*bad) == E
+    sargs = [FAKE, need, None, None, FAKE, 2, 2, 8, 64, 1, 64, 64, None]
+    bad = list(sargs)
+    bad[0] = None
+    assert scan(*bad) == E
+    bad = list(sargs)
+    bad[4] = None                        # y
+    assert scan(*bad) == E
+    bad = list(sargs)
+    bad[2] = MISALIGNED                  # W0
+    assert scan(*bad) == E
+    bad = list(sargs)
+    bad[5] = 0                           # empty batch: nothing to do
+    assert scan(*bad) == OK

@@ -162,6 +162,22 @@ def test_forward_resume_equals_whole():
     assert maxrel(f64(Wb), f64(W)) <= 2e-2
 
 
+def test_prepare_then_scan_equals_forward():
+    """The two phases, enqueued one after the other, give exactly what the
+    one-call forward gives (same kernels, same arithmetic)."""
+    for (B, H, L, nu, w0) in [(2, 4, 200, 2, True), (4, 8, 512, 1, False)]:
+        d = to_dev(inputs.random_forward_inputs(B, H, L, 64, nu, 64, "bf16", 0.01 if w0 else None, seed=L))
+        y, Wf = fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=d["W0"], nu=nu, chunk=64)
+        need = fw.fw_delta_forward_workspace_size(B, H, L, 64, nu, 64, 64, torch.bfloat16)
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        y2 = torch.empty_like(y)
+        W2 = torch.empty_like(Wf)
+        fw.fw_delta_forward_prepare(d["q"], d["k"], d["v"], d["beta"], ws, nu=nu, chunk=64)
+        fw.fw_delta_forward_scan(ws, y2, W0=d["W0"], W_final=W2, nu=nu, chunk=64)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y2) and torch.equal(Wf, W2)
+
+
 # ---------------------------------------------------------------- K3 decode
 def test_decode_small_stepped():
     B, H, d_key, nu, d_v, steps = 3, 2, 64, 2, 128, 6
