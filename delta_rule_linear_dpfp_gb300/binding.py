@@ -25,7 +25,8 @@ FW_DTYPE_BF16 = 1
 #: every entry point include/*.h declares
 EXPORTS = ("fw_status_string", "fw_dpfp", "fw_delta_forward_workspace_size", "fw_delta_forward",
            "fw_delta_decode_step", "fw_device_status", "fw_selftest_umma",
-           "fw_delta_forward_noalloc", "fw_delta_forward_prepare", "fw_delta_forward_scan")
+           "fw_delta_forward_noalloc", "fw_delta_forward_prepare", "fw_delta_forward_scan",
+           "fw_selftest_wait_timeout")
 
 #: bytes of the library's own scratch array behind fw_delta_forward_noalloc
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -72,6 +73,8 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.fw_delta_forward_scan.argtypes = [vp, sz, vp, vp, vp] + [i32] * 7 + [vp]
     lib.fw_delta_forward_noalloc.restype = i32
     lib.fw_delta_forward_noalloc.argtypes = [vp] * 7 + [i32] * 8 + [f32, vp]
+    lib.fw_selftest_wait_timeout.restype = i32
+    lib.fw_selftest_wait_timeout.argtypes = [i32, vp]
     lib.fw_selftest_umma.restype = i32
     lib.fw_selftest_umma.argtypes = [vp, vp, vp] + [i32] * 5 + [vp]
     if path is None:
@@ -260,3 +263,8 @@ def fw_selftest_umma(A, B, a_mn: int = 0, b_mn: int = 0, swap_mn: int = 0, strea
     rc = load().fw_selftest_umma(_ptr(A), _ptr(B), _ptr(D), N, K, a_mn, b_mn, swap_mn, _stream(stream))
     _check(rc, "fw_selftest_umma")
     return D
+
+
+def fw_selftest_wait_timeout(limit_us: int = 2000, stream=None):
+    """Run the bounded-wait failure path once (see include/fastweight_selftest.h)."""
+    _check(load().fw_selftest_wait_timeout(int(limit_us), _stream(stream)), "fw_selftest_wait_timeout")

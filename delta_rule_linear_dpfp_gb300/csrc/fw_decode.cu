@@ -75,17 +75,14 @@ __global__ void __launch_bounds__(256)
         const T *src = (rr == 1 ? q : k) + bh * DK;
         float x[8];
         dpfp_load_x<G>(src, g, valid, x);
-        const float inv = 1.0f / (dpfp_row_sum<G>(x, g, base_lane, nu) + eps);
         float *dst = rr == 1 ? phq : phk;
-        for (int i = 1; i <= nu; ++i) {
-            float p[8];
-            dpfp_block_dispatch<G>(x, p, g, base_lane, i);
+        dpfp_row_emit<G, 4>(x, g, base_lane, nu, eps, [&](int i, float (&p)[8]) {
             if (valid) {
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
-                    dst[(i - 1) * N2 + 8 * g + c] = p[c] * inv;
+                    dst[(i - 1) * N2 + 8 * g + c] = p[c];
             }
-        }
+        });
     }
     __syncthreads();
     if (warp == 0) {

@@ -24,13 +24,12 @@ namespace fw {
 
 namespace {
 
-// Products of the first NUC blocks kept in registers (one shuffle pass) when
-// nu <= NUC; otherwise a second pass recomputes them.  The normaliser is
-// applied as one reciprocal per row.
-constexpr int NUC = 4;
+// Products of up to NUC blocks stay in registers between the sum and the
+// output (dpfp_row_emit); larger nu recomputes them.
+constexpr int NUC = 3;
 
 template <int DK, typename Tin, typename Tout>
-__global__ void __launch_bounds__(256) dpfp_kernel(const Tin *__restrict__ xin, Tout *__restrict__ out,
+__global__ void __launch_bounds__(256, 4) dpfp_kernel(const Tin *__restrict__ xin, Tout *__restrict__ out,
                                                    int64_t rows, int nu, float eps) {
     constexpr int G = DK / 4;         // lanes per row
     constexpr int RPW = 32 / G;       // rows per warp
@@ -47,44 +46,10 @@ __global__ void __launch_bounds__(256) dpfp_kernel(const Tin *__restrict__ xin, 
         float x[8];
         dpfp_load_x<G>(xin + (valid ? row : 0) * DK, g, valid, x);
         Tout *orow = out + row * d_dot + 8 * g;
-        if (nu <= NUC) {
-            float p[NUC][8];
-            float s = 0.f;
-#pragma unroll
-            for (int i = 0; i < NUC; ++i) {
-                if (i < nu) {
-                    dpfp_block_dispatch<G>(x, p[i], g, base_lane, i + 1); // i is static once unrolled
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        s += p[i][c];
-                }
-            }
-#pragma unroll
-            for (int o = G / 2; o > 0; o >>= 1)
-                s += __shfl_xor_sync(0xffffffffu, s, o);
-            const float inv = 1.0f / (s + eps);
-#pragma unroll
-            for (int i = 0; i < NUC; ++i) {
-                if (i < nu) {
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        p[i][c] *= inv;
-                    if (valid)
-                        store8(orow + (int64_t)i * N, p[i]);
-                }
-            }
-        } else {
-            const float inv = 1.0f / (dpfp_row_sum<G>(x, g, base_lane, nu) + eps);
-            for (int i = 1; i <= nu; ++i) {
-                float p[8];
-                dpfp_block_dispatch<G>(x, p, g, base_lane, i);
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    p[c] *= inv;
-                if (valid)
-                    store8(orow + (int64_t)(i - 1) * N, p);
-            }
-        }
+        dpfp_row_emit<G, NUC>(x, g, base_lane, nu, eps, [&](int i, float (&p)[8]) {
+            if (valid)
+                store8(orow + (int64_t)(i - 1) * N, p);
+        });
     }
 }
 

@@ -45,6 +45,19 @@ FW_DEV void dpfp_block_dispatch(const float (&x)[8], float (&p)[8], int g, int b
     }
 }
 
+// The 8 raw key values behind this lane's entries of x (row `src`, d_key =
+// 4*G elements), zeros when valid = false.
+template <int G, typename T>
+FW_DEV void dpfp_load_raw(const T *src, int g, bool valid, float (&kv)[8]) {
+    if (valid) {
+        load8(src + 8 * (g % (G / 2)), kv);
+    } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            kv[c] = 0.f;
+    }
+}
+
 // Load the 8 entries of x this lane owns from row `src` (d_key = 4*G
 // elements): lanes g < G/2 take ReLU(k), the others ReLU(-k).  valid = false
 // gives zeros (a padded row).
@@ -80,6 +93,50 @@ FW_DEV float dpfp_row_sum(const float (&x)[8], int g, int base_lane, int nu) {
     for (int o = G / 2; o > 0; o >>= 1)
         s += __shfl_xor_sync(0xffffffffu, s, o);
     return s;
+}
+
+// phi of one row, normalised, handed block by block to emit(i, p) with
+// i = 1..nu and p[8] this lane's 8 entries of block i (already divided by
+// sum + eps).  For nu <= NUC the products stay in registers between the sum
+// and the output; beyond that they are recomputed.
+template <int G, int NUC, typename Emit>
+FW_DEV void dpfp_row_emit(const float (&x)[8], int g, int base_lane, int nu, float eps, Emit emit) {
+    if (nu <= NUC) {
+        float p[NUC][8];
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < NUC; ++i) {
+            if (i < nu) {
+                dpfp_block_dispatch<G>(x, p[i], g, base_lane, i + 1); // i is static once unrolled
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    s += p[i][c];
+            }
+        }
+#pragma unroll
+        for (int o = G / 2; o > 0; o >>= 1)
+            s += __shfl_xor_sync(0xffffffffu, s, o);
+        const float inv = 1.0f / (s + eps);
+#pragma unroll
+        for (int i = 0; i < NUC; ++i) {
+            if (i < nu) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    p[i][c] *= inv;
+                emit(i + 1, p[i]);
+            }
+        }
+    } else {
+        const float inv = 1.0f / (dpfp_row_sum<G>(x, g, base_lane, nu) + eps);
+        for (int i = 1; i <= nu; ++i) {
+            float p[8];
+            dpfp_block_dispatch<G>(x, p, g, base_lane, i);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                p[c] *= inv;
+            emit(i, p);
+        }
+    }
 }
 
 } // namespace fw

@@ -124,25 +124,47 @@ FW_DEV void unit_lower_inverse(const float *A, float *N, float *R, int tid) {
             N[(o + i) * LDS + o + j] = col[i];
     }
     __syncthreads();
+    // off-diagonal blocks; each thread computes 4 adjacent outputs of a row,
+    // so every A (or N) element it loads feeds 4 FMAs
     for (int I = 1; I < 4; ++I) {
-        for (int idx = tid; idx < 256 * I; idx += NT) {
-            const int J = idx >> 8, ii = (idx >> 4) & 15, jj = idx & 15;
-            float acc = 0.f;
+        for (int idx = tid; idx < 64 * I; idx += NT) {
+            const int J = idx >> 6, ii = (idx >> 2) & 15, j0 = 16 * J + 4 * (idx & 3);
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
             for (int K = J; K < I; ++K) {
 #pragma unroll
-                for (int s = 0; s < 16; ++s)
-                    acc = fmaf(A[(16 * I + ii) * LDS + 16 * K + s], N[(16 * K + s) * LDS + 16 * J + jj], acc);
+                for (int s = 0; s < 16; ++s) {
+                    const float a = A[(16 * I + ii) * LDS + 16 * K + s];
+                    const float *nr = N + (16 * K + s) * LDS + j0;
+                    a0 = fmaf(a, nr[0], a0);
+                    a1 = fmaf(a, nr[1], a1);
+                    a2 = fmaf(a, nr[2], a2);
+                    a3 = fmaf(a, nr[3], a3);
+                }
             }
-            R[ii * LDS + 16 * J + jj] = acc;
+            float *rr = R + ii * LDS + j0;
+            rr[0] = a0;
+            rr[1] = a1;
+            rr[2] = a2;
+            rr[3] = a3;
         }
         __syncthreads();
-        for (int idx = tid; idx < 256 * I; idx += NT) {
-            const int J = idx >> 8, ii = (idx >> 4) & 15, jj = idx & 15;
-            float acc = 0.f;
+        for (int idx = tid; idx < 64 * I; idx += NT) {
+            const int J = idx >> 6, ii = (idx >> 2) & 15, j0 = 16 * J + 4 * (idx & 3);
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-            for (int s = 0; s < 16; ++s)
-                acc = fmaf(N[(16 * I + ii) * LDS + 16 * I + s], R[s * LDS + 16 * J + jj], acc);
-            N[(16 * I + ii) * LDS + 16 * J + jj] = -acc;
+            for (int s = 0; s < 16; ++s) {
+                const float n = N[(16 * I + ii) * LDS + 16 * I + s];
+                const float *rr = R + s * LDS + j0;
+                a0 = fmaf(n, rr[0], a0);
+                a1 = fmaf(n, rr[1], a1);
+                a2 = fmaf(n, rr[2], a2);
+                a3 = fmaf(n, rr[3], a3);
+            }
+            float *nd = N + (16 * I + ii) * LDS + j0;
+            nd[0] = -a0;
+            nd[1] = -a1;
+            nd[2] = -a2;
+            nd[3] = -a3;
         }
         __syncthreads();
     }
@@ -230,15 +252,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                 for (int e = 0; e < 8; ++e)
                     x[e] = fmaxf(neg ? -kv[e] : kv[e], 0.f);
             }
-            const float inv = 1.0f / (dpfp_row_sum<G>(x, g, base_lane, nu) + eps);
-            for (int i = 1; i <= nu; ++i) {
-                float p[8];
-                dpfp_block_dispatch<G>(x, p, g, base_lane, i);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    p[e] *= inv;
+            dpfp_row_emit<G, 3>(x, g, base_lane, nu, eps, [&](int i, float (&p)[8]) {
                 *reinterpret_cast<uint4 *>(kq + kmajor_chunk(r, (i - 1) * N2 + 8 * g, 128)) = pack8(p);
-            }
+            });
         }
         const int padc = (Dp - d_dot) / 8; // zero columns d_dot .. Dp-1
         for (int idx = tid; idx < 128 * padc; idx += kPrepThreads) {

@@ -113,3 +113,31 @@ extern "C" FW_API int fw_selftest_umma(const float *A, const float *B, float *D,
                                                                               swap_mn, status);
     return cudaGetLastError() == cudaSuccess ? FW_OK : FW_ERR_CUDA;
 }
+
+namespace {
+
+// One CTA waits on an mbarrier that nothing arrives at: the bounded wait
+// gives up after limit_ns, records the timeout and the kernel returns.
+__global__ void wait_timeout_kernel(uint64_t limit_ns, unsigned *status) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        (void)mbar_wait_ns(&bar, 0, status, limit_ns);
+    __syncthreads();
+}
+
+} // namespace
+
+extern "C" FW_API int fw_selftest_wait_timeout(int limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > 100000)
+        return FW_ERR_INVALID_ARG;
+    unsigned *status = nullptr;
+    if (fw::status_word(&status) != cudaSuccess)
+        return FW_ERR_CUDA;
+    wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>((uint64_t)limit_us * 1000u, status);
+    return cudaGetLastError() == cudaSuccess ? FW_OK : FW_ERR_CUDA;
+}

@@ -53,10 +53,11 @@ FW_DEV uint64_t globaltimer_ns() {
     return t;
 }
 
-// Wait for the phase with the given parity to complete; false on timeout.
+// Wait for the phase with the given parity to complete; false once limit_ns
+// has passed (the device status word then records kStatusTimeout).
 // try_wait itself suspends the thread for a while in hardware, so the loop
 // only re-polls; the elapsed time is checked every 64 polls.
-FW_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *status) {
+FW_DEV bool mbar_wait_ns(uint64_t *bar, uint32_t parity, unsigned *status, uint64_t limit_ns) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity))
         return true;
@@ -64,11 +65,15 @@ FW_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *status) {
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(a, parity))
             return true;
-        if ((i & 63) == 0 && globaltimer_ns() - t0 > kWaitLimitNs)
+        if ((i & 63) == 0 && globaltimer_ns() - t0 > limit_ns)
             break;
     }
     record_status(status, kStatusTimeout);
     return false;
+}
+
+FW_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *status) {
+    return mbar_wait_ns(bar, parity, status, kWaitLimitNs);
 }
 
 FW_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {

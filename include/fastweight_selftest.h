@@ -34,6 +34,16 @@ extern "C" {
 FW_API int fw_selftest_umma(const float *A, const float *B, float *D, int N, int K, int a_mn,
                             int b_mn, int swap_mn, void *stream);
 
+/*
+ * fw_selftest_wait_timeout -- exercises the failure path of the library's
+ * bounded waits without hanging or faulting the GPU: one CTA waits on an
+ * mbarrier that nothing ever arrives at, gives up after limit_us
+ * microseconds (1 .. 100000), records FW_ERR_TIMEOUT in the device status
+ * word and exits normally.  The next fw_device_status() returns
+ * FW_ERR_TIMEOUT and clears it; the CUDA context stays usable.
+ */
+FW_API int fw_selftest_wait_timeout(int limit_us, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

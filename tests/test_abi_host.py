@@ -103,6 +103,9 @@ def test_forward_argument_checks(lib):
     assert _fwd(lib, io=3) == E
     assert _fwd(lib, eps=-1e-6) == E
     assert _fwd(lib, d_key=24) == U
+    assert _fwd(lib, d_key=128, nu=2) == U           # bf16: padded d_dot 512 > 384
+    assert _fwd(lib, d_key=64, nu=3, d_v=256) == U   # bf16: d_v outside {16, 32, 64, 128}
+    assert _fwd(lib, d_key=128, nu=5, io=0) == U     # fp32: d_dot 1280 > 1024
     need = lib.fw_delta_forward_workspace_size(2, 2, 8, 64, 1, 64, 64, 1)
     if need > 0:
         assert _fwd(lib, ws=None, wsb=0) == E

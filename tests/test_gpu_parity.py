@@ -102,6 +102,10 @@ EDGE = [
     (1, 1, 200, 16, 3, 16, 64, "f32", True),      # fp32, several tiles
     (2, 2, 33, 8, 1, 24, 16, "f32", False),       # fp32, odd d_v
     (1, 1, 70, 128, 2, 32, 64, "f32", True),      # d_dot 512
+    (1, 2, 70, 128, 4, 16, 32, "f32", True),      # fp32 at the largest d_dot (1024)
+    (1, 2, 150, 64, 3, 128, 64, "bf16", True),    # bf16 at the largest padded d_dot + d_v (384 + 128)
+    (2, 2, 90, 128, 1, 128, 64, "bf16", False),   # d_key 128, d_v 128
+    (3, 1, 64, 8, 1, 16, 16, "bf16", True),       # the smallest d_key and d_v, exactly one chunk
 ]
 
 
@@ -189,6 +193,20 @@ def test_decode_small_stepped():
                                     d["beta"][t].cuda(), W, nu=nu)
         y_ref, Wr = oracle.delta_decode_step(f64(d["q"][t]), f64(d["k"][t]), f64(d["v"][t]),
                                              f64(d["beta"][t]), Wr, nu, 1e-6, NT)
+        assert maxrel(f64(y), y_ref) <= 2e-2
+    assert maxrel(f64(W), Wr) <= 2e-2
+
+
+def test_decode_largest_state_row():
+    """d_dot = 1024 (d_key 128, nu 4): the widest row the decode kernel holds."""
+    d = inputs.decode_inputs(2, 2, 128, 4, 64, 3, "bf16", w0_var=0.01, seed=8)
+    W = d["W0"].cuda()
+    Wr = f64(d["W0"])
+    for t in range(3):
+        y = fw.fw_delta_decode_step(d["q"][t].cuda(), d["k"][t].cuda(), d["v"][t].cuda(),
+                                    d["beta"][t].cuda(), W, nu=4)
+        y_ref, Wr = oracle.delta_decode_step(f64(d["q"][t]), f64(d["k"][t]), f64(d["v"][t]),
+                                             f64(d["beta"][t]), Wr, 4, 1e-6, NT)
         assert maxrel(f64(y), y_ref) <= 2e-2
     assert maxrel(f64(W), Wr) <= 2e-2
 

@@ -51,3 +51,16 @@ def test_swapped_mn_offsets_are_detected():
     assert fw.fw_device_status() == fw.FW_OK
     ref = A.double() @ B.double().T
     assert not np.array_equal(D.cpu().double().numpy(), ref.numpy())
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait on an mbarrier nothing arrives at gives up after its bound, the
+    status word reports FW_ERR_TIMEOUT once, and the GPU keeps working."""
+    assert fw.fw_device_status() == fw.FW_OK
+    fw.fw_selftest_wait_timeout(3000)
+    assert fw.fw_device_status() == fw.FW_ERR_TIMEOUT
+    assert fw.fw_device_status() == fw.FW_OK            # cleared by the read
+    A, B = _operands(64, 64, seed=5)
+    D = fw.fw_selftest_umma(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(D.cpu().double().numpy(), (A.double() @ B.double().T).numpy())
