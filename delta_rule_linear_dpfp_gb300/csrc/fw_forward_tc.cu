@@ -374,48 +374,76 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     tc_fence_after();
     if (__syncthreads_or(!ok))
         goto teardown;
-    {
-        // [W'; Q'] image: rows < 64 take W', rows >= 64 take Q - P W'
-        uint8_t *ai = rec + rc.a;
-        for (int c0 = 32 * half; c0 < Dp; c0 += 64) { // 32 columns per pass (Dp % 64 == 0)
-            float w[32];
-            tmem_ld16(tm + lb + (uint32_t)c0, w);
-            tmem_ld16(tm + lb + (uint32_t)(c0 + 16), w + 16);
-            tmem_ld_wait();
+    // Record out.  1) the key rows of the [K; Q] tile go out as the K image
+    // (bulk copies of the 64-row halves of each 64-column block);
+    if (tid == 0) {
+        for (int kb = 0; kb < Dp / 64; ++kb)
+            bulk_s2g(rec + rc.k + (size_t)kb * 8192, kq + (size_t)kb * 16384, 8192);
+        bulk_commit();
+        bulk_wait_read();
+    }
+    __syncthreads();
+    // 2) W' replaces the key rows and Q' = Q - P W' the query rows of the
+    //    tile in place;
+    for (int c0 = 32 * half; c0 < Dp; c0 += 64) { // 32 columns per pass (Dp % 64 == 0)
+        float w[32];
+        tmem_ld16(tm + lb + (uint32_t)c0, w);
+        tmem_ld16(tm + lb + (uint32_t)(c0 + 16), w + 16);
+        tmem_ld_wait();
+#pragma unroll
+        for (int h2 = 0; h2 < 4; ++h2) {
+            uint4 *dst = reinterpret_cast<uint4 *>(kq + kmajor_chunk(row, c0 + 8 * h2, 128));
             if (row >= 64) {
+                float qv[8];
+                unpack8(*dst, qv);
 #pragma unroll
-                for (int h2 = 0; h2 < 4; ++h2) {
-                    float qv[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(kq + kmajor_chunk(row, c0 + 8 * h2, 128)), qv);
+                for (int e = 0; e < 8; ++e)
+                    w[8 * h2 + e] = qv[e] - w[8 * h2 + e];
+            }
+            *dst = pack8(w + 8 * h2);
+        }
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0)
+        bulk_s2g(rec + rc.a, kq, 256u * (uint32_t)Dp); // 3) the [W'; Q'] tile goes out
+    // 4) U' (rows < 64) and Y' (rows >= 64) in fp32 through the freed space
+    //    from the [I; P] tile on (62 KB): both at once when they fit, else U'
+    //    then Y'.
+    {
+        float *uy = (float *)ip;
+        const bool both = 128 * d_v * 4 <= (int)((uint8_t *)bs - ip);
+        for (int pass = 0; pass < (both ? 1 : 2); ++pass) {
+            const bool mine = both || ((row >= 64) == (pass == 1));
+            if (mine) {
+                for (int c0 = 16 * half; c0 < d_v; c0 += 32) {
+                    float w[16];
+                    tmem_ld16(tm + lb + (uint32_t)(Dp + c0), w);
+                    tmem_ld_wait();
+                    float *dst = uy + (size_t)(both ? row : (row & 63)) * d_v + c0;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        w[8 * h2 + e] = qv[e] - w[8 * h2 + e];
+                    for (int e = 0; e < 16; e += 4)
+                        *reinterpret_cast<float4 *>(dst + e) = make_float4(w[e], w[e + 1], w[e + 2], w[e + 3]);
                 }
             }
-#pragma unroll
-            for (int h2 = 0; h2 < 4; ++h2)
-                *reinterpret_cast<uint4 *>(ai + kmajor_chunk(row, c0 + 8 * h2, 128)) = pack8(w + 8 * h2);
-        }
-        // U' (rows < 64) and Y' (rows >= 64), fp32
-        float *dst = (float *)(rec + (row < 64 ? rc.up : rc.yp)) + (size_t)(row & 63) * d_v;
-        for (int c0 = 16 * half; c0 < d_v; c0 += 32) {
-            float w[16];
-            tmem_ld16(tm + lb + (uint32_t)(Dp + c0), w);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 16; e += 4)
-                *reinterpret_cast<float4 *>(dst + c0 + e) = make_float4(w[e], w[e + 1], w[e + 2], w[e + 3]);
-        }
-        // K image: the key rows of the [K; Q] tile, re-blocked to 64-row blocks
-        uint8_t *ki = rec + rc.k;
-        const int cpr = Dp / 8;
-        for (int idx = tid; idx < 64 * cpr; idx += kPrepThreads) {
-            const int t = idx / cpr, m = 8 * (idx % cpr);
-            *reinterpret_cast<uint4 *>(ki + kmajor_chunk(t, m, 64)) =
-                *reinterpret_cast<const uint4 *>(kq + kmajor_chunk(t, m, 128));
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                if (both) {
+                    bulk_s2g(rec + rc.up, uy, 256u * (uint32_t)d_v);
+                    bulk_s2g(rec + rc.yp, uy + 64 * d_v, 256u * (uint32_t)d_v);
+                } else {
+                    bulk_s2g(rec + (pass ? rc.yp : rc.up), uy, 256u * (uint32_t)d_v);
+                }
+                bulk_commit();
+                bulk_wait_read(); // the staging space may be reused / released
+            }
+            __syncthreads();
         }
     }
 teardown:
+    if (tid == 0)
+        bulk_wait_all(); // the record is in global memory before the CTA retires
     tc_fence_before();
     __syncthreads();
     if (warp == 0)

@@ -91,6 +91,20 @@ FW_DEV void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) 
                  : "memory");
 }
 
+// shared -> global, tracked by this thread's bulk-async group.  dst, src and
+// bytes must be multiples of 16.
+FW_DEV void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+FW_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk store of this thread has finished reading
+// its shared-memory source (the source may then be overwritten or released).
+FW_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk store of this thread has fully completed.
+FW_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor core, bulk copies) once followed by a CTA barrier.
 FW_DEV void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
