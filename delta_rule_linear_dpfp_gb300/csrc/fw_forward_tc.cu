@@ -451,38 +451,16 @@ teardown:
 }
 
 // ---------------------------------------------------------------------------
-// Row `row` of an MN-major SW128 operand tile whose rows are the contraction
-// index and whose columns are value channels (64-column blocks `blk` bytes
-// apart): write DVB values as bf16.
-template <int DVB>
-FW_DEV void write_vrow(uint8_t *tile, int row, const float *v, uint32_t blk) {
-#pragma unroll
-    for (int j0 = 0; j0 < DVB; j0 += 8) {
-        const uint32_t off = (uint32_t)(j0 >> 6) * blk + (uint32_t)row * 128u +
-                             ((uint32_t)(((j0 & 63) >> 3) ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4 *>(tile + off) = pack8(v + j0);
-    }
+// 16-byte chunk holding columns j0 .. j0+7 of row `row` of an MN-major SW128
+// operand tile whose rows are the contraction index and whose columns are
+// value channels (64-column blocks `blk` bytes apart).
+FW_DEV uint32_t vtile_chunk(int row, int j0, uint32_t blk) {
+    return (uint32_t)(j0 >> 6) * blk + (uint32_t)row * 128u + ((uint32_t)(((j0 & 63) >> 3) ^ (row & 7)) << 4);
 }
 
-template <int DVB>
-FW_DEV void tmem_ld_row(uint32_t taddr, float *r) {
+FW_DEV void load16_f32(const float *src, float *dst) {
 #pragma unroll
-    for (int j0 = 0; j0 < DVB; j0 += 16)
-        tmem_ld16(taddr + (uint32_t)j0, r + j0);
-}
-
-// Column d of the K-major S tile (rows = value channel, DVB rows): S[j][d] = s[j].
-template <int DVB>
-FW_DEV void write_scol(uint8_t *st, int d, const float *s) {
-#pragma unroll
-    for (int j = 0; j < DVB; ++j)
-        *reinterpret_cast<__nv_bfloat16 *>(st + kmajor_off(j, d, DVB)) = __float2bfloat16_rn(s[j]);
-}
-
-template <int DVB>
-FW_DEV void load_row_f32(const float *src, float *dst) {
-#pragma unroll
-    for (int j = 0; j < DVB; j += 4) {
+    for (int j = 0; j < 16; j += 4) {
         const float4 f = __ldg(reinterpret_cast<const float4 *>(src + j));
         dst[j] = f.x;
         dst[j + 1] = f.y;
@@ -491,20 +469,27 @@ FW_DEV void load_row_f32(const float *src, float *dst) {
     }
 }
 
-template <int DVB>
+// One CTA walks the chunks of one (batch, head) for DVB value channels.
+// Everything per thread is done 16 value channels at a time.  NKB = number
+// of K buffers (2: K images two chunks ahead; 1: the next K image is
+// fetched as soon as MMA3 has read the current one).
+template <int DVB, int NKB>
 __global__ void __launch_bounds__(kScanThreads)
     chunk_scan_kernel(const float *W0, float *Wf, __nv_bfloat16 *__restrict__ y, const uint8_t *__restrict__ ws,
                       int L, int C, int nch, int d_v, int d_dot, int Dp, unsigned *status) {
     constexpr int DS = DVB < 32 ? 32 : DVB;          // TMEM columns per accumulator region
+    constexpr int VB = (DVB + 63) / 64;              // 64-column blocks of the value tiles
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const Record rc = record_layout(Dp, d_v);
     const uint32_t a_bytes = 256u * (uint32_t)Dp, k_bytes = 128u * (uint32_t)Dp;
+    const uint32_t sblk = 128u * (uint32_t)Dp;       // bytes of one 64-column block of the S tile
     uint8_t *at = smem;                               // [W'; Q']  128 x Dp
-    uint8_t *kt0 = at + a_bytes, *kt1 = kt0 + k_bytes; // K, two buffers
-    uint8_t *st = kt1 + k_bytes;                      // S: rows v, columns d (K-major, DVB rows)
-    uint8_t *ut = st + 2u * DVB * (uint32_t)Dp;       // U: rows t, columns v (MN-major)
-    uint64_t *bar_a = (uint64_t *)(ut + 8192);
+    uint8_t *kt0 = at + a_bytes;                      // K image(s)
+    uint8_t *kt1 = NKB == 2 ? kt0 + k_bytes : kt0;
+    uint8_t *st = kt0 + NKB * k_bytes;                // S: rows d, columns v (MN-major)
+    uint8_t *ut = st + VB * sblk;                     // U: rows t, columns v (MN-major)
+    uint64_t *bar_a = (uint64_t *)(ut + VB * 8192);
     uint64_t *bar_k = bar_a + 1;                      // [2]
     uint64_t *bar_mma = bar_a + 3;
     uint32_t *slot = (uint32_t *)(bar_a + 4);
@@ -537,12 +522,12 @@ __global__ void __launch_bounds__(kScanThreads)
     const uint32_t at_s = smem_u32(at), st_s = smem_u32(st), ut_s = smem_u32(ut);
     const uint32_t kt0_s = smem_u32(kt0), kt1_s = smem_u32(kt1);
 
-    if (tid == 0) { // chunk 0's [W'; Q'] and the first two K images
+    if (tid == 0) { // chunk 0's [W'; Q'] and the first K image(s)
         mbar_arrive_expect_tx(bar_a, a_bytes);
         bulk_g2s(at, rec0 + rc.a, a_bytes, bar_a);
         mbar_arrive_expect_tx(bar_k, k_bytes);
         bulk_g2s(kt0, rec0 + rc.k, k_bytes, bar_k);
-        if (nch > 1) {
+        if (NKB == 2 && nch > 1) {
             mbar_arrive_expect_tx(bar_k + 1, k_bytes);
             bulk_g2s(kt1, rec0 + rc.bytes + rc.k, k_bytes, bar_k + 1);
         }
@@ -550,16 +535,17 @@ __global__ void __launch_bounds__(kScanThreads)
     // initial state: S^T in TMEM (fp32) and S as the bf16 operand of MMA1
     for (int mb = 0; mb < MB; ++mb) {
         const int d = 128 * mb + tid;
-        float w[DVB];
 #pragma unroll
-        for (int j = 0; j < DVB; ++j)
-            w[j] = (has_w0 && d < d_dot) ? W0[((size_t)bh * d_v + v0 + j) * d_dot + d] : 0.f;
-        if (has_w0) {
+        for (int j0 = 0; j0 < DVB; j0 += 16) {
+            float w[16];
 #pragma unroll
-            for (int j0 = 0; j0 < DVB; j0 += 16)
-                tmem_st16(tS + (uint32_t)(mb * DS + j0) + lb, w + j0);
+            for (int j = 0; j < 16; ++j)
+                w[j] = (has_w0 && d < d_dot) ? W0[((size_t)bh * d_v + v0 + j0 + j) * d_dot + d] : 0.f;
+            if (has_w0)
+                tmem_st16(tS + (uint32_t)(mb * DS + j0) + lb, w);
+            *reinterpret_cast<uint4 *>(st + vtile_chunk(d, j0, sblk)) = pack8(w);
+            *reinterpret_cast<uint4 *>(st + vtile_chunk(d, j0 + 8, sblk)) = pack8(w + 8);
         }
-        write_scol<DVB>(st, d, w);
     }
     if (has_w0)
         tmem_st_wait();
@@ -569,11 +555,17 @@ __global__ void __launch_bounds__(kScanThreads)
 
     uint32_t mma_phase = 0;
     for (int c = 0; c < nch; ++c) {
-        const int t0 = c * C, Lc = min(C, L - t0), kb = c & 1;
+        const int t0 = c * C, Lc = min(C, L - t0), kb = NKB == 2 ? (c & 1) : 0;
+        const uint32_t k_parity = NKB == 2 ? (uint32_t)((c >> 1) & 1) : (uint32_t)(c & 1);
         const uint8_t *rec = rec0 + (size_t)c * rc.bytes;
         // U' (rows 0..63, threads 0..63) or Y' (threads 64..127) of this chunk
         float pre[DVB];
-        load_row_f32<DVB>((const float *)(rec + (tid < 64 ? rc.up : rc.yp)) + (size_t)(tid & 63) * d_v + v0, pre);
+        {
+            const float *src = (const float *)(rec + (tid < 64 ? rc.up : rc.yp)) + (size_t)(tid & 63) * d_v + v0;
+#pragma unroll
+            for (int j0 = 0; j0 < DVB; j0 += 16)
+                load16_f32(src + j0, pre + j0);
+        }
         bool ok = mbar_wait(bar_a, (uint32_t)(c & 1), status);
         if (__syncthreads_or(!ok))
             break;
@@ -581,10 +573,10 @@ __global__ void __launch_bounds__(kScanThreads)
         // MMA1: D1 = [W'; Q'] S^T
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t idesc = idesc_bf16(128, DVB, 0, 0);
+            const uint32_t idesc = idesc_bf16(128, DVB, 0, 1);
             for (int s = 0; s < Dp / 16; ++s)
                 mma_bf16(tD1, desc_sw128(at_s + kmajor_step(s, 128), 16, 1024),
-                         desc_sw128(st_s + kmajor_step(s, DVB), 16, 1024), idesc, s > 0);
+                         desc_sw128(st_s + (uint32_t)s * 2048u, sblk, 1024), idesc, s > 0);
             mma_commit(bar_mma);
         }
         ok = mbar_wait(bar_mma, mma_phase, status);
@@ -598,26 +590,31 @@ __global__ void __launch_bounds__(kScanThreads)
         }
         {
             float d1[DVB];
-            tmem_ld_row<DVB>(tD1 + lb, d1);
+#pragma unroll
+            for (int j0 = 0; j0 < DVB; j0 += 16) // every load in flight, then one wait
+                tmem_ld16(tD1 + lb + (uint32_t)j0, d1 + j0);
             tmem_ld_wait();
-            if (tid < 64) {                       // U = U' - W' S^T
 #pragma unroll
-                for (int j = 0; j < DVB; ++j)
-                    d1[j] = pre[j] - d1[j];
-                write_vrow<DVB>(ut, tid, d1, 8192u);
-            } else if (tid - 64 < Lc) {           // y = Y' + Q' S^T
+            for (int j0 = 0; j0 < DVB; j0 += 16) {
+                if (tid < 64) {                       // U = U' - W' S^T
 #pragma unroll
-                for (int j = 0; j < DVB; ++j)
-                    d1[j] += pre[j];
-                __nv_bfloat16 *dst = y + ((size_t)bh * L + t0 + (tid - 64)) * d_v + v0;
+                    for (int j = 0; j < 16; ++j)
+                        d1[j0 + j] = pre[j0 + j] - d1[j0 + j];
+                    *reinterpret_cast<uint4 *>(ut + vtile_chunk(tid, j0, 8192u)) = pack8(d1 + j0);
+                    *reinterpret_cast<uint4 *>(ut + vtile_chunk(tid, j0 + 8, 8192u)) = pack8(d1 + j0 + 8);
+                } else if (tid - 64 < Lc) {           // y = Y' + Q' S^T
 #pragma unroll
-                for (int j0 = 0; j0 < DVB; j0 += 8)
-                    *reinterpret_cast<uint4 *>(dst + j0) = pack8(d1 + j0);
+                    for (int j = 0; j < 16; ++j)
+                        d1[j0 + j] += pre[j0 + j];
+                    __nv_bfloat16 *dst = y + ((size_t)bh * L + t0 + (tid - 64)) * d_v + v0 + j0;
+                    *reinterpret_cast<uint4 *>(dst) = pack8(d1 + j0);
+                    *reinterpret_cast<uint4 *>(dst + 8) = pack8(d1 + j0 + 8);
+                }
             }
         }
         fence_async_smem();
         tc_fence_before();
-        ok = mbar_wait(bar_k + kb, (uint32_t)((c >> 1) & 1), status);
+        ok = mbar_wait(bar_k + kb, k_parity, status);
         if (__syncthreads_or(!ok))
             break;
 
@@ -625,12 +622,12 @@ __global__ void __launch_bounds__(kScanThreads)
         if (tid == 0) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(128, DVB, 1, 1);
+            const uint32_t kbase = kb ? kt1_s : kt0_s;
             for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     mma_bf16(tS + (uint32_t)(mb * DS),
-                             desc_sw128((kb ? kt1_s : kt0_s) + (uint32_t)(2 * mb) * 8192u + (uint32_t)s * 2048u,
-                                        8192, 1024),
+                             desc_sw128(kbase + (uint32_t)(2 * mb) * 8192u + (uint32_t)s * 2048u, 8192, 1024),
                              desc_sw128(ut_s + (uint32_t)s * 2048u, 8192, 1024), idesc,
                              (s > 0 || c > 0 || has_w0) ? 1u : 0u);
             mma_commit(bar_mma);
@@ -640,21 +637,27 @@ __global__ void __launch_bounds__(kScanThreads)
         if (__syncthreads_or(!ok))
             break;
         tc_fence_after();
-        if (tid == 0 && c + 2 < nch) { // K buffer kb consumed: fetch chunk c+2's
+        if (tid == 0 && c + NKB < nch) { // this K buffer is consumed: fetch a later chunk's
             mbar_arrive_expect_tx(bar_k + kb, k_bytes);
-            bulk_g2s(kb ? kt1 : kt0, rec + 2 * rc.bytes + rc.k, k_bytes, bar_k + kb);
+            bulk_g2s(kb ? kt1 : kt0, rec + (size_t)NKB * rc.bytes + rc.k, k_bytes, bar_k + kb);
         }
         for (int mb = 0; mb < MB; ++mb) {
             const int d = 128 * mb + tid;
             float sv[DVB];
-            tmem_ld_row<DVB>(tS + (uint32_t)(mb * DS) + lb, sv);
-            tmem_ld_wait();
-            if (c + 1 < nch) {
-                write_scol<DVB>(st, d, sv);
-            } else if (Wf && d < d_dot) {
 #pragma unroll
-                for (int j = 0; j < DVB; ++j)
-                    Wf[((size_t)bh * d_v + v0 + j) * d_dot + d] = sv[j];
+            for (int j0 = 0; j0 < DVB; j0 += 16) // every load in flight, then one wait
+                tmem_ld16(tS + (uint32_t)(mb * DS + j0) + lb, sv + j0);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j0 = 0; j0 < DVB; j0 += 16) {
+                if (c + 1 < nch) {
+                    *reinterpret_cast<uint4 *>(st + vtile_chunk(d, j0, sblk)) = pack8(sv + j0);
+                    *reinterpret_cast<uint4 *>(st + vtile_chunk(d, j0 + 8, sblk)) = pack8(sv + j0 + 8);
+                } else if (Wf && d < d_dot) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        Wf[((size_t)bh * d_v + v0 + j0 + j) * d_dot + d] = sv[j0 + j];
+                }
             }
         }
         fence_async_smem();
@@ -674,24 +677,27 @@ size_t prep_smem(int Dp, int d_v) {
     return (size_t)256 * Dp + 16384 + 8192 + (2 * 64 + 16) * LDS * 4 + 64 * 4 + 16 + 1024;
 }
 
-size_t scan_smem(int Dp, int dvb) {
-    return (size_t)512 * Dp + (size_t)2 * dvb * Dp + 8192 + 64 + 1024;
+size_t scan_smem(int Dp, int dvb, int nkb) {
+    const int VB = (dvb + 63) / 64;
+    return (size_t)256 * Dp + (size_t)nkb * 128 * Dp + (size_t)VB * 128 * Dp + (size_t)VB * 8192 + 64 + 1024;
 }
 
 constexpr size_t kMaxSmem = 227 * 1024;
 
 bool fits(int Dp, int d_v, int dvb) {
-    return Dp <= kMaxDp && Dp + d_v <= 512 && scan_smem(Dp, dvb) <= kMaxSmem && prep_smem(Dp, d_v) <= kMaxSmem;
+    return Dp <= kMaxDp && Dp + d_v <= 512 && scan_smem(Dp, dvb, 1) <= kMaxSmem && prep_smem(Dp, d_v) <= kMaxSmem;
 }
 
-// Channels per scan CTA: 16 spreads the serial chunk walk over the most CTAs;
-// 32 only when 16 would exceed two CTAs per SM.
-int choose_dvb(int BH, int d_v, int Dp, int num_sms) {
-    int dvb = 16;
-    while (dvb < d_v && dvb < 32 && (int64_t)BH * (d_v / dvb) > 2 * (int64_t)num_sms && fits(Dp, d_v, 2 * dvb))
-        dvb *= 2;
-    return dvb;
-}
+// Value channels per scan CTA.  The walk over the chunks is serial, so the
+// per-chunk latency decides: a tcgen05.mma of M = 128 costs about the same
+// for any N up to 128, but the per-thread work between the MMAs (TMEM loads,
+// the U and S tiles, y) grows with the channel count.  Measured on the
+// b4h8 L512 and nu = 3 L2048 workloads, 16 channels per CTA beat 32 and 64
+// (scan 14.4 / 18.5 / 24.5 us and 80 / 96 / 141 us).
+int choose_dvb(int d_v) { return 16 <= d_v ? 16 : d_v; }
+
+// Two K buffers when they fit in shared memory, else one.
+int choose_nkb(int Dp, int dvb) { return scan_smem(Dp, dvb, 2) <= kMaxSmem ? 2 : 1; }
 
 template <int DK>
 cudaError_t launch_prep(const void *q, const void *k, const void *v, const void *beta, uint8_t *ws, int BH,
@@ -709,17 +715,25 @@ cudaError_t launch_prep(const void *q, const void *k, const void *v, const void 
     return cudaGetLastError();
 }
 
-template <int DVB>
+template <int DVB, int NKB>
 cudaError_t launch_scan(const float *W0, float *Wf, void *y, const uint8_t *ws, int BH, int L, int C, int nch,
                         int d_v, int d_dot, int Dp, unsigned *status, cudaStream_t st) {
-    const size_t smem = scan_smem(Dp, DVB);
-    auto kern = chunk_scan_kernel<DVB>;
+    const size_t smem = scan_smem(Dp, DVB, NKB);
+    auto kern = chunk_scan_kernel<DVB, NKB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
     kern<<<dim3((unsigned)(d_v / DVB), (unsigned)BH), kScanThreads, smem, st>>>(
         W0, Wf, static_cast<__nv_bfloat16 *>(y), ws, L, C, nch, d_v, d_dot, Dp, status);
     return cudaGetLastError();
+}
+
+template <int DVB>
+cudaError_t launch_scan_nkb(const float *W0, float *Wf, void *y, const uint8_t *ws, int BH, int L, int C, int nch,
+                            int d_v, int d_dot, int Dp, unsigned *status, cudaStream_t st) {
+    if (choose_nkb(Dp, DVB) == 2)
+        return launch_scan<DVB, 2>(W0, Wf, y, ws, BH, L, C, nch, d_v, d_dot, Dp, status, st);
+    return launch_scan<DVB, 1>(W0, Wf, y, ws, BH, L, C, nch, d_v, d_dot, Dp, status, st);
 }
 
 } // namespace
@@ -731,7 +745,7 @@ bool tc_forward_supported(int d_key, int nu, int d_v, int chunk) {
         return false;
     if (chunk < 1 || chunk > kTile)
         return false;
-    return fits(padded_ddot(2 * d_key * nu), d_v, 16);
+    return fits(padded_ddot(2 * d_key * nu), d_v, choose_dvb(d_v));
 }
 
 size_t tc_forward_workspace_bytes(int B, int H, int L, int d_key, int nu, int d_v, int chunk) {
@@ -763,9 +777,11 @@ cudaError_t tc_scan_launch(const void *workspace, const float *W0, float *W_fina
     const int d_dot = 2 * d_key * nu;
     const int Dp = padded_ddot(d_dot);
     const uint8_t *ws = static_cast<const uint8_t *>(workspace);
-    switch (choose_dvb(BH, d_v, Dp, num_sms)) {
-    case 16: return launch_scan<16>(W0, W_final, y, ws, BH, L, chunk, nch, d_v, d_dot, Dp, status, st);
-    case 32: return launch_scan<32>(W0, W_final, y, ws, BH, L, chunk, nch, d_v, d_dot, Dp, status, st);
+    (void)num_sms;
+    switch (choose_dvb(d_v)) {
+    case 16: return launch_scan_nkb<16>(W0, W_final, y, ws, BH, L, chunk, nch, d_v, d_dot, Dp, status, st);
+    case 32: return launch_scan_nkb<32>(W0, W_final, y, ws, BH, L, chunk, nch, d_v, d_dot, Dp, status, st);
+    case 64: return launch_scan_nkb<64>(W0, W_final, y, ws, BH, L, chunk, nch, d_v, d_dot, Dp, status, st);
     default: return cudaErrorInvalidValue;
     }
 }
