@@ -203,6 +203,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     uint8_t *rec = ws + ((size_t)bh * nch + c) * rc.bytes;
     const uint32_t ncols = tmem_cols_pow2(max(64, Dp + d_v));
 
+    griddep_launch_dependents(); // the scan may start its prologue on free SMs
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_barrier_init();
@@ -522,17 +523,9 @@ __global__ void __launch_bounds__(kScanThreads)
     const uint32_t at_s = smem_u32(at), st_s = smem_u32(st), ut_s = smem_u32(ut);
     const uint32_t kt0_s = smem_u32(kt0), kt1_s = smem_u32(kt1);
 
-    if (tid == 0) { // chunk 0's [W'; Q'] and the first K image(s)
-        mbar_arrive_expect_tx(bar_a, a_bytes);
-        bulk_g2s(at, rec0 + rc.a, a_bytes, bar_a);
-        mbar_arrive_expect_tx(bar_k, k_bytes);
-        bulk_g2s(kt0, rec0 + rc.k, k_bytes, bar_k);
-        if (NKB == 2 && nch > 1) {
-            mbar_arrive_expect_tx(bar_k + 1, k_bytes);
-            bulk_g2s(kt1, rec0 + rc.bytes + rc.k, k_bytes, bar_k + 1);
-        }
-    }
-    // initial state: S^T in TMEM (fp32) and S as the bf16 operand of MMA1
+    // initial state: S^T in TMEM (fp32) and S as the bf16 operand of MMA1.
+    // W0 is the caller's, never written by the prep kernel, so this runs
+    // before the wait for the prep to finish.
     for (int mb = 0; mb < MB; ++mb) {
         const int d = 128 * mb + tid;
 #pragma unroll
@@ -549,6 +542,18 @@ __global__ void __launch_bounds__(kScanThreads)
     }
     if (has_w0)
         tmem_st_wait();
+    // the workspace records are the prep kernel's: wait for it to complete
+    griddep_wait();
+    if (tid == 0) { // chunk 0's [W'; Q'] and the first K image(s)
+        mbar_arrive_expect_tx(bar_a, a_bytes);
+        bulk_g2s(at, rec0 + rc.a, a_bytes, bar_a);
+        mbar_arrive_expect_tx(bar_k, k_bytes);
+        bulk_g2s(kt0, rec0 + rc.k, k_bytes, bar_k);
+        if (NKB == 2 && nch > 1) {
+            mbar_arrive_expect_tx(bar_k + 1, k_bytes);
+            bulk_g2s(kt1, rec0 + rc.bytes + rc.k, k_bytes, bar_k + 1);
+        }
+    }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -723,9 +728,21 @@ cudaError_t launch_scan(const float *W0, float *Wf, void *y, const uint8_t *ws, 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    kern<<<dim3((unsigned)(d_v / DVB), (unsigned)BH), kScanThreads, smem, st>>>(
-        W0, Wf, static_cast<__nv_bfloat16 *>(y), ws, L, C, nch, d_v, d_dot, Dp, status);
-    return cudaGetLastError();
+    // programmatic dependent launch: the scan's CTAs may be scheduled while
+    // the preceding kernel (the prep) finishes; they wait in griddep_wait
+    // before reading its output
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(d_v / DVB), (unsigned)BH);
+    cfg.blockDim = dim3(kScanThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, W0, Wf, static_cast<__nv_bfloat16 *>(y), ws, L, C, nch, d_v, d_dot, Dp,
+                              status);
 }
 
 template <int DVB>
