@@ -54,7 +54,7 @@ using namespace tc;
 constexpr int kTile = 64;          // token rows of a chunk tile (chunk <= 64, padded)
 constexpr int kPrepThreads = 256;
 constexpr int kScanThreads = 128;
-constexpr int LDS = 65;            // fp32 row stride of the 64 x 64 work matrices
+constexpr int LDS = 68;            // fp32 row stride of the 64 x 64 work matrices (16-byte rows)
 constexpr int kMaxDp = 384;        // padded d_dot the scan's shared memory holds
 
 __host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
@@ -68,13 +68,17 @@ __host__ __device__ inline Record record_layout(int Dp, int d_v) {
     Record r;
     r.a = 0;                                // [W'; Q']: 128 x Dp bf16, K-major SW128
     r.k = (size_t)256 * Dp;                 // K: 64 x Dp bf16, K-major SW128 (64-row blocks)
-    r.up = r.k + (size_t)128 * Dp;          // U': 64 x d_v fp32, row-major
-    r.yp = r.up + (size_t)256 * d_v;        // Y': 64 x d_v fp32, row-major
+    r.up = r.k + (size_t)128 * Dp;          // U': 64 x d_v fp32, [d_v/4][64 rows][4 channels]
+    r.yp = r.up + (size_t)256 * d_v;        // Y': 64 x d_v fp32, same layout
     r.bytes = r.yp + (size_t)256 * d_v;
     return r;
 }
 
-FW_DEV uint8_t *align1024(uint8_t *p) { return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023); }
+// First 1024-byte boundary at or after the dynamic shared-memory base.  The
+// result is the base plus an offset, never a pointer rebuilt from an integer,
+// so the compiler still knows it addresses shared memory and emits shared
+// (not generic) loads and stores through it.
+FW_DEV uint8_t *align1024(uint8_t *p) { return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u); }
 
 FW_DEV uint4 pack8(const float *v) {
     uint4 u;
@@ -102,12 +106,11 @@ FW_DEV uint32_t tmem_cols_pow2(int need) {
 // (I + A)^-1 for a strictly lower 64 x 64 A, by 16 x 16 blocks:
 //   diagonal blocks by forward substitution (one column per thread), then
 //   block row I: N_IJ = -N_II * sum_{K=J}^{I-1} A_IK N_KJ   (J < I).
-// A, N: [64][LDS]; R: [16][LDS] scratch.  NT threads; ends synchronised.
+// A, N: [64][LDS]; R: [16][LDS] scratch; all 16-byte aligned.  Only the
+// blocks on and below the diagonal of N are written (the ones above are
+// zero and never read here).  NT threads; ends synchronised.
 template <int NT>
 FW_DEV void unit_lower_inverse(const float *A, float *N, float *R, int tid) {
-    for (int i = tid; i < 64 * LDS; i += NT)
-        N[i] = 0.f;
-    __syncthreads();
     if (tid < 64) {
         const int o = 16 * (tid >> 4), j = tid & 15;
         float col[16];
@@ -124,49 +127,109 @@ FW_DEV void unit_lower_inverse(const float *A, float *N, float *R, int tid) {
             N[(o + i) * LDS + o + j] = col[i];
     }
     __syncthreads();
-    // off-diagonal blocks; each thread computes 4 adjacent outputs of a row,
-    // so every A (or N) element it loads feeds 4 FMAs
+    // off-diagonal blocks; each thread computes 4 adjacent outputs of a row
+    // from 16-byte loads, so every A (or N) element it loads feeds 4 FMAs
     for (int I = 1; I < 4; ++I) {
         for (int idx = tid; idx < 64 * I; idx += NT) {
             const int J = idx >> 6, ii = (idx >> 2) & 15, j0 = 16 * J + 4 * (idx & 3);
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int K = J; K < I; ++K) {
+                const float *ar = A + (16 * I + ii) * LDS + 16 * K;
 #pragma unroll
-                for (int s = 0; s < 16; ++s) {
-                    const float a = A[(16 * I + ii) * LDS + 16 * K + s];
-                    const float *nr = N + (16 * K + s) * LDS + j0;
-                    a0 = fmaf(a, nr[0], a0);
-                    a1 = fmaf(a, nr[1], a1);
-                    a2 = fmaf(a, nr[2], a2);
-                    a3 = fmaf(a, nr[3], a3);
+                for (int s4 = 0; s4 < 16; s4 += 4) {
+                    const float4 a = *reinterpret_cast<const float4 *>(ar + s4);
+                    const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 n = *reinterpret_cast<const float4 *>(N + (16 * K + s4 + e) * LDS + j0);
+                        acc.x = fmaf(av[e], n.x, acc.x);
+                        acc.y = fmaf(av[e], n.y, acc.y);
+                        acc.z = fmaf(av[e], n.z, acc.z);
+                        acc.w = fmaf(av[e], n.w, acc.w);
+                    }
                 }
             }
-            float *rr = R + ii * LDS + j0;
-            rr[0] = a0;
-            rr[1] = a1;
-            rr[2] = a2;
-            rr[3] = a3;
+            *reinterpret_cast<float4 *>(R + ii * LDS + j0) = acc;
         }
         __syncthreads();
         for (int idx = tid; idx < 64 * I; idx += NT) {
-            const int J = idx >> 6, ii = (idx >> 2) & 15, j0 = 16 * J + 4 * (idx & 3);
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            const int ii = (idx >> 2) & 15, j0 = 16 * (idx >> 6) + 4 * (idx & 3);
+            const float *nr = N + (16 * I + ii) * LDS + 16 * I;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int s = 0; s < 16; ++s) {
-                const float n = N[(16 * I + ii) * LDS + 16 * I + s];
-                const float *rr = R + s * LDS + j0;
-                a0 = fmaf(n, rr[0], a0);
-                a1 = fmaf(n, rr[1], a1);
-                a2 = fmaf(n, rr[2], a2);
-                a3 = fmaf(n, rr[3], a3);
+            for (int s4 = 0; s4 < 16; s4 += 4) {
+                const float4 nn = *reinterpret_cast<const float4 *>(nr + s4);
+                const float nv[4] = {nn.x, nn.y, nn.z, nn.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 r = *reinterpret_cast<const float4 *>(R + (s4 + e) * LDS + j0);
+                    acc.x = fmaf(nv[e], r.x, acc.x);
+                    acc.y = fmaf(nv[e], r.y, acc.y);
+                    acc.z = fmaf(nv[e], r.z, acc.z);
+                    acc.w = fmaf(nv[e], r.w, acc.w);
+                }
             }
-            float *nd = N + (16 * I + ii) * LDS + j0;
-            nd[0] = -a0;
-            nd[1] = -a1;
-            nd[2] = -a2;
-            nd[3] = -a3;
+            *reinterpret_cast<float4 *>(N + (16 * I + ii) * LDS + j0) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// DPFP of one row of the [K; Q] tile by two threads (d_key <= 64).  Row x =
+// ReLU([k, -k]) has n = 2 DK entries; the thread with hs = 0 owns
+// x[0 .. DK-1] = ReLU(k), the one with hs = 1 owns x[DK .. n-1] = ReLU(-k)
+// (the same DK raw values, opposite sign).  Block i of phi needs
+// x[j] * x[(j - i) mod n] (torch.roll(shifts=i), DPFP source of the Fast
+// Weights Transformer guide), so besides its own half the thread builds the
+// NUMAX entries that precede it around the row: going back h places from
+// the start of a half crosses ceil(h / DK) half boundaries (each one flips
+// the sign) and lands on raw index (-h) mod DK.  Every index is static and
+// every product a register operation; the two halves of a row add their
+// sums with one shuffle (partner lane ^ 8).
+template <int DK, int NUMAX>
+FW_DEV void dpfp_half_row(const uint4 (&raw)[DK / 8], int hs, int r, int nu, float eps, uint8_t *kq) {
+    constexpr int N2 = 2 * DK;
+    const float sg = hs ? -1.f : 1.f;
+    float kf[DK];
+#pragma unroll
+    for (int c8 = 0; c8 < DK / 8; ++c8)
+        unpack8(raw[c8], kf + 8 * c8);
+    float xs[NUMAX + DK]; // xs[NUMAX + t] = x[hs DK + t],  xs[NUMAX - h] = x[(hs DK - h) mod n]
+#pragma unroll
+    for (int h = 1; h <= NUMAX; ++h) {
+        const int m = (DK - h % DK) % DK;               // raw index (static)
+        const bool flip = ((h + DK - 1) / DK) & 1;      // odd number of half boundaries crossed
+        xs[NUMAX - h] = fmaxf((flip ? -sg : sg) * kf[m], 0.f);
+    }
+#pragma unroll
+    for (int t = 0; t < DK; ++t)
+        xs[NUMAX + t] = fmaxf(sg * kf[t], 0.f);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 1; i <= NUMAX; ++i) {
+        if (i <= nu) {
+#pragma unroll
+            for (int t = 0; t < DK; ++t)
+                acc[t & 3] = fmaf(xs[NUMAX + t], xs[NUMAX + t - i], acc[t & 3]);
+        }
+    }
+    float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+    const float inv = 1.0f / (sum + eps);
+#pragma unroll
+    for (int i = 1; i <= NUMAX; ++i) {
+        if (i <= nu) {
+#pragma unroll
+            for (int c8 = 0; c8 < DK / 8; ++c8) {
+                float p[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    p[e] = (xs[NUMAX + 8 * c8 + e] * xs[NUMAX + 8 * c8 + e - i]) * inv;
+                *reinterpret_cast<uint4 *>(kq + kmajor_chunk(r, (i - 1) * N2 + hs * DK + 8 * c8, 128)) = pack8(p);
+            }
+        }
     }
 }
 
@@ -204,18 +267,33 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     const uint32_t ncols = tmem_cols_pow2(max(64, Dp + d_v));
 
     griddep_launch_dependents(); // the scan may start its prologue on free SMs
-    if (tid == 0) {
-        mbar_init(bar, 1);
-        fence_barrier_init();
+    // Global loads first, all in flight before any is used: the key and query
+    // rows for the DPFP, the chunk's V rows (kept in registers until their
+    // tile's space is free) and beta (stored to shared memory after the DPFP).
+    constexpr bool kHalfRows = DK <= 64;
+    constexpr int kRaw = kHalfRows ? DK / 8 : 128 / (8 * RPW);
+    uint4 raw[kRaw];
+    // kHalfRows: thread = (row r, half hs of x); lanes l and l ^ 8 share a row
+    const int hs = (lane >> 3) & 1;
+    const int hr = 16 * warp + ((lane & 7) | ((lane >> 4) << 3));
+    if constexpr (kHalfRows) {
+        const int t = hr & 63;
+        const __nv_bfloat16 *src = (hr < 64 ? k : q) + ((size_t)bh * L + t0 + t) * DK;
+#pragma unroll
+        for (int c8 = 0; c8 < kRaw; ++c8)
+            raw[c8] = t < Lc ? __ldg(reinterpret_cast<const uint4 *>(src) + c8) : make_uint4(0, 0, 0, 0);
+    } else {
+        const int g = lane % G;
+#pragma unroll
+        for (int ps = 0; ps < kRaw; ++ps) {
+            const int r = ps * 8 * RPW + warp * RPW + lane / G;
+            const int t = r & 63;
+            raw[ps] = make_uint4(0, 0, 0, 0);
+            if (t < Lc)
+                raw[ps] = __ldg(reinterpret_cast<const uint4 *>((r < 64 ? k : q) + ((size_t)bh * L + t0 + t) * DK +
+                                                               8 * (g % (G / 2))));
+        }
     }
-    if (warp == 0) {
-        tmem_alloc(slot, ncols);
-        tmem_relinquish();
-    }
-    if (tid < 64)
-        bs[tid] = tid < Lc ? __bfloat162float(beta[bh * L + t0 + tid]) : 0.f;
-    // V rows of the chunk, held in registers until their tile's space is free
-    // (64 rows x d_v/8 chunks of 16 bytes; zero on padded rows)
     constexpr int kVChunks = 4; // 64 * 128 / 8 / kPrepThreads
     uint4 vpre[kVChunks];
     const int vcpr = d_v / 8;
@@ -226,23 +304,25 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         if (idx < 64 * vcpr && t < Lc)
             vpre[i] = __ldg(reinterpret_cast<const uint4 *>(v + ((size_t)bh * L + t0 + t) * d_v + j));
     }
-    // DPFP rows: r < 64 are keys, r >= 64 queries of token r & 63.  Every
-    // pass's 16-byte load is issued before any is used.
-    {
+    float beta_t = 0.f;
+    if (tid < Lc && tid < 64)
+        beta_t = __bfloat162float(beta[bh * L + t0 + tid]);
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(slot, ncols);
+        tmem_relinquish();
+    }
+    // DPFP rows: r < 64 are keys, r >= 64 queries of token r & 63.
+    if constexpr (kHalfRows) {
+        dpfp_half_row<DK, kMaxDp / (2 * DK)>(raw, hs, hr, nu, eps, kq);
+    } else {
         const int g = lane % G, base_lane = lane - g;
-        constexpr int kPasses = 128 / (8 * RPW);
-        uint4 raw[kPasses];
 #pragma unroll
-        for (int ps = 0; ps < kPasses; ++ps) {
-            const int r = ps * 8 * RPW + warp * RPW + lane / G;
-            const int t = r & 63;
-            raw[ps] = make_uint4(0, 0, 0, 0);
-            if (t < Lc)
-                raw[ps] = __ldg(reinterpret_cast<const uint4 *>((r < 64 ? k : q) + ((size_t)bh * L + t0 + t) * DK +
-                                                               8 * (g % (G / 2))));
-        }
-#pragma unroll
-        for (int ps = 0; ps < kPasses; ++ps) {
+        for (int ps = 0; ps < kRaw; ++ps) {
             const int r = ps * 8 * RPW + warp * RPW + lane / G;
             float x[8];
             {
@@ -257,12 +337,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                 *reinterpret_cast<uint4 *>(kq + kmajor_chunk(r, (i - 1) * N2 + 8 * g, 128)) = pack8(p);
             });
         }
+    }
+    {
         const int padc = (Dp - d_dot) / 8; // zero columns d_dot .. Dp-1
         for (int idx = tid; idx < 128 * padc; idx += kPrepThreads) {
             const int r = idx / padc, m = d_dot + 8 * (idx % padc);
             *reinterpret_cast<uint4 *>(kq + kmajor_chunk(r, m, 128)) = make_uint4(0, 0, 0, 0);
         }
     }
+    if (tid < 64)
+        bs[tid] = beta_t; // 0 on padded rows
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -289,15 +373,23 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         tmem_ld16(tm + lb + (uint32_t)(32 * half), gr);
         tmem_ld16(tm + lb + (uint32_t)(32 * half + 16), gr + 16);
         tmem_ld_wait();
+        if (row < 64) { // A row (16-byte stores; rows are 16-byte aligned) and the I row
+            const float br = bs[row];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int s = 32 * half + j;
-            if (row < 64) {
-                Am[row * LDS + s] = s < row ? bs[row] * gr[j] : 0.f;
-                gr[j] = s == row ? 1.f : 0.f;
-            } else {
-                gr[j] = s <= row - 64 ? gr[j] : 0.f;
+            for (int j4 = 0; j4 < 32; j4 += 4) {
+                float a4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int s = 32 * half + j4 + e;
+                    a4[e] = s < row ? br * gr[j4 + e] : 0.f;
+                    gr[j4 + e] = s == row ? 1.f : 0.f;
+                }
+                *reinterpret_cast<float4 *>(Am + row * LDS + 32 * half + j4) = make_float4(a4[0], a4[1], a4[2], a4[3]);
             }
+        } else {        // P row: Q K^T on and below the diagonal
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                gr[j] = 32 * half + j <= row - 64 ? gr[j] : 0.f;
         }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
@@ -313,7 +405,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         float t8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-            t8[e] = Nm[kk * LDS + 8 * cc + e] * bs[8 * cc + e];
+            t8[e] = (cc >> 1) > (kk >> 4) ? 0.f : Nm[kk * LDS + 8 * cc + e] * bs[8 * cc + e];
         *reinterpret_cast<uint4 *>(tt + kk * 128 + ((cc ^ (kk & 7)) << 4)) = pack8(t8);
     }
     __syncthreads(); // A and N are done: their space takes the V tile
@@ -417,14 +509,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         for (int pass = 0; pass < (both ? 1 : 2); ++pass) {
             const bool mine = both || ((row >= 64) == (pass == 1));
             if (mine) {
+                // [d_v/4][64][4]: a warp's 16-byte stores are consecutive
+                float *base = uy + ((both && row >= 64) ? 64 * d_v : 0) + 4 * (row & 63);
                 for (int c0 = 16 * half; c0 < d_v; c0 += 32) {
                     float w[16];
                     tmem_ld16(tm + lb + (uint32_t)(Dp + c0), w);
                     tmem_ld_wait();
-                    float *dst = uy + (size_t)(both ? row : (row & 63)) * d_v + c0;
 #pragma unroll
                     for (int e = 0; e < 16; e += 4)
-                        *reinterpret_cast<float4 *>(dst + e) = make_float4(w[e], w[e + 1], w[e + 2], w[e + 3]);
+                        *reinterpret_cast<float4 *>(base + 256 * ((c0 + e) >> 2)) =
+                            make_float4(w[e], w[e + 1], w[e + 2], w[e + 3]);
                 }
             }
             fence_async_smem();
@@ -457,17 +551,6 @@ teardown:
 // value channels (64-column blocks `blk` bytes apart).
 FW_DEV uint32_t vtile_chunk(int row, int j0, uint32_t blk) {
     return (uint32_t)(j0 >> 6) * blk + (uint32_t)row * 128u + ((uint32_t)(((j0 & 63) >> 3) ^ (row & 7)) << 4);
-}
-
-FW_DEV void load16_f32(const float *src, float *dst) {
-#pragma unroll
-    for (int j = 0; j < 16; j += 4) {
-        const float4 f = __ldg(reinterpret_cast<const float4 *>(src + j));
-        dst[j] = f.x;
-        dst[j + 1] = f.y;
-        dst[j + 2] = f.z;
-        dst[j + 3] = f.w;
-    }
 }
 
 // One CTA walks the chunks of one (batch, head) for DVB value channels.
@@ -565,11 +648,16 @@ __global__ void __launch_bounds__(kScanThreads)
         const uint8_t *rec = rec0 + (size_t)c * rc.bytes;
         // U' (rows 0..63, threads 0..63) or Y' (threads 64..127) of this chunk
         float pre[DVB];
-        {
-            const float *src = (const float *)(rec + (tid < 64 ? rc.up : rc.yp)) + (size_t)(tid & 63) * d_v + v0;
+        {   // [d_v/4][64][4]: each 16-byte load of a warp is one 512-byte run
+            const float *src = (const float *)(rec + (tid < 64 ? rc.up : rc.yp)) + 4 * (tid & 63) + 64 * v0;
 #pragma unroll
-            for (int j0 = 0; j0 < DVB; j0 += 16)
-                load16_f32(src + j0, pre + j0);
+            for (int j = 0; j < DVB; j += 4) {
+                const float4 f = __ldg(reinterpret_cast<const float4 *>(src + 64 * j));
+                pre[j] = f.x;
+                pre[j + 1] = f.y;
+                pre[j + 2] = f.z;
+                pre[j + 3] = f.w;
+            }
         }
         bool ok = mbar_wait(bar_a, (uint32_t)(c & 1), status);
         if (__syncthreads_or(!ok))

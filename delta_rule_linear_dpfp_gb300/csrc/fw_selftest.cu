@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(const float *A, cons
                                                             int K, int a_mn, int b_mn, int swap,
                                                             unsigned *status) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u); // stays a shared pointer
     uint8_t *ta = smem;
     uint8_t *tb = smem + kRegionA;
     uint64_t *bar = (uint64_t *)(smem + kRegionA + kRegionB);
