@@ -16,7 +16,7 @@
 // static and the roll costs 8 warp shuffles per block.  The products are
 // summed (reduced over the G lanes with xor shuffles), scaled by one
 // reciprocal of (sum + eps) per row and written 8 per lane with 16-byte
-// stores; for nu <= 4 they stay in registers between the two steps, beyond
+// stores; for nu <= 3 they stay in registers between the two steps, beyond
 // that they are recomputed.
 #include "fw_dpfp.cuh"
 
@@ -27,29 +27,79 @@ namespace {
 // Products of up to NUC blocks stay in registers between the sum and the
 // output (dpfp_row_emit); larger nu recomputes them.
 constexpr int NUC = 3;
+constexpr int kBlocksPerSM = 4; // resident CTAs of 256 threads (__launch_bounds__ below)
 
+// The 8 raw input values behind one lane's entries of x, as loaded (the
+// load is issued one row ahead of its use, so only the registers travel).
+template <typename T> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
+    uint4 u;
+    FW_DEV void load(const __nv_bfloat16 *p, bool valid) {
+        u = valid ? __ldg(reinterpret_cast<const uint4 *>(p)) : make_uint4(0, 0, 0, 0);
+    }
+    FW_DEV void widen(float (&o)[8]) const {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            o[2 * i] = __uint_as_float(w[i] << 16);
+            o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+template <> struct Raw8<float> {
+    float4 a, b;
+    FW_DEV void load(const float *p, bool valid) {
+        a = valid ? __ldg(reinterpret_cast<const float4 *>(p)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        b = valid ? __ldg(reinterpret_cast<const float4 *>(p) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    FW_DEV void widen(float (&o)[8]) const {
+        o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+        o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+    }
+};
+
+// A persistent grid (kBlocksPerSM CTAs per SM, one wave): each warp walks
+// its rows RPW at a time with a grid stride, and the next rows' input is
+// loaded before the current rows are worked on, so the load latency is paid
+// once per warp rather than once per row.
 template <int DK, typename Tin, typename Tout>
-__global__ void __launch_bounds__(256, 4) dpfp_kernel(const Tin *__restrict__ xin, Tout *__restrict__ out,
-                                                   int64_t rows, int nu, float eps) {
+__global__ void __launch_bounds__(256, kBlocksPerSM) dpfp_kernel(const Tin *__restrict__ xin, Tout *__restrict__ out,
+                                                              int64_t rows, int nu, float eps) {
     constexpr int G = DK / 4;         // lanes per row
     constexpr int RPW = 32 / G;       // rows per warp
     constexpr int N = 2 * DK;         // length of [k, -k]
     const int lane = threadIdx.x & 31;
     const int g = lane % G;
     const int base_lane = lane - g;
+    const bool neg = g >= G / 2;      // lanes of the second half hold ReLU(-k)
+    const int koff = 8 * (g % (G / 2));
     const int64_t d_dot = (int64_t)N * nu;
     const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
     int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    Raw8<Tin> cur;
+    {
+        const int64_t row = wid * RPW + lane / G;
+        cur.load(xin + (row < rows ? row : 0) * DK + koff, row < rows);
+    }
     for (; wid * RPW < rows; wid += warps_total) {
         const int64_t row = wid * RPW + lane / G;
         const bool valid = row < rows;
+        Raw8<Tin> nxt;
+        {
+            const int64_t nrow = row + warps_total * RPW;
+            nxt.load(xin + (nrow < rows ? nrow : 0) * DK + koff, nrow < rows);
+        }
         float x[8];
-        dpfp_load_x<G>(xin + (valid ? row : 0) * DK, g, valid, x);
+        cur.widen(x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            x[e] = fmaxf(neg ? -x[e] : x[e], 0.f);
         Tout *orow = out + row * d_dot + 8 * g;
         dpfp_row_emit<G, NUC>(x, g, base_lane, nu, eps, [&](int i, float (&p)[8]) {
             if (valid)
                 store8(orow + (int64_t)(i - 1) * N, p);
         });
+        cur = nxt;
     }
 }
 
@@ -59,7 +109,7 @@ cudaError_t launch_dpfp_t(const void *x, void *phi, int64_t rows, int nu, float 
     constexpr int RPW = 32 / (DK / 4);
     const int64_t warps = (rows + RPW - 1) / RPW;
     int64_t blocks = (warps + 7) / 8;
-    const int64_t cap = (int64_t)num_sms * 16;
+    const int64_t cap = (int64_t)num_sms * kBlocksPerSM;
     if (blocks > cap)
         blocks = cap;
     dpfp_kernel<DK, Tin, Tout><<<(unsigned)blocks, 256, 0, stream>>>(

@@ -103,14 +103,21 @@ FW_DEV uint32_t tmem_cols_pow2(int need) {
 }
 
 // ---------------------------------------------------------------------------
+// Element offset helpers of the T operand tile (rows k, columns n; MN-major,
+// 128-byte rows, 16-byte chunks swizzled by k & 7).
+FW_DEV uint32_t ttile_chunk(int kk, int n) { return (uint32_t)kk * 128u + ((uint32_t)((n >> 3) ^ (kk & 7)) << 4); }
+
 // (I + A)^-1 for a strictly lower 64 x 64 A, by 16 x 16 blocks:
 //   diagonal blocks by forward substitution (one column per thread), then
 //   block row I: N_IJ = -N_II * sum_{K=J}^{I-1} A_IK N_KJ   (J < I).
 // A, N: [64][LDS]; R: [16][LDS] scratch; all 16-byte aligned.  Only the
 // blocks on and below the diagonal of N are written (the ones above are
-// zero and never read here).  NT threads; ends synchronised.
+// zero and never read here).  As each block of N is final it also goes out,
+// times beta of its column, in bf16 to the T operand tile tt (T = N diag(beta));
+// the blocks above the diagonal are written as zeros.  NT threads (>= 256);
+// ends synchronised.
 template <int NT>
-FW_DEV void unit_lower_inverse(const float *A, float *N, float *R, int tid) {
+FW_DEV void unit_lower_inverse(const float *A, float *N, float *R, const float *bs, uint8_t *tt, int tid) {
     if (tid < 64) {
         const int o = 16 * (tid >> 4), j = tid & 15;
         float col[16];
@@ -122,9 +129,19 @@ FW_DEV void unit_lower_inverse(const float *A, float *N, float *R, int tid) {
                 acc = fmaf(-A[(o + i) * LDS + o + s], col[s], acc);
             col[i] = acc;
         }
+        const float bj = bs[o + j];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < 16; ++i) {
             N[(o + i) * LDS + o + j] = col[i];
+            *reinterpret_cast<__nv_bfloat16 *>(tt + ttile_chunk(o + i, o + j) + 2 * (j & 7)) =
+                __float2bfloat16_rn(col[i] * bj);
+        }
+    } else if (tid < 64 + 192) { // zero chunks of the 6 blocks above the diagonal
+        const int idx = tid - 64, blk = idx >> 5;
+        const int I = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        const int kk = 16 * I + ((idx & 31) >> 1), n0 = 16 * J + 8 * (idx & 1);
+        *reinterpret_cast<uint4 *>(tt + ttile_chunk(kk, n0)) = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
     // off-diagonal blocks; each thread computes 4 adjacent outputs of a row
@@ -169,8 +186,12 @@ FW_DEV void unit_lower_inverse(const float *A, float *N, float *R, int tid) {
                     acc.w = fmaf(nv[e], r.w, acc.w);
                 }
             }
-            *reinterpret_cast<float4 *>(N + (16 * I + ii) * LDS + j0) =
-                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            const int kk = 16 * I + ii;
+            *reinterpret_cast<float4 *>(N + kk * LDS + j0) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            uint2 t4;
+            t4.x = pack_bf16x2(-acc.x * bs[j0], -acc.y * bs[j0 + 1]);
+            t4.y = pack_bf16x2(-acc.z * bs[j0 + 2], -acc.w * bs[j0 + 3]);
+            *reinterpret_cast<uint2 *>(tt + ttile_chunk(kk, j0) + 2 * (j0 & 7)) = t4;
         }
         __syncthreads();
     }
@@ -354,8 +375,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     const uint32_t tm = *slot;
     const uint32_t lb = tmem_lane_base(warp);
 
-    // MMA: [K; Q] K^T  (B = the first 64 rows of the same tile)
+    // MMA: [K; Q] K^T  (B = the first 64 rows of the same tile).  The key
+    // rows of the tile are final here and go out as the record's K image
+    // (bulk copies of the 64-row halves of each 64-column block) while the
+    // rest of the chunk is worked out.
     if (tid == 0) {
+        for (int kb = 0; kb < Dp / 64; ++kb)
+            bulk_s2g(rec + rc.k + (size_t)kb * 8192, kq + (size_t)kb * 16384, 8192);
+        bulk_commit();
         const uint32_t idesc = idesc_bf16(128, 64, 0, 0);
         const uint32_t base = smem_u32(kq);
         for (int s = 0; s < Dp / 16; ++s) {
@@ -398,17 +425,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     tc_fence_before();
     __syncthreads();
 
-    unit_lower_inverse<kPrepThreads>(Am, Nm, Rm, tid);
-    // T = (I + A)^-1 diag(beta) -> MN-major operand (rows k, columns n)
-    for (int idx = tid; idx < 64 * 8; idx += kPrepThreads) {
-        const int kk = idx >> 3, cc = idx & 7;
-        float t8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            t8[e] = (cc >> 1) > (kk >> 4) ? 0.f : Nm[kk * LDS + 8 * cc + e] * bs[8 * cc + e];
-        *reinterpret_cast<uint4 *>(tt + kk * 128 + ((cc ^ (kk & 7)) << 4)) = pack8(t8);
-    }
-    __syncthreads(); // A and N are done: their space takes the V tile
+    // (I + A)^-1, and T = (I + A)^-1 diag(beta) as the MN-major operand tile
+    // (rows k, columns n); ends synchronised, so A and N's space is free for V
+    unit_lower_inverse<kPrepThreads>(Am, Nm, Rm, bs, tt, tid);
 #pragma unroll
     for (int i = 0; i < kVChunks; ++i) {
         const int idx = tid + i * kPrepThreads, t = idx / vcpr, j = 8 * (idx % vcpr);
@@ -462,22 +481,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
             mma_bf16(tm + (uint32_t)Dp, ad, desc_sw128(bv + (uint32_t)s * 2048u, 8192, 1024), idv, s > 0);
         }
         mma_commit(bar);
+        bulk_wait_read(); // the K image has been read out of the key rows
     }
     ok = mbar_wait(bar, 0, status);
     tc_fence_after();
     if (__syncthreads_or(!ok))
         goto teardown;
-    // Record out.  1) the key rows of the [K; Q] tile go out as the K image
-    // (bulk copies of the 64-row halves of each 64-column block);
-    if (tid == 0) {
-        for (int kb = 0; kb < Dp / 64; ++kb)
-            bulk_s2g(rec + rc.k + (size_t)kb * 8192, kq + (size_t)kb * 16384, 8192);
-        bulk_commit();
-        bulk_wait_read();
-    }
-    __syncthreads();
-    // 2) W' replaces the key rows and Q' = Q - P W' the query rows of the
-    //    tile in place;
+    // Record out.  W' replaces the key rows and Q' = Q - P W' the query rows
+    // of the [K; Q] tile in place (the K image's bulk read of the key rows
+    // finished before the barrier above); the tile goes out as one bulk copy.
     for (int c0 = 32 * half; c0 < Dp; c0 += 64) { // 32 columns per pass (Dp % 64 == 0)
         float w[32];
         tmem_ld16(tm + lb + (uint32_t)c0, w);
@@ -498,47 +510,27 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     }
     fence_async_smem();
     __syncthreads();
-    if (tid == 0)
-        bulk_s2g(rec + rc.a, kq, 256u * (uint32_t)Dp); // 3) the [W'; Q'] tile goes out
-    // 4) U' (rows < 64) and Y' (rows >= 64) in fp32 through the freed space
-    //    from the [I; P] tile on (62 KB): both at once when they fit, else U'
-    //    then Y'.
+    if (tid == 0) {
+        bulk_s2g(rec + rc.a, kq, 256u * (uint32_t)Dp);
+        bulk_commit();
+    }
+    // U' (rows < 64) and Y' (rows >= 64) go straight from registers to the
+    // record in fp32 as [d_v/4][64][4], so a warp's 16-byte stores are one
+    // contiguous run
     {
-        float *uy = (float *)ip;
-        const bool both = 128 * d_v * 4 <= (int)((uint8_t *)bs - ip);
-        for (int pass = 0; pass < (both ? 1 : 2); ++pass) {
-            const bool mine = both || ((row >= 64) == (pass == 1));
-            if (mine) {
-                // [d_v/4][64][4]: a warp's 16-byte stores are consecutive
-                float *base = uy + ((both && row >= 64) ? 64 * d_v : 0) + 4 * (row & 63);
-                for (int c0 = 16 * half; c0 < d_v; c0 += 32) {
-                    float w[16];
-                    tmem_ld16(tm + lb + (uint32_t)(Dp + c0), w);
-                    tmem_ld_wait();
+        float *uy = reinterpret_cast<float *>(rec + (row < 64 ? rc.up : rc.yp)) + 4 * (row & 63);
+        for (int c0 = 16 * half; c0 < d_v; c0 += 32) {
+            float w[16];
+            tmem_ld16(tm + lb + (uint32_t)(Dp + c0), w);
+            tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 16; e += 4)
-                        *reinterpret_cast<float4 *>(base + 256 * ((c0 + e) >> 2)) =
-                            make_float4(w[e], w[e + 1], w[e + 2], w[e + 3]);
-                }
-            }
-            fence_async_smem();
-            __syncthreads();
-            if (tid == 0) {
-                if (both) {
-                    bulk_s2g(rec + rc.up, uy, 256u * (uint32_t)d_v);
-                    bulk_s2g(rec + rc.yp, uy + 64 * d_v, 256u * (uint32_t)d_v);
-                } else {
-                    bulk_s2g(rec + (pass ? rc.yp : rc.up), uy, 256u * (uint32_t)d_v);
-                }
-                bulk_commit();
-                bulk_wait_read(); // the staging space may be reused / released
-            }
-            __syncthreads();
+            for (int e = 0; e < 16; e += 4)
+                *reinterpret_cast<float4 *>(uy + 256 * ((c0 + e) >> 2)) = make_float4(w[e], w[e + 1], w[e + 2], w[e + 3]);
         }
     }
 teardown:
     if (tid == 0)
-        bulk_wait_all(); // the record is in global memory before the CTA retires
+        bulk_wait_all(); // the bulk copies are done before the CTA retires
     tc_fence_before();
     __syncthreads();
     if (warp == 0)
