@@ -70,6 +70,33 @@ FW_DEV void store8(__nv_bfloat16 *p, const float (&v)[8]) {
     *reinterpret_cast<uint4 *>(p) = u;
 }
 
+// -------------------------------------------- programmatic dependent launch
+// The next kernel on the stream may start launching (it still waits in
+// griddep_wait before touching what this kernel writes).
+FW_DEV void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Block until the preceding kernel on the stream has completed and its memory
+// operations are visible (returns at once when the launch did not overlap).
+FW_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch with programmatic stream serialization: the kernel's CTAs may be
+// scheduled while the preceding kernel on the stream finishes, so the launch
+// latency is hidden behind its tail.  Every kernel launched this way calls
+// griddep_wait before its first global access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 FW_DEV float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)

@@ -57,6 +57,8 @@ __global__ void __launch_bounds__(256)
         }
     };
 
+    griddep_launch_dependents();
+    griddep_wait(); // q, k, v, beta or W may be the preceding kernel's output
     float4 cur[NQ];
     load_row(0, cur); // first row in flight while phi is built
 
@@ -157,16 +159,14 @@ cudaError_t launch_decode_t(const void *q, const void *k, const void *v, const v
             *bb = static_cast<const T *>(beta);
     T *yy = static_cast<T *>(y);
     if (d_dot <= 128)
-        decode_kernel<DK, T, 1><<<grid, 256, 0, st>>>(qq, kk, vv, bb, W, yy, nu, d_v, eps);
+        return launch_pdl(decode_kernel<DK, T, 1>, grid, dim3(256), 0, st, qq, kk, vv, bb, W, yy, nu, d_v, eps);
     else if (d_dot <= 256)
-        decode_kernel<DK, T, 2><<<grid, 256, 0, st>>>(qq, kk, vv, bb, W, yy, nu, d_v, eps);
+        return launch_pdl(decode_kernel<DK, T, 2>, grid, dim3(256), 0, st, qq, kk, vv, bb, W, yy, nu, d_v, eps);
     else if (d_dot <= 512)
-        decode_kernel<DK, T, 4><<<grid, 256, 0, st>>>(qq, kk, vv, bb, W, yy, nu, d_v, eps);
+        return launch_pdl(decode_kernel<DK, T, 4>, grid, dim3(256), 0, st, qq, kk, vv, bb, W, yy, nu, d_v, eps);
     else if (d_dot <= 1024)
-        decode_kernel<DK, T, 8><<<grid, 256, 0, st>>>(qq, kk, vv, bb, W, yy, nu, d_v, eps);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+        return launch_pdl(decode_kernel<DK, T, 8>, grid, dim3(256), 0, st, qq, kk, vv, bb, W, yy, nu, d_v, eps);
+    return cudaErrorInvalidValue;
 }
 
 template <typename T>

@@ -61,7 +61,8 @@ template <> struct Raw8<float> {
 // A persistent grid (kBlocksPerSM CTAs per SM, one wave): each warp walks
 // its rows RPW at a time with a grid stride, and the next rows' input is
 // loaded before the current rows are worked on, so the load latency is paid
-// once per warp rather than once per row.
+// once per warp rather than once per row.  Launched with programmatic
+// dependent launch (its set-up overlaps the tail of the preceding kernel).
 template <int DK, typename Tin, typename Tout>
 __global__ void __launch_bounds__(256, kBlocksPerSM) dpfp_kernel(const Tin *__restrict__ xin, Tout *__restrict__ out,
                                                               int64_t rows, int nu, float eps) {
@@ -76,6 +77,8 @@ __global__ void __launch_bounds__(256, kBlocksPerSM) dpfp_kernel(const Tin *__re
     const int64_t d_dot = (int64_t)N * nu;
     const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
     int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    griddep_launch_dependents();
+    griddep_wait(); // x may be the preceding kernel's output
     Raw8<Tin> cur;
     {
         const int64_t row = wid * RPW + lane / G;
@@ -112,9 +115,8 @@ cudaError_t launch_dpfp_t(const void *x, void *phi, int64_t rows, int nu, float 
     const int64_t cap = (int64_t)num_sms * kBlocksPerSM;
     if (blocks > cap)
         blocks = cap;
-    dpfp_kernel<DK, Tin, Tout><<<(unsigned)blocks, 256, 0, stream>>>(
-        static_cast<const Tin *>(x), static_cast<Tout *>(phi), rows, nu, eps);
-    return cudaGetLastError();
+    return launch_pdl(dpfp_kernel<DK, Tin, Tout>, dim3((unsigned)blocks), dim3(256), 0, stream,
+                      static_cast<const Tin *>(x), static_cast<Tout *>(phi), rows, nu, eps);
 }
 
 template <int DK>

@@ -288,6 +288,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     const uint32_t ncols = tmem_cols_pow2(max(64, Dp + d_v));
 
     griddep_launch_dependents(); // the scan may start its prologue on free SMs
+    griddep_wait(); // the inputs may be, and the workspace may still be read by, the preceding kernel
     // Global loads first, all in flight before any is used: the key and query
     // rows for the DPFP, the chunk's V rows (kept in registers until their
     // tile's space is free) and beta (stored to shared memory after the DPFP).
@@ -618,6 +619,8 @@ __global__ void __launch_bounds__(kScanThreads)
     if (has_w0)
         tmem_st_wait();
     // the workspace records are the prep kernel's: wait for it to complete
+    // (and let the next kernel on the stream start its set-up meanwhile)
+    griddep_launch_dependents();
     griddep_wait();
     if (tid == 0) { // chunk 0's [W'; Q'] and the first K image(s)
         mbar_arrive_expect_tx(bar_a, a_bytes);
@@ -793,11 +796,10 @@ cudaError_t launch_prep(const void *q, const void *k, const void *v, const void 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    kern<<<dim3((unsigned)nch, (unsigned)BH), kPrepThreads, smem, st>>>(
-        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-        static_cast<const __nv_bfloat16 *>(v), static_cast<const __nv_bfloat16 *>(beta), ws, L, C, nch, nu, Dp,
-        d_v, eps, status);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)nch, (unsigned)BH), dim3(kPrepThreads), smem, st,
+                      static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+                      static_cast<const __nv_bfloat16 *>(v), static_cast<const __nv_bfloat16 *>(beta), ws, L, C,
+                      nch, nu, Dp, d_v, eps, status);
 }
 
 template <int DVB, int NKB>

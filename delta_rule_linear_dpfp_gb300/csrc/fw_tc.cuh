@@ -109,13 +109,8 @@ FW_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "me
 // proxy (tensor core, bulk copies) once followed by a CTA barrier.
 FW_DEV void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// -------------------------------------------- programmatic dependent launch
-// The next kernel on the stream may start launching (its CTAs still wait in
-// griddep_wait before touching what this kernel writes).
-FW_DEV void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-// Block until the preceding kernel on the stream has completed and its memory
-// operations are visible (a no-op when the launch did not overlap).
-FW_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// (programmatic dependent launch: griddep_wait / griddep_launch_dependents
+// and launch_pdl live in fw_common.cuh)
 
 // ------------------------------------------------------------------- TMEM
 FW_DEV void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) { // whole warp
