@@ -547,10 +547,12 @@ FW_DEV uint32_t vtile_chunk(int row, int j0, uint32_t blk) {
 }
 
 // One CTA walks the chunks of one (batch, head) for DVB value channels.
-// Everything per thread is done 16 value channels at a time.  NKB = number
+// Everything per thread is done 16 value channels at a time.  NA = number
+// of [W'; Q'] buffers (2: the image of chunk c + 2 is fetched as soon as
+// MMA1 has read chunk c's; 1: chunk c + 1's, into the same buffer).  NKB = number
 // of K buffers (2: K images two chunks ahead; 1: the next K image is
 // fetched as soon as MMA3 has read the current one).
-template <int DVB, int NKB>
+template <int DVB, int NKB, int NA>
 __global__ void __launch_bounds__(kScanThreads)
     chunk_scan_kernel(const float *W0, float *Wf, __nv_bfloat16 *__restrict__ y, const uint8_t *__restrict__ ws,
                       int L, int C, int nch, int d_v, int d_dot, int Dp, unsigned *status) {
@@ -561,15 +563,16 @@ __global__ void __launch_bounds__(kScanThreads)
     const Record rc = record_layout(Dp, d_v);
     const uint32_t a_bytes = 256u * (uint32_t)Dp, k_bytes = 128u * (uint32_t)Dp;
     const uint32_t sblk = 128u * (uint32_t)Dp;       // bytes of one 64-column block of the S tile
-    uint8_t *at = smem;                               // [W'; Q']  128 x Dp
-    uint8_t *kt0 = at + a_bytes;                      // K image(s)
+    uint8_t *at0 = smem;                              // [W'; Q']  128 x Dp (NA buffers)
+    uint8_t *at1 = NA == 2 ? at0 + a_bytes : at0;
+    uint8_t *kt0 = at0 + NA * a_bytes;                // K image(s)
     uint8_t *kt1 = NKB == 2 ? kt0 + k_bytes : kt0;
     uint8_t *st = kt0 + NKB * k_bytes;                // S: rows d, columns v (MN-major)
     uint8_t *ut = st + VB * sblk;                     // U: rows t, columns v (MN-major)
-    uint64_t *bar_a = (uint64_t *)(ut + VB * 8192);
-    uint64_t *bar_k = bar_a + 1;                      // [2]
-    uint64_t *bar_mma = bar_a + 3;
-    uint32_t *slot = (uint32_t *)(bar_a + 4);
+    uint64_t *bar_a = (uint64_t *)(ut + VB * 8192);  // [2]
+    uint64_t *bar_k = bar_a + 2;                      // [2]
+    uint64_t *bar_mma = bar_a + 4;
+    uint32_t *slot = (uint32_t *)(bar_a + 5);
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int v0 = blockIdx.x * DVB;
@@ -582,6 +585,7 @@ __global__ void __launch_bounds__(kScanThreads)
 
     if (tid == 0) {
         mbar_init(bar_a, 1);
+        mbar_init(bar_a + 1, 1);
         mbar_init(bar_k, 1);
         mbar_init(bar_k + 1, 1);
         mbar_init(bar_mma, 1);
@@ -596,7 +600,7 @@ __global__ void __launch_bounds__(kScanThreads)
     tc_fence_after();
     const uint32_t tm = *slot;
     const uint32_t tD1 = tm, tS = tm + DS;
-    const uint32_t at_s = smem_u32(at), st_s = smem_u32(st), ut_s = smem_u32(ut);
+    const uint32_t st_s = smem_u32(st), ut_s = smem_u32(ut);
     const uint32_t kt0_s = smem_u32(kt0), kt1_s = smem_u32(kt1);
 
     // initial state: S^T in TMEM (fp32) and S as the bf16 operand of MMA1.
@@ -624,7 +628,11 @@ __global__ void __launch_bounds__(kScanThreads)
     griddep_wait();
     if (tid == 0) { // chunk 0's [W'; Q'] and the first K image(s)
         mbar_arrive_expect_tx(bar_a, a_bytes);
-        bulk_g2s(at, rec0 + rc.a, a_bytes, bar_a);
+        bulk_g2s(at0, rec0 + rc.a, a_bytes, bar_a);
+        if (NA == 2 && nch > 1) {
+            mbar_arrive_expect_tx(bar_a + 1, a_bytes);
+            bulk_g2s(at1, rec0 + rc.bytes + rc.a, a_bytes, bar_a + 1);
+        }
         mbar_arrive_expect_tx(bar_k, k_bytes);
         bulk_g2s(kt0, rec0 + rc.k, k_bytes, bar_k);
         if (NKB == 2 && nch > 1) {
@@ -638,7 +646,8 @@ __global__ void __launch_bounds__(kScanThreads)
 
     uint32_t mma_phase = 0;
     for (int c = 0; c < nch; ++c) {
-        const int t0 = c * C, Lc = min(C, L - t0), kb = NKB == 2 ? (c & 1) : 0;
+        const int t0 = c * C, Lc = min(C, L - t0), kb = NKB == 2 ? (c & 1) : 0, ab = NA == 2 ? (c & 1) : 0;
+        const uint32_t a_parity = NA == 2 ? (uint32_t)((c >> 1) & 1) : (uint32_t)(c & 1);
         const uint32_t k_parity = NKB == 2 ? (uint32_t)((c >> 1) & 1) : (uint32_t)(c & 1);
         const uint8_t *rec = rec0 + (size_t)c * rc.bytes;
         // U' (rows 0..63, threads 0..63) or Y' (threads 64..127) of this chunk
@@ -654,7 +663,7 @@ __global__ void __launch_bounds__(kScanThreads)
                 pre[j + 3] = f.w;
             }
         }
-        bool ok = mbar_wait(bar_a, (uint32_t)(c & 1), status);
+        bool ok = mbar_wait(bar_a + ab, a_parity, status);
         if (__syncthreads_or(!ok))
             break;
 
@@ -663,7 +672,7 @@ __global__ void __launch_bounds__(kScanThreads)
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(128, DVB, 0, 1);
             for (int s = 0; s < Dp / 16; ++s)
-                mma_bf16(tD1, desc_sw128(at_s + kmajor_step(s, 128), 16, 1024),
+                mma_bf16(tD1, desc_sw128(smem_u32(ab ? at1 : at0) + kmajor_step(s, 128), 16, 1024),
                          desc_sw128(st_s + (uint32_t)s * 2048u, sblk, 1024), idesc, s > 0);
             mma_commit(bar_mma);
         }
@@ -672,9 +681,9 @@ __global__ void __launch_bounds__(kScanThreads)
         if (__syncthreads_or(!ok))
             break;
         tc_fence_after();
-        if (tid == 0 && c + 1 < nch) { // [W'; Q'] consumed: fetch the next chunk's
-            mbar_arrive_expect_tx(bar_a, a_bytes);
-            bulk_g2s(at, rec + rc.bytes + rc.a, a_bytes, bar_a);
+        if (tid == 0 && c + NA < nch) { // this [W'; Q'] buffer is consumed: fetch a later chunk's
+            mbar_arrive_expect_tx(bar_a + ab, a_bytes);
+            bulk_g2s(ab ? at1 : at0, rec + (size_t)NA * rc.bytes + rc.a, a_bytes, bar_a + ab);
         }
         {
             float d1[DVB];
@@ -765,15 +774,15 @@ size_t prep_smem(int Dp, int d_v) {
     return (size_t)256 * Dp + 16384 + 8192 + (2 * 64 + 16) * LDS * 4 + 64 * 4 + 16 + 1024;
 }
 
-size_t scan_smem(int Dp, int dvb, int nkb) {
+size_t scan_smem(int Dp, int dvb, int nkb, int na) {
     const int VB = (dvb + 63) / 64;
-    return (size_t)256 * Dp + (size_t)nkb * 128 * Dp + (size_t)VB * 128 * Dp + (size_t)VB * 8192 + 64 + 1024;
+    return (size_t)na * 256 * Dp + (size_t)nkb * 128 * Dp + (size_t)VB * 128 * Dp + (size_t)VB * 8192 + 64 + 1024;
 }
 
 constexpr size_t kMaxSmem = 227 * 1024;
 
 bool fits(int Dp, int d_v, int dvb) {
-    return Dp <= kMaxDp && Dp + d_v <= 512 && scan_smem(Dp, dvb, 1) <= kMaxSmem && prep_smem(Dp, d_v) <= kMaxSmem;
+    return Dp <= kMaxDp && Dp + d_v <= 512 && scan_smem(Dp, dvb, 1, 1) <= kMaxSmem && prep_smem(Dp, d_v) <= kMaxSmem;
 }
 
 // Value channels per scan CTA.  The walk over the chunks is serial, so the
@@ -784,8 +793,10 @@ bool fits(int Dp, int d_v, int dvb) {
 // (scan 14.4 / 18.5 / 24.5 us and 80 / 96 / 141 us).
 int choose_dvb(int d_v) { return 16 <= d_v ? 16 : d_v; }
 
-// Two K buffers when they fit in shared memory, else one.
-int choose_nkb(int Dp, int dvb) { return scan_smem(Dp, dvb, 2) <= kMaxSmem ? 2 : 1; }
+// Two K buffers when they fit in shared memory, else one; then two [W'; Q']
+// buffers when those fit as well.
+int choose_nkb(int Dp, int dvb) { return scan_smem(Dp, dvb, 2, 1) <= kMaxSmem ? 2 : 1; }
+int choose_na(int Dp, int dvb) { return scan_smem(Dp, dvb, choose_nkb(Dp, dvb), 2) <= kMaxSmem ? 2 : 1; }
 
 template <int DK>
 cudaError_t launch_prep(const void *q, const void *k, const void *v, const void *beta, uint8_t *ws, int BH,
@@ -802,11 +813,11 @@ cudaError_t launch_prep(const void *q, const void *k, const void *v, const void 
                       nch, nu, Dp, d_v, eps, status);
 }
 
-template <int DVB, int NKB>
+template <int DVB, int NKB, int NA>
 cudaError_t launch_scan(const float *W0, float *Wf, void *y, const uint8_t *ws, int BH, int L, int C, int nch,
                         int d_v, int d_dot, int Dp, unsigned *status, cudaStream_t st) {
-    const size_t smem = scan_smem(Dp, DVB, NKB);
-    auto kern = chunk_scan_kernel<DVB, NKB>;
+    const size_t smem = scan_smem(Dp, DVB, NKB, NA);
+    auto kern = chunk_scan_kernel<DVB, NKB, NA>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
@@ -830,9 +841,12 @@ cudaError_t launch_scan(const float *W0, float *Wf, void *y, const uint8_t *ws, 
 template <int DVB>
 cudaError_t launch_scan_nkb(const float *W0, float *Wf, void *y, const uint8_t *ws, int BH, int L, int C, int nch,
                             int d_v, int d_dot, int Dp, unsigned *status, cudaStream_t st) {
-    if (choose_nkb(Dp, DVB) == 2)
-        return launch_scan<DVB, 2>(W0, Wf, y, ws, BH, L, C, nch, d_v, d_dot, Dp, status, st);
-    return launch_scan<DVB, 1>(W0, Wf, y, ws, BH, L, C, nch, d_v, d_dot, Dp, status, st);
+    if (choose_nkb(Dp, DVB) == 2) {
+        if (choose_na(Dp, DVB) == 2)
+            return launch_scan<DVB, 2, 2>(W0, Wf, y, ws, BH, L, C, nch, d_v, d_dot, Dp, status, st);
+        return launch_scan<DVB, 2, 1>(W0, Wf, y, ws, BH, L, C, nch, d_v, d_dot, Dp, status, st);
+    }
+    return launch_scan<DVB, 1, 1>(W0, Wf, y, ws, BH, L, C, nch, d_v, d_dot, Dp, status, st);
 }
 
 } // namespace
