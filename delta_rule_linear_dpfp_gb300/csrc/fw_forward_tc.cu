@@ -644,6 +644,23 @@ __global__ void __launch_bounds__(kScanThreads)
     tc_fence_before();
     __syncthreads();
 
+    // U' (rows 0..63, threads 0..63) or Y' (threads 64..127) of a chunk,
+    // [d_v/4][64][4] in the record: each 16-byte load of a warp is one
+    // 512-byte run.  Chunk c + 1's are loaded as soon as chunk c's are used.
+    float pre[DVB];
+    auto load_pre = [&](int cc) {
+        const float *src =
+            (const float *)(rec0 + (size_t)cc * rc.bytes + (tid < 64 ? rc.up : rc.yp)) + 4 * (tid & 63) + 64 * v0;
+#pragma unroll
+        for (int j = 0; j < DVB; j += 4) {
+            const float4 f = __ldg(reinterpret_cast<const float4 *>(src + 64 * j));
+            pre[j] = f.x;
+            pre[j + 1] = f.y;
+            pre[j + 2] = f.z;
+            pre[j + 3] = f.w;
+        }
+    };
+    load_pre(0);
     uint32_t mma_phase = 0;
     for (int c = 0; c < nch; ++c) {
         const int t0 = c * C, Lc = min(C, L - t0), kb = NKB == 2 ? (c & 1) : 0, ab = NA == 2 ? (c & 1) : 0;
@@ -651,18 +668,6 @@ __global__ void __launch_bounds__(kScanThreads)
         const uint32_t k_parity = NKB == 2 ? (uint32_t)((c >> 1) & 1) : (uint32_t)(c & 1);
         const uint8_t *rec = rec0 + (size_t)c * rc.bytes;
         // U' (rows 0..63, threads 0..63) or Y' (threads 64..127) of this chunk
-        float pre[DVB];
-        {   // [d_v/4][64][4]: each 16-byte load of a warp is one 512-byte run
-            const float *src = (const float *)(rec + (tid < 64 ? rc.up : rc.yp)) + 4 * (tid & 63) + 64 * v0;
-#pragma unroll
-            for (int j = 0; j < DVB; j += 4) {
-                const float4 f = __ldg(reinterpret_cast<const float4 *>(src + 64 * j));
-                pre[j] = f.x;
-                pre[j + 1] = f.y;
-                pre[j + 2] = f.z;
-                pre[j + 3] = f.w;
-            }
-        }
         bool ok = mbar_wait(bar_a + ab, a_parity, status);
         if (__syncthreads_or(!ok))
             break;
@@ -709,6 +714,8 @@ __global__ void __launch_bounds__(kScanThreads)
                 }
             }
         }
+        if (c + 1 < nch)
+            load_pre(c + 1);
         fence_async_smem();
         tc_fence_before();
         ok = mbar_wait(bar_k + kb, k_parity, status);
