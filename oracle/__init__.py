@@ -8,6 +8,8 @@ Contents
   dpfp(x, nu, eps)                  -- the DPFP feature map, plain C, fp64
   delta_forward(q, k, v, beta, ...) -- O1: the sequential recurrence, plain C
   delta_decode_step(...)            -- one token against a persistent W
+  linear_forward(q, k, v, ...)      -- the sum rule (linear attention, with or
+                                       without the z normaliser), plain C
   chunked.delta_forward_chunked     -- O2: the chunked (WY / UT) form in numpy,
                                        for tiny brute-force checks of O1
 
@@ -56,6 +58,9 @@ class OracleLib:
         lib.fwo_delta_decode_step.restype = ctypes.c_int
         lib.fwo_delta_decode_step.argtypes = [_c_double_p] * 6 + [ctypes.c_int64] * 2 + [
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int]
+        lib.fwo_linear_forward.restype = ctypes.c_int
+        lib.fwo_linear_forward.argtypes = [_c_double_p] * 8 + [ctypes.c_int64] * 3 + [
+            ctypes.c_int] * 4 + [ctypes.c_double, ctypes.c_int]
         self._lib = lib
         self.path = path
 
@@ -113,6 +118,32 @@ class OracleLib:
         return y, W
 
 
+    def linear_forward(self, q, k, v, W0=None, z0=None, nu: int = 1, normalize: bool = True,
+                       eps: float = 1e-6, nthreads: int = 1):
+        """The sum rule (linear attention) as a recurrence.
+
+        q, k: [B,H,L,d_key]; v: [B,H,L,d_v]; W0: [B,H,d_v,d_dot] or None;
+        z0: [B,H,d_dot] or None (zeros).  Returns (y [B,H,L,d_v], W_final,
+        z_final) in fp64.
+        """
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, H, L, d_key = q.shape
+        d_v = v.shape[-1]
+        d_dot = 2 * d_key * nu
+        assert k.shape == q.shape and v.shape == (B, H, L, d_v)
+        W0 = None if W0 is None else _f64(W0)
+        z0 = None if z0 is None else _f64(z0)
+        y = np.empty((B, H, L, d_v), dtype=np.float64)
+        W_final = np.empty((B, H, d_v, d_dot), dtype=np.float64)
+        z_final = np.empty((B, H, d_dot), dtype=np.float64)
+        rc = self._lib.fwo_linear_forward(_p(q), _p(k), _p(v), _p(W0), _p(z0), _p(W_final), _p(z_final),
+                                          _p(y), B, H, L, d_key, nu, d_v, int(bool(normalize)), eps,
+                                          int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle linear_forward rejected arguments")
+        return y, W_final, z_final
+
+
 _default = None
 
 
@@ -134,3 +165,8 @@ def delta_forward(q, k, v, beta, W0=None, nu: int = 1, eps: float = 1e-6, nthrea
 
 def delta_decode_step(q, k, v, beta, W, nu: int = 1, eps: float = 1e-6, nthreads: int = 1):
     return lib().delta_decode_step(q, k, v, beta, W, nu, eps, nthreads)
+
+
+def linear_forward(q, k, v, W0=None, z0=None, nu: int = 1, normalize: bool = True, eps: float = 1e-6,
+                   nthreads: int = 1):
+    return lib().linear_forward(q, k, v, W0, z0, nu, normalize, eps, nthreads)

@@ -23,7 +23,14 @@
  *     shape [batch, heads, d_value, d_dot] and phi is applied to query and
  *     key, not to value;
  *   - section "token_wise variant": one token at a time against a W that
- *     persists across calls (the decode step).
+ *     persists across calls (the decode step);
+ *   - section "linear self-attention, the fast form" (the sum rule the
+ *     delta rule replaces): W_i = W_{i-1} + v_i outer phi(k_i),
+ *     z_i = z_{i-1} + phi(k_i), y_i = W_i phi(q_i) / (z_i . phi(q_i)) -- the
+ *     kernel-attention ratio written as a recurrence; the unnormalised form
+ *     drops the division.  The pages give no guard for a zero denominator;
+ *     here y_i = 0 when z_i . phi(q_i) == 0 (then every phi(k_j) . phi(q_i)
+ *     is 0, the numerator too, as all phi >= 0).
  *
  * Every routine below follows those steps in that order, one token at a time,
  * with no blocking, fusion or reordering.
@@ -195,4 +202,114 @@ int fwo_delta_decode_step(const double *q, const double *k, const double *v, con
                           double eps, int nthreads)
 {
     return fwo_delta_forward(q, k, v, beta, W, W, y, B, H, 1, d_key, nu, d_v, eps, nthreads);
+}
+
+/* ---------------------------------------------------------------------- */
+/* The sum rule (linear attention) for one (batch, head) pair.            */
+/*   q, k: [L, d_key]; v, y: [L, d_v]; W: [d_v, d_dot], z: [d_dot] in/out.*/
+/* ---------------------------------------------------------------------- */
+static void linear_one(const double *q, const double *k, const double *v, double *W, double *z,
+                       double *y, int64_t L, int d_key, int nu, int d_v, int normalize, double eps)
+{
+    const int d_dot = 2 * d_key * nu;
+    double *pk = (double *)malloc(sizeof(double) * d_dot);
+    double *pq = (double *)malloc(sizeof(double) * d_dot);
+    double *x = (double *)malloc(sizeof(double) * 2 * d_key);
+    for (int64_t t = 0; t < L; ++t) {
+        dpfp_one(k + t * d_key, pk, x, d_key, nu, eps);
+        dpfp_one(q + t * d_key, pq, x, d_key, nu, eps);
+        /* W_t = W_{t-1} + v_t outer phi(k_t);  z_t = z_{t-1} + phi(k_t) */
+        for (int r = 0; r < d_v; ++r)
+            for (int m = 0; m < d_dot; ++m)
+                W[(size_t)r * d_dot + m] += v[t * d_v + r] * pk[m];
+        for (int m = 0; m < d_dot; ++m)
+            z[m] += pk[m];
+        /* y_t = W_t phi(q_t), divided by z_t . phi(q_t) when normalising */
+        double den = 1.0;
+        if (normalize) {
+            den = 0.0;
+            for (int m = 0; m < d_dot; ++m)
+                den += z[m] * pq[m];
+        }
+        for (int r = 0; r < d_v; ++r) {
+            double acc = 0.0;
+            for (int m = 0; m < d_dot; ++m)
+                acc += W[(size_t)r * d_dot + m] * pq[m];
+            y[t * d_v + r] = den != 0.0 ? acc / den : 0.0;
+        }
+    }
+    free(pk);
+    free(pq);
+    free(x);
+}
+
+typedef struct {
+    const double *q, *k, *v, *W0, *z0;
+    double *W_final, *z_final, *y;
+    int64_t L;
+    int d_key, nu, d_v, normalize;
+    double eps;
+    int64_t first, last;
+} ljob_t;
+
+static void *run_ljob(void *arg)
+{
+    ljob_t *j = (ljob_t *)arg;
+    const int d_dot = 2 * j->d_key * j->nu;
+    const size_t wsz = (size_t)j->d_v * d_dot;
+    double *z = (double *)malloc(sizeof(double) * d_dot);
+    for (int64_t bh = j->first; bh < j->last; ++bh) {
+        double *W = j->W_final + bh * wsz;
+        if (j->W0 && j->W0 + bh * wsz != W)
+            memcpy(W, j->W0 + bh * wsz, sizeof(double) * wsz);
+        else if (!j->W0)
+            memset(W, 0, sizeof(double) * wsz);
+        for (int m = 0; m < d_dot; ++m)
+            z[m] = j->z0 ? j->z0[bh * d_dot + m] : 0.0;
+        linear_one(j->q + bh * j->L * j->d_key, j->k + bh * j->L * j->d_key, j->v + bh * j->L * j->d_v, W, z,
+                   j->y + bh * j->L * j->d_v, j->L, j->d_key, j->nu, j->d_v, j->normalize, j->eps);
+        if (j->z_final)
+            memcpy(j->z_final + bh * d_dot, z, sizeof(double) * d_dot);
+    }
+    free(z);
+    return NULL;
+}
+
+/* The sum rule over [B,H,L,*] inputs: q, k [B,H,L,d_key]; v [B,H,L,d_v];
+ * W0 [B,H,d_v,d_dot] and z0 [B,H,d_dot] or NULL (zeros).  Outputs y
+ * [B,H,L,d_v], W_final (required; may equal W0) and z_final (or NULL).
+ * normalize = 1 divides by z . phi(q), 0 does not. */
+int fwo_linear_forward(const double *q, const double *k, const double *v, const double *W0, const double *z0,
+                       double *W_final, double *z_final, double *y, int64_t B, int64_t H, int64_t L, int d_key,
+                       int nu, int d_v, int normalize, double eps, int nthreads)
+{
+    if (!q || !k || !v || !W_final || !y || B < 0 || H < 0 || L < 0 || d_key <= 0 || d_v <= 0 || nu < 1 ||
+        nu > 2 * d_key - 1 || (normalize != 0 && normalize != 1))
+        return FWO_BAD_ARG;
+    const int64_t BH = B * H;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > BH)
+        nthreads = BH > 0 ? (int)BH : 1;
+    ljob_t *jobs = (ljob_t *)calloc((size_t)nthreads, sizeof(ljob_t));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    for (int i = 0; i < nthreads; ++i) {
+        ljob_t *j = &jobs[i];
+        j->q = q; j->k = k; j->v = v; j->W0 = W0; j->z0 = z0;
+        j->W_final = W_final; j->z_final = z_final; j->y = y; j->L = L;
+        j->d_key = d_key; j->nu = nu; j->d_v = d_v; j->normalize = normalize; j->eps = eps;
+        j->first = BH * i / nthreads;
+        j->last = BH * (i + 1) / nthreads;
+    }
+    if (nthreads == 1) {
+        run_ljob(&jobs[0]);
+    } else {
+        for (int i = 0; i < nthreads; ++i)
+            pthread_create(&tids[i], NULL, run_ljob, &jobs[i]);
+        for (int i = 0; i < nthreads; ++i)
+            pthread_join(tids[i], NULL);
+    }
+    free(jobs);
+    free(tids);
+    return FWO_OK;
 }

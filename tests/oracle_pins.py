@@ -251,9 +251,79 @@ def pin_decode_stepped_equals_forward(o):
     assert np.allclose(Ws, W, rtol=1e-13, atol=1e-15)
 
 
+# ------------------------------------------------- sum rule (linear attention)
+def _attention_form(o, q, k, v, W0, z0, nu, normalize):
+    """The kernel-attention form the sum rule is the recurrence of (the
+    guide's linear self-attention section): with weights
+    w_ij = phi(k_j) . phi(q_i) for j <= i,
+    num_i = W0 phi(q_i) + sum_j v_j w_ij,  den_i = z0 . phi(q_i) + sum_j w_ij.
+    Built from the DPFP map and plain matrix products, all L^2 weights at once."""
+    pq, pk = o.dpfp(q, nu, 1e-6), o.dpfp(k, nu, 1e-6)       # [B,H,L,d_dot]
+    L = q.shape[2]
+    w = np.einsum("bhid,bhjd->bhij", pq, pk) * np.tril(np.ones((L, L)))
+    num = np.einsum("bhij,bhjv->bhiv", w, v) + np.einsum("bhvd,bhid->bhiv", W0, pq)
+    den = w.sum(-1) + np.einsum("bhd,bhid->bhi", z0, pq)
+    y = num / den[..., None] if normalize else num
+    W = W0 + np.einsum("bhjv,bhjd->bhvd", v, pk)
+    z = z0 + pk.sum(2)
+    return y, W, z
+
+
+def pin_linear_attention_form(o):
+    """The sum-rule recurrence equals its kernel-attention form (the ratio of
+    weighted sums over all earlier tokens), normalised or not, with an
+    initial state carried in."""
+    rng = _rng(20)
+    for normalize in (True, False):
+        B, H, L, d_key, nu, d_v = 2, 3, 9, 4, 2, 3
+        q, k, v = (rng.standard_normal((B, H, L, n)) for n in (d_key, d_key, d_v))
+        d_dot = 2 * d_key * nu
+        W0 = rng.standard_normal((B, H, d_v, d_dot))
+        z0 = np.abs(rng.standard_normal((B, H, d_dot))) + 0.1    # a running sum of phi >= 0
+        y1, W1, z1 = o.linear_forward(q, k, v, W0, z0, nu, normalize, 1e-6)
+        y2, W2, z2 = _attention_form(o, q, k, v, W0, z0, nu, normalize)
+        assert np.allclose(y1, y2, rtol=1e-11, atol=1e-13), (normalize, np.abs(y1 - y2).max())
+        assert np.allclose(W1, W2, rtol=1e-12, atol=1e-13)
+        assert np.allclose(z1, z2, rtol=1e-12, atol=1e-13)
+
+
+def pin_linear_first_token_and_convexity(o):
+    """Normalised, from a zero state: the first output is v_1 itself (the
+    single weight cancels), and every output is a convex combination of the
+    values so far, so it stays inside their range channel by channel."""
+    rng = _rng(21)
+    B, H, L, d_key, nu, d_v = 2, 2, 12, 5, 2, 4
+    k = rng.standard_normal((B, H, L, d_key))
+    q = k + 0.3 * rng.standard_normal((B, H, L, d_key))
+    q[:, :, 0] = k[:, :, 0]                                       # phi(q_1) . phi(k_1) > 0
+    v = rng.standard_normal((B, H, L, d_v))
+    y, _, _ = o.linear_forward(q, k, v, None, None, nu, True, 1e-6)
+    assert np.allclose(y[:, :, 0], v[:, :, 0], rtol=1e-12, atol=1e-14)
+    for t in range(L):
+        lo, hi = v[:, :, : t + 1].min(2), v[:, :, : t + 1].max(2)
+        assert np.all(y[:, :, t] >= lo - 1e-12) and np.all(y[:, :, t] <= hi + 1e-12), t
+
+
+def pin_linear_zero_denominator(o):
+    """A query with phi(q) = 0 (q = 0) has a zero denominator: its output is
+    0 (the reading taken where the pages give no guard), never NaN; the
+    unnormalised output is 0 as well, and the state is unaffected by q."""
+    rng = _rng(22)
+    q = rng.standard_normal((1, 1, 4, 3))
+    k = rng.standard_normal((1, 1, 4, 3))
+    v = rng.standard_normal((1, 1, 4, 2))
+    q[:, :, 2] = 0.0
+    for normalize in (True, False):
+        y, W, z = o.linear_forward(q, k, v, None, None, 1, normalize, 1e-6)
+        assert np.all(np.isfinite(y)) and np.all(y[:, :, 2] == 0.0)
+        _, W2, z2 = o.linear_forward(rng.standard_normal(q.shape), k, v, None, None, 1, normalize, 1e-6)
+        assert np.array_equal(W, W2) and np.array_equal(z, z2)
+
+
 ALL_PINS = [
     pin_dpfp_hand, pin_dpfp_block_sums_fft, pin_dpfp_invariants, pin_dpfp_sparsity_and_gram,
     pin_recurrence_hand, pin_beta_zero, pin_one_step_closed_form, pin_linearity,
     pin_value_channel_permutation, pin_contraction_bound, pin_one_hot_recall,
-    pin_decode_stepped_equals_forward,
+    pin_decode_stepped_equals_forward, pin_linear_attention_form, pin_linear_first_token_and_convexity,
+    pin_linear_zero_denominator,
 ]

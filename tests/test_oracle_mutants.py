@@ -36,6 +36,14 @@ MUTANTS = {
                               "memset(W, 0, sizeof(double) * wsz);"),
     "state_transposed": ("W[(size_t)r * d_dot + m] += u * pk[m];",
                          "W[(size_t)m * d_v + r] += u * pk[m];"),
+    # the sum rule (linear attention)
+    "sum_rule_writes_query": ("W[(size_t)r * d_dot + m] += v[t * d_v + r] * pk[m];",
+                              "W[(size_t)r * d_dot + m] += v[t * d_v + r] * pq[m];"),
+    "sum_rule_z_not_accumulated": ("z[m] += pk[m];", "z[m] = pk[m];"),
+    "sum_rule_denominator_with_key": ("den += z[m] * pq[m];", "den += z[m] * pk[m];"),
+    "sum_rule_read_before_write": ("        for (int m = 0; m < d_dot; ++m)\n            z[m] += pk[m];\n",
+                                   "        for (int m = 0; m < d_dot; ++m)\n            z[m] += 0.0 * pk[m];\n"),
+    "sum_rule_initial_z_ignored": ("z[m] = j->z0 ? j->z0[bh * d_dot + m] : 0.0;", "z[m] = 0.0;"),
 }
 
 
