@@ -26,7 +26,7 @@ FW_DTYPE_BF16 = 1
 EXPORTS = ("fw_status_string", "fw_dpfp", "fw_delta_forward_workspace_size", "fw_delta_forward",
            "fw_delta_decode_step", "fw_device_status", "fw_selftest_umma",
            "fw_delta_forward_noalloc", "fw_delta_forward_prepare", "fw_delta_forward_scan",
-           "fw_selftest_wait_timeout")
+           "fw_selftest_wait_timeout", "fw_linear_forward_workspace_size", "fw_linear_forward")
 
 #: bytes of the library's own scratch array behind fw_delta_forward_noalloc
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -75,6 +75,10 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.fw_delta_forward_noalloc.argtypes = [vp] * 7 + [i32] * 8 + [f32, vp]
     lib.fw_selftest_wait_timeout.restype = i32
     lib.fw_selftest_wait_timeout.argtypes = [i32, vp]
+    lib.fw_linear_forward_workspace_size.restype = sz
+    lib.fw_linear_forward_workspace_size.argtypes = [i32] * 9
+    lib.fw_linear_forward.restype = i32
+    lib.fw_linear_forward.argtypes = [vp] * 9 + [sz] + [i32] * 9 + [f32, vp]
     lib.fw_selftest_umma.restype = i32
     lib.fw_selftest_umma.argtypes = [vp, vp, vp] + [i32] * 5 + [vp]
     if path is None:
@@ -198,6 +202,50 @@ def fw_delta_forward_scan(workspace, y, W0=None, W_final=None, nu: int = 1, chun
                                       _stream(stream))
     _check(rc, "fw_delta_forward_scan")
     return y, W_final
+
+
+def fw_linear_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk, normalize=True,
+                                     io_dtype=torch.bfloat16) -> int:
+    code = io_dtype if isinstance(io_dtype, int) else _dtype_code(io_dtype)
+    return int(load().fw_linear_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk, int(bool(normalize)),
+                                                       code))
+
+
+def fw_linear_forward(q, k, v, W0=None, z0=None, nu: int = 1, normalize: bool = True, chunk: int = 64,
+                      eps: float = 1e-6, return_state: bool = True, y=None, W_final=None, z_final=None,
+                      workspace=None, stream=None):
+    """The sum rule (linear attention) over [B,H,L,*] bf16 inputs.
+    Returns (y, W_final or None, z_final or None)."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _dev(t, name)
+    B, H, L, d_key = q.shape
+    d_v = v.shape[-1]
+    d_dot = 2 * d_key * nu
+    if k.shape != q.shape or v.shape != (B, H, L, d_v):
+        raise ValueError("shape mismatch among q, k, v")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share the I/O dtype")
+    for name, t, shape in (("W0", W0, (B, H, d_v, d_dot)), ("z0", z0, (B, H, d_dot))):
+        if t is not None:
+            _dev(t, name)
+            if t.dtype != torch.float32 or tuple(t.shape) != shape:
+                raise ValueError(f"{name} must be fp32 {list(shape)}")
+    if y is None:
+        y = torch.empty(B, H, L, d_v, dtype=q.dtype, device=q.device)
+    if W_final is None and return_state:
+        W_final = torch.empty(B, H, d_v, d_dot, dtype=torch.float32, device=q.device)
+    if z_final is None and return_state and normalize:
+        z_final = torch.empty(B, H, d_dot, dtype=torch.float32, device=q.device)
+    code = _dtype_code(q.dtype)
+    need = fw_linear_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk, normalize, code)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().fw_linear_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(W0), _ptr(z0), _ptr(W_final), _ptr(z_final),
+                                  _ptr(y), _ptr(workspace), ws_bytes, B, H, L, d_key, nu, d_v, chunk,
+                                  int(bool(normalize)), code, eps, _stream(stream))
+    _check(rc, "fw_linear_forward")
+    return y, W_final, z_final
 
 
 def fw_delta_forward_noalloc(q, k, v, beta, W0=None, nu: int = 1, chunk: int = 64,

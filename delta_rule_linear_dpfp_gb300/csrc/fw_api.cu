@@ -193,6 +193,76 @@ FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const v
 
 namespace {
 
+int check_linear_shape(int B, int H, int L, int d_key, int nu, int d_v, int chunk, int normalize, int io_dtype) {
+    if (B < 0 || H < 0 || L < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 ||
+        !dtype_ok(io_dtype) || !(chunk == 16 || chunk == 32 || chunk == 64) || (normalize != 0 && normalize != 1))
+        return FW_ERR_INVALID_ARG;
+    if (!dkey_supported(d_key) || io_dtype != FW_DTYPE_BF16)
+        return FW_ERR_UNSUPPORTED;
+    return fw::tc_linear_supported(d_key, nu, d_v, chunk, normalize) ? FW_OK : FW_ERR_UNSUPPORTED;
+}
+
+} // namespace
+
+FW_API size_t fw_linear_forward_workspace_size(int B, int H, int L, int d_key, int nu, int d_v, int chunk,
+                                               int normalize, int io_dtype) {
+    if (check_linear_shape(B, H, L, d_key, nu, d_v, chunk, normalize, io_dtype) != FW_OK)
+        return 0;
+    return fw::tc_linear_workspace_bytes(B, H, L, d_key, nu, d_v, chunk, normalize);
+}
+
+FW_API int fw_linear_forward(const void *q, const void *k, const void *v, const float *W0, const float *z0,
+                             float *W_final, float *z_final, void *y, void *workspace, size_t workspace_bytes,
+                             int B, int H, int L, int d_key, int nu, int d_v, int chunk, int normalize,
+                             int io_dtype, float eps, void *stream) {
+    if (!eps_ok(eps))
+        return FW_ERR_INVALID_ARG;
+    const int rc = check_linear_shape(B, H, L, d_key, nu, d_v, chunk, normalize, io_dtype);
+    if (rc != FW_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t BH = (int64_t)B * H;
+    if (BH == 0)
+        return FW_OK; // empty: no pointer is used and any may be NULL
+    if ((W0 && !aligned16(W0)) || (W_final && !aligned16(W_final)) || (z0 && !aligned16(z0)) ||
+        (z_final && !aligned16(z_final)))
+        return FW_ERR_INVALID_ARG;
+    if (L > 0) {
+        if (!q || !k || !v || !y || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(y))
+            return FW_ERR_INVALID_ARG;
+        const size_t need = fw_linear_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk, normalize, io_dtype);
+        if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+            return FW_ERR_INVALID_ARG;
+    }
+    if (BH > (int64_t)1 << 30)
+        return FW_ERR_UNSUPPORTED;
+    const int d_dot = 2 * d_key * nu;
+    if (L == 0) {
+        // no token: the final state is the initial one
+        cudaError_t e = cudaSuccess;
+        if (W_final && W_final != W0) {
+            const size_t bytes = sizeof(float) * (size_t)BH * d_v * d_dot;
+            e = W0 ? cudaMemcpyAsync(W_final, W0, bytes, cudaMemcpyDeviceToDevice, st)
+                   : cudaMemsetAsync(W_final, 0, bytes, st);
+        }
+        if (e == cudaSuccess && normalize && z_final && z_final != z0) {
+            const size_t bytes = sizeof(float) * (size_t)BH * d_dot;
+            e = z0 ? cudaMemcpyAsync(z_final, z0, bytes, cudaMemcpyDeviceToDevice, st)
+                   : cudaMemsetAsync(z_final, 0, bytes, st);
+        }
+        return cuda_status(e);
+    }
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess)
+        return FW_ERR_CUDA;
+    e = fw::tc_linear_launch(q, k, v, W0, normalize ? z0 : nullptr, W_final, normalize ? z_final : nullptr, y,
+                             workspace, B, H, L, d_key, nu, d_v, chunk, normalize, eps, di.num_sms, di.status, st);
+    return cuda_status(e);
+}
+
+namespace {
+
 // Checks shared by the two phases of the bf16 forward.  Returns FW_OK with
 // *empty set when nothing has to be enqueued.
 int check_phase(int B, int H, int L, int d_key, int nu, int d_v, int chunk, const void *workspace,

@@ -255,12 +255,17 @@ FW_DEV void dpfp_half_row(const uint4 (&raw)[DK / 8], int hs, int r, int nu, flo
 }
 
 // ---------------------------------------------------------------------------
-template <int DK>
+// SUM = false: the delta rule.  SUM = true: the sum rule (linear attention):
+// W' = 0, Q' = Q, U' = V', Y' = P V' with V' = V (d_vr channels) followed,
+// when d_v > d_vr, by a 16-channel block whose first channel is 1 on every
+// token (its running sum is z, its output the denominator z . phi(q)).  The
+// scan is the same for both rules.
+template <int DK, bool SUM>
 __global__ void __launch_bounds__(kPrepThreads, 2)
     chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                       const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ beta,
-                      uint8_t *__restrict__ ws, int L, int C, int nch, int nu, int Dp, int d_v, float eps,
-                      unsigned *status) {
+                      uint8_t *__restrict__ ws, int L, int C, int nch, int nu, int Dp, int d_v, int d_vr,
+                      float eps, unsigned *status) {
     constexpr int G = DK / 4, RPW = 32 / G, N2 = 2 * DK;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
@@ -318,16 +323,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     }
     constexpr int kVChunks = 4; // 64 * 128 / 8 / kPrepThreads
     uint4 vpre[kVChunks];
-    const int vcpr = d_v / 8;
+    const int vcpr = d_vr / 8;
 #pragma unroll
     for (int i = 0; i < kVChunks; ++i) {
         const int idx = tid + i * kPrepThreads, t = idx / vcpr, j = 8 * (idx % vcpr);
         vpre[i] = make_uint4(0, 0, 0, 0);
         if (idx < 64 * vcpr && t < Lc)
-            vpre[i] = __ldg(reinterpret_cast<const uint4 *>(v + ((size_t)bh * L + t0 + t) * d_v + j));
+            vpre[i] = __ldg(reinterpret_cast<const uint4 *>(v + ((size_t)bh * L + t0 + t) * d_vr + j));
     }
     float beta_t = 0.f;
-    if (tid < Lc && tid < 64)
+    if (!SUM && tid < Lc && tid < 64)
         beta_t = __bfloat162float(beta[bh * L + t0 + tid]);
 
     if (tid == 0) {
@@ -401,7 +406,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         tmem_ld16(tm + lb + (uint32_t)(32 * half), gr);
         tmem_ld16(tm + lb + (uint32_t)(32 * half + 16), gr + 16);
         tmem_ld_wait();
-        if (row < 64) { // A row (16-byte stores; rows are 16-byte aligned) and the I row
+        if (SUM && row < 64) { // the I row only (no triangular solve)
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                gr[j] = 32 * half + j == row ? 1.f : 0.f;
+        } else if (row < 64) { // A row (16-byte stores; rows are 16-byte aligned) and the I row
             const float br = bs[row];
 #pragma unroll
             for (int j4 = 0; j4 < 32; j4 += 4) {
@@ -426,87 +435,127 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     tc_fence_before();
     __syncthreads();
 
-    // (I + A)^-1, and T = (I + A)^-1 diag(beta) as the MN-major operand tile
-    // (rows k, columns n); ends synchronised, so A and N's space is free for V
-    unit_lower_inverse<kPrepThreads>(Am, Nm, Rm, bs, tt, tid);
+    if constexpr (SUM) {
+        // V' (values, then the ones block when normalising) into the A / N space
+        // as the MN-major B operand, then [I; P] V' = [V'; P V'] = [U'; Y'].
 #pragma unroll
-    for (int i = 0; i < kVChunks; ++i) {
-        const int idx = tid + i * kPrepThreads, t = idx / vcpr, j = 8 * (idx % vcpr);
-        if (idx < 64 * vcpr)
-            *reinterpret_cast<uint4 *>(vt + (uint32_t)(j >> 6) * 8192u + (uint32_t)t * 128u +
-                                       ((uint32_t)(((j & 63) >> 3) ^ (t & 7)) << 4)) = vpre[i];
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // MMA: [I; P] T = [T; P T]
-    if (tid == 0) {
-        const uint32_t idesc = idesc_bf16(128, 64, 0, 1);
-        const uint32_t a = smem_u32(ip), b = smem_u32(tt);
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-            mma_bf16(tm, desc_sw128(a + (uint32_t)s * 32u, 16, 1024), desc_sw128(b + (uint32_t)s * 2048u, 8192, 1024),
-                     idesc, s > 0);
-        mma_commit(bar);
-    }
-    ok = mbar_wait(bar, 1, status);
-    tc_fence_after();
-    if (__syncthreads_or(!ok))
-        goto teardown;
-    {
-        float tr[32];
-        tmem_ld16(tm + lb + (uint32_t)(32 * half), tr);
-        tmem_ld16(tm + lb + (uint32_t)(32 * half + 16), tr + 16);
-        tmem_ld_wait();
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-            *reinterpret_cast<uint4 *>(tp + kmajor_chunk(row, 32 * half + 8 * cc, 128)) = pack8(tr + 8 * cc);
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // MMA: [T; P T] [K | V] = [W', P W' | U', P U']  (columns 0..Dp-1 | Dp..Dp+d_v-1)
-    if (tid == 0) {
-        const uint32_t a = smem_u32(tp), bk = smem_u32(kq), bv = smem_u32(vt);
-        const uint32_t idk = idesc_bf16(128, 128, 0, 1), idv = idesc_bf16(128, d_v, 0, 1);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            const uint64_t ad = desc_sw128(a + (uint32_t)s * 32u, 16, 1024);
-            for (int j = 0; j < Dp / 128; ++j)
-                mma_bf16(tm + (uint32_t)(128 * j), ad,
-                         desc_sw128(bk + (uint32_t)(2 * j) * 16384u + (uint32_t)s * 2048u, 16384, 1024), idk, s > 0);
-            mma_bf16(tm + (uint32_t)Dp, ad, desc_sw128(bv + (uint32_t)s * 2048u, 8192, 1024), idv, s > 0);
+        for (int i = 0; i < kVChunks; ++i) {
+            const int idx = tid + i * kPrepThreads, t = idx / vcpr, j = 8 * (idx % vcpr);
+            if (idx < 64 * vcpr)
+                *reinterpret_cast<uint4 *>(vt + (uint32_t)(j >> 6) * 8192u + (uint32_t)t * 128u +
+                                           ((uint32_t)(((j & 63) >> 3) ^ (t & 7)) << 4)) = vpre[i];
         }
-        mma_commit(bar);
-        bulk_wait_read(); // the K image has been read out of the key rows
-    }
-    ok = mbar_wait(bar, 0, status);
-    tc_fence_after();
-    if (__syncthreads_or(!ok))
-        goto teardown;
-    // Record out.  W' replaces the key rows and Q' = Q - P W' the query rows
-    // of the [K; Q] tile in place (the K image's bulk read of the key rows
-    // finished before the barrier above); the tile goes out as one bulk copy.
-    for (int c0 = 32 * half; c0 < Dp; c0 += 64) { // 32 columns per pass (Dp % 64 == 0)
-        float w[32];
-        tmem_ld16(tm + lb + (uint32_t)c0, w);
-        tmem_ld16(tm + lb + (uint32_t)(c0 + 16), w + 16);
-        tmem_ld_wait();
+        if (d_v > d_vr && tid < 128) { // channel d_vr = 1 on the chunk's tokens, the rest of the block 0
+            const int t = tid >> 1, j = d_vr + 8 * (tid & 1);
+            const uint4 one = make_uint4((tid & 1) == 0 && t < Lc ? 0x3f80u : 0u, 0, 0, 0); // bf16 1.0 in the low half
+            *reinterpret_cast<uint4 *>(vt + (uint32_t)(j >> 6) * 8192u + (uint32_t)t * 128u +
+                                       ((uint32_t)(((j & 63) >> 3) ^ (t & 7)) << 4)) = one;
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            const uint32_t a = smem_u32(ip), bv = smem_u32(vt);
+            const uint32_t idv = idesc_bf16(128, d_v, 0, 1);
 #pragma unroll
-        for (int h2 = 0; h2 < 4; ++h2) {
-            uint4 *dst = reinterpret_cast<uint4 *>(kq + kmajor_chunk(row, c0 + 8 * h2, 128));
-            if (row >= 64) {
-                float qv[8];
-                unpack8(*dst, qv);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    w[8 * h2 + e] = qv[e] - w[8 * h2 + e];
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tm + (uint32_t)Dp, desc_sw128(a + (uint32_t)s * 32u, 16, 1024),
+                         desc_sw128(bv + (uint32_t)s * 2048u, 8192, 1024), idv, s > 0);
+            mma_commit(bar);
+            bulk_wait_read(); // the K image has been read out of the key rows
+        }
+        ok = mbar_wait(bar, 1, status);
+        tc_fence_after();
+        if (__syncthreads_or(!ok))
+            goto teardown;
+        // Record out: [W'; Q'] = [0; Q] (the key rows of the tile zeroed)
+        const int cpr = Dp / 8;
+        for (int idx = tid; idx < 64 * cpr; idx += kPrepThreads)
+            *reinterpret_cast<uint4 *>(kq + kmajor_chunk(idx / cpr, 8 * (idx % cpr), 128)) = make_uint4(0, 0, 0, 0);
+    } else {
+        // (I + A)^-1, and T = (I + A)^-1 diag(beta) as the MN-major operand tile
+        // (rows k, columns n); ends synchronised, so A and N's space is free for V
+        unit_lower_inverse<kPrepThreads>(Am, Nm, Rm, bs, tt, tid);
+    #pragma unroll
+        for (int i = 0; i < kVChunks; ++i) {
+            const int idx = tid + i * kPrepThreads, t = idx / vcpr, j = 8 * (idx % vcpr);
+            if (idx < 64 * vcpr)
+                *reinterpret_cast<uint4 *>(vt + (uint32_t)(j >> 6) * 8192u + (uint32_t)t * 128u +
+                                           ((uint32_t)(((j & 63) >> 3) ^ (t & 7)) << 4)) = vpre[i];
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // MMA: [I; P] T = [T; P T]
+        if (tid == 0) {
+            const uint32_t idesc = idesc_bf16(128, 64, 0, 1);
+            const uint32_t a = smem_u32(ip), b = smem_u32(tt);
+    #pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tm, desc_sw128(a + (uint32_t)s * 32u, 16, 1024), desc_sw128(b + (uint32_t)s * 2048u, 8192, 1024),
+                         idesc, s > 0);
+            mma_commit(bar);
+        }
+        ok = mbar_wait(bar, 1, status);
+        tc_fence_after();
+        if (__syncthreads_or(!ok))
+            goto teardown;
+        {
+            float tr[32];
+            tmem_ld16(tm + lb + (uint32_t)(32 * half), tr);
+            tmem_ld16(tm + lb + (uint32_t)(32 * half + 16), tr + 16);
+            tmem_ld_wait();
+    #pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+                *reinterpret_cast<uint4 *>(tp + kmajor_chunk(row, 32 * half + 8 * cc, 128)) = pack8(tr + 8 * cc);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // MMA: [T; P T] [K | V] = [W', P W' | U', P U']  (columns 0..Dp-1 | Dp..Dp+d_v-1)
+        if (tid == 0) {
+            const uint32_t a = smem_u32(tp), bk = smem_u32(kq), bv = smem_u32(vt);
+            const uint32_t idk = idesc_bf16(128, 128, 0, 1), idv = idesc_bf16(128, d_v, 0, 1);
+    #pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t ad = desc_sw128(a + (uint32_t)s * 32u, 16, 1024);
+                for (int j = 0; j < Dp / 128; ++j)
+                    mma_bf16(tm + (uint32_t)(128 * j), ad,
+                             desc_sw128(bk + (uint32_t)(2 * j) * 16384u + (uint32_t)s * 2048u, 16384, 1024), idk, s > 0);
+                mma_bf16(tm + (uint32_t)Dp, ad, desc_sw128(bv + (uint32_t)s * 2048u, 8192, 1024), idv, s > 0);
             }
-            *dst = pack8(w + 8 * h2);
+            mma_commit(bar);
+            bulk_wait_read(); // the K image has been read out of the key rows
+        }
+        ok = mbar_wait(bar, 0, status);
+        tc_fence_after();
+        if (__syncthreads_or(!ok))
+            goto teardown;
+        // Record out.  W' replaces the key rows and Q' = Q - P W' the query rows
+        // of the [K; Q] tile in place (the K image's bulk read of the key rows
+        // finished before the barrier above); the tile goes out as one bulk copy.
+        for (int c0 = 32 * half; c0 < Dp; c0 += 64) { // 32 columns per pass (Dp % 64 == 0)
+            float w[32];
+            tmem_ld16(tm + lb + (uint32_t)c0, w);
+            tmem_ld16(tm + lb + (uint32_t)(c0 + 16), w + 16);
+            tmem_ld_wait();
+    #pragma unroll
+            for (int h2 = 0; h2 < 4; ++h2) {
+                uint4 *dst = reinterpret_cast<uint4 *>(kq + kmajor_chunk(row, c0 + 8 * h2, 128));
+                if (row >= 64) {
+                    float qv[8];
+                    unpack8(*dst, qv);
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        w[8 * h2 + e] = qv[e] - w[8 * h2 + e];
+                }
+                *dst = pack8(w + 8 * h2);
+            }
         }
     }
     fence_async_smem();
@@ -552,10 +601,18 @@ FW_DEV uint32_t vtile_chunk(int row, int j0, uint32_t blk) {
 // MMA1 has read chunk c's; 1: chunk c + 1's, into the same buffer).  NKB = number
 // of K buffers (2: K images two chunks ahead; 1: the next K image is
 // fetched as soon as MMA3 has read the current one).
-template <int DVB, int NKB, int NA>
+// ZN = true (the normalised sum rule): the CTA's block is 16 value channels
+// followed by the record's 16-channel normaliser block (channel d_vr holds
+// the running z, its output the denominator z . phi(q)); DVB = 32, and y is
+// written as the ratio of the value columns to that denominator (0 where it
+// is 0).  d_v = the record's channel count, d_vr = the value channels of y,
+// W0 and W_final; z0 / zf: the normaliser state in and out ([B,H,d_dot]).
+template <int DVB, int NKB, int NA, bool ZN>
 __global__ void __launch_bounds__(kScanThreads)
-    chunk_scan_kernel(const float *W0, float *Wf, __nv_bfloat16 *__restrict__ y, const uint8_t *__restrict__ ws,
-                      int L, int C, int nch, int d_v, int d_dot, int Dp, unsigned *status) {
+    chunk_scan_kernel(const float *W0, float *Wf, const float *z0, float *zf, __nv_bfloat16 *__restrict__ y,
+                      const uint8_t *__restrict__ ws, int L, int C, int nch, int d_v, int d_vr, int d_dot, int Dp,
+                      unsigned *status) {
+    static_assert(!ZN || DVB == 32, "the normalised form takes 16 value + 16 normaliser channels");
     constexpr int DS = DVB < 32 ? 32 : DVB;          // TMEM columns per accumulator region
     constexpr int VB = (DVB + 63) / 64;              // 64-column blocks of the value tiles
     extern __shared__ uint8_t smem_raw[];
@@ -575,12 +632,14 @@ __global__ void __launch_bounds__(kScanThreads)
     uint32_t *slot = (uint32_t *)(bar_a + 5);
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int v0 = blockIdx.x * DVB;
+    const int v0 = blockIdx.x * (ZN ? 16 : DVB);
     const int64_t bh = blockIdx.y;
+    // record channel of the CTA's column j (column groups of 4 stay contiguous)
+    auto chan = [&](int j) { return (ZN && j >= 16) ? d_vr + (j - 16) : v0 + j; };
     const int MB = Dp / 128;
     const uint32_t ncols = tmem_cols_pow2((1 + MB) * DS);
     const uint8_t *rec0 = ws + (size_t)bh * nch * rc.bytes;
-    const bool has_w0 = W0 != nullptr;
+    const bool has_w0 = W0 != nullptr || (ZN && z0 != nullptr);
     const uint32_t lb = tmem_lane_base(warp);
 
     if (tid == 0) {
@@ -612,8 +671,13 @@ __global__ void __launch_bounds__(kScanThreads)
         for (int j0 = 0; j0 < DVB; j0 += 16) {
             float w[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                w[j] = (has_w0 && d < d_dot) ? W0[((size_t)bh * d_v + v0 + j0 + j) * d_dot + d] : 0.f;
+            for (int j = 0; j < 16; ++j) {
+                const int jj = j0 + j;
+                if (ZN && jj >= 16)
+                    w[j] = (jj == 16 && z0 && d < d_dot) ? z0[(size_t)bh * d_dot + d] : 0.f;
+                else
+                    w[j] = (W0 && d < d_dot) ? W0[((size_t)bh * d_vr + v0 + jj) * d_dot + d] : 0.f;
+            }
             if (has_w0)
                 tmem_st16(tS + (uint32_t)(mb * DS + j0) + lb, w);
             *reinterpret_cast<uint4 *>(st + vtile_chunk(d, j0, sblk)) = pack8(w);
@@ -649,11 +713,10 @@ __global__ void __launch_bounds__(kScanThreads)
     // 512-byte run.  Chunk c + 1's are loaded as soon as chunk c's are used.
     float pre[DVB];
     auto load_pre = [&](int cc) {
-        const float *src =
-            (const float *)(rec0 + (size_t)cc * rc.bytes + (tid < 64 ? rc.up : rc.yp)) + 4 * (tid & 63) + 64 * v0;
+        const float *src = (const float *)(rec0 + (size_t)cc * rc.bytes + (tid < 64 ? rc.up : rc.yp)) + 4 * (tid & 63);
 #pragma unroll
         for (int j = 0; j < DVB; j += 4) {
-            const float4 f = __ldg(reinterpret_cast<const float4 *>(src + 64 * j));
+            const float4 f = __ldg(reinterpret_cast<const float4 *>(src + 64 * chan(j)));
             pre[j] = f.x;
             pre[j + 1] = f.y;
             pre[j + 2] = f.z;
@@ -696,22 +759,30 @@ __global__ void __launch_bounds__(kScanThreads)
             for (int j0 = 0; j0 < DVB; j0 += 16) // every load in flight, then one wait
                 tmem_ld16(tD1 + lb + (uint32_t)j0, d1 + j0);
             tmem_ld_wait();
+            if (tid < 64) {                           // U = U' - W' S^T
 #pragma unroll
-            for (int j0 = 0; j0 < DVB; j0 += 16) {
-                if (tid < 64) {                       // U = U' - W' S^T
+                for (int j0 = 0; j0 < DVB; j0 += 16) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         d1[j0 + j] = pre[j0 + j] - d1[j0 + j];
                     *reinterpret_cast<uint4 *>(ut + vtile_chunk(tid, j0, 8192u)) = pack8(d1 + j0);
                     *reinterpret_cast<uint4 *>(ut + vtile_chunk(tid, j0 + 8, 8192u)) = pack8(d1 + j0 + 8);
-                } else if (tid - 64 < Lc) {           // y = Y' + Q' S^T
+                }
+            } else if (tid - 64 < Lc) {               // y = Y' + Q' S^T
+#pragma unroll
+                for (int j = 0; j < DVB; ++j)
+                    d1[j] += pre[j];
+                if constexpr (ZN) {                   // the ratio to the normaliser column
+                    const float den = d1[16];
+                    const float inv = den != 0.f ? 1.0f / den : 0.f;
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        d1[j0 + j] += pre[j0 + j];
-                    __nv_bfloat16 *dst = y + ((size_t)bh * L + t0 + (tid - 64)) * d_v + v0 + j0;
-                    *reinterpret_cast<uint4 *>(dst) = pack8(d1 + j0);
-                    *reinterpret_cast<uint4 *>(dst + 8) = pack8(d1 + j0 + 8);
+                        d1[j] *= inv;
                 }
+                __nv_bfloat16 *dst = y + ((size_t)bh * L + t0 + (tid - 64)) * d_vr + v0;
+#pragma unroll
+                for (int j0 = 0; j0 < (ZN ? 16 : DVB); j0 += 8)
+                    *reinterpret_cast<uint4 *>(dst + j0) = pack8(d1 + j0);
             }
         }
         if (c + 1 < nch)
@@ -757,10 +828,15 @@ __global__ void __launch_bounds__(kScanThreads)
                 if (c + 1 < nch) {
                     *reinterpret_cast<uint4 *>(st + vtile_chunk(d, j0, sblk)) = pack8(sv + j0);
                     *reinterpret_cast<uint4 *>(st + vtile_chunk(d, j0 + 8, sblk)) = pack8(sv + j0 + 8);
-                } else if (Wf && d < d_dot) {
+                } else if (d < d_dot) {
+                    if (ZN && j0 >= 16) {             // the normaliser state: column 16
+                        if (j0 == 16 && zf && blockIdx.x == 0)
+                            zf[(size_t)bh * d_dot + d] = sv[16];
+                    } else if (Wf) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        Wf[((size_t)bh * d_v + v0 + j0 + j) * d_dot + d] = sv[j0 + j];
+                        for (int j = 0; j < 16; ++j)
+                            Wf[((size_t)bh * d_vr + v0 + j0 + j) * d_dot + d] = sv[j0 + j];
+                    }
                 }
             }
         }
@@ -792,68 +868,62 @@ bool fits(int Dp, int d_v, int dvb) {
     return Dp <= kMaxDp && Dp + d_v <= 512 && scan_smem(Dp, dvb, 1, 1) <= kMaxSmem && prep_smem(Dp, d_v) <= kMaxSmem;
 }
 
-// Value channels per scan CTA.  The walk over the chunks is serial, so the
-// per-chunk latency decides: a tcgen05.mma of M = 128 costs about the same
-// for any N up to 128, but the per-thread work between the MMAs (TMEM loads,
-// the U and S tiles, y) grows with the channel count.  Measured on the
-// b4h8 L512 and nu = 3 L2048 workloads, 16 channels per CTA beat 32 and 64
-// (scan 14.4 / 18.5 / 24.5 us and 80 / 96 / 141 us).
-int choose_dvb(int d_v) { return 16 <= d_v ? 16 : d_v; }
+// Value channels per scan CTA: 16 (32 with the normaliser block).  The walk
+// over the chunks is serial, so the per-chunk latency decides: a tcgen05.mma
+// of M = 128 costs about the same for any N up to 128, but the per-thread
+// work between the MMAs (TMEM loads, the U and S tiles, y) grows with the
+// channel count.  Measured on the b4h8 L512 and nu = 3 L2048 workloads, 16
+// channels per CTA beat 32 and 64 (scan 14.4 / 18.5 / 24.5 us and
+// 80 / 96 / 141 us).
+constexpr int kDVB = 16;
 
 // Two K buffers when they fit in shared memory, else one; then two [W'; Q']
 // buffers when those fit as well.
 int choose_nkb(int Dp, int dvb) { return scan_smem(Dp, dvb, 2, 1) <= kMaxSmem ? 2 : 1; }
 int choose_na(int Dp, int dvb) { return scan_smem(Dp, dvb, choose_nkb(Dp, dvb), 2) <= kMaxSmem ? 2 : 1; }
 
-template <int DK>
+template <int DK, bool SUM>
 cudaError_t launch_prep(const void *q, const void *k, const void *v, const void *beta, uint8_t *ws, int BH,
-                        int L, int C, int nch, int nu, int Dp, int d_v, float eps, unsigned *status,
+                        int L, int C, int nch, int nu, int Dp, int d_v, int d_vr, float eps, unsigned *status,
                         cudaStream_t st) {
     const size_t smem = prep_smem(Dp, d_v);
-    auto kern = chunk_prep_kernel<DK>;
+    auto kern = chunk_prep_kernel<DK, SUM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
     return launch_pdl(kern, dim3((unsigned)nch, (unsigned)BH), dim3(kPrepThreads), smem, st,
                       static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
                       static_cast<const __nv_bfloat16 *>(v), static_cast<const __nv_bfloat16 *>(beta), ws, L, C,
-                      nch, nu, Dp, d_v, eps, status);
+                      nch, nu, Dp, d_v, d_vr, eps, status);
 }
 
-template <int DVB, int NKB, int NA>
-cudaError_t launch_scan(const float *W0, float *Wf, void *y, const uint8_t *ws, int BH, int L, int C, int nch,
-                        int d_v, int d_dot, int Dp, unsigned *status, cudaStream_t st) {
+template <int DVB, int NKB, int NA, bool ZN>
+cudaError_t launch_scan(const float *W0, float *Wf, const float *z0, float *zf, void *y, const uint8_t *ws, int BH,
+                        int L, int C, int nch, int d_v, int d_vr, int d_dot, int Dp, unsigned *status,
+                        cudaStream_t st) {
     const size_t smem = scan_smem(Dp, DVB, NKB, NA);
-    auto kern = chunk_scan_kernel<DVB, NKB, NA>;
+    auto kern = chunk_scan_kernel<DVB, NKB, NA, ZN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
     // programmatic dependent launch: the scan's CTAs may be scheduled while
     // the preceding kernel (the prep) finishes; they wait in griddep_wait
     // before reading its output
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(d_v / DVB), (unsigned)BH);
-    cfg.blockDim = dim3(kScanThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, W0, Wf, static_cast<__nv_bfloat16 *>(y), ws, L, C, nch, d_v, d_dot, Dp,
-                              status);
+    const dim3 grid((unsigned)(ZN ? d_vr / 16 : d_v / DVB), (unsigned)BH);
+    return launch_pdl(kern, grid, dim3(kScanThreads), smem, st, W0, Wf, z0, zf, static_cast<__nv_bfloat16 *>(y), ws,
+                      L, C, nch, d_v, d_vr, d_dot, Dp, status);
 }
 
-template <int DVB>
-cudaError_t launch_scan_nkb(const float *W0, float *Wf, void *y, const uint8_t *ws, int BH, int L, int C, int nch,
-                            int d_v, int d_dot, int Dp, unsigned *status, cudaStream_t st) {
+template <int DVB, bool ZN>
+cudaError_t launch_scan_bufs(const float *W0, float *Wf, const float *z0, float *zf, void *y, const uint8_t *ws,
+                             int BH, int L, int C, int nch, int d_v, int d_vr, int d_dot, int Dp, unsigned *status,
+                             cudaStream_t st) {
     if (choose_nkb(Dp, DVB) == 2) {
         if (choose_na(Dp, DVB) == 2)
-            return launch_scan<DVB, 2, 2>(W0, Wf, y, ws, BH, L, C, nch, d_v, d_dot, Dp, status, st);
-        return launch_scan<DVB, 2, 1>(W0, Wf, y, ws, BH, L, C, nch, d_v, d_dot, Dp, status, st);
+            return launch_scan<DVB, 2, 2, ZN>(W0, Wf, z0, zf, y, ws, BH, L, C, nch, d_v, d_vr, d_dot, Dp, status, st);
+        return launch_scan<DVB, 2, 1, ZN>(W0, Wf, z0, zf, y, ws, BH, L, C, nch, d_v, d_vr, d_dot, Dp, status, st);
     }
-    return launch_scan<DVB, 1, 1>(W0, Wf, y, ws, BH, L, C, nch, d_v, d_dot, Dp, status, st);
+    return launch_scan<DVB, 1, 1, ZN>(W0, Wf, z0, zf, y, ws, BH, L, C, nch, d_v, d_vr, d_dot, Dp, status, st);
 }
 
 } // namespace
@@ -865,7 +935,7 @@ bool tc_forward_supported(int d_key, int nu, int d_v, int chunk) {
         return false;
     if (chunk < 1 || chunk > kTile)
         return false;
-    return fits(padded_ddot(2 * d_key * nu), d_v, choose_dvb(d_v));
+    return fits(padded_ddot(2 * d_key * nu), d_v, kDVB);
 }
 
 size_t tc_forward_workspace_bytes(int B, int H, int L, int d_key, int nu, int d_v, int chunk) {
@@ -873,21 +943,32 @@ size_t tc_forward_workspace_bytes(int B, int H, int L, int d_key, int nu, int d_
     return (size_t)B * H * nch * record_layout(padded_ddot(2 * d_key * nu), d_v).bytes;
 }
 
-cudaError_t tc_prepare_launch(const void *q, const void *k, const void *v, const void *beta, void *workspace,
-                              int B, int H, int L, int d_key, int nu, int d_v, int chunk, float eps,
-                              unsigned *status, cudaStream_t st) {
+namespace {
+
+template <bool SUM>
+cudaError_t prep_dispatch(const void *q, const void *k, const void *v, const void *beta, void *workspace, int B,
+                          int H, int L, int d_key, int nu, int d_v, int d_vr, int chunk, float eps, unsigned *status,
+                          cudaStream_t st) {
     const int BH = B * H;
     const int nch = (L + chunk - 1) / chunk;
     const int Dp = padded_ddot(2 * d_key * nu);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     switch (d_key) {
-    case 8: return launch_prep<8>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st);
-    case 16: return launch_prep<16>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st);
-    case 32: return launch_prep<32>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st);
-    case 64: return launch_prep<64>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st);
-    case 128: return launch_prep<128>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, eps, status, st);
+    case 8: return launch_prep<8, SUM>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, d_vr, eps, status, st);
+    case 16: return launch_prep<16, SUM>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, d_vr, eps, status, st);
+    case 32: return launch_prep<32, SUM>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, d_vr, eps, status, st);
+    case 64: return launch_prep<64, SUM>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, d_vr, eps, status, st);
+    case 128: return launch_prep<128, SUM>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, d_vr, eps, status, st);
     default: return cudaErrorInvalidValue;
     }
+}
+
+} // namespace
+
+cudaError_t tc_prepare_launch(const void *q, const void *k, const void *v, const void *beta, void *workspace,
+                              int B, int H, int L, int d_key, int nu, int d_v, int chunk, float eps,
+                              unsigned *status, cudaStream_t st) {
+    return prep_dispatch<false>(q, k, v, beta, workspace, B, H, L, d_key, nu, d_v, d_v, chunk, eps, status, st);
 }
 
 cudaError_t tc_scan_launch(const void *workspace, const float *W0, float *W_final, void *y, int B, int H, int L,
@@ -898,12 +979,8 @@ cudaError_t tc_scan_launch(const void *workspace, const float *W0, float *W_fina
     const int Dp = padded_ddot(d_dot);
     const uint8_t *ws = static_cast<const uint8_t *>(workspace);
     (void)num_sms;
-    switch (choose_dvb(d_v)) {
-    case 16: return launch_scan_nkb<16>(W0, W_final, y, ws, BH, L, chunk, nch, d_v, d_dot, Dp, status, st);
-    case 32: return launch_scan_nkb<32>(W0, W_final, y, ws, BH, L, chunk, nch, d_v, d_dot, Dp, status, st);
-    case 64: return launch_scan_nkb<64>(W0, W_final, y, ws, BH, L, chunk, nch, d_v, d_dot, Dp, status, st);
-    default: return cudaErrorInvalidValue;
-    }
+    return launch_scan_bufs<kDVB, false>(W0, W_final, nullptr, nullptr, y, ws, BH, L, chunk, nch, d_v, d_v, d_dot, Dp,
+                                         status, st);
 }
 
 cudaError_t tc_forward_launch(const void *q, const void *k, const void *v, const void *beta,
@@ -914,6 +991,49 @@ cudaError_t tc_forward_launch(const void *q, const void *k, const void *v, const
     if (e != cudaSuccess)
         return e;
     return tc_scan_launch(workspace, W0, W_final, y, B, H, L, d_key, nu, d_v, chunk, num_sms, status, st);
+}
+
+// ------------------------------------------------ the sum rule (linear attention)
+bool tc_linear_supported(int d_key, int nu, int d_v, int chunk, int normalize) {
+    if (!(d_key == 8 || d_key == 16 || d_key == 32 || d_key == 64 || d_key == 128))
+        return false;
+    if (!(d_v == 16 || d_v == 32 || d_v == 64 || d_v == 128))
+        return false;
+    if (chunk < 1 || chunk > kTile)
+        return false;
+    return fits(padded_ddot(2 * d_key * nu), d_v + (normalize ? 16 : 0), normalize ? 32 : kDVB);
+}
+
+size_t tc_linear_workspace_bytes(int B, int H, int L, int d_key, int nu, int d_v, int chunk, int normalize) {
+    const int nch = (L + chunk - 1) / chunk;
+    return (size_t)B * H * nch * record_layout(padded_ddot(2 * d_key * nu), d_v + (normalize ? 16 : 0)).bytes;
+}
+
+// The same two kernels as the delta rule: the prep in its sum-rule form
+// (records with W' = 0, Q' = Q, U' = V', Y' = P V'), then the scan, which
+// with W' = 0 reduces to y = Y' + Q S^T, S += K^T V'.  With the normaliser,
+// V' carries a ones column whose state is z and whose output is the
+// denominator, and each scan CTA takes that block beside its 16 channels.
+cudaError_t tc_linear_launch(const void *q, const void *k, const void *v, const float *W0, const float *z0,
+                             float *W_final, float *z_final, void *y, void *workspace, int B, int H, int L,
+                             int d_key, int nu, int d_v, int chunk, int normalize, float eps, int num_sms,
+                             unsigned *status, cudaStream_t st) {
+    (void)num_sms;
+    const int dv2 = d_v + (normalize ? 16 : 0);
+    cudaError_t e = prep_dispatch<true>(q, k, v, nullptr, workspace, B, H, L, d_key, nu, dv2, d_v, chunk, eps,
+                                        status, st);
+    if (e != cudaSuccess)
+        return e;
+    const int BH = B * H;
+    const int nch = (L + chunk - 1) / chunk;
+    const int d_dot = 2 * d_key * nu;
+    const int Dp = padded_ddot(d_dot);
+    const uint8_t *ws = static_cast<const uint8_t *>(workspace);
+    if (normalize)
+        return launch_scan_bufs<32, true>(W0, W_final, z0, z_final, y, ws, BH, L, chunk, nch, dv2, d_v, d_dot, Dp,
+                                          status, st);
+    return launch_scan_bufs<kDVB, false>(W0, W_final, nullptr, nullptr, y, ws, BH, L, chunk, nch, d_v, d_v, d_dot,
+                                         Dp, status, st);
 }
 
 } // namespace fw

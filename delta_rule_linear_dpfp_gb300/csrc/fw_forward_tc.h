@@ -30,4 +30,14 @@ cudaError_t tc_forward_launch(const void *q, const void *k, const void *v, const
                               int H, int L, int d_key, int nu, int d_v, int chunk, float eps,
                               int num_sms, unsigned *status, cudaStream_t st);
 
+// The sum rule (linear attention), bf16 I/O: W_i = W_{i-1} + v_i phi(k_i)^T,
+// y_i = W_i phi(q_i), divided by z_i . phi(q_i) (z_i = sum of phi(k)) when
+// normalize != 0.  Arguments validated by the caller.
+bool tc_linear_supported(int d_key, int nu, int d_v, int chunk, int normalize);
+size_t tc_linear_workspace_bytes(int B, int H, int L, int d_key, int nu, int d_v, int chunk, int normalize);
+cudaError_t tc_linear_launch(const void *q, const void *k, const void *v, const float *W0, const float *z0,
+                             float *W_final, float *z_final, void *y, void *workspace, int B, int H, int L,
+                             int d_key, int nu, int d_v, int chunk, int normalize, float eps, int num_sms,
+                             unsigned *status, cudaStream_t st);
+
 } // namespace fw

@@ -73,6 +73,26 @@ def random_forward_inputs(B, H, L, d_key, nu, d_v, io="bf16", w0_var=None, seed=
                 beta=beta.to(dt).contiguous(), W0=W0)
 
 
+def linear_inputs(B, H, L, d_key, nu, d_v, with_state=False, seed=0):
+    """Inputs of the sum rule (linear attention): q, k, v ~ N(0,1) in bf16;
+    with_state adds W0 ~ N(0, 0.01) and a normaliser z0 = 0.05 |N(0,1)|
+    (non-negative, like a running sum of DPFP features), both fp32.
+
+    Draw order: q, k, v, W0, z0.  Returns a dict of CPU tensors.
+    """
+    g = _gen(seed)
+    d_dot = 2 * d_key * nu
+    q = torch.randn(B, H, L, d_key, generator=g, dtype=torch.float32)
+    k = torch.randn(B, H, L, d_key, generator=g, dtype=torch.float32)
+    v = torch.randn(B, H, L, d_v, generator=g, dtype=torch.float32)
+    W0 = z0 = None
+    if with_state:
+        W0 = torch.randn(B, H, d_v, d_dot, generator=g, dtype=torch.float32) * 0.1
+        z0 = torch.randn(B, H, d_dot, generator=g, dtype=torch.float32).abs() * 0.05
+    bf = torch.bfloat16
+    return dict(q=q.to(bf).contiguous(), k=k.to(bf).contiguous(), v=v.to(bf).contiguous(), W0=W0, z0=z0)
+
+
 def projected_inputs(B, H, L, d_model, nu, io="bf16", seed=0):
     """x ~ N(0,1) [B,L,d_model] through bias-free W_q, W_k, W_v [d_model, d_model]
     and W_beta [d_model, H], all ~ N(0, 1/d_model), computed on the host in

@@ -140,6 +140,47 @@ FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const v
                             int d_v, int chunk, int io_dtype, float eps, void *stream);
 
 /*
+ * Bytes of device workspace fw_linear_forward needs for this shape (0 for
+ * arguments it would reject).  The caller allocates it.
+ */
+FW_API size_t fw_linear_forward_workspace_size(int B, int H, int L, int d_key, int nu, int d_v,
+                                               int chunk, int normalize, int io_dtype);
+
+/*
+ * fw_linear_forward -- the sum rule that the delta rule replaces: linear
+ * self-attention with the DPFP kernel, written as a fast-weight recurrence.
+ * [Fast Weights Transformer guide, section on the fast form of linear
+ * self-attention: W_i = W_{i-1} + v_i outer phi(k_i), z_i = z_{i-1} +
+ * phi(k_i), y_i = W_i phi(q_i) / (z_i . phi(q_i)).]  The guide gives no
+ * guard for a zero denominator; here y_i = 0 where z_i . phi(q_i) == 0
+ * (every phi is non-negative, so the numerator is 0 there as well).
+ *
+ *   q, k     : [B, H, L, d_key]   bf16              (read)
+ *   v        : [B, H, L, d_v]     bf16              (read)
+ *   W0       : [B, H, d_v, d_dot] fp32 initial state, or NULL for zeros
+ *   z0       : [B, H, d_dot]      fp32 initial normaliser, or NULL for zeros
+ *   W_final  : [B, H, d_v, d_dot] fp32 final state, or NULL to skip it
+ *   z_final  : [B, H, d_dot]      fp32 final normaliser, or NULL to skip it
+ *              (W_final == W0 and z_final == z0 in place are allowed)
+ *   y        : [B, H, L, d_v]     bf16              (written)
+ *   workspace: device scratch of at least fw_linear_forward_workspace_size()
+ *              bytes; contents on entry do not matter, garbage on return
+ *   chunk    : in {16, 32, 64}, as for fw_delta_forward
+ *   normalize: 1 divides by z . phi(q); 0 returns W phi(q) (z0 and z_final
+ *              are then not used)
+ *   io_dtype : FW_DTYPE_BF16 (the tensor-core path; FW_DTYPE_F32 returns
+ *              FW_ERR_UNSUPPORTED)
+ *   eps      : DPFP normaliser (1e-6 in the guide)
+ * Errors as for fw_delta_forward; with normalize the state must also fit the
+ * tensor memory with 16 more channels (padded d_dot + d_v + 16 <= 512).
+ */
+FW_API int fw_linear_forward(const void *q, const void *k, const void *v, const float *W0,
+                             const float *z0, float *W_final, float *z_final, void *y,
+                             void *workspace, size_t workspace_bytes, int B, int H, int L,
+                             int d_key, int nu, int d_v, int chunk, int normalize, int io_dtype,
+                             float eps, void *stream);
+
+/*
  * fw_delta_forward_prepare / fw_delta_forward_scan -- the two phases of the
  * bf16 fw_delta_forward, callable on their own (bf16 I/O only).  Enqueuing
  * prepare then scan on one stream computes exactly what fw_delta_forward

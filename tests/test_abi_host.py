@@ -180,3 +180,37 @@ def test_phase_argument_checks(lib):
     bad = list(sargs)
     bad[5] = 0                           # empty batch: nothing to do
     assert scan(*bad) == OK
+
+
+def test_linear_argument_checks(lib):
+    E, U, OK = binding.FW_ERR_INVALID_ARG, binding.FW_ERR_UNSUPPORTED, binding.FW_OK
+    f, ws = lib.fw_linear_forward, lib.fw_linear_forward_workspace_size
+    need = ws(2, 2, 8, 64, 1, 64, 64, 1, 1)
+    assert need > 0
+    assert ws(2, 2, 8, 64, 1, 64, 64, 1, 0) == 0            # fp32 I/O is not compiled
+    assert ws(2, 2, 8, 64, 1, 64, 64, 2, 1) == 0            # normalize must be 0 or 1
+    assert ws(2, 2, 8, 64, 1, 64, 64, 0, 1) < need          # no normaliser block
+    base = [FAKE] * 9 + [need, 2, 2, 8, 64, 1, 64, 64, 1, 1, 1e-6, None]
+
+    def call(**kw):
+        a = list(base)
+        names = ["q", "k", "v", "W0", "z0", "Wf", "zf", "y", "ws", "wsb", "B", "H", "L", "d_key", "nu",
+                 "d_v", "chunk", "normalize", "io", "eps", "stream"]
+        for key, val in kw.items():
+            a[names.index(key)] = val
+        return f(*a)
+
+    for name in ("q", "k", "v", "y", "ws"):
+        assert call(**{name: None}) == E
+        assert call(**{name: MISALIGNED}) == E
+    for name in ("W0", "z0", "Wf", "zf"):
+        assert call(**{name: MISALIGNED}) == E
+    assert call(wsb=need - 1) == E
+    assert call(normalize=3) == E
+    assert call(io=0) == U
+    assert call(d_key=24) == U
+    assert call(d_key=128, nu=2) == U                       # padded d_dot 512 > 384
+    assert call(nu=0) == E
+    assert call(chunk=48) == E
+    assert call(eps=-1.0) == E
+    assert call(B=0, q=None, k=None, v=None, y=None, ws=None) == OK
