@@ -411,6 +411,22 @@ def measure_rows(fw, inputs, dev, stream, pk):
                  forward_bytes(B, H, L, d_key, d_v, d_dot, 2, w0=True), ms, pk)
     r["tokens/s"] = B * L / (ms * 1e-3)
     rows[name] = r
+    # the sum rule (linear attention, z-normalised) on the bench workload's shapes
+    B, H, L, d_key, nu, d_v, C = 4, 8, 512, 64, 1, 64, 64
+    d_dot = 2 * d_key * nu
+    li = {k: (None if v is None else v.to(dev)) for k, v in inputs.linear_inputs(B, H, L, d_key, nu, d_v).items()}
+    yl = torch.empty(B, H, L, d_v, dtype=torch.bfloat16, device=dev)
+    Wl = torch.empty(B, H, d_v, d_dot, dtype=torch.float32, device=dev)
+    zl = torch.empty(B, H, d_dot, dtype=torch.float32, device=dev)
+    nws = fw.fw_linear_forward_workspace_size(B, H, L, d_key, nu, d_v, C, True)
+    wsl = torch.empty(nws, dtype=torch.uint8, device=dev)
+    ms = _time(lambda i: fw.fw_linear_forward(li["q"], li["k"], li["v"], nu=nu, normalize=True, chunk=C, y=yl,
+                                              W_final=Wl, z_final=zl, workspace=wsl, stream=stream), 200, stream)
+    flops = (C * d_dot + C * (d_v + 1) + 4.0 * d_dot * (d_v + 1)) * B * H * L
+    nbytes = B * H * L * 2 * (2 * d_key + 2 * d_v) + B * H * (d_v + 1) * d_dot * 4
+    r = roofline("fw_linear_forward (prepare + scan)", flops, nbytes, ms, pk)
+    r["tokens/s"] = B * L / (ms * 1e-3)
+    rows["linear_b4h8_l512_normalised"] = r
     return rows
 
 
