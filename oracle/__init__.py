@@ -8,6 +8,8 @@ Contents
   dpfp(x, nu, eps)                  -- the DPFP feature map, plain C, fp64
   delta_forward(q, k, v, beta, ...) -- O1: the sequential recurrence, plain C
   delta_decode_step(...)            -- one token against a persistent W
+  delta_backward(q, k, v, beta, ...) -- gradients of the recurrence (reverse
+                                       sweep over the kept history of W), plain C
   linear_forward(q, k, v, ...)      -- the sum rule (linear attention, with or
                                        without the z normaliser), plain C
   chunked.delta_forward_chunked     -- O2: the chunked (WY / UT) form in numpy,
@@ -58,6 +60,9 @@ class OracleLib:
         lib.fwo_delta_decode_step.restype = ctypes.c_int
         lib.fwo_delta_decode_step.argtypes = [_c_double_p] * 6 + [ctypes.c_int64] * 2 + [
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int]
+        lib.fwo_delta_backward.restype = ctypes.c_int
+        lib.fwo_delta_backward.argtypes = [_c_double_p] * 12 + [ctypes.c_int64] * 3 + [
+            ctypes.c_int] * 3 + [ctypes.c_double, ctypes.c_int]
         lib.fwo_linear_forward.restype = ctypes.c_int
         lib.fwo_linear_forward.argtypes = [_c_double_p] * 8 + [ctypes.c_int64] * 3 + [
             ctypes.c_int] * 4 + [ctypes.c_double, ctypes.c_int]
@@ -118,6 +123,28 @@ class OracleLib:
         return y, W
 
 
+    def delta_backward(self, q, k, v, beta, gy, W0=None, gW=None, nu: int = 1, eps: float = 1e-6,
+                       nthreads: int = 1):
+        """Gradients of sum(gy * y) + sum(gW * W_final) for the forward above.
+
+        gy: [B,H,L,d_v]; gW: [B,H,d_v,d_dot] or None (zero).  Returns
+        (gq, gk, gv, gbeta, gW0) in fp64.
+        """
+        q, k, v, beta, gy = _f64(q), _f64(k), _f64(v), _f64(beta), _f64(gy)
+        B, H, L, d_key = q.shape
+        d_v = v.shape[-1]
+        d_dot = 2 * d_key * nu
+        W0 = None if W0 is None else _f64(W0)
+        gW = None if gW is None else _f64(gW)
+        gq, gk = np.empty_like(q), np.empty_like(k)
+        gv, gbeta = np.empty_like(v), np.empty_like(beta)
+        gW0 = np.empty((B, H, d_v, d_dot), dtype=np.float64)
+        rc = self._lib.fwo_delta_backward(_p(q), _p(k), _p(v), _p(beta), _p(W0), _p(gy), _p(gW), _p(gq), _p(gk),
+                                          _p(gv), _p(gbeta), _p(gW0), B, H, L, d_key, nu, d_v, eps, int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle delta_backward rejected arguments")
+        return gq, gk, gv, gbeta, gW0
+
     def linear_forward(self, q, k, v, W0=None, z0=None, nu: int = 1, normalize: bool = True,
                        eps: float = 1e-6, nthreads: int = 1):
         """The sum rule (linear attention) as a recurrence.
@@ -170,3 +197,7 @@ def delta_decode_step(q, k, v, beta, W, nu: int = 1, eps: float = 1e-6, nthreads
 def linear_forward(q, k, v, W0=None, z0=None, nu: int = 1, normalize: bool = True, eps: float = 1e-6,
                    nthreads: int = 1):
     return lib().linear_forward(q, k, v, W0, z0, nu, normalize, eps, nthreads)
+
+
+def delta_backward(q, k, v, beta, gy, W0=None, gW=None, nu: int = 1, eps: float = 1e-6, nthreads: int = 1):
+    return lib().delta_backward(q, k, v, beta, gy, W0, gW, nu, eps, nthreads)

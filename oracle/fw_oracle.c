@@ -24,6 +24,10 @@
  *     key, not to value;
  *   - section "token_wise variant": one token at a time against a W that
  *     persists across calls (the decode step);
+ *   - the backward of the recurrence (the gradients the guide's training
+ *     loop takes through it by autograd; the pages print no backward): the
+ *     chain rule applied to the steps above in reverse order, with the whole
+ *     history of W kept (see fwo_delta_backward);
  *   - section "linear self-attention, the fast form" (the sum rule the
  *     delta rule replaces): W_i = W_{i-1} + v_i outer phi(k_i),
  *     z_i = z_{i-1} + phi(k_i), y_i = W_i phi(q_i) / (z_i . phi(q_i)) -- the
@@ -306,6 +310,197 @@ int fwo_linear_forward(const double *q, const double *k, const double *v, const 
     } else {
         for (int i = 0; i < nthreads; ++i)
             pthread_create(&tids[i], NULL, run_ljob, &jobs[i]);
+        for (int i = 0; i < nthreads; ++i)
+            pthread_join(tids[i], NULL);
+    }
+    free(jobs);
+    free(tids);
+    return FWO_OK;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Backward of the delta rule for one (batch, head) pair.                 */
+/* Forward, per token: pk = phi(k_t), pq = phi(q_t), a = W_{t-1} pk,        */
+/* u = beta_t (v_t - a), W_t = W_{t-1} + u pk^T, y_t = W_t pq.              */
+/* Given gy_t = dL/dy_t and gW = dL/dW_L, the chain rule in reverse order:  */
+/*   gW += gy_t pq^T;  gpq = W_t^T gy_t;  gu = gW pk;                       */
+/*   gbeta_t = gu . (v_t - a);  gv_t = beta_t gu;                           */
+/*   gpk = gW^T u - W_{t-1}^T (beta_t gu);  gW -= (beta_t gu) pk^T;         */
+/* then through phi: with p the unnormalised products and s their sum,      */
+/* phi = p/(s+eps): gp_l = gphi_l/(s+eps) - (gphi . p)/(s+eps)^2;           */
+/* p_{(i-1)n+j} = x_j x_{(j-i) mod n} sends gp to x_j and x_{(j-i) mod n};  */
+/* x = ReLU([k, -k]) sends gx_j to k_j (k_j > 0) and -gx_{d_key+j} to k_j   */
+/* (-k_j > 0).  gW after token 1 is dL/dW_0.                                */
+/* ---------------------------------------------------------------------- */
+static void dpfp_backward_one(const double *k, const double *gphi, double *gk, double *x, double *p,
+                              int d_key, int nu, double eps)
+{
+    const int n = 2 * d_key;
+    const int d_dot = n * nu;
+    for (int j = 0; j < d_key; ++j) {
+        x[j] = k[j] > 0.0 ? k[j] : 0.0;
+        x[d_key + j] = -k[j] > 0.0 ? -k[j] : 0.0;
+    }
+    double s = 0.0;
+    for (int i = 1; i <= nu; ++i)
+        for (int j = 0; j < n; ++j) {
+            p[(size_t)(i - 1) * n + j] = x[j] * x[((j - i) % n + n) % n];
+            s += p[(size_t)(i - 1) * n + j];
+        }
+    double gp_dot_p = 0.0;
+    for (int m = 0; m < d_dot; ++m)
+        gp_dot_p += gphi[m] * p[m];
+    double *gx = (double *)calloc((size_t)n, sizeof(double));
+    for (int i = 1; i <= nu; ++i)
+        for (int j = 0; j < n; ++j) {
+            const int m = (i - 1) * n + j, src = ((j - i) % n + n) % n;
+            const double gp = gphi[m] / (s + eps) - gp_dot_p / ((s + eps) * (s + eps));
+            gx[j] += gp * x[src];
+            gx[src] += gp * x[j];
+        }
+    for (int j = 0; j < d_key; ++j)
+        gk[j] = (k[j] > 0.0 ? gx[j] : 0.0) - (-k[j] > 0.0 ? gx[d_key + j] : 0.0);
+    free(gx);
+}
+
+static void backward_one(const double *q, const double *k, const double *v, const double *beta, const double *W0,
+                         const double *gy, const double *gWL, double *gq, double *gk, double *gv, double *gbeta,
+                         double *gW0, int64_t L, int d_key, int nu, int d_v, double eps)
+{
+    const int d_dot = 2 * d_key * nu;
+    const size_t wsz = (size_t)d_v * d_dot;
+    /* the forward, keeping W_0 .. W_L, phi(k_t), phi(q_t) and a_t = W_{t-1} phi(k_t) */
+    double *Ws = (double *)malloc(sizeof(double) * wsz * (size_t)(L + 1));
+    double *pk = (double *)malloc(sizeof(double) * d_dot * (size_t)(L > 0 ? L : 1));
+    double *pq = (double *)malloc(sizeof(double) * d_dot * (size_t)(L > 0 ? L : 1));
+    double *a = (double *)malloc(sizeof(double) * d_v * (size_t)(L > 0 ? L : 1));
+    double *x = (double *)malloc(sizeof(double) * 2 * d_key);
+    double *p = (double *)malloc(sizeof(double) * d_dot);
+    for (size_t e = 0; e < wsz; ++e)
+        Ws[e] = W0 ? W0[e] : 0.0;
+    for (int64_t t = 0; t < L; ++t) {
+        double *Wp = Ws + (size_t)t * wsz, *Wn = Ws + (size_t)(t + 1) * wsz;
+        dpfp_one(k + t * d_key, pk + t * d_dot, x, d_key, nu, eps);
+        dpfp_one(q + t * d_key, pq + t * d_dot, x, d_key, nu, eps);
+        for (int r = 0; r < d_v; ++r) {
+            double acc = 0.0;
+            for (int m = 0; m < d_dot; ++m)
+                acc += Wp[(size_t)r * d_dot + m] * pk[t * d_dot + m];
+            a[t * d_v + r] = acc;
+        }
+        for (int r = 0; r < d_v; ++r) {
+            const double u = beta[t] * (v[t * d_v + r] - a[t * d_v + r]);
+            for (int m = 0; m < d_dot; ++m)
+                Wn[(size_t)r * d_dot + m] = Wp[(size_t)r * d_dot + m] + u * pk[t * d_dot + m];
+        }
+    }
+    /* the reverse sweep */
+    double *gW = (double *)malloc(sizeof(double) * wsz);
+    double *gu = (double *)malloc(sizeof(double) * d_v);
+    double *gpq = (double *)malloc(sizeof(double) * d_dot);
+    double *gpk = (double *)malloc(sizeof(double) * d_dot);
+    for (size_t e = 0; e < wsz; ++e)
+        gW[e] = gWL ? gWL[e] : 0.0;
+    for (int64_t t = L - 1; t >= 0; --t) {
+        const double *Wp = Ws + (size_t)t * wsz, *Wn = Ws + (size_t)(t + 1) * wsz;
+        const double *pkt = pk + t * d_dot, *pqt = pq + t * d_dot;
+        /* y_t = W_t pq */
+        for (int r = 0; r < d_v; ++r)
+            for (int m = 0; m < d_dot; ++m)
+                gW[(size_t)r * d_dot + m] += gy[t * d_v + r] * pqt[m];
+        for (int m = 0; m < d_dot; ++m) {
+            double acc = 0.0;
+            for (int r = 0; r < d_v; ++r)
+                acc += Wn[(size_t)r * d_dot + m] * gy[t * d_v + r];
+            gpq[m] = acc;
+        }
+        /* W_t = W_{t-1} + u pk^T */
+        for (int r = 0; r < d_v; ++r) {
+            double acc = 0.0;
+            for (int m = 0; m < d_dot; ++m)
+                acc += gW[(size_t)r * d_dot + m] * pkt[m];
+            gu[r] = acc;
+        }
+        double gb = 0.0;
+        for (int r = 0; r < d_v; ++r)
+            gb += gu[r] * (v[t * d_v + r] - a[t * d_v + r]);
+        gbeta[t] = gb;
+        for (int r = 0; r < d_v; ++r)
+            gv[t * d_v + r] = beta[t] * gu[r];
+        for (int m = 0; m < d_dot; ++m) {
+            double acc = 0.0;
+            for (int r = 0; r < d_v; ++r) {
+                const double u = beta[t] * (v[t * d_v + r] - a[t * d_v + r]);
+                acc += gW[(size_t)r * d_dot + m] * u - Wp[(size_t)r * d_dot + m] * beta[t] * gu[r];
+            }
+            gpk[m] = acc;
+        }
+        for (int r = 0; r < d_v; ++r)
+            for (int m = 0; m < d_dot; ++m)
+                gW[(size_t)r * d_dot + m] -= beta[t] * gu[r] * pkt[m];
+        dpfp_backward_one(q + t * d_key, gpq, gq + t * d_key, x, p, d_key, nu, eps);
+        dpfp_backward_one(k + t * d_key, gpk, gk + t * d_key, x, p, d_key, nu, eps);
+    }
+    if (gW0)
+        memcpy(gW0, gW, sizeof(double) * wsz);
+    free(Ws); free(pk); free(pq); free(a); free(x); free(p);
+    free(gW); free(gu); free(gpq); free(gpk);
+}
+
+typedef struct {
+    const double *q, *k, *v, *beta, *W0, *gy, *gWL;
+    double *gq, *gk, *gv, *gbeta, *gW0;
+    int64_t L;
+    int d_key, nu, d_v;
+    double eps;
+    int64_t first, last;
+} bjob_t;
+
+static void *run_bjob(void *arg)
+{
+    bjob_t *j = (bjob_t *)arg;
+    const int d_dot = 2 * j->d_key * j->nu;
+    const size_t wsz = (size_t)j->d_v * d_dot;
+    for (int64_t bh = j->first; bh < j->last; ++bh)
+        backward_one(j->q + bh * j->L * j->d_key, j->k + bh * j->L * j->d_key, j->v + bh * j->L * j->d_v,
+                     j->beta + bh * j->L, j->W0 ? j->W0 + bh * wsz : NULL, j->gy + bh * j->L * j->d_v,
+                     j->gWL ? j->gWL + bh * wsz : NULL, j->gq + bh * j->L * j->d_key, j->gk + bh * j->L * j->d_key,
+                     j->gv + bh * j->L * j->d_v, j->gbeta + bh * j->L, j->gW0 ? j->gW0 + bh * wsz : NULL, j->L,
+                     j->d_key, j->nu, j->d_v, j->eps);
+    return NULL;
+}
+
+/* Gradients of L = sum(gy * y) + sum(gWL * W_final) with respect to q, k, v,
+ * beta and W0, for the forward fwo_delta_forward computes.  gWL and W0 may
+ * be NULL (zeros); gW0 may be NULL (not returned). */
+int fwo_delta_backward(const double *q, const double *k, const double *v, const double *beta, const double *W0,
+                       const double *gy, const double *gWL, double *gq, double *gk, double *gv, double *gbeta,
+                       double *gW0, int64_t B, int64_t H, int64_t L, int d_key, int nu, int d_v, double eps,
+                       int nthreads)
+{
+    if (!q || !k || !v || !beta || !gy || !gq || !gk || !gv || !gbeta || B < 0 || H < 0 || L < 0 ||
+        d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * d_key - 1)
+        return FWO_BAD_ARG;
+    const int64_t BH = B * H;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > BH)
+        nthreads = BH > 0 ? (int)BH : 1;
+    bjob_t *jobs = (bjob_t *)calloc((size_t)nthreads, sizeof(bjob_t));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    for (int i = 0; i < nthreads; ++i) {
+        bjob_t *j = &jobs[i];
+        j->q = q; j->k = k; j->v = v; j->beta = beta; j->W0 = W0; j->gy = gy; j->gWL = gWL;
+        j->gq = gq; j->gk = gk; j->gv = gv; j->gbeta = gbeta; j->gW0 = gW0; j->L = L;
+        j->d_key = d_key; j->nu = nu; j->d_v = d_v; j->eps = eps;
+        j->first = BH * i / nthreads;
+        j->last = BH * (i + 1) / nthreads;
+    }
+    if (nthreads == 1) {
+        run_bjob(&jobs[0]);
+    } else {
+        for (int i = 0; i < nthreads; ++i)
+            pthread_create(&tids[i], NULL, run_bjob, &jobs[i]);
         for (int i = 0; i < nthreads; ++i)
             pthread_join(tids[i], NULL);
     }

@@ -251,6 +251,64 @@ def pin_decode_stepped_equals_forward(o):
     assert np.allclose(Ws, W, rtol=1e-13, atol=1e-15)
 
 
+# ---------------------------------------------------------------- backward
+def _fd_loss(o, q, k, v, beta, W0, gy, gW, nu):
+    y, Wf = o.delta_forward(q, k, v, beta, W0, nu, 1e-6)
+    return float((gy * y).sum() + (gW * Wf).sum())
+
+
+def pin_backward_finite_differences(o):
+    """Every gradient of the backward (q, k, v, beta, W0) equals the central
+    finite difference of L = sum(gy * y) + sum(gW * W_final) through the
+    forward, entry by entry; inputs are kept away from the ReLU kink."""
+    rng = _rng(30)
+    B, H, L, d_key, nu, d_v = 1, 2, 5, 3, 2, 2
+    d_dot = 2 * d_key * nu
+
+    def away(a):
+        return np.sign(a) * (np.abs(a) + 0.2)
+    q, k = away(rng.standard_normal((B, H, L, d_key))), away(rng.standard_normal((B, H, L, d_key)))
+    v = rng.standard_normal((B, H, L, d_v))
+    beta = rng.uniform(0.1, 0.9, (B, H, L))
+    W0 = rng.standard_normal((B, H, d_v, d_dot))
+    gy = rng.standard_normal((B, H, L, d_v))
+    gW = rng.standard_normal((B, H, d_v, d_dot))
+    grads = o.delta_backward(q, k, v, beta, gy, W0, gW, nu, 1e-6)
+    args = [q, k, v, beta, W0]
+    h = 1e-6
+    for which, g in enumerate(grads):
+        x = args[which]
+        for idx in np.ndindex(x.shape):
+            xp, xm = [a.copy() for a in args], [a.copy() for a in args]
+            xp[which][idx] += h
+            xm[which][idx] -= h
+            fd = (_fd_loss(o, *xp, gy, gW, nu) - _fd_loss(o, *xm, gy, gW, nu)) / (2 * h)
+            assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(fd)), (which, idx, fd, g[idx])
+
+
+def pin_backward_special_cases(o):
+    """beta = 0: the state never changes, so gv = 0, gk = 0, gW0 = the summed
+    read-out gradients plus gW, and gq is the plain read-out gradient; the
+    backward is linear in (gy, gW)."""
+    rng = _rng(31)
+    B, H, L, d_key, nu, d_v = 2, 1, 6, 4, 1, 3
+    d_dot = 2 * d_key * nu
+    q, k = rng.standard_normal((B, H, L, d_key)), rng.standard_normal((B, H, L, d_key))
+    v = rng.standard_normal((B, H, L, d_v))
+    W0 = rng.standard_normal((B, H, d_v, d_dot))
+    gy = rng.standard_normal((B, H, L, d_v))
+    gW = rng.standard_normal((B, H, d_v, d_dot))
+    gq, gk, gv, gb, gW0 = o.delta_backward(q, k, v, np.zeros((B, H, L)), gy, W0, gW, nu, 1e-6)
+    pq = o.dpfp(q, nu, 1e-6)
+    assert np.allclose(gv, 0.0) and np.allclose(gk, 0.0)
+    assert np.allclose(gW0, gW + np.einsum("bhtv,bhtd->bhvd", gy, pq), rtol=1e-12, atol=1e-12)
+    beta = rng.uniform(0, 1, (B, H, L))
+    g1 = o.delta_backward(q, k, v, beta, gy, W0, gW, nu, 1e-6)
+    g2 = o.delta_backward(q, k, v, beta, 2 * gy, W0, 2 * gW, nu, 1e-6)
+    for x1, x2 in zip(g1, g2):
+        assert np.allclose(x2, 2 * x1, rtol=1e-12, atol=1e-13)
+
+
 # ------------------------------------------------- sum rule (linear attention)
 def _attention_form(o, q, k, v, W0, z0, nu, normalize):
     """The kernel-attention form the sum rule is the recurrence of (the
@@ -325,5 +383,5 @@ ALL_PINS = [
     pin_recurrence_hand, pin_beta_zero, pin_one_step_closed_form, pin_linearity,
     pin_value_channel_permutation, pin_contraction_bound, pin_one_hot_recall,
     pin_decode_stepped_equals_forward, pin_linear_attention_form, pin_linear_first_token_and_convexity,
-    pin_linear_zero_denominator,
+    pin_linear_zero_denominator, pin_backward_finite_differences, pin_backward_special_cases,
 ]

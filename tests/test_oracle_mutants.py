@@ -44,6 +44,16 @@ MUTANTS = {
     "sum_rule_read_before_write": ("        for (int m = 0; m < d_dot; ++m)\n            z[m] += pk[m];\n",
                                    "        for (int m = 0; m < d_dot; ++m)\n            z[m] += 0.0 * pk[m];\n"),
     "sum_rule_initial_z_ignored": ("z[m] = j->z0 ? j->z0[bh * d_dot + m] : 0.0;", "z[m] = 0.0;"),
+    # the backward
+    "backward_state_sign": ("gW[(size_t)r * d_dot + m] -= beta[t] * gu[r] * pkt[m];",
+                            "gW[(size_t)r * d_dot + m] += beta[t] * gu[r] * pkt[m];"),
+    "backward_key_drops_retrieve": ("acc += gW[(size_t)r * d_dot + m] * u - Wp[(size_t)r * d_dot + m] * beta[t] * gu[r];",
+                                    "acc += gW[(size_t)r * d_dot + m] * u;"),
+    "backward_query_with_old_state": ("acc += Wn[(size_t)r * d_dot + m] * gy[t * d_v + r];",
+                                      "acc += Wp[(size_t)r * d_dot + m] * gy[t * d_v + r];"),
+    "backward_normaliser_term_dropped": ("const double gp = gphi[m] / (s + eps) - gp_dot_p / ((s + eps) * (s + eps));",
+                                         "const double gp = gphi[m] / (s + eps);"),
+    "backward_roll_partner_dropped": ("            gx[src] += gp * x[j];\n", "\n"),
 }
 
 
