@@ -427,6 +427,22 @@ def measure_rows(fw, inputs, dev, stream, pk):
     r = roofline("fw_linear_forward (prepare + scan)", flops, nbytes, ms, pk)
     r["tokens/s"] = B * L / (ms * 1e-3)
     rows["linear_b4h8_l512_normalised"] = r
+    # the backward of the delta rule on the bench workload (dq, dk, dv, dbeta, dW0 from dy)
+    c = inputs.FORWARD_CONFIGS["b4h8_l512"]
+    B, H, L, d_key, nu, d_v = (c[n] for n in ("B", "H", "L", "d_key", "nu", "d_v"))
+    d_dot = 2 * d_key * nu
+    fi = {k: (None if v is None else v.to(dev)) for k, v in inputs.forward_inputs("b4h8_l512").items()}
+    dyb = torch.randn(B, H, L, d_v, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16).to(dev)
+    nws = fw.fw_delta_backward_workspace_size(B, H, L, d_key, nu, d_v, torch.bfloat16)
+    wsb = torch.empty(nws, dtype=torch.uint8, device=dev)
+    ms = _time(lambda i: fw.fw_delta_backward(fi["q"], fi["k"], fi["v"], fi["beta"], dyb, nu=nu, workspace=wsb,
+                                              stream=stream), 20, stream)
+    # per head-token: the forward sweep (2 d_dot d_v) and the reverse sweep (about 12 d_dot d_v) in fp32
+    flops = 14.0 * d_dot * d_v * B * H * L
+    nbytes = B * H * L * 2 * (2 * 2 * d_key + 2 * 2 * d_v + 2) + B * H * d_v * d_dot * 4
+    r = roofline("fw_delta_backward (fp32, token-serial)", flops, nbytes, ms, pk)
+    r["tokens/s"] = B * L / (ms * 1e-3)
+    rows["backward_b4h8_l512"] = r
     return rows
 
 

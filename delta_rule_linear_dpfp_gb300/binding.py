@@ -26,7 +26,8 @@ FW_DTYPE_BF16 = 1
 EXPORTS = ("fw_status_string", "fw_dpfp", "fw_delta_forward_workspace_size", "fw_delta_forward",
            "fw_delta_decode_step", "fw_device_status", "fw_selftest_umma",
            "fw_delta_forward_noalloc", "fw_delta_forward_prepare", "fw_delta_forward_scan",
-           "fw_selftest_wait_timeout", "fw_linear_forward_workspace_size", "fw_linear_forward")
+           "fw_selftest_wait_timeout", "fw_linear_forward_workspace_size", "fw_linear_forward",
+           "fw_delta_backward_workspace_size", "fw_delta_backward")
 
 #: bytes of the library's own scratch array behind fw_delta_forward_noalloc
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -79,6 +80,10 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.fw_linear_forward_workspace_size.argtypes = [i32] * 9
     lib.fw_linear_forward.restype = i32
     lib.fw_linear_forward.argtypes = [vp] * 9 + [sz] + [i32] * 9 + [f32, vp]
+    lib.fw_delta_backward_workspace_size.restype = sz
+    lib.fw_delta_backward_workspace_size.argtypes = [i32] * 7
+    lib.fw_delta_backward.restype = i32
+    lib.fw_delta_backward.argtypes = [vp] * 13 + [sz] + [i32] * 7 + [f32, vp]
     lib.fw_selftest_umma.restype = i32
     lib.fw_selftest_umma.argtypes = [vp, vp, vp] + [i32] * 5 + [vp]
     if path is None:
@@ -202,6 +207,43 @@ def fw_delta_forward_scan(workspace, y, W0=None, W_final=None, nu: int = 1, chun
                                       _stream(stream))
     _check(rc, "fw_delta_forward_scan")
     return y, W_final
+
+
+def fw_delta_backward_workspace_size(B, H, L, d_key, nu, d_v, io_dtype) -> int:
+    code = io_dtype if isinstance(io_dtype, int) else _dtype_code(io_dtype)
+    return int(load().fw_delta_backward_workspace_size(B, H, L, d_key, nu, d_v, code))
+
+
+def fw_delta_backward(q, k, v, beta, dy, W0=None, dW_final=None, nu: int = 1, eps: float = 1e-6,
+                      return_dW0: bool = True, workspace=None, stream=None):
+    """Gradients of the delta-rule forward: given dy [B,H,L,d_v] (and dW_final),
+    returns (dq, dk, dv, dbeta, dW0 or None)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("dy", dy)):
+        _dev(t, name)
+    B, H, L, d_key = q.shape
+    d_v = v.shape[-1]
+    d_dot = 2 * d_key * nu
+    if k.shape != q.shape or v.shape != (B, H, L, d_v) or beta.shape != (B, H, L) or dy.shape != v.shape:
+        raise ValueError("shape mismatch among q, k, v, beta, dy")
+    if not (q.dtype == k.dtype == v.dtype == beta.dtype == dy.dtype):
+        raise ValueError("q, k, v, beta, dy must share the I/O dtype")
+    for name, t in (("W0", W0), ("dW_final", dW_final)):
+        if t is not None:
+            _dev(t, name)
+            if t.dtype != torch.float32 or tuple(t.shape) != (B, H, d_v, d_dot):
+                raise ValueError(f"{name} must be fp32 [B,H,d_v,d_dot]")
+    dq, dk, dv, dbeta = (torch.empty_like(t) for t in (q, k, v, beta))
+    dW0 = torch.empty(B, H, d_v, d_dot, dtype=torch.float32, device=q.device) if return_dW0 else None
+    code = _dtype_code(q.dtype)
+    need = fw_delta_backward_workspace_size(B, H, L, d_key, nu, d_v, code)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().fw_delta_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(W0), _ptr(dy), _ptr(dW_final),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dW0), _ptr(workspace), ws_bytes,
+                                  B, H, L, d_key, nu, d_v, code, eps, _stream(stream))
+    _check(rc, "fw_delta_backward")
+    return dq, dk, dv, dbeta, dW0
 
 
 def fw_linear_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk, normalize=True,

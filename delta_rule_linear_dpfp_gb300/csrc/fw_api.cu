@@ -193,6 +193,61 @@ FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const v
 
 namespace {
 
+int check_backward_shape(int B, int H, int L, int d_key, int nu, int d_v, int io_dtype) {
+    if (B < 0 || H < 0 || L < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 || !dtype_ok(io_dtype))
+        return FW_ERR_INVALID_ARG;
+    if (!dkey_supported(d_key) || fw::backward_smem_bytes(d_key, nu, d_v) > (size_t)227 * 1024)
+        return FW_ERR_UNSUPPORTED;
+    return FW_OK;
+}
+
+} // namespace
+
+FW_API size_t fw_delta_backward_workspace_size(int B, int H, int L, int d_key, int nu, int d_v, int io_dtype) {
+    if (check_backward_shape(B, H, L, d_key, nu, d_v, io_dtype) != FW_OK)
+        return 0;
+    return sizeof(float) * (size_t)B * H * L * d_v;
+}
+
+FW_API int fw_delta_backward(const void *q, const void *k, const void *v, const void *beta, const float *W0,
+                             const void *dy, const float *dW_final, void *dq, void *dk, void *dv, void *dbeta,
+                             float *dW0, void *workspace, size_t workspace_bytes, int B, int H, int L, int d_key,
+                             int nu, int d_v, int io_dtype, float eps, void *stream) {
+    if (!eps_ok(eps))
+        return FW_ERR_INVALID_ARG;
+    const int rc = check_backward_shape(B, H, L, d_key, nu, d_v, io_dtype);
+    if (rc != FW_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t BH = (int64_t)B * H;
+    if (BH == 0)
+        return FW_OK;
+    if ((W0 && !aligned16(W0)) || (dW_final && !aligned16(dW_final)) || (dW0 && !aligned16(dW0)))
+        return FW_ERR_INVALID_ARG;
+    if (BH > (int64_t)1 << 30)
+        return FW_ERR_UNSUPPORTED;
+    const int d_dot = 2 * d_key * nu;
+    if (L == 0) { // no token: dL/dW0 = dL/dW_final
+        if (!dW0 || dW0 == dW_final)
+            return FW_OK;
+        const size_t bytes = sizeof(float) * (size_t)BH * d_v * d_dot;
+        return cuda_status(dW_final ? cudaMemcpyAsync(dW0, dW_final, bytes, cudaMemcpyDeviceToDevice, st)
+                                    : cudaMemsetAsync(dW0, 0, bytes, st));
+    }
+    const void *in[] = {q, k, v, beta, dy, dq, dk, dv, dbeta};
+    for (const void *p : in)
+        if (!p || !aligned16(p))
+            return FW_ERR_INVALID_ARG;
+    const size_t need = fw_delta_backward_workspace_size(B, H, L, d_key, nu, d_v, io_dtype);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+        return FW_ERR_INVALID_ARG;
+    return cuda_status(fw::launch_backward(q, k, v, beta, W0, dy, dW_final, dq, dk, dv, dbeta, dW0,
+                                           static_cast<float *>(workspace), (int)BH, L, d_key, nu, d_v,
+                                           io_dtype == FW_DTYPE_BF16, eps, st));
+}
+
+namespace {
+
 int check_linear_shape(int B, int H, int L, int d_key, int nu, int d_v, int chunk, int normalize, int io_dtype) {
     if (B < 0 || H < 0 || L < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 ||
         !dtype_ok(io_dtype) || !(chunk == 16 || chunk == 32 || chunk == 64) || (normalize != 0 && normalize != 1))

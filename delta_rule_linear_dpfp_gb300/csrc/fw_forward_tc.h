@@ -40,4 +40,13 @@ cudaError_t tc_linear_launch(const void *q, const void *k, const void *v, const 
                              int d_key, int nu, int d_v, int chunk, int normalize, float eps, int num_sms,
                              unsigned *status, cudaStream_t st);
 
+// The backward of the delta rule (fp32 arithmetic, fp32 or bf16 I/O): one
+// CTA per (b,h) with W and its gradient in shared memory.  scratch holds u_t
+// for every token (BH * L * d_v floats).  Arguments validated by the caller.
+size_t backward_smem_bytes(int d_key, int nu, int d_v);
+cudaError_t launch_backward(const void *q, const void *k, const void *v, const void *beta, const float *W0,
+                            const void *gy, const float *gWL, void *gq, void *gk, void *gv, void *gbeta,
+                            float *gW0, float *scratch, int BH, int L, int d_key, int nu, int d_v, int bf16,
+                            float eps, cudaStream_t st);
+
 } // namespace fw

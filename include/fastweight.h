@@ -140,6 +140,42 @@ FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const v
                             int d_v, int chunk, int io_dtype, float eps, void *stream);
 
 /*
+ * Bytes of device workspace fw_delta_backward needs for this shape (0 for
+ * arguments it would reject).  The caller allocates it.
+ */
+FW_API size_t fw_delta_backward_workspace_size(int B, int H, int L, int d_key, int nu, int d_v,
+                                               int io_dtype);
+
+/*
+ * fw_delta_backward -- gradients of the delta-rule forward (fw_delta_forward,
+ * any chunk: the result does not depend on it) with respect to q, k, v, beta
+ * and the initial state, given the gradients of y and of the final state.
+ * [The chain rule applied in reverse token order to the recurrence of the
+ * Fast Weights Transformer guide, section "FastWeightsAttention: the new
+ * update rule", and through its DPFP map; the pages print no backward, the
+ * guide trains through the loop with autograd.]
+ *
+ *   q, k, v, beta : as for fw_delta_forward                 (read)
+ *   W0       : [B, H, d_v, d_dot] fp32 initial state, or NULL for zeros
+ *   dy       : [B, H, L, d_v]     io_dtype, dL/dy           (read)
+ *   dW_final : [B, H, d_v, d_dot] fp32 dL/dW_final, or NULL for zeros
+ *   dq, dk   : [B, H, L, d_key]   io_dtype                  (written)
+ *   dv       : [B, H, L, d_v]     io_dtype                  (written)
+ *   dbeta    : [B, H, L]          io_dtype                  (written)
+ *   dW0      : [B, H, d_v, d_dot] fp32 dL/dW0, or NULL to skip it
+ *   workspace: device scratch of fw_delta_backward_workspace_size() bytes
+ * fp32 arithmetic on CUDA cores for both I/O dtypes, one CTA per (batch,
+ * head) with the state and its gradient in shared memory, so
+ * 8 * d_v * d_dot bytes must fit a CTA's shared memory (about 220 KB).
+ * Errors as for fw_delta_forward; FW_ERR_UNSUPPORTED for larger states.
+ */
+FW_API int fw_delta_backward(const void *q, const void *k, const void *v, const void *beta,
+                             const float *W0, const void *dy, const float *dW_final, void *dq,
+                             void *dk, void *dv, void *dbeta, float *dW0, void *workspace,
+                             size_t workspace_bytes, int B, int H, int L, int d_key, int nu,
+                             int d_v, int io_dtype, float eps, void *stream);
+
+/*
  * Bytes of device workspace fw_linear_forward needs for this shape (0 for
  * arguments it would reject).  The caller allocates it.
  */
