@@ -32,23 +32,26 @@ namespace {
 constexpr int kBwdThreads = 512;
 constexpr int kBwdWarps = kBwdThreads / 32;
 
-// phi of one row (d_key raw values) by one warp: x = ReLU([k, -k]) into xs,
-// phi into ph.  Block i of phi holds x[j] * x[(j - i) mod n].
-template <typename T>
-FW_DEV void dpfp_warp(const T *src, float *xs, float *ph, int d_key, int nu, float eps, int lane) {
+// phi of one row by one warp from its d_key raw values in shared memory
+// (kr): x = ReLU([k, -k]) into xs, phi into ph.  Block i of phi holds
+// x[j] * x[(j - i) mod n].
+FW_DEV void dpfp_warp(const float *kr, float *xs, float *ph, int d_key, int nu, float eps, int lane) {
     const int n = 2 * d_key, d_dot = n * nu;
     for (int j = lane; j < d_key; j += 32) {
-        const float kv = io<T>::load(src + j);
+        const float kv = kr[j];
         xs[j] = fmaxf(kv, 0.f);
         xs[d_key + j] = fmaxf(-kv, 0.f);
     }
     __syncwarp();
     float s = 0.f;
+    int i = lane / n + 1, j = lane - (i - 1) * n; // m = (i - 1) n + j, stepped by 32
     for (int m = lane; m < d_dot; m += 32) {
-        const int i = m / n + 1, j = m - (i - 1) * n;
-        const float p = xs[j] * xs[(j - i + n) % n];
+        const int src = j - i < 0 ? j - i + n : j - i;
+        const float p = xs[j] * xs[src];
         ph[m] = p;
         s += p;
+        for (j += 32; j >= n; j -= n)
+            ++i;
     }
     s = warp_sum(s);
     const float inv = 1.0f / (s + eps);
@@ -57,45 +60,131 @@ FW_DEV void dpfp_warp(const T *src, float *xs, float *ph, int d_key, int nu, flo
     __syncwarp();
 }
 
-// The DPFP backward of one row by one warp: given g = dL/dphi (shared), the
-// raw row src, writes dL/dk to dst.  xs: scratch of 2 d_key floats.
+// The DPFP backward of one row by one warp: given g = dL/dphi and the raw row
+// kr (both in shared memory), writes dL/dk to dst.  xs: scratch of 2 d_key.
 template <typename T>
-FW_DEV void dpfp_backward_warp(const T *src, const float *g, float *xs, T *dst, int d_key, int nu, float eps,
+FW_DEV void dpfp_backward_warp(const float *kr, const float *g, float *xs, T *dst, int d_key, int nu, float eps,
                                int lane) {
     const int n = 2 * d_key, d_dot = n * nu;
     for (int j = lane; j < d_key; j += 32) {
-        const float kv = io<T>::load(src + j);
+        const float kv = kr[j];
         xs[j] = fmaxf(kv, 0.f);
         xs[d_key + j] = fmaxf(-kv, 0.f);
     }
     __syncwarp();
     float s = 0.f, gp = 0.f; // sum of the products, g . products
+    int i = lane / n + 1, j = lane - (i - 1) * n;
     for (int m = lane; m < d_dot; m += 32) {
-        const int i = m / n + 1, j = m - (i - 1) * n;
-        const float p = xs[j] * xs[(j - i + n) % n];
+        const int src = j - i < 0 ? j - i + n : j - i;
+        const float p = xs[j] * xs[src];
         s += p;
         gp = fmaf(g[m], p, gp);
+        for (j += 32; j >= n; j -= n)
+            ++i;
     }
     s = warp_sum(s);
     gp = warp_sum(gp);
     const float c1 = 1.0f / (s + eps), c2 = gp * c1 * c1; // d phi_m / d p_l = delta_ml c1 - p_m c1^2
-    for (int j = lane; j < d_key; j += 32) {
+    for (int j0 = lane; j0 < d_key; j0 += 32) {
         float gx[2] = {0.f, 0.f};
 #pragma unroll
-        for (int h = 0; h < 2; ++h) { // x[j] (from k) and x[d_key + j] (from -k)
-            const int jj = j + h * d_key;
-            for (int i = 1; i <= nu; ++i) {
-                const int lo = (jj - i + n) % n, hi = (jj + i) % n;
-                // x[jj] is the left factor of product (i, jj) and the rolled
-                // factor of product (i, jj + i)
-                gx[h] = fmaf(g[(i - 1) * n + jj] * c1 - c2, xs[lo], gx[h]);
-                gx[h] = fmaf(g[(i - 1) * n + hi] * c1 - c2, xs[hi], gx[h]);
+        for (int h = 0; h < 2; ++h) { // x[j0] (from k) and x[d_key + j0] (from -k)
+            const int jj = j0 + h * d_key;
+            for (int ii = 1; ii <= nu; ++ii) {
+                const int lo = jj - ii < 0 ? jj - ii + n : jj - ii, hi = jj + ii >= n ? jj + ii - n : jj + ii;
+                // x[jj] is the left factor of product (ii, jj) and the rolled
+                // factor of product (ii, jj + ii)
+                gx[h] = fmaf(g[(ii - 1) * n + jj] * c1 - c2, xs[lo], gx[h]);
+                gx[h] = fmaf(g[(ii - 1) * n + hi] * c1 - c2, xs[hi], gx[h]);
             }
         }
-        const float kv = io<T>::load(src + j);
-        io<T>::store(dst + j, (kv > 0.f ? gx[0] : 0.f) - (kv < 0.f ? gx[1] : 0.f));
+        const float kv = kr[j0];
+        io<T>::store(dst + j0, (kv > 0.f ? gx[0] : 0.f) - (kv < 0.f ? gx[1] : 0.f));
     }
     __syncwarp();
+}
+
+// f(e, r, m) for the elements e = r * d_dot + m this thread owns (e = tid,
+// tid + 512, ...), with (r, m) stepped without a division per element.
+template <typename F>
+FW_DEV void for_elements(int nel, int d_dot, int tid, F f) {
+    const int dr = kBwdThreads / d_dot, dm = kBwdThreads - dr * d_dot;
+    int r = tid / d_dot, m = tid - r * d_dot;
+    for (int e = tid; e < nel; e += kBwdThreads) {
+        f(e, r, m);
+        r += dr;
+        m += dm;
+        if (m >= d_dot) {
+            m -= d_dot;
+            ++r;
+        }
+    }
+}
+
+// Row dot products x[r] = A[r] . p (and y[r] = B[r] . p when B is given)
+// for every row: warp w takes rows w, w + 16, ... (up to 8 per warp); the
+// lanes stride the columns and the rows' sums are reduced together.
+FW_DEV void row_dots2(const float *A, const float *B, const float *p, float *x, float *y, int d_v, int d_dot,
+                      int warp, int lane) {
+    constexpr int kMaxRows = 8; // d_v <= 128
+    float sa[kMaxRows], sb[kMaxRows];
+#pragma unroll
+    for (int i = 0; i < kMaxRows; ++i) {
+        sa[i] = 0.f;
+        sb[i] = 0.f;
+    }
+    for (int m = lane; m < d_dot; m += 32) {
+        const float pm = p[m];
+#pragma unroll
+        for (int i = 0; i < kMaxRows; ++i) {
+            const int r = warp + kBwdWarps * i;
+            if (r < d_v) {
+                sa[i] = fmaf(A[r * d_dot + m], pm, sa[i]);
+                if (B)
+                    sb[i] = fmaf(B[r * d_dot + m], pm, sb[i]);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int i = 0; i < kMaxRows; ++i) {
+            sa[i] += __shfl_xor_sync(0xffffffffu, sa[i], o);
+            sb[i] += __shfl_xor_sync(0xffffffffu, sb[i], o);
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < kMaxRows; ++i) {
+            const int r = warp + kBwdWarps * i;
+            if (r < d_v) {
+                x[r] = sa[i];
+                if (B)
+                    y[r] = sb[i];
+            }
+        }
+    }
+}
+
+// Sum over the d_v rows of a[r][m] * b[r] (plus c[r][m] * d[r] when c is
+// given) for column m: four independent accumulators.
+FW_DEV float col_sum(const float *a, const float *b, const float *c, const float *d, int m, int d_v, int d_dot) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int r = 0;
+    for (; r + 4 <= d_v; r += 4) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc[e] = fmaf(a[(r + e) * d_dot + m], b[r + e], acc[e]);
+            if (c)
+                acc[e] = fmaf(c[(r + e) * d_dot + m], d[r + e], acc[e]);
+        }
+    }
+    for (; r < d_v; ++r) {
+        acc[0] = fmaf(a[r * d_dot + m], b[r], acc[0]);
+        if (c)
+            acc[0] = fmaf(c[r * d_dot + m], d[r], acc[0]);
+    }
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
 template <typename T>
@@ -108,20 +197,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     extern __shared__ float sm[];
     const int d_dot = 2 * d_key * nu, n = 2 * d_key;
     const int nel = d_v * d_dot;
+    // one token's inputs, staged: k, q (d_key each), v, gy, u (d_v each), beta
+    const int ntok = 2 * d_key + 3 * d_v + 1;
     float *W = sm;                 // [d_v][d_dot] the state W_t
     float *G = W + nel;            // [d_v][d_dot] dL/dW_t
     float *pk = G + nel;           // phi(k_t)
     float *pq = pk + d_dot;        // phi(q_t)
     float *gpq = pq + d_dot;       // dL/dphi(q_t)
     float *gpk = gpq + d_dot;      // dL/dphi(k_t)
-    float *gyv = gpk + d_dot;      // gy_t
-    float *vv = gyv + d_v;         // v_t
-    float *uu = vv + d_v;          // u_t
-    float *gu = uu + d_v;          // dL/du_t, then beta_t dL/du_t
+    float *gu = gpk + d_dot;       // dL/du_t, then beta_t dL/du_t
     float *aa = gu + d_v;          // W_{t-1} phi(k_t)
     float *xk = aa + d_v;          // x of k_t (one warp's scratch)
     float *xq = xk + n;            // x of q_t
-    float *sc = xq + n;            // scalars: [0] beta_t
+    float *stg = xq + n;           // [2][ntok] staged token inputs (double-buffered)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t bh = blockIdx.x;
@@ -129,113 +217,119 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const T *gyb = gy + bh * L * d_v;
     float *ub = us + bh * L * d_v;
 
+    // Thread tid loads entries tid and tid + 512 of token t's staged vector
+    // into registers; they are stored to shared memory one phase later, so
+    // the load latency hides behind the current token's work.
+    auto fetch = [&](int t, bool reverse, float (&r)[2]) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int e = tid + h * kBwdThreads;
+            float x = 0.f;
+            if (t >= 0 && t < L && e < ntok) {
+                if (e < d_key)
+                    x = io<T>::load(kb + (int64_t)t * d_key + e);
+                else if (e < 2 * d_key)
+                    x = reverse ? io<T>::load(qb + (int64_t)t * d_key + e - d_key) : 0.f;
+                else if (e < 2 * d_key + d_v)
+                    x = io<T>::load(vb + (int64_t)t * d_v + e - 2 * d_key);
+                else if (e < 2 * d_key + 2 * d_v)
+                    x = reverse ? io<T>::load(gyb + (int64_t)t * d_v + e - 2 * d_key - d_v) : 0.f;
+                else if (e < 2 * d_key + 3 * d_v)
+                    x = reverse ? ub[(int64_t)t * d_v + e - 2 * d_key - 2 * d_v] : 0.f;
+                else
+                    x = io<T>::load(bb + t);
+            }
+            r[h] = x;
+        }
+    };
+    auto stage = [&](int t, const float (&r)[2]) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int e = tid + h * kBwdThreads;
+            if (e < ntok)
+                stg[(t & 1) * ntok + e] = r[h];
+        }
+    };
+
     griddep_launch_dependents();
     griddep_wait();
     for (int e = tid; e < nel; e += kBwdThreads) {
         W[e] = W0 ? W0[bh * nel + e] : 0.f;
         G[e] = gWL ? gWL[bh * nel + e] : 0.f;
     }
+    float nxt[2];
     // ---- forward sweep: keep u_t
+    fetch(0, false, nxt);
+    stage(0, nxt);
     for (int t = 0; t < L; ++t) {
+        fetch(t + 1, false, nxt);
+        const float *tk = stg + (t & 1) * ntok, *tv = tk + 2 * d_key;
         __syncthreads();
         if (warp == 0)
-            dpfp_warp(kb + (int64_t)t * d_key, xk, pk, d_key, nu, eps, lane);
-        else if (warp == 1) {
-            for (int r = lane; r < d_v; r += 32)
-                vv[r] = io<T>::load(vb + (int64_t)t * d_v + r);
-            if (lane == 0)
-                sc[0] = io<T>::load(bb + t);
+            dpfp_warp(tk, xk, pk, d_key, nu, eps, lane);
+        __syncthreads();
+        const float bt = tk[ntok - 1];
+        row_dots2(W, nullptr, pk, aa, nullptr, d_v, d_dot, warp, lane); // a = W_{t-1} phi(k)
+        __syncthreads();
+        for (int r = tid; r < d_v; r += kBwdThreads) { // u = beta (v - a)
+            const float u = bt * (tv[r] - aa[r]);
+            gu[r] = u;
+            ub[(int64_t)t * d_v + r] = u;
         }
         __syncthreads();
-        for (int r = warp; r < d_v; r += kBwdWarps) { // a = W_{t-1} phi(k), u = beta (v - a)
-            float acc = 0.f;
-            for (int m = lane; m < d_dot; m += 32)
-                acc = fmaf(W[r * d_dot + m], pk[m], acc);
-            acc = warp_sum(acc);
-            if (lane == 0) {
-                const float u = sc[0] * (vv[r] - acc);
-                uu[r] = u;
-                ub[(int64_t)t * d_v + r] = u;
-            }
-        }
-        __syncthreads();
-        for (int e = tid; e < nel; e += kBwdThreads) // W_t = W_{t-1} + u phi(k)^T
-            W[e] = fmaf(uu[e / d_dot], pk[e % d_dot], W[e]);
+        for_elements(nel, d_dot, tid, [&](int e, int r, int m) { W[e] = fmaf(gu[r], pk[m], W[e]); }); // W_t = W_{t-1} + u phi(k)^T
+        stage(t + 1, nxt);
     }
+    __syncthreads(); // the u_t written above are read back below by other threads
     // ---- reverse sweep
+    fetch(L - 1, true, nxt);
+    __syncthreads();
+    stage(L - 1, nxt);
     for (int t = L - 1; t >= 0; --t) {
+        fetch(t - 1, true, nxt);
+        const float *tk = stg + (t & 1) * ntok, *tq = tk + d_key, *tv = tq + d_key, *tg = tv + d_v, *tu = tg + d_v;
+        const float bt = tk[ntok - 1];
         __syncthreads();
         if (warp == 0)
-            dpfp_warp(kb + (int64_t)t * d_key, xk, pk, d_key, nu, eps, lane);
+            dpfp_warp(tk, xk, pk, d_key, nu, eps, lane);
         else if (warp == 1)
-            dpfp_warp(qb + (int64_t)t * d_key, xq, pq, d_key, nu, eps, lane);
-        else if (warp == 2) {
-            for (int r = lane; r < d_v; r += 32) {
-                gyv[r] = io<T>::load(gyb + (int64_t)t * d_v + r);
-                vv[r] = io<T>::load(vb + (int64_t)t * d_v + r);
-                uu[r] = ub[(int64_t)t * d_v + r];
-            }
-            if (lane == 0)
-                sc[0] = io<T>::load(bb + t);
-        }
+            dpfp_warp(tq, xq, pq, d_key, nu, eps, lane);
         __syncthreads();
-        for (int m = tid; m < d_dot; m += kBwdThreads) { // g_phi(q) = W_t^T gy
-            float acc = 0.f;
-            for (int r = 0; r < d_v; ++r)
-                acc = fmaf(W[r * d_dot + m], gyv[r], acc);
-            gpq[m] = acc;
-        }
+        for (int m = tid; m < d_dot; m += kBwdThreads) // g_phi(q) = W_t^T gy
+            gpq[m] = col_sum(W, tg, nullptr, nullptr, m, d_v, d_dot);
         __syncthreads();
-        for (int e = tid; e < nel; e += kBwdThreads) { // gW += gy phi(q)^T; W_{t-1} = W_t - u phi(k)^T
-            const int r = e / d_dot, m = e - r * d_dot;
-            G[e] = fmaf(gyv[r], pq[m], G[e]);
-            W[e] = fmaf(-uu[r], pk[m], W[e]);
-        }
+        for_elements(nel, d_dot, tid, [&](int e, int r, int m) { // gW += gy phi(q)^T; W_{t-1} = W_t - u phi(k)^T
+            G[e] = fmaf(tg[r], pq[m], G[e]);
+            W[e] = fmaf(-tu[r], pk[m], W[e]);
+        });
         __syncthreads();
-        for (int r = warp; r < d_v; r += kBwdWarps) { // gu = gW phi(k), a = W_{t-1} phi(k)
-            float g = 0.f, a = 0.f;
-            for (int m = lane; m < d_dot; m += 32) {
-                g = fmaf(G[r * d_dot + m], pk[m], g);
-                a = fmaf(W[r * d_dot + m], pk[m], a);
-            }
-            g = warp_sum(g);
-            a = warp_sum(a);
-            if (lane == 0) {
-                gu[r] = g;
-                aa[r] = a;
-            }
-        }
+        row_dots2(G, W, pk, gu, aa, d_v, d_dot, warp, lane); // gu = gW phi(k), a = W_{t-1} phi(k)
         __syncthreads();
-        const float bt = sc[0];
         if (warp == 0) { // gbeta = gu . (v - a)
             float acc = 0.f;
             for (int r = lane; r < d_v; r += 32)
-                acc = fmaf(gu[r], vv[r] - aa[r], acc);
+                acc = fmaf(gu[r], tv[r] - aa[r], acc);
             acc = warp_sum(acc);
             if (lane == 0)
                 io<T>::store(gbeta + bh * L + t, acc);
         }
         __syncthreads();
-        for (int r = tid; r < d_v; r += kBwdThreads) { // gv = beta gu; keep e = beta gu
+        for (int r = tid; r < d_v; r += kBwdThreads) { // gv = beta gu; keep e = beta gu (and -e)
             gu[r] *= bt;
+            aa[r] = -gu[r];
             io<T>::store(gv + (bh * L + t) * d_v + r, gu[r]);
         }
         __syncthreads();
-        for (int m = tid; m < d_dot; m += kBwdThreads) { // g_phi(k) = gW^T u - W_{t-1}^T e
-            float acc = 0.f;
-            for (int r = 0; r < d_v; ++r)
-                acc = fmaf(G[r * d_dot + m], uu[r], fmaf(-W[r * d_dot + m], gu[r], acc));
-            gpk[m] = acc;
-        }
+        for (int m = tid; m < d_dot; m += kBwdThreads) // g_phi(k) = gW^T u - W_{t-1}^T e
+            gpk[m] = col_sum(G, tu, W, aa, m, d_v, d_dot);
         __syncthreads();
-        for (int e = tid; e < nel; e += kBwdThreads) { // gW_{t-1} = gW - e phi(k)^T
-            const int r = e / d_dot, m = e - r * d_dot;
-            G[e] = fmaf(-gu[r], pk[m], G[e]);
-        }
+        for_elements(nel, d_dot, tid, [&](int e, int r, int m) { G[e] = fmaf(-gu[r], pk[m], G[e]); }); // gW_{t-1} = gW - e phi(k)^T
         if (warp == kBwdWarps - 1)
-            dpfp_backward_warp(qb + (int64_t)t * d_key, gpq, xq, gq + (bh * L + t) * d_key, d_key, nu, eps, lane);
+            dpfp_backward_warp(tq, gpq, xq, gq + (bh * L + t) * d_key, d_key, nu, eps, lane);
         else if (warp == kBwdWarps - 2)
-            dpfp_backward_warp(kb + (int64_t)t * d_key, gpk, xk, gk + (bh * L + t) * d_key, d_key, nu, eps, lane);
+            dpfp_backward_warp(tk, gpk, xk, gk + (bh * L + t) * d_key, d_key, nu, eps, lane);
+        if (t > 0)
+            stage(t - 1, nxt);
     }
     __syncthreads();
     if (gW0)
@@ -261,10 +355,11 @@ cudaError_t launch_backward_t(const void *q, const void *k, const void *v, const
 
 } // namespace
 
-// Shared memory of one CTA: W and gW, six vectors, the x scratch, scalars.
+// Shared memory of one CTA: W and gW, four d_dot vectors, two d_v vectors,
+// the x scratch and two staged copies of one token's inputs.
 size_t backward_smem_bytes(int d_key, int nu, int d_v) {
-    const size_t d_dot = (size_t)2 * d_key * nu;
-    return sizeof(float) * (2 * (size_t)d_v * d_dot + 4 * d_dot + 5 * (size_t)d_v + 4 * (size_t)d_key + 8);
+    const size_t d_dot = (size_t)2 * d_key * nu, ntok = 2 * (size_t)d_key + 3 * (size_t)d_v + 1;
+    return sizeof(float) * (2 * (size_t)d_v * d_dot + 4 * d_dot + 2 * (size_t)d_v + 4 * (size_t)d_key + 2 * ntok);
 }
 
 cudaError_t launch_backward(const void *q, const void *k, const void *v, const void *beta, const float *W0,
