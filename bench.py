@@ -392,6 +392,21 @@ def measure_rows(fw, inputs, dev, stream, pk):
     nb = B * H * d_v * d_dot * 4 * 2 + B * H * (2 * d_key + 2 * d_v + 1) * 2
     r = roofline("decode_kernel", B * H * d_v * d_dot * 6.0, nb, ms, pk)
     r["tokens/s"] = B / (ms * 1e-3)
+    # the same 128-step decode as one CUDA graph (each step its own launch inside the graph)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(128):
+            t = i % 8
+            fw.fw_delta_decode_step(dd["q"][t], dd["k"][t], dd["v"][t], dd["beta"][t], W, nu=nu, y=yd)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(4):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    r["graph128_ms_per_step"] = e0.elapsed_time(e1) / (4 * 128)
     rows["decode_b256h16_nu2_dv128"] = r
     # a1-a5 on the long nu = 3 workload with W0 in, W_final out
     name = "b2h8_l2048_nu3"
