@@ -442,6 +442,23 @@ def measure_rows(fw, inputs, dev, stream, pk):
     r = roofline("fw_linear_forward (prepare + scan)", flops, nbytes, ms, pk)
     r["tokens/s"] = B * L / (ms * 1e-3)
     rows["linear_b4h8_l512_normalised"] = r
+    # the projected workload from x: projection prologue (tcgen05 GEMM) + the chunked forward
+    B, H, L, d_model, d_key, d_v, nu, C = 1, 8, 1024, 512, 64, 64, 1, 64
+    d_dot = 2 * d_key * nu
+    lx = inputs.layer_inputs(B, H, L, d_model, d_key, d_v)
+    xp, Wp = lx["x"].to(dev), lx["W_all"].to(dev)
+    yp = torch.empty(B, H, L, d_v, dtype=torch.bfloat16, device=dev)
+    Wfp = torch.empty(B, H, d_v, d_dot, dtype=torch.float32, device=dev)
+    nws = fw.fw_delta_forward_projected_workspace_size(B, L, d_model, H, d_key, nu, d_v, C)
+    wsp = torch.empty(nws, dtype=torch.uint8, device=dev)
+    ms = _time(lambda i: fw.fw_delta_forward_projected(xp, Wp, H, d_key, d_v, nu=nu, chunk=C, y=yp, W_final=Wfp,
+                                                       workspace=wsp, stream=stream), 200, stream)
+    N = H * (2 * d_key + d_v + 1)
+    flops = 2.0 * B * L * d_model * N + forward_flops_per_head_token(C, d_dot, d_v) * B * H * L
+    nbytes = B * L * d_model * 2 + d_model * N * 2 + B * H * L * d_v * 2 + B * H * d_v * d_dot * 4
+    r = roofline("fw_delta_forward_projected (projection + prepare + scan)", flops, nbytes, ms, pk)
+    r["tokens/s"] = B * L / (ms * 1e-3)
+    rows["projected_b1h8_l1024_dmodel512"] = r
     # the backward of the delta rule on the bench workload (dq, dk, dv, dbeta, dW0 from dy)
     c = inputs.FORWARD_CONFIGS["b4h8_l512"]
     B, H, L, d_key, nu, d_v = (c[n] for n in ("B", "H", "L", "d_key", "nu", "d_v"))

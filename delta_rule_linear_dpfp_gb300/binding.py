@@ -27,7 +27,8 @@ EXPORTS = ("fw_status_string", "fw_dpfp", "fw_delta_forward_workspace_size", "fw
            "fw_delta_decode_step", "fw_device_status", "fw_selftest_umma",
            "fw_delta_forward_noalloc", "fw_delta_forward_prepare", "fw_delta_forward_scan",
            "fw_selftest_wait_timeout", "fw_linear_forward_workspace_size", "fw_linear_forward",
-           "fw_delta_backward_workspace_size", "fw_delta_backward")
+           "fw_delta_backward_workspace_size", "fw_delta_backward",
+           "fw_delta_forward_projected_workspace_size", "fw_delta_forward_projected")
 
 #: bytes of the library's own scratch array behind fw_delta_forward_noalloc
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -84,6 +85,10 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.fw_delta_backward_workspace_size.argtypes = [i32] * 7
     lib.fw_delta_backward.restype = i32
     lib.fw_delta_backward.argtypes = [vp] * 13 + [sz] + [i32] * 7 + [f32, vp]
+    lib.fw_delta_forward_projected_workspace_size.restype = sz
+    lib.fw_delta_forward_projected_workspace_size.argtypes = [i32] * 8
+    lib.fw_delta_forward_projected.restype = i32
+    lib.fw_delta_forward_projected.argtypes = [vp, vp, i32, vp, vp, vp, vp, sz] + [i32] * 8 + [f32, vp]
     lib.fw_selftest_umma.restype = i32
     lib.fw_selftest_umma.argtypes = [vp, vp, vp] + [i32] * 5 + [vp]
     if path is None:
@@ -206,6 +211,39 @@ def fw_delta_forward_scan(workspace, y, W0=None, W_final=None, nu: int = 1, chun
                                       _ptr(W0), _ptr(W_final), _ptr(y), B, H, L, d_key, nu, d_v, chunk,
                                       _stream(stream))
     _check(rc, "fw_delta_forward_scan")
+    return y, W_final
+
+
+def fw_delta_forward_projected_workspace_size(B, L, d_model, H, d_key, nu, d_v, chunk) -> int:
+    return int(load().fw_delta_forward_projected_workspace_size(B, L, d_model, H, d_key, nu, d_v, chunk))
+
+
+def fw_delta_forward_projected(x, W_all, H: int, d_key: int, d_v: int, nu: int = 1, chunk: int = 64,
+                               W0=None, eps: float = 1e-6, return_state: bool = True, y=None, W_final=None,
+                               workspace=None, stream=None):
+    """The layer core from x [B,L,d_model] (bf16) and W_all = [W_q | W_k | W_v |
+    W_beta] ([d_model, ldw] bf16, ldw a multiple of 8).  Returns (y, W_final or None)."""
+    _dev(x, "x")
+    _dev(W_all, "W_all")
+    B, L, d_model = x.shape
+    ldw = W_all.shape[1]
+    d_dot = 2 * d_key * nu
+    if W_all.shape[0] != d_model or x.dtype != torch.bfloat16 or W_all.dtype != torch.bfloat16:
+        raise ValueError("x [B,L,d_model] and W_all [d_model, ldw] must be bf16 and agree on d_model")
+    if W0 is not None:
+        _dev(W0, "W0")
+    if y is None:
+        y = torch.empty(B, H, L, d_v, dtype=torch.bfloat16, device=x.device)
+    if W_final is None and return_state:
+        W_final = torch.empty(B, H, d_v, d_dot, dtype=torch.float32, device=x.device)
+    need = fw_delta_forward_projected_workspace_size(B, L, d_model, H, d_key, nu, d_v, chunk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().fw_delta_forward_projected(_ptr(x), _ptr(W_all), ldw, _ptr(W0), _ptr(W_final), _ptr(y),
+                                           _ptr(workspace), ws_bytes, B, L, d_model, H, d_key, nu, d_v, chunk,
+                                           eps, _stream(stream))
+    _check(rc, "fw_delta_forward_projected")
     return y, W_final
 
 

@@ -193,6 +193,82 @@ FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const v
 
 namespace {
 
+// The projected q, k, v, beta inside the workspace, each 256-byte aligned,
+// then the forward's own workspace.
+struct ProjLayout {
+    size_t q, k, v, beta, fwd, bytes;
+};
+ProjLayout proj_layout(int B, int L, int H, int d_key, int d_v, size_t fwd_bytes) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t tok = (size_t)B * H * L;
+    ProjLayout p;
+    p.q = 0;
+    p.k = up(p.q + tok * d_key * 2);
+    p.v = up(p.k + tok * d_key * 2);
+    p.beta = up(p.v + tok * d_v * 2);
+    p.fwd = up(p.beta + tok * 2);
+    p.bytes = p.fwd + fwd_bytes;
+    return p;
+}
+
+} // namespace
+
+FW_API size_t fw_delta_forward_projected_workspace_size(int B, int L, int d_model, int H, int d_key, int nu,
+                                                        int d_v, int chunk) {
+    if (d_model <= 0 || d_model % 64 || H <= 0 || check_forward_shape(B, H, L, d_key, nu, d_v, chunk,
+                                                                      FW_DTYPE_BF16) != FW_OK)
+        return 0;
+    return proj_layout(B, L, H, d_key, d_v, fw::tc_forward_workspace_bytes(B, H, L, d_key, nu, d_v, chunk)).bytes;
+}
+
+FW_API int fw_delta_forward_projected(const void *x, const void *W_all, int ldw, const float *W0, float *W_final,
+                                      void *y, void *workspace, size_t workspace_bytes, int B, int L, int d_model,
+                                      int H, int d_key, int nu, int d_v, int chunk, float eps, void *stream) {
+    if (!eps_ok(eps) || d_model <= 0 || d_model % 64 || H <= 0)
+        return FW_ERR_INVALID_ARG;
+    const int rc = check_forward_shape(B, H, L, d_key, nu, d_v, chunk, FW_DTYPE_BF16);
+    if (rc != FW_OK)
+        return rc;
+    const int64_t N = (int64_t)H * (2 * d_key + d_v + 1);
+    if (ldw % 8 || ldw < (N + 7) / 8 * 8)
+        return FW_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t BH = (int64_t)B * H;
+    if (BH == 0)
+        return FW_OK;
+    if ((W0 && !aligned16(W0)) || (W_final && !aligned16(W_final)))
+        return FW_ERR_INVALID_ARG;
+    if (BH > (int64_t)1 << 30 || (int64_t)B * L > (int64_t)1 << 30 || N > 65535 * 128)
+        return FW_ERR_UNSUPPORTED;
+    const int d_dot = 2 * d_key * nu;
+    if (L == 0) {
+        if (!W_final || W0 == W_final)
+            return FW_OK;
+        const size_t bytes = sizeof(float) * (size_t)BH * d_v * d_dot;
+        return cuda_status(W0 ? cudaMemcpyAsync(W_final, W0, bytes, cudaMemcpyDeviceToDevice, st)
+                              : cudaMemsetAsync(W_final, 0, bytes, st));
+    }
+    if (!x || !W_all || !y || !aligned16(x) || !aligned16(W_all) || !aligned16(y))
+        return FW_ERR_INVALID_ARG;
+    const ProjLayout pl = proj_layout(B, L, H, d_key, d_v, fw::tc_forward_workspace_bytes(B, H, L, d_key, nu, d_v, chunk));
+    if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes)
+        return FW_ERR_INVALID_ARG;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess)
+        return FW_ERR_CUDA;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    e = fw::launch_project(x, W_all, ldw, ws + pl.q, ws + pl.k, ws + pl.v, ws + pl.beta, B, L, H, d_key, d_v, d_model,
+                           di.status, st);
+    if (e != cudaSuccess)
+        return cuda_status(e);
+    e = fw::tc_forward_launch(ws + pl.q, ws + pl.k, ws + pl.v, ws + pl.beta, W0, W_final, y, ws + pl.fwd, B, H, L,
+                              d_key, nu, d_v, chunk, eps, di.num_sms, di.status, st);
+    return cuda_status(e);
+}
+
+namespace {
+
 int check_backward_shape(int B, int H, int L, int d_key, int nu, int d_v, int io_dtype) {
     if (B < 0 || H < 0 || L < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 || !dtype_ok(io_dtype))
         return FW_ERR_INVALID_ARG;

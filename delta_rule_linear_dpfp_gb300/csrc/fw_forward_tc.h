@@ -49,4 +49,12 @@ cudaError_t launch_backward(const void *q, const void *k, const void *v, const v
                             float *gW0, float *scratch, int BH, int L, int d_key, int nu, int d_v, int bf16,
                             float eps, cudaStream_t st);
 
+// The projection prologue: q, k, v, beta (bf16, [B,H,L,*]) = x [B*L, d_model]
+// times W_all = [W_q | W_k | W_v | W_beta] ([d_model, ldw], the first
+// N = H (2 d_key + d_v + 1) columns used; beta through the sigmoid), on
+// tcgen05.  d_model % 64 == 0, ldw % 8 == 0, ldw >= N rounded up to 8.
+size_t project_smem_bytes();
+cudaError_t launch_project(const void *x, const void *Wall, int ldw, void *q, void *k, void *v, void *beta, int B,
+                           int L, int H, int d_key, int d_v, int d_model, unsigned *status, cudaStream_t st);
+
 } // namespace fw

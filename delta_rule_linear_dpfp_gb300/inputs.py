@@ -118,6 +118,24 @@ def projected_inputs(B, H, L, d_model, nu, io="bf16", seed=0):
                 beta=beta.to(dt).contiguous(), W0=None)
 
 
+def layer_inputs(B, H, L, d_model, d_key, d_v, nu=1, w0_var=None, seed=0):
+    """Token activations and the four projection matrices side by side, for
+    the forward from x: x ~ N(0,1) [B,L,d_model]; W_all = [W_q | W_k | W_v |
+    W_beta] ~ N(0, 1/d_model) with H*d_key, H*d_key, H*d_v and H columns,
+    padded with zero columns to a multiple of 8 (ldw); both rounded once to
+    bf16.  Optional W0 ~ N(0, w0_var) fp32.  Draw order: x, W_all, W0."""
+    g = _gen(seed)
+    N = H * (2 * d_key + d_v + 1)
+    ldw = (N + 7) // 8 * 8
+    x = torch.randn(B, L, d_model, generator=g, dtype=torch.float32)
+    W = torch.zeros(d_model, ldw, dtype=torch.float32)
+    W[:, :N] = torch.randn(d_model, N, generator=g, dtype=torch.float32) / math.sqrt(d_model)
+    W0 = None
+    if w0_var is not None:
+        W0 = torch.randn(B, H, d_v, 2 * d_key * nu, generator=g, dtype=torch.float32) * math.sqrt(w0_var)
+    return dict(x=x.to(torch.bfloat16).contiguous(), W_all=W.to(torch.bfloat16).contiguous(), ldw=ldw, W0=W0)
+
+
 def forward_inputs(name: str, seed: int = 0):
     cfg = FORWARD_CONFIGS[name]
     if "d_model" in cfg:

@@ -140,6 +140,40 @@ FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const v
                             int d_v, int chunk, int io_dtype, float eps, void *stream);
 
 /*
+ * Bytes of device workspace fw_delta_forward_projected needs (0 for
+ * arguments it would reject).  The caller allocates it.
+ */
+FW_API size_t fw_delta_forward_projected_workspace_size(int B, int L, int d_model, int H, int d_key,
+                                                        int nu, int d_v, int chunk);
+
+/*
+ * fw_delta_forward_projected -- the layer core from the token activations:
+ * the bias-free projections of the attention module (q, k, v of every head
+ * and one beta per head through the sigmoid) on the tensor cores, then
+ * fw_delta_forward on their bf16 results.  [Fast Weights Transformer guide,
+ * the attention module's projections and the sigmoid on beta, then the
+ * sections cited for fw_delta_forward.]
+ *
+ *   x        : [B, L, d_model] bf16 token activations            (read)
+ *   W_all    : [d_model, ldw]  bf16, the four weight matrices side by side:
+ *              columns [0, H d_key) W_q, then H d_key of W_k, H d_v of W_v
+ *              and H of W_beta (head h owns columns h d .. (h + 1) d - 1 of
+ *              its block); ldw % 8 == 0 and ldw >= H (2 d_key + d_v + 1)
+ *              rounded up to 8 (the padding columns are read, not used)
+ *   W0, W_final, y, chunk, eps : as for fw_delta_forward (y [B, H, L, d_v])
+ *   workspace: device scratch of fw_delta_forward_projected_workspace_size()
+ *              bytes: the projected q, k, v, beta, then the forward's
+ * q, k, v and beta are rounded to bf16 once (fp32 accumulation).
+ * Errors as for fw_delta_forward; FW_ERR_INVALID_ARG also for d_model not a
+ * multiple of 64 or a bad ldw.  Three kernels, chained by programmatic
+ * dependent launch.
+ */
+FW_API int fw_delta_forward_projected(const void *x, const void *W_all, int ldw, const float *W0,
+                                      float *W_final, void *y, void *workspace, size_t workspace_bytes,
+                                      int B, int L, int d_model, int H, int d_key, int nu, int d_v,
+                                      int chunk, float eps, void *stream);
+
+/*
  * Bytes of device workspace fw_delta_backward needs for this shape (0 for
  * arguments it would reject).  The caller allocates it.
  */

@@ -8,6 +8,9 @@ Contents
   dpfp(x, nu, eps)                  -- the DPFP feature map, plain C, fp64
   delta_forward(q, k, v, beta, ...) -- O1: the sequential recurrence, plain C
   delta_decode_step(...)            -- one token against a persistent W
+  project(x, W_all, H, d_key, d_v)  -- the attention module's projections:
+                                       q, k, v per head and beta = sigmoid(.),
+                                       numpy fp64
   delta_backward(q, k, v, beta, ...) -- gradients of the recurrence (reverse
                                        sweep over the kept history of W), plain C
   linear_forward(q, k, v, ...)      -- the sum rule (linear attention, with or
@@ -201,3 +204,25 @@ def linear_forward(q, k, v, W0=None, z0=None, nu: int = 1, normalize: bool = Tru
 
 def delta_backward(q, k, v, beta, gy, W0=None, gW=None, nu: int = 1, eps: float = 1e-6, nthreads: int = 1):
     return lib().delta_backward(q, k, v, beta, gy, W0, gW, nu, eps, nthreads)
+
+
+def project(x, W_all, H: int, d_key: int, d_v: int):
+    """The bias-free projections of the attention module (the Fast Weights
+    Transformer guide: q, k, v from linear maps of the model width to each
+    head's width, beta from a linear map to one scalar per head followed by
+    the sigmoid), in fp64: P = x W_all with W_all = [W_q | W_k | W_v | W_beta]
+    side by side; head h takes columns h*d .. (h+1)*d - 1 of its block.
+    x: [B, L, d_model]; returns q, k [B,H,L,d_key], v [B,H,L,d_v], beta [B,H,L]."""
+    x = _f64(x)
+    W = _f64(W_all)
+    B, L, _ = x.shape
+    P = np.matmul(x, W)
+    nq, nv = H * d_key, H * d_v
+
+    def heads(a, d):
+        return np.ascontiguousarray(a.reshape(B, L, H, d).transpose(0, 2, 1, 3))
+    q = heads(P[..., :nq], d_key)
+    k = heads(P[..., nq:2 * nq], d_key)
+    v = heads(P[..., 2 * nq:2 * nq + nv], d_v)
+    beta = np.ascontiguousarray((1.0 / (1.0 + np.exp(-P[..., 2 * nq + nv:2 * nq + nv + H]))).transpose(0, 2, 1))
+    return q, k, v, beta

@@ -251,6 +251,31 @@ def pin_decode_stepped_equals_forward(o):
     assert np.allclose(Ws, W, rtol=1e-13, atol=1e-15)
 
 
+# ---------------------------------------------------------- the projections
+def pin_projection_selection(o):
+    """With W_all made of unit columns that pick features of x (and W_beta
+    picking a feature equal to log 3, or a zero column), the projections are
+    those features, split into heads, and beta is sigmoid(log 3) = 3/4 or
+    sigmoid(0) = 1/2 exactly."""
+    import oracle
+    B, L, H, d_key, d_v = 2, 3, 2, 2, 3
+    N = H * (2 * d_key + d_v + 1)
+    d_model = 2 * H * d_key + H * d_v + 1
+    rng = _rng(40)
+    x = rng.standard_normal((B, L, d_model))
+    x[..., -1] = np.log(3.0)
+    W = np.zeros((d_model, N))
+    for c in range(2 * H * d_key + H * d_v):
+        W[c, c] = 1.0                                  # q, k, v take features 0 .. 2 H d_key + H d_v - 1
+    W[-1, N - H] = 1.0                                 # head 0's beta from log 3; head 1's from a zero column
+    q, k, v, beta = oracle.project(x, W, H, d_key, d_v)
+    for h in range(H):
+        assert np.array_equal(q[:, h], x[..., h * d_key:(h + 1) * d_key])
+        assert np.array_equal(k[:, h], x[..., H * d_key + h * d_key:H * d_key + (h + 1) * d_key])
+        assert np.array_equal(v[:, h], x[..., 2 * H * d_key + h * d_v:2 * H * d_key + (h + 1) * d_v])
+    assert np.allclose(beta[:, 0], 0.75, rtol=0, atol=1e-15) and np.all(beta[:, 1] == 0.5)
+
+
 # ---------------------------------------------------------------- backward
 def _fd_loss(o, q, k, v, beta, W0, gy, gW, nu):
     y, Wf = o.delta_forward(q, k, v, beta, W0, nu, 1e-6)
@@ -384,4 +409,5 @@ ALL_PINS = [
     pin_value_channel_permutation, pin_contraction_bound, pin_one_hot_recall,
     pin_decode_stepped_equals_forward, pin_linear_attention_form, pin_linear_first_token_and_convexity,
     pin_linear_zero_denominator, pin_backward_finite_differences, pin_backward_special_cases,
+    pin_projection_selection,
 ]
