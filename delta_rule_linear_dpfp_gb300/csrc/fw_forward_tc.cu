@@ -690,18 +690,23 @@ __global__ void __launch_bounds__(kScanThreads)
     // (and let the next kernel on the stream start its set-up meanwhile)
     griddep_launch_dependents();
     griddep_wait();
+    InFlight fl; // bulk loads on bar_a[0..1], bar_k[0..1] (contiguous)
     if (tid == 0) { // chunk 0's [W'; Q'] and the first K image(s)
         mbar_arrive_expect_tx(bar_a, a_bytes);
         bulk_g2s(at0, rec0 + rc.a, a_bytes, bar_a);
+        fl.issued(0);
         if (NA == 2 && nch > 1) {
             mbar_arrive_expect_tx(bar_a + 1, a_bytes);
             bulk_g2s(at1, rec0 + rc.bytes + rc.a, a_bytes, bar_a + 1);
+            fl.issued(1);
         }
         mbar_arrive_expect_tx(bar_k, k_bytes);
         bulk_g2s(kt0, rec0 + rc.k, k_bytes, bar_k);
+        fl.issued(2);
         if (NKB == 2 && nch > 1) {
             mbar_arrive_expect_tx(bar_k + 1, k_bytes);
             bulk_g2s(kt1, rec0 + rc.bytes + rc.k, k_bytes, bar_k + 1);
+            fl.issued(3);
         }
     }
     fence_async_smem();
@@ -732,6 +737,8 @@ __global__ void __launch_bounds__(kScanThreads)
         const uint8_t *rec = rec0 + (size_t)c * rc.bytes;
         // U' (rows 0..63, threads 0..63) or Y' (threads 64..127) of this chunk
         bool ok = mbar_wait(bar_a + ab, a_parity, status);
+        if (ok)
+            fl.consumed(ab);
         if (__syncthreads_or(!ok))
             break;
 
@@ -752,6 +759,7 @@ __global__ void __launch_bounds__(kScanThreads)
         if (tid == 0 && c + NA < nch) { // this [W'; Q'] buffer is consumed: fetch a later chunk's
             mbar_arrive_expect_tx(bar_a + ab, a_bytes);
             bulk_g2s(ab ? at1 : at0, rec + (size_t)NA * rc.bytes + rc.a, a_bytes, bar_a + ab);
+            fl.issued(ab);
         }
         {
             float d1[DVB];
@@ -790,6 +798,8 @@ __global__ void __launch_bounds__(kScanThreads)
         fence_async_smem();
         tc_fence_before();
         ok = mbar_wait(bar_k + kb, k_parity, status);
+        if (ok)
+            fl.consumed(2 + kb);
         if (__syncthreads_or(!ok))
             break;
 
@@ -815,6 +825,7 @@ __global__ void __launch_bounds__(kScanThreads)
         if (tid == 0 && c + NKB < nch) { // this K buffer is consumed: fetch a later chunk's
             mbar_arrive_expect_tx(bar_k + kb, k_bytes);
             bulk_g2s(kb ? kt1 : kt0, rec + (size_t)NKB * rc.bytes + rc.k, k_bytes, bar_k + kb);
+            fl.issued(2 + kb);
         }
         for (int mb = 0; mb < MB; ++mb) {
             const int d = 128 * mb + tid;
@@ -844,6 +855,8 @@ __global__ void __launch_bounds__(kScanThreads)
         tc_fence_before();
         __syncthreads();
     }
+    if (tid == 0)
+        fl.drain(bar_a, 4, status); // only after an early exit is anything still in flight
     tc_fence_before();
     __syncthreads();
     if (warp == 0)
