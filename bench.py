@@ -544,6 +544,51 @@ def measure_rows(fw, inputs, dev, stream, pk):
     r = roofline("fw_delta_backward (fp32, token-serial)", flops, nbytes, ms, pk)
     r["tokens/s"] = B * L / (ms * 1e-3)
     rows["backward_b4h8_l512"] = r
+    # the token-wise layer stack: one token of 256 sequences through 6 layers (d_model 512, 8 heads of 64,
+    # d_ff 2048), each layer's 64 MiB of fast weights read and written once per token
+    c = inputs.STACK_CONFIGS["stack_b256_l6"]
+    B, H, d_key, nu, d_v, d_model, d_ff, nl = (c[n] for n in ("B", "H", "d_key", "nu", "d_v", "d_model", "d_ff",
+                                                               "n_layers"))
+    d_dot = 2 * d_key * nu
+    si = inputs.stack_inputs(B, H, d_key, nu, d_v, d_model, d_ff, nl, 8, seed=0)
+    sl = [{n: (None if t is None else t.to(dev)) for n, t in ly.items()} for ly in si["layers"]]
+    sx = si["x"].to(dev)
+    sg, sb = si["ln_gamma"].to(dev), si["ln_beta"].to(dev)
+    so = torch.empty(B, d_model, dtype=torch.float32, device=dev)
+    wss = torch.empty(fw.fw_decode_stack_workspace_size(B, H, d_key, d_v, d_model, d_ff), dtype=torch.uint8,
+                      device=dev)
+
+    def stack_step(i, st=stream):
+        fw.fw_decode_stack_step(sx[i % 8], sl, H, d_key, d_v, nu=nu, ln_gamma=sg, ln_beta=sb, out=so, workspace=wss,
+                                stream=st)
+    ms = _time(stack_step, 50, stream)
+    N = H * (2 * d_key + d_v + 1)
+    wbytes = (d_model * sl[0]["W_in"].shape[1] + H * d_v * d_model + 2 * d_model * d_ff) * 2
+    nbytes = nl * (2 * B * H * d_v * d_dot * 4 + wbytes) + 2 * B * d_model * 4
+    flops = nl * (2.0 * B * (d_model * N + H * d_v * d_model + 2 * d_model * d_ff) + 6.0 * B * H * d_v * d_dot)
+    r = roofline("fw_decode_stack_step (6 layers, 37 kernels)", flops, nbytes, ms, pk)
+    r["tokens/s"] = B / (ms * 1e-3)
+    # the same token step captured once as a CUDA graph and replayed (8 tokens per timing)
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(gs):
+        stack_step(0, gs)
+    gs.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        stack_step(0, gs)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(16):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    r["graph_ms_per_token"] = e0.elapsed_time(e1) / 16
+    r["graph_tokens/s"] = B / (r["graph_ms_per_token"] * 1e-3)
+    rows["stack_b256_l6_dmodel512"] = r
     return rows
 
 

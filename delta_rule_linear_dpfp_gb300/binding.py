@@ -28,12 +28,21 @@ EXPORTS = ("fw_status_string", "fw_dpfp", "fw_delta_forward_workspace_size", "fw
            "fw_delta_forward_noalloc", "fw_delta_forward_prepare", "fw_delta_forward_scan",
            "fw_selftest_wait_timeout", "fw_linear_forward_workspace_size", "fw_linear_forward",
            "fw_delta_backward_workspace_size", "fw_delta_backward",
-           "fw_delta_forward_projected_workspace_size", "fw_delta_forward_projected")
+           "fw_delta_forward_projected_workspace_size", "fw_delta_forward_projected",
+           "fw_decode_stack_workspace_size", "fw_decode_stack_step")
+
+#: the members of fw_stack_layer, in order
+STACK_FIELDS = ("W_in", "W_o", "b_o", "ln_gamma", "ln_beta", "W_1", "b_1", "W_2", "b_2", "W")
 
 #: bytes of the library's own scratch array behind fw_delta_forward_noalloc
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
+
+
+class FwStackLayer(ctypes.Structure):
+    """fw_stack_layer of fastweight.h: one layer's device pointers."""
+    _fields_ = [(n, ctypes.c_void_p) for n in STACK_FIELDS]
 
 
 class FwError(RuntimeError):
@@ -89,6 +98,11 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.fw_delta_forward_projected_workspace_size.argtypes = [i32] * 8
     lib.fw_delta_forward_projected.restype = i32
     lib.fw_delta_forward_projected.argtypes = [vp, vp, i32, vp, vp, vp, vp, sz] + [i32] * 8 + [f32, vp]
+    lib.fw_decode_stack_workspace_size.restype = sz
+    lib.fw_decode_stack_workspace_size.argtypes = [i32] * 6
+    lib.fw_decode_stack_step.restype = i32
+    lib.fw_decode_stack_step.argtypes = [ctypes.POINTER(FwStackLayer), i32, vp, vp, vp, vp, vp, sz] + [i32] * 8 + [
+        f32, f32, vp]
     lib.fw_selftest_umma.restype = i32
     lib.fw_selftest_umma.argtypes = [vp, vp, vp] + [i32] * 5 + [vp]
     if path is None:
@@ -245,6 +259,60 @@ def fw_delta_forward_projected(x, W_all, H: int, d_key: int, d_v: int, nu: int =
                                            eps, _stream(stream))
     _check(rc, "fw_delta_forward_projected")
     return y, W_final
+
+
+def fw_decode_stack_workspace_size(B, H, d_key, d_v, d_model, d_ff) -> int:
+    return int(load().fw_decode_stack_workspace_size(B, H, d_key, d_v, d_model, d_ff))
+
+
+def fw_decode_stack_step(x, layers, H: int, d_key: int, d_v: int, nu: int = 1, ln_gamma=None, ln_beta=None,
+                         eps: float = 1e-6, ln_eps: float = 1e-5, out=None, workspace=None, stream=None):
+    """One token of B sequences through the layer stack.  x: [B, d_model] fp32;
+    layers: sequence of dicts keyed by STACK_FIELDS (W_in [d_model, ldw] and
+    W_o, W_1, W_2 bf16 [in, out]; b_o, b_1, b_2, ln_gamma, ln_beta fp32 or
+    None; W fp32 [B, H, d_v, d_dot], updated in place).  Returns out [B, d_model]
+    fp32, the final norm of the last layer's output."""
+    _dev(x, "x")
+    if x.dtype != torch.float32 or x.dim() != 2:
+        raise ValueError("x must be fp32 [B, d_model]")
+    B, d_model = x.shape
+    d_dot = 2 * d_key * nu
+    arr = (FwStackLayer * max(1, len(layers)))()
+    ldw_in, d_ff = 0, 64
+    for i, ly in enumerate(layers):
+        for n in ("W_in", "W_o", "W_1", "W_2"):
+            _dev(ly[n], n)
+            if ly[n].dtype != torch.bfloat16:
+                raise ValueError(f"{n} must be bf16")
+        for n in ("b_o", "ln_gamma", "ln_beta", "b_1", "b_2"):
+            if ly.get(n) is not None:
+                _dev(ly[n], n)
+                if ly[n].dtype != torch.float32:
+                    raise ValueError(f"{n} must be fp32")
+        _dev(ly["W"], "W")
+        if ly["W"].dtype != torch.float32 or tuple(ly["W"].shape) != (B, H, d_v, d_dot):
+            raise ValueError("W must be fp32 [B, H, d_v, d_dot]")
+        if i == 0:
+            ldw_in, d_ff = ly["W_in"].shape[1], ly["W_1"].shape[1]
+        if (tuple(ly["W_in"].shape) != (d_model, ldw_in) or tuple(ly["W_o"].shape) != (H * d_v, d_model) or
+                tuple(ly["W_1"].shape) != (d_model, d_ff) or tuple(ly["W_2"].shape) != (d_ff, d_model)):
+            raise ValueError(f"layer {i}: weight shapes disagree")
+        for n in STACK_FIELDS:
+            setattr(arr[i], n, None if ly.get(n) is None else ly[n].data_ptr())
+    for name, t in (("ln_gamma", ln_gamma), ("ln_beta", ln_beta)):
+        if t is not None:
+            _dev(t, name)
+    if out is None:
+        out = torch.empty(B, d_model, dtype=torch.float32, device=x.device)
+    need = fw_decode_stack_workspace_size(B, H, d_key, d_v, d_model, d_ff)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().fw_decode_stack_step(arr, len(layers), _ptr(x), _ptr(ln_gamma), _ptr(ln_beta), _ptr(out),
+                                     _ptr(workspace), ws_bytes, B, H, d_key, nu, d_v, d_model, d_ff, ldw_in, eps,
+                                     ln_eps, _stream(stream))
+    _check(rc, "fw_decode_stack_step")
+    return out
 
 
 def fw_delta_backward_workspace_size(B, H, L, d_key, nu, d_v, io_dtype) -> int:

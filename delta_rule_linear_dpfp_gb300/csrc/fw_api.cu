@@ -4,6 +4,7 @@
 #include "fastweight.h"
 #include "fw_common.cuh"
 #include "fw_forward_tc.h"
+#include "fw_stack.h"
 
 #include <cmath>
 #include <mutex>
@@ -484,6 +485,66 @@ FW_API int fw_delta_decode_step(const void *q, const void *k, const void *v, con
     e = fw::launch_decode(q, k, v, beta, W, y, (int)BH, d_key, nu, d_v, io_dtype == FW_DTYPE_BF16,
                           eps, di.num_sms, static_cast<cudaStream_t>(stream));
     return cuda_status(e);
+}
+
+namespace {
+
+int check_stack_shape(int n_layers, int B, int H, int d_key, int nu, int d_v, int d_model, int d_ff) {
+    if (n_layers < 0 || B < 0 || H <= 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 ||
+        d_model <= 0 || d_ff <= 0)
+        return FW_ERR_INVALID_ARG;
+    if (!dkey_supported(d_key) || 2 * d_key * nu > 1024 || d_model % 128 || d_model > 1024 || (H * d_v) % 64 ||
+        d_ff % 64 || (int64_t)H * (2 * d_key + d_v + 1) > 65535 * 128 || d_ff > 65535 * 128 ||
+        (int64_t)B * H > (int64_t)1 << 30)
+        return FW_ERR_UNSUPPORTED;
+    return FW_OK;
+}
+
+} // namespace
+
+FW_API size_t fw_decode_stack_workspace_size(int B, int H, int d_key, int d_v, int d_model, int d_ff) {
+    if (check_stack_shape(0, B, H, d_key, 1, d_v, d_model, d_ff) != FW_OK)
+        return 0;
+    return fw::stack_layout(B, H, d_key, d_v, d_model, d_ff).bytes;
+}
+
+FW_API int fw_decode_stack_step(const fw_stack_layer *layers, int n_layers, const float *x, const float *ln_gamma,
+                                const float *ln_beta, float *out, void *workspace, size_t workspace_bytes, int B,
+                                int H, int d_key, int nu, int d_v, int d_model, int d_ff, int ldw_in, float eps,
+                                float ln_eps, void *stream) {
+    if (!eps_ok(eps) || !eps_ok(ln_eps))
+        return FW_ERR_INVALID_ARG;
+    const int rc = check_stack_shape(n_layers, B, H, d_key, nu, d_v, d_model, d_ff);
+    if (rc != FW_OK)
+        return rc;
+    const int64_t N = (int64_t)H * (2 * d_key + d_v + 1);
+    if (n_layers > 0 && (ldw_in % 8 || ldw_in < (N + 7) / 8 * 8))
+        return FW_ERR_INVALID_ARG;
+    if (B == 0)
+        return FW_OK; // no sequence: nothing is read or written
+    if (!x || !out || !aligned16(x) || !aligned16(out) || (ln_gamma && !aligned16(ln_gamma)) ||
+        (ln_beta && !aligned16(ln_beta)))
+        return FW_ERR_INVALID_ARG;
+    if (n_layers > 0 && !layers)
+        return FW_ERR_INVALID_ARG;
+    for (int l = 0; l < n_layers; ++l) {
+        const fw_stack_layer &ly = layers[l];
+        if (!ly.W_in || !ly.W_o || !ly.W_1 || !ly.W_2 || !ly.W)
+            return FW_ERR_INVALID_ARG;
+        const void *ptrs[] = {ly.W_in, ly.W_o, ly.b_o, ly.ln_gamma, ly.ln_beta, ly.W_1, ly.b_1, ly.W_2, ly.b_2, ly.W};
+        for (const void *p : ptrs)
+            if (p && !aligned16(p))
+                return FW_ERR_INVALID_ARG;
+    }
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < fw::stack_layout(B, H, d_key, d_v, d_model, d_ff).bytes)
+        return FW_ERR_INVALID_ARG;
+    DeviceInfo di;
+    if (device_info(&di) != cudaSuccess)
+        return FW_ERR_CUDA;
+    return cuda_status(fw::stack_step_launch(layers, n_layers, x, ln_gamma, ln_beta, out, workspace, B, H, d_key, nu,
+                                             d_v, d_model, d_ff, ldw_in, eps, ln_eps, di.num_sms, di.status,
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 FW_API int fw_device_status(void *stream) {

@@ -253,6 +253,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     griddep_launch_dependents();
     griddep_wait();
+    qb = after_wait(qb);
+    kb = after_wait(kb);
+    vb = after_wait(vb);
+    bb = after_wait(bb);
+    gyb = after_wait(gyb);
+    ub = after_wait(ub);
+    W0 = after_wait(W0);
+    gWL = after_wait(gWL);
     for (int e = tid; e < nel; e += kBwdThreads) {
         W[e] = W0 ? W0[bh * nel + e] : 0.f;
         G[e] = gWL ? gWL[bh * nel + e] : 0.f;

@@ -17,14 +17,14 @@ enum : unsigned { kStatusTimeout = 1u };
 template <typename T> struct io;
 
 template <> struct io<float> {
-    static FW_DEV float load(const float *p) { return __ldg(p); }
+    static FW_DEV float load(const float *p) { return __ldcg(p); }
     static FW_DEV float to_f(float x) { return x; }
     static FW_DEV float from_f(float x) { return x; }
     static FW_DEV void store(float *p, float x) { *p = x; }
 };
 
 template <> struct io<__nv_bfloat16> {
-    static FW_DEV float load(const __nv_bfloat16 *p) { return __bfloat162float(__ldg(p)); }
+    static FW_DEV float load(const __nv_bfloat16 *p) { return __bfloat162float(__ldcg(p)); }
     static FW_DEV float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
     static FW_DEV __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
     static FW_DEV void store(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
@@ -33,14 +33,14 @@ template <> struct io<__nv_bfloat16> {
 // Load 8 consecutive elements (16-byte aligned for bf16, 32-byte for fp32)
 // and widen them to fp32.
 FW_DEV void load8(const float *p, float (&o)[8]) {
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    const float4 a = __ldcg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldcg(reinterpret_cast<const float4 *>(p) + 1);
     o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
     o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
 }
 
 FW_DEV void load8(const __nv_bfloat16 *p, float (&o)[8]) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint4 u = __ldcg(reinterpret_cast<const uint4 *>(p));
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -77,11 +77,25 @@ FW_DEV void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_de
 // Block until the preceding kernel on the stream has completed and its memory
 // operations are visible (returns at once when the launch did not overlap).
 FW_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// A pointer read after griddep_wait: its value passes through an opaque step
+// placed after the wait, so the compiler cannot schedule a load through it
+// (a read-only or cache-hinted load included) ahead of the wait.  Loads of
+// data another kernel may have written use the coherent L2 path (__ldcg),
+// not the read-only path, whose contract is data constant for the kernel's
+// whole lifetime -- which an overlapped launch does not give.
+template <class T> FW_DEV T *after_wait(T *p) {
+    asm volatile("" : "+l"(p)::"memory");
+    return p;
+}
 
 // Launch with programmatic stream serialization: the kernel's CTAs may be
 // scheduled while the preceding kernel on the stream finishes, so the launch
 // latency is hidden behind its tail.  Every kernel launched this way calls
-// griddep_wait before its first global access.
+// griddep_wait before its first global access.  Because each kernel lets its
+// successor launch early, a kernel may start while kernels two or more places
+// before it still run: a load before griddep_wait would race with them (the
+// one exception, the forward's scan reading W0, is made safe by its
+// predecessor triggering only after its own wait).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
     cudaLaunchConfig_t cfg = {};

@@ -44,7 +44,6 @@ __global__ void __launch_bounds__(256)
     const int64_t bh = blockIdx.x / nrb;
     const int r0 = (blockIdx.x % nrb) * kRowsPerCta;
     const int d_dot = N2 * nu;
-    const float b = io<T>::load(beta + bh);
 
     auto row_ptr = [&](int j) { return W + (bh * d_v + r0 + warp + kWarps * j) * (int64_t)d_dot; };
     auto row_ok = [&](int j) { return r0 + warp + kWarps * j < d_v; };
@@ -58,7 +57,13 @@ __global__ void __launch_bounds__(256)
     };
 
     griddep_launch_dependents();
-    griddep_wait(); // q, k, v, beta or W may be the preceding kernel's output
+    griddep_wait(); // q, k, v, beta or W may be the preceding kernel's output: no load before this
+    q = after_wait(q);
+    k = after_wait(k);
+    v = after_wait(v);
+    beta = after_wait(beta);
+    W = after_wait(W);
+    const float b = io<T>::load(beta + bh);
     float4 cur[NQ];
     load_row(0, cur); // first row in flight while phi is built
 

@@ -35,7 +35,7 @@ template <typename T> struct Raw8;
 template <> struct Raw8<__nv_bfloat16> {
     uint4 u;
     FW_DEV void load(const __nv_bfloat16 *p, bool valid) {
-        u = valid ? __ldg(reinterpret_cast<const uint4 *>(p)) : make_uint4(0, 0, 0, 0);
+        u = valid ? __ldcg(reinterpret_cast<const uint4 *>(p)) : make_uint4(0, 0, 0, 0);
     }
     FW_DEV void widen(float (&o)[8]) const {
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -49,8 +49,8 @@ template <> struct Raw8<__nv_bfloat16> {
 template <> struct Raw8<float> {
     float4 a, b;
     FW_DEV void load(const float *p, bool valid) {
-        a = valid ? __ldg(reinterpret_cast<const float4 *>(p)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        b = valid ? __ldg(reinterpret_cast<const float4 *>(p) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        a = valid ? __ldcg(reinterpret_cast<const float4 *>(p)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        b = valid ? __ldcg(reinterpret_cast<const float4 *>(p) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     FW_DEV void widen(float (&o)[8]) const {
         o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(256, kBlocksPerSM) dpfp_kernel(const Tin *__re
     int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     griddep_launch_dependents();
     griddep_wait(); // x may be the preceding kernel's output
+    xin = after_wait(xin);
     Raw8<Tin> cur;
     {
         const int64_t row = wid * RPW + lane / G;

@@ -292,8 +292,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     uint8_t *rec = ws + ((size_t)bh * nch + c) * rc.bytes;
     const uint32_t ncols = tmem_cols_pow2(max(64, Dp + d_v));
 
-    griddep_launch_dependents(); // the scan may start its prologue on free SMs
     griddep_wait(); // the inputs may be, and the workspace may still be read by, the preceding kernel
+    q = after_wait(q);
+    k = after_wait(k);
+    v = after_wait(v);
+    beta = after_wait(beta);
+    // Only now may the scan start its prologue (on free SMs): it reads the
+    // caller's W0 before its own wait, which is safe once everything enqueued
+    // before this kernel has completed, as it has here.
+    griddep_launch_dependents();
     // Global loads first, all in flight before any is used: the key and query
     // rows for the DPFP, the chunk's V rows (kept in registers until their
     // tile's space is free) and beta (stored to shared memory after the DPFP).
@@ -308,7 +315,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         const __nv_bfloat16 *src = (hr < 64 ? k : q) + ((size_t)bh * L + t0 + t) * DK;
 #pragma unroll
         for (int c8 = 0; c8 < kRaw; ++c8)
-            raw[c8] = t < Lc ? __ldg(reinterpret_cast<const uint4 *>(src) + c8) : make_uint4(0, 0, 0, 0);
+            raw[c8] = t < Lc ? __ldcg(reinterpret_cast<const uint4 *>(src) + c8) : make_uint4(0, 0, 0, 0);
     } else {
         const int g = lane % G;
 #pragma unroll
@@ -317,7 +324,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
             const int t = r & 63;
             raw[ps] = make_uint4(0, 0, 0, 0);
             if (t < Lc)
-                raw[ps] = __ldg(reinterpret_cast<const uint4 *>((r < 64 ? k : q) + ((size_t)bh * L + t0 + t) * DK +
+                raw[ps] = __ldcg(reinterpret_cast<const uint4 *>((r < 64 ? k : q) + ((size_t)bh * L + t0 + t) * DK +
                                                                8 * (g % (G / 2))));
         }
     }
@@ -329,7 +336,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         const int idx = tid + i * kPrepThreads, t = idx / vcpr, j = 8 * (idx % vcpr);
         vpre[i] = make_uint4(0, 0, 0, 0);
         if (idx < 64 * vcpr && t < Lc)
-            vpre[i] = __ldg(reinterpret_cast<const uint4 *>(v + ((size_t)bh * L + t0 + t) * d_vr + j));
+            vpre[i] = __ldcg(reinterpret_cast<const uint4 *>(v + ((size_t)bh * L + t0 + t) * d_vr + j));
     }
     float beta_t = 0.f;
     if (!SUM && tid < Lc && tid < 64)
@@ -663,8 +670,9 @@ __global__ void __launch_bounds__(kScanThreads)
     const uint32_t kt0_s = smem_u32(kt0), kt1_s = smem_u32(kt1);
 
     // initial state: S^T in TMEM (fp32) and S as the bf16 operand of MMA1.
-    // W0 is the caller's, never written by the prep kernel, so this runs
-    // before the wait for the prep to finish.
+    // W0 is the caller's and never written by the prep kernel, which lets
+    // this kernel start only after its own wait (so everything enqueued
+    // before the prep has completed): it runs before the wait for the prep.
     for (int mb = 0; mb < MB; ++mb) {
         const int d = 128 * mb + tid;
 #pragma unroll
@@ -690,23 +698,34 @@ __global__ void __launch_bounds__(kScanThreads)
     // (and let the next kernel on the stream start its set-up meanwhile)
     griddep_launch_dependents();
     griddep_wait();
-    InFlight fl; // bulk loads on bar_a[0..1], bar_k[0..1] (contiguous)
+    rec0 = after_wait(rec0);
+    // On an early exit (a wait that gave up) thread 0 waits, bounded, for the
+    // bulk loads still in flight, so that none lands after the CTA has left.
+    // Which are in flight follows from the chunk and the step that failed
+    // (0: its [W'; Q'] image, 1: MMA1, 2: its K image, 3: MMA3): the image of
+    // chunk j sits in buffer j % NA (j % NKB), in that buffer's phase j / NA.
+    auto drain = [&](int c, int step) {
+        if (tid != 0)
+            return;
+        const int a_hi = min(nch - 1, step >= 2 ? c + NA : c + NA - 1);
+        for (int j = step >= 1 ? c + 1 : c; j <= a_hi; ++j)
+            mbar_wait(bar_a + (NA == 2 ? (j & 1) : 0), (uint32_t)((NA == 2 ? j >> 1 : j) & 1), status);
+        const int k_hi = min(nch - 1, c + NKB - 1);
+        for (int j = step >= 3 ? c + 1 : c; j <= k_hi; ++j)
+            mbar_wait(bar_k + (NKB == 2 ? (j & 1) : 0), (uint32_t)((NKB == 2 ? j >> 1 : j) & 1), status);
+    };
     if (tid == 0) { // chunk 0's [W'; Q'] and the first K image(s)
         mbar_arrive_expect_tx(bar_a, a_bytes);
         bulk_g2s(at0, rec0 + rc.a, a_bytes, bar_a);
-        fl.issued(0);
         if (NA == 2 && nch > 1) {
             mbar_arrive_expect_tx(bar_a + 1, a_bytes);
             bulk_g2s(at1, rec0 + rc.bytes + rc.a, a_bytes, bar_a + 1);
-            fl.issued(1);
         }
         mbar_arrive_expect_tx(bar_k, k_bytes);
         bulk_g2s(kt0, rec0 + rc.k, k_bytes, bar_k);
-        fl.issued(2);
         if (NKB == 2 && nch > 1) {
             mbar_arrive_expect_tx(bar_k + 1, k_bytes);
             bulk_g2s(kt1, rec0 + rc.bytes + rc.k, k_bytes, bar_k + 1);
-            fl.issued(3);
         }
     }
     fence_async_smem();
@@ -721,7 +740,7 @@ __global__ void __launch_bounds__(kScanThreads)
         const float *src = (const float *)(rec0 + (size_t)cc * rc.bytes + (tid < 64 ? rc.up : rc.yp)) + 4 * (tid & 63);
 #pragma unroll
         for (int j = 0; j < DVB; j += 4) {
-            const float4 f = __ldg(reinterpret_cast<const float4 *>(src + 64 * chan(j)));
+            const float4 f = __ldcg(reinterpret_cast<const float4 *>(src + 64 * chan(j)));
             pre[j] = f.x;
             pre[j + 1] = f.y;
             pre[j + 2] = f.z;
@@ -737,10 +756,10 @@ __global__ void __launch_bounds__(kScanThreads)
         const uint8_t *rec = rec0 + (size_t)c * rc.bytes;
         // U' (rows 0..63, threads 0..63) or Y' (threads 64..127) of this chunk
         bool ok = mbar_wait(bar_a + ab, a_parity, status);
-        if (ok)
-            fl.consumed(ab);
-        if (__syncthreads_or(!ok))
+        if (__syncthreads_or(!ok)) {
+            drain(c, 0);
             break;
+        }
 
         // MMA1: D1 = [W'; Q'] S^T
         if (tid == 0) {
@@ -753,13 +772,14 @@ __global__ void __launch_bounds__(kScanThreads)
         }
         ok = mbar_wait(bar_mma, mma_phase, status);
         mma_phase ^= 1;
-        if (__syncthreads_or(!ok))
+        if (__syncthreads_or(!ok)) {
+            drain(c, 1);
             break;
+        }
         tc_fence_after();
         if (tid == 0 && c + NA < nch) { // this [W'; Q'] buffer is consumed: fetch a later chunk's
             mbar_arrive_expect_tx(bar_a + ab, a_bytes);
             bulk_g2s(ab ? at1 : at0, rec + (size_t)NA * rc.bytes + rc.a, a_bytes, bar_a + ab);
-            fl.issued(ab);
         }
         {
             float d1[DVB];
@@ -798,10 +818,10 @@ __global__ void __launch_bounds__(kScanThreads)
         fence_async_smem();
         tc_fence_before();
         ok = mbar_wait(bar_k + kb, k_parity, status);
-        if (ok)
-            fl.consumed(2 + kb);
-        if (__syncthreads_or(!ok))
+        if (__syncthreads_or(!ok)) {
+            drain(c, 2);
             break;
+        }
 
         // MMA3: S^T += K^T U   (K^T: the K image read MN-major)
         if (tid == 0) {
@@ -819,13 +839,14 @@ __global__ void __launch_bounds__(kScanThreads)
         }
         ok = mbar_wait(bar_mma, mma_phase, status);
         mma_phase ^= 1;
-        if (__syncthreads_or(!ok))
+        if (__syncthreads_or(!ok)) {
+            drain(c, 3);
             break;
+        }
         tc_fence_after();
         if (tid == 0 && c + NKB < nch) { // this K buffer is consumed: fetch a later chunk's
             mbar_arrive_expect_tx(bar_k + kb, k_bytes);
             bulk_g2s(kb ? kt1 : kt0, rec + (size_t)NKB * rc.bytes + rc.k, k_bytes, bar_k + kb);
-            fl.issued(2 + kb);
         }
         for (int mb = 0; mb < MB; ++mb) {
             const int d = 128 * mb + tid;
@@ -855,8 +876,6 @@ __global__ void __launch_bounds__(kScanThreads)
         tc_fence_before();
         __syncthreads();
     }
-    if (tid == 0)
-        fl.drain(bar_a, 4, status); // only after an early exit is anything still in flight
     tc_fence_before();
     __syncthreads();
     if (warp == 0)

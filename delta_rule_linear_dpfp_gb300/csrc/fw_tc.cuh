@@ -81,24 +81,6 @@ FW_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 
-// Bulk loads in flight on up to 32 buffer mbarriers (one bit each) and the
-// parity of each one's next phase.  On an early exit the issuing thread
-// waits (bounded) for every load still in flight, so that no copy lands in
-// shared memory after the CTA has left.
-struct InFlight {
-    uint32_t pending = 0, parity = 0;
-    FW_DEV void issued(int i) { pending |= 1u << i; }
-    FW_DEV void consumed(int i) {
-        pending &= ~(1u << i);
-        parity ^= 1u << i;
-    }
-    FW_DEV void drain(uint64_t *bar, int n, unsigned *status) {
-        for (int i = 0; i < n; ++i)
-            if ((pending >> i) & 1u)
-                mbar_wait(bar + i, (parity >> i) & 1u, status);
-    }
-};
-
 // ------------------------------------------------ 1-D bulk copy (TMA engine)
 // global -> shared, completion counted on `bar` in bytes.  dst, src and
 // bytes must be multiples of 16.

@@ -17,6 +17,9 @@ in for its activations):
   proj_d512       B1 H8 L1024 from x [1,1024,512] through bias-free random
                   projections W_q/W_k/W_v/W_beta ~ N(0, 1/512), bf16, chunk 64
   decode_b256     B256 H16 d_key64 nu2 d_v128, 128 tokens, bf16, W fp32 zeros
+  stack_b256_l6   the guide's model shape for token-wise inference: 6 layers of
+                  d_model 512, 8 heads of 64, nu 1, d_ff 2048; B256 sequences,
+                  one token per step, every layer's W fp32 starting at zero
 
 q, k, v ~ N(0, 1); beta = sigmoid(N(0, 1)); variances are the second
 argument of N(.,.) (so W0 has standard deviation 0.1).
@@ -36,6 +39,10 @@ FORWARD_CONFIGS = {
 
 DECODE_CONFIGS = {
     "decode_b256": dict(B=256, H=16, d_key=64, nu=2, d_v=128, steps=128, io="bf16", w0_var=None),
+}
+
+STACK_CONFIGS = {
+    "stack_b256_l6": dict(B=256, H=8, d_key=64, nu=1, d_v=64, d_model=512, d_ff=2048, n_layers=6),
 }
 
 EPS = 1e-6
@@ -163,3 +170,41 @@ def decode_inputs(B, H, d_key, nu, d_v, steps, io="bf16", w0_var=None, seed=0):
         W0 = W0 * math.sqrt(w0_var)
     return dict(q=q.to(dt).contiguous(), k=k.to(dt).contiguous(), v=v.to(dt).contiguous(),
                 beta=beta.to(dt).contiguous(), W0=W0)
+
+
+def stack_inputs(B, H, d_key, nu, d_v, d_model, d_ff, n_layers, steps, w0_var=None, ldw_pad=0, seed=0):
+    """Random-init weights of an n_layers token-wise stack and `steps` tokens.
+
+    x ~ N(0,1) [steps, B, d_model] fp32.  Per layer: W_in = [W_q | W_k | W_v |
+    W_beta] ~ N(0, 1/d_model) ([d_model, ldw], ldw = N rounded up to 8 plus
+    ldw_pad zero columns), W_o ~ N(0, 1/(H d_v)), W_1 ~ N(0, 1/d_model), W_2 ~
+    N(0, 1/d_ff) (bf16, [in, out]); b_o, b_1, b_2 ~ N(0, 0.01); ln_gamma = 1 +
+    N(0, 0.01), ln_beta ~ N(0, 0.01) (fp32); the layer's fast weights W fp32
+    [B, H, d_v, 2 d_key nu], zeros unless w0_var.  Then the final norm's
+    gamma and beta as above.  Draw order: x, then each layer's W_in, W_o,
+    b_o, ln_gamma, ln_beta, W_1, b_1, W_2, b_2, W, then the final gamma,
+    beta."""
+    g = _gen(seed)
+    N = H * (2 * d_key + d_v + 1)
+    ldw = (N + 7) // 8 * 8 + ldw_pad
+
+    def rn(*shape, std=1.0):
+        return torch.randn(*shape, generator=g, dtype=torch.float32) * std
+
+    x = rn(steps, B, d_model)
+    layers = []
+    for _ in range(n_layers):
+        W_in = torch.zeros(d_model, ldw, dtype=torch.float32)
+        W_in[:, :N] = rn(d_model, N, std=1.0 / math.sqrt(d_model))
+        ly = dict(W_in=W_in.to(torch.bfloat16).contiguous(),
+                  W_o=rn(H * d_v, d_model, std=1.0 / math.sqrt(H * d_v)).to(torch.bfloat16).contiguous(),
+                  b_o=rn(d_model, std=0.1), ln_gamma=1.0 + rn(d_model, std=0.1), ln_beta=rn(d_model, std=0.1),
+                  W_1=rn(d_model, d_ff, std=1.0 / math.sqrt(d_model)).to(torch.bfloat16).contiguous(),
+                  b_1=rn(d_ff, std=0.1),
+                  W_2=rn(d_ff, d_model, std=1.0 / math.sqrt(d_ff)).to(torch.bfloat16).contiguous(),
+                  b_2=rn(d_model, std=0.1))
+        d_dot = 2 * d_key * nu
+        ly["W"] = (torch.zeros(B, H, d_v, d_dot, dtype=torch.float32) if w0_var is None
+                   else rn(B, H, d_v, d_dot, std=math.sqrt(w0_var)))
+        layers.append(ly)
+    return dict(x=x, layers=layers, ln_gamma=1.0 + rn(d_model, std=0.1), ln_beta=rn(d_model, std=0.1))

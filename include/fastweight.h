@@ -328,6 +328,71 @@ FW_API int fw_delta_decode_step(const void *q, const void *k, const void *v, con
                                 int io_dtype, float eps, void *stream);
 
 /*
+ * One layer of the token-wise stack (fw_decode_stack_step): the weights of
+ * its fast-weight attention module and feed-forward block, and its fast
+ * weights.  All pointers are device pointers; bf16 matrices are row-major
+ * [in, out] (P = x W); every bias may be NULL (zero) and each norm's gamma /
+ * beta may be NULL (one / zero).
+ */
+typedef struct fw_stack_layer {
+    const void *W_in;      /* bf16 [d_model, ldw_in]: [W_q | W_k | W_v | W_beta], the
+                              layout of fw_delta_forward_projected's W_all            */
+    const void *W_o;       /* bf16 [H d_v, d_model]: the module's output map          */
+    const float *b_o;      /* fp32 [d_model]                                          */
+    const float *ln_gamma; /* fp32 [d_model]: the norm before the feed-forward block  */
+    const float *ln_beta;  /* fp32 [d_model]                                          */
+    const void *W_1;       /* bf16 [d_model, d_ff]                                    */
+    const float *b_1;      /* fp32 [d_ff]                                             */
+    const void *W_2;       /* bf16 [d_ff, d_model]                                    */
+    const float *b_2;      /* fp32 [d_model]                                          */
+    float *W;              /* fp32 [B, H, d_v, d_dot]: this layer's fast weights,
+                              read and written (persist from token to token)          */
+} fw_stack_layer;
+
+/*
+ * Bytes of device workspace fw_decode_stack_step needs (0 for a shape it
+ * would reject).  The caller allocates it.
+ */
+FW_API size_t fw_decode_stack_workspace_size(int B, int H, int d_key, int d_v, int d_model, int d_ff);
+
+/*
+ * fw_decode_stack_step -- one new token of B sequences through n_layers
+ * fast-weight Transformer layers, each layer's fast weights kept from token
+ * to token, then the final LayerNorm.
+ * [Fast Weights Transformer guide, section "token_wise variant" (one weight
+ * entry per layer; each token passes through every layer in turn, then the
+ * final norm), section "layer and model assembly" (attention output added to
+ * the input, LayerNorm, feed-forward block of linear, ReLU, linear added
+ * again; no norm before the attention), section "module structure" (q, k, v
+ * and beta projections without bias, beta through the sigmoid, the output
+ * linear layer with bias); dropout is the identity at inference]
+ *
+ *   layers   : HOST array of n_layers fw_stack_layer (read during the call only)
+ *   x        : [B, d_model] fp32, the token's input to layer 0       (read)
+ *   ln_gamma, ln_beta : fp32 [d_model], the final norm (NULL: one / zero)
+ *   out      : [B, d_model] fp32, the final norm's output          (written)
+ *   workspace: device scratch of fw_decode_stack_workspace_size() bytes
+ *   ldw_in   : row stride of every layer's W_in, as for
+ *              fw_delta_forward_projected (ldw % 8 == 0, >= N rounded up to 8)
+ *   eps      : DPFP eps;  ln_eps: the norms' eps (1e-5 in PyTorch)
+ * Per layer: q, k, v, beta = x W_in (beta through the sigmoid, all rounded to
+ * bf16), y = fw_delta_decode_step on the layer's W, x += y W_o + b_o,
+ * x += relu(LN(x) W_1 + b_1) W_2 + b_2.  The residual stream x is fp32;
+ * what the tensor cores read (x, y, LN(x), the hidden layer) is rounded to
+ * bf16 and every product accumulates in fp32.  6 n_layers + 1 kernels,
+ * chained by programmatic dependent launch (capturable in one CUDA graph).
+ * Errors: FW_ERR_INVALID_ARG for bad sizes, NULL or unaligned pointers, a
+ * small workspace; FW_ERR_UNSUPPORTED for d_key outside {8, 16, 32, 64, 128},
+ * d_dot > 1024, d_model not a multiple of 128 or above 1024, H d_v or d_ff
+ * not a multiple of 64.
+ */
+FW_API int fw_decode_stack_step(const fw_stack_layer *layers, int n_layers, const float *x,
+                                const float *ln_gamma, const float *ln_beta, float *out,
+                                void *workspace, size_t workspace_bytes, int B, int H, int d_key,
+                                int nu, int d_v, int d_model, int d_ff, int ldw_in, float eps,
+                                float ln_eps, void *stream);
+
+/*
  * fw_device_status -- waits for `stream`, then reports and clears the
  * device-side status word of the current device: FW_ERR_TIMEOUT if any
  * kernel of this library gave up a bounded wait (its outputs are then

@@ -17,6 +17,9 @@ Contents
                                        without the z normaliser), plain C
   chunked.delta_forward_chunked     -- O2: the chunked (WY / UT) form in numpy,
                                        for tiny brute-force checks of O1
+  stack.stack_step, stack.layer_norm -- one token through the token-wise layer
+                                       stack (projections, decode step, output
+                                       map, LayerNorm, feed-forward), numpy fp64
 
 All arrays are numpy float64 (inputs are converted with np.asarray(...,
 dtype=float64), so rounded bf16/fp32 values enter exactly).  fw_oracle.c cites
@@ -24,7 +27,8 @@ the passage of the Fast Weights Transformer guide (xdnf.cn/news/308600) that
 each routine follows.  Parity is pinned by tests/test_oracle_*.py against
 hand-worked examples (tests/golden/), closed forms, invariants, an FFT
 identity and the independent chunked form O2; tests/test_oracle_mutants.py
-shows that planted mistakes in fw_oracle.c fail those pins.  No function is
+shows that planted mistakes in fw_oracle.c fail those pins, and
+tests/test_oracle_stack.py does the same for stack.py.  No function is
 left unpinned.
 """
 import ctypes

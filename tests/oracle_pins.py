@@ -411,3 +411,153 @@ ALL_PINS = [
     pin_linear_zero_denominator, pin_backward_finite_differences, pin_backward_special_cases,
     pin_projection_selection,
 ]
+
+
+# ---------------------------------------------------- token-wise layer stack
+# These take the OracleLib `o` (its sequence-level forward O1 is the
+# independent reference for the stack's per-token state updates) and the
+# stack module `st` (oracle/stack.py or a mutated copy).
+def _torch_layer_norm(x, gamma=None, beta=None, eps=1e-5):
+    import torch
+    t = torch.from_numpy(np.asarray(x, dtype=np.float64))
+    g = None if gamma is None else torch.from_numpy(np.asarray(gamma, dtype=np.float64))
+    b = None if beta is None else torch.from_numpy(np.asarray(beta, dtype=np.float64))
+    return torch.nn.functional.layer_norm(t, (t.shape[-1],), g, b, eps).numpy()
+
+
+def _stack_layer(rng, H, d_key, d_v, d_model, d_ff, B, nu, zero=()):
+    N = H * (2 * d_key + d_v + 1)
+    ly = dict(W_in=rng.normal(0, 1 / np.sqrt(d_model), (d_model, N + 8)),
+              W_o=rng.normal(0, 1 / np.sqrt(H * d_v), (H * d_v, d_model)), b_o=rng.normal(0, 0.1, d_model),
+              ln_gamma=1 + rng.normal(0, 0.1, d_model), ln_beta=rng.normal(0, 0.1, d_model),
+              W_1=rng.normal(0, 1 / np.sqrt(d_model), (d_model, d_ff)), b_1=rng.normal(0, 0.1, d_ff),
+              W_2=rng.normal(0, 1 / np.sqrt(d_ff), (d_ff, d_model)), b_2=rng.normal(0, 0.1, d_model),
+              W=rng.normal(0, 0.1, (B, H, d_v, 2 * d_key * nu)))
+    for name in zero:
+        ly[name] = np.zeros_like(ly[name])
+    return ly
+
+
+def pin_stack_layer_norm(o, st):
+    """The norm equals PyTorch's LayerNorm (biased variance, eps inside the
+    square root, then gamma and beta); without gamma / beta each row has mean
+    0 and variance var / (var + eps); a constant row maps to beta."""
+    rng = _rng(40)
+    x = rng.normal(0.3, 2.0, (7, 48))
+    g, b = rng.normal(1, 0.2, 48), rng.normal(0, 0.2, 48)
+    assert np.allclose(st.layer_norm(x, g, b, 1e-5), _torch_layer_norm(x, g, b, 1e-5), rtol=0, atol=1e-12)
+    z = st.layer_norm(x, None, None, 1e-5)
+    var = x.var(axis=-1)
+    assert np.allclose(z.mean(axis=-1), 0, atol=1e-12)
+    assert np.allclose(z.var(axis=-1), var / (var + 1e-5), rtol=1e-12, atol=0)
+    c = st.layer_norm(np.full((2, 48), 3.5), g, b, 1e-5)
+    assert np.allclose(c, np.broadcast_to(b, c.shape), rtol=0, atol=1e-12)
+
+
+def pin_stack_zero_weights(o, st):
+    """With every weight matrix zero, q = k = 0 so phi = 0: no layer changes
+    its fast weights or the residual stream beyond its biases (none here), and
+    the output is the final norm of the input."""
+    rng = _rng(41)
+    H, d_key, d_v, d_model, d_ff, B, nu = 2, 4, 3, 6, 5, 3, 2
+    layers = []
+    for _ in range(2):
+        ly = _stack_layer(rng, H, d_key, d_v, d_model, d_ff, B, nu, zero=("W_in", "W_o", "W_1", "W_2"))
+        ly.update(b_o=None, b_1=None, b_2=None)
+        layers.append(ly)
+    x = rng.normal(0, 1, (B, d_model))
+    g, b = rng.normal(1, 0.2, d_model), rng.normal(0, 0.2, d_model)
+    out, res, states = st.stack_step(x, layers, H, d_key, d_v, nu, g, b)
+    assert np.allclose(res, x, rtol=0, atol=0)
+    assert np.allclose(out, _torch_layer_norm(x, g, b), rtol=0, atol=1e-12)
+    for ly, W in zip(layers, states):
+        assert np.array_equal(W, ly["W"])
+
+
+def _project_sequence(o, xs, W_in, H, d_key, d_v):
+    """q, k, v, beta [B, H, T, *] of the token sequence xs [T, B, d_model]."""
+    from oracle import project
+    return project(np.transpose(xs, (1, 0, 2)), W_in, H, d_key, d_v)
+
+
+def pin_stack_state_follows_forward(o, st):
+    """One layer whose output map and second feed-forward map are zero leaves
+    the residual stream as it is, so stepping it token by token over a
+    sequence must leave its fast weights where the sequence-level recurrence
+    O1 (one C loop over the tokens) leaves them, and each output is the final
+    norm of that token's input."""
+    rng = _rng(42)
+    H, d_key, d_v, d_model, d_ff, B, nu, T = 2, 4, 3, 8, 6, 3, 2, 5
+    ly = _stack_layer(rng, H, d_key, d_v, d_model, d_ff, B, nu, zero=("W_o", "W_2"))
+    ly.update(b_o=None, b_2=None)
+    xs = rng.normal(0, 1, (T, B, d_model))
+    W = ly["W"]
+    for t in range(T):
+        out, res, (W,) = st.stack_step(xs[t], [dict(ly, W=W)], H, d_key, d_v, nu)
+        assert np.allclose(res, xs[t], rtol=0, atol=0)
+        assert np.allclose(out, _torch_layer_norm(xs[t]), rtol=0, atol=1e-12)
+    q, k, v, beta = _project_sequence(o, xs, ly["W_in"], H, d_key, d_v)
+    _, W_ref = o.delta_forward(q, k, v, beta, ly["W"], nu)
+    assert np.allclose(W, W_ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_stack_attention_output(o, st):
+    """With d_model = H d_v, the identity as output map and the feed-forward
+    block reduced to its last bias c2, a layer's residual output is
+    x_t + y_t + b_o + c2, with y_t the heads' outputs of O1 over the sequence
+    laid side by side (head h in columns h d_v .. (h + 1) d_v - 1)."""
+    rng = _rng(43)
+    H, d_key, d_v, d_ff, B, nu, T = 3, 4, 2, 5, 2, 1, 4
+    d_model = H * d_v
+    ly = _stack_layer(rng, H, d_key, d_v, d_model, d_ff, B, nu, zero=("W_1", "W_2"))
+    ly.update(W_o=np.eye(d_model), b_1=None)
+    xs = rng.normal(0, 1, (T, B, d_model))
+    q, k, v, beta = _project_sequence(o, xs, ly["W_in"], H, d_key, d_v)
+    y_ref, _ = o.delta_forward(q, k, v, beta, ly["W"], nu)
+    W = ly["W"]
+    for t in range(T):
+        _, res, (W,) = st.stack_step(xs[t], [dict(ly, W=W)], H, d_key, d_v, nu)
+        want = xs[t] + y_ref[:, :, t, :].reshape(B, d_model) + ly["b_o"] + ly["b_2"]
+        assert np.allclose(res, want, rtol=1e-12, atol=1e-12)
+
+
+def pin_stack_feed_forward(o, st):
+    """With the projections zero (y = 0), identity linear maps in the
+    feed-forward block and a first bias far above |LN(x)|, ReLU passes
+    everything: x1 = x + b_o + LN(x + b_o) + b_1 + b_2; with the first bias
+    far below, ReLU blocks everything: x1 = x + b_o + b_2."""
+    rng = _rng(44)
+    H, d_key, d_v, B, nu = 2, 4, 4, 3, 1
+    d_model = d_ff = 8
+    x = rng.normal(0, 1, (B, d_model))
+    for sign in (1.0, -1.0):
+        ly = _stack_layer(rng, H, d_key, d_v, d_model, d_ff, B, nu, zero=("W_in",))
+        ly.update(W_1=np.eye(d_model), W_2=np.eye(d_model), b_1=np.full(d_ff, sign * 1e3))
+        _, res, _ = st.stack_step(x, [ly], H, d_key, d_v, nu)
+        a = x + ly["b_o"]
+        if sign > 0:
+            want = a + _torch_layer_norm(a, ly["ln_gamma"], ly["ln_beta"]) + ly["b_1"] + ly["b_2"]
+        else:
+            want = a + ly["b_2"]
+        assert np.allclose(res, want, rtol=1e-12, atol=1e-9)
+
+
+def pin_stack_composition(o, st):
+    """Layers apply in order, each to the previous one's residual output and
+    each with its own fast weights: a two-layer step equals the first layer's
+    step followed by the second's."""
+    rng = _rng(45)
+    H, d_key, d_v, d_model, d_ff, B, nu = 2, 4, 4, 8, 6, 3, 2
+    l1 = _stack_layer(rng, H, d_key, d_v, d_model, d_ff, B, nu)
+    l2 = _stack_layer(rng, H, d_key, d_v, d_model, d_ff, B, nu)
+    x = rng.normal(0, 1, (B, d_model))
+    _, r12, (W1, W2) = st.stack_step(x, [l1, l2], H, d_key, d_v, nu)
+    _, r1, (V1,) = st.stack_step(x, [l1], H, d_key, d_v, nu)
+    _, r2, (V2,) = st.stack_step(r1, [l2], H, d_key, d_v, nu)
+    assert np.allclose(r12, r2, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(W1, V1) and np.array_equal(W2, V2)
+    assert not np.allclose(W1, l1["W"]) and not np.allclose(W2, l2["W"])
+
+
+STACK_PINS = (pin_stack_layer_norm, pin_stack_zero_weights, pin_stack_state_follows_forward,
+              pin_stack_attention_output, pin_stack_feed_forward, pin_stack_composition)

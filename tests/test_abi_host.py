@@ -214,3 +214,44 @@ def test_linear_argument_checks(lib):
     assert call(chunk=48) == E
     assert call(eps=-1.0) == E
     assert call(B=0, q=None, k=None, v=None, y=None, ws=None) == OK
+
+
+def _stack(lib, layers=None, n=1, **kw):
+    a = dict(x=FAKE, g=None, b=None, out=FAKE, ws=FAKE, wsb=1 << 30, B=4, H=2, d_key=16, nu=1, d_v=32, d_model=128,
+             d_ff=128, ldw=136, eps=1e-6, ln_eps=1e-5)
+    a.update(kw)
+    if layers is None:
+        ly = binding.FwStackLayer(*([0x10000] * len(binding.STACK_FIELDS)))
+        layers = (binding.FwStackLayer * 1)(ly)
+    return lib.fw_decode_stack_step(layers, n, a["x"], a["g"], a["b"], a["out"], a["ws"], a["wsb"], a["B"], a["H"],
+                                    a["d_key"], a["nu"], a["d_v"], a["d_model"], a["d_ff"], a["ldw"], a["eps"],
+                                    a["ln_eps"], None)
+
+
+def test_stack_argument_checks(lib):
+    E, U, OK = binding.FW_ERR_INVALID_ARG, binding.FW_ERR_UNSUPPORTED, binding.FW_OK
+    ws = lib.fw_decode_stack_workspace_size
+    assert ws(4, 2, 16, 32, 128, 128) > 0
+    assert ws(4, 2, 16, 32, 96, 128) == 0          # d_model not a multiple of 128
+    assert ws(4, 2, 16, 32, 2048, 128) == 0        # d_model above 1024
+    assert ws(4, 2, 16, 24, 128, 128) == 0         # H d_v not a multiple of 64
+    assert ws(4, 2, 12, 32, 128, 128) == 0         # d_key not compiled
+    assert _stack(lib, x=None) == E
+    assert _stack(lib, out=MISALIGNED) == E
+    assert _stack(lib, ws=None) == E
+    assert _stack(lib, wsb=16) == E                # workspace too small
+    assert _stack(lib, ldw=100) == E               # N = 2 (2 16 + 32 + 1) = 130 > 100
+    assert _stack(lib, ldw=140) == E               # not a multiple of 8
+    assert _stack(lib, eps=-1.0) == E
+    assert _stack(lib, ln_eps=float("nan")) == E
+    assert _stack(lib, n=-1) == E
+    assert _stack(lib, d_model=96) == U
+    assert _stack(lib, d_ff=100) == U
+    assert _stack(lib, nu=32) == E                 # nu > 2 d_key - 1
+    assert _stack(lib, d_key=64, nu=9) == U        # d_dot 1152 > 1024
+    bad = binding.FwStackLayer(*([0x10000] * len(binding.STACK_FIELDS)))
+    bad.W = None                                    # the layer's fast weights missing
+    assert _stack(lib, layers=(binding.FwStackLayer * 1)(bad)) == E
+    bad.W, bad.b_o = 0x10000, 0x10004               # a misaligned bias
+    assert _stack(lib, layers=(binding.FwStackLayer * 1)(bad)) == E
+    assert _stack(lib, B=0, x=None, out=None, ws=None, wsb=0) == OK   # empty: nothing enqueued

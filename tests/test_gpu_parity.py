@@ -166,6 +166,33 @@ def test_forward_resume_equals_whole():
     assert maxrel(f64(Wb), f64(W)) <= 2e-2
 
 
+def test_forward_memory_passing_back_to_back():
+    """Segments enqueued back to back with nothing between them, each call's
+    W0 the previous call's W_final (the chunked interface's memory passing):
+    every kernel lets its successor launch early, so this checks that no
+    call reads its initial state before the previous call has written it."""
+    B, H, L, S = 2, 8, 512, 8
+    d = to_dev(inputs.random_forward_inputs(B, H, L, 64, 2, 64, "bf16", 0.01, seed=21))
+    y, W = fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=d["W0"], nu=2)
+    seg = L // S
+    parts = [{n: d[n][:, :, i * seg:(i + 1) * seg].contiguous() for n in ("q", "k", "v", "beta")}
+             for i in range(S)]
+    need = fw.fw_delta_forward_workspace_size(B, H, seg, 64, 2, 64, 64, torch.bfloat16)
+    wss = [torch.empty(need, dtype=torch.uint8, device="cuda") for _ in range(S)]
+    ys = [torch.empty(B, H, seg, 64, dtype=torch.bfloat16, device="cuda") for _ in range(S)]
+    Ws = [torch.empty_like(d["W0"]) for _ in range(S)]
+    torch.cuda.synchronize()
+    prev = d["W0"]
+    for i in range(S):
+        p = parts[i]
+        fw.fw_delta_forward(p["q"], p["k"], p["v"], p["beta"], W0=prev, nu=2, y=ys[i], W_final=Ws[i],
+                            workspace=wss[i])
+        prev = Ws[i]
+    torch.cuda.synchronize()
+    assert maxrel(f64(torch.cat(ys, 2)), f64(y)) <= 2e-2
+    assert maxrel(f64(Ws[-1]), f64(W)) <= 2e-2
+
+
 def test_prepare_then_scan_equals_forward():
     """The two phases, enqueued one after the other, give exactly what the
     one-call forward gives (same kernels, same arithmetic)."""
