@@ -197,9 +197,9 @@ namespace {
 // The projected q, k, v, beta inside the workspace, each 256-byte aligned,
 // then the forward's own workspace.
 struct ProjLayout {
-    size_t q, k, v, beta, fwd, bytes;
+    size_t q, k, v, beta, scratch, fwd, bytes;
 };
-ProjLayout proj_layout(int B, int L, int H, int d_key, int d_v, size_t fwd_bytes) {
+ProjLayout proj_layout(int B, int L, int d_model, int H, int d_key, int d_v, size_t fwd_bytes) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t tok = (size_t)B * H * L;
     ProjLayout p;
@@ -207,7 +207,8 @@ ProjLayout proj_layout(int B, int L, int H, int d_key, int d_v, size_t fwd_bytes
     p.k = up(p.q + tok * d_key * 2);
     p.v = up(p.k + tok * d_key * 2);
     p.beta = up(p.v + tok * d_v * 2);
-    p.fwd = up(p.beta + tok * 2);
+    p.scratch = up(p.beta + tok * 2);
+    p.fwd = up(p.scratch + fw::gemm_scratch_bytes(B * L, H * (2 * d_key + d_v + 1), d_model));
     p.bytes = p.fwd + fwd_bytes;
     return p;
 }
@@ -219,7 +220,8 @@ FW_API size_t fw_delta_forward_projected_workspace_size(int B, int L, int d_mode
     if (d_model <= 0 || d_model % 64 || H <= 0 || check_forward_shape(B, H, L, d_key, nu, d_v, chunk,
                                                                       FW_DTYPE_BF16) != FW_OK)
         return 0;
-    return proj_layout(B, L, H, d_key, d_v, fw::tc_forward_workspace_bytes(B, H, L, d_key, nu, d_v, chunk)).bytes;
+    return proj_layout(B, L, d_model, H, d_key, d_v, fw::tc_forward_workspace_bytes(B, H, L, d_key, nu, d_v, chunk))
+        .bytes;
 }
 
 FW_API int fw_delta_forward_projected(const void *x, const void *W_all, int ldw, const float *W0, float *W_final,
@@ -251,7 +253,8 @@ FW_API int fw_delta_forward_projected(const void *x, const void *W_all, int ldw,
     }
     if (!x || !W_all || !y || !aligned16(x) || !aligned16(W_all) || !aligned16(y))
         return FW_ERR_INVALID_ARG;
-    const ProjLayout pl = proj_layout(B, L, H, d_key, d_v, fw::tc_forward_workspace_bytes(B, H, L, d_key, nu, d_v, chunk));
+    const ProjLayout pl =
+        proj_layout(B, L, d_model, H, d_key, d_v, fw::tc_forward_workspace_bytes(B, H, L, d_key, nu, d_v, chunk));
     if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes)
         return FW_ERR_INVALID_ARG;
     DeviceInfo di;
@@ -260,7 +263,7 @@ FW_API int fw_delta_forward_projected(const void *x, const void *W_all, int ldw,
         return FW_ERR_CUDA;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     e = fw::launch_project(x, W_all, ldw, ws + pl.q, ws + pl.k, ws + pl.v, ws + pl.beta, B, L, H, d_key, d_v, d_model,
-                           di.status, st);
+                           ws + pl.scratch, di.status, st);
     if (e != cudaSuccess)
         return cuda_status(e);
     e = fw::tc_forward_launch(ws + pl.q, ws + pl.k, ws + pl.v, ws + pl.beta, W0, W_final, y, ws + pl.fwd, B, H, L,

@@ -49,22 +49,31 @@ cudaError_t launch_backward(const void *q, const void *k, const void *v, const v
                             float *gW0, float *scratch, int BH, int L, int d_key, int nu, int d_v, int bf16,
                             float eps, cudaStream_t st);
 
-// The projection prologue: q, k, v, beta (bf16, [B,H,L,*]) = x [B*L, d_model]
-// times W_all = [W_q | W_k | W_v | W_beta] ([d_model, ldw], the first
-// N = H (2 d_key + d_v + 1) columns used; beta through the sigmoid), on
-// tcgen05.  d_model % 64 == 0, ldw % 8 == 0, ldw >= N rounded up to 8.
-// x may be fp32 (x_f32, rounded to bf16 as it is staged) instead of bf16.
+// The dense layers run on one tcgen05 GEMM fed by TMA (fw_project.cu).  When
+// the output tiles alone would leave most SMs idle, K is split into slices
+// whose fp32 partial tiles a second kernel adds in slice order; that needs
+// gemm_scratch_bytes() of device scratch (0 when K is not split).
+int gemm_slices(int M, int N, int K);
+size_t gemm_scratch_bytes(int M, int N, int K);
 size_t project_smem_bytes();
-cudaError_t launch_project(const void *x, const void *Wall, int ldw, void *q, void *k, void *v, void *beta, int B,
-                           int L, int H, int d_key, int d_v, int d_model, unsigned *status, cudaStream_t st,
-                           bool x_f32 = false);
 
-// A dense layer on the same tensor-core kernel: P = A W + bias with A
-// [M, K] bf16 and W [K, N] bf16 (row-major), then out = resid + P (fp32,
-// resid may be NULL or equal to out) or, with relu, out = bf16(max(P, 0)).
-// K % 64 == 0, N % 8 == 0; bias (fp32 [N]) may be NULL.
+// The projection prologue: q, k, v, beta (bf16, [B,H,L,*]) = x [B*L, d_model]
+// (bf16) times W_all = [W_q | W_k | W_v | W_beta] ([d_model, ldw], the first
+// N = H (2 d_key + d_v + 1) columns used; beta through the sigmoid).
+// d_model % 64 == 0, ldw % 8 == 0, ldw >= N rounded up to 8; x and W_all
+// 16-byte aligned.
+cudaError_t launch_project(const void *x, const void *Wall, int ldw, void *q, void *k, void *v, void *beta, int B,
+                           int L, int H, int d_key, int d_v, int d_model, void *scratch, unsigned *status,
+                           cudaStream_t st);
+
+// A dense layer: P = A W + bias with A [M, K] bf16 and W [K, N] bf16
+// (row-major), then out = resid + P (fp32; resid may be NULL or equal to
+// out; out_bf16_copy, when not NULL, receives the same values in bf16) or,
+// with relu, out = bf16(max(P, 0)).  K % 64 == 0, N % 8 == 0; bias (fp32
+// [N]) may be NULL.
 cudaError_t launch_dense(const void *A, const void *W, int K, int M, int N, const float *bias, const float *resid,
-                         void *out, bool relu, unsigned *status, cudaStream_t st);
+                         void *out, bool relu, void *out_bf16_copy, void *scratch, unsigned *status,
+                         cudaStream_t st);
 
 // Row-wise layer normalisation (biased variance): out[m] = (x[m] - mean) /
 // sqrt(var + eps) * gamma + beta over D columns; x fp32 [M, D]; out bf16

@@ -22,11 +22,13 @@
 // on the decode kernel, the norms on the row kernel below; consecutive
 // kernels are chained by programmatic dependent launch, so one token of an
 // L-layer stack is 6 L + 1 launches that a caller can capture as one graph.
-// The residual stream is fp32; the activations the tensor cores read (x as
-// staged, y, LN output, the hidden layer) are rounded to bf16.
+// The residual stream is fp32; the activations the tensor cores read (a bf16
+// copy of x written beside it, y, LN output, the hidden layer) are bf16.
 #include "fw_forward_tc.h"
 #include "fw_common.cuh"
 #include "fw_stack.h"
+
+#include <algorithm>
 
 namespace fw {
 
@@ -89,7 +91,29 @@ __global__ void __launch_bounds__(32 * kLnRows)
         }
 }
 
+// The layer stack's input rounded to bf16: the first projection's A.
+__global__ void __launch_bounds__(256) to_bf16_kernel(const float *__restrict__ x, __nv_bfloat16 *__restrict__ y,
+                                                      int64_t n8) {
+    griddep_launch_dependents();
+    griddep_wait(); // x may be the preceding kernel's output
+    x = after_wait(x);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+        float v[8];
+        load8(x + 8 * i, v);
+        store8(y + 8 * i, v);
+    }
+}
+
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+size_t stack_scratch(int B, int H, int d_key, int d_v, int d_model, int d_ff) {
+    const int N = H * (2 * d_key + d_v + 1);
+    size_t m = gemm_scratch_bytes(B, N, d_model);
+    m = std::max(m, gemm_scratch_bytes(B, d_model, H * d_v));
+    m = std::max(m, gemm_scratch_bytes(B, d_ff, d_model));
+    m = std::max(m, gemm_scratch_bytes(B, d_model, d_ff));
+    return m;
+}
 
 } // namespace
 
@@ -114,7 +138,9 @@ StackLayout stack_layout(int B, int H, int d_key, int d_v, int d_model, int d_ff
     p.z = up256(p.y + bh * d_v * 2);
     p.h = up256(p.z + (size_t)B * d_model * 2);
     p.x = up256(p.h + (size_t)B * d_ff * 2);
-    p.bytes = up256(p.x + (size_t)B * d_model * 4);
+    p.x16 = up256(p.x + (size_t)B * d_model * 4);
+    p.scratch = up256(p.x16 + (size_t)B * d_model * 2);
+    p.bytes = up256(p.scratch + stack_scratch(B, H, d_key, d_v, d_model, d_ff));
     return p;
 }
 
@@ -125,23 +151,31 @@ cudaError_t stack_step_launch(const fw_stack_layer *layers, int n_layers, const 
     const StackLayout pl = stack_layout(B, H, d_key, d_v, d_model, d_ff);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *xr = reinterpret_cast<float *>(ws + pl.x);
+    void *x16 = ws + pl.x16, *scratch = ws + pl.scratch;
     cudaError_t e = cudaSuccess;
+    if (n_layers > 0) {
+        const int64_t n8 = (int64_t)B * d_model / 8;
+        e = launch_pdl(to_bf16_kernel, dim3((unsigned)std::min<int64_t>((n8 + 255) / 256, 4 * num_sms)), dim3(256),
+                           0, st, x, static_cast<__nv_bfloat16 *>(x16), n8);
+    }
     for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
         const fw_stack_layer &ly = layers[l];
         const float *xin = l == 0 ? x : xr;
-        e = launch_project(xin, ly.W_in, ldw_in, ws + pl.q, ws + pl.k, ws + pl.v, ws + pl.beta, B, 1, H, d_key, d_v,
-                           d_model, status, st, true);
+        e = launch_project(x16, ly.W_in, ldw_in, ws + pl.q, ws + pl.k, ws + pl.v, ws + pl.beta, B, 1, H, d_key, d_v,
+                           d_model, scratch, status, st);
         if (e == cudaSuccess)
             e = launch_decode(ws + pl.q, ws + pl.k, ws + pl.v, ws + pl.beta, ly.W, ws + pl.y, B * H, d_key, nu, d_v,
                               1, eps, num_sms, st);
         if (e == cudaSuccess) // x <- x + y W_o + b_o
-            e = launch_dense(ws + pl.y, ly.W_o, H * d_v, B, d_model, ly.b_o, xin, xr, false, status, st);
+            e = launch_dense(ws + pl.y, ly.W_o, H * d_v, B, d_model, ly.b_o, xin, xr, false, nullptr, scratch, status,
+                             st);
         if (e == cudaSuccess)
             e = launch_layernorm(xr, ly.ln_gamma, ly.ln_beta, ws + pl.z, true, B, d_model, ln_eps, st);
         if (e == cudaSuccess) // hidden = relu(LN(x) W_1 + b_1)
-            e = launch_dense(ws + pl.z, ly.W_1, d_model, B, d_ff, ly.b_1, nullptr, ws + pl.h, true, status, st);
-        if (e == cudaSuccess) // x <- x + hidden W_2 + b_2
-            e = launch_dense(ws + pl.h, ly.W_2, d_ff, B, d_model, ly.b_2, xr, xr, false, status, st);
+            e = launch_dense(ws + pl.z, ly.W_1, d_model, B, d_ff, ly.b_1, nullptr, ws + pl.h, true, nullptr, scratch,
+                             status, st);
+        if (e == cudaSuccess) // x <- x + hidden W_2 + b_2, and its bf16 copy for the next projection
+            e = launch_dense(ws + pl.h, ly.W_2, d_ff, B, d_model, ly.b_2, xr, xr, false, x16, scratch, status, st);
     }
     if (e == cudaSuccess)
         e = launch_layernorm(n_layers ? xr : x, ln_gamma, ln_beta, out, false, B, d_model, ln_eps, st);
