@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-rows", action="store_true", help="skip the per-row extra measurements")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--stack-steps", type=int, default=0,
+                   help="only run this many token steps of the 6-layer stack workload (for profilers), then exit")
     return p.parse_args()
 
 
@@ -592,6 +594,28 @@ def measure_rows(fw, inputs, dev, stream, pk):
     return rows
 
 
+def stack_only(steps):
+    """`steps` token steps of the stack_b256_l6 workload through the public API
+    (62 launches each), nothing else: the command the stack's launch list is
+    captured from."""
+    from delta_rule_linear_dpfp_gb300 import binding as fw, build, inputs
+    build.build()
+    fw.load()
+    c = inputs.STACK_CONFIGS["stack_b256_l6"]
+    B, H, d_key, nu, d_v, d_model, d_ff, nl = (c[n] for n in ("B", "H", "d_key", "nu", "d_v", "d_model", "d_ff",
+                                                               "n_layers"))
+    si = inputs.stack_inputs(B, H, d_key, nu, d_v, d_model, d_ff, nl, 4, seed=0)
+    sl = [{n: (None if t is None else t.cuda()) for n, t in ly.items()} for ly in si["layers"]]
+    sx, sg, sb = si["x"].cuda(), si["ln_gamma"].cuda(), si["ln_beta"].cuda()
+    out = torch.empty(B, d_model, device="cuda")
+    ws = torch.empty(fw.fw_decode_stack_workspace_size(B, H, d_key, d_v, d_model, d_ff), dtype=torch.uint8,
+                     device="cuda")
+    for i in range(steps):
+        fw.fw_decode_stack_step(sx[i % 4], sl, H, d_key, d_v, nu=nu, ln_gamma=sg, ln_beta=sb, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"stack_steps": steps, "launches_per_step": 10 * nl + 2}))
+
+
 # ------------------------------------------------------------ the oracle
 class OracleSample:
     """The fp64 CPU oracle on the host cores over a bounded sample of the
@@ -675,6 +699,9 @@ def main():
         if rank != 0:
             return
         print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if args.stack_steps:
+        stack_only(args.stack_steps)
         return
     if world > 1:
         torch.cuda.set_device(local_rank)

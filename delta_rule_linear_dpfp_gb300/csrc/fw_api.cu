@@ -276,7 +276,7 @@ namespace {
 int check_backward_shape(int B, int H, int L, int d_key, int nu, int d_v, int io_dtype) {
     if (B < 0 || H < 0 || L < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 || !dtype_ok(io_dtype))
         return FW_ERR_INVALID_ARG;
-    if (!dkey_supported(d_key) || fw::backward_smem_bytes(d_key, nu, d_v) > (size_t)227 * 1024)
+    if (!dkey_supported(d_key) || 2 * d_key * nu > 1024 || fw::backward_smem_bytes(d_key, nu, d_v) > (size_t)227 * 1024)
         return FW_ERR_UNSUPPORTED;
     return FW_OK;
 }
@@ -286,7 +286,7 @@ int check_backward_shape(int B, int H, int L, int d_key, int nu, int d_v, int io
 FW_API size_t fw_delta_backward_workspace_size(int B, int H, int L, int d_key, int nu, int d_v, int io_dtype) {
     if (check_backward_shape(B, H, L, d_key, nu, d_v, io_dtype) != FW_OK)
         return 0;
-    return sizeof(float) * (size_t)B * H * L * d_v;
+    return fw::backward_workspace_bytes(B * H, L, d_key, nu, d_v);
 }
 
 FW_API int fw_delta_backward(const void *q, const void *k, const void *v, const void *beta, const float *W0,

@@ -13,24 +13,32 @@
 // then through the DPFP map (quotient rule of the normalisation, both
 // factors of each rolled product, the two ReLU halves of [k, -k]).
 //
-// Mapping: one CTA of 512 threads per (batch, head); W and gW stay in shared
-// memory in fp32 for the whole sequence.  A forward sweep keeps u_t for every
-// token (global scratch, d_v floats per token); the reverse sweep steps W
-// back exactly as the forward stepped it up (W_{t-1} = W_t - u_t phi(k_t)^T,
-// one rounding per element and token).  Row dot products take one warp per
-// row, column sums one thread per column (deterministic order), updates one
-// thread per element; one warp builds phi of a row, one warp takes the DPFP
-// backward.  fp32 arithmetic on CUDA cores throughout: the token loop is
-// serial, so this kernel is latency-bound.
+// Mapping.  The rows of W are independent in both sweeps except for three
+// sums over rows per token (g_phi(q), g_phi(k), gbeta), which only feed the
+// outputs.  So the state is split by rows: one CTA of 256 threads per
+// (batch, head) and block of up to 16 rows keeps those rows of W and gW in
+// shared memory (fp32) for the whole sequence and writes, per token, its
+// partial sums over its rows; a second kernel adds the blocks' partials in
+// block order (deterministic) and takes the DPFP backward of q and k, one
+// warp per token.  The forward sweep keeps u_t for every token (global
+// scratch); the reverse sweep steps W back exactly as the forward stepped it
+// up (W_{t-1} = W_t - u_t phi(k_t)^T, one rounding per element and token).
+// Row dot products take one warp per row, column sums one thread per column
+// (deterministic order), updates one thread per element.  fp32 arithmetic on
+// CUDA cores throughout: the token loop is serial, so the first kernel is
+// latency-bound, and the split multiplies the CTAs that hide that latency.
 #include "fw_common.cuh"
 #include "fw_forward_tc.h"
+
+#include <algorithm>
 
 namespace fw {
 
 namespace {
 
-constexpr int kBwdThreads = 512;
+constexpr int kBwdThreads = 256;
 constexpr int kBwdWarps = kBwdThreads / 32;
+constexpr int kBwdRows = 16;  // rows of W per CTA
 
 // phi of one row by one warp from its d_key raw values in shared memory
 // (kr): x = ReLU([k, -k]) into xs, phi into ph.  Block i of phi holds
@@ -122,11 +130,11 @@ FW_DEV void for_elements(int nel, int d_dot, int tid, F f) {
 }
 
 // Row dot products x[r] = A[r] . p (and y[r] = B[r] . p when B is given)
-// for every row: warp w takes rows w, w + 16, ... (up to 8 per warp); the
+// for every row: warp w takes rows w, w + 8, ... (up to 8 per warp); the
 // lanes stride the columns and the rows' sums are reduced together.
 FW_DEV void row_dots2(const float *A, const float *B, const float *p, float *x, float *y, int d_v, int d_dot,
                       int warp, int lane) {
-    constexpr int kMaxRows = 8; // d_v <= 128
+    constexpr int kMaxRows = 8; // rows <= 64
     float sa[kMaxRows], sb[kMaxRows];
 #pragma unroll
     for (int i = 0; i < kMaxRows; ++i) {
@@ -187,67 +195,71 @@ FW_DEV float col_sum(const float *a, const float *b, const float *c, const float
     return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
+// Block z of rows [r0, r0 + R) of one (batch, head).  part: [blocks][BH][L]
+// [2 d_dot + 4]: per token this block's sums over its rows of g_phi(q) (first
+// d_dot), g_phi(k) (next d_dot) and gbeta (at 2 d_dot).
 template <typename T>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads)
     delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                           const T *__restrict__ beta, const float *__restrict__ W0, const T *__restrict__ gy,
-                          const float *__restrict__ gWL, T *__restrict__ gq, T *__restrict__ gk, T *__restrict__ gv,
-                          T *__restrict__ gbeta, float *__restrict__ gW0, float *__restrict__ us, int L, int d_key,
-                          int nu, int d_v, float eps) {
+                          const float *__restrict__ gWL, T *__restrict__ gv, float *__restrict__ gW0,
+                          float *__restrict__ us, float *__restrict__ part, int L, int d_key, int nu, int d_v,
+                          float eps) {
     extern __shared__ float sm[];
     const int d_dot = 2 * d_key * nu, n = 2 * d_key;
-    const int nel = d_v * d_dot;
-    // one token's inputs, staged: k, q (d_key each), v, gy, u (d_v each), beta
-    const int ntok = 2 * d_key + 3 * d_v + 1;
-    float *W = sm;                 // [d_v][d_dot] the state W_t
-    float *G = W + nel;            // [d_v][d_dot] dL/dW_t
+    const int r0 = blockIdx.y * kBwdRows, R = min(kBwdRows, d_v - r0);
+    const int nel = R * d_dot;
+    const int64_t BH = gridDim.x, bh = blockIdx.x;
+    const size_t pst = 2 * (size_t)d_dot + 4; // floats per token in part
+    // one token's inputs, staged: k, q (d_key each), v, gy, u (R each), beta
+    const int ntok = 2 * d_key + 3 * R + 1;
+    float *W = sm;                 // [R][d_dot] rows r0.. of the state W_t
+    float *G = W + nel;            // [R][d_dot] the same rows of dL/dW_t
     float *pk = G + nel;           // phi(k_t)
     float *pq = pk + d_dot;        // phi(q_t)
-    float *gpq = pq + d_dot;       // dL/dphi(q_t)
-    float *gpk = gpq + d_dot;      // dL/dphi(k_t)
-    float *gu = gpk + d_dot;       // dL/du_t, then beta_t dL/du_t
-    float *aa = gu + d_v;          // W_{t-1} phi(k_t)
-    float *xk = aa + d_v;          // x of k_t (one warp's scratch)
+    float *gu = pq + d_dot;        // dL/du_t, then beta_t dL/du_t
+    float *aa = gu + kBwdRows;     // W_{t-1} phi(k_t)
+    float *xk = aa + kBwdRows;     // x of k_t (one warp's scratch)
     float *xq = xk + n;            // x of q_t
     float *stg = xq + n;           // [2][ntok] staged token inputs (double-buffered)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t bh = blockIdx.x;
-    const T *qb = q + bh * L * d_key, *kb = k + bh * L * d_key, *vb = v + bh * L * d_v, *bb = beta + bh * L;
-    const T *gyb = gy + bh * L * d_v;
-    float *ub = us + bh * L * d_v;
+    const T *qb = q + bh * L * d_key, *kb = k + bh * L * d_key, *vb = v + bh * L * d_v + r0, *bb = beta + bh * L;
+    const T *gyb = gy + bh * L * d_v + r0;
+    float *ub = us + bh * L * d_v + r0;
+    float *pb = part + ((size_t)blockIdx.y * BH + bh) * L * pst;
 
-    // Thread tid loads entries tid and tid + 512 of token t's staged vector
+    // Thread tid loads entries tid and tid + 256 of token t's staged vector
     // into registers; they are stored to shared memory one phase later, so
     // the load latency hides behind the current token's work.
-    auto fetch = [&](int t, bool reverse, float (&r)[2]) {
+    auto fetch = [&](int t, bool reverse, float (&x)[2]) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int e = tid + h * kBwdThreads;
-            float x = 0.f;
+            float val = 0.f;
             if (t >= 0 && t < L && e < ntok) {
                 if (e < d_key)
-                    x = io<T>::load(kb + (int64_t)t * d_key + e);
+                    val = io<T>::load(kb + (int64_t)t * d_key + e);
                 else if (e < 2 * d_key)
-                    x = reverse ? io<T>::load(qb + (int64_t)t * d_key + e - d_key) : 0.f;
-                else if (e < 2 * d_key + d_v)
-                    x = io<T>::load(vb + (int64_t)t * d_v + e - 2 * d_key);
-                else if (e < 2 * d_key + 2 * d_v)
-                    x = reverse ? io<T>::load(gyb + (int64_t)t * d_v + e - 2 * d_key - d_v) : 0.f;
-                else if (e < 2 * d_key + 3 * d_v)
-                    x = reverse ? ub[(int64_t)t * d_v + e - 2 * d_key - 2 * d_v] : 0.f;
+                    val = reverse ? io<T>::load(qb + (int64_t)t * d_key + e - d_key) : 0.f;
+                else if (e < 2 * d_key + R)
+                    val = io<T>::load(vb + (int64_t)t * d_v + e - 2 * d_key);
+                else if (e < 2 * d_key + 2 * R)
+                    val = reverse ? io<T>::load(gyb + (int64_t)t * d_v + e - 2 * d_key - R) : 0.f;
+                else if (e < 2 * d_key + 3 * R)
+                    val = reverse ? __ldcg(ub + (int64_t)t * d_v + e - 2 * d_key - 2 * R) : 0.f;
                 else
-                    x = io<T>::load(bb + t);
+                    val = io<T>::load(bb + t);
             }
-            r[h] = x;
+            x[h] = val;
         }
     };
-    auto stage = [&](int t, const float (&r)[2]) {
+    auto stage = [&](int t, const float (&x)[2]) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int e = tid + h * kBwdThreads;
             if (e < ntok)
-                stg[(t & 1) * ntok + e] = r[h];
+                stg[(t & 1) * ntok + e] = x[h];
         }
     };
 
@@ -261,9 +273,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ub = after_wait(ub);
     W0 = after_wait(W0);
     gWL = after_wait(gWL);
+    const size_t wofs = (size_t)bh * d_v * d_dot + (size_t)r0 * d_dot; // this block's rows in W0, gW
     for (int e = tid; e < nel; e += kBwdThreads) {
-        W[e] = W0 ? W0[bh * nel + e] : 0.f;
-        G[e] = gWL ? gWL[bh * nel + e] : 0.f;
+        W[e] = W0 ? __ldcg(W0 + wofs + e) : 0.f;
+        G[e] = gWL ? __ldcg(gWL + wofs + e) : 0.f;
     }
     float nxt[2];
     // ---- forward sweep: keep u_t
@@ -277,9 +290,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             dpfp_warp(tk, xk, pk, d_key, nu, eps, lane);
         __syncthreads();
         const float bt = tk[ntok - 1];
-        row_dots2(W, nullptr, pk, aa, nullptr, d_v, d_dot, warp, lane); // a = W_{t-1} phi(k)
+        row_dots2(W, nullptr, pk, aa, nullptr, R, d_dot, warp, lane); // a = W_{t-1} phi(k)
         __syncthreads();
-        for (int r = tid; r < d_v; r += kBwdThreads) { // u = beta (v - a)
+        for (int r = tid; r < R; r += kBwdThreads) { // u = beta (v - a)
             const float u = bt * (tv[r] - aa[r]);
             gu[r] = u;
             ub[(int64_t)t * d_v + r] = u;
@@ -295,79 +308,137 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     stage(L - 1, nxt);
     for (int t = L - 1; t >= 0; --t) {
         fetch(t - 1, true, nxt);
-        const float *tk = stg + (t & 1) * ntok, *tq = tk + d_key, *tv = tq + d_key, *tg = tv + d_v, *tu = tg + d_v;
+        const float *tk = stg + (t & 1) * ntok, *tq = tk + d_key, *tv = tq + d_key, *tg = tv + R, *tu = tg + R;
         const float bt = tk[ntok - 1];
+        float *pt = pb + (size_t)t * pst;
         __syncthreads();
         if (warp == 0)
             dpfp_warp(tk, xk, pk, d_key, nu, eps, lane);
         else if (warp == 1)
             dpfp_warp(tq, xq, pq, d_key, nu, eps, lane);
         __syncthreads();
-        for (int m = tid; m < d_dot; m += kBwdThreads) // g_phi(q) = W_t^T gy
-            gpq[m] = col_sum(W, tg, nullptr, nullptr, m, d_v, d_dot);
-        __syncthreads();
+        for (int m = tid; m < d_dot; m += kBwdThreads) // this block's share of g_phi(q) = W_t^T gy
+            pt[m] = col_sum(W, tg, nullptr, nullptr, m, R, d_dot);
+        __syncthreads(); // W_t is read above before it is stepped back below
         for_elements(nel, d_dot, tid, [&](int e, int r, int m) { // gW += gy phi(q)^T; W_{t-1} = W_t - u phi(k)^T
             G[e] = fmaf(tg[r], pq[m], G[e]);
             W[e] = fmaf(-tu[r], pk[m], W[e]);
         });
         __syncthreads();
-        row_dots2(G, W, pk, gu, aa, d_v, d_dot, warp, lane); // gu = gW phi(k), a = W_{t-1} phi(k)
+        row_dots2(G, W, pk, gu, aa, R, d_dot, warp, lane); // gu = gW phi(k), a = W_{t-1} phi(k)
         __syncthreads();
-        if (warp == 0) { // gbeta = gu . (v - a)
+        if (warp == 0) { // this block's share of gbeta = gu . (v - a)
             float acc = 0.f;
-            for (int r = lane; r < d_v; r += 32)
+            for (int r = lane; r < R; r += 32)
                 acc = fmaf(gu[r], tv[r] - aa[r], acc);
             acc = warp_sum(acc);
             if (lane == 0)
-                io<T>::store(gbeta + bh * L + t, acc);
+                pt[2 * d_dot] = acc;
         }
         __syncthreads();
-        for (int r = tid; r < d_v; r += kBwdThreads) { // gv = beta gu; keep e = beta gu (and -e)
+        for (int r = tid; r < R; r += kBwdThreads) { // gv = beta gu; keep e = beta gu (and -e)
             gu[r] *= bt;
             aa[r] = -gu[r];
-            io<T>::store(gv + (bh * L + t) * d_v + r, gu[r]);
+            io<T>::store(gv + (bh * L + t) * d_v + r0 + r, gu[r]);
         }
         __syncthreads();
-        for (int m = tid; m < d_dot; m += kBwdThreads) // g_phi(k) = gW^T u - W_{t-1}^T e
-            gpk[m] = col_sum(G, tu, W, aa, m, d_v, d_dot);
+        for (int m = tid; m < d_dot; m += kBwdThreads) // this block's share of g_phi(k) = gW^T u - W_{t-1}^T e
+            pt[d_dot + m] = col_sum(G, tu, W, aa, m, R, d_dot);
         __syncthreads();
         for_elements(nel, d_dot, tid, [&](int e, int r, int m) { G[e] = fmaf(-gu[r], pk[m], G[e]); }); // gW_{t-1} = gW - e phi(k)^T
-        if (warp == kBwdWarps - 1)
-            dpfp_backward_warp(tq, gpq, xq, gq + (bh * L + t) * d_key, d_key, nu, eps, lane);
-        else if (warp == kBwdWarps - 2)
-            dpfp_backward_warp(tk, gpk, xk, gk + (bh * L + t) * d_key, d_key, nu, eps, lane);
         if (t > 0)
             stage(t - 1, nxt);
     }
     __syncthreads();
     if (gW0)
         for (int e = tid; e < nel; e += kBwdThreads)
-            gW0[bh * nel + e] = G[e];
+            gW0[wofs + e] = G[e];
+}
+
+// The blocks' partial sums added in block order, then the DPFP backward of
+// q_t and k_t and gbeta_t: one warp per (batch, head, token).
+template <typename T>
+__global__ void __launch_bounds__(kBwdThreads)
+    backward_finish_kernel(const T *__restrict__ q, const T *__restrict__ k, const float *__restrict__ part,
+                           T *__restrict__ gq, T *__restrict__ gk, T *__restrict__ gbeta, int64_t rows, int blocks,
+                           int d_key, int nu, float eps) {
+    extern __shared__ float sm[];
+    const int d_dot = 2 * d_key * nu, n = 2 * d_key;
+    const size_t pst = 2 * (size_t)d_dot + 4;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float *ws = sm + (size_t)warp * (2 * d_dot + 2 * d_key + 2 * n);
+    float *gpq = ws, *gpk = gpq + d_dot, *kr = gpk + d_dot, *qr = kr + d_key, *xs = qr + d_key; // xs: 2 n
+    griddep_launch_dependents();
+    griddep_wait(); // the partial sums are the preceding kernel's
+    q = after_wait(q);
+    k = after_wait(k);
+    part = after_wait(part);
+    for (int64_t row = (int64_t)blockIdx.x * kBwdWarps + warp; row < rows; row += (int64_t)gridDim.x * kBwdWarps) {
+        for (int j = lane; j < d_key; j += 32) {
+            kr[j] = io<T>::load(k + row * d_key + j);
+            qr[j] = io<T>::load(q + row * d_key + j);
+        }
+        for (int m = lane; m < 2 * d_dot + 1; m += 32) {
+            float acc = 0.f;
+            for (int z = 0; z < blocks; ++z)
+                acc += __ldcg(part + ((size_t)z * rows + row) * pst + m);
+            if (m < 2 * d_dot)
+                gpq[m] = acc; // gpk follows gpq contiguously
+            else
+                io<T>::store(gbeta + row, acc);
+        }
+        __syncwarp();
+        dpfp_backward_warp(qr, gpq, xs, gq + row * d_key, d_key, nu, eps, lane);
+        dpfp_backward_warp(kr, gpk, xs + n, gk + row * d_key, d_key, nu, eps, lane);
+        __syncwarp();
+    }
 }
 
 template <typename T>
 cudaError_t launch_backward_t(const void *q, const void *k, const void *v, const void *beta, const float *W0,
                               const void *gy, const float *gWL, void *gq, void *gk, void *gv, void *gbeta,
-                              float *gW0, float *us, int BH, int L, int d_key, int nu, int d_v, float eps,
+                              float *gW0, float *scratch, int BH, int L, int d_key, int nu, int d_v, float eps,
                               cudaStream_t st) {
+    const int blocks = (d_v + kBwdRows - 1) / kBwdRows, d_dot = 2 * d_key * nu;
+    float *us = scratch, *part = scratch + (size_t)BH * L * d_v;
     const size_t smem = backward_smem_bytes(d_key, nu, d_v);
     auto kern = delta_backward_kernel<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(kern, dim3((unsigned)BH), dim3(kBwdThreads), smem, st, static_cast<const T *>(q),
-                      static_cast<const T *>(k), static_cast<const T *>(v), static_cast<const T *>(beta), W0,
-                      static_cast<const T *>(gy), gWL, static_cast<T *>(gq), static_cast<T *>(gk),
-                      static_cast<T *>(gv), static_cast<T *>(gbeta), gW0, us, L, d_key, nu, d_v, eps);
+    e = launch_pdl(kern, dim3((unsigned)BH, (unsigned)blocks), dim3(kBwdThreads), smem, st, static_cast<const T *>(q),
+                   static_cast<const T *>(k), static_cast<const T *>(v), static_cast<const T *>(beta), W0,
+                   static_cast<const T *>(gy), gWL, static_cast<T *>(gv), gW0, us, part, L, d_key, nu, d_v, eps);
+    if (e != cudaSuccess)
+        return e;
+    const size_t fsmem = sizeof(float) * kBwdWarps * (2 * (size_t)d_dot + 6 * (size_t)d_key);
+    auto fin = backward_finish_kernel<T>;
+    e = cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t rows = (int64_t)BH * L;
+    const unsigned grid = (unsigned)std::min<int64_t>((rows + kBwdWarps - 1) / kBwdWarps, 4096);
+    return launch_pdl(fin, dim3(grid), dim3(kBwdThreads), fsmem, st, static_cast<const T *>(q),
+                      static_cast<const T *>(k), (const float *)part, static_cast<T *>(gq), static_cast<T *>(gk),
+                      static_cast<T *>(gbeta), rows, blocks, d_key, nu, eps);
 }
 
 } // namespace
 
-// Shared memory of one CTA: W and gW, four d_dot vectors, two d_v vectors,
-// the x scratch and two staged copies of one token's inputs.
+// Shared memory of one CTA of the first kernel: its rows of W and gW, two
+// d_dot vectors, two row vectors, the x scratch and two staged copies of one
+// token's inputs.
 size_t backward_smem_bytes(int d_key, int nu, int d_v) {
-    const size_t d_dot = (size_t)2 * d_key * nu, ntok = 2 * (size_t)d_key + 3 * (size_t)d_v + 1;
-    return sizeof(float) * (2 * (size_t)d_v * d_dot + 4 * d_dot + 2 * (size_t)d_v + 4 * (size_t)d_key + 2 * ntok);
+    const size_t d_dot = (size_t)2 * d_key * nu, R = std::min(d_v, kBwdRows);
+    const size_t ntok = 2 * (size_t)d_key + 3 * R + 1;
+    return sizeof(float) * (2 * R * d_dot + 2 * d_dot + 2 * (size_t)kBwdRows + 4 * (size_t)d_key + 2 * ntok);
+}
+
+// Global scratch: u_t for every token and row, then the row blocks' partial
+// sums per token.
+size_t backward_workspace_bytes(int BH, int L, int d_key, int nu, int d_v) {
+    const size_t d_dot = (size_t)2 * d_key * nu, blocks = (d_v + kBwdRows - 1) / kBwdRows;
+    return sizeof(float) * ((size_t)BH * L * d_v + blocks * BH * L * (2 * d_dot + 4));
 }
 
 cudaError_t launch_backward(const void *q, const void *k, const void *v, const void *beta, const float *W0,

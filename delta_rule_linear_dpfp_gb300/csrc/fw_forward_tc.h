@@ -44,6 +44,7 @@ cudaError_t tc_linear_launch(const void *q, const void *k, const void *v, const 
 // CTA per (b,h) with W and its gradient in shared memory.  scratch holds u_t
 // for every token (BH * L * d_v floats).  Arguments validated by the caller.
 size_t backward_smem_bytes(int d_key, int nu, int d_v);
+size_t backward_workspace_bytes(int BH, int L, int d_key, int nu, int d_v);
 cudaError_t launch_backward(const void *q, const void *k, const void *v, const void *beta, const float *W0,
                             const void *gy, const float *gWL, void *gq, void *gk, void *gv, void *gbeta,
                             float *gW0, float *scratch, int BH, int L, int d_key, int nu, int d_v, int bf16,

@@ -49,6 +49,8 @@ CASES = [  # B, H, L, d_key, nu, d_v
     (1, 1, 40, 64, 3, 64),
     (1, 1, 33, 128, 1, 16),
     (2, 1, 20, 8, 5, 128),
+    (1, 3, 45, 32, 1, 40),      # row blocks of 16, 16 and 8
+    (1, 2, 30, 64, 4, 128),     # d_dot 512 with d_v 128: 8 row blocks
 ]
 
 
