@@ -129,12 +129,13 @@ FW_DEV void for_elements(int nel, int d_dot, int tid, F f) {
     }
 }
 
-// Row dot products x[r] = A[r] . p (and y[r] = B[r] . p when B is given)
-// for every row: warp w takes rows w, w + 8, ... (up to 8 per warp); the
-// lanes stride the columns and the rows' sums are reduced together.
-FW_DEV void row_dots2(const float *A, const float *B, const float *p, float *x, float *y, int d_v, int d_dot,
-                      int warp, int lane) {
-    constexpr int kMaxRows = 8; // rows <= 64
+// Row dot products a = A[r] . p and, with HAS_B, b = B[r] . p for every row,
+// then fin(r, a, b) on lane 0 of the warp that owns the row; warp w takes
+// rows w and w + 8 (rows <= 16).
+template <bool HAS_B, typename F>
+FW_DEV void row_dots_fin(const float *A, const float *B, const float *p, int rows, int d_dot, int warp, int lane,
+                         F fin) {
+    constexpr int kMaxRows = (kBwdRows + kBwdWarps - 1) / kBwdWarps;
     float sa[kMaxRows], sb[kMaxRows];
 #pragma unroll
     for (int i = 0; i < kMaxRows; ++i) {
@@ -146,9 +147,9 @@ FW_DEV void row_dots2(const float *A, const float *B, const float *p, float *x, 
 #pragma unroll
         for (int i = 0; i < kMaxRows; ++i) {
             const int r = warp + kBwdWarps * i;
-            if (r < d_v) {
+            if (r < rows) {
                 sa[i] = fmaf(A[r * d_dot + m], pm, sa[i]);
-                if (B)
+                if (HAS_B)
                     sb[i] = fmaf(B[r * d_dot + m], pm, sb[i]);
             }
         }
@@ -158,18 +159,16 @@ FW_DEV void row_dots2(const float *A, const float *B, const float *p, float *x, 
 #pragma unroll
         for (int i = 0; i < kMaxRows; ++i) {
             sa[i] += __shfl_xor_sync(0xffffffffu, sa[i], o);
-            sb[i] += __shfl_xor_sync(0xffffffffu, sb[i], o);
+            if (HAS_B)
+                sb[i] += __shfl_xor_sync(0xffffffffu, sb[i], o);
         }
     }
     if (lane == 0) {
 #pragma unroll
         for (int i = 0; i < kMaxRows; ++i) {
             const int r = warp + kBwdWarps * i;
-            if (r < d_v) {
-                x[r] = sa[i];
-                if (B)
-                    y[r] = sb[i];
-            }
+            if (r < rows)
+                fin(r, sa[i], sb[i]);
         }
     }
 }
@@ -290,13 +289,11 @@ __global__ void __launch_bounds__(kBwdThreads)
             dpfp_warp(tk, xk, pk, d_key, nu, eps, lane);
         __syncthreads();
         const float bt = tk[ntok - 1];
-        row_dots2(W, nullptr, pk, aa, nullptr, R, d_dot, warp, lane); // a = W_{t-1} phi(k)
-        __syncthreads();
-        for (int r = tid; r < R; r += kBwdThreads) { // u = beta (v - a)
-            const float u = bt * (tv[r] - aa[r]);
+        row_dots_fin<false>(W, nullptr, pk, R, d_dot, warp, lane, [&](int r, float a, float) { // u = beta (v - W_{t-1} phi(k))
+            const float u = bt * (tv[r] - a);
             gu[r] = u;
             ub[(int64_t)t * d_v + r] = u;
-        }
+        });
         __syncthreads();
         for_elements(nel, d_dot, tid, [&](int e, int r, int m) { W[e] = fmaf(gu[r], pk[m], W[e]); }); // W_t = W_{t-1} + u phi(k)^T
         stage(t + 1, nxt);
@@ -316,30 +313,31 @@ __global__ void __launch_bounds__(kBwdThreads)
             dpfp_warp(tk, xk, pk, d_key, nu, eps, lane);
         else if (warp == 1)
             dpfp_warp(tq, xq, pq, d_key, nu, eps, lane);
-        __syncthreads();
-        for (int m = tid; m < d_dot; m += kBwdThreads) // this block's share of g_phi(q) = W_t^T gy
-            pt[m] = col_sum(W, tg, nullptr, nullptr, m, R, d_dot);
-        __syncthreads(); // W_t is read above before it is stepped back below
+        else // meanwhile this block's share of g_phi(q) = W_t^T gy
+            for (int m = tid - 64; m < d_dot; m += kBwdThreads - 64)
+                pt[m] = col_sum(W, tg, nullptr, nullptr, m, R, d_dot);
+        __syncthreads(); // phi ready; W_t read above before it is stepped back below
         for_elements(nel, d_dot, tid, [&](int e, int r, int m) { // gW += gy phi(q)^T; W_{t-1} = W_t - u phi(k)^T
             G[e] = fmaf(tg[r], pq[m], G[e]);
             W[e] = fmaf(-tu[r], pk[m], W[e]);
         });
         __syncthreads();
-        row_dots2(G, W, pk, gu, aa, R, d_dot, warp, lane); // gu = gW phi(k), a = W_{t-1} phi(k)
+        row_dots_fin<true>(G, W, pk, R, d_dot, warp, lane, [&](int r, float g, float a) { // gu = gW phi(k), a = W_{t-1} phi(k)
+            gu[r] = g;
+            aa[r] = a;
+        });
         __syncthreads();
-        if (warp == 0) { // this block's share of gbeta = gu . (v - a)
-            float acc = 0.f;
-            for (int r = lane; r < R; r += 32)
-                acc = fmaf(gu[r], tv[r] - aa[r], acc);
-            acc = warp_sum(acc);
+        if (warp == 0) { // R <= 32 rows, one lane each
+            const int r = lane;
+            const float g = r < R ? gu[r] : 0.f;
+            const float acc = warp_sum(r < R ? g * (tv[r] - aa[r]) : 0.f); // this block's share of gbeta
             if (lane == 0)
                 pt[2 * d_dot] = acc;
-        }
-        __syncthreads();
-        for (int r = tid; r < R; r += kBwdThreads) { // gv = beta gu; keep e = beta gu (and -e)
-            gu[r] *= bt;
-            aa[r] = -gu[r];
-            io<T>::store(gv + (bh * L + t) * d_v + r0 + r, gu[r]);
+            if (r < R) { // gv = beta gu; keep e = beta gu (and -e)
+                gu[r] = g * bt;
+                aa[r] = -g * bt;
+                io<T>::store(gv + (bh * L + t) * d_v + r0 + r, g * bt);
+            }
         }
         __syncthreads();
         for (int m = tid; m < d_dot; m += kBwdThreads) // this block's share of g_phi(k) = gW^T u - W_{t-1}^T e
