@@ -306,9 +306,9 @@ __global__ void __launch_bounds__(kBwdThreads)
     for (int t = L - 1; t >= 0; --t) {
         fetch(t - 1, true, nxt);
         const float *tk = stg + (t & 1) * ntok, *tq = tk + d_key, *tv = tq + d_key, *tg = tv + R, *tu = tg + R;
-        const float bt = tk[ntok - 1];
         float *pt = pb + (size_t)t * pst;
-        __syncthreads();
+        __syncthreads(); // token t's inputs were staged by every thread at the end of the previous step
+        const float bt = tk[ntok - 1];
         if (warp == 0)
             dpfp_warp(tk, xk, pk, d_key, nu, eps, lane);
         else if (warp == 1)
