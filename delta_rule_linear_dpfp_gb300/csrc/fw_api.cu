@@ -321,9 +321,12 @@ FW_API int fw_delta_backward(const void *q, const void *k, const void *v, const 
     const size_t need = fw_delta_backward_workspace_size(B, H, L, d_key, nu, d_v, io_dtype);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need)
         return FW_ERR_INVALID_ARG;
+    DeviceInfo di;
+    if (device_info(&di) != cudaSuccess)
+        return FW_ERR_CUDA;
     return cuda_status(fw::launch_backward(q, k, v, beta, W0, dy, dW_final, dq, dk, dv, dbeta, dW0,
                                            static_cast<float *>(workspace), (int)BH, L, d_key, nu, d_v,
-                                           io_dtype == FW_DTYPE_BF16, eps, st));
+                                           io_dtype == FW_DTYPE_BF16, eps, di.num_sms, st));
 }
 
 namespace {

@@ -20,7 +20,9 @@
 // shared memory (fp32) for the whole sequence and writes, per token, its
 // partial sums over its rows; a second kernel adds the blocks' partials in
 // block order (deterministic) and takes the DPFP backward of q and k, one
-// warp per token.  The forward sweep keeps u_t for every token (global
+// warp per token.  phi(k_t) and phi(q_t) of every token are made first by
+// the DPFP kernel (fp32, in the scratch), so the serial token loop only
+// stages them.  The forward sweep keeps u_t for every token (global
 // scratch); the reverse sweep steps W back exactly as the forward stepped it
 // up (W_{t-1} = W_t - u_t phi(k_t)^T, one rounding per element and token).
 // Row dot products take one warp per row, column sums one thread per column
@@ -31,6 +33,7 @@
 #include "fw_forward_tc.h"
 
 #include <algorithm>
+#include <type_traits>
 
 namespace fw {
 
@@ -39,34 +42,7 @@ namespace {
 constexpr int kBwdThreads = 256;
 constexpr int kBwdWarps = kBwdThreads / 32;
 constexpr int kBwdRows = 16;  // rows of W per CTA
-
-// phi of one row by one warp from its d_key raw values in shared memory
-// (kr): x = ReLU([k, -k]) into xs, phi into ph.  Block i of phi holds
-// x[j] * x[(j - i) mod n].
-FW_DEV void dpfp_warp(const float *kr, float *xs, float *ph, int d_key, int nu, float eps, int lane) {
-    const int n = 2 * d_key, d_dot = n * nu;
-    for (int j = lane; j < d_key; j += 32) {
-        const float kv = kr[j];
-        xs[j] = fmaxf(kv, 0.f);
-        xs[d_key + j] = fmaxf(-kv, 0.f);
-    }
-    __syncwarp();
-    float s = 0.f;
-    int i = lane / n + 1, j = lane - (i - 1) * n; // m = (i - 1) n + j, stepped by 32
-    for (int m = lane; m < d_dot; m += 32) {
-        const int src = j - i < 0 ? j - i + n : j - i;
-        const float p = xs[j] * xs[src];
-        ph[m] = p;
-        s += p;
-        for (j += 32; j >= n; j -= n)
-            ++i;
-    }
-    s = warp_sum(s);
-    const float inv = 1.0f / (s + eps);
-    for (int m = lane; m < d_dot; m += 32)
-        ph[m] *= inv;
-    __syncwarp();
-}
+constexpr int kStageLoads = 9; // staged entries per thread: 2 d_dot + 3 * 16 + 1 <= 9 * 256 for d_dot <= 1024
 
 // The DPFP backward of one row by one warp: given g = dL/dphi and the raw row
 // kr (both in shared memory), writes dL/dk to dst.  xs: scratch of 2 d_key.
@@ -194,68 +170,64 @@ FW_DEV float col_sum(const float *a, const float *b, const float *c, const float
     return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
-// Block z of rows [r0, r0 + R) of one (batch, head).  part: [blocks][BH][L]
-// [2 d_dot + 4]: per token this block's sums over its rows of g_phi(q) (first
-// d_dot), g_phi(k) (next d_dot) and gbeta (at 2 d_dot).
+// Block z of rows [r0, r0 + R) of one (batch, head).  phk, phq: phi(k),
+// phi(q) of every token ([BH, L, d_dot] fp32, made by the DPFP kernel
+// beforehand).  part: [blocks][BH][L][2 d_dot + 4]: per token this block's
+// sums over its rows of g_phi(q) (first d_dot), g_phi(k) (next d_dot) and
+// gbeta (at 2 d_dot).
 template <typename T>
-__global__ void __launch_bounds__(kBwdThreads)
-    delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    delta_backward_kernel(const float *__restrict__ phk, const float *__restrict__ phq, const T *__restrict__ v,
                           const T *__restrict__ beta, const float *__restrict__ W0, const T *__restrict__ gy,
                           const float *__restrict__ gWL, T *__restrict__ gv, float *__restrict__ gW0,
-                          float *__restrict__ us, float *__restrict__ part, int L, int d_key, int nu, int d_v,
-                          float eps) {
+                          float *__restrict__ us, float *__restrict__ part, int L, int d_dot, int d_v) {
     extern __shared__ float sm[];
-    const int d_dot = 2 * d_key * nu, n = 2 * d_key;
     const int r0 = blockIdx.y * kBwdRows, R = min(kBwdRows, d_v - r0);
     const int nel = R * d_dot;
     const int64_t BH = gridDim.x, bh = blockIdx.x;
     const size_t pst = 2 * (size_t)d_dot + 4; // floats per token in part
-    // one token's inputs, staged: k, q (d_key each), v, gy, u (R each), beta
-    const int ntok = 2 * d_key + 3 * R + 1;
+    // one token's inputs, staged: phi(k), phi(q) (d_dot each), v, gy, u (R each), beta
+    const int ntok = 2 * d_dot + 3 * R + 1;
     float *W = sm;                 // [R][d_dot] rows r0.. of the state W_t
     float *G = W + nel;            // [R][d_dot] the same rows of dL/dW_t
-    float *pk = G + nel;           // phi(k_t)
-    float *pq = pk + d_dot;        // phi(q_t)
-    float *gu = pq + d_dot;        // dL/du_t, then beta_t dL/du_t
+    float *gu = G + nel;           // dL/du_t, then beta_t dL/du_t
     float *aa = gu + kBwdRows;     // W_{t-1} phi(k_t)
-    float *xk = aa + kBwdRows;     // x of k_t (one warp's scratch)
-    float *xq = xk + n;            // x of q_t
-    float *stg = xq + n;           // [2][ntok] staged token inputs (double-buffered)
+    float *stg = aa + kBwdRows;    // [2][ntok] staged token inputs (double-buffered)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const T *qb = q + bh * L * d_key, *kb = k + bh * L * d_key, *vb = v + bh * L * d_v + r0, *bb = beta + bh * L;
-    const T *gyb = gy + bh * L * d_v + r0;
+    const float *pkb = phk + bh * L * d_dot, *pqb = phq + bh * L * d_dot;
+    const T *vb = v + bh * L * d_v + r0, *bb = beta + bh * L, *gyb = gy + bh * L * d_v + r0;
     float *ub = us + bh * L * d_v + r0;
     float *pb = part + ((size_t)blockIdx.y * BH + bh) * L * pst;
 
-    // Thread tid loads entries tid and tid + 256 of token t's staged vector
-    // into registers; they are stored to shared memory one phase later, so
+    // Thread tid loads entries tid, tid + 256, ... of token t's staged vector
+    // into registers; they are stored to shared memory one token later, so
     // the load latency hides behind the current token's work.
-    auto fetch = [&](int t, bool reverse, float (&x)[2]) {
+    auto fetch = [&](int t, bool reverse, float (&x)[kStageLoads]) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kStageLoads; ++h) {
             const int e = tid + h * kBwdThreads;
             float val = 0.f;
             if (t >= 0 && t < L && e < ntok) {
-                if (e < d_key)
-                    val = io<T>::load(kb + (int64_t)t * d_key + e);
-                else if (e < 2 * d_key)
-                    val = reverse ? io<T>::load(qb + (int64_t)t * d_key + e - d_key) : 0.f;
-                else if (e < 2 * d_key + R)
-                    val = io<T>::load(vb + (int64_t)t * d_v + e - 2 * d_key);
-                else if (e < 2 * d_key + 2 * R)
-                    val = reverse ? io<T>::load(gyb + (int64_t)t * d_v + e - 2 * d_key - R) : 0.f;
-                else if (e < 2 * d_key + 3 * R)
-                    val = reverse ? __ldcg(ub + (int64_t)t * d_v + e - 2 * d_key - 2 * R) : 0.f;
+                if (e < d_dot)
+                    val = __ldcg(pkb + (int64_t)t * d_dot + e);
+                else if (e < 2 * d_dot)
+                    val = reverse ? __ldcg(pqb + (int64_t)t * d_dot + e - d_dot) : 0.f;
+                else if (e < 2 * d_dot + R)
+                    val = io<T>::load(vb + (int64_t)t * d_v + e - 2 * d_dot);
+                else if (e < 2 * d_dot + 2 * R)
+                    val = reverse ? io<T>::load(gyb + (int64_t)t * d_v + e - 2 * d_dot - R) : 0.f;
+                else if (e < 2 * d_dot + 3 * R)
+                    val = reverse ? __ldcg(ub + (int64_t)t * d_v + e - 2 * d_dot - 2 * R) : 0.f;
                 else
                     val = io<T>::load(bb + t);
             }
             x[h] = val;
         }
     };
-    auto stage = [&](int t, const float (&x)[2]) {
+    auto stage = [&](int t, const float (&x)[kStageLoads]) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kStageLoads; ++h) {
             const int e = tid + h * kBwdThreads;
             if (e < ntok)
                 stg[(t & 1) * ntok + e] = x[h];
@@ -264,8 +236,8 @@ __global__ void __launch_bounds__(kBwdThreads)
 
     griddep_launch_dependents();
     griddep_wait();
-    qb = after_wait(qb);
-    kb = after_wait(kb);
+    pkb = after_wait(pkb);
+    pqb = after_wait(pqb);
     vb = after_wait(vb);
     bb = after_wait(bb);
     gyb = after_wait(gyb);
@@ -277,18 +249,15 @@ __global__ void __launch_bounds__(kBwdThreads)
         W[e] = W0 ? __ldcg(W0 + wofs + e) : 0.f;
         G[e] = gWL ? __ldcg(gWL + wofs + e) : 0.f;
     }
-    float nxt[2];
+    float nxt[kStageLoads];
     // ---- forward sweep: keep u_t
     fetch(0, false, nxt);
     stage(0, nxt);
     for (int t = 0; t < L; ++t) {
         fetch(t + 1, false, nxt);
-        const float *tk = stg + (t & 1) * ntok, *tv = tk + 2 * d_key;
-        __syncthreads();
-        if (warp == 0)
-            dpfp_warp(tk, xk, pk, d_key, nu, eps, lane);
-        __syncthreads();
-        const float bt = tk[ntok - 1];
+        const float *pk = stg + (t & 1) * ntok, *tv = pk + 2 * d_dot;
+        __syncthreads(); // token t's inputs were staged by every thread at the end of the previous step
+        const float bt = pk[ntok - 1];
         row_dots_fin<false>(W, nullptr, pk, R, d_dot, warp, lane, [&](int r, float a, float) { // u = beta (v - W_{t-1} phi(k))
             const float u = bt * (tv[r] - a);
             gu[r] = u;
@@ -301,22 +270,16 @@ __global__ void __launch_bounds__(kBwdThreads)
     __syncthreads(); // the u_t written above are read back below by other threads
     // ---- reverse sweep
     fetch(L - 1, true, nxt);
-    __syncthreads();
     stage(L - 1, nxt);
     for (int t = L - 1; t >= 0; --t) {
         fetch(t - 1, true, nxt);
-        const float *tk = stg + (t & 1) * ntok, *tq = tk + d_key, *tv = tq + d_key, *tg = tv + R, *tu = tg + R;
+        const float *pk = stg + (t & 1) * ntok, *pq = pk + d_dot, *tv = pq + d_dot, *tg = tv + R, *tu = tg + R;
         float *pt = pb + (size_t)t * pst;
         __syncthreads(); // token t's inputs were staged by every thread at the end of the previous step
-        const float bt = tk[ntok - 1];
-        if (warp == 0)
-            dpfp_warp(tk, xk, pk, d_key, nu, eps, lane);
-        else if (warp == 1)
-            dpfp_warp(tq, xq, pq, d_key, nu, eps, lane);
-        else // meanwhile this block's share of g_phi(q) = W_t^T gy
-            for (int m = tid - 64; m < d_dot; m += kBwdThreads - 64)
-                pt[m] = col_sum(W, tg, nullptr, nullptr, m, R, d_dot);
-        __syncthreads(); // phi ready; W_t read above before it is stepped back below
+        const float bt = pk[ntok - 1];
+        for (int m = tid; m < d_dot; m += kBwdThreads) // this block's share of g_phi(q) = W_t^T gy
+            pt[m] = col_sum(W, tg, nullptr, nullptr, m, R, d_dot);
+        __syncthreads(); // W_t read above before it is stepped back below
         for_elements(nel, d_dot, tid, [&](int e, int r, int m) { // gW += gy phi(q)^T; W_{t-1} = W_t - u phi(k)^T
             G[e] = fmaf(tg[r], pq[m], G[e]);
             W[e] = fmaf(-tu[r], pk[m], W[e]);
@@ -396,17 +359,25 @@ template <typename T>
 cudaError_t launch_backward_t(const void *q, const void *k, const void *v, const void *beta, const float *W0,
                               const void *gy, const float *gWL, void *gq, void *gk, void *gv, void *gbeta,
                               float *gW0, float *scratch, int BH, int L, int d_key, int nu, int d_v, float eps,
-                              cudaStream_t st) {
+                              int num_sms, cudaStream_t st) {
     const int blocks = (d_v + kBwdRows - 1) / kBwdRows, d_dot = 2 * d_key * nu;
-    float *us = scratch, *part = scratch + (size_t)BH * L * d_v;
-    const size_t smem = backward_smem_bytes(d_key, nu, d_v);
-    auto kern = delta_backward_kernel<T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const int64_t rows = (int64_t)BH * L;
+    float *us = scratch, *phk = us + (size_t)rows * d_v, *phq = phk + (size_t)rows * d_dot;
+    float *part = phq + (size_t)rows * d_dot;
+    const int bf16 = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
+    cudaError_t e = launch_dpfp(k, phk, rows, d_key, nu, bf16, 0, eps, num_sms, st);
+    if (e == cudaSuccess)
+        e = launch_dpfp(q, phq, rows, d_key, nu, bf16, 0, eps, num_sms, st);
     if (e != cudaSuccess)
         return e;
-    e = launch_pdl(kern, dim3((unsigned)BH, (unsigned)blocks), dim3(kBwdThreads), smem, st, static_cast<const T *>(q),
-                   static_cast<const T *>(k), static_cast<const T *>(v), static_cast<const T *>(beta), W0,
-                   static_cast<const T *>(gy), gWL, static_cast<T *>(gv), gW0, us, part, L, d_key, nu, d_v, eps);
+    const size_t smem = backward_smem_bytes(d_key, nu, d_v);
+    auto kern = delta_backward_kernel<T>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    e = launch_pdl(kern, dim3((unsigned)BH, (unsigned)blocks), dim3(kBwdThreads), smem, st, (const float *)phk,
+                   (const float *)phq, static_cast<const T *>(v), static_cast<const T *>(beta), W0,
+                   static_cast<const T *>(gy), gWL, static_cast<T *>(gv), gW0, us, part, L, d_dot, d_v);
     if (e != cudaSuccess)
         return e;
     const size_t fsmem = sizeof(float) * kBwdWarps * (2 * (size_t)d_dot + 6 * (size_t)d_key);
@@ -414,7 +385,6 @@ cudaError_t launch_backward_t(const void *q, const void *k, const void *v, const
     e = cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
     if (e != cudaSuccess)
         return e;
-    const int64_t rows = (int64_t)BH * L;
     const unsigned grid = (unsigned)std::min<int64_t>((rows + kBwdWarps - 1) / kBwdWarps, 4096);
     return launch_pdl(fin, dim3(grid), dim3(kBwdThreads), fsmem, st, static_cast<const T *>(q),
                       static_cast<const T *>(k), (const float *)part, static_cast<T *>(gq), static_cast<T *>(gk),
@@ -424,30 +394,30 @@ cudaError_t launch_backward_t(const void *q, const void *k, const void *v, const
 } // namespace
 
 // Shared memory of one CTA of the first kernel: its rows of W and gW, two
-// d_dot vectors, two row vectors, the x scratch and two staged copies of one
-// token's inputs.
+// row vectors and two staged copies of one token's inputs.
 size_t backward_smem_bytes(int d_key, int nu, int d_v) {
     const size_t d_dot = (size_t)2 * d_key * nu, R = std::min(d_v, kBwdRows);
-    const size_t ntok = 2 * (size_t)d_key + 3 * R + 1;
-    return sizeof(float) * (2 * R * d_dot + 2 * d_dot + 2 * (size_t)kBwdRows + 4 * (size_t)d_key + 2 * ntok);
+    const size_t ntok = 2 * d_dot + 3 * R + 1;
+    return sizeof(float) * (2 * R * d_dot + 2 * (size_t)kBwdRows + 2 * ntok);
 }
 
-// Global scratch: u_t for every token and row, then the row blocks' partial
-// sums per token.
+// Global scratch: u_t for every token and row, phi(k_t) and phi(q_t) for
+// every token, then the row blocks' partial sums per token.
 size_t backward_workspace_bytes(int BH, int L, int d_key, int nu, int d_v) {
     const size_t d_dot = (size_t)2 * d_key * nu, blocks = (d_v + kBwdRows - 1) / kBwdRows;
-    return sizeof(float) * ((size_t)BH * L * d_v + blocks * BH * L * (2 * d_dot + 4));
+    const size_t rows = (size_t)BH * L;
+    return sizeof(float) * (rows * d_v + 2 * rows * d_dot + blocks * rows * (2 * d_dot + 4));
 }
 
 cudaError_t launch_backward(const void *q, const void *k, const void *v, const void *beta, const float *W0,
                             const void *gy, const float *gWL, void *gq, void *gk, void *gv, void *gbeta,
                             float *gW0, float *scratch, int BH, int L, int d_key, int nu, int d_v, int bf16,
-                            float eps, cudaStream_t st) {
+                            float eps, int num_sms, cudaStream_t st) {
     if (bf16)
         return launch_backward_t<__nv_bfloat16>(q, k, v, beta, W0, gy, gWL, gq, gk, gv, gbeta, gW0, scratch, BH, L,
-                                                d_key, nu, d_v, eps, st);
+                                                d_key, nu, d_v, eps, num_sms, st);
     return launch_backward_t<float>(q, k, v, beta, W0, gy, gWL, gq, gk, gv, gbeta, gW0, scratch, BH, L, d_key, nu,
-                                    d_v, eps, st);
+                                    d_v, eps, num_sms, st);
 }
 
 } // namespace fw

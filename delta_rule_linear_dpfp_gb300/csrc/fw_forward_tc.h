@@ -48,7 +48,9 @@ size_t backward_workspace_bytes(int BH, int L, int d_key, int nu, int d_v);
 cudaError_t launch_backward(const void *q, const void *k, const void *v, const void *beta, const float *W0,
                             const void *gy, const float *gWL, void *gq, void *gk, void *gv, void *gbeta,
                             float *gW0, float *scratch, int BH, int L, int d_key, int nu, int d_v, int bf16,
-                            float eps, cudaStream_t st);
+                            float eps, int num_sms, cudaStream_t st);
+cudaError_t launch_dpfp(const void *x, void *phi, int64_t rows, int d_key, int nu, int in_bf16, int out_bf16,
+                        float eps, int num_sms, cudaStream_t st);
 
 // The dense layers run on one tcgen05 GEMM fed by TMA (fw_project.cu).  When
 // the output tiles alone would leave most SMs idle, K is split into slices
