@@ -26,7 +26,7 @@
 // scratch); the reverse sweep steps W back exactly as the forward stepped it
 // up (W_{t-1} = W_t - u_t phi(k_t)^T, one rounding per element and token).
 // Row dot products take one warp per row, column sums one thread per column
-// (deterministic order), updates one thread per element.  fp32 arithmetic on
+// (deterministic order), updates one thread per 4 elements.  fp32 arithmetic on
 // CUDA cores throughout: the token loop is serial, so the first kernel is
 // latency-bound, and the split multiplies the CTAs that hide that latency.
 #include "fw_common.cuh"
@@ -88,21 +88,26 @@ FW_DEV void dpfp_backward_warp(const float *kr, const float *g, float *xs, T *ds
     __syncwarp();
 }
 
-// f(e, r, m) for the elements e = r * d_dot + m this thread owns (e = tid,
-// tid + 512, ...), with (r, m) stepped without a division per element.
+// f(e4, r, m4) for the float4 groups e4 = r * d_dot / 4 + m4 this thread
+// owns (e4 = tid, tid + 256, ...); d_dot % 4 == 0.
 template <typename F>
-FW_DEV void for_elements(int nel, int d_dot, int tid, F f) {
-    const int dr = kBwdThreads / d_dot, dm = kBwdThreads - dr * d_dot;
-    int r = tid / d_dot, m = tid - r * d_dot;
-    for (int e = tid; e < nel; e += kBwdThreads) {
-        f(e, r, m);
+FW_DEV void for_groups(int nel, int d_dot, int tid, F f) {
+    const int g = d_dot / 4, ng = nel / 4;
+    const int dr = kBwdThreads / g, dm = kBwdThreads - dr * g;
+    int r = tid / g, m4 = tid - r * g;
+    for (int e4 = tid; e4 < ng; e4 += kBwdThreads) {
+        f(e4, r, m4);
         r += dr;
-        m += dm;
-        if (m >= d_dot) {
-            m -= d_dot;
+        m4 += dm;
+        if (m4 >= g) {
+            m4 -= g;
             ++r;
         }
     }
+}
+
+FW_DEV float4 fma4(float s, float4 x, float4 y) {
+    return make_float4(fmaf(s, x.x, y.x), fmaf(s, x.y, y.y), fmaf(s, x.z, y.z), fmaf(s, x.w, y.w));
 }
 
 // Row dot products a = A[r] . p and, with HAS_B, b = B[r] . p for every row,
@@ -118,15 +123,18 @@ FW_DEV void row_dots_fin(const float *A, const float *B, const float *p, int row
         sa[i] = 0.f;
         sb[i] = 0.f;
     }
-    for (int m = lane; m < d_dot; m += 32) {
-        const float pm = p[m];
+    for (int m = 4 * lane; m < d_dot; m += 128) { // d_dot % 4 == 0, 16-byte aligned rows and p
+        const float4 pm = *reinterpret_cast<const float4 *>(p + m);
 #pragma unroll
         for (int i = 0; i < kMaxRows; ++i) {
             const int r = warp + kBwdWarps * i;
             if (r < rows) {
-                sa[i] = fmaf(A[r * d_dot + m], pm, sa[i]);
-                if (HAS_B)
-                    sb[i] = fmaf(B[r * d_dot + m], pm, sb[i]);
+                const float4 x = *reinterpret_cast<const float4 *>(A + r * d_dot + m);
+                sa[i] = fmaf(x.x, pm.x, fmaf(x.y, pm.y, fmaf(x.z, pm.z, fmaf(x.w, pm.w, sa[i]))));
+                if (HAS_B) {
+                    const float4 y = *reinterpret_cast<const float4 *>(B + r * d_dot + m);
+                    sb[i] = fmaf(y.x, pm.x, fmaf(y.y, pm.y, fmaf(y.z, pm.z, fmaf(y.w, pm.w, sb[i]))));
+                }
             }
         }
     }
@@ -187,12 +195,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int64_t BH = gridDim.x, bh = blockIdx.x;
     const size_t pst = 2 * (size_t)d_dot + 4; // floats per token in part
     // one token's inputs, staged: phi(k), phi(q) (d_dot each), v, gy, u (R each), beta
-    const int ntok = 2 * d_dot + 3 * R + 1;
+    const int ntok = 2 * d_dot + 3 * R + 1, sstr = (ntok + 3) & ~3; // slot stride keeps phi 16-byte aligned
     float *W = sm;                 // [R][d_dot] rows r0.. of the state W_t
     float *G = W + nel;            // [R][d_dot] the same rows of dL/dW_t
     float *gu = G + nel;           // dL/du_t, then beta_t dL/du_t
     float *aa = gu + kBwdRows;     // W_{t-1} phi(k_t)
-    float *stg = aa + kBwdRows;    // [2][ntok] staged token inputs (double-buffered)
+    float *stg = aa + kBwdRows;    // [2][sstr] staged token inputs (double-buffered)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float *pkb = phk + bh * L * d_dot, *pqb = phq + bh * L * d_dot;
@@ -230,7 +238,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int h = 0; h < kStageLoads; ++h) {
             const int e = tid + h * kBwdThreads;
             if (e < ntok)
-                stg[(t & 1) * ntok + e] = x[h];
+                stg[(t & 1) * sstr + e] = x[h];
         }
     };
 
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     stage(0, nxt);
     for (int t = 0; t < L; ++t) {
         fetch(t + 1, false, nxt);
-        const float *pk = stg + (t & 1) * ntok, *tv = pk + 2 * d_dot;
+        const float *pk = stg + (t & 1) * sstr, *tv = pk + 2 * d_dot;
         __syncthreads(); // token t's inputs were staged by every thread at the end of the previous step
         const float bt = pk[ntok - 1];
         row_dots_fin<false>(W, nullptr, pk, R, d_dot, warp, lane, [&](int r, float a, float) { // u = beta (v - W_{t-1} phi(k))
@@ -264,7 +272,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             ub[(int64_t)t * d_v + r] = u;
         });
         __syncthreads();
-        for_elements(nel, d_dot, tid, [&](int e, int r, int m) { W[e] = fmaf(gu[r], pk[m], W[e]); }); // W_t = W_{t-1} + u phi(k)^T
+        for_groups(nel, d_dot, tid, [&](int e4, int r, int m4) { // W_t = W_{t-1} + u phi(k)^T
+            float4 *w = reinterpret_cast<float4 *>(W) + e4;
+            *w = fma4(gu[r], reinterpret_cast<const float4 *>(pk)[m4], *w);
+        });
         stage(t + 1, nxt);
     }
     __syncthreads(); // the u_t written above are read back below by other threads
@@ -273,16 +284,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     stage(L - 1, nxt);
     for (int t = L - 1; t >= 0; --t) {
         fetch(t - 1, true, nxt);
-        const float *pk = stg + (t & 1) * ntok, *pq = pk + d_dot, *tv = pq + d_dot, *tg = tv + R, *tu = tg + R;
+        const float *pk = stg + (t & 1) * sstr, *pq = pk + d_dot, *tv = pq + d_dot, *tg = tv + R, *tu = tg + R;
         float *pt = pb + (size_t)t * pst;
         __syncthreads(); // token t's inputs were staged by every thread at the end of the previous step
         const float bt = pk[ntok - 1];
         for (int m = tid; m < d_dot; m += kBwdThreads) // this block's share of g_phi(q) = W_t^T gy
             pt[m] = col_sum(W, tg, nullptr, nullptr, m, R, d_dot);
         __syncthreads(); // W_t read above before it is stepped back below
-        for_elements(nel, d_dot, tid, [&](int e, int r, int m) { // gW += gy phi(q)^T; W_{t-1} = W_t - u phi(k)^T
-            G[e] = fmaf(tg[r], pq[m], G[e]);
-            W[e] = fmaf(-tu[r], pk[m], W[e]);
+        for_groups(nel, d_dot, tid, [&](int e4, int r, int m4) { // gW += gy phi(q)^T; W_{t-1} = W_t - u phi(k)^T
+            float4 *g = reinterpret_cast<float4 *>(G) + e4, *w = reinterpret_cast<float4 *>(W) + e4;
+            *g = fma4(tg[r], reinterpret_cast<const float4 *>(pq)[m4], *g);
+            *w = fma4(-tu[r], reinterpret_cast<const float4 *>(pk)[m4], *w);
         });
         __syncthreads();
         row_dots_fin<true>(G, W, pk, R, d_dot, warp, lane, [&](int r, float g, float a) { // gu = gW phi(k), a = W_{t-1} phi(k)
@@ -306,7 +318,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int m = tid; m < d_dot; m += kBwdThreads) // this block's share of g_phi(k) = gW^T u - W_{t-1}^T e
             pt[d_dot + m] = col_sum(G, tu, W, aa, m, R, d_dot);
         __syncthreads();
-        for_elements(nel, d_dot, tid, [&](int e, int r, int m) { G[e] = fmaf(-gu[r], pk[m], G[e]); }); // gW_{t-1} = gW - e phi(k)^T
+        for_groups(nel, d_dot, tid, [&](int e4, int r, int m4) { // gW_{t-1} = gW - e phi(k)^T
+            float4 *g = reinterpret_cast<float4 *>(G) + e4;
+            *g = fma4(-gu[r], reinterpret_cast<const float4 *>(pk)[m4], *g);
+        });
         if (t > 0)
             stage(t - 1, nxt);
     }
@@ -397,8 +412,8 @@ cudaError_t launch_backward_t(const void *q, const void *k, const void *v, const
 // row vectors and two staged copies of one token's inputs.
 size_t backward_smem_bytes(int d_key, int nu, int d_v) {
     const size_t d_dot = (size_t)2 * d_key * nu, R = std::min(d_v, kBwdRows);
-    const size_t ntok = 2 * d_dot + 3 * R + 1;
-    return sizeof(float) * (2 * R * d_dot + 2 * (size_t)kBwdRows + 2 * ntok);
+    const size_t ntok = 2 * d_dot + 3 * R + 1, sstr = (ntok + 3) & ~(size_t)3;
+    return sizeof(float) * (2 * R * d_dot + 2 * (size_t)kBwdRows + 2 * sstr);
 }
 
 // Global scratch: u_t for every token and row, phi(k_t) and phi(q_t) for

@@ -86,3 +86,16 @@ def test_backward_zero_beta():
     dq, dk, dv, db, dW0 = fw.fw_delta_backward(dd["q"], dd["k"], dd["v"], dd["beta"], dy, W0=dd["W0"], nu=1)
     assert torch.count_nonzero(dv) == 0 and torch.count_nonzero(dk) == 0
     assert torch.all(torch.isfinite(dq)) and torch.all(torch.isfinite(db))
+
+
+def test_backward_deterministic():
+    # fixed summation orders and no races: repeated calls give the same bits (bf16 and fp32 I/O)
+    for io in ("bf16", "f32"):
+        d = to_dev(inputs.random_forward_inputs(2, 4, 150, 64, 1, 64, io, w0_var=0.01, seed=11))
+        dy = torch.randn(2, 4, 150, 64, generator=torch.Generator().manual_seed(3)).to(inputs.torch_dtype(io)).cuda()
+        dWf = torch.randn(2, 4, 64, 128, generator=torch.Generator().manual_seed(4)).cuda()
+        first = fw.fw_delta_backward(d["q"], d["k"], d["v"], d["beta"], dy, W0=d["W0"], dW_final=dWf, nu=1)
+        for _ in range(4):
+            again = fw.fw_delta_backward(d["q"], d["k"], d["v"], d["beta"], dy, W0=d["W0"], dW_final=dWf, nu=1)
+            for a, b in zip(first, again):
+                assert torch.equal(a, b)

@@ -289,3 +289,15 @@ def test_decode_stepped_equals_forward():
     torch.cuda.synchronize()
     assert maxrel(f64(torch.stack(ys, 2)), f64(y)) <= 2e-2
     assert maxrel(f64(W), f64(Wf)) <= 2e-2
+
+
+def test_forward_deterministic():
+    # no atomics and fixed accumulation orders: repeated calls give the same bits
+    for name in ("b4h8_l512", "b2h8_l2048_nu3"):
+        cfg = inputs.FORWARD_CONFIGS[name]
+        d = to_dev(inputs.forward_inputs(name))
+        first = fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=d["W0"], nu=cfg["nu"], chunk=cfg["chunk"])
+        for _ in range(3):
+            again = fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=d["W0"], nu=cfg["nu"],
+                                        chunk=cfg["chunk"])
+            assert torch.equal(first[0], again[0]) and torch.equal(first[1], again[1])
