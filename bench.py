@@ -48,6 +48,8 @@ def parse():
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--stack-steps", type=int, default=0,
                    help="only run this many token steps of the 6-layer stack workload (for profilers), then exit")
+    p.add_argument("--backward-steps", type=int, default=0,
+                   help="only run this many backward calls on the b4h8_l512 workload (for profilers), then exit")
     return p.parse_args()
 
 
@@ -616,6 +618,25 @@ def stack_only(steps):
     print(json.dumps({"stack_steps": steps, "launches_per_step": 10 * nl + 2}))
 
 
+def backward_only(steps):
+    """`steps` fw_delta_backward calls on b4h8_l512 (bf16 I/O) through the public
+    API (4 launches each), nothing else: the command the backward's profiles
+    are captured from."""
+    from delta_rule_linear_dpfp_gb300 import binding as fw, build, inputs
+    build.build()
+    fw.load()
+    c = inputs.FORWARD_CONFIGS["b4h8_l512"]
+    B, H, L, d_key, nu, d_v = (c[n] for n in ("B", "H", "L", "d_key", "nu", "d_v"))
+    fi = {k: (None if v is None else v.cuda()) for k, v in inputs.forward_inputs("b4h8_l512").items()}
+    dy = torch.randn(B, H, L, d_v, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16).cuda()
+    ws = torch.empty(fw.fw_delta_backward_workspace_size(B, H, L, d_key, nu, d_v, torch.bfloat16), dtype=torch.uint8,
+                     device="cuda")
+    for _ in range(steps):
+        fw.fw_delta_backward(fi["q"], fi["k"], fi["v"], fi["beta"], dy, nu=nu, workspace=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"backward_steps": steps, "launches_per_step": 4}))
+
+
 # ------------------------------------------------------------ the oracle
 class OracleSample:
     """The fp64 CPU oracle on the host cores over a bounded sample of the
@@ -702,6 +723,9 @@ def main():
         return
     if args.stack_steps:
         stack_only(args.stack_steps)
+        return
+    if args.backward_steps:
+        backward_only(args.backward_steps)
         return
     if world > 1:
         torch.cuda.set_device(local_rank)

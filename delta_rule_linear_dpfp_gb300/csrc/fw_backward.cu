@@ -42,7 +42,6 @@ namespace {
 constexpr int kBwdThreads = 256;
 constexpr int kBwdWarps = kBwdThreads / 32;
 constexpr int kBwdRows = 16;  // rows of W per CTA
-constexpr int kStageLoads = 9; // staged entries per thread: 2 d_dot + 3 * 16 + 1 <= 9 * 256 for d_dot <= 1024
 
 // The DPFP backward of one row by one warp: given g = dL/dphi and the raw row
 // kr (both in shared memory), writes dL/dk to dst.  xs: scratch of 2 d_key.
@@ -183,7 +182,9 @@ FW_DEV float col_sum(const float *a, const float *b, const float *c, const float
 // beforehand).  part: [blocks][BH][L][2 d_dot + 4]: per token this block's
 // sums over its rows of g_phi(q) (first d_dot), g_phi(k) (next d_dot) and
 // gbeta (at 2 d_dot).
-template <typename T>
+// NH: staged entries per thread, the least with 256 NH >= 2 d_dot + 3 R + 1
+// (each token's staging costs NH loads and stores per thread).
+template <typename T, int NH>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     delta_backward_kernel(const float *__restrict__ phk, const float *__restrict__ phq, const T *__restrict__ v,
                           const T *__restrict__ beta, const float *__restrict__ W0, const T *__restrict__ gy,
@@ -211,9 +212,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // Thread tid loads entries tid, tid + 256, ... of token t's staged vector
     // into registers; they are stored to shared memory one token later, so
     // the load latency hides behind the current token's work.
-    auto fetch = [&](int t, bool reverse, float (&x)[kStageLoads]) {
+    auto fetch = [&](int t, bool reverse, float (&x)[NH]) {
 #pragma unroll
-        for (int h = 0; h < kStageLoads; ++h) {
+        for (int h = 0; h < NH; ++h) {
             const int e = tid + h * kBwdThreads;
             float val = 0.f;
             if (t >= 0 && t < L && e < ntok) {
@@ -233,9 +234,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             x[h] = val;
         }
     };
-    auto stage = [&](int t, const float (&x)[kStageLoads]) {
+    auto stage = [&](int t, const float (&x)[NH]) {
 #pragma unroll
-        for (int h = 0; h < kStageLoads; ++h) {
+        for (int h = 0; h < NH; ++h) {
             const int e = tid + h * kBwdThreads;
             if (e < ntok)
                 stg[(t & 1) * sstr + e] = x[h];
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         W[e] = W0 ? __ldcg(W0 + wofs + e) : 0.f;
         G[e] = gWL ? __ldcg(gWL + wofs + e) : 0.f;
     }
-    float nxt[kStageLoads];
+    float nxt[NH];
     // ---- forward sweep: keep u_t
     fetch(0, false, nxt);
     stage(0, nxt);
@@ -386,7 +387,12 @@ cudaError_t launch_backward_t(const void *q, const void *k, const void *v, const
     if (e != cudaSuccess)
         return e;
     const size_t smem = backward_smem_bytes(d_key, nu, d_v);
-    auto kern = delta_backward_kernel<T>;
+    const int ntok = 2 * d_dot + 3 * std::min(d_v, kBwdRows) + 1;
+    auto kern = ntok <= kBwdThreads       ? delta_backward_kernel<T, 1>
+                : ntok <= 2 * kBwdThreads ? delta_backward_kernel<T, 2>
+                : ntok <= 3 * kBwdThreads ? delta_backward_kernel<T, 3>
+                : ntok <= 5 * kBwdThreads ? delta_backward_kernel<T, 5>
+                                          : delta_backward_kernel<T, 9>; // d_dot <= 1024
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
