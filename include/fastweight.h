@@ -198,10 +198,11 @@ FW_API size_t fw_delta_backward_workspace_size(int B, int H, int L, int d_key, i
  *   dbeta    : [B, H, L]          io_dtype                  (written)
  *   dW0      : [B, H, d_v, d_dot] fp32 dL/dW0, or NULL to skip it
  *   workspace: device scratch of fw_delta_backward_workspace_size() bytes
- * fp32 arithmetic on CUDA cores for both I/O dtypes: one CTA per (batch,
- * head) and block of 16 rows of the state, with those rows of the state and
- * of its gradient in shared memory (128 * d_dot bytes, so d_dot <= 1024),
- * then one kernel that adds the blocks' shares and takes the DPFP backward.
+ * fp32 arithmetic on CUDA cores for both I/O dtypes: the DPFP map of every
+ * k and q first (fp32, into the workspace), then one CTA per (batch, head)
+ * and block of 16 rows of the state, with those rows of the state and of
+ * its gradient in shared memory (128 * d_dot bytes; d_dot <= 1024), then
+ * one kernel that adds the blocks' shares and takes the DPFP backward.
  * The result does not depend on the run (fixed summation orders).
  * Errors as for fw_delta_forward.
  */
