@@ -255,3 +255,11 @@ def test_stack_argument_checks(lib):
     bad.W, bad.b_o = 0x10000, 0x10004               # a misaligned bias
     assert _stack(lib, layers=(binding.FwStackLayer * 1)(bad)) == E
     assert _stack(lib, B=0, x=None, out=None, ws=None, wsb=0) == OK   # empty: nothing enqueued
+
+
+def test_backward_workspace_limits(lib):
+    ws = lib.fw_delta_backward_workspace_size
+    assert ws(2, 2, 16, 64, 1, 64, 1) > 0
+    assert ws(2, 2, 16, 128, 4, 200, 1) > 0       # d_dot 1024, d_v not a multiple of the row block
+    assert ws(2, 2, 16, 128, 5, 64, 1) == 0       # d_dot 1280 > 1024
+    assert ws(2, 2, 16, 12, 1, 64, 1) == 0        # d_key not compiled
