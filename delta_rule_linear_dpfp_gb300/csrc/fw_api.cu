@@ -10,8 +10,6 @@
 #include <mutex>
 
 namespace fw {
-cudaError_t launch_dpfp(const void *x, void *phi, int64_t rows, int d_key, int nu, int in_bf16,
-                        int out_bf16, float eps, int num_sms, cudaStream_t st);
 cudaError_t launch_rowscan(const void *q, const void *k, const void *v, const void *beta,
                            const float *W0, float *Wout, void *y, int BH, int L, int d_key, int nu,
                            int d_v, int bf16, float eps, cudaStream_t st);

@@ -200,8 +200,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     float *W = sm;                 // [R][d_dot] rows r0.. of the state W_t
     float *G = W + nel;            // [R][d_dot] the same rows of dL/dW_t
     float *gu = G + nel;           // dL/du_t, then beta_t dL/du_t
-    float *aa = gu + kBwdRows;     // W_{t-1} phi(k_t)
-    float *stg = aa + kBwdRows;    // [2][sstr] staged token inputs (double-buffered)
+    float *aa = gu + kBwdRows;     // W_{t-1} phi(k_t), then -beta_t dL/du_t
+    float *gbr = aa + kBwdRows;    // per row: dL/du_t (v_t - W_{t-1} phi(k_t)), the terms of gbeta
+    float *stg = gbr + kBwdRows;   // [2][sstr] staged token inputs (double-buffered)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float *pkb = phk + bh * L * d_dot, *pqb = phq + bh * L * d_dot;
@@ -298,26 +299,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             *w = fma4(-tu[r], reinterpret_cast<const float4 *>(pk)[m4], *w);
         });
         __syncthreads();
-        row_dots_fin<true>(G, W, pk, R, d_dot, warp, lane, [&](int r, float g, float a) { // gu = gW phi(k), a = W_{t-1} phi(k)
-            gu[r] = g;
-            aa[r] = a;
+        // g = gW phi(k), a = W_{t-1} phi(k); gv = beta g; keep e = beta g (and -e) and g (v - a)
+        row_dots_fin<true>(G, W, pk, R, d_dot, warp, lane, [&](int r, float g, float a) {
+            gu[r] = g * bt;
+            aa[r] = -g * bt;
+            gbr[r] = g * (tv[r] - a);
+            io<T>::store(gv + (bh * L + t) * d_v + r0 + r, g * bt);
         });
-        __syncthreads();
-        if (warp == 0) { // R <= 32 rows, one lane each
-            const int r = lane;
-            const float g = r < R ? gu[r] : 0.f;
-            const float acc = warp_sum(r < R ? g * (tv[r] - aa[r]) : 0.f); // this block's share of gbeta
-            if (lane == 0)
-                pt[2 * d_dot] = acc;
-            if (r < R) { // gv = beta gu; keep e = beta gu (and -e)
-                gu[r] = g * bt;
-                aa[r] = -g * bt;
-                io<T>::store(gv + (bh * L + t) * d_v + r0 + r, g * bt);
-            }
-        }
         __syncthreads();
         for (int m = tid; m < d_dot; m += kBwdThreads) // this block's share of g_phi(k) = gW^T u - W_{t-1}^T e
             pt[d_dot + m] = col_sum(G, tu, W, aa, m, R, d_dot);
+        if (warp == 0) { // and of gbeta (R <= 32 rows, one lane each, a fixed order)
+            const float acc = warp_sum(lane < R ? gbr[lane] : 0.f);
+            if (lane == 0)
+                pt[2 * d_dot] = acc;
+        }
         __syncthreads();
         for_groups(nel, d_dot, tid, [&](int e4, int r, int m4) { // gW_{t-1} = gW - e phi(k)^T
             float4 *g = reinterpret_cast<float4 *>(G) + e4;
@@ -414,12 +410,12 @@ cudaError_t launch_backward_t(const void *q, const void *k, const void *v, const
 
 } // namespace
 
-// Shared memory of one CTA of the first kernel: its rows of W and gW, two
+// Shared memory of one CTA of the first kernel: its rows of W and gW, three
 // row vectors and two staged copies of one token's inputs.
 size_t backward_smem_bytes(int d_key, int nu, int d_v) {
     const size_t d_dot = (size_t)2 * d_key * nu, R = std::min(d_v, kBwdRows);
     const size_t ntok = 2 * d_dot + 3 * R + 1, sstr = (ntok + 3) & ~(size_t)3;
-    return sizeof(float) * (2 * R * d_dot + 2 * (size_t)kBwdRows + 2 * sstr);
+    return sizeof(float) * (2 * R * d_dot + 3 * (size_t)kBwdRows + 2 * sstr);
 }
 
 // Global scratch: u_t for every token and row, phi(k_t) and phi(q_t) for

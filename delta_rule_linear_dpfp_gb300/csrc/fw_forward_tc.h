@@ -49,6 +49,8 @@ cudaError_t launch_backward(const void *q, const void *k, const void *v, const v
                             const void *gy, const float *gWL, void *gq, void *gk, void *gv, void *gbeta,
                             float *gW0, float *scratch, int BH, int L, int d_key, int nu, int d_v, int bf16,
                             float eps, int num_sms, cudaStream_t st);
+// K1, the standalone DPFP map: phi [rows, 2 d_key nu] of x [rows, d_key]
+// (bf16 or fp32 each way; arguments validated by the caller).
 cudaError_t launch_dpfp(const void *x, void *phi, int64_t rows, int d_key, int nu, int in_bf16, int out_bf16,
                         float eps, int num_sms, cudaStream_t st);
 
