@@ -70,6 +70,13 @@ FW_DEV void store8(__nv_bfloat16 *p, const float (&v)[8]) {
     *reinterpret_cast<uint4 *>(p) = u;
 }
 
+// Warm L2 with `bytes` from global memory (16-byte aligned address, a
+// multiple of 16 bytes): no data reaches the issuing thread, and L2 is the
+// point of coherence, so it is safe on data another kernel is still writing.
+FW_DEV void l2_prefetch(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // -------------------------------------------- programmatic dependent launch
 // The next kernel on the stream may start launching (it still waits in
 // griddep_wait before touching what this kernel writes).

@@ -77,6 +77,13 @@ __global__ void __launch_bounds__(256, kBlocksPerSM) dpfp_kernel(const Tin *__re
     const int64_t d_dot = (int64_t)N * nu;
     const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
     int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    // this warp's first rows are pulled into L2 while the preceding kernel
+    // finishes (a prefetch is safe before the wait: see l2_prefetch)
+    if (lane == 0 && wid * RPW < rows) {
+        const int64_t n = rows - wid * RPW < RPW ? rows - wid * RPW : RPW;
+        if ((DK * sizeof(Tin)) % 16 == 0)
+            l2_prefetch(xin + wid * RPW * DK, (uint32_t)(n * DK * sizeof(Tin)));
+    }
     griddep_launch_dependents();
     griddep_wait(); // x may be the preceding kernel's output
     xin = after_wait(xin);

@@ -292,6 +292,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     uint8_t *rec = ws + ((size_t)bh * nch + c) * rc.bytes;
     const uint32_t ncols = tmem_cols_pow2(max(64, Dp + d_v));
 
+    // This chunk's q, k and v rows are pulled into L2 while the preceding
+    // kernel finishes (a prefetch is safe before the wait: see l2_prefetch).
+    if (tid == 0) {
+        const size_t tok = (size_t)bh * L + t0;
+        l2_prefetch(k + tok * DK, (uint32_t)(Lc * DK * 2));
+        l2_prefetch(q + tok * DK, (uint32_t)(Lc * DK * 2));
+        if ((d_vr * 2) % 16 == 0)
+            l2_prefetch(v + tok * d_vr, (uint32_t)(Lc * d_vr * 2));
+    }
     griddep_wait(); // the inputs may be, and the workspace may still be read by, the preceding kernel
     q = after_wait(q);
     k = after_wait(k);
