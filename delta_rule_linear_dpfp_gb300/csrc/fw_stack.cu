@@ -21,7 +21,8 @@
 // dense layers run on the tcgen05 GEMM of fw_project.cu, the state update
 // on the decode kernel, the norms on the row kernel below; consecutive
 // kernels are chained by programmatic dependent launch, so one token of an
-// L-layer stack is 6 L + 1 launches that a caller can capture as one graph.
+// L-layer stack is 6 L + 2 operations (a split GEMM adds its reduction
+// kernel) that a caller can capture as one graph.
 // The residual stream is fp32; the activations the tensor cores read (a bf16
 // copy of x written beside it, y, LN output, the hidden layer) are bf16.
 #include "fw_forward_tc.h"

@@ -382,7 +382,10 @@ FW_API size_t fw_decode_stack_workspace_size(int B, int H, int d_key, int d_v, i
  * bf16), y = fw_delta_decode_step on the layer's W, x += y W_o + b_o,
  * x += relu(LN(x) W_1 + b_1) W_2 + b_2.  The residual stream x is fp32;
  * what the tensor cores read (x, y, LN(x), the hidden layer) is rounded to
- * bf16 and every product accumulates in fp32.  6 n_layers + 1 kernels,
+ * bf16 and every product accumulates in fp32.  Six operations per layer
+ * plus a cast and the final norm, each one kernel, or two when a dense
+ * layer's K is split across CTAs (a reduction kernel follows): 10 n_layers
+ * + 2 kernels at the 256-sequence, d_model 512 shape; all on `stream`,
  * chained by programmatic dependent launch (capturable in one CUDA graph).
  * Errors: FW_ERR_INVALID_ARG for bad sizes, NULL or unaligned pointers, a
  * small workspace; FW_ERR_UNSUPPORTED for d_key outside {8, 16, 32, 64, 128},
