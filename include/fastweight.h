@@ -165,8 +165,9 @@ FW_API size_t fw_delta_forward_projected_workspace_size(int B, int L, int d_mode
  *              bytes: the projected q, k, v, beta, then the forward's
  * q, k, v and beta are rounded to bf16 once (fp32 accumulation).
  * Errors as for fw_delta_forward; FW_ERR_INVALID_ARG also for d_model not a
- * multiple of 64 or a bad ldw.  Three kernels, chained by programmatic
- * dependent launch.
+ * multiple of 64 or a bad ldw.  The projections' GEMM (with a reduction
+ * kernel after it when B L is small and K is split across CTAs), then the
+ * forward's two kernels, chained by programmatic dependent launch.
  */
 FW_API int fw_delta_forward_projected(const void *x, const void *W_all, int ldw, const float *W0,
                                       float *W_final, void *y, void *workspace, size_t workspace_bytes,
