@@ -99,3 +99,17 @@ def test_backward_deterministic():
             again = fw.fw_delta_backward(d["q"], d["k"], d["v"], d["beta"], dy, W0=d["W0"], dW_final=dWf, nu=1)
             for a, b in zip(first, again):
                 assert torch.equal(a, b)
+
+
+def test_backward_bench_workload():
+    # the bench row's shape and launch configuration: B4 H8 L512 d_key 64 nu 1 d_v 64, bf16, W0 = 0
+    d = inputs.forward_inputs("b4h8_l512")
+    dd = to_dev(d)
+    dy = torch.randn(4, 8, 512, 64, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    got = fw.fw_delta_backward(dd["q"], dd["k"], dd["v"], dd["beta"], dy.cuda(), nu=1)
+    torch.cuda.synchronize()
+    want = oracle.delta_backward(f64(d["q"]), f64(d["k"]), f64(d["v"]), f64(d["beta"]), f64(dy), None, None, 1,
+                                 1e-6, NT)
+    for name, a, b in zip(["dq", "dk", "dv", "dbeta", "dW0"], got, want):
+        err = maxrel(f64(a), b)
+        assert err <= tol_for(torch.bfloat16), (name, err)
