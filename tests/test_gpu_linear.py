@@ -103,3 +103,9 @@ def test_linear_chunk_invariance():
                                  chunk=c)[0] for c in (16, 32, 64)]
     for o in outs[1:]:
         assert maxrel(f64(o), f64(outs[0])) <= TOL_BF16
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+def test_linear_bench_shapes(normalize):
+    # the bench row's shapes: B4 H8 L512 d_key 64 nu 1 d_v 64, bf16, from zero state
+    _check(inputs.linear_inputs(4, 8, 512, 64, 1, 64, seed=0), 1, normalize)
