@@ -7,7 +7,7 @@ oracle with a planted mistake and expects at least one to fail.
 None of these re-types the oracle's own loop: they compare it with
 hand-worked fractions (tests/golden/), with an FFT identity for the DPFP block
 sums, with closed forms and invariants of the recurrence, and with the
-independent chunked form O2 (oracle/chunked.py).
+independent chunked forms of the forward and the backward (oracle/chunked.py).
 """
 import json
 import os
@@ -236,6 +236,25 @@ def pin_chunked_equals_sequential(o, chunked):
                     sw = max(1.0, np.abs(W1).max())
                     assert np.abs(y2 - y1).max() <= 1e-12 * sy, (L, C, np.abs(y2 - y1).max())
                     assert np.abs(W2 - W1).max() <= 1e-12 * sw, (L, C)
+
+
+def pin_chunked_backward_equals_sequential(o, chunked_backward):
+    """The sequential backward (one token at a time, walked in reverse) equals
+    the chunked backward (the transpose of the WY chunk algebra) to rounding,
+    for every chunk length, with and without W0 and an incoming dW."""
+    rng = _rng(13)
+    for L in (1, 2, 5, 9):
+        for d_key, nu, d_v in [(2, 1, 1), (3, 2, 2), (4, 3, 5)]:
+            for with_w0 in (False, True):
+                q, k, v, beta, W0 = _rand_inputs(rng, 2, 1, L, d_key, nu, d_v, with_w0)
+                gy = rng.normal(size=v.shape)
+                gW = rng.normal(size=(2, 1, d_v, 2 * d_key * nu)) if with_w0 else None
+                want = o.delta_backward(q, k, v, beta, gy, W0, gW, nu, 1e-6)
+                for C in sorted({1, 2, 3, L}):
+                    got = chunked_backward(q, k, v, beta, gy, W0, gW, nu, 1e-6, C)
+                    for name, a, b in zip(("gq", "gk", "gv", "gbeta", "gW0"), got, want):
+                        scale = max(1.0, np.abs(b).max())
+                        assert np.abs(a - b).max() <= 1e-11 * scale, (L, C, name, np.abs(a - b).max())
 
 
 def pin_decode_stepped_equals_forward(o):

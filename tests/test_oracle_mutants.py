@@ -14,7 +14,7 @@ import pytest
 
 from oracle import OracleLib
 from oracle.build import SRC
-from oracle.chunked import delta_forward_chunked
+from oracle.chunked import delta_backward_chunked, delta_forward_chunked
 from tests import oracle_pins
 
 MUTANTS = {
@@ -75,7 +75,8 @@ def test_mutant_is_caught(tmp_path, name):
     o = _build_mutant(tmp_path, name, old, new)
     failed = []
     pins = list(oracle_pins.ALL_PINS) + [
-        lambda ob: oracle_pins.pin_chunked_equals_sequential(ob, delta_forward_chunked)]
+        lambda ob: oracle_pins.pin_chunked_equals_sequential(ob, delta_forward_chunked),
+        lambda ob: oracle_pins.pin_chunked_backward_equals_sequential(ob, delta_backward_chunked)]
     for pin in pins:
         try:
             pin(o)

@@ -2,7 +2,7 @@
 import pytest
 
 import oracle
-from oracle.chunked import delta_forward_chunked
+from oracle.chunked import delta_backward_chunked, delta_forward_chunked
 from tests import oracle_pins
 
 
@@ -13,6 +13,10 @@ def test_pin(pin):
 
 def test_chunked_equals_sequential():
     oracle_pins.pin_chunked_equals_sequential(oracle.lib(), delta_forward_chunked)
+
+
+def test_chunked_backward_equals_sequential():
+    oracle_pins.pin_chunked_backward_equals_sequential(oracle.lib(), delta_backward_chunked)
 
 
 def test_rejects_bad_nu():
