@@ -65,8 +65,9 @@ def peaks():
 
 
 def forward_flops_per_head_token(C, d_dot, d_v):
-    """Algorithmic FLOPs of the chunked form per (b,h,token): the C x C
-    triangular products counted at half."""
+    """Algorithmic FLOPs of the chunked form per (b,h,token): the chunk-local
+    part plus the scan's state products, the C x C triangular products counted
+    at half (only their lower triangle carries work)."""
     return prep_flops_per_head_token(C, d_dot, d_v) + scan_flops_per_head_token(d_dot, d_v)
 
 
