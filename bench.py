@@ -543,10 +543,11 @@ def measure_rows(fw, inputs, dev, stream, pk):
     wsb = torch.empty(nws, dtype=torch.uint8, device=dev)
     ms = _time(lambda i: fw.fw_delta_backward(fi["q"], fi["k"], fi["v"], fi["beta"], dyb, nu=nu, workspace=wsb,
                                               stream=stream), 20, stream)
-    # per head-token: the forward sweep (2 d_dot d_v) and the reverse sweep (about 12 d_dot d_v) in fp32
+    # the recurrence's own work per head-token, whatever the method: the forward sweep (2 d_dot d_v) and
+    # the reverse sweep (about 12 d_dot d_v), fp32
     flops = 14.0 * d_dot * d_v * B * H * L
     nbytes = B * H * L * 2 * (2 * 2 * d_key + 2 * 2 * d_v + 2) + B * H * d_v * d_dot * 4
-    r = roofline("fw_delta_backward (fp32, token-serial)", flops, nbytes, ms, pk)
+    r = roofline("fw_delta_backward (fp32, chunk-parallel)", flops, nbytes, ms, pk)
     r["tokens/s"] = B * L / (ms * 1e-3)
     rows["backward_b4h8_l512"] = r
     # the token-wise layer stack: one token of 256 sequences through 6 layers (d_model 512, 8 heads of 64,
@@ -621,7 +622,7 @@ def stack_only(steps):
 
 def backward_only(steps):
     """`steps` fw_delta_backward calls on b4h8_l512 (bf16 I/O) through the public
-    API (4 launches each), nothing else: the command the backward's profiles
+    API (7 launches each), nothing else: the command the backward's profiles
     are captured from."""
     from delta_rule_linear_dpfp_gb300 import binding as fw, build, inputs
     build.build()
@@ -635,7 +636,7 @@ def backward_only(steps):
     for _ in range(steps):
         fw.fw_delta_backward(fi["q"], fi["k"], fi["v"], fi["beta"], dy, nu=nu, workspace=ws)
     torch.cuda.synchronize()
-    print(json.dumps({"backward_steps": steps, "launches_per_step": 4}))
+    print(json.dumps({"backward_steps": steps, "launches_per_step": 7}))
 
 
 # ------------------------------------------------------------ the oracle

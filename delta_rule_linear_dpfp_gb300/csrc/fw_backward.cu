@@ -372,9 +372,12 @@ cudaError_t launch_backward_t(const void *q, const void *k, const void *v, const
                               const void *gy, const float *gWL, void *gq, void *gk, void *gv, void *gbeta,
                               float *gW0, float *scratch, int BH, int L, int d_key, int nu, int d_v, float eps,
                               int num_sms, cudaStream_t st) {
-    const int blocks = (d_v + kBwdRows - 1) / kBwdRows, d_dot = 2 * d_key * nu;
+    const bool chunked = backward_chunked_supported(d_key, nu, d_v, L);
+    const int blocks = chunked ? 1 : (d_v + kBwdRows - 1) / kBwdRows, d_dot = 2 * d_key * nu;
     const int64_t rows = (int64_t)BH * L;
-    float *us = scratch, *phk = us + (size_t)rows * d_v, *phq = phk + (size_t)rows * d_dot;
+    const size_t pst = 2 * (size_t)d_dot + 4;
+    float *us = chunked ? nullptr : scratch;
+    float *phk = chunked ? scratch : us + (size_t)rows * d_v, *phq = phk + (size_t)rows * d_dot;
     float *part = phq + (size_t)rows * d_dot;
     const int bf16 = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
     cudaError_t e = launch_dpfp(k, phk, rows, d_key, nu, bf16, 0, eps, num_sms, st);
@@ -382,21 +385,28 @@ cudaError_t launch_backward_t(const void *q, const void *k, const void *v, const
         e = launch_dpfp(q, phq, rows, d_key, nu, bf16, 0, eps, num_sms, st);
     if (e != cudaSuccess)
         return e;
-    const size_t smem = backward_smem_bytes(d_key, nu, d_v);
-    const int ntok = 2 * d_dot + 3 * std::min(d_v, kBwdRows) + 1;
-    auto kern = ntok <= kBwdThreads       ? delta_backward_kernel<T, 1>
-                : ntok <= 2 * kBwdThreads ? delta_backward_kernel<T, 2>
-                : ntok <= 3 * kBwdThreads ? delta_backward_kernel<T, 3>
-                : ntok <= 5 * kBwdThreads ? delta_backward_kernel<T, 5>
-                                          : delta_backward_kernel<T, 9>; // d_dot <= 1024
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess)
-        return e;
-    e = launch_pdl(kern, dim3((unsigned)BH, (unsigned)blocks), dim3(kBwdThreads), smem, st, (const float *)phk,
-                   (const float *)phq, static_cast<const T *>(v), static_cast<const T *>(beta), W0,
-                   static_cast<const T *>(gy), gWL, static_cast<T *>(gv), gW0, us, part, L, d_dot, d_v);
-    if (e != cudaSuccess)
-        return e;
+    if (chunked) {
+        e = launch_backward_chunked(phk, phq, v, beta, W0, gy, gWL, gv, gW0, part, part + (size_t)rows * pst, BH, L,
+                                    d_dot, d_v, bf16, st);
+        if (e != cudaSuccess)
+            return e;
+    } else {
+        const size_t smem = backward_smem_bytes(d_key, nu, d_v);
+        const int ntok = 2 * d_dot + 3 * std::min(d_v, kBwdRows) + 1;
+        auto kern = ntok <= kBwdThreads       ? delta_backward_kernel<T, 1>
+                    : ntok <= 2 * kBwdThreads ? delta_backward_kernel<T, 2>
+                    : ntok <= 3 * kBwdThreads ? delta_backward_kernel<T, 3>
+                    : ntok <= 5 * kBwdThreads ? delta_backward_kernel<T, 5>
+                                              : delta_backward_kernel<T, 9>; // d_dot <= 1024
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        e = launch_pdl(kern, dim3((unsigned)BH, (unsigned)blocks), dim3(kBwdThreads), smem, st, (const float *)phk,
+                       (const float *)phq, static_cast<const T *>(v), static_cast<const T *>(beta), W0,
+                       static_cast<const T *>(gy), gWL, static_cast<T *>(gv), gW0, us, part, L, d_dot, d_v);
+        if (e != cudaSuccess)
+            return e;
+    }
     const size_t fsmem = sizeof(float) * kBwdWarps * (2 * (size_t)d_dot + 6 * (size_t)d_key);
     auto fin = backward_finish_kernel<T>;
     e = cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
@@ -421,8 +431,11 @@ size_t backward_smem_bytes(int d_key, int nu, int d_v) {
 // Global scratch: u_t for every token and row, phi(k_t) and phi(q_t) for
 // every token, then the row blocks' partial sums per token.
 size_t backward_workspace_bytes(int BH, int L, int d_key, int nu, int d_v) {
-    const size_t d_dot = (size_t)2 * d_key * nu, blocks = (d_v + kBwdRows - 1) / kBwdRows;
-    const size_t rows = (size_t)BH * L;
+    const size_t d_dot = (size_t)2 * d_key * nu, rows = (size_t)BH * L;
+    if (backward_chunked_supported(d_key, nu, d_v, L))
+        return sizeof(float) * (2 * rows * d_dot + rows * (2 * d_dot + 4) +
+                                backward_chunked_buffer_floats(BH, L, d_key, nu, d_v));
+    const size_t blocks = (d_v + kBwdRows - 1) / kBwdRows;
     return sizeof(float) * (rows * d_v + 2 * rows * d_dot + blocks * rows * (2 * d_dot + 4));
 }
 

@@ -40,15 +40,28 @@ cudaError_t tc_linear_launch(const void *q, const void *k, const void *v, const 
                              int d_key, int nu, int d_v, int chunk, int normalize, float eps, int num_sms,
                              unsigned *status, cudaStream_t st);
 
-// The backward of the delta rule (fp32 arithmetic, fp32 or bf16 I/O): one
-// CTA per (b,h) with W and its gradient in shared memory.  scratch holds u_t
-// for every token (BH * L * d_v floats).  Arguments validated by the caller.
+// The backward of the delta rule (fp32 arithmetic, fp32 or bf16 I/O).  Where
+// backward_chunked_supported() holds, the chunk-parallel form
+// (fw_backward_chunk.cu); otherwise one CTA per (b,h) and block of 16 rows of
+// W, token by token, with those rows of W and of its gradient in shared
+// memory.  Arguments validated by the caller.
 size_t backward_smem_bytes(int d_key, int nu, int d_v);
 size_t backward_workspace_bytes(int BH, int L, int d_key, int nu, int d_v);
 cudaError_t launch_backward(const void *q, const void *k, const void *v, const void *beta, const float *W0,
                             const void *gy, const float *gWL, void *gq, void *gk, void *gv, void *gbeta,
                             float *gW0, float *scratch, int BH, int L, int d_key, int nu, int d_v, int bf16,
                             float eps, int num_sms, cudaStream_t st);
+// The chunk-parallel backward (chunks of 64 tokens): d_dot <= 512, d_v <= 128.
+// It reads phi(k), phi(q) (fp32, made by launch_dpfp), writes gv and gW0,
+// and leaves per token [g_phi(q) | g_phi(k) | gbeta | pad] (2 d_dot + 4
+// floats) in part for the DPFP-backward kernel; buf holds
+// backward_chunked_buffer_floats() floats of intermediate chunk data.
+bool backward_chunked_supported(int d_key, int nu, int d_v, int L);
+size_t backward_chunked_buffer_floats(int BH, int L, int d_key, int nu, int d_v);
+cudaError_t launch_backward_chunked(const float *phk, const float *phq, const void *v, const void *beta,
+                                    const float *W0, const void *gy, const float *gWL, void *gv, float *gW0,
+                                    float *part, float *buf, int BH, int L, int d_dot, int d_v, int bf16,
+                                    cudaStream_t st);
 // K1, the standalone DPFP map: phi [rows, 2 d_key nu] of x [rows, d_key]
 // (bf16 or fp32 each way; arguments validated by the caller).
 cudaError_t launch_dpfp(const void *x, void *phi, int64_t rows, int d_key, int nu, int in_bf16, int out_bf16,

@@ -199,11 +199,16 @@ FW_API size_t fw_delta_backward_workspace_size(int B, int H, int L, int d_key, i
  *   dbeta    : [B, H, L]          io_dtype                  (written)
  *   dW0      : [B, H, d_v, d_dot] fp32 dL/dW0, or NULL to skip it
  *   workspace: device scratch of fw_delta_backward_workspace_size() bytes
- * fp32 arithmetic on CUDA cores for both I/O dtypes: the DPFP map of every
- * k and q first (fp32, into the workspace), then one CTA per (batch, head)
- * and block of 16 rows of the state, with those rows of the state and of
- * its gradient in shared memory (128 * d_dot bytes; d_dot <= 1024), then
- * one kernel that adds the blocks' shares and takes the DPFP backward.
+ * fp32 arithmetic on CUDA cores for both I/O dtypes, after the DPFP map of
+ * every k and q (fp32, into the workspace).  For d_dot <= 512 and d_v <= 128
+ * the chunk-parallel form: the transpose of the forward's chunk algebra
+ * (chunks of 64 tokens), as a per-chunk preparation kernel, a scan of the
+ * chunk-start states, a reverse scan of their gradients (both split over
+ * blocks of 16 rows of the state) and a per-chunk gradient kernel.  Other
+ * shapes (d_dot <= 1024) walk the tokens one at a time: one CTA per
+ * (batch, head) and block of 16 rows of the state, with those rows of the
+ * state and of its gradient in shared memory.  Either way a last kernel
+ * takes the DPFP backward of q and k.
  * The result does not depend on the run (fixed summation orders).
  * Errors as for fw_delta_forward.
  */
