@@ -18,12 +18,14 @@
 // of the chunk algebra above, equal to the token-by-token chain rule.
 //
 // Kernels (fp32 on CUDA cores, deterministic summation orders):
-//   chunk_prep   one CTA per (b,h, chunk): K K^T, P, and M by forward
-//                substitution, column by column;
+//   chunk_prep   one CTA per (b,h, chunk): K K^T, P, M by forward
+//                substitution column by column, T = M diag(beta), and
+//                G = dY^T Q (the part of dS that does not depend on the scan);
 //   state_scan   one CTA per (b,h, 16 value rows): the chunk-start states S
 //                in chunk order (kept for the gradient kernel), X and U;
 //   grad_scan    the same split, chunks in reverse: dS' kept per chunk, dU,
-//                dX (= dV, written out), and dW0 at the end;
+//                dX (= dV, written out), dS = dS' + G - dX^T K, and dW0 at
+//                the end;
 //   chunk_grad   one CTA per (b,h, chunk): dT, dP, dA, dbeta and the phi-space
 //                gradients of q and k, written where the DPFP-backward kernel
 //                of fw_backward.cu reads them.
@@ -43,32 +45,71 @@ namespace fw {
 
 namespace {
 
-constexpr int kCC = 64;       // chunk length
-constexpr int kCT = 256;      // threads per CTA
-constexpr int kCR = 16;       // value rows per scan CTA
-constexpr int kSl = 32;       // width of a staged slice of a contraction dimension
-constexpr int kLd = kCC + 1;  // row stride of a C x C tile in shared memory
-constexpr int kSd = kSl + 1;  // row stride of a staged slice
-constexpr int kRd = kCR + 1;  // row stride of a C x 16 tile
+constexpr int kCC = 64;        // chunk length
+constexpr int kCT = 256;       // threads per CTA
+constexpr int kCR = 16;        // value rows per scan CTA
+constexpr int kSl = 32;        // width of a staged slice of a contraction dimension
+constexpr int kLd = kCC + 1;   // row stride of a C x C tile read along rows and columns
+constexpr int kLdP = kCC + 4;  // row stride of the dP tile (16-byte rows)
+constexpr int kSd = kSl + 1;   // row stride of a staged slice
+constexpr int kRd = kCR + 4;   // row stride of a C x 16 tile (16-byte rows)
 
 FW_DEV float ldf(const float *p) { return __ldcg(p); }
 
+FW_DEV float4 lds4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+
+// Stage a rows x cols block of fp32 (cols a multiple of 4, every source row
+// 16-byte aligned, source row stride lds floats) into shared memory (row
+// stride ldd floats); rows at or past `valid` read as zero.  16-byte loads,
+// four per thread in flight before the first store.
+FW_DEV void stage4(float *dst, int ldd, const float *src, size_t lds, int rows, int valid, int cols, int tid,
+                   int nt) {
+    const int c4 = cols >> 2, n = rows * c4;
+    for (int e0 = tid; e0 < n; e0 += 4 * nt) {
+        float4 t[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * nt, i = e / c4;
+            t[u] = (e < n && i < valid) ? __ldcg(reinterpret_cast<const float4 *>(src + (size_t)i * lds) + e % c4)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * nt;
+            if (e < n) {
+                float *d = dst + (size_t)(e / c4) * ldd + (e % c4) * 4;
+                d[0] = t[u].x;
+                d[1] = t[u].y;
+                d[2] = t[u].z;
+                d[3] = t[u].w;
+            }
+        }
+    }
+}
+
+FW_DEV float dot4(float4 a, float4 b, float acc) {
+    return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, acc))));
+}
+
 // ----------------------------------------------------------- chunk_prep
 // Shared memory: ks, qs [C][kSd] (a slice of the chunk's K and Q rows),
-// kk, pq, ms [C][kLd], bs [C].
+// kk, pq, ms [C][kLd], dyv [C][dvp + 1] (dY, dvp = d_v rounded up to 8), bs [C].
 template <typename T>
 __global__ void __launch_bounds__(kCT)
     chunk_prep_kernel(const float *__restrict__ phk, const float *__restrict__ phq, const T *__restrict__ beta,
-                      float *__restrict__ Mb, float *__restrict__ Pb, float *__restrict__ KKb, int L, int d_dot,
-                      int nC) {
+                      const T *__restrict__ gy, float *__restrict__ Mb, float *__restrict__ Tb,
+                      float *__restrict__ Pb, float *__restrict__ KKb, float *__restrict__ Gb, int L, int d_dot,
+                      int d_v, int nC) {
     extern __shared__ float sm[];
+    const int dvp = (d_v + 7) & ~7, yd = dvp + 1;
     float *ks = sm, *qs = ks + kCC * kSd, *kk = qs + kCC * kSd, *pq = kk + kCC * kLd, *ms = pq + kCC * kLd;
-    float *bs = ms + kCC * kLd;
+    float *dyv = ms + kCC * kLd, *bs = dyv + kCC * yd;
     const int tid = threadIdx.x, nt = blockDim.x;
     const int bh = blockIdx.x, c = blockIdx.y;
     const int t0 = c * kCC, cl = min(kCC, L - t0);
     const size_t tok0 = (size_t)bh * L + t0;
     const size_t cc0 = ((size_t)bh * nC + c) * kCC * kCC;
+    const size_t gs0 = ((size_t)bh * nC + c) * d_v;
 
     for (int i = tid; i < kCC; i += nt)
         bs[i] = i < cl ? io<T>::load(beta + tok0 + i) : 0.f;
@@ -76,16 +117,17 @@ __global__ void __launch_bounds__(kCT)
         kk[(e / kCC) * kLd + e % kCC] = 0.f;
         pq[(e / kCC) * kLd + e % kCC] = 0.f;
     }
+    for (int e = tid; e < kCC * dvp; e += nt) {
+        const int i = e / dvp, r = e % dvp;
+        dyv[i * yd + r] = (i < cl && r < d_v) ? io<T>::load(gy + (tok0 + i) * d_v + r) : 0.f;
+    }
     __syncthreads();
     for (int s0 = 0; s0 < d_dot; s0 += kSl) {
-        for (int e = tid; e < kCC * kSl; e += nt) {
-            const int i = e / kSl, j = e % kSl;
-            const bool in = i < cl && s0 + j < d_dot;
-            ks[i * kSd + j] = in ? ldf(phk + (tok0 + i) * d_dot + s0 + j) : 0.f;
-            qs[i * kSd + j] = in ? ldf(phq + (tok0 + i) * d_dot + s0 + j) : 0.f;
-        }
+        const int sw = min(kSl, d_dot - s0);
+        stage4(ks, kSd, phk + tok0 * d_dot + s0, d_dot, kCC, cl, sw, tid, nt);
+        stage4(qs, kSd, phq + tok0 * d_dot + s0, d_dot, kCC, cl, sw, tid, nt);
         __syncthreads();
-        // 256 tiles of 4 x 4 outputs: rows ty + 16a, columns tx + 16b
+        // K K^T and Q K^T: 256 tiles of 4 x 4 outputs, rows ty + 16a, columns tx + 16b
         for (int w = tid; w < 256; w += nt) {
             const int tx = w & 15, ty = w >> 4;
             float ak[4][4], aq[4][4];
@@ -96,7 +138,7 @@ __global__ void __launch_bounds__(kCT)
                     ak[a][b] = kk[(ty + 16 * a) * kLd + tx + 16 * b];
                     aq[a][b] = pq[(ty + 16 * a) * kLd + tx + 16 * b];
                 }
-            for (int j = 0; j < kSl; ++j) {
+            for (int j = 0; j < sw; ++j) {
                 float ki[4], qi[4], kj[4];
 #pragma unroll
                 for (int a = 0; a < 4; ++a) {
@@ -119,6 +161,26 @@ __global__ void __launch_bounds__(kCT)
                     kk[(ty + 16 * a) * kLd + tx + 16 * b] = ak[a][b];
                     pq[(ty + 16 * a) * kLd + tx + 16 * b] = aq[a][b];
                 }
+        }
+        // G = dY^T Q for this slice: slice column j = w & 31, rows rb .. rb + 7
+        for (int w = tid; w < (dvp / 8) * 32; w += nt) {
+            const int j = w & 31, rb = (w >> 5) * 8;
+            if (j < sw) {
+                float acc[8];
+#pragma unroll
+                for (int a = 0; a < 8; ++a)
+                    acc[a] = 0.f;
+                for (int i = 0; i < cl; ++i) {
+                    const float qv = qs[i * kSd + j];
+#pragma unroll
+                    for (int a = 0; a < 8; ++a)
+                        acc[a] = fmaf(dyv[i * yd + rb + a], qv, acc[a]);
+                }
+#pragma unroll
+                for (int a = 0; a < 8; ++a)
+                    if (rb + a < d_v)
+                        Gb[(gs0 + rb + a) * d_dot + s0 + j] = acc[a];
+            }
         }
         __syncthreads();
     }
@@ -144,29 +206,32 @@ __global__ void __launch_bounds__(kCT)
         }
     }
     __syncthreads();
-    for (int e = tid; e < kCC * kCC; e += nt)
-        Mb[cc0 + e] = ms[(e / kCC) * kLd + e % kCC];
+    for (int e = tid; e < kCC * kCC; e += nt) {
+        const float mv = ms[(e / kCC) * kLd + e % kCC];
+        Mb[cc0 + e] = mv;
+        Tb[cc0 + e] = mv * bs[e % kCC];
+    }
 }
 
 // ----------------------------------------------------------- state_scan
-// Shared memory: ss [kCR][d_dot + 1] (the CTA's rows of S), kc [C][d_dot + 1],
-// mc [C][kLd], xs, us [C][kRd], bs [C].
+// Shared memory: ss [kCR][d_dot + 4] (the CTA's rows of S), kc [C][d_dot + 4],
+// tc [C][kLd] (T), xs, us [C][kRd].
 template <typename T>
 __global__ void __launch_bounds__(kCT)
-    state_scan_kernel(const float *__restrict__ phk, const T *__restrict__ v, const T *__restrict__ beta,
-                      const float *__restrict__ W0, const float *__restrict__ Mb, float *__restrict__ Sb,
-                      float *__restrict__ Xb, float *__restrict__ Ub, int L, int d_dot, int d_v, int nC) {
+    state_scan_kernel(const float *__restrict__ phk, const T *__restrict__ v, const float *__restrict__ W0,
+                      const float *__restrict__ Tb, float *__restrict__ Sb, float *__restrict__ Xb,
+                      float *__restrict__ Ub, int L, int d_dot, int d_v, int nC) {
     extern __shared__ float sm[];
-    const int sd = d_dot + 1;
-    float *ss = sm, *kc = ss + kCR * sd, *mc = kc + kCC * sd, *xs = mc + kCC * kLd, *us = xs + kCC * kRd;
-    float *bs = us + kCC * kRd;
+    const int sd = d_dot + 4, d4 = d_dot >> 2;
+    float *ss = sm, *kc = ss + kCR * sd, *tc = kc + kCC * sd, *xs = tc + kCC * kLd, *us = xs + kCC * kRd;
     const int tid = threadIdx.x, nt = blockDim.x;
     const int bh = blockIdx.x, r0 = blockIdx.y * kCR, R = min(kCR, d_v - r0);
 
-    for (int e = tid; e < kCR * d_dot; e += nt) {
-        const int r = e / d_dot, m = e % d_dot;
-        ss[r * sd + m] = (r < R && W0) ? ldf(W0 + ((size_t)bh * d_v + r0 + r) * d_dot + m) : 0.f;
-    }
+    if (W0)
+        stage4(ss, sd, W0 + ((size_t)bh * d_v + r0) * d_dot, d_dot, kCR, R, d_dot, tid, nt);
+    else
+        for (int e = tid; e < kCR * d_dot; e += nt)
+            ss[(e / d_dot) * sd + e % d_dot] = 0.f;
     __syncthreads();
     for (int c = 0; c < nC; ++c) {
         const int t0 = c * kCC, cl = min(kCC, L - t0);
@@ -176,18 +241,12 @@ __global__ void __launch_bounds__(kCT)
             const int r = e / d_dot, m = e % d_dot;
             Sb[(st0 + r0 + r) * d_dot + m] = ss[r * sd + m];
         }
-        for (int e = tid; e < kCC * d_dot; e += nt) {
-            const int i = e / d_dot, m = e % d_dot;
-            kc[i * sd + m] = i < cl ? ldf(phk + (tok0 + i) * d_dot + m) : 0.f;
-        }
-        for (int e = tid; e < kCC * kCC; e += nt)
-            mc[(e / kCC) * kLd + e % kCC] = ldf(Mb + ((size_t)bh * nC + c) * kCC * kCC + e);
+        stage4(kc, sd, phk + tok0 * d_dot, d_dot, kCC, cl, d_dot, tid, nt);
+        stage4(tc, kLd, Tb + ((size_t)bh * nC + c) * kCC * kCC, kCC, kCC, kCC, kCC, tid, nt);
         for (int e = tid; e < kCC * kCR; e += nt) {
             const int i = e / kCR, r = e % kCR;
             xs[i * kRd + r] = (i < cl && r < R) ? io<T>::load(v + (tok0 + i) * d_v + r0 + r) : 0.f;
         }
-        for (int i = tid; i < kCC; i += nt)
-            bs[i] = i < cl ? io<T>::load(beta + tok0 + i) : 0.f;
         __syncthreads();
         // X = V - K S^T: 256 tiles, row r = w & 15, tokens (w >> 4) + 16a
         for (int w = tid; w < 256; w += nt) {
@@ -195,23 +254,24 @@ __global__ void __launch_bounds__(kCT)
             float acc[4];
 #pragma unroll
             for (int a = 0; a < 4; ++a)
-                acc[a] = xs[(i0 + 16 * a) * kRd + r];
-            for (int m = 0; m < d_dot; ++m) {
-                const float s = ss[r * sd + m];
+                acc[a] = 0.f;
+            for (int m4 = 0; m4 < d4; ++m4) {
+                const float4 s = lds4(ss + r * sd + 4 * m4);
 #pragma unroll
                 for (int a = 0; a < 4; ++a)
-                    acc[a] = fmaf(-kc[(i0 + 16 * a) * sd + m], s, acc[a]);
+                    acc[a] = dot4(lds4(kc + (i0 + 16 * a) * sd + 4 * m4), s, acc[a]);
             }
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
                 const int i = i0 + 16 * a;
-                xs[i * kRd + r] = acc[a];
+                const float x = xs[i * kRd + r] - acc[a];
+                xs[i * kRd + r] = x;
                 if (i < cl && r < R)
-                    Xb[(tok0 + i) * d_v + r0 + r] = acc[a];
+                    Xb[(tok0 + i) * d_v + r0 + r] = x;
             }
         }
         __syncthreads();
-        // U = M diag(beta) X (M unit lower)
+        // U = T X (T lower)
         for (int w = tid; w < 256; w += nt) {
             const int r = w & 15, i0 = w >> 4;
 #pragma unroll
@@ -219,7 +279,7 @@ __global__ void __launch_bounds__(kCT)
                 const int i = i0 + 16 * a;
                 float acc = 0.f;
                 for (int s = 0; s <= i; ++s)
-                    acc = fmaf(mc[i * kLd + s] * bs[s], xs[s * kRd + r], acc);
+                    acc = fmaf(tc[i * kLd + s], xs[s * kRd + r], acc);
                 us[i * kRd + r] = acc;
                 if (i < cl && r < R)
                     Ub[(tok0 + i) * d_v + r0 + r] = acc;
@@ -235,9 +295,15 @@ __global__ void __launch_bounds__(kCT)
                 acc[r] = ss[(rh + r) * sd + m];
             for (int i = 0; i < cl; ++i) {
                 const float kv = kc[i * sd + m];
-#pragma unroll
-                for (int r = 0; r < kCR / 2; ++r)
-                    acc[r] = fmaf(us[i * kRd + rh + r], kv, acc[r]);
+                const float4 u0 = lds4(us + i * kRd + rh), u1 = lds4(us + i * kRd + rh + 4);
+                acc[0] = fmaf(u0.x, kv, acc[0]);
+                acc[1] = fmaf(u0.y, kv, acc[1]);
+                acc[2] = fmaf(u0.z, kv, acc[2]);
+                acc[3] = fmaf(u0.w, kv, acc[3]);
+                acc[4] = fmaf(u1.x, kv, acc[4]);
+                acc[5] = fmaf(u1.y, kv, acc[5]);
+                acc[6] = fmaf(u1.z, kv, acc[6]);
+                acc[7] = fmaf(u1.w, kv, acc[7]);
             }
 #pragma unroll
             for (int r = 0; r < kCR / 2; ++r)
@@ -248,26 +314,26 @@ __global__ void __launch_bounds__(kCT)
 }
 
 // ------------------------------------------------------------ grad_scan
-// Shared memory: ds [kCR][d_dot + 1] (the CTA's rows of dS), kc [C][d_dot + 1],
-// mc, pc [C][kLd], dys, dus, dxs [C][kRd], bs [C].
+// Shared memory: ds [kCR][d_dot + 4] (the CTA's rows of dS), kc [C][d_dot + 4],
+// tc, pc [C][kLd] (T and P), dys, dus, dxs [C][kRd].
 template <typename T>
 __global__ void __launch_bounds__(kCT)
-    grad_scan_kernel(const float *__restrict__ phk, const float *__restrict__ phq, const T *__restrict__ beta,
-                     const T *__restrict__ gy, const float *__restrict__ gWL, const float *__restrict__ Mb,
-                     const float *__restrict__ Pb, float *__restrict__ dSb, float *__restrict__ dXb,
-                     float *__restrict__ dUb, T *__restrict__ gv, float *__restrict__ gW0, int L, int d_dot, int d_v,
-                     int nC) {
+    grad_scan_kernel(const float *__restrict__ phk, const T *__restrict__ gy, const float *__restrict__ gWL,
+                     const float *__restrict__ Tb, const float *__restrict__ Pb, const float *__restrict__ Gb,
+                     float *__restrict__ dSb, float *__restrict__ dXb, float *__restrict__ dUb, T *__restrict__ gv,
+                     float *__restrict__ gW0, int L, int d_dot, int d_v, int nC) {
     extern __shared__ float sm[];
-    const int sd = d_dot + 1;
-    float *ds = sm, *kc = ds + kCR * sd, *mc = kc + kCC * sd, *pc = mc + kCC * kLd, *dys = pc + kCC * kLd;
-    float *dus = dys + kCC * kRd, *dxs = dus + kCC * kRd, *bs = dxs + kCC * kRd;
+    const int sd = d_dot + 4, d4 = d_dot >> 2;
+    float *ds = sm, *kc = ds + kCR * sd, *tc = kc + kCC * sd, *pc = tc + kCC * kLd, *dys = pc + kCC * kLd;
+    float *dus = dys + kCC * kRd, *dxs = dus + kCC * kRd;
     const int tid = threadIdx.x, nt = blockDim.x;
     const int bh = blockIdx.x, r0 = blockIdx.y * kCR, R = min(kCR, d_v - r0);
 
-    for (int e = tid; e < kCR * d_dot; e += nt) {
-        const int r = e / d_dot, m = e % d_dot;
-        ds[r * sd + m] = (r < R && gWL) ? ldf(gWL + ((size_t)bh * d_v + r0 + r) * d_dot + m) : 0.f;
-    }
+    if (gWL)
+        stage4(ds, sd, gWL + ((size_t)bh * d_v + r0) * d_dot, d_dot, kCR, R, d_dot, tid, nt);
+    else
+        for (int e = tid; e < kCR * d_dot; e += nt)
+            ds[(e / d_dot) * sd + e % d_dot] = 0.f;
     __syncthreads();
     for (int c = nC - 1; c >= 0; --c) {
         const int t0 = c * kCC, cl = min(kCC, L - t0);
@@ -278,33 +344,26 @@ __global__ void __launch_bounds__(kCT)
             const int r = e / d_dot, m = e % d_dot;
             dSb[(st0 + r0 + r) * d_dot + m] = ds[r * sd + m];
         }
-        for (int e = tid; e < kCC * d_dot; e += nt) {
-            const int i = e / d_dot, m = e % d_dot;
-            kc[i * sd + m] = i < cl ? ldf(phk + (tok0 + i) * d_dot + m) : 0.f;
-        }
-        for (int e = tid; e < kCC * kCC; e += nt) {
-            mc[(e / kCC) * kLd + e % kCC] = ldf(Mb + cc0 + e);
-            pc[(e / kCC) * kLd + e % kCC] = ldf(Pb + cc0 + e);
-        }
+        stage4(kc, sd, phk + tok0 * d_dot, d_dot, kCC, cl, d_dot, tid, nt);
+        stage4(tc, kLd, Tb + cc0, kCC, kCC, kCC, kCC, tid, nt);
+        stage4(pc, kLd, Pb + cc0, kCC, kCC, kCC, kCC, tid, nt);
         for (int e = tid; e < kCC * kCR; e += nt) {
             const int i = e / kCR, r = e % kCR;
             dys[i * kRd + r] = (i < cl && r < R) ? io<T>::load(gy + (tok0 + i) * d_v + r0 + r) : 0.f;
         }
-        for (int i = tid; i < kCC; i += nt)
-            bs[i] = i < cl ? io<T>::load(beta + tok0 + i) : 0.f;
         __syncthreads();
-        // dU = P^T dY + K dS'^T (P lower, so P_si is zero for s < i)
+        // dU = K dS'^T + P^T dY (P lower, so P_si is zero for s < i)
         for (int w = tid; w < 256; w += nt) {
             const int r = w & 15, i0 = w >> 4;
             float acc[4];
 #pragma unroll
             for (int a = 0; a < 4; ++a)
                 acc[a] = 0.f;
-            for (int m = 0; m < d_dot; ++m) {
-                const float s = ds[r * sd + m];
+            for (int m4 = 0; m4 < d4; ++m4) {
+                const float4 s = lds4(ds + r * sd + 4 * m4);
 #pragma unroll
                 for (int a = 0; a < 4; ++a)
-                    acc[a] = fmaf(kc[(i0 + 16 * a) * sd + m], s, acc[a]);
+                    acc[a] = dot4(lds4(kc + (i0 + 16 * a) * sd + 4 * m4), s, acc[a]);
             }
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
@@ -317,7 +376,7 @@ __global__ void __launch_bounds__(kCT)
             }
         }
         __syncthreads();
-        // dX = diag(beta) M^T dU = dV
+        // dX = T^T dU = dV
         for (int w = tid; w < 256; w += nt) {
             const int r = w & 15, i0 = w >> 4;
 #pragma unroll
@@ -325,8 +384,7 @@ __global__ void __launch_bounds__(kCT)
                 const int i = i0 + 16 * a;
                 float acc = 0.f;
                 for (int s = i; s < kCC; ++s)
-                    acc = fmaf(mc[s * kLd + i], dus[s * kRd + r], acc);
-                acc *= bs[i];
+                    acc = fmaf(tc[s * kLd + i], dus[s * kRd + r], acc);
                 dxs[i * kRd + r] = acc;
                 if (i < cl && r < R) {
                     dXb[(tok0 + i) * d_v + r0 + r] = acc;
@@ -335,18 +393,24 @@ __global__ void __launch_bounds__(kCT)
             }
         }
         __syncthreads();
-        // dS = dS' + dY^T Q - dX^T K: thread per (column m, half of the rows)
+        // dS = dS' + G - dX^T K: thread per (column m, half of the rows)
         for (int e = tid; e < 2 * d_dot; e += nt) {
             const int m = e % d_dot, rh = (e / d_dot) * (kCR / 2);
             float acc[kCR / 2];
 #pragma unroll
             for (int r = 0; r < kCR / 2; ++r)
-                acc[r] = ds[(rh + r) * sd + m];
+                acc[r] = ds[(rh + r) * sd + m] + (rh + r < R ? ldf(Gb + (st0 + r0 + rh + r) * d_dot + m) : 0.f);
             for (int i = 0; i < cl; ++i) {
-                const float qv = ldf(phq + (tok0 + i) * d_dot + m), kv = kc[i * sd + m];
-#pragma unroll
-                for (int r = 0; r < kCR / 2; ++r)
-                    acc[r] = fmaf(dys[i * kRd + rh + r], qv, fmaf(-dxs[i * kRd + rh + r], kv, acc[r]));
+                const float kv = kc[i * sd + m];
+                const float4 x0 = lds4(dxs + i * kRd + rh), x1 = lds4(dxs + i * kRd + rh + 4);
+                acc[0] = fmaf(-x0.x, kv, acc[0]);
+                acc[1] = fmaf(-x0.y, kv, acc[1]);
+                acc[2] = fmaf(-x0.z, kv, acc[2]);
+                acc[3] = fmaf(-x0.w, kv, acc[3]);
+                acc[4] = fmaf(-x1.x, kv, acc[4]);
+                acc[5] = fmaf(-x1.y, kv, acc[5]);
+                acc[6] = fmaf(-x1.z, kv, acc[6]);
+                acc[7] = fmaf(-x1.w, kv, acc[7]);
             }
 #pragma unroll
             for (int r = 0; r < kCR / 2; ++r)
@@ -362,23 +426,28 @@ __global__ void __launch_bounds__(kCT)
 }
 
 // ------------------------------------------------------------ chunk_grad
-// Shared memory: c1 (dT, then dA), c2 (dP), c3 (M), c4 (M^T dT diag(beta),
-// then B + B^T), each [C][kLd]; dys, uvs, dxs [C][d_v + 1]; a staging region
-// of 2 d_v kSd + 2 C kSd floats (slices of dU and X, later of S, dS', K, Q);
-// bs, gb [C].
-template <typename T>
+// Shared memory: c1 (dT, then dA), c3 (M), c4 (M^T dT diag(beta), then
+// B + B^T), each [C][kLd]; c2 (dP) [C][kLdP]; dys, uvs, dxs [C][d_v + 1]; a
+// staging region (slices of dU and X, later of S, dS' [d_v][SW + 4] and K, Q
+// [C][SW + 4]); bs, gb [C].  SW: the width of a feature slice (64 or 32).
+template <int SW> __host__ __device__ constexpr int grad_stage_floats(int d_v) {
+    return 2 * kCC * kSd > (2 * d_v + 2 * kCC) * (SW + 4) ? 2 * kCC * kSd : (2 * d_v + 2 * kCC) * (SW + 4);
+}
+
+template <typename T, int SW>
 __global__ void __launch_bounds__(kCT)
     chunk_grad_kernel(const float *__restrict__ phk, const float *__restrict__ phq, const T *__restrict__ beta,
                       const T *__restrict__ gy, const float *__restrict__ Sb, const float *__restrict__ dSb,
                       const float *__restrict__ Xb, const float *__restrict__ Ub, const float *__restrict__ dXb,
                       const float *__restrict__ dUb, const float *__restrict__ Mb, const float *__restrict__ KKb,
                       float *__restrict__ part, int L, int d_dot, int d_v, int nC) {
+    constexpr int NCG = SW / 4, NTG = kCT / NCG, TPT = kCC / NTG, ld6 = SW + 4;
     extern __shared__ float sm[];
     const int vd = d_v + 1;
     const size_t pst = 2 * (size_t)d_dot + 4;
-    float *c1 = sm, *c2 = c1 + kCC * kLd, *c3 = c2 + kCC * kLd, *c4 = c3 + kCC * kLd;
-    float *dys = c4 + kCC * kLd, *uvs = dys + kCC * vd, *dxs = uvs + kCC * vd, *stg = dxs + kCC * vd;
-    float *bs = stg + 2 * d_v * kSd + 2 * kCC * kSd, *gb = bs + kCC;
+    float *c1 = sm, *c3 = c1 + kCC * kLd, *c4 = c3 + kCC * kLd, *c2 = c4 + kCC * kLd;
+    float *dys = c2 + kCC * kLdP, *uvs = dys + kCC * vd, *dxs = uvs + kCC * vd, *stg = dxs + kCC * vd;
+    float *bs = stg + grad_stage_floats<SW>(d_v), *gb = bs + kCC;
     const int tid = threadIdx.x, nt = blockDim.x;
     const int bh = blockIdx.x, c = blockIdx.y;
     const int t0 = c * kCC, cl = min(kCC, L - t0);
@@ -398,21 +467,20 @@ __global__ void __launch_bounds__(kCT)
     for (int e = tid; e < kCC * kCC; e += nt) {
         const int i = e / kCC, j = e % kCC;
         c1[i * kLd + j] = 0.f;
-        c2[i * kLd + j] = 0.f;
-        c3[i * kLd + j] = ldf(Mb + cc0 + e);
+        c2[i * kLdP + j] = 0.f;
     }
     __syncthreads();
     // dT = dU X^T and dY U^T, over slices of the value dimension
     float *dul = stg, *xl = stg + kCC * kSd;
     for (int r0 = 0; r0 < d_v; r0 += kSl) {
+        const int rn = min(kSl, d_v - r0);
         for (int e = tid; e < kCC * kSl; e += nt) {
             const int i = e / kSl, j = e % kSl;
-            const bool in = i < cl && r0 + j < d_v;
+            const bool in = i < cl && j < rn;
             dul[i * kSd + j] = in ? ldf(dUb + (tok0 + i) * d_v + r0 + j) : 0.f;
             xl[i * kSd + j] = in ? ldf(Xb + (tok0 + i) * d_v + r0 + j) : 0.f;
         }
         __syncthreads();
-        const int rn = min(kSl, d_v - r0);
         for (int w = tid; w < 256; w += nt) {
             const int tx = w & 15, ty = w >> 4;
             float at[4][4], ap[4][4];
@@ -421,7 +489,7 @@ __global__ void __launch_bounds__(kCT)
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
                     at[a][b] = c1[(ty + 16 * a) * kLd + tx + 16 * b];
-                    ap[a][b] = c2[(ty + 16 * a) * kLd + tx + 16 * b];
+                    ap[a][b] = c2[(ty + 16 * a) * kLdP + tx + 16 * b];
                 }
             for (int j = 0; j < rn; ++j) {
                 float du[4], xj[4], dy[4], uj[4];
@@ -445,25 +513,26 @@ __global__ void __launch_bounds__(kCT)
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
                     c1[(ty + 16 * a) * kLd + tx + 16 * b] = at[a][b];
-                    c2[(ty + 16 * a) * kLd + tx + 16 * b] = ap[a][b];
+                    c2[(ty + 16 * a) * kLdP + tx + 16 * b] = ap[a][b];
                 }
         }
         __syncthreads();
     }
-    // dP = tril_inclusive(dY U^T); dbeta's first part, column sums of M * dT
+    // M in; dP = tril_inclusive(dY U^T)
+    stage4(c3, kLd, Mb + cc0, kCC, kCC, kCC, kCC, tid, nt);
     for (int e = tid; e < kCC * kCC; e += nt) {
         const int i = e / kCC, j = e % kCC;
         if (j > i)
-            c2[i * kLd + j] = 0.f;
+            c2[i * kLdP + j] = 0.f;
     }
+    __syncthreads();
+    // dbeta's first part, column sums of M * dT; c4 = M^T (dT diag(beta))
     for (int i = tid; i < kCC; i += nt) {
         float acc = 0.f;
         for (int j = i; j < kCC; ++j)
             acc = fmaf(c3[j * kLd + i], c1[j * kLd + i], acc);
         gb[i] = acc;
     }
-    __syncthreads();
-    // c4 = M^T (dT diag(beta))
     for (int e = tid; e < kCC * kCC; e += nt) {
         const int i = e / kCC, j = e % kCC;
         float acc = 0.f;
@@ -497,77 +566,89 @@ __global__ void __launch_bounds__(kCT)
     for (int i = tid; i < cl; i += nt)
         part[(tok0 + i) * pst + 2 * (size_t)d_dot] = gb[i];
     // dQ = dY S + dP K and dK = U dS' - dX S + dP^T Q + (B + B^T) K, over
-    // slices of the feature dimension
-    float *sl = stg, *dsl = sl + d_v * kSd, *kl = dsl + d_v * kSd, *ql = kl + kCC * kSd;
-    for (int m0 = 0; m0 < d_dot; m0 += kSl) {
-        for (int e = tid; e < d_v * kSl; e += nt) {
-            const int r = e / kSl, j = e % kSl;
-            const bool in = m0 + j < d_dot;
-            sl[r * kSd + j] = in ? ldf(Sb + (st0 + r) * d_dot + m0 + j) : 0.f;
-            dsl[r * kSd + j] = in ? ldf(dSb + (st0 + r) * d_dot + m0 + j) : 0.f;
-        }
-        for (int e = tid; e < kCC * kSl; e += nt) {
-            const int i = e / kSl, j = e % kSl;
-            const bool in = i < cl && m0 + j < d_dot;
-            kl[i * kSd + j] = in ? ldf(phk + (tok0 + i) * d_dot + m0 + j) : 0.f;
-            ql[i * kSd + j] = in ? ldf(phq + (tok0 + i) * d_dot + m0 + j) : 0.f;
-        }
+    // slices of the feature dimension; a thread owns TPT tokens x 4 columns
+    float *sl = stg, *dsl = sl + d_v * ld6, *kl = dsl + d_v * ld6, *ql = kl + kCC * ld6;
+    for (int m0 = 0; m0 < d_dot; m0 += SW) {
+        const int sw = min(SW, d_dot - m0);
+        stage4(sl, ld6, Sb + st0 * d_dot + m0, d_dot, d_v, d_v, sw, tid, nt);
+        stage4(dsl, ld6, dSb + st0 * d_dot + m0, d_dot, d_v, d_v, sw, tid, nt);
+        stage4(kl, ld6, phk + tok0 * d_dot + m0, d_dot, kCC, cl, sw, tid, nt);
+        stage4(ql, ld6, phq + tok0 * d_dot + m0, d_dot, kCC, cl, sw, tid, nt);
         __syncthreads();
-        // 256 tiles: slice column j = w & 31, tokens (w >> 5) + 8a
-        for (int w = tid; w < 256; w += nt) {
-            const int j = w & 31, i0 = w >> 5;
-            float aq[8], ak[8];
+        for (int w = tid; w < kCT; w += nt) {
+            const int cg = w % NCG, i0 = (w / NCG) * TPT, j4 = 4 * cg;
+            if (j4 < sw) {
+                float aq[TPT][4], ak[TPT][4];
 #pragma unroll
-            for (int a = 0; a < 8; ++a)
-                aq[a] = ak[a] = 0.f;
-            for (int r = 0; r < d_v; ++r) {
-                const float s = sl[r * kSd + j], dsv = dsl[r * kSd + j];
+                for (int a = 0; a < TPT; ++a)
 #pragma unroll
-                for (int a = 0; a < 8; ++a) {
-                    const int i = i0 + 8 * a;
-                    aq[a] = fmaf(dys[i * vd + r], s, aq[a]);
-                    ak[a] = fmaf(uvs[i * vd + r], dsv, fmaf(-dxs[i * vd + r], s, ak[a]));
-                }
-            }
-            for (int s = 0; s < kCC; ++s) {
-                const float kv = kl[s * kSd + j], qv = ql[s * kSd + j];
+                    for (int b = 0; b < 4; ++b)
+                        aq[a][b] = ak[a][b] = 0.f;
+                for (int r = 0; r < d_v; ++r) {
+                    const float4 s = lds4(sl + r * ld6 + j4), d = lds4(dsl + r * ld6 + j4);
 #pragma unroll
-                for (int a = 0; a < 8; ++a) {
-                    const int i = i0 + 8 * a;
-                    aq[a] = fmaf(c2[i * kLd + s], kv, aq[a]);
-                    ak[a] = fmaf(c2[s * kLd + i], qv, fmaf(c4[i * kLd + s], kv, ak[a]));
-                }
-            }
-            if (m0 + j < d_dot)
-#pragma unroll
-                for (int a = 0; a < 8; ++a) {
-                    const int i = i0 + 8 * a;
-                    if (i < cl) {
-                        part[(tok0 + i) * pst + m0 + j] = aq[a];
-                        part[(tok0 + i) * pst + d_dot + m0 + j] = ak[a];
+                    for (int a = 0; a < TPT; ++a) {
+                        const float y = dys[(i0 + a) * vd + r], u = uvs[(i0 + a) * vd + r];
+                        const float x = -dxs[(i0 + a) * vd + r];
+                        aq[a][0] = fmaf(y, s.x, aq[a][0]);
+                        aq[a][1] = fmaf(y, s.y, aq[a][1]);
+                        aq[a][2] = fmaf(y, s.z, aq[a][2]);
+                        aq[a][3] = fmaf(y, s.w, aq[a][3]);
+                        ak[a][0] = fmaf(u, d.x, fmaf(x, s.x, ak[a][0]));
+                        ak[a][1] = fmaf(u, d.y, fmaf(x, s.y, ak[a][1]));
+                        ak[a][2] = fmaf(u, d.z, fmaf(x, s.z, ak[a][2]));
+                        ak[a][3] = fmaf(u, d.w, fmaf(x, s.w, ak[a][3]));
                     }
                 }
+                for (int s = 0; s < cl; ++s) {
+                    const float4 kv = lds4(kl + s * ld6 + j4), qv = lds4(ql + s * ld6 + j4);
+#pragma unroll
+                    for (int a = 0; a < TPT; ++a) {
+                        const float p = c2[(i0 + a) * kLdP + s], pt = c2[s * kLdP + i0 + a];
+                        const float b = c4[(i0 + a) * kLd + s];
+                        aq[a][0] = fmaf(p, kv.x, aq[a][0]);
+                        aq[a][1] = fmaf(p, kv.y, aq[a][1]);
+                        aq[a][2] = fmaf(p, kv.z, aq[a][2]);
+                        aq[a][3] = fmaf(p, kv.w, aq[a][3]);
+                        ak[a][0] = fmaf(b, kv.x, fmaf(pt, qv.x, ak[a][0]));
+                        ak[a][1] = fmaf(b, kv.y, fmaf(pt, qv.y, ak[a][1]));
+                        ak[a][2] = fmaf(b, kv.z, fmaf(pt, qv.z, ak[a][2]));
+                        ak[a][3] = fmaf(b, kv.w, fmaf(pt, qv.w, ak[a][3]));
+                    }
+                }
+#pragma unroll
+                for (int a = 0; a < TPT; ++a)
+                    if (i0 + a < cl) {
+                        float *dst = part + (tok0 + i0 + a) * pst + m0 + j4;
+                        *reinterpret_cast<float4 *>(dst) = make_float4(aq[a][0], aq[a][1], aq[a][2], aq[a][3]);
+                        *reinterpret_cast<float4 *>(dst + d_dot) = make_float4(ak[a][0], ak[a][1], ak[a][2], ak[a][3]);
+                    }
+            }
         }
         __syncthreads();
     }
 }
 
-size_t prep_smem() { return sizeof(float) * (2 * kCC * kSd + 3 * kCC * kLd + kCC); }
+size_t prep_smem(int d_v) {
+    const size_t dvp = ((size_t)d_v + 7) & ~(size_t)7;
+    return sizeof(float) * (2 * kCC * kSd + 3 * kCC * kLd + kCC * (dvp + 1) + kCC);
+}
 size_t scan_smem(int d_dot) {
-    return sizeof(float) * ((size_t)(kCR + kCC) * (d_dot + 1) + kCC * kLd + 2 * kCC * kRd + kCC);
+    return sizeof(float) * ((size_t)(kCR + kCC) * (d_dot + 4) + kCC * kLd + 2 * kCC * kRd);
 }
 size_t gscan_smem(int d_dot) {
-    return sizeof(float) * ((size_t)(kCR + kCC) * (d_dot + 1) + 2 * kCC * kLd + 3 * kCC * kRd + kCC);
+    return sizeof(float) * ((size_t)(kCR + kCC) * (d_dot + 4) + 2 * kCC * kLd + 3 * kCC * kRd);
 }
-size_t cgrad_smem(int d_v) {
-    return sizeof(float) * (4 * kCC * kLd + 3 * (size_t)kCC * (d_v + 1) + 2 * (size_t)d_v * kSd + 2 * kCC * kSd +
+template <int SW> size_t cgrad_smem(int d_v) {
+    return sizeof(float) * (3 * kCC * kLd + kCC * kLdP + 3 * (size_t)kCC * (d_v + 1) + grad_stage_floats<SW>(d_v) +
                             2 * kCC);
 }
+constexpr size_t kSmemCap = (size_t)227 * 1024;
 
 // Offsets (in floats) of the buffers after phi(k), phi(q) and the per-token
 // gradient records inside the workspace.
 struct ChunkLayout {
-    size_t M, P, KK, S, dS, X, U, dX, dU, end;
+    size_t M, T, P, KK, G, S, dS, X, U, dX, dU, end;
 };
 
 ChunkLayout chunk_layout(int BH, int L, int d_dot, int d_v) {
@@ -575,9 +656,11 @@ ChunkLayout chunk_layout(int BH, int L, int d_dot, int d_v) {
     const size_t sts = (size_t)BH * nC * d_v * d_dot;
     ChunkLayout o;
     o.M = 0;
-    o.P = o.M + cc;
+    o.T = o.M + cc;
+    o.P = o.T + cc;
     o.KK = o.P + cc;
-    o.S = o.KK + cc;
+    o.G = o.KK + cc;
+    o.S = o.G + sts;
     o.dS = o.S + sts;
     o.X = o.dS + sts;
     o.U = o.X + rows * d_v;
@@ -594,14 +677,15 @@ cudaError_t launch_chunked_t(const float *phk, const float *phq, const void *v, 
     const int nC = (L + kCC - 1) / kCC, nRB = (d_v + kCR - 1) / kCR;
     const ChunkLayout o = chunk_layout(BH, L, d_dot, d_v);
     const T *vt = static_cast<const T *>(v), *bt = static_cast<const T *>(beta), *gyt = static_cast<const T *>(gy);
+    const dim3 chunks((unsigned)BH, (unsigned)nC), rowblocks((unsigned)BH, (unsigned)nRB);
     cudaError_t e;
     {
         auto kern = chunk_prep_kernel<T>;
-        const size_t smem = prep_smem();
+        const size_t smem = prep_smem(d_v);
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
             return e;
-        kern<<<dim3((unsigned)BH, (unsigned)nC), kCT, smem, st>>>(phk, phq, bt, buf + o.M, buf + o.P, buf + o.KK, L,
-                                                                  d_dot, nC);
+        kern<<<chunks, kCT, smem, st>>>(phk, phq, bt, gyt, buf + o.M, buf + o.T, buf + o.P, buf + o.KK, buf + o.G, L,
+                                        d_dot, d_v, nC);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
@@ -610,8 +694,8 @@ cudaError_t launch_chunked_t(const float *phk, const float *phq, const void *v, 
         const size_t smem = scan_smem(d_dot);
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
             return e;
-        kern<<<dim3((unsigned)BH, (unsigned)nRB), kCT, smem, st>>>(phk, vt, bt, W0, buf + o.M, buf + o.S, buf + o.X,
-                                                                   buf + o.U, L, d_dot, d_v, nC);
+        kern<<<rowblocks, kCT, smem, st>>>(phk, vt, W0, buf + o.T, buf + o.S, buf + o.X, buf + o.U, L, d_dot, d_v,
+                                           nC);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
@@ -620,19 +704,18 @@ cudaError_t launch_chunked_t(const float *phk, const float *phq, const void *v, 
         const size_t smem = gscan_smem(d_dot);
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
             return e;
-        kern<<<dim3((unsigned)BH, (unsigned)nRB), kCT, smem, st>>>(phk, phq, bt, gyt, gWL, buf + o.M, buf + o.P,
-                                                                   buf + o.dS, buf + o.dX, buf + o.dU,
-                                                                   static_cast<T *>(gv), gW0, L, d_dot, d_v, nC);
+        kern<<<rowblocks, kCT, smem, st>>>(phk, gyt, gWL, buf + o.T, buf + o.P, buf + o.G, buf + o.dS, buf + o.dX,
+                                           buf + o.dU, static_cast<T *>(gv), gW0, L, d_dot, d_v, nC);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
-    auto kern = chunk_grad_kernel<T>;
-    const size_t smem = cgrad_smem(d_v);
+    const bool wide = cgrad_smem<64>(d_v) <= kSmemCap;
+    auto kern = wide ? chunk_grad_kernel<T, 64> : chunk_grad_kernel<T, 32>;
+    const size_t smem = wide ? cgrad_smem<64>(d_v) : cgrad_smem<32>(d_v);
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;
-    kern<<<dim3((unsigned)BH, (unsigned)nC), kCT, smem, st>>>(phk, phq, bt, gyt, buf + o.S, buf + o.dS, buf + o.X,
-                                                              buf + o.U, buf + o.dX, buf + o.dU, buf + o.M,
-                                                              buf + o.KK, part, L, d_dot, d_v, nC);
+    kern<<<chunks, kCT, smem, st>>>(phk, phq, bt, gyt, buf + o.S, buf + o.dS, buf + o.X, buf + o.U, buf + o.dX,
+                                    buf + o.dU, buf + o.M, buf + o.KK, part, L, d_dot, d_v, nC);
     return cudaGetLastError();
 }
 
@@ -640,9 +723,8 @@ cudaError_t launch_chunked_t(const float *phk, const float *phq, const void *v, 
 
 bool backward_chunked_supported(int d_key, int nu, int d_v, int L) {
     const int d_dot = 2 * d_key * nu;
-    const size_t cap = (size_t)227 * 1024;
-    return d_dot <= 512 && d_v <= 128 && (L + kCC - 1) / kCC <= 65535 && scan_smem(d_dot) <= cap &&
-           gscan_smem(d_dot) <= cap && cgrad_smem(d_v) <= cap;
+    return d_dot <= 512 && d_v <= 128 && (L + kCC - 1) / kCC <= 65535 && prep_smem(d_v) <= kSmemCap &&
+           scan_smem(d_dot) <= kSmemCap && gscan_smem(d_dot) <= kSmemCap && cgrad_smem<32>(d_v) <= kSmemCap;
 }
 
 size_t backward_chunked_buffer_floats(int BH, int L, int d_key, int nu, int d_v) {

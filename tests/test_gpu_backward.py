@@ -1,7 +1,9 @@
 """GPU parity of the delta-rule backward (fw_delta_backward) against the fp64
 oracle's backward (itself pinned to finite differences of the forward), on
-the same seeded inputs, through the C ABI.  Tolerances: max normwise relative
-error per gradient tensor, 1e-4 for fp32 I/O and 2e-2 for bf16 I/O."""
+the same seeded inputs, through the C ABI: the chunk-parallel form for
+d_dot <= 512 and d_v <= 128, the token-serial kernel past that.
+Tolerances: max normwise relative error per gradient tensor, 1e-4 for fp32
+I/O and 2e-2 for bf16 I/O."""
 import numpy as np
 import pytest
 import torch
@@ -51,6 +53,8 @@ CASES = [  # B, H, L, d_key, nu, d_v
     (2, 1, 20, 8, 5, 128),
     (1, 3, 45, 32, 1, 40),      # row blocks of 16, 16 and 8
     (1, 2, 30, 64, 4, 128),     # d_dot 512 with d_v 128: 8 row blocks
+    (1, 1, 70, 128, 3, 32),     # d_dot 768: past the chunked form's limit, token by token
+    (1, 2, 25, 16, 1, 150),     # d_v 150: token by token, 10 row blocks, the last of 6 rows
 ]
 
 
