@@ -622,7 +622,7 @@ def stack_only(steps):
 
 def backward_only(steps):
     """`steps` fw_delta_backward calls on b4h8_l512 (bf16 I/O) through the public
-    API (7 launches each), nothing else: the command the backward's profiles
+    API (6 launches each), nothing else: the command the backward's profiles
     are captured from."""
     from delta_rule_linear_dpfp_gb300 import binding as fw, build, inputs
     build.build()
@@ -636,7 +636,7 @@ def backward_only(steps):
     for _ in range(steps):
         fw.fw_delta_backward(fi["q"], fi["k"], fi["v"], fi["beta"], dy, nu=nu, workspace=ws)
     torch.cuda.synchronize()
-    print(json.dumps({"backward_steps": steps, "launches_per_step": 7}))
+    print(json.dumps({"backward_steps": steps, "launches_per_step": 6}))
 
 
 # ------------------------------------------------------------ the oracle

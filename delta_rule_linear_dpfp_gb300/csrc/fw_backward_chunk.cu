@@ -21,11 +21,12 @@
 //   chunk_prep   one CTA per (b,h, chunk): K K^T, P, M by forward
 //                substitution column by column, T = M diag(beta), and
 //                G = dY^T Q (the part of dS that does not depend on the scan);
-//   state_scan   one CTA per (b,h, 16 value rows): the chunk-start states S
-//                in chunk order (kept for the gradient kernel), X and U;
-//   grad_scan    the same split, chunks in reverse: dS' kept per chunk, dU,
+//   scans        one launch, two independent kinds of CTA, each per (b,h,
+//                16 value rows): the state scan (the chunk-start states S in
+//                chunk order, kept for the gradient kernel, with X and U) and
+//                the reverse scan (chunks in reverse: dS' kept per chunk, dU,
 //                dX (= dV, written out), dS = dS' + G - dX^T K, and dW0 at
-//                the end;
+//                the end);
 //   chunk_grad   one CTA per (b,h, chunk): dT, dP, dA, dbeta and the phi-space
 //                gradients of q and k, written where the DPFP-backward kernel
 //                of fw_backward.cu reads them.
@@ -87,6 +88,28 @@ FW_DEV void stage4(float *dst, int ldd, const float *src, size_t lds, int rows, 
     }
 }
 
+// Stage a rows x cols block of T (source row stride lds elements) into
+// shared memory as fp32 (row stride ldd); rows at or past `valid` read as
+// zero.  Four loads per thread in flight before the first store.
+template <typename T>
+FW_DEV void stage1(float *dst, int ldd, const T *src, size_t lds, int rows, int valid, int cols, int tid, int nt) {
+    const int n = rows * cols;
+    for (int e0 = tid; e0 < n; e0 += 4 * nt) {
+        float t[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * nt, i = e / cols;
+            t[u] = (e < n && i < valid) ? io<T>::load(src + (size_t)i * lds + e % cols) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * nt;
+            if (e < n)
+                dst[(size_t)(e / cols) * ldd + e % cols] = t[u];
+        }
+    }
+}
+
 FW_DEV float dot4(float4 a, float4 b, float acc) {
     return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, acc))));
 }
@@ -117,10 +140,9 @@ __global__ void __launch_bounds__(kCT)
         kk[(e / kCC) * kLd + e % kCC] = 0.f;
         pq[(e / kCC) * kLd + e % kCC] = 0.f;
     }
-    for (int e = tid; e < kCC * dvp; e += nt) {
-        const int i = e / dvp, r = e % dvp;
-        dyv[i * yd + r] = (i < cl && r < d_v) ? io<T>::load(gy + (tok0 + i) * d_v + r) : 0.f;
-    }
+    for (int e = tid; e < kCC * (dvp - d_v); e += nt)
+        dyv[(e / (dvp - d_v)) * yd + d_v + e % (dvp - d_v)] = 0.f;
+    stage1(dyv, yd, gy + tok0 * d_v, d_v, kCC, cl, d_v, tid, nt);
     __syncthreads();
     for (int s0 = 0; s0 < d_dot; s0 += kSl) {
         const int sw = min(kSl, d_dot - s0);
@@ -217,15 +239,13 @@ __global__ void __launch_bounds__(kCT)
 // Shared memory: ss [kCR][d_dot + 4] (the CTA's rows of S), kc [C][d_dot + 4],
 // tc [C][kLd] (T), xs, us [C][kRd].
 template <typename T>
-__global__ void __launch_bounds__(kCT)
-    state_scan_kernel(const float *__restrict__ phk, const T *__restrict__ v, const float *__restrict__ W0,
-                      const float *__restrict__ Tb, float *__restrict__ Sb, float *__restrict__ Xb,
-                      float *__restrict__ Ub, int L, int d_dot, int d_v, int nC) {
-    extern __shared__ float sm[];
+FW_DEV void state_scan(float *sm, const float *__restrict__ phk, const T *__restrict__ v, const float *__restrict__ W0,
+                       const float *__restrict__ Tb, float *__restrict__ Sb, float *__restrict__ Xb,
+                       float *__restrict__ Ub, int L, int d_dot, int d_v, int nC, int bh, int rb) {
     const int sd = d_dot + 4, d4 = d_dot >> 2;
     float *ss = sm, *kc = ss + kCR * sd, *tc = kc + kCC * sd, *xs = tc + kCC * kLd, *us = xs + kCC * kRd;
     const int tid = threadIdx.x, nt = blockDim.x;
-    const int bh = blockIdx.x, r0 = blockIdx.y * kCR, R = min(kCR, d_v - r0);
+    const int r0 = rb * kCR, R = min(kCR, d_v - r0);
 
     if (W0)
         stage4(ss, sd, W0 + ((size_t)bh * d_v + r0) * d_dot, d_dot, kCR, R, d_dot, tid, nt);
@@ -243,10 +263,9 @@ __global__ void __launch_bounds__(kCT)
         }
         stage4(kc, sd, phk + tok0 * d_dot, d_dot, kCC, cl, d_dot, tid, nt);
         stage4(tc, kLd, Tb + ((size_t)bh * nC + c) * kCC * kCC, kCC, kCC, kCC, kCC, tid, nt);
-        for (int e = tid; e < kCC * kCR; e += nt) {
-            const int i = e / kCR, r = e % kCR;
-            xs[i * kRd + r] = (i < cl && r < R) ? io<T>::load(v + (tok0 + i) * d_v + r0 + r) : 0.f;
-        }
+        for (int e = tid; e < kCC * (kCR - R); e += nt)
+            xs[(e / (kCR - R)) * kRd + R + e % (kCR - R)] = 0.f;
+        stage1(xs, kRd, v + tok0 * d_v + r0, d_v, kCC, cl, R, tid, nt);
         __syncthreads();
         // X = V - K S^T: 256 tiles, row r = w & 15, tokens (w >> 4) + 16a
         for (int w = tid; w < 256; w += nt) {
@@ -317,17 +336,16 @@ __global__ void __launch_bounds__(kCT)
 // Shared memory: ds [kCR][d_dot + 4] (the CTA's rows of dS), kc [C][d_dot + 4],
 // tc, pc [C][kLd] (T and P), dys, dus, dxs [C][kRd].
 template <typename T>
-__global__ void __launch_bounds__(kCT)
-    grad_scan_kernel(const float *__restrict__ phk, const T *__restrict__ gy, const float *__restrict__ gWL,
-                     const float *__restrict__ Tb, const float *__restrict__ Pb, const float *__restrict__ Gb,
-                     float *__restrict__ dSb, float *__restrict__ dXb, float *__restrict__ dUb, T *__restrict__ gv,
-                     float *__restrict__ gW0, int L, int d_dot, int d_v, int nC) {
-    extern __shared__ float sm[];
+FW_DEV void grad_scan(float *sm, const float *__restrict__ phk, const T *__restrict__ gy,
+                      const float *__restrict__ gWL, const float *__restrict__ Tb, const float *__restrict__ Pb,
+                      const float *__restrict__ Gb, float *__restrict__ dSb, float *__restrict__ dXb,
+                      float *__restrict__ dUb, T *__restrict__ gv, float *__restrict__ gW0, int L, int d_dot, int d_v,
+                      int nC, int bh, int rb) {
     const int sd = d_dot + 4, d4 = d_dot >> 2;
     float *ds = sm, *kc = ds + kCR * sd, *tc = kc + kCC * sd, *pc = tc + kCC * kLd, *dys = pc + kCC * kLd;
     float *dus = dys + kCC * kRd, *dxs = dus + kCC * kRd;
     const int tid = threadIdx.x, nt = blockDim.x;
-    const int bh = blockIdx.x, r0 = blockIdx.y * kCR, R = min(kCR, d_v - r0);
+    const int r0 = rb * kCR, R = min(kCR, d_v - r0);
 
     if (gWL)
         stage4(ds, sd, gWL + ((size_t)bh * d_v + r0) * d_dot, d_dot, kCR, R, d_dot, tid, nt);
@@ -347,10 +365,9 @@ __global__ void __launch_bounds__(kCT)
         stage4(kc, sd, phk + tok0 * d_dot, d_dot, kCC, cl, d_dot, tid, nt);
         stage4(tc, kLd, Tb + cc0, kCC, kCC, kCC, kCC, tid, nt);
         stage4(pc, kLd, Pb + cc0, kCC, kCC, kCC, kCC, tid, nt);
-        for (int e = tid; e < kCC * kCR; e += nt) {
-            const int i = e / kCR, r = e % kCR;
-            dys[i * kRd + r] = (i < cl && r < R) ? io<T>::load(gy + (tok0 + i) * d_v + r0 + r) : 0.f;
-        }
+        for (int e = tid; e < kCC * (kCR - R); e += nt)
+            dys[(e / (kCR - R)) * kRd + R + e % (kCR - R)] = 0.f;
+        stage1(dys, kRd, gy + tok0 * d_v + r0, d_v, kCC, cl, R, tid, nt);
         __syncthreads();
         // dU = K dS'^T + P^T dY (P lower, so P_si is zero for s < i)
         for (int w = tid; w < 256; w += nt) {
@@ -425,6 +442,26 @@ __global__ void __launch_bounds__(kCT)
         }
 }
 
+// ----------------------------------------------------------------- scans
+// The two scans do not depend on each other (the reverse scan needs T, P, G,
+// K and dY, not S), so one launch runs both: blocks y < nRB scan the states,
+// the others their gradients.
+template <typename T>
+__global__ void __launch_bounds__(kCT)
+    scans_kernel(const float *__restrict__ phk, const T *__restrict__ v, const T *__restrict__ gy,
+                 const float *__restrict__ W0, const float *__restrict__ gWL, const float *__restrict__ Tb,
+                 const float *__restrict__ Pb, const float *__restrict__ Gb, float *__restrict__ Sb,
+                 float *__restrict__ Xb, float *__restrict__ Ub, float *__restrict__ dSb, float *__restrict__ dXb,
+                 float *__restrict__ dUb, T *__restrict__ gv, float *__restrict__ gW0, int L, int d_dot, int d_v,
+                 int nC, int nRB) {
+    extern __shared__ float sm[];
+    if ((int)blockIdx.y < nRB)
+        state_scan<T>(sm, phk, v, W0, Tb, Sb, Xb, Ub, L, d_dot, d_v, nC, blockIdx.x, blockIdx.y);
+    else
+        grad_scan<T>(sm, phk, gy, gWL, Tb, Pb, Gb, dSb, dXb, dUb, gv, gW0, L, d_dot, d_v, nC, blockIdx.x,
+                     blockIdx.y - nRB);
+}
+
 // ------------------------------------------------------------ chunk_grad
 // Shared memory: c1 (dT, then dA), c3 (M), c4 (M^T dT diag(beta), then
 // B + B^T), each [C][kLd]; c2 (dP) [C][kLdP]; dys, uvs, dxs [C][d_v + 1]; a
@@ -457,13 +494,9 @@ __global__ void __launch_bounds__(kCT)
 
     for (int i = tid; i < kCC; i += nt)
         bs[i] = i < cl ? io<T>::load(beta + tok0 + i) : 0.f;
-    for (int e = tid; e < kCC * d_v; e += nt) {
-        const int i = e / d_v, r = e % d_v;
-        const bool in = i < cl;
-        dys[i * vd + r] = in ? io<T>::load(gy + (tok0 + i) * d_v + r) : 0.f;
-        uvs[i * vd + r] = in ? ldf(Ub + (tok0 + i) * d_v + r) : 0.f;
-        dxs[i * vd + r] = in ? ldf(dXb + (tok0 + i) * d_v + r) : 0.f;
-    }
+    stage1(dys, vd, gy + tok0 * d_v, d_v, kCC, cl, d_v, tid, nt);
+    stage1(uvs, vd, Ub + tok0 * d_v, d_v, kCC, cl, d_v, tid, nt);
+    stage1(dxs, vd, dXb + tok0 * d_v, d_v, kCC, cl, d_v, tid, nt);
     for (int e = tid; e < kCC * kCC; e += nt) {
         const int i = e / kCC, j = e % kCC;
         c1[i * kLd + j] = 0.f;
@@ -474,12 +507,8 @@ __global__ void __launch_bounds__(kCT)
     float *dul = stg, *xl = stg + kCC * kSd;
     for (int r0 = 0; r0 < d_v; r0 += kSl) {
         const int rn = min(kSl, d_v - r0);
-        for (int e = tid; e < kCC * kSl; e += nt) {
-            const int i = e / kSl, j = e % kSl;
-            const bool in = i < cl && j < rn;
-            dul[i * kSd + j] = in ? ldf(dUb + (tok0 + i) * d_v + r0 + j) : 0.f;
-            xl[i * kSd + j] = in ? ldf(Xb + (tok0 + i) * d_v + r0 + j) : 0.f;
-        }
+        stage1(dul, kSd, dUb + tok0 * d_v + r0, d_v, kCC, cl, rn, tid, nt);
+        stage1(xl, kSd, Xb + tok0 * d_v + r0, d_v, kCC, cl, rn, tid, nt);
         __syncthreads();
         for (int w = tid; w < 256; w += nt) {
             const int tx = w & 15, ty = w >> 4;
@@ -518,8 +547,10 @@ __global__ void __launch_bounds__(kCT)
         }
         __syncthreads();
     }
-    // M in; dP = tril_inclusive(dY U^T)
+    // M in, K K^T into the staging region; dP = tril_inclusive(dY U^T)
+    float *kks = stg;
     stage4(c3, kLd, Mb + cc0, kCC, kCC, kCC, kCC, tid, nt);
+    stage4(kks, kLd, KKb + cc0, kCC, kCC, kCC, kCC, tid, nt);
     for (int e = tid; e < kCC * kCC; e += nt) {
         const int i = e / kCC, j = e % kCC;
         if (j > i)
@@ -555,7 +586,7 @@ __global__ void __launch_bounds__(kCT)
     for (int i = tid; i < kCC; i += nt) {
         float acc = gb[i];
         for (int j = 0; j < i; ++j)
-            acc = fmaf(c1[i * kLd + j], ldf(KKb + cc0 + (size_t)i * kCC + j), acc);
+            acc = fmaf(c1[i * kLd + j], kks[i * kLd + j], acc);
         gb[i] = acc;
     }
     for (int e = tid; e < kCC * kCC; e += nt) {
@@ -677,7 +708,7 @@ cudaError_t launch_chunked_t(const float *phk, const float *phq, const void *v, 
     const int nC = (L + kCC - 1) / kCC, nRB = (d_v + kCR - 1) / kCR;
     const ChunkLayout o = chunk_layout(BH, L, d_dot, d_v);
     const T *vt = static_cast<const T *>(v), *bt = static_cast<const T *>(beta), *gyt = static_cast<const T *>(gy);
-    const dim3 chunks((unsigned)BH, (unsigned)nC), rowblocks((unsigned)BH, (unsigned)nRB);
+    const dim3 chunks((unsigned)BH, (unsigned)nC);
     cudaError_t e;
     {
         auto kern = chunk_prep_kernel<T>;
@@ -690,22 +721,13 @@ cudaError_t launch_chunked_t(const float *phk, const float *phq, const void *v, 
             return e;
     }
     {
-        auto kern = state_scan_kernel<T>;
-        const size_t smem = scan_smem(d_dot);
+        auto kern = scans_kernel<T>;
+        const size_t smem = std::max(scan_smem(d_dot), gscan_smem(d_dot));
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
             return e;
-        kern<<<rowblocks, kCT, smem, st>>>(phk, vt, W0, buf + o.T, buf + o.S, buf + o.X, buf + o.U, L, d_dot, d_v,
-                                           nC);
-        if ((e = cudaGetLastError()) != cudaSuccess)
-            return e;
-    }
-    {
-        auto kern = grad_scan_kernel<T>;
-        const size_t smem = gscan_smem(d_dot);
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
-            return e;
-        kern<<<rowblocks, kCT, smem, st>>>(phk, gyt, gWL, buf + o.T, buf + o.P, buf + o.G, buf + o.dS, buf + o.dX,
-                                           buf + o.dU, static_cast<T *>(gv), gW0, L, d_dot, d_v, nC);
+        kern<<<dim3((unsigned)BH, 2u * nRB), kCT, smem, st>>>(
+            phk, vt, gyt, W0, gWL, buf + o.T, buf + o.P, buf + o.G, buf + o.S, buf + o.X, buf + o.U, buf + o.dS,
+            buf + o.dX, buf + o.dU, static_cast<T *>(gv), gW0, L, d_dot, d_v, nC, nRB);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
