@@ -105,6 +105,19 @@ def roofline(name, flops, nbytes, ms, pk):
     return r
 
 
+# fp32 FMA peak of the CUDA cores, from unit counts and clocks: 152 SMs x 128 fp32 lanes x 2 FLOP per FMA x
+# the 2070 MHz maximum SM clock
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def alu_roofline(name, flops, ms):
+    """Achieved fp32 rate of a path that runs on the CUDA cores' FMA units."""
+    a = flops / (ms * 1e-3) / 1e12
+    return {"bound": "alu", "achieved": a, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": a / FP32_ALU_TFLOPS,
+            "kernel": name, "kernel_ms": ms, "algorithmic_flops": flops,
+            "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x 2.07 GHz"}
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples while the timed region runs."""
 
@@ -547,7 +560,8 @@ def measure_rows(fw, inputs, dev, stream, pk):
     # the reverse sweep (about 12 d_dot d_v), fp32
     flops = 14.0 * d_dot * d_v * B * H * L
     nbytes = B * H * L * 2 * (2 * 2 * d_key + 2 * 2 * d_v + 2) + B * H * d_v * d_dot * 4
-    r = roofline("fw_delta_backward (fp32, chunk-parallel)", flops, nbytes, ms, pk)
+    r = alu_roofline("fw_delta_backward (fp32, chunk-parallel)", flops, ms)
+    r["algorithmic_bytes"] = nbytes
     r["tokens/s"] = B * L / (ms * 1e-3)
     rows["backward_b4h8_l512"] = r
     # the token-wise layer stack: one token of 256 sequences through 6 layers (d_model 512, 8 heads of 64,
