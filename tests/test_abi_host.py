@@ -263,3 +263,31 @@ def test_backward_workspace_limits(lib):
     assert ws(2, 2, 16, 128, 4, 200, 1) > 0       # d_dot 1024, d_v not a multiple of the row block
     assert ws(2, 2, 16, 128, 5, 64, 1) == 0       # d_dot 1280 > 1024
     assert ws(2, 2, 16, 12, 1, 64, 1) == 0        # d_key not compiled
+
+
+def _chunked_ws(BH, L, d_dot, d_v):
+    # phi(k), phi(q), the per-token records, then per chunk M, T, P, K K^T (64 x 64 each) and G, S, dS'
+    # (d_v x d_dot each), then X, U, dX, dU per token (fp32 throughout)
+    rows, nC = BH * L, -(-L // 64)
+    return 4 * (2 * rows * d_dot + rows * (2 * d_dot + 4) + 4 * BH * nC * 64 * 64 + 3 * BH * nC * d_v * d_dot
+                + 4 * rows * d_v)
+
+
+def _serial_ws(BH, L, d_dot, d_v):
+    # u_t per token, phi(k), phi(q), then each block of 16 rows' per-token records
+    rows = BH * L
+    return 4 * (rows * d_v + 2 * rows * d_dot + -(-d_v // 16) * rows * (2 * d_dot + 4))
+
+
+def test_backward_path_choice_by_workspace(lib):
+    """The backward takes the chunk-parallel path for d_dot <= 512, d_v <= 128
+    and at most 65535 chunks of 64 tokens, the token-serial one past that;
+    the workspace size says which."""
+    ws = lib.fw_delta_backward_workspace_size
+    assert ws(4, 8, 512, 64, 1, 64, 1) == _chunked_ws(32, 512, 128, 64) == 92_536_832   # the bench shape
+    assert ws(1, 2, 30, 64, 4, 128, 0) == _chunked_ws(2, 30, 512, 128)                  # both limits met
+    assert ws(1, 1, 70, 128, 3, 32, 0) == _serial_ws(1, 70, 768, 32)                    # d_dot 768
+    assert ws(1, 2, 25, 16, 1, 129, 0) == _serial_ws(2, 25, 32, 129)                    # d_v 129
+    L = 64 * 65535
+    assert ws(1, 1, L, 8, 1, 16, 1) == _chunked_ws(1, L, 16, 16)
+    assert ws(1, 1, L + 1, 8, 1, 16, 1) == _serial_ws(1, L + 1, 16, 16)                 # 65536 chunks
