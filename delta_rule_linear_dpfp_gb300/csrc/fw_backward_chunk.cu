@@ -18,8 +18,9 @@
 // of the chunk algebra above, equal to the token-by-token chain rule.
 //
 // Kernels (fp32 on CUDA cores, deterministic summation orders):
-//   chunk_prep   one CTA per (b,h, chunk): K K^T, P, M by forward
-//                substitution column by column, T = M diag(beta), and
+//   chunk_prep   one CTA per (b,h, chunk): K K^T, P, M (blocked: forward
+//                substitution inside 16 x 16 diagonal blocks, products
+//                below them), T = M diag(beta), and
 //                G = dY^T Q (the part of dS that does not depend on the scan);
 //   scans        one launch, two independent kinds of CTA, each per (b,h,
 //                16 value rows): the state scan (the chunk-start states S in
@@ -215,12 +216,21 @@ __global__ void __launch_bounds__(kCT)
         pq[i * kLd + j] = j < i ? bs[i] * g : 0.f;
     }
     __syncthreads();
-    // M = (I + A)^-1, unit lower: column j by forward substitution
-    for (int j = tid; j < kCC; j += nt) {
-        for (int i = 0; i < j; ++i)
+    // M = (I + A)^-1, unit lower, in blocks of kB: the diagonal blocks by
+    // forward substitution (one thread per column), then the blocks below
+    // the diagonal one block distance d at a time, from (I + A) M = I:
+    //   M_IJ = -M_II Z_IJ,  Z_IJ = sum_{K=J}^{I-1} A_IK M_KJ  (I = J + d),
+    // with Z in the dead K slice buffer.
+    constexpr int kB = 16, kNB = kCC / kB;
+    for (int e = tid; e < kCC * kCC; e += nt) {
+        const int i = e / kCC, j = e % kCC;
+        if (i < j)
             ms[i * kLd + j] = 0.f;
+    }
+    for (int j = tid; j < kCC; j += nt) {
+        const int bend = (j / kB + 1) * kB;
         ms[j * kLd + j] = 1.f;
-        for (int i = j + 1; i < kCC; ++i) {
+        for (int i = j + 1; i < bend; ++i) {
             float acc = 0.f;
             for (int m = j; m < i; ++m)
                 acc = fmaf(pq[i * kLd + m], ms[m * kLd + j], acc);
@@ -228,6 +238,26 @@ __global__ void __launch_bounds__(kCT)
         }
     }
     __syncthreads();
+    float *zb = ks; // (kNB - 1) blocks of kB x kB
+    for (int d = 1; d < kNB; ++d) {
+        const int nblk = kNB - d;
+        for (int w = tid; w < nblk * kB * kB; w += nt) {
+            const int J = w / (kB * kB), a = (w / kB) % kB, b = w % kB, I = J + d;
+            float acc = 0.f;
+            for (int m = J * kB; m < I * kB; ++m)
+                acc = fmaf(pq[(I * kB + a) * kLd + m], ms[m * kLd + J * kB + b], acc);
+            zb[w] = acc;
+        }
+        __syncthreads();
+        for (int w = tid; w < nblk * kB * kB; w += nt) {
+            const int J = w / (kB * kB), a = (w / kB) % kB, b = w % kB, I = J + d;
+            float acc = 0.f;
+            for (int c = 0; c < kB; ++c)
+                acc = fmaf(ms[(I * kB + a) * kLd + I * kB + c], zb[J * kB * kB + c * kB + b], acc);
+            ms[(I * kB + a) * kLd + J * kB + b] = -acc;
+        }
+        __syncthreads();
+    }
     for (int e = tid; e < kCC * kCC; e += nt) {
         const float mv = ms[(e / kCC) * kLd + e % kCC];
         Mb[cc0 + e] = mv;
