@@ -284,7 +284,10 @@ int check_backward_shape(int B, int H, int L, int d_key, int nu, int d_v, int io
 FW_API size_t fw_delta_backward_workspace_size(int B, int H, int L, int d_key, int nu, int d_v, int io_dtype) {
     if (check_backward_shape(B, H, L, d_key, nu, d_v, io_dtype) != FW_OK)
         return 0;
-    return fw::backward_workspace_bytes(B * H, L, d_key, nu, d_v);
+    const int64_t BH = (int64_t)B * H;
+    if (BH > (int64_t)1 << 30) // fw_delta_backward rejects it too
+        return 0;
+    return fw::backward_workspace_bytes((int)BH, L, d_key, nu, d_v);
 }
 
 FW_API int fw_delta_backward(const void *q, const void *k, const void *v, const void *beta, const float *W0,

@@ -263,6 +263,7 @@ def test_backward_workspace_limits(lib):
     assert ws(2, 2, 16, 128, 4, 200, 1) > 0       # d_dot 1024, d_v not a multiple of the row block
     assert ws(2, 2, 16, 128, 5, 64, 1) == 0       # d_dot 1280 > 1024
     assert ws(2, 2, 16, 12, 1, 64, 1) == 0        # d_key not compiled
+    assert ws(65536, 65536, 1, 64, 1, 64, 1) == 0  # B H past 2^30 (and past int): rejected, not wrapped
 
 
 def _chunked_ws(BH, L, d_dot, d_v):
