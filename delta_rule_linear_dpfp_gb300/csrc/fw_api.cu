@@ -6,6 +6,7 @@
 #include "fw_forward_tc.h"
 #include "fw_stack.h"
 
+#include <climits>
 #include <cmath>
 #include <mutex>
 
@@ -58,6 +59,9 @@ cudaError_t device_info(DeviceInfo *out) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool dtype_ok(int d) { return d == FW_DTYPE_F32 || d == FW_DTYPE_BF16; }
+// Longest sequence: chunk counts are formed as (L + chunk - 1) / chunk in int.
+constexpr int kMaxL = INT_MAX - 64;
+
 bool dkey_supported(int d_key) {
     return d_key == 8 || d_key == 16 || d_key == 32 || d_key == 64 || d_key == 128;
 }
@@ -93,7 +97,7 @@ FW_API const char *fw_status_string(int status) {
 
 FW_API int fw_dpfp(const void *x, void *phi, int64_t rows, int d_key, int nu, int in_dtype,
                    int out_dtype, float eps, void *stream) {
-    if (rows < 0 || d_key <= 0 || nu < 1 || nu > 2 * d_key - 1 || !dtype_ok(in_dtype) ||
+    if (rows < 0 || d_key <= 0 || nu < 1 || nu > 2 * (int64_t)d_key - 1 || !dtype_ok(in_dtype) ||
         !dtype_ok(out_dtype) || !eps_ok(eps))
         return FW_ERR_INVALID_ARG;
     if (!dkey_supported(d_key))
@@ -116,9 +120,11 @@ namespace {
 // Shape checks shared by the forward and its workspace query.
 // Returns FW_OK, FW_ERR_INVALID_ARG or FW_ERR_UNSUPPORTED.
 int check_forward_shape(int B, int H, int L, int d_key, int nu, int d_v, int chunk, int io_dtype) {
-    if (B < 0 || H < 0 || L < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 ||
+    if (B < 0 || H < 0 || L < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * (int64_t)d_key - 1 ||
         !dtype_ok(io_dtype) || !(chunk == 16 || chunk == 32 || chunk == 64))
         return FW_ERR_INVALID_ARG;
+    if (L > kMaxL)
+        return FW_ERR_UNSUPPORTED;
     if (!dkey_supported(d_key))
         return FW_ERR_UNSUPPORTED;
     const int d_dot = 2 * d_key * nu;
@@ -272,8 +278,11 @@ FW_API int fw_delta_forward_projected(const void *x, const void *W_all, int ldw,
 namespace {
 
 int check_backward_shape(int B, int H, int L, int d_key, int nu, int d_v, int io_dtype) {
-    if (B < 0 || H < 0 || L < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 || !dtype_ok(io_dtype))
+    if (B < 0 || H < 0 || L < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * (int64_t)d_key - 1 ||
+        !dtype_ok(io_dtype))
         return FW_ERR_INVALID_ARG;
+    if (L > kMaxL)
+        return FW_ERR_UNSUPPORTED;
     if (!dkey_supported(d_key) || 2 * d_key * nu > 1024 || fw::backward_smem_bytes(d_key, nu, d_v) > (size_t)227 * 1024)
         return FW_ERR_UNSUPPORTED;
     return FW_OK;
@@ -333,9 +342,11 @@ FW_API int fw_delta_backward(const void *q, const void *k, const void *v, const 
 namespace {
 
 int check_linear_shape(int B, int H, int L, int d_key, int nu, int d_v, int chunk, int normalize, int io_dtype) {
-    if (B < 0 || H < 0 || L < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 ||
+    if (B < 0 || H < 0 || L < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * (int64_t)d_key - 1 ||
         !dtype_ok(io_dtype) || !(chunk == 16 || chunk == 32 || chunk == 64) || (normalize != 0 && normalize != 1))
         return FW_ERR_INVALID_ARG;
+    if (L > kMaxL)
+        return FW_ERR_UNSUPPORTED;
     if (!dkey_supported(d_key) || io_dtype != FW_DTYPE_BF16)
         return FW_ERR_UNSUPPORTED;
     return fw::tc_linear_supported(d_key, nu, d_v, chunk, normalize) ? FW_OK : FW_ERR_UNSUPPORTED;
@@ -470,7 +481,7 @@ FW_API int fw_delta_forward_scan(const void *workspace, size_t workspace_bytes, 
 FW_API int fw_delta_decode_step(const void *q, const void *k, const void *v, const void *beta,
                                 float *W, void *y, int B, int H, int d_key, int nu, int d_v,
                                 int io_dtype, float eps, void *stream) {
-    if (!eps_ok(eps) || B < 0 || H < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 ||
+    if (!eps_ok(eps) || B < 0 || H < 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * (int64_t)d_key - 1 ||
         !dtype_ok(io_dtype))
         return FW_ERR_INVALID_ARG;
     if (!dkey_supported(d_key) || 2 * d_key * nu > 1024)
@@ -497,10 +508,10 @@ FW_API int fw_delta_decode_step(const void *q, const void *k, const void *v, con
 namespace {
 
 int check_stack_shape(int n_layers, int B, int H, int d_key, int nu, int d_v, int d_model, int d_ff) {
-    if (n_layers < 0 || B < 0 || H <= 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * d_key - 1 ||
+    if (n_layers < 0 || B < 0 || H <= 0 || d_key <= 0 || d_v <= 0 || nu < 1 || nu > 2 * (int64_t)d_key - 1 ||
         d_model <= 0 || d_ff <= 0)
         return FW_ERR_INVALID_ARG;
-    if (!dkey_supported(d_key) || 2 * d_key * nu > 1024 || d_model % 128 || d_model > 1024 || (H * d_v) % 64 ||
+    if (!dkey_supported(d_key) || 2 * d_key * nu > 1024 || d_model % 128 || d_model > 1024 || ((int64_t)H * d_v) % 64 ||
         d_ff % 64 || (int64_t)H * (2 * d_key + d_v + 1) > 65535 * 128 || d_ff > 65535 * 128 ||
         (int64_t)B * H > (int64_t)1 << 30)
         return FW_ERR_UNSUPPORTED;

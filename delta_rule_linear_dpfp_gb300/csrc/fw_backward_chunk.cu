@@ -775,7 +775,7 @@ cudaError_t launch_chunked_t(const float *phk, const float *phq, const void *v, 
 
 bool backward_chunked_supported(int d_key, int nu, int d_v, int L) {
     const int d_dot = 2 * d_key * nu;
-    return d_dot <= 512 && d_v <= 128 && (L + kCC - 1) / kCC <= 65535 && prep_smem(d_v) <= kSmemCap &&
+    return d_dot <= 512 && d_v <= 128 && ((int64_t)L + kCC - 1) / kCC <= 65535 && prep_smem(d_v) <= kSmemCap &&
            scan_smem(d_dot) <= kSmemCap && gscan_smem(d_dot) <= kSmemCap && cgrad_smem<32>(d_v) <= kSmemCap;
 }
 

@@ -292,3 +292,14 @@ def test_backward_path_choice_by_workspace(lib):
     L = 64 * 65535
     assert ws(1, 1, L, 8, 1, 16, 1) == _chunked_ws(1, L, 16, 16)
     assert ws(1, 1, L + 1, 8, 1, 16, 1) == _serial_ws(1, L + 1, 16, 16)                 # 65536 chunks
+
+
+def test_size_queries_at_integer_limits(lib):
+    """Sequence lengths whose chunk count would wrap in int, and key widths
+    whose 2 d_key would, are refused by the size queries (0), not computed."""
+    big = 2**31 - 1
+    assert lib.fw_delta_forward_workspace_size(1, 1, big, 64, 1, 64, 64, 1) == 0
+    assert lib.fw_delta_backward_workspace_size(1, 1, big, 64, 1, 64, 1) == 0
+    assert lib.fw_linear_forward_workspace_size(1, 1, big, 64, 1, 64, 64, 1, 1) == 0
+    assert lib.fw_delta_backward_workspace_size(1, 1, 16, big, 3, 64, 1) == 0
+    assert lib.fw_delta_forward_workspace_size(1, 1, 2**31 - 65, 64, 1, 64, 64, 1) > 0   # the longest L taken
