@@ -980,7 +980,7 @@ bool tc_forward_supported(int d_key, int nu, int d_v, int chunk) {
 }
 
 size_t tc_forward_workspace_bytes(int B, int H, int L, int d_key, int nu, int d_v, int chunk) {
-    const size_t nch = ((size_t)L + chunk - 1) / chunk;
+    const int nch = (L + chunk - 1) / chunk;
     return (size_t)B * H * nch * record_layout(padded_ddot(2 * d_key * nu), d_v).bytes;
 }
 
@@ -1046,7 +1046,7 @@ bool tc_linear_supported(int d_key, int nu, int d_v, int chunk, int normalize) {
 }
 
 size_t tc_linear_workspace_bytes(int B, int H, int L, int d_key, int nu, int d_v, int chunk, int normalize) {
-    const size_t nch = ((size_t)L + chunk - 1) / chunk;
+    const int nch = (L + chunk - 1) / chunk;
     return (size_t)B * H * nch * record_layout(padded_ddot(2 * d_key * nu), d_v + (normalize ? 16 : 0)).bytes;
 }
 
