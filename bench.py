@@ -1,20 +1,23 @@
 """Benchmark of the delta-rule fast-weight layer core on GB300.
 
 One step = one fw_delta_forward call (DPFP of q and k fused, the chunked
-delta rule, y and the final state written) over the B4 H8 L512 d_key 64
-nu 1 d_v 64 bf16 workload (chunk 64), with inputs resident in HBM.  Every
-rank runs its own replica of that workload (weak scaling, no data-path
-collective); the timing is bracketed by a barrier and a device
-synchronisation on both sides and the slowest rank's time is reported.
+delta rule, y and the final state written) over the B2 H8 L2048 d_key 64
+nu 3 (d_dot 384) d_v 64 bf16 workload (chunk 64), with a non-zero initial
+state W0 read and W_final written, inputs resident in HBM.  Every rank runs
+its own replica of that workload (weak scaling, no data-path collective); the
+timing is bracketed by a barrier and a device synchronisation on both sides
+and the slowest rank's time is reported.
 
 Between steps the inputs rotate over enough distinct sets that their total
 exceeds 3x the 129 MB L2, so no step finds its inputs in L2.
 
 The JSON line also carries the other rows of the hot path measured on their
-own (the standalone DPFP kernel, the decode step on its 512 MiB state, and
-the long nu = 3 forward), the roofline of the dominant kernel, an end-to-end
-number with host buffers, clocks sampled during the timed region, and the
-CPU oracle's throughput on the host cores.
+own (the B4 H8 L512 nu 1 forward, the same nu = 3 forward with B = 16, the
+standalone DPFP kernel, the decode step on its 512 MiB state, the sum rule,
+the projected forward, the backward and the token-wise layer stack), the
+roofline of the dominant kernel, an end-to-end number with host buffers,
+clocks sampled over the whole run, and the CPU oracle's throughput on the
+host cores (all threads, and one thread).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -34,7 +37,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "delta-rule fast-weight forward tokens/s (1 GB300) + % tensor/HBM roofline"
-WORKLOAD = "b4h8_l512"
+WORKLOAD = "b2h8_l2048_nu3"
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -239,22 +242,20 @@ def run_ours(args, rank, world, local_rank):
 
     def step(i):
         d = sets[i % nsets]
-        fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=None, nu=nu, chunk=C,
+        fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=d.get("W0"), nu=nu, chunk=C,
                             y=y, W_final=Wf, workspace=ws, stream=stream)
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    assert fw.fw_device_status() == fw.FW_OK
-
+    # nvidia-smi samples from the warm-up to the end of the end-to-end loop
     clocks = ClockSampler(local_rank)
     clocks.start()
     for i in range(args.warmup):
         step(i)
+    torch.cuda.synchronize()
+    assert fw.fw_device_status() == fw.FW_OK
     barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -264,7 +265,6 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    clk = clocks.stop()
     ms_total = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_step = ms_total / args.steps
     tokens_per_step = B * L
@@ -272,12 +272,13 @@ def run_ours(args, rank, world, local_rank):
 
     # ---------------------------------------------------------------- e2e
     # A serving loop through the public API: every step copies its inputs
-    # from pinned host memory (q, k, v, beta packed in one buffer: one copy),
-    # runs fw_delta_forward and reads y and W_final back (packed: one copy).
+    # from pinned host memory (q, k, v, beta and W0 packed in one buffer: one
+    # copy), runs fw_delta_forward and reads y and W_final back (packed: one
+    # copy).
     # Two slots: the input copy of step i + 1 runs on a copy stream while the
     # forward of step i computes, and the read-back of step i on a third
     # stream; each step's own copies stay inside the timed region.
-    names = ("q", "k", "v", "beta")
+    names = tuple(n for n in ("q", "k", "v", "beta", "W0") if host.get(n) is not None)
 
     def packed(shapes_dtypes):
         offs, tot = [], 0
@@ -322,10 +323,10 @@ def run_ours(args, rank, world, local_rank):
         comp.wait_event(ev_in[sl])
         if reuse:
             comp.wait_event(ev_out[sl])         # this slot's previous read-back is done
-        qd, kd, vd, bd = in_v[sl]
+        ins = dict(zip(names, in_v[sl]))
         yo, Wo = out_v[sl]
-        fw.fw_delta_forward(qd, kd, vd, bd, W0=None, nu=nu, chunk=C, y=yo, W_final=Wo, workspace=ws,
-                            stream=comp)
+        fw.fw_delta_forward(ins["q"], ins["k"], ins["v"], ins["beta"], W0=ins.get("W0"), nu=nu, chunk=C, y=yo,
+                            W_final=Wo, workspace=ws, stream=comp)
         ev_comp[sl].record(comp)
         s_d2h.wait_event(ev_comp[sl])
         with torch.cuda.stream(s_d2h):
@@ -352,7 +353,8 @@ def run_ours(args, rank, world, local_rank):
             e2e_step(i, cap, reuse=i >= 2)
         cap.wait_stream(s_h2d)
         cap.wait_stream(s_d2h)
-    e2e_steps = max(E2E_GRAPH, min(args.steps, 2000) // E2E_GRAPH * E2E_GRAPH)
+    # as many end-to-end steps as timed steps (rounded up to whole graphs)
+    e2e_steps = max(E2E_GRAPH, (args.steps + E2E_GRAPH - 1) // E2E_GRAPH * E2E_GRAPH)
     for _ in range(2):
         graph.replay()
     barrier()
@@ -364,6 +366,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    clk = clocks.stop()
     # the last step's results came back intact
     y_back = views(h_out[(E2E_GRAPH - 1) & 1], out_offs, out_sd)[0]
     assert torch.isfinite(y_back.float()).all()
@@ -372,28 +375,27 @@ def run_ours(args, rank, world, local_rank):
     # the two kernels of the forward, each timed on its own with CUDA events
     # on the launching stream (fw_delta_forward = prepare + scan)
     pk = peaks()
-    ms_prep, ms_scan = phase_ms(fw, sets, y, Wf, ws, nu, C, stream)
-    BHL = B * H * L
-    r_prep = roofline("chunk_prep_kernel", prep_flops_per_head_token(C, d_dot, d_v) * BHL,
-                      BHL * io_bytes * (2 * d_key + d_v + 1), ms_prep, pk)
-    r_scan = roofline("chunk_scan_kernel", scan_flops_per_head_token(d_dot, d_v) * BHL,
-                      BHL * io_bytes * d_v + B * H * d_v * d_dot * 4, ms_scan, pk)
-    r_fwd = roofline("fw_delta_forward (prepare + scan)", forward_flops_per_head_token(C, d_dot, d_v) * BHL,
-                     forward_bytes(B, H, L, d_key, d_v, d_dot, io_bytes), ms_step, pk)
-    roof = dict(r_prep if ms_prep >= ms_scan else r_scan)
-    roof["traffic"] = recorded_traffic(roof["kernel"], FORWARD_SOURCES)
+    has_w0 = host.get("W0") is not None
+    kern = forward_kernels(fw, sets, y, Wf, ws, B, H, L, d_key, nu, d_v, C, io_bytes, stream, pk, WORKLOAD)
+    r_fwd = roofline("fw_delta_forward (prepare + scan)", forward_flops_per_head_token(C, d_dot, d_v) * B * H * L,
+                     forward_bytes(B, H, L, d_key, d_v, d_dot, io_bytes, w0=has_w0), ms_step, pk)
+    r_prep, r_scan = kern["chunk_prep_kernel"], kern["chunk_scan_kernel"]
+    roof = dict(r_prep if r_prep["kernel_ms"] >= r_scan["kernel_ms"] else r_scan)
     launches_per_step = FORWARD_LAUNCHES
 
     rows = None
     if rank == 0 and not args.no_rows:
         rows = measure_rows(fw, inputs, dev, stream, pk)
+        for name in ROW_FORWARDS:
+            rows[name] = forward_row(fw, inputs, name, dev, stream, pk)
 
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: B{B} H{H} L{L} d_key{d_key} nu{nu} d_v{d_v} "
-                               f"bf16 I/O, fp32 state, chunk {C}, W0 = 0, y and W_final out",
+        "config": {"workload": f"{WORKLOAD}: B{B} H{H} L{L} d_key{d_key} nu{nu} (d_dot {d_dot}) d_v{d_v} "
+                               f"bf16 I/O, fp32 state, chunk {C}, "
+                               f"{'W0 ~ N(0, 0.01) in' if has_w0 else 'W0 = 0'}, y and W_final out",
                    "global_batch": B * world, "seq_len": L,
                    "parallelism": "replicas" if world == 1 else f"replicas x{world}",
                    "l2": f"inputs rotate over {nsets} sets ({nsets * set_bytes / 2**20:.0f} MiB "
@@ -401,7 +403,10 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": {"value": tokens_per_step * world / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "steps": e2e_steps},
+                "steps": e2e_steps,
+                "how": f"pinned host buffers; per step one packed copy in ({', '.join(names)}), the forward, one "
+                       f"packed copy out (y, W_final); two slots on three streams, {E2E_GRAPH} steps per "
+                       f"replayed CUDA graph"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roof,
         "kernels": {"chunk_prep_kernel": r_prep, "chunk_scan_kernel": r_scan, "forward": r_fwd},
@@ -411,11 +416,14 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
-# the forward's launches per call and the kernel the roofline is taken on
+# the forward's launches per call and the sources the recorded DRAM traffic was captured from
 FORWARD_LAUNCHES = 2
 FORWARD_SOURCES = ["delta_rule_linear_dpfp_gb300/csrc/fw_forward_tc.cu",
                    "delta_rule_linear_dpfp_gb300/csrc/fw_tc.cuh",
                    "delta_rule_linear_dpfp_gb300/csrc/fw_dpfp.cuh"]
+# forward workloads measured as rows beside the headline: the nu = 1 workload, and the headline's
+# shape with 8x the batch, where the serial chunk chain is not the only limit
+ROW_FORWARDS = ["b4h8_l512", "b16h8_l2048_nu3"]
 
 
 def phase_ms(fw, sets, y, Wf, ws, nu, C, stream, reps=200):
@@ -432,11 +440,56 @@ def phase_ms(fw, sets, y, Wf, ws, nu, C, stream, reps=200):
     ms_prep = e0.elapsed_time(e1) / reps
     e0.record(stream)
     for i in range(reps):
-        fw.fw_delta_forward_scan(ws, y, W0=None, W_final=Wf, nu=nu, chunk=C, stream=stream)
+        fw.fw_delta_forward_scan(ws, y, W0=sets[0].get("W0"), W_final=Wf, nu=nu, chunk=C, stream=stream)
     e1.record(stream)
     torch.cuda.synchronize()
     ms_scan = e0.elapsed_time(e1) / reps
     return ms_prep, ms_scan
+
+
+def forward_kernels(fw, sets, y, Wf, ws, B, H, L, d_key, nu, d_v, C, io_bytes, stream, pk, workload):
+    """Roofline entries of the forward's two kernels, each timed on its own."""
+    d_dot = 2 * d_key * nu
+    ms_prep, ms_scan = phase_ms(fw, sets, y, Wf, ws, nu, C, stream)
+    BHL = B * H * L
+    w0 = sets[0].get("W0") is not None
+    r_prep = roofline("chunk_prep_kernel", prep_flops_per_head_token(C, d_dot, d_v) * BHL,
+                      BHL * io_bytes * (2 * d_key + d_v + 1), ms_prep, pk)
+    r_scan = roofline("chunk_scan_kernel", scan_flops_per_head_token(d_dot, d_v) * BHL,
+                      BHL * io_bytes * d_v + B * H * d_v * d_dot * 4 * (1 + int(w0)), ms_scan, pk)
+    for r in (r_prep, r_scan):
+        r["traffic"] = recorded_traffic(f"{r['kernel']}@{workload}", FORWARD_SOURCES)
+    return {"chunk_prep_kernel": r_prep, "chunk_scan_kernel": r_scan}
+
+
+def forward_row(fw, inputs, name, dev, stream, pk, reps=50):
+    """A whole forward call on one of inputs.FORWARD_CONFIGS, with its two kernels."""
+    c = inputs.FORWARD_CONFIGS[name]
+    B, H, L, d_key, nu, d_v, C = (c[n] for n in ("B", "H", "L", "d_key", "nu", "d_v", "chunk"))
+    d_dot = 2 * d_key * nu
+    one = inputs.forward_inputs(name)
+    set_bytes = sum(t.numel() * t.element_size() for t in one.values() if t is not None)
+    nsets = max(2, min(16, math.ceil(3 * L2_BYTES / set_bytes)))
+    sets = [{k: (None if v is None else v.to(dev)) for k, v in (inputs.forward_inputs(name, seed=s) if s else one).items()}
+            for s in range(nsets)]
+    y = torch.empty(B, H, L, d_v, dtype=torch.bfloat16, device=dev)
+    Wf = torch.empty(B, H, d_v, d_dot, dtype=torch.float32, device=dev)
+    nws = fw.fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, C, torch.bfloat16)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+
+    def call(i):
+        d = sets[i % nsets]
+        fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=d.get("W0"), nu=nu, chunk=C, y=y, W_final=Wf,
+                            workspace=ws, stream=stream)
+    ms = _time(call, reps, stream)
+    w0 = sets[0].get("W0") is not None
+    r = roofline("fw_delta_forward (prepare + scan)", forward_flops_per_head_token(C, d_dot, d_v) * B * H * L,
+                 forward_bytes(B, H, L, d_key, d_v, d_dot, 2, w0=w0), ms, pk)
+    r["tokens/s"] = B * L / (ms * 1e-3)
+    r["kernels"] = forward_kernels(fw, sets, y, Wf, ws, B, H, L, d_key, nu, d_v, C, 2, stream, pk, name)
+    r["workload"] = (f"B{B} H{H} L{L} d_key{d_key} nu{nu} (d_dot {d_dot}) d_v{d_v} bf16, chunk {C}, "
+                     f"{'W0 in' if w0 else 'W0 = 0'}, y and W_final out, {nsets} rotating input sets")
+    return r
 
 
 def _time(fn, reps, stream):
@@ -495,24 +548,6 @@ def measure_rows(fw, inputs, dev, stream, pk):
     torch.cuda.synchronize()
     r["graph128_ms_per_step"] = e0.elapsed_time(e1) / (4 * 128)
     rows["decode_b256h16_nu2_dv128"] = r
-    # a1-a5 on the long nu = 3 workload with W0 in, W_final out
-    name = "b2h8_l2048_nu3"
-    c = inputs.FORWARD_CONFIGS[name]
-    d = {k: (None if v is None else v.to(dev)) for k, v in inputs.forward_inputs(name).items()}
-    B, H, L, d_key, nu, d_v, C = (c[n] for n in ("B", "H", "L", "d_key", "nu", "d_v", "chunk"))
-    d_dot = 2 * d_key * nu
-    y = torch.empty(B, H, L, d_v, dtype=torch.bfloat16, device=dev)
-    Wf = torch.empty(B, H, d_v, d_dot, dtype=torch.float32, device=dev)
-    nws = fw.fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, C, torch.bfloat16)
-    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
-    ms = _time(lambda i: fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=d["W0"], nu=nu,
-                                             chunk=C, y=y, W_final=Wf, workspace=ws, stream=stream),
-               50, stream)
-    flops = forward_flops_per_head_token(C, d_dot, d_v) * B * H * L
-    r = roofline("fw_delta_forward (prepare + scan)", flops,
-                 forward_bytes(B, H, L, d_key, d_v, d_dot, 2, w0=True), ms, pk)
-    r["tokens/s"] = B * L / (ms * 1e-3)
-    rows[name] = r
     # the sum rule (linear attention, z-normalised) on the bench workload's shapes
     B, H, L, d_key, nu, d_v, C = 4, 8, 512, 64, 1, 64, 64
     d_dot = 2 * d_key * nu
@@ -586,7 +621,7 @@ def measure_rows(fw, inputs, dev, stream, pk):
     wbytes = (d_model * sl[0]["W_in"].shape[1] + H * d_v * d_model + 2 * d_model * d_ff) * 2
     nbytes = nl * (2 * B * H * d_v * d_dot * 4 + wbytes) + 2 * B * d_model * 4
     flops = nl * (2.0 * B * (d_model * N + H * d_v * d_model + 2 * d_model * d_ff) + 6.0 * B * H * d_v * d_dot)
-    r = roofline("fw_decode_stack_step (6 layers, 37 kernels)", flops, nbytes, ms, pk)
+    r = roofline("fw_decode_stack_step (6 layers, 62 launches)", flops, nbytes, ms, pk)
     r["tokens/s"] = B / (ms * 1e-3)
     # the same token step captured once as a CUDA graph and replayed (8 tokens per timing)
     gs = torch.cuda.Stream()
@@ -681,17 +716,18 @@ class OracleSample:
         self.oracle.delta_forward(sl(f["q"]), sl(f["k"]), sl(f["v"]), sl(f["beta"]), None, self.nu,
                                   1e-6, threads)
 
-    def plan(self, budget_s):
-        pairs = int(max(1, min(self.B * self.H, budget_s * self.threads / self.t_pair)))
+    def plan(self, budget_s, threads):
+        pairs = int(max(1, min(self.B * self.H, budget_s * threads / self.t_pair)))
         tokens = self.L
         if pairs == 1 and budget_s < self.t_pair:
             tokens = int(max(1, self.L * budget_s / self.t_pair))
         return pairs, tokens
 
-    def measure(self, budget_s):
+    def measure(self, budget_s, max_threads=None):
         """Returns (tokens/s, threads used, sample description, seconds)."""
-        pairs, tokens = self.plan(budget_s)
-        threads = min(self.threads, pairs)
+        cap = self.threads if max_threads is None else min(self.threads, max_threads)
+        pairs, tokens = self.plan(budget_s, cap)
+        threads = min(cap, pairs)
         t0 = time.perf_counter()
         self._run(pairs, tokens, threads)
         dt = time.perf_counter() - t0
@@ -754,8 +790,11 @@ def main():
             orc = OracleSample(cfg["B"], cfg["H"], cfg["L"], cfg["d_key"], cfg["nu"], cfg["d_v"],
                                cfg["io"])
             v, cores, sample, _ = orc.measure(12.0)
+            v1, _, sample1, _ = orc.measure(6.0, max_threads=1)
             res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                   "sample": sample}
+                                   "sample": sample,
+                                   "single_thread": {"value": v1, "unit": "tokens/s", "cores": 1,
+                                                     "sample": sample1}}
         print(json.dumps(res), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -537,14 +537,17 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         if (tid == 0) {
             const uint32_t a = smem_u32(tp), bk = smem_u32(kq), bv = smem_u32(vt);
             const uint32_t idk = idesc_bf16(128, 128, 0, 1), idv = idesc_bf16(128, d_v, 0, 1);
+            // accumulator by accumulator: consecutive MMAs into one accumulator
+            // issue about 3x faster than MMAs that alternate between accumulators
+            for (int j = 0; j < Dp / 128; ++j)
     #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t ad = desc_sw128(a + (uint32_t)s * 32u, 16, 1024);
-                for (int j = 0; j < Dp / 128; ++j)
-                    mma_bf16(tm + (uint32_t)(128 * j), ad,
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tm + (uint32_t)(128 * j), desc_sw128(a + (uint32_t)s * 32u, 16, 1024),
                              desc_sw128(bk + (uint32_t)(2 * j) * 16384u + (uint32_t)s * 2048u, 16384, 1024), idk, s > 0);
-                mma_bf16(tm + (uint32_t)Dp, ad, desc_sw128(bv + (uint32_t)s * 2048u, 8192, 1024), idv, s > 0);
-            }
+    #pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tm + (uint32_t)Dp, desc_sw128(a + (uint32_t)s * 32u, 16, 1024),
+                         desc_sw128(bv + (uint32_t)s * 2048u, 8192, 1024), idv, s > 0);
             mma_commit(bar);
             bulk_wait_read(); // the K image has been read out of the key rows
         }

@@ -33,6 +33,9 @@ FORWARD_CONFIGS = {
     "b4h8_l512": dict(B=4, H=8, L=512, d_key=64, nu=1, d_v=64, chunk=64, io="bf16", w0_var=None),
     "b2h8_l2048_nu3": dict(B=2, H=8, L=2048, d_key=64, nu=3, d_v=64, chunk=64, io="bf16",
                            w0_var=0.01),
+    # the same shape with 8x the batch (128 independent (b,h) sequences)
+    "b16h8_l2048_nu3": dict(B=16, H=8, L=2048, d_key=64, nu=3, d_v=64, chunk=64, io="bf16",
+                            w0_var=0.01),
     "proj_d512": dict(B=1, H=8, L=1024, d_key=64, nu=1, d_v=64, chunk=64, io="bf16", w0_var=None,
                       d_model=512),
 }
