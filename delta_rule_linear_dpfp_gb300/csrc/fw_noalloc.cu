@@ -10,10 +10,15 @@
 //
 // The array is a file-scope __device__ variable: in host code its name is
 // only a stand-in, so its device address is looked up with
-// cudaGetSymbolAddress, once per device, the first time this entry point runs
-// with that device current.
+// cudaGetSymbolAddress with the device current.  The address belongs to the
+// context that loaded the library's device code, so it is cached per
+// (device, context) pair: a new context on the device (after
+// cudaDeviceReset, or a context the caller made current through the driver
+// API) is looked up afresh instead of reusing an address from a context that
+// no longer exists.
 #include "fastweight.h"
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <mutex>
 
@@ -24,8 +29,25 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void *g_scratch_ptr[kMaxDevices];
+CUcontext g_scratch_ctx[kMaxDevices];
 
-// Device address of the scratch array on the current device (looked up once).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+// The driver's cuCtxGetCurrent, reached through the runtime (the library
+// does not link the driver library itself).
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<CtxGetCurrentFn>(p);
+    }();
+    return fn;
+}
+
+// Device address of the scratch array in the current context.
 cudaError_t scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -33,13 +55,24 @@ cudaError_t scratch_address(void **out) {
         return e;
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
+    CtxGetCurrentFn get = ctx_get_current();
+    if (!get)
+        return cudaErrorDeviceUninitialized;
+    CUcontext ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS)
+        return cudaErrorDeviceUninitialized;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!ctx || !g_scratch_ptr[dev] || g_scratch_ctx[dev] != ctx) {
+        // (with no context current yet, the lookup itself sets up the
+        // device's primary context, which is then the one recorded)
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_fw_noalloc_scratch);
         if (e != cudaSuccess)
             return e;
+        if (!ctx && (get(&ctx) != CUDA_SUCCESS || !ctx))
+            return cudaErrorDeviceUninitialized;
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
     return cudaSuccess;
