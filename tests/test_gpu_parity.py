@@ -9,7 +9,7 @@ import torch
 import oracle
 from delta_rule_linear_dpfp_gb300 import binding as fw
 from delta_rule_linear_dpfp_gb300 import build, inputs
-from tests.parity_util import f64, maxrel, to_dev, tol_for
+from tests.parity_util import check, f64, maxrel, to_dev, tol_for
 
 pytestmark = pytest.mark.gpu
 
@@ -87,9 +87,8 @@ def test_forward_configs(name):
     tol = tol_for(inputs.torch_dtype(cfg["io"]))
     assert Wf.dtype == torch.float32 and tuple(Wf.shape) == W_ref.shape
     assert Wf.is_contiguous() and Wf.stride() == torch.empty(W_ref.shape).stride()
-    ey, ew = maxrel(f64(y), y_ref), maxrel(f64(Wf), W_ref)
-    print(f"{name}: y maxrel {ey:.3e}  W_final maxrel {ew:.3e}")
-    assert ey <= tol and ew <= tol
+    check(f"{name} y", f64(y), y_ref, tol)
+    check(f"{name} W_final", f64(Wf), W_ref, tol)
 
 
 EDGE = [
@@ -116,8 +115,8 @@ def test_forward_edge_shapes(case):
     d = inputs.random_forward_inputs(B, H, L, d_key, nu, d_v, io, 0.01 if w0 else None, seed=L)
     y, Wf, y_ref, W_ref = _forward_case(d, nu, chunk)
     tol = tol_for(inputs.torch_dtype(io))
-    assert maxrel(f64(y), y_ref) <= tol
-    assert maxrel(f64(Wf), W_ref) <= tol
+    check("y", f64(y), y_ref, tol)
+    check("W_final", f64(Wf), W_ref, tol)
 
 
 def test_forward_zero_keys_and_beta_zero():
@@ -220,8 +219,8 @@ def test_decode_small_stepped():
                                     d["beta"][t].cuda(), W, nu=nu)
         y_ref, Wr = oracle.delta_decode_step(f64(d["q"][t]), f64(d["k"][t]), f64(d["v"][t]),
                                              f64(d["beta"][t]), Wr, nu, 1e-6, NT)
-        assert maxrel(f64(y), y_ref) <= 2e-2
-    assert maxrel(f64(W), Wr) <= 2e-2
+        check(f"y[{t}]", f64(y), y_ref, 2e-2)
+    check("W", f64(W), Wr, 2e-2)
 
 
 def test_decode_largest_state_row():
@@ -234,8 +233,8 @@ def test_decode_largest_state_row():
                                     d["beta"][t].cuda(), W, nu=4)
         y_ref, Wr = oracle.delta_decode_step(f64(d["q"][t]), f64(d["k"][t]), f64(d["v"][t]),
                                              f64(d["beta"][t]), Wr, 4, 1e-6, NT)
-        assert maxrel(f64(y), y_ref) <= 2e-2
-    assert maxrel(f64(W), Wr) <= 2e-2
+        check(f"y[{t}]", f64(y), y_ref, 2e-2)
+    check("W", f64(W), Wr, 2e-2)
 
 
 def test_decode_f32():
@@ -247,8 +246,8 @@ def test_decode_f32():
                                     d["beta"][t].cuda(), W, nu=3)
         y_ref, Wr = oracle.delta_decode_step(f64(d["q"][t]), f64(d["k"][t]), f64(d["v"][t]),
                                              f64(d["beta"][t]), Wr, 3, 1e-6, NT)
-        assert maxrel(f64(y), y_ref) <= 1e-4
-    assert maxrel(f64(W), Wr) <= 1e-4
+        check(f"y[{t}]", f64(y), y_ref, 1e-4)
+    check("W", f64(W), Wr, 1e-4)
 
 
 def test_decode_full_size_sampled():
@@ -272,8 +271,8 @@ def test_decode_full_size_sampled():
         for t in range(steps):
             y_ref, Wr = oracle.delta_decode_step(sel(d["q"])[t], sel(d["k"])[t], sel(d["v"])[t],
                                                  sel(d["beta"])[t], Wr, nu, 1e-6)
-            assert maxrel(f64(ys[t][b:b + 1, h:h + 1]), y_ref) <= 2e-2, (b, h, t)
-        assert maxrel(f64(W[b:b + 1, h:h + 1]), Wr) <= 2e-2, (b, h)
+            check(f"y[{b},{h},{t}]", f64(ys[t][b:b + 1, h:h + 1]), y_ref, 2e-2)
+        check(f"W[{b},{h}]", f64(W[b:b + 1, h:h + 1]), Wr, 2e-2)
 
 
 def test_decode_stepped_equals_forward():
