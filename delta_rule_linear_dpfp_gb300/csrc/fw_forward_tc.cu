@@ -39,6 +39,14 @@
 //      S^T -> bf16 operand tile for the next MMA1
 //    The [W'; Q'] image of chunk c+1 is bulk-copied in as soon as MMA1 has
 //    read chunk c's; K images are double-buffered, two chunks ahead.
+//    The serial walk is bound by how fast MMAs issue: one thread issues a
+//    tcgen05.mma about every 80 SM cycles whatever N (up to 128), while two
+//    or more warps issuing at once reach about 44 cycles each in aggregate.
+//    So MMA1 is issued by two threads (warps 0 and 1), each over half of the
+//    contraction into its own accumulator (the read-out adds the two), and
+//    MMA3 by one thread per 128-row block of S^T (warp mb).  Every
+//    accumulator is written by one thread only, so no two threads' MMAs
+//    ever need ordering against each other.
 //
 // Partial chunks are padded to 64 token rows with zero phi rows and
 // beta = 0, which makes the padded rows of T, P, W', Q', U' and Y' zero.
@@ -647,8 +655,9 @@ __global__ void __launch_bounds__(kScanThreads)
     uint8_t *ut = st + VB * sblk;                     // U: rows t, columns v (MN-major)
     uint64_t *bar_a = (uint64_t *)(ut + VB * 8192);  // [2]
     uint64_t *bar_k = bar_a + 2;                      // [2]
-    uint64_t *bar_mma = bar_a + 4;
-    uint32_t *slot = (uint32_t *)(bar_a + 5);
+    uint64_t *bar_m1 = bar_a + 4;                     // MMA1 done (both issuers)
+    uint64_t *bar_m3 = bar_a + 5;                     // MMA3 done (every block's issuer)
+    uint32_t *slot = (uint32_t *)(bar_a + 6);
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int v0 = blockIdx.x * (ZN ? 16 : DVB);
@@ -656,7 +665,7 @@ __global__ void __launch_bounds__(kScanThreads)
     // record channel of the CTA's column j (column groups of 4 stay contiguous)
     auto chan = [&](int j) { return (ZN && j >= 16) ? d_vr + (j - 16) : v0 + j; };
     const int MB = Dp / 128;
-    const uint32_t ncols = tmem_cols_pow2((1 + MB) * DS);
+    const uint32_t ncols = tmem_cols_pow2((2 + MB) * DS);
     const uint8_t *rec0 = ws + (size_t)bh * nch * rc.bytes;
     const bool has_w0 = W0 != nullptr || (ZN && z0 != nullptr);
     const uint32_t lb = tmem_lane_base(warp);
@@ -666,7 +675,8 @@ __global__ void __launch_bounds__(kScanThreads)
         mbar_init(bar_a + 1, 1);
         mbar_init(bar_k, 1);
         mbar_init(bar_k + 1, 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(bar_m1, 2);
+        mbar_init(bar_m3, (uint32_t)MB);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -677,7 +687,9 @@ __global__ void __launch_bounds__(kScanThreads)
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *slot;
-    const uint32_t tD1 = tm, tS = tm + DS;
+    // D1 as two partial sums (contraction halves), then the MB blocks of S^T
+    const uint32_t tD1 = tm, tD1b = tm + DS, tS = tm + 2 * DS;
+    const bool lead = (tid & 31) == 0;
     const uint32_t st_s = smem_u32(st), ut_s = smem_u32(ut);
     const uint32_t kt0_s = smem_u32(kt0), kt1_s = smem_u32(kt1);
 
@@ -760,7 +772,7 @@ __global__ void __launch_bounds__(kScanThreads)
         }
     };
     load_pre(0);
-    uint32_t mma_phase = 0;
+    uint32_t m1_phase = 0, m3_phase = 0;
     for (int c = 0; c < nch; ++c) {
         const int t0 = c * C, Lc = min(C, L - t0), kb = NKB == 2 ? (c & 1) : 0, ab = NA == 2 ? (c & 1) : 0;
         const uint32_t a_parity = NA == 2 ? (uint32_t)((c >> 1) & 1) : (uint32_t)(c & 1);
@@ -773,17 +785,19 @@ __global__ void __launch_bounds__(kScanThreads)
             break;
         }
 
-        // MMA1: D1 = [W'; Q'] S^T
-        if (tid == 0) {
+        // MMA1: D1 = [W'; Q'] S^T, warp 0 over the first half of the
+        // contraction into tD1, warp 1 over the second into tD1b
+        if (lead && warp < 2) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(128, DVB, 0, 1);
-            for (int s = 0; s < Dp / 16; ++s)
-                mma_bf16(tD1, desc_sw128(smem_u32(ab ? at1 : at0) + kmajor_step(s, 128), 16, 1024),
-                         desc_sw128(st_s + (uint32_t)s * 2048u, sblk, 1024), idesc, s > 0);
-            mma_commit(bar_mma);
+            const int s0 = warp * (Dp / 32);
+            for (int s = s0; s < s0 + Dp / 32; ++s)
+                mma_bf16(warp ? tD1b : tD1, desc_sw128(smem_u32(ab ? at1 : at0) + kmajor_step(s, 128), 16, 1024),
+                         desc_sw128(st_s + (uint32_t)s * 2048u, sblk, 1024), idesc, s > s0);
+            mma_commit(bar_m1);
         }
-        ok = mbar_wait(bar_mma, mma_phase, status);
-        mma_phase ^= 1;
+        ok = mbar_wait(bar_m1, m1_phase, status);
+        m1_phase ^= 1;
         if (__syncthreads_or(!ok)) {
             drain(c, 1);
             break;
@@ -794,11 +808,16 @@ __global__ void __launch_bounds__(kScanThreads)
             bulk_g2s(ab ? at1 : at0, rec + (size_t)NA * rc.bytes + rc.a, a_bytes, bar_a + ab);
         }
         {
-            float d1[DVB];
+            float d1[DVB], d1b[DVB];
 #pragma unroll
-            for (int j0 = 0; j0 < DVB; j0 += 16) // every load in flight, then one wait
+            for (int j0 = 0; j0 < DVB; j0 += 16) { // every load in flight, then one wait
                 tmem_ld16(tD1 + lb + (uint32_t)j0, d1 + j0);
+                tmem_ld16(tD1b + lb + (uint32_t)j0, d1b + j0);
+            }
             tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < DVB; ++j)
+                d1[j] += d1b[j];
             if (tid < 64) {                           // U = U' - W' S^T
 #pragma unroll
                 for (int j0 = 0; j0 < DVB; j0 += 16) {
@@ -835,22 +854,23 @@ __global__ void __launch_bounds__(kScanThreads)
             break;
         }
 
-        // MMA3: S^T += K^T U   (K^T: the K image read MN-major)
-        if (tid == 0) {
+        // MMA3: S^T += K^T U   (K^T: the K image read MN-major); block mb of
+        // S^T by warp mb
+        if (lead && warp < MB) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(128, DVB, 1, 1);
             const uint32_t kbase = kb ? kt1_s : kt0_s;
-            for (int mb = 0; mb < MB; ++mb)
+            const int mb = warp;
 #pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_bf16(tS + (uint32_t)(mb * DS),
-                             desc_sw128(kbase + (uint32_t)(2 * mb) * 8192u + (uint32_t)s * 2048u, 8192, 1024),
-                             desc_sw128(ut_s + (uint32_t)s * 2048u, 8192, 1024), idesc,
-                             (s > 0 || c > 0 || has_w0) ? 1u : 0u);
-            mma_commit(bar_mma);
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tS + (uint32_t)(mb * DS),
+                         desc_sw128(kbase + (uint32_t)(2 * mb) * 8192u + (uint32_t)s * 2048u, 8192, 1024),
+                         desc_sw128(ut_s + (uint32_t)s * 2048u, 8192, 1024), idesc,
+                         (s > 0 || c > 0 || has_w0) ? 1u : 0u);
+            mma_commit(bar_m3);
         }
-        ok = mbar_wait(bar_mma, mma_phase, status);
-        mma_phase ^= 1;
+        ok = mbar_wait(bar_m3, m3_phase, status);
+        m3_phase ^= 1;
         if (__syncthreads_or(!ok)) {
             drain(c, 3);
             break;
