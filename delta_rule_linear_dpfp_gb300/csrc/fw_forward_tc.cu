@@ -286,8 +286,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     float *Rm = Nm + 64 * LDS;                           // block-solve scratch [16][LDS]
     float *bs = Rm + 16 * LDS;                           // beta (0 on padded rows)
     uint8_t *vt = (uint8_t *)Am;                         // V (MN-major B), once A and N are done
-    uint64_t *bar = (uint64_t *)(bs + 64);
-    uint32_t *slot = (uint32_t *)(bar + 1);
+    // MMA completion: the Gram matrix (2 issuers), [I; P] T (2 issuers; the
+    // sum rule's [I; P] V' by 1), the final product (one issuer per accumulator)
+    uint64_t *bar_g = (uint64_t *)(bs + 64);
+    uint64_t *bar_i = bar_g + 1;
+    uint64_t *bar_f = bar_g + 2;
+    uint32_t *slot = (uint32_t *)(bar_g + 3);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sp = warp & 3, half = warp >> 2;           // TMEM sub-partition, column half
@@ -360,7 +364,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         beta_t = __bfloat162float(beta[bh * L + t0 + tid]);
 
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(bar_g, 2);
+        mbar_init(bar_i, SUM ? 1 : 2);
+        mbar_init(bar_f, (uint32_t)(Dp / 128 + 1));
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -404,32 +410,45 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     tc_fence_after();
     const uint32_t tm = *slot;
     const uint32_t lb = tmem_lane_base(warp);
+    // MMAs are issued by lane 0 of several warps at once (one thread issues a
+    // tcgen05.mma about every 80 SM cycles; several warps together reach
+    // about 44 each), every accumulator by one thread only
+    const bool lead = lane == 0;
 
-    // MMA: [K; Q] K^T  (B = the first 64 rows of the same tile).  The key
-    // rows of the tile are final here and go out as the record's K image
-    // (bulk copies of the 64-row halves of each 64-column block) while the
-    // rest of the chunk is worked out.
+    // MMA: [K; Q] K^T  (B = the first 64 rows of the same tile), warp 0 over
+    // the first half of the contraction into columns 0..63, warp 1 over the
+    // second into 64..127.  The key rows of the tile are final here and go
+    // out as the record's K image (bulk copies of the 64-row halves of each
+    // 64-column block) while the rest of the chunk is worked out.
     if (tid == 0) {
         for (int kb = 0; kb < Dp / 64; ++kb)
             bulk_s2g(rec + rc.k + (size_t)kb * 8192, kq + (size_t)kb * 16384, 8192);
         bulk_commit();
+    }
+    if (lead && warp < 2) {
         const uint32_t idesc = idesc_bf16(128, 64, 0, 0);
         const uint32_t base = smem_u32(kq);
-        for (int s = 0; s < Dp / 16; ++s) {
+        const int s0 = warp * (Dp / 32);
+        for (int s = s0; s < s0 + Dp / 32; ++s) {
             const uint64_t d = desc_sw128(base + kmajor_step(s, 128), 16, 1024);
-            mma_bf16(tm, d, d, idesc, s > 0);
+            mma_bf16(tm + (uint32_t)(64 * warp), d, d, idesc, s > s0);
         }
-        mma_commit(bar);
+        mma_commit(bar_g);
     }
-    bool ok = mbar_wait(bar, 0, status);
+    bool ok = mbar_wait(bar_g, 0, status);
     tc_fence_after();
     if (__syncthreads_or(!ok))
         goto teardown;
     {   // A (keys) and P (queries); [I; P] operand tile
-        float gr[32];
+        float gr[32], g2[32];
         tmem_ld16(tm + lb + (uint32_t)(32 * half), gr);
         tmem_ld16(tm + lb + (uint32_t)(32 * half + 16), gr + 16);
+        tmem_ld16(tm + lb + (uint32_t)(64 + 32 * half), g2);
+        tmem_ld16(tm + lb + (uint32_t)(64 + 32 * half + 16), g2 + 16);
         tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            gr[j] += g2[j];
         if (SUM && row < 64) { // the I row only (no triangular solve)
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -486,10 +505,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tm + (uint32_t)Dp, desc_sw128(a + (uint32_t)s * 32u, 16, 1024),
                          desc_sw128(bv + (uint32_t)s * 2048u, 8192, 1024), idv, s > 0);
-            mma_commit(bar);
+            mma_commit(bar_i);
             bulk_wait_read(); // the K image has been read out of the key rows
         }
-        ok = mbar_wait(bar, 1, status);
+        ok = mbar_wait(bar_i, 0, status);
         tc_fence_after();
         if (__syncthreads_or(!ok))
             goto teardown;
@@ -513,25 +532,31 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         __syncthreads();
         tc_fence_after();
 
-        // MMA: [I; P] T = [T; P T]
-        if (tid == 0) {
+        // MMA: [I; P] T = [T; P T], contraction halves by warps 0 and 1 into
+        // columns 0..63 and 64..127
+        if (lead && warp < 2) {
             const uint32_t idesc = idesc_bf16(128, 64, 0, 1);
             const uint32_t a = smem_u32(ip), b = smem_u32(tt);
     #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tm, desc_sw128(a + (uint32_t)s * 32u, 16, 1024), desc_sw128(b + (uint32_t)s * 2048u, 8192, 1024),
-                         idesc, s > 0);
-            mma_commit(bar);
+            for (int s = 2 * warp; s < 2 * warp + 2; ++s)
+                mma_bf16(tm + (uint32_t)(64 * warp), desc_sw128(a + (uint32_t)s * 32u, 16, 1024),
+                         desc_sw128(b + (uint32_t)s * 2048u, 8192, 1024), idesc, s > 2 * warp);
+            mma_commit(bar_i);
         }
-        ok = mbar_wait(bar, 1, status);
+        ok = mbar_wait(bar_i, 0, status);
         tc_fence_after();
         if (__syncthreads_or(!ok))
             goto teardown;
         {
-            float tr[32];
+            float tr[32], t2[32];
             tmem_ld16(tm + lb + (uint32_t)(32 * half), tr);
             tmem_ld16(tm + lb + (uint32_t)(32 * half + 16), tr + 16);
+            tmem_ld16(tm + lb + (uint32_t)(64 + 32 * half), t2);
+            tmem_ld16(tm + lb + (uint32_t)(64 + 32 * half + 16), t2 + 16);
             tmem_ld_wait();
+    #pragma unroll
+            for (int j = 0; j < 32; ++j)
+                tr[j] += t2[j];
     #pragma unroll
             for (int cc = 0; cc < 4; ++cc)
                 *reinterpret_cast<uint4 *>(tp + kmajor_chunk(row, 32 * half + 8 * cc, 128)) = pack8(tr + 8 * cc);
@@ -541,25 +566,30 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         __syncthreads();
         tc_fence_after();
 
-        // MMA: [T; P T] [K | V] = [W', P W' | U', P U']  (columns 0..Dp-1 | Dp..Dp+d_v-1)
-        if (tid == 0) {
+        // MMA: [T; P T] [K | V] = [W', P W' | U', P U']  (columns 0..Dp-1 |
+        // Dp..Dp+d_v-1): warp j issues the 128 columns of block j, warp Dp/128
+        // the V columns
+        if (lead && warp <= Dp / 128) {
             const uint32_t a = smem_u32(tp), bk = smem_u32(kq), bv = smem_u32(vt);
             const uint32_t idk = idesc_bf16(128, 128, 0, 1), idv = idesc_bf16(128, d_v, 0, 1);
-            // accumulator by accumulator: consecutive MMAs into one accumulator
-            // issue about 3x faster than MMAs that alternate between accumulators
-            for (int j = 0; j < Dp / 128; ++j)
+            const int j = warp;
+            if (j < Dp / 128) {
     #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     mma_bf16(tm + (uint32_t)(128 * j), desc_sw128(a + (uint32_t)s * 32u, 16, 1024),
-                             desc_sw128(bk + (uint32_t)(2 * j) * 16384u + (uint32_t)s * 2048u, 16384, 1024), idk, s > 0);
+                             desc_sw128(bk + (uint32_t)(2 * j) * 16384u + (uint32_t)s * 2048u, 16384, 1024), idk,
+                             s > 0);
+            } else {
     #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tm + (uint32_t)Dp, desc_sw128(a + (uint32_t)s * 32u, 16, 1024),
-                         desc_sw128(bv + (uint32_t)s * 2048u, 8192, 1024), idv, s > 0);
-            mma_commit(bar);
-            bulk_wait_read(); // the K image has been read out of the key rows
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tm + (uint32_t)Dp, desc_sw128(a + (uint32_t)s * 32u, 16, 1024),
+                             desc_sw128(bv + (uint32_t)s * 2048u, 8192, 1024), idv, s > 0);
+            }
+            mma_commit(bar_f);
         }
-        ok = mbar_wait(bar, 0, status);
+        if (tid == 0)
+            bulk_wait_read(); // the K image has been read out of the key rows
+        ok = mbar_wait(bar_f, 0, status);
         tc_fence_after();
         if (__syncthreads_or(!ok))
             goto teardown;
@@ -918,7 +948,7 @@ __global__ void __launch_bounds__(kScanThreads)
 size_t prep_smem(int Dp, int d_v) {
     const int VB = (d_v + 63) / 64;
     (void)VB; // the V tile (<= 16 KB) reuses the fp32 work space (37 KB)
-    return (size_t)256 * Dp + 16384 + 8192 + (2 * 64 + 16) * LDS * 4 + 64 * 4 + 16 + 1024;
+    return (size_t)256 * Dp + 16384 + 8192 + (2 * 64 + 16) * LDS * 4 + 64 * 4 + 32 + 1024;
 }
 
 size_t scan_smem(int Dp, int dvb, int nkb, int na) {
