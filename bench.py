@@ -3,7 +3,9 @@
 One step = one fw_delta_forward call (DPFP of q and k fused, the chunked
 delta rule, y and the final state written) over the B2 H8 L2048 d_key 64
 nu 3 (d_dot 384) d_v 64 bf16 workload (chunk 64), with a non-zero initial
-state W0 read and W_final written, inputs resident in HBM.  Every rank runs
+state W0 read and W_final written, inputs resident in HBM.  On this workload
+the call is one cooperative launch (chunk_fused_kernel) in which the walk
+over the chunks overlaps the preparation of the later chunks.  Every rank runs
 its own replica of that workload (weak scaling, no data-path collective); the
 timing is bracketed by a barrier and a device synchronisation on both sides
 and the slowest rank's time is reported.
@@ -122,41 +124,46 @@ def alu_roofline(name, flops, ms):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    """nvidia-smi clock / throttle-reason samples while the timed region runs.
+
+    One `nvidia-smi --query-gpu` call every `period` seconds from a thread:
+    nvidia-smi's own loop mode buffers its output when writing to a pipe, so
+    its samples only arrive when it exits (and are lost when it is stopped)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index):
+    def __init__(self, device_index, period=0.2):
         self.dev = device_index
-        self.proc = None
+        self.period = period
         self.lines = []
+        self.failed = False
+        self._stop = threading.Event()
+        self._t = None
+
+    def _query(self):
+        r = subprocess.run(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                            "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10)
+        return r.stdout.strip().splitlines() if r.returncode == 0 else []
+
+    def _loop(self):
+        while not self._stop.is_set():
+            try:
+                self.lines.extend(self._query())
+            except (OSError, subprocess.SubprocessError):
+                self.failed = True
+                return
+            self._stop.wait(self.period)
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self._t = threading.Thread(target=self._read, daemon=True)
-            self._t.start()
-        except OSError:
-            self.proc = None
-
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+        self._t = threading.Thread(target=self._loop, daemon=True)
+        self._t.start()
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self._t.join(timeout=2)
+        self._stop.set()
+        if self._t is not None:
+            self._t.join(timeout=15)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
@@ -171,9 +178,10 @@ class ClockSampler:
             for name, val in zip(names, parts[4:8]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
 
 
 def source_hash(paths):
@@ -372,16 +380,28 @@ def run_ours(args, rank, world, local_rank):
     assert torch.isfinite(y_back.float()).all()
 
     # ----------------------------------------------------------- roofline
-    # the two kernels of the forward, each timed on its own with CUDA events
-    # on the launching stream (fw_delta_forward = prepare + scan)
+    # fw_delta_forward runs either as one launch (chunk_fused_kernel: the
+    # preparation and the walk overlapped) or as its two kernels; the two
+    # kernels are also timed on their own (CUDA events on the launching
+    # stream) to show the phases
     pk = peaks()
     has_w0 = host.get("W0") is not None
+    launches_per_step = fw.fw_delta_forward_kernel_count(B, H, L, d_key, nu, d_v, C, torch.bfloat16)
+    assert launches_per_step in (1, 2), launches_per_step
     kern = forward_kernels(fw, sets, y, Wf, ws, B, H, L, d_key, nu, d_v, C, io_bytes, stream, pk, WORKLOAD)
-    r_fwd = roofline("fw_delta_forward (prepare + scan)", forward_flops_per_head_token(C, d_dot, d_v) * B * H * L,
+    fwd_name = "fw_delta_forward (one launch)" if launches_per_step == 1 else "fw_delta_forward (prepare + scan)"
+    r_fwd = roofline(fwd_name, forward_flops_per_head_token(C, d_dot, d_v) * B * H * L,
                      forward_bytes(B, H, L, d_key, d_v, d_dot, io_bytes, w0=has_w0), ms_step, pk)
     r_prep, r_scan = kern["chunk_prep_kernel"], kern["chunk_scan_kernel"]
-    roof = dict(r_prep if r_prep["kernel_ms"] >= r_scan["kernel_ms"] else r_scan)
-    launches_per_step = FORWARD_LAUNCHES
+    if launches_per_step == 1:
+        roof = dict(r_fwd, kernel="chunk_fused_kernel",
+                    note="kernel_ms is the whole call: the one kernel plus the memset of its ready flags")
+        roof["traffic"] = recorded_traffic(f"chunk_fused_kernel@{WORKLOAD}", FORWARD_SOURCES)
+        kernels = {"chunk_fused_kernel": roof, "chunk_prep_kernel (two-kernel path, alone)": r_prep,
+                   "chunk_scan_kernel (two-kernel path, alone)": r_scan, "forward": r_fwd}
+    else:
+        roof = dict(r_prep if r_prep["kernel_ms"] >= r_scan["kernel_ms"] else r_scan)
+        kernels = {"chunk_prep_kernel": r_prep, "chunk_scan_kernel": r_scan, "forward": r_fwd}
 
     rows = None
     if rank == 0 and not args.no_rows:
@@ -409,15 +429,14 @@ def run_ours(args, rank, world, local_rank):
                        f"replayed CUDA graph"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roof,
-        "kernels": {"chunk_prep_kernel": r_prep, "chunk_scan_kernel": r_scan, "forward": r_fwd},
+        "kernels": kernels,
     }
     if rows is not None:
         result["rows"] = rows
     return result
 
 
-# the forward's launches per call and the sources the recorded DRAM traffic was captured from
-FORWARD_LAUNCHES = 2
+# the sources the recorded DRAM traffic of the forward's kernels was captured from
 FORWARD_SOURCES = ["delta_rule_linear_dpfp_gb300/csrc/fw_forward_tc.cu",
                    "delta_rule_linear_dpfp_gb300/csrc/fw_tc.cuh",
                    "delta_rule_linear_dpfp_gb300/csrc/fw_dpfp.cuh"]
@@ -483,8 +502,11 @@ def forward_row(fw, inputs, name, dev, stream, pk, reps=50):
                             workspace=ws, stream=stream)
     ms = _time(call, reps, stream)
     w0 = sets[0].get("W0") is not None
-    r = roofline("fw_delta_forward (prepare + scan)", forward_flops_per_head_token(C, d_dot, d_v) * B * H * L,
+    launches = fw.fw_delta_forward_kernel_count(B, H, L, d_key, nu, d_v, C, torch.bfloat16)
+    r = roofline("fw_delta_forward (one launch)" if launches == 1 else "fw_delta_forward (prepare + scan)",
+                 forward_flops_per_head_token(C, d_dot, d_v) * B * H * L,
                  forward_bytes(B, H, L, d_key, d_v, d_dot, 2, w0=w0), ms, pk)
+    r["launches"] = launches
     r["tokens/s"] = B * L / (ms * 1e-3)
     r["kernels"] = forward_kernels(fw, sets, y, Wf, ws, B, H, L, d_key, nu, d_v, C, 2, stream, pk, name)
     r["workload"] = (f"B{B} H{H} L{L} d_key{d_key} nu{nu} (d_dot {d_dot}) d_v{d_v} bf16, chunk {C}, "

@@ -24,6 +24,7 @@ FW_DTYPE_BF16 = 1
 
 #: every entry point include/*.h declares
 EXPORTS = ("fw_status_string", "fw_dpfp", "fw_delta_forward_workspace_size", "fw_delta_forward",
+           "fw_delta_forward_kernel_count",
            "fw_delta_decode_step", "fw_device_status", "fw_selftest_umma",
            "fw_delta_forward_noalloc", "fw_delta_forward_prepare", "fw_delta_forward_scan",
            "fw_selftest_wait_timeout", "fw_linear_forward_workspace_size", "fw_linear_forward",
@@ -74,6 +75,8 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.fw_delta_forward_workspace_size.argtypes = [i32] * 8
     lib.fw_delta_forward.restype = i32
     lib.fw_delta_forward.argtypes = [vp] * 8 + [sz] + [i32] * 8 + [f32, vp]
+    lib.fw_delta_forward_kernel_count.restype = i32
+    lib.fw_delta_forward_kernel_count.argtypes = [i32] * 8
     lib.fw_delta_decode_step.restype = i32
     lib.fw_delta_decode_step.argtypes = [vp] * 6 + [i32] * 6 + [f32, vp]
     lib.fw_device_status.restype = i32
@@ -160,6 +163,14 @@ def fw_dpfp(x, nu: int = 1, eps: float = 1e-6, out_dtype=None, out=None, stream=
 def fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk, io_dtype) -> int:
     code = io_dtype if isinstance(io_dtype, int) else _dtype_code(io_dtype)
     return int(load().fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, chunk, code))
+
+
+def fw_delta_forward_kernel_count(B, H, L, d_key, nu, d_v, chunk, io_dtype) -> int:
+    """Kernels fw_delta_forward enqueues for this shape on the current device:
+    1 (one cooperative launch) or 2 (prep, then scan) with bf16 I/O; -1 if
+    the shape is rejected."""
+    code = io_dtype if isinstance(io_dtype, int) else _dtype_code(io_dtype)
+    return int(load().fw_delta_forward_kernel_count(B, H, L, d_key, nu, d_v, chunk, code))
 
 
 def fw_delta_forward(q, k, v, beta, W0=None, nu: int = 1, chunk: int = 64, eps: float = 1e-6,

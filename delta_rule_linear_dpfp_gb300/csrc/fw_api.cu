@@ -144,6 +144,20 @@ FW_API size_t fw_delta_forward_workspace_size(int B, int H, int L, int d_key, in
     return fw::tc_forward_workspace_bytes(B, H, L, d_key, nu, d_v, chunk);
 }
 
+FW_API int fw_delta_forward_kernel_count(int B, int H, int L, int d_key, int nu, int d_v, int chunk,
+                                         int io_dtype) {
+    if (check_forward_shape(B, H, L, d_key, nu, d_v, chunk, io_dtype) != FW_OK)
+        return -1;
+    if ((int64_t)B * H == 0 || L == 0)
+        return 0;
+    if (io_dtype == FW_DTYPE_F32)
+        return 1;
+    DeviceInfo di;
+    if (device_info(&di) != cudaSuccess)
+        return -1;
+    return fw::tc_forward_kernel_count(B, H, L, d_key, nu, d_v, chunk, di.num_sms);
+}
+
 FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const void *beta,
                             const float *W0, float *W_final, void *y, void *workspace,
                             size_t workspace_bytes, int B, int H, int L, int d_key, int nu,

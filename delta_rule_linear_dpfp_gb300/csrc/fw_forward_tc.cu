@@ -50,6 +50,8 @@
 //
 // Partial chunks are padded to 64 token rows with zero phi rows and
 // beta = 0, which makes the padded rows of T, P, W', Q', U' and Y' zero.
+#include <algorithm>
+
 #include "fw_dpfp.cuh"
 #include "fw_forward_tc.h"
 #include "fw_tc.cuh"
@@ -61,7 +63,6 @@ using namespace tc;
 
 constexpr int kTile = 64;          // token rows of a chunk tile (chunk <= 64, padded)
 constexpr int kPrepThreads = 256;
-constexpr int kScanThreads = 128;
 constexpr int LDS = 68;            // fp32 row stride of the 64 x 64 work matrices (16-byte rows)
 constexpr int kMaxDp = 384;        // padded d_dot the scan's shared memory holds
 
@@ -106,7 +107,7 @@ FW_DEV void unpack8(uint4 u, float *v) {
     }
 }
 
-FW_DEV uint32_t tmem_cols_pow2(int need) {
+__host__ __device__ inline uint32_t tmem_cols_pow2(int need) {
     return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
 }
 
@@ -268,111 +269,148 @@ FW_DEV void dpfp_half_row(const uint4 (&raw)[DK / 8], int hs, int r, int nu, flo
 // when d_v > d_vr, by a 16-channel block whose first channel is 1 on every
 // token (its running sum is z, its output the denominator z . phi(q)).  The
 // scan is the same for both rules.
-template <int DK, bool SUM>
-__global__ void __launch_bounds__(kPrepThreads, 2)
-    chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                      const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ beta,
-                      uint8_t *__restrict__ ws, int L, int C, int nch, int nu, int Dp, int d_v, int d_vr,
-                      float eps, unsigned *status) {
-    constexpr int G = DK / 4, RPW = 32 / G, N2 = 2 * DK;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
-    uint8_t *kq = smem;                                  // [K; Q]: 128 x Dp, K-major
-    uint8_t *ip = kq + 256 * Dp;                         // [I; P]: 128 x 64, K-major A
-    uint8_t *tp = ip;                                    // [T; P T] replaces [I; P] once read
-    uint8_t *tt = ip + 16384;                            // T: rows k, columns n (MN-major B)
-    float *Am = (float *)(tt + 8192);                    // A = strict_lower(beta K K^T)
-    float *Nm = Am + 64 * LDS;                           // (I + A)^-1
-    float *Rm = Nm + 64 * LDS;                           // block-solve scratch [16][LDS]
-    float *bs = Rm + 16 * LDS;                           // beta (0 on padded rows)
-    uint8_t *vt = (uint8_t *)Am;                         // V (MN-major B), once A and N are done
+// Shared-memory layout of the prep (one chunk at a time).
+struct PrepSmem {
+    uint8_t *kq;     // [K; Q]: 128 x Dp, K-major
+    uint8_t *ip;     // [I; P]: 128 x 64, K-major A; [T; P T] replaces it once read
+    uint8_t *tt;     // T: rows k, columns n (MN-major B)
+    float *Am;       // A = strict_lower(beta K K^T)
+    float *Nm;       // (I + A)^-1
+    float *Rm;       // block-solve scratch [16][LDS]
+    float *bs;       // beta (0 on padded rows)
+    uint8_t *vt;     // V (MN-major B), once A and N are done
     // MMA completion: the Gram matrix (2 issuers), [I; P] T (2 issuers; the
     // sum rule's [I; P] V' by 1), the final product (one issuer per accumulator)
-    uint64_t *bar_g = (uint64_t *)(bs + 64);
-    uint64_t *bar_i = bar_g + 1;
-    uint64_t *bar_f = bar_g + 2;
-    uint32_t *slot = (uint32_t *)(bar_g + 3);
+    uint64_t *bar_g, *bar_i, *bar_f;
+    uint32_t *slot;  // TMEM base address
+};
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int sp = warp & 3, half = warp >> 2;           // TMEM sub-partition, column half
-    const int row = 32 * sp + lane;                      // accumulator row of this thread
-    const int c = blockIdx.x;
-    const int64_t bh = blockIdx.y;
-    const int t0 = c * C, Lc = min(C, L - t0);
-    const int d_dot = N2 * nu;
-    const Record rc = record_layout(Dp, d_v);
-    uint8_t *rec = ws + ((size_t)bh * nch + c) * rc.bytes;
-    const uint32_t ncols = tmem_cols_pow2(max(64, Dp + d_v));
+FW_DEV PrepSmem prep_layout(uint8_t *smem, int Dp) {
+    PrepSmem m;
+    m.kq = smem;
+    m.ip = m.kq + 256 * Dp;
+    m.tt = m.ip + 16384;
+    m.Am = (float *)(m.tt + 8192);
+    m.Nm = m.Am + 64 * LDS;
+    m.Rm = m.Nm + 64 * LDS;
+    m.bs = m.Rm + 16 * LDS;
+    m.vt = (uint8_t *)m.Am;
+    m.bar_g = (uint64_t *)(m.bs + 64);
+    m.bar_i = m.bar_g + 1;
+    m.bar_f = m.bar_g + 2;
+    m.slot = (uint32_t *)(m.bar_g + 3);
+    return m;
+}
 
-    // This chunk's q, k and v rows are pulled into L2 while the preceding
-    // kernel finishes (a prefetch is safe before the wait: see l2_prefetch).
-    if (tid == 0) {
-        const size_t tok = (size_t)bh * L + t0;
-        l2_prefetch(k + tok * DK, (uint32_t)(Lc * DK * 2));
-        l2_prefetch(q + tok * DK, (uint32_t)(Lc * DK * 2));
-        if ((d_vr * 2) % 16 == 0)
-            l2_prefetch(v + tok * d_vr, (uint32_t)(Lc * d_vr * 2));
-    }
-    griddep_wait(); // the inputs may be, and the workspace may still be read by, the preceding kernel
-    q = after_wait(q);
-    k = after_wait(k);
-    v = after_wait(v);
-    beta = after_wait(beta);
-    // Only now may the scan start its prologue (on free SMs): it reads the
-    // caller's W0 before its own wait, which is safe once everything enqueued
-    // before this kernel has completed, as it has here.
-    griddep_launch_dependents();
-    // Global loads first, all in flight before any is used: the key and query
-    // rows for the DPFP, the chunk's V rows (kept in registers until their
-    // tile's space is free) and beta (stored to shared memory after the DPFP).
-    constexpr bool kHalfRows = DK <= 64;
-    constexpr int kRaw = kHalfRows ? DK / 8 : 128 / (8 * RPW);
+struct PrepArgs {
+    const __nv_bfloat16 *q, *k, *v, *beta;
+    uint8_t *ws;
+    int L, C, nch, nu, Dp, d_v, d_vr;
+    float eps;
+    unsigned *status;
+};
+
+__host__ __device__ inline uint32_t prep_tmem_cols(int Dp, int d_v) { return tmem_cols_pow2(Dp + d_v > 64 ? Dp + d_v : 64); }
+
+// The chunk's inputs in registers: the key and query rows for the DPFP, the
+// V rows (kept until their tile's space is free) and beta (stored to shared
+// memory after the DPFP).
+template <int DK> struct PrepRegs {
+    static constexpr int G = DK / 4, RPW = 32 / G;
+    static constexpr bool kHalfRows = DK <= 64;
+    static constexpr int kRaw = kHalfRows ? DK / 8 : 128 / (8 * RPW);
+    static constexpr int kVChunks = 4; // 64 * 128 / 8 / kPrepThreads
     uint4 raw[kRaw];
-    // kHalfRows: thread = (row r, half hs of x); lanes l and l ^ 8 share a row
-    const int hs = (lane >> 3) & 1;
-    const int hr = 16 * warp + ((lane & 7) | ((lane >> 4) << 3));
-    if constexpr (kHalfRows) {
+    uint4 vpre[kVChunks];
+    float beta_t;
+};
+
+// Global loads of chunk c of (b,h), all in flight before any is used.
+template <int DK, bool SUM>
+FW_DEV void prep_load(const PrepArgs &g, int c, int64_t bh, int tid, PrepRegs<DK> &r) {
+    using R = PrepRegs<DK>;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int t0 = c * g.C, Lc = min(g.C, g.L - t0);
+    if constexpr (R::kHalfRows) { // thread = (row r, half hs of x); lanes l and l ^ 8 share a row
+        const int hr = 16 * warp + ((lane & 7) | ((lane >> 4) << 3));
         const int t = hr & 63;
-        const __nv_bfloat16 *src = (hr < 64 ? k : q) + ((size_t)bh * L + t0 + t) * DK;
+        const __nv_bfloat16 *src = (hr < 64 ? g.k : g.q) + ((size_t)bh * g.L + t0 + t) * DK;
 #pragma unroll
-        for (int c8 = 0; c8 < kRaw; ++c8)
-            raw[c8] = t < Lc ? __ldcg(reinterpret_cast<const uint4 *>(src) + c8) : make_uint4(0, 0, 0, 0);
+        for (int c8 = 0; c8 < R::kRaw; ++c8)
+            r.raw[c8] = t < Lc ? __ldcg(reinterpret_cast<const uint4 *>(src) + c8) : make_uint4(0, 0, 0, 0);
     } else {
-        const int g = lane % G;
+        const int gg = lane % R::G;
 #pragma unroll
-        for (int ps = 0; ps < kRaw; ++ps) {
-            const int r = ps * 8 * RPW + warp * RPW + lane / G;
-            const int t = r & 63;
-            raw[ps] = make_uint4(0, 0, 0, 0);
+        for (int ps = 0; ps < R::kRaw; ++ps) {
+            const int rr = ps * 8 * R::RPW + warp * R::RPW + lane / R::G;
+            const int t = rr & 63;
+            r.raw[ps] = make_uint4(0, 0, 0, 0);
             if (t < Lc)
-                raw[ps] = __ldcg(reinterpret_cast<const uint4 *>((r < 64 ? k : q) + ((size_t)bh * L + t0 + t) * DK +
-                                                               8 * (g % (G / 2))));
+                r.raw[ps] = __ldcg(reinterpret_cast<const uint4 *>((rr < 64 ? g.k : g.q) + ((size_t)bh * g.L + t0 + t) * DK +
+                                                                  8 * (gg % (R::G / 2))));
         }
     }
-    constexpr int kVChunks = 4; // 64 * 128 / 8 / kPrepThreads
-    uint4 vpre[kVChunks];
-    const int vcpr = d_vr / 8;
+    const int vcpr = g.d_vr / 8;
 #pragma unroll
-    for (int i = 0; i < kVChunks; ++i) {
+    for (int i = 0; i < R::kVChunks; ++i) {
         const int idx = tid + i * kPrepThreads, t = idx / vcpr, j = 8 * (idx % vcpr);
-        vpre[i] = make_uint4(0, 0, 0, 0);
+        r.vpre[i] = make_uint4(0, 0, 0, 0);
         if (idx < 64 * vcpr && t < Lc)
-            vpre[i] = __ldcg(reinterpret_cast<const uint4 *>(v + ((size_t)bh * L + t0 + t) * d_vr + j));
+            r.vpre[i] = __ldcg(reinterpret_cast<const uint4 *>(g.v + ((size_t)bh * g.L + t0 + t) * g.d_vr + j));
     }
-    float beta_t = 0.f;
+    r.beta_t = 0.f;
     if (!SUM && tid < Lc && tid < 64)
-        beta_t = __bfloat162float(beta[bh * L + t0 + tid]);
+        r.beta_t = __bfloat162float(g.beta[bh * g.L + t0 + tid]);
+}
 
+// Barriers and tensor memory of a prep CTA (once per CTA; published by the
+// first barrier inside prep_compute).
+template <bool SUM>
+FW_DEV void prep_init(const PrepSmem &m, int Dp, int d_v, int tid) {
     if (tid == 0) {
-        mbar_init(bar_g, 2);
-        mbar_init(bar_i, SUM ? 1 : 2);
-        mbar_init(bar_f, (uint32_t)(Dp / 128 + 1));
+        mbar_init(m.bar_g, 2);
+        mbar_init(m.bar_i, SUM ? 1 : 2);
+        mbar_init(m.bar_f, (uint32_t)(Dp / 128 + 1));
         fence_barrier_init();
     }
-    if (warp == 0) {
-        tmem_alloc(slot, ncols);
+    if ((tid >> 5) == 0) {
+        tmem_alloc(m.slot, prep_tmem_cols(Dp, d_v));
         tmem_relinquish();
     }
+}
+
+// Chunk c of (b,h), from the DPFP to the record: [W'; Q'] and K images, U'
+// and Y'.  `parity` is the phase of this chunk on the CTA's three MMA
+// barriers (each completes once per chunk).  Ends with every bulk copy
+// complete and a CTA barrier; false if a wait gave up.
+template <int DK, bool SUM>
+FW_DEV bool prep_compute(const PrepArgs &g, const PrepSmem &m, const PrepRegs<DK> &regs, int c, int64_t bh,
+                         uint32_t parity, int tid) {
+    using R = PrepRegs<DK>;
+    constexpr int G = R::G, RPW = R::RPW, N2 = 2 * DK;
+    constexpr bool kHalfRows = R::kHalfRows;
+    constexpr int kRaw = R::kRaw, kVChunks = R::kVChunks;
+    uint8_t *kq = m.kq, *ip = m.ip, *tp = m.ip, *tt = m.tt, *vt = m.vt;
+    float *Am = m.Am, *Nm = m.Nm, *Rm = m.Rm, *bs = m.bs;
+    uint64_t *bar_g = m.bar_g, *bar_i = m.bar_i, *bar_f = m.bar_f;
+    const auto &raw = regs.raw;
+    const auto &vpre = regs.vpre;
+    const float beta_t = regs.beta_t;
+    const int nu = g.nu, Dp = g.Dp, d_v = g.d_v, d_vr = g.d_vr;
+    const float eps = g.eps;
+    unsigned *status = g.status;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int sp = warp & 3, half = warp >> 2;           // TMEM sub-partition, column half
+    const int row = 32 * sp + lane;                      // accumulator row of this thread
+    const int t0 = c * g.C, Lc = min(g.C, g.L - t0);
+    const int d_dot = N2 * nu;
+    const Record rc = record_layout(Dp, d_v);
+    uint8_t *rec = g.ws + ((size_t)bh * g.nch + c) * rc.bytes;
+    const int hs = (lane >> 3) & 1;
+    const int hr = 16 * warp + ((lane & 7) | ((lane >> 4) << 3));
+    const int vcpr = d_vr / 8;
+    (void)G; (void)RPW; (void)kRaw; (void)t0;
+    bool ok = true;
     // DPFP rows: r < 64 are keys, r >= 64 queries of token r & 63.
     if constexpr (kHalfRows) {
         dpfp_half_row<DK, kMaxDp / (2 * DK)>(raw, hs, hr, nu, eps, kq);
@@ -408,7 +446,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tm = *slot;
+    const uint32_t tm = *m.slot;
     const uint32_t lb = tmem_lane_base(warp);
     // MMAs are issued by lane 0 of several warps at once (one thread issues a
     // tcgen05.mma about every 80 SM cycles; several warps together reach
@@ -435,7 +473,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         }
         mma_commit(bar_g);
     }
-    bool ok = mbar_wait(bar_g, 0, status);
+    ok = mbar_wait(bar_g, parity, status);
     tc_fence_after();
     if (__syncthreads_or(!ok))
         goto teardown;
@@ -508,7 +546,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
             mma_commit(bar_i);
             bulk_wait_read(); // the K image has been read out of the key rows
         }
-        ok = mbar_wait(bar_i, 0, status);
+        ok = mbar_wait(bar_i, parity, status);
         tc_fence_after();
         if (__syncthreads_or(!ok))
             goto teardown;
@@ -543,7 +581,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                          desc_sw128(b + (uint32_t)s * 2048u, 8192, 1024), idesc, s > 2 * warp);
             mma_commit(bar_i);
         }
-        ok = mbar_wait(bar_i, 0, status);
+        ok = mbar_wait(bar_i, parity, status);
         tc_fence_after();
         if (__syncthreads_or(!ok))
             goto teardown;
@@ -589,7 +627,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         }
         if (tid == 0)
             bulk_wait_read(); // the K image has been read out of the key rows
-        ok = mbar_wait(bar_f, 0, status);
+        ok = mbar_wait(bar_f, parity, status);
         tc_fence_after();
         if (__syncthreads_or(!ok))
             goto teardown;
@@ -637,11 +675,44 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     }
 teardown:
     if (tid == 0)
-        bulk_wait_all(); // the bulk copies are done before the CTA retires
+        bulk_wait_all(); // every bulk copy of the chunk is complete
     tc_fence_before();
-    __syncthreads();
-    if (warp == 0)
-        tmem_dealloc(tm, ncols);
+    return !__syncthreads_or(!ok);
+}
+
+template <int DK, bool SUM>
+__global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(PrepArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    const PrepSmem m = prep_layout(align1024(smem_raw), g.Dp);
+    const int tid = threadIdx.x;
+    const int c = blockIdx.x;
+    const int64_t bh = blockIdx.y;
+    const int t0 = c * g.C, Lc = min(g.C, g.L - t0);
+    // This chunk's q, k and v rows are pulled into L2 while the preceding
+    // kernel finishes (a prefetch is safe before the wait: see l2_prefetch).
+    if (tid == 0) {
+        const size_t tok = (size_t)bh * g.L + t0;
+        l2_prefetch(g.k + tok * DK, (uint32_t)(Lc * DK * 2));
+        l2_prefetch(g.q + tok * DK, (uint32_t)(Lc * DK * 2));
+        if ((g.d_vr * 2) % 16 == 0)
+            l2_prefetch(g.v + tok * g.d_vr, (uint32_t)(Lc * g.d_vr * 2));
+    }
+    griddep_wait(); // the inputs may be, and the workspace may still be read by, the preceding kernel
+    PrepArgs a = g;
+    a.q = after_wait(a.q);
+    a.k = after_wait(a.k);
+    a.v = after_wait(a.v);
+    a.beta = after_wait(a.beta);
+    // Only now may the scan start its prologue (on free SMs): it reads the
+    // caller's W0 before its own wait, which is safe once everything enqueued
+    // before this kernel has completed, as it has here.
+    griddep_launch_dependents();
+    PrepRegs<DK> r;
+    prep_load<DK, SUM>(a, c, bh, tid, r);
+    prep_init<SUM>(m, a.Dp, a.d_v, tid);
+    prep_compute<DK, SUM>(a, m, r, c, bh, 0, tid);
+    if ((tid >> 5) == 0)
+        tmem_dealloc(*m.slot, prep_tmem_cols(a.Dp, a.d_v));
 }
 
 // ---------------------------------------------------------------------------
@@ -652,28 +723,86 @@ FW_DEV uint32_t vtile_chunk(int row, int j0, uint32_t blk) {
     return (uint32_t)(j0 >> 6) * blk + (uint32_t)row * 128u + ((uint32_t)(((j0 & 63) >> 3) ^ (row & 7)) << 4);
 }
 
-// One CTA walks the chunks of one (batch, head) for DVB value channels.
-// Everything per thread is done 16 value channels at a time.  NA = number
-// of [W'; Q'] buffers (2: the image of chunk c + 2 is fetched as soon as
-// MMA1 has read chunk c's; 1: chunk c + 1's, into the same buffer).  NKB = number
+// Ready flags of the single-launch forward: flag (b,h, c) is set once chunk
+// c's record of (b,h) is complete.  The writer orders every write of the
+// record (bulk copies included) before a release store; the reader's acquire
+// load orders every later read, bulk copies included, after it.
+FW_DEV void flag_set(unsigned *f) {
+    asm volatile("fence.proxy.async.global;" ::: "memory"); // bulk-copy writes before the release
+    __threadfence();
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
+}
+FW_DEV unsigned flag_load(const unsigned *f) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+// Bounded wait for a flag (false after kWaitLimitNs, with kStatusTimeout
+// recorded); on success later bulk copies observe what the writer released.
+FW_DEV bool flag_wait(const unsigned *f, unsigned *status) {
+    bool ok = flag_load(f) != 0;
+    if (!ok) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t i = 1;; ++i) {
+            __nanosleep(100);
+            if (flag_load(f) != 0) {
+                ok = true;
+                break;
+            }
+            if ((i & 31) == 0 && globaltimer_ns() - t0 > kWaitLimitNs)
+                break;
+        }
+    }
+    if (!ok) {
+        record_status(status, kStatusTimeout);
+        return false;
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
+struct ScanArgs {
+    const float *W0;
+    float *Wf;
+    const float *z0;
+    float *zf;
+    __nv_bfloat16 *y;
+    const uint8_t *ws;
+    const unsigned *flags; // ready flags when the records are being written meanwhile, else null
+    int L, C, nch, d_v, d_vr, d_dot, Dp;
+    unsigned *status;
+};
+
+// One CTA walks the chunks of one (batch, head) for DVB value channels, with
+// NTH threads: thread t owns accumulator row t % 128 and DVB * 128 / NTH of
+// the CTA's columns (16 or 32), worked 16 at a time.  NA = number of
+// [W'; Q'] buffers (2: the image of chunk c + 2 is fetched as soon as MMA1
+// has read chunk c's; 1: chunk c + 1's, into the same buffer).  NKB = number
 // of K buffers (2: K images two chunks ahead; 1: the next K image is
 // fetched as soon as MMA3 has read the current one).
 // ZN = true (the normalised sum rule): the CTA's block is 16 value channels
 // followed by the record's 16-channel normaliser block (channel d_vr holds
-// the running z, its output the denominator z . phi(q)); DVB = 32, and y is
-// written as the ratio of the value columns to that denominator (0 where it
-// is 0).  d_v = the record's channel count, d_vr = the value channels of y,
-// W0 and W_final; z0 / zf: the normaliser state in and out ([B,H,d_dot]).
-template <int DVB, int NKB, int NA, bool ZN>
-__global__ void __launch_bounds__(kScanThreads)
-    chunk_scan_kernel(const float *W0, float *Wf, const float *z0, float *zf, __nv_bfloat16 *__restrict__ y,
-                      const uint8_t *__restrict__ ws, int L, int C, int nch, int d_v, int d_vr, int d_dot, int Dp,
-                      unsigned *status) {
-    static_assert(!ZN || DVB == 32, "the normalised form takes 16 value + 16 normaliser channels");
+// the running z, its output the denominator z . phi(q)); DVB = 32, NTH = 128,
+// and y is written as the ratio of the value columns to that denominator (0
+// where it is 0).  d_v = the record's channel count, d_vr = the value
+// channels of y, W0 and W_final; z0 / zf: the normaliser state in and out
+// ([B,H,d_dot]).
+// FUSED = true: the records are written by other CTAs of the same launch;
+// thread 0 acquires chunk j's ready flag before anything of record j is read.
+template <int DVB, int NTH, int NKB, int NA, bool ZN, bool FUSED>
+FW_DEV void scan_walk(const ScanArgs &g, uint8_t *smem, int vblk, int64_t bh, int tid) {
+    static_assert(!ZN || (DVB == 32 && NTH == 128), "the normalised form takes 16 value + 16 normaliser channels");
+    constexpr int CPT = DVB * 128 / NTH;             // columns per thread
+    static_assert(CPT % 16 == 0, "16 columns at a time");
     constexpr int DS = DVB < 32 ? 32 : DVB;          // TMEM columns per accumulator region
     constexpr int VB = (DVB + 63) / 64;              // 64-column blocks of the value tiles
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
+    const float *W0 = g.W0;
+    float *Wf = g.Wf;
+    const float *z0 = g.z0;
+    float *zf = g.zf;
+    __nv_bfloat16 *y = g.y;
+    const int L = g.L, C = g.C, nch = g.nch, d_v = g.d_v, d_vr = g.d_vr, d_dot = g.d_dot, Dp = g.Dp;
+    unsigned *status = g.status;
     const Record rc = record_layout(Dp, d_v);
     const uint32_t a_bytes = 256u * (uint32_t)Dp, k_bytes = 128u * (uint32_t)Dp;
     const uint32_t sblk = 128u * (uint32_t)Dp;       // bytes of one 64-column block of the S tile
@@ -689,14 +818,13 @@ __global__ void __launch_bounds__(kScanThreads)
     uint64_t *bar_m3 = bar_a + 5;                     // MMA3 done (every block's issuer)
     uint32_t *slot = (uint32_t *)(bar_a + 6);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int v0 = blockIdx.x * (ZN ? 16 : DVB);
-    const int64_t bh = blockIdx.y;
+    const int warp = tid >> 5, row = tid & 127, col0 = (tid >> 7) * CPT;
+    const int v0 = vblk * (ZN ? 16 : DVB);
     // record channel of the CTA's column j (column groups of 4 stay contiguous)
     auto chan = [&](int j) { return (ZN && j >= 16) ? d_vr + (j - 16) : v0 + j; };
     const int MB = Dp / 128;
     const uint32_t ncols = tmem_cols_pow2((2 + MB) * DS);
-    const uint8_t *rec0 = ws + (size_t)bh * nch * rc.bytes;
+    const uint8_t *rec0 = g.ws + (size_t)bh * nch * rc.bytes;
     const bool has_w0 = W0 != nullptr || (ZN && z0 != nullptr);
     const uint32_t lb = tmem_lane_base(warp);
 
@@ -724,77 +852,126 @@ __global__ void __launch_bounds__(kScanThreads)
     const uint32_t kt0_s = smem_u32(kt0), kt1_s = smem_u32(kt1);
 
     // initial state: S^T in TMEM (fp32) and S as the bf16 operand of MMA1.
-    // W0 is the caller's and never written by the prep kernel, which lets
-    // this kernel start only after its own wait (so everything enqueued
+    // W0 is the caller's and never written by the prep, which lets the
+    // standalone scan start only after its own wait (so everything enqueued
     // before the prep has completed): it runs before the wait for the prep.
     for (int mb = 0; mb < MB; ++mb) {
-        const int d = 128 * mb + tid;
+        const int d = 128 * mb + row;
 #pragma unroll
-        for (int j0 = 0; j0 < DVB; j0 += 16) {
+        for (int j0 = 0; j0 < CPT; j0 += 16) {
+            const int jc = col0 + j0;
             float w[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const int jj = j0 + j;
+                const int jj = jc + j;
                 if (ZN && jj >= 16)
                     w[j] = (jj == 16 && z0 && d < d_dot) ? z0[(size_t)bh * d_dot + d] : 0.f;
                 else
                     w[j] = (W0 && d < d_dot) ? W0[((size_t)bh * d_vr + v0 + jj) * d_dot + d] : 0.f;
             }
             if (has_w0)
-                tmem_st16(tS + (uint32_t)(mb * DS + j0) + lb, w);
-            *reinterpret_cast<uint4 *>(st + vtile_chunk(d, j0, sblk)) = pack8(w);
-            *reinterpret_cast<uint4 *>(st + vtile_chunk(d, j0 + 8, sblk)) = pack8(w + 8);
+                tmem_st16(tS + (uint32_t)(mb * DS + jc) + lb, w);
+            *reinterpret_cast<uint4 *>(st + vtile_chunk(d, jc, sblk)) = pack8(w);
+            *reinterpret_cast<uint4 *>(st + vtile_chunk(d, jc + 8, sblk)) = pack8(w + 8);
         }
     }
     if (has_w0)
         tmem_st_wait();
-    // the workspace records are the prep kernel's: wait for it to complete
-    // (and let the next kernel on the stream start its set-up meanwhile)
-    griddep_launch_dependents();
-    griddep_wait();
-    rec0 = after_wait(rec0);
+    // Thread 0's bookkeeping of the bulk loads: images issued and images
+    // waited for (its own waits), and the ready flags acquired (FUSED).
+    int a_issued = 0, a_waited = 0, k_issued = 0, k_waited = 0, acquired = 0;
+    // FUSED: the flag of chunk `acquired` is read one chunk ahead (an acquire
+    // load whose value is only looked at when the chunk is needed, so the
+    // round trip to L2 stays off the serial path); ahead_v = that value.
+    unsigned ahead_v = 0;
+    bool ahead = false;
+    const unsigned *fl = FUSED ? g.flags + (size_t)bh * nch : nullptr;
+    auto read_ahead = [&]() {
+        if constexpr (FUSED) {
+            if (acquired < nch) {
+                ahead_v = flag_load(fl + acquired);
+                ahead = true;
+            }
+        }
+    };
+    // acquire the ready flags of chunks up to cc (thread 0)
+    auto acquire_to = [&](int cc) -> bool {
+        if constexpr (FUSED) {
+            for (; acquired <= cc && acquired < nch; ++acquired) {
+                if (ahead && ahead_v != 0) {
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                } else if (!flag_wait(fl + acquired, status)) {
+                    return false;
+                }
+                ahead = false;
+            }
+        }
+        return true;
+    };
+    auto fetch_a = [&](int j) { // image of chunk j into buffer j % NA (thread 0)
+        uint64_t *b = bar_a + (NA == 2 ? (j & 1) : 0);
+        mbar_arrive_expect_tx(b, a_bytes);
+        bulk_g2s(NA == 2 && (j & 1) ? at1 : at0, rec0 + (size_t)j * rc.bytes + rc.a, a_bytes, b);
+        ++a_issued;
+    };
+    auto fetch_k = [&](int j) {
+        uint64_t *b = bar_k + (NKB == 2 ? (j & 1) : 0);
+        mbar_arrive_expect_tx(b, k_bytes);
+        bulk_g2s(NKB == 2 && (j & 1) ? kt1 : kt0, rec0 + (size_t)j * rc.bytes + rc.k, k_bytes, b);
+        ++k_issued;
+    };
     // On an early exit (a wait that gave up) thread 0 waits, bounded, for the
-    // bulk loads still in flight, so that none lands after the CTA has left.
-    // Which are in flight follows from the chunk and the step that failed
-    // (0: its [W'; Q'] image, 1: MMA1, 2: its K image, 3: MMA3): the image of
-    // chunk j sits in buffer j % NA (j % NKB), in that buffer's phase j / NA.
-    auto drain = [&](int c, int step) {
+    // bulk loads still in flight, so that none lands after the CTA has left:
+    // image j sits in buffer j % NA (j % NKB), in that buffer's phase j / NA.
+    auto drain = [&]() {
         if (tid != 0)
             return;
-        const int a_hi = min(nch - 1, step >= 2 ? c + NA : c + NA - 1);
-        for (int j = step >= 1 ? c + 1 : c; j <= a_hi; ++j)
+        for (int j = a_waited; j < a_issued; ++j)
             mbar_wait(bar_a + (NA == 2 ? (j & 1) : 0), (uint32_t)((NA == 2 ? j >> 1 : j) & 1), status);
-        const int k_hi = min(nch - 1, c + NKB - 1);
-        for (int j = step >= 3 ? c + 1 : c; j <= k_hi; ++j)
+        for (int j = k_waited; j < k_issued; ++j)
             mbar_wait(bar_k + (NKB == 2 ? (j & 1) : 0), (uint32_t)((NKB == 2 ? j >> 1 : j) & 1), status);
     };
+    const uint8_t *wsr = g.ws;
+    if constexpr (!FUSED) {
+        // the workspace records are the prep kernel's: wait for it to complete
+        // (and let the next kernel on the stream start its set-up meanwhile)
+        griddep_launch_dependents();
+        griddep_wait();
+        wsr = after_wait(wsr);
+        rec0 = wsr + (size_t)bh * nch * rc.bytes;
+    }
+    bool ok = true;
     if (tid == 0) { // chunk 0's [W'; Q'] and the first K image(s)
-        mbar_arrive_expect_tx(bar_a, a_bytes);
-        bulk_g2s(at0, rec0 + rc.a, a_bytes, bar_a);
-        if (NA == 2 && nch > 1) {
-            mbar_arrive_expect_tx(bar_a + 1, a_bytes);
-            bulk_g2s(at1, rec0 + rc.bytes + rc.a, a_bytes, bar_a + 1);
-        }
-        mbar_arrive_expect_tx(bar_k, k_bytes);
-        bulk_g2s(kt0, rec0 + rc.k, k_bytes, bar_k);
-        if (NKB == 2 && nch > 1) {
-            mbar_arrive_expect_tx(bar_k + 1, k_bytes);
-            bulk_g2s(kt1, rec0 + rc.bytes + rc.k, k_bytes, bar_k + 1);
+        ok = acquire_to(NA == 2 || NKB == 2 ? 1 : 0);
+        if (ok) {
+            fetch_a(0);
+            if (NA == 2 && nch > 1)
+                fetch_a(1);
+            fetch_k(0);
+            if (NKB == 2 && nch > 1)
+                fetch_k(1);
         }
     }
     fence_async_smem();
     tc_fence_before();
-    __syncthreads();
+    if (__syncthreads_or(!ok)) { // nothing in flight yet
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0)
+            tmem_dealloc(tm, ncols);
+        return;
+    }
 
-    // U' (rows 0..63, threads 0..63) or Y' (threads 64..127) of a chunk,
-    // [d_v/4][64][4] in the record: each 16-byte load of a warp is one
-    // 512-byte run.  Chunk c + 1's are loaded as soon as chunk c's are used.
-    float pre[DVB];
+    // U' (rows 0..63) or Y' (rows 64..127) of a chunk, [d_v/4][64][4] in the
+    // record: each 16-byte load of a warp is one 512-byte run.  Chunk c + 1's
+    // are loaded once MMA3 of chunk c may start (its flag acquired by then).
+    float pre[CPT];
     auto load_pre = [&](int cc) {
-        const float *src = (const float *)(rec0 + (size_t)cc * rc.bytes + (tid < 64 ? rc.up : rc.yp)) + 4 * (tid & 63);
+        const float *src =
+            (const float *)(rec0 + (size_t)cc * rc.bytes + (row < 64 ? rc.up : rc.yp)) + 4 * (row & 63);
 #pragma unroll
-        for (int j = 0; j < DVB; j += 4) {
-            const float4 f = __ldcg(reinterpret_cast<const float4 *>(src + 64 * chan(j)));
+        for (int j = 0; j < CPT; j += 4) {
+            const float4 f = __ldcg(reinterpret_cast<const float4 *>(src + 64 * chan(col0 + j)));
             pre[j] = f.x;
             pre[j + 1] = f.y;
             pre[j + 2] = f.z;
@@ -807,11 +984,11 @@ __global__ void __launch_bounds__(kScanThreads)
         const int t0 = c * C, Lc = min(C, L - t0), kb = NKB == 2 ? (c & 1) : 0, ab = NA == 2 ? (c & 1) : 0;
         const uint32_t a_parity = NA == 2 ? (uint32_t)((c >> 1) & 1) : (uint32_t)(c & 1);
         const uint32_t k_parity = NKB == 2 ? (uint32_t)((c >> 1) & 1) : (uint32_t)(c & 1);
-        const uint8_t *rec = rec0 + (size_t)c * rc.bytes;
-        // U' (rows 0..63, threads 0..63) or Y' (threads 64..127) of this chunk
-        bool ok = mbar_wait(bar_a + ab, a_parity, status);
+        ok = mbar_wait(bar_a + ab, a_parity, status);
+        if (tid == 0 && ok)
+            ++a_waited;
         if (__syncthreads_or(!ok)) {
-            drain(c, 0);
+            drain();
             break;
         }
 
@@ -829,37 +1006,41 @@ __global__ void __launch_bounds__(kScanThreads)
         ok = mbar_wait(bar_m1, m1_phase, status);
         m1_phase ^= 1;
         if (__syncthreads_or(!ok)) {
-            drain(c, 1);
+            drain();
             break;
         }
         tc_fence_after();
-        if (tid == 0 && c + NA < nch) { // this [W'; Q'] buffer is consumed: fetch a later chunk's
-            mbar_arrive_expect_tx(bar_a + ab, a_bytes);
-            bulk_g2s(ab ? at1 : at0, rec + (size_t)NA * rc.bytes + rc.a, a_bytes, bar_a + ab);
+        // this [W'; Q'] buffer is consumed: fetch a later chunk's (thread 0,
+        // after the ready flags of the chunks the next loads read)
+        bool ok_f = true;
+        if (tid == 0) {
+            ok_f = acquire_to(c + (NA > NKB ? NA : NKB));
+            if (ok_f && c + NA < nch)
+                fetch_a(c + NA);
         }
         {
-            float d1[DVB], d1b[DVB];
+            float d1[CPT], d1b[CPT];
 #pragma unroll
-            for (int j0 = 0; j0 < DVB; j0 += 16) { // every load in flight, then one wait
-                tmem_ld16(tD1 + lb + (uint32_t)j0, d1 + j0);
-                tmem_ld16(tD1b + lb + (uint32_t)j0, d1b + j0);
+            for (int j0 = 0; j0 < CPT; j0 += 16) { // every load in flight, then one wait
+                tmem_ld16(tD1 + lb + (uint32_t)(col0 + j0), d1 + j0);
+                tmem_ld16(tD1b + lb + (uint32_t)(col0 + j0), d1b + j0);
             }
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < DVB; ++j)
+            for (int j = 0; j < CPT; ++j)
                 d1[j] += d1b[j];
-            if (tid < 64) {                           // U = U' - W' S^T
+            if (row < 64) {                           // U = U' - W' S^T
 #pragma unroll
-                for (int j0 = 0; j0 < DVB; j0 += 16) {
+                for (int j0 = 0; j0 < CPT; j0 += 16) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         d1[j0 + j] = pre[j0 + j] - d1[j0 + j];
-                    *reinterpret_cast<uint4 *>(ut + vtile_chunk(tid, j0, 8192u)) = pack8(d1 + j0);
-                    *reinterpret_cast<uint4 *>(ut + vtile_chunk(tid, j0 + 8, 8192u)) = pack8(d1 + j0 + 8);
+                    *reinterpret_cast<uint4 *>(ut + vtile_chunk(row, col0 + j0, 8192u)) = pack8(d1 + j0);
+                    *reinterpret_cast<uint4 *>(ut + vtile_chunk(row, col0 + j0 + 8, 8192u)) = pack8(d1 + j0 + 8);
                 }
-            } else if (tid - 64 < Lc) {               // y = Y' + Q' S^T
+            } else if (row - 64 < Lc) {               // y = Y' + Q' S^T
 #pragma unroll
-                for (int j = 0; j < DVB; ++j)
+                for (int j = 0; j < CPT; ++j)
                     d1[j] += pre[j];
                 if constexpr (ZN) {                   // the ratio to the normaliser column
                     const float den = d1[16];
@@ -868,21 +1049,23 @@ __global__ void __launch_bounds__(kScanThreads)
                     for (int j = 0; j < 16; ++j)
                         d1[j] *= inv;
                 }
-                __nv_bfloat16 *dst = y + ((size_t)bh * L + t0 + (tid - 64)) * d_vr + v0;
+                __nv_bfloat16 *dst = y + ((size_t)bh * L + t0 + (row - 64)) * d_vr + v0 + col0;
 #pragma unroll
-                for (int j0 = 0; j0 < (ZN ? 16 : DVB); j0 += 8)
+                for (int j0 = 0; j0 < (ZN ? 16 : CPT); j0 += 8)
                     *reinterpret_cast<uint4 *>(dst + j0) = pack8(d1 + j0);
             }
         }
-        if (c + 1 < nch)
-            load_pre(c + 1);
         fence_async_smem();
         tc_fence_before();
-        ok = mbar_wait(bar_k + kb, k_parity, status);
+        ok = ok_f && mbar_wait(bar_k + kb, k_parity, status);
+        if (tid == 0 && ok)
+            ++k_waited;
         if (__syncthreads_or(!ok)) {
-            drain(c, 2);
+            drain();
             break;
         }
+        if (c + 1 < nch)
+            load_pre(c + 1);
 
         // MMA3: S^T += K^T U   (K^T: the K image read MN-major); block mb of
         // S^T by warp mb
@@ -902,34 +1085,36 @@ __global__ void __launch_bounds__(kScanThreads)
         ok = mbar_wait(bar_m3, m3_phase, status);
         m3_phase ^= 1;
         if (__syncthreads_or(!ok)) {
-            drain(c, 3);
+            drain();
             break;
         }
         tc_fence_after();
-        if (tid == 0 && c + NKB < nch) { // this K buffer is consumed: fetch a later chunk's
-            mbar_arrive_expect_tx(bar_k + kb, k_bytes);
-            bulk_g2s(kb ? kt1 : kt0, rec + (size_t)NKB * rc.bytes + rc.k, k_bytes, bar_k + kb);
+        if (tid == 0) {
+            if (c + NKB < nch) // this K buffer is consumed: fetch a later chunk's
+                fetch_k(c + NKB);
+            read_ahead();      // the next chunk's flag, looked at after its MMA1
         }
         for (int mb = 0; mb < MB; ++mb) {
-            const int d = 128 * mb + tid;
-            float sv[DVB];
+            const int d = 128 * mb + row;
+            float sv[CPT];
 #pragma unroll
-            for (int j0 = 0; j0 < DVB; j0 += 16) // every load in flight, then one wait
-                tmem_ld16(tS + (uint32_t)(mb * DS + j0) + lb, sv + j0);
+            for (int j0 = 0; j0 < CPT; j0 += 16) // every load in flight, then one wait
+                tmem_ld16(tS + (uint32_t)(mb * DS + col0 + j0) + lb, sv + j0);
             tmem_ld_wait();
 #pragma unroll
-            for (int j0 = 0; j0 < DVB; j0 += 16) {
+            for (int j0 = 0; j0 < CPT; j0 += 16) {
+                const int jc = col0 + j0;
                 if (c + 1 < nch) {
-                    *reinterpret_cast<uint4 *>(st + vtile_chunk(d, j0, sblk)) = pack8(sv + j0);
-                    *reinterpret_cast<uint4 *>(st + vtile_chunk(d, j0 + 8, sblk)) = pack8(sv + j0 + 8);
+                    *reinterpret_cast<uint4 *>(st + vtile_chunk(d, jc, sblk)) = pack8(sv + j0);
+                    *reinterpret_cast<uint4 *>(st + vtile_chunk(d, jc + 8, sblk)) = pack8(sv + j0 + 8);
                 } else if (d < d_dot) {
-                    if (ZN && j0 >= 16) {             // the normaliser state: column 16
-                        if (j0 == 16 && zf && blockIdx.x == 0)
-                            zf[(size_t)bh * d_dot + d] = sv[16];
+                    if (ZN && jc >= 16) {             // the normaliser state: column 16
+                        if (jc == 16 && zf && vblk == 0)
+                            zf[(size_t)bh * d_dot + d] = sv[j0];
                     } else if (Wf) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            Wf[((size_t)bh * d_vr + v0 + j0 + j) * d_dot + d] = sv[j0 + j];
+                            Wf[((size_t)bh * d_vr + v0 + jc + j) * d_dot + d] = sv[j0 + j];
                     }
                 }
             }
@@ -942,6 +1127,51 @@ __global__ void __launch_bounds__(kScanThreads)
     __syncthreads();
     if (warp == 0)
         tmem_dealloc(tm, ncols);
+}
+
+template <int DVB, int NTH, int NKB, int NA, bool ZN>
+__global__ void __launch_bounds__(NTH) chunk_scan_kernel(ScanArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    scan_walk<DVB, NTH, NKB, NA, ZN, false>(g, align1024(smem_raw), blockIdx.x, blockIdx.y, threadIdx.x);
+}
+
+// The whole forward in one launch: CTAs [0, nscan) walk the chunks of a
+// (value block, batch*head) as chunk_scan_kernel does, the others prepare
+// chunks as chunk_prep_kernel does, chunk-major (chunk c of every (b,h)
+// before chunk c + 1 of any), so the walk finds its next record ready (or
+// nearly so) while the rest of the records are still being prepared.  A
+// record is handed over through its ready flag, which the caller zeroes
+// before the launch.  The launch is cooperative, so every CTA is resident and
+// a walk that waits on a flag always waits on a CTA that is running.
+// Same arithmetic as the two kernels, bit for bit.
+template <int DK, int DVB, int NTH, int NKB, int NA>
+__global__ void __launch_bounds__(NTH, 1) chunk_fused_kernel(PrepArgs pa, ScanArgs sa, unsigned *flags, int nscan) {
+    static_assert(NTH == kPrepThreads, "one block size for both roles");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const int tid = threadIdx.x;
+    const int nvb = sa.d_v / DVB;
+    if ((int)blockIdx.x < nscan) {
+        scan_walk<DVB, NTH, NKB, NA, false, true>(sa, smem, (int)blockIdx.x % nvb, (int)blockIdx.x / nvb, tid);
+        return;
+    }
+    const PrepSmem m = prep_layout(smem, pa.Dp);
+    const int nprep = (int)gridDim.x - nscan, BH = nscan / nvb;
+    const int jobs = BH * pa.nch;
+    prep_init<false>(m, pa.Dp, pa.d_v, tid);
+    uint32_t parity = 0;
+    for (int job = (int)blockIdx.x - nscan; job < jobs; job += nprep, parity ^= 1u) {
+        const int c = job / BH;
+        const int64_t bh = job % BH;
+        PrepRegs<DK> r;
+        prep_load<DK, false>(pa, c, bh, tid, r);
+        if (!prep_compute<DK, false>(pa, m, r, c, bh, parity, tid))
+            break;
+        if (tid == 0)
+            flag_set(flags + (size_t)bh * pa.nch + c);
+    }
+    if ((tid >> 5) == 0)
+        tmem_dealloc(*m.slot, prep_tmem_cols(pa.Dp, pa.d_v));
 }
 
 // ---------------------------------------------------------------- host side
@@ -958,67 +1188,208 @@ size_t scan_smem(int Dp, int dvb, int nkb, int na) {
 
 constexpr size_t kMaxSmem = 227 * 1024;
 
+// Dynamic shared memory of a kernel, with the whole unified L1 / shared
+// array given to shared memory (these kernels keep their data there and read
+// global memory through L2), so that the occupancy the runtime reports is the
+// one the kernel gets.
+template <typename K> cudaError_t set_smem(K kern, size_t bytes) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    return e;
+}
+
 bool fits(int Dp, int d_v, int dvb) {
     return Dp <= kMaxDp && Dp + d_v <= 512 && scan_smem(Dp, dvb, 1, 1) <= kMaxSmem && prep_smem(Dp, d_v) <= kMaxSmem;
 }
 
-// Value channels per scan CTA: 16 (32 with the normaliser block).  The walk
-// over the chunks is serial, so the per-chunk latency decides: a tcgen05.mma
-// of M = 128 costs about the same for any N up to 128, but the per-thread
-// work between the MMAs (TMEM loads, the U and S tiles, y) grows with the
-// channel count.  Measured on the b4h8 L512 and nu = 3 L2048 workloads, 16
-// channels per CTA beat 32 and 64 (scan 14.4 / 18.5 / 24.5 us and
-// 80 / 96 / 141 us).
-constexpr int kDVB = 16;
+// Value channels per scan CTA and threads per scan CTA.  The walk over the
+// chunks is serial, so the per-chunk latency decides: a tcgen05.mma costs
+// about the same for any N up to 128, but the per-thread work between the
+// MMAs (TMEM loads, the U and S tiles, y) grows with the columns a thread
+// owns, so every thread owns 16 columns: 32 channels on 256 threads, or 16
+// on 128 threads where d_v is not a multiple of 32.  (Measured with 128
+// threads on the b4h8 L512 and nu = 3 L2048 workloads: 16 channels per CTA
+// beat 32 and 64, scan 14.4 / 18.5 / 24.5 us and 80 / 96 / 141 us.)  The
+// normalised sum rule takes 16 value + 16 normaliser channels on 128 threads.
+bool wide_scan(int d_v) { return d_v % 32 == 0; }
 
 // Two K buffers when they fit in shared memory, else one; then two [W'; Q']
 // buffers when those fit as well.
 int choose_nkb(int Dp, int dvb) { return scan_smem(Dp, dvb, 2, 1) <= kMaxSmem ? 2 : 1; }
 int choose_na(int Dp, int dvb) { return scan_smem(Dp, dvb, choose_nkb(Dp, dvb), 2) <= kMaxSmem ? 2 : 1; }
 
-template <int DK, bool SUM>
-cudaError_t launch_prep(const void *q, const void *k, const void *v, const void *beta, uint8_t *ws, int BH,
-                        int L, int C, int nch, int nu, int Dp, int d_v, int d_vr, float eps, unsigned *status,
-                        cudaStream_t st) {
-    const size_t smem = prep_smem(Dp, d_v);
-    auto kern = chunk_prep_kernel<DK, SUM>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess)
-        return e;
-    return launch_pdl(kern, dim3((unsigned)nch, (unsigned)BH), dim3(kPrepThreads), smem, st,
-                      static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-                      static_cast<const __nv_bfloat16 *>(v), static_cast<const __nv_bfloat16 *>(beta), ws, L, C,
-                      nch, nu, Dp, d_v, d_vr, eps, status);
+PrepArgs prep_args(const void *q, const void *k, const void *v, const void *beta, uint8_t *ws, int L, int C,
+                   int nch, int nu, int Dp, int d_v, int d_vr, float eps, unsigned *status) {
+    PrepArgs a;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.k = static_cast<const __nv_bfloat16 *>(k);
+    a.v = static_cast<const __nv_bfloat16 *>(v);
+    a.beta = static_cast<const __nv_bfloat16 *>(beta);
+    a.ws = ws;
+    a.L = L;
+    a.C = C;
+    a.nch = nch;
+    a.nu = nu;
+    a.Dp = Dp;
+    a.d_v = d_v;
+    a.d_vr = d_vr;
+    a.eps = eps;
+    a.status = status;
+    return a;
 }
 
-template <int DVB, int NKB, int NA, bool ZN>
-cudaError_t launch_scan(const float *W0, float *Wf, const float *z0, float *zf, void *y, const uint8_t *ws, int BH,
-                        int L, int C, int nch, int d_v, int d_vr, int d_dot, int Dp, unsigned *status,
-                        cudaStream_t st) {
-    const size_t smem = scan_smem(Dp, DVB, NKB, NA);
-    auto kern = chunk_scan_kernel<DVB, NKB, NA, ZN>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+ScanArgs scan_args(const float *W0, float *Wf, const float *z0, float *zf, void *y, const uint8_t *ws,
+                   const unsigned *flags, int L, int C, int nch, int d_v, int d_vr, int d_dot, int Dp,
+                   unsigned *status) {
+    ScanArgs a;
+    a.W0 = W0;
+    a.Wf = Wf;
+    a.z0 = z0;
+    a.zf = zf;
+    a.y = static_cast<__nv_bfloat16 *>(y);
+    a.ws = ws;
+    a.flags = flags;
+    a.L = L;
+    a.C = C;
+    a.nch = nch;
+    a.d_v = d_v;
+    a.d_vr = d_vr;
+    a.d_dot = d_dot;
+    a.Dp = Dp;
+    a.status = status;
+    return a;
+}
+
+template <int DK, bool SUM>
+cudaError_t launch_prep(const PrepArgs &a, int BH, cudaStream_t st) {
+    const size_t smem = prep_smem(a.Dp, a.d_v);
+    auto kern = chunk_prep_kernel<DK, SUM>;
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(kern, dim3((unsigned)a.nch, (unsigned)BH), dim3(kPrepThreads), smem, st, a);
+}
+
+template <int DVB, int NTH, int NKB, int NA, bool ZN>
+cudaError_t launch_scan(const ScanArgs &a, int BH, cudaStream_t st) {
+    const size_t smem = scan_smem(a.Dp, DVB, NKB, NA);
+    auto kern = chunk_scan_kernel<DVB, NTH, NKB, NA, ZN>;
+    cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;
     // programmatic dependent launch: the scan's CTAs may be scheduled while
     // the preceding kernel (the prep) finishes; they wait in griddep_wait
     // before reading its output
-    const dim3 grid((unsigned)(ZN ? d_vr / 16 : d_v / DVB), (unsigned)BH);
-    return launch_pdl(kern, grid, dim3(kScanThreads), smem, st, W0, Wf, z0, zf, static_cast<__nv_bfloat16 *>(y), ws,
-                      L, C, nch, d_v, d_vr, d_dot, Dp, status);
+    const dim3 grid((unsigned)(ZN ? a.d_vr / 16 : a.d_v / DVB), (unsigned)BH);
+    return launch_pdl(kern, grid, dim3(NTH), smem, st, a);
 }
 
-template <int DVB, bool ZN>
-cudaError_t launch_scan_bufs(const float *W0, float *Wf, const float *z0, float *zf, void *y, const uint8_t *ws,
-                             int BH, int L, int C, int nch, int d_v, int d_vr, int d_dot, int Dp, unsigned *status,
-                             cudaStream_t st) {
-    if (choose_nkb(Dp, DVB) == 2) {
-        if (choose_na(Dp, DVB) == 2)
-            return launch_scan<DVB, 2, 2, ZN>(W0, Wf, z0, zf, y, ws, BH, L, C, nch, d_v, d_vr, d_dot, Dp, status, st);
-        return launch_scan<DVB, 2, 1, ZN>(W0, Wf, z0, zf, y, ws, BH, L, C, nch, d_v, d_vr, d_dot, Dp, status, st);
+template <int DVB, int NTH, bool ZN>
+cudaError_t launch_scan_bufs(const ScanArgs &a, int BH, cudaStream_t st) {
+    if (choose_nkb(a.Dp, DVB) == 2) {
+        if (choose_na(a.Dp, DVB) == 2)
+            return launch_scan<DVB, NTH, 2, 2, ZN>(a, BH, st);
+        return launch_scan<DVB, NTH, 2, 1, ZN>(a, BH, st);
     }
-    return launch_scan<DVB, 1, 1, ZN>(W0, Wf, z0, zf, y, ws, BH, L, C, nch, d_v, d_vr, d_dot, Dp, status, st);
+    return launch_scan<DVB, NTH, 1, 1, ZN>(a, BH, st);
 }
+
+// The single-launch forward (chunk_fused_kernel): nscan walking CTAs and
+// the rest preparing, as many CTAs as the GPU holds at once.  Its plan (grid
+// and walking CTAs), or cudaErrorNotSupported where the two kernels are the
+// better choice: when the standalone prep covers every chunk in one wave
+// (there is then no later wave to overlap with the walk), or when the
+// walking CTAs alone would fill the GPU.
+template <int DK, int NKB, int NA>
+cudaError_t fused_plan(int BH, int nch, int Dp, int d_v, int num_sms, int *grid, int *nscan) {
+    constexpr int DVB = 32, NTH = 256;
+    if (nch < 2 || !wide_scan(d_v) || num_sms <= 0)
+        return cudaErrorNotSupported;
+    const long long jobs = (long long)BH * nch;
+    {
+        // prep CTAs per SM: shared memory, tensor memory (512 columns per SM)
+        // and registers (the kernel is built for two CTAs of 256 threads).
+        // Counted here: the runtime's occupancy query reports one CTA per SM
+        // for this kernel whatever its resources, while two do run at once.
+        int dev = 0, smem_sm = 0, rsv = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        if (e != cudaSuccess)
+            return e;
+        const int by_smem = (int)((size_t)smem_sm / (prep_smem(Dp, d_v) + (size_t)rsv));
+        const int by_tmem = 512 / (int)prep_tmem_cols(Dp, d_v);
+        const int prep_per_sm = std::min(std::min(by_smem, by_tmem), 2);
+        if (jobs <= (long long)prep_per_sm * num_sms)
+            return cudaErrorNotSupported;
+    }
+    const size_t smem = std::max(prep_smem(Dp, d_v), scan_smem(Dp, DVB, NKB, NA));
+    auto kern = chunk_fused_kernel<DK, DVB, NTH, NKB, NA>;
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess)
+        return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NTH, smem);
+    if (e != cudaSuccess)
+        return e;
+    *nscan = BH * (d_v / DVB);
+    const long long resident = (long long)per_sm * num_sms;
+    if (resident <= *nscan)
+        return cudaErrorNotSupported;
+    *grid = (int)std::min(resident, (long long)*nscan + jobs);
+    return cudaSuccess;
+}
+
+template <int DK, int NKB, int NA>
+cudaError_t launch_fused(const PrepArgs &pa, const ScanArgs &sa, unsigned *flags, int BH, int num_sms,
+                         cudaStream_t st) {
+    constexpr int DVB = 32, NTH = 256;
+    int grid = 0, nscan = 0;
+    cudaError_t e = fused_plan<DK, NKB, NA>(BH, pa.nch, pa.Dp, pa.d_v, num_sms, &grid, &nscan);
+    if (e != cudaSuccess)
+        return e;
+    const size_t smem = std::max(prep_smem(pa.Dp, pa.d_v), scan_smem(pa.Dp, DVB, NKB, NA));
+    e = cudaMemsetAsync(flags, 0, (size_t)BH * pa.nch * sizeof(unsigned), st);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NTH);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, chunk_fused_kernel<DK, DVB, NTH, NKB, NA>, pa, sa, flags, nscan);
+}
+
+template <int DK>
+cudaError_t launch_fused_bufs(const PrepArgs &pa, const ScanArgs &sa, unsigned *flags, int BH, int num_sms,
+                              cudaStream_t st) {
+    if (choose_nkb(pa.Dp, 32) == 2) {
+        if (choose_na(pa.Dp, 32) == 2)
+            return launch_fused<DK, 2, 2>(pa, sa, flags, BH, num_sms, st);
+        return launch_fused<DK, 2, 1>(pa, sa, flags, BH, num_sms, st);
+    }
+    return launch_fused<DK, 1, 1>(pa, sa, flags, BH, num_sms, st);
+}
+
+template <int DK>
+cudaError_t fused_plan_bufs(int BH, int nch, int Dp, int d_v, int num_sms, int *grid, int *nscan) {
+    if (choose_nkb(Dp, 32) == 2) {
+        if (choose_na(Dp, 32) == 2)
+            return fused_plan<DK, 2, 2>(BH, nch, Dp, d_v, num_sms, grid, nscan);
+        return fused_plan<DK, 2, 1>(BH, nch, Dp, d_v, num_sms, grid, nscan);
+    }
+    return fused_plan<DK, 1, 1>(BH, nch, Dp, d_v, num_sms, grid, nscan);
+}
+
+size_t records_bytes(int BH, int nch, int Dp, int d_v) { return (size_t)BH * nch * record_layout(Dp, d_v).bytes; }
 
 } // namespace
 
@@ -1029,32 +1400,60 @@ bool tc_forward_supported(int d_key, int nu, int d_v, int chunk) {
         return false;
     if (chunk < 1 || chunk > kTile)
         return false;
-    return fits(padded_ddot(2 * d_key * nu), d_v, kDVB);
+    return fits(padded_ddot(2 * d_key * nu), d_v, wide_scan(d_v) ? 32 : 16);
 }
 
+// The records, then one ready flag per chunk (the single-launch forward).
 size_t tc_forward_workspace_bytes(int B, int H, int L, int d_key, int nu, int d_v, int chunk) {
     const int nch = (L + chunk - 1) / chunk;
-    return (size_t)B * H * nch * record_layout(padded_ddot(2 * d_key * nu), d_v).bytes;
+    return records_bytes(B * H, nch, padded_ddot(2 * d_key * nu), d_v) + (size_t)B * H * nch * sizeof(unsigned);
 }
 
 namespace {
 
 template <bool SUM>
-cudaError_t prep_dispatch(const void *q, const void *k, const void *v, const void *beta, void *workspace, int B,
-                          int H, int L, int d_key, int nu, int d_v, int d_vr, int chunk, float eps, unsigned *status,
-                          cudaStream_t st) {
-    const int BH = B * H;
-    const int nch = (L + chunk - 1) / chunk;
-    const int Dp = padded_ddot(2 * d_key * nu);
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
+cudaError_t prep_dispatch(const PrepArgs &a, int BH, int d_key, cudaStream_t st) {
     switch (d_key) {
-    case 8: return launch_prep<8, SUM>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, d_vr, eps, status, st);
-    case 16: return launch_prep<16, SUM>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, d_vr, eps, status, st);
-    case 32: return launch_prep<32, SUM>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, d_vr, eps, status, st);
-    case 64: return launch_prep<64, SUM>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, d_vr, eps, status, st);
-    case 128: return launch_prep<128, SUM>(q, k, v, beta, ws, BH, L, chunk, nch, nu, Dp, d_v, d_vr, eps, status, st);
+    case 8: return launch_prep<8, SUM>(a, BH, st);
+    case 16: return launch_prep<16, SUM>(a, BH, st);
+    case 32: return launch_prep<32, SUM>(a, BH, st);
+    case 64: return launch_prep<64, SUM>(a, BH, st);
+    case 128: return launch_prep<128, SUM>(a, BH, st);
     default: return cudaErrorInvalidValue;
     }
+}
+
+// The scan of the delta rule or of the unnormalised sum rule: 16 channels
+// per CTA (128 threads) where those CTAs fit on the GPU at once, else 32
+// (256 threads: half as many CTAs for the same per-chunk time).  `wide`
+// forces 32, as the single-launch forward uses, so that the standalone
+// phases of a shape that forward takes give the same bits.
+cudaError_t scan_dispatch(const ScanArgs &a, int BH, int num_sms, bool wide, cudaStream_t st) {
+    if (wide_scan(a.d_v) && (wide || (long long)BH * (a.d_v / 16) > num_sms))
+        return launch_scan_bufs<32, 256, false>(a, BH, st);
+    return launch_scan_bufs<16, 128, false>(a, BH, st);
+}
+
+// Kernels the bf16 forward enqueues for this shape: 1 where fused_plan
+// accepts it, else 2.
+cudaError_t forward_plan(int B, int H, int L, int d_key, int nu, int d_v, int chunk, int num_sms, int *count) {
+    const int nch = (L + chunk - 1) / chunk;
+    const int Dp = padded_ddot(2 * d_key * nu);
+    int grid = 0, nscan = 0;
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (d_key) {
+    case 8: e = fused_plan_bufs<8>(B * H, nch, Dp, d_v, num_sms, &grid, &nscan); break;
+    case 16: e = fused_plan_bufs<16>(B * H, nch, Dp, d_v, num_sms, &grid, &nscan); break;
+    case 32: e = fused_plan_bufs<32>(B * H, nch, Dp, d_v, num_sms, &grid, &nscan); break;
+    case 64: e = fused_plan_bufs<64>(B * H, nch, Dp, d_v, num_sms, &grid, &nscan); break;
+    case 128: e = fused_plan_bufs<128>(B * H, nch, Dp, d_v, num_sms, &grid, &nscan); break;
+    default: break;
+    }
+    if (e == cudaSuccess || e == cudaErrorNotSupported) {
+        *count = e == cudaSuccess ? 1 : 2;
+        return cudaSuccess;
+    }
+    return e;
 }
 
 } // namespace
@@ -1062,29 +1461,64 @@ cudaError_t prep_dispatch(const void *q, const void *k, const void *v, const voi
 cudaError_t tc_prepare_launch(const void *q, const void *k, const void *v, const void *beta, void *workspace,
                               int B, int H, int L, int d_key, int nu, int d_v, int chunk, float eps,
                               unsigned *status, cudaStream_t st) {
-    return prep_dispatch<false>(q, k, v, beta, workspace, B, H, L, d_key, nu, d_v, d_v, chunk, eps, status, st);
+    const int nch = (L + chunk - 1) / chunk;
+    const PrepArgs a = prep_args(q, k, v, beta, static_cast<uint8_t *>(workspace), L, chunk, nch, nu,
+                                 padded_ddot(2 * d_key * nu), d_v, d_v, eps, status);
+    return prep_dispatch<false>(a, B * H, d_key, st);
 }
 
 cudaError_t tc_scan_launch(const void *workspace, const float *W0, float *W_final, void *y, int B, int H, int L,
                            int d_key, int nu, int d_v, int chunk, int num_sms, unsigned *status, cudaStream_t st) {
-    const int BH = B * H;
     const int nch = (L + chunk - 1) / chunk;
     const int d_dot = 2 * d_key * nu;
-    const int Dp = padded_ddot(d_dot);
-    const uint8_t *ws = static_cast<const uint8_t *>(workspace);
-    (void)num_sms;
-    return launch_scan_bufs<kDVB, false>(W0, W_final, nullptr, nullptr, y, ws, BH, L, chunk, nch, d_v, d_v, d_dot, Dp,
-                                         status, st);
+    const ScanArgs a = scan_args(W0, W_final, nullptr, nullptr, y, static_cast<const uint8_t *>(workspace), nullptr,
+                                 L, chunk, nch, d_v, d_v, d_dot, padded_ddot(d_dot), status);
+    int count = 0;
+    const cudaError_t e = forward_plan(B, H, L, d_key, nu, d_v, chunk, num_sms, &count);
+    if (e != cudaSuccess)
+        return e;
+    return scan_dispatch(a, B * H, num_sms, count == 1, st);
 }
 
+int tc_forward_kernel_count(int B, int H, int L, int d_key, int nu, int d_v, int chunk, int num_sms) {
+    int count = 0;
+    return forward_plan(B, H, L, d_key, nu, d_v, chunk, num_sms, &count) == cudaSuccess ? count : -1;
+}
+
+// One launch (chunk_fused_kernel) where fused_plan accepts the shape;
+// otherwise the two kernels.  Both give the same bits.
 cudaError_t tc_forward_launch(const void *q, const void *k, const void *v, const void *beta,
                               const float *W0, float *W_final, void *y, void *workspace, int B,
                               int H, int L, int d_key, int nu, int d_v, int chunk, float eps,
                               int num_sms, unsigned *status, cudaStream_t st) {
-    const cudaError_t e = tc_prepare_launch(q, k, v, beta, workspace, B, H, L, d_key, nu, d_v, chunk, eps, status, st);
+    const int BH = B * H;
+    const int nch = (L + chunk - 1) / chunk;
+    const int d_dot = 2 * d_key * nu;
+    const int Dp = padded_ddot(d_dot);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const PrepArgs pa = prep_args(q, k, v, beta, ws, L, chunk, nch, nu, Dp, d_v, d_v, eps, status);
+    {
+        unsigned *flags = reinterpret_cast<unsigned *>(ws + records_bytes(BH, nch, Dp, d_v));
+        const ScanArgs sa = scan_args(W0, W_final, nullptr, nullptr, y, ws, flags, L, chunk, nch, d_v, d_v, d_dot,
+                                      Dp, status);
+        cudaError_t e = cudaErrorNotSupported;
+        switch (d_key) {
+        case 8: e = launch_fused_bufs<8>(pa, sa, flags, BH, num_sms, st); break;
+        case 16: e = launch_fused_bufs<16>(pa, sa, flags, BH, num_sms, st); break;
+        case 32: e = launch_fused_bufs<32>(pa, sa, flags, BH, num_sms, st); break;
+        case 64: e = launch_fused_bufs<64>(pa, sa, flags, BH, num_sms, st); break;
+        case 128: e = launch_fused_bufs<128>(pa, sa, flags, BH, num_sms, st); break;
+        default: return cudaErrorInvalidValue;
+        }
+        if (e != cudaErrorNotSupported)
+            return e;
+    }
+    const cudaError_t e = prep_dispatch<false>(pa, BH, d_key, st);
     if (e != cudaSuccess)
         return e;
-    return tc_scan_launch(workspace, W0, W_final, y, B, H, L, d_key, nu, d_v, chunk, num_sms, status, st);
+    const ScanArgs sa = scan_args(W0, W_final, nullptr, nullptr, y, ws, nullptr, L, chunk, nch, d_v, d_v, d_dot, Dp,
+                                  status);
+    return scan_dispatch(sa, BH, num_sms, false, st);
 }
 
 // ------------------------------------------------ the sum rule (linear attention)
@@ -1095,7 +1529,7 @@ bool tc_linear_supported(int d_key, int nu, int d_v, int chunk, int normalize) {
         return false;
     if (chunk < 1 || chunk > kTile)
         return false;
-    return fits(padded_ddot(2 * d_key * nu), d_v + (normalize ? 16 : 0), normalize ? 32 : kDVB);
+    return fits(padded_ddot(2 * d_key * nu), d_v + (normalize ? 16 : 0), normalize || wide_scan(d_v) ? 32 : 16);
 }
 
 size_t tc_linear_workspace_bytes(int B, int H, int L, int d_key, int nu, int d_v, int chunk, int normalize) {
@@ -1112,22 +1546,22 @@ cudaError_t tc_linear_launch(const void *q, const void *k, const void *v, const 
                              float *W_final, float *z_final, void *y, void *workspace, int B, int H, int L,
                              int d_key, int nu, int d_v, int chunk, int normalize, float eps, int num_sms,
                              unsigned *status, cudaStream_t st) {
-    (void)num_sms;
     const int dv2 = d_v + (normalize ? 16 : 0);
-    cudaError_t e = prep_dispatch<true>(q, k, v, nullptr, workspace, B, H, L, d_key, nu, dv2, d_v, chunk, eps,
-                                        status, st);
-    if (e != cudaSuccess)
-        return e;
     const int BH = B * H;
     const int nch = (L + chunk - 1) / chunk;
     const int d_dot = 2 * d_key * nu;
     const int Dp = padded_ddot(d_dot);
-    const uint8_t *ws = static_cast<const uint8_t *>(workspace);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const PrepArgs pa = prep_args(q, k, v, nullptr, ws, L, chunk, nch, nu, Dp, dv2, d_v, eps, status);
+    cudaError_t e = prep_dispatch<true>(pa, BH, d_key, st);
+    if (e != cudaSuccess)
+        return e;
     if (normalize)
-        return launch_scan_bufs<32, true>(W0, W_final, z0, z_final, y, ws, BH, L, chunk, nch, dv2, d_v, d_dot, Dp,
-                                          status, st);
-    return launch_scan_bufs<kDVB, false>(W0, W_final, nullptr, nullptr, y, ws, BH, L, chunk, nch, d_v, d_v, d_dot,
-                                         Dp, status, st);
+        return launch_scan_bufs<32, 128, true>(
+            scan_args(W0, W_final, z0, z_final, y, ws, nullptr, L, chunk, nch, dv2, d_v, d_dot, Dp, status), BH, st);
+    return scan_dispatch(scan_args(W0, W_final, nullptr, nullptr, y, ws, nullptr, L, chunk, nch, d_v, d_v, d_dot, Dp,
+                                   status),
+                         BH, num_sms, false, st);
 }
 
 } // namespace fw

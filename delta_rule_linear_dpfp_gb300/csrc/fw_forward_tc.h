@@ -24,7 +24,13 @@ cudaError_t tc_prepare_launch(const void *q, const void *k, const void *v, const
 cudaError_t tc_scan_launch(const void *workspace, const float *W0, float *W_final, void *y, int B, int H, int L,
                            int d_key, int nu, int d_v, int chunk, int num_sms, unsigned *status, cudaStream_t st);
 
-// Enqueue the bf16 forward: both phases (arguments validated by the caller).
+// Kernels tc_forward_launch enqueues for this shape: 1 (one cooperative
+// launch, the flags zeroed by a memset before it), 2 (prep, then scan), or
+// -1 on a CUDA error.
+int tc_forward_kernel_count(int B, int H, int L, int d_key, int nu, int d_v, int chunk, int num_sms);
+
+// Enqueue the bf16 forward: both phases (arguments validated by the caller),
+// as one launch or as the two kernels.
 cudaError_t tc_forward_launch(const void *q, const void *k, const void *v, const void *beta,
                               const float *W0, float *W_final, void *y, void *workspace, int B,
                               int H, int L, int d_key, int nu, int d_v, int chunk, float eps,

@@ -140,6 +140,21 @@ FW_API int fw_delta_forward(const void *q, const void *k, const void *v, const v
                             int d_v, int chunk, int io_dtype, float eps, void *stream);
 
 /*
+ * How many of this library's kernels fw_delta_forward enqueues for this shape
+ * on the current device.  (An engineering query: the pages have no
+ * counterpart.)  With bf16 I/O the forward has two phases -- preparing every
+ * chunk, then walking the chunks in order -- run either as two kernels (2) or
+ * as one cooperative launch in which the walk overlaps the rest of the
+ * preparation (1; a memset of the workspace's ready flags precedes it).  The
+ * one launch is taken where the preparation needs more than one wave of CTAs
+ * and the walking CTAs leave SMs free; both give the same bits.  fp32 I/O: 1.
+ * 0 when nothing is launched (B*H == 0 or L == 0); -1 for arguments
+ * fw_delta_forward would reject, or a CUDA error.
+ */
+FW_API int fw_delta_forward_kernel_count(int B, int H, int L, int d_key, int nu, int d_v, int chunk,
+                                         int io_dtype);
+
+/*
  * Bytes of device workspace fw_delta_forward_projected needs (0 for
  * arguments it would reject).  The caller allocates it.
  */

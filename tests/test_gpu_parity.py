@@ -192,20 +192,33 @@ def test_forward_memory_passing_back_to_back():
     assert maxrel(f64(Ws[-1]), f64(W)) <= 2e-2
 
 
-def test_prepare_then_scan_equals_forward():
+# (B, H, L, d_key, nu, d_v, chunk, W0): the first two are one-wave preps (two
+# kernels), the rest have more chunks than the prep covers in one wave, which
+# the forward runs as one launch with the prep and the walk overlapped.
+PHASE_CASES = [(2, 4, 200, 64, 2, 64, 64, True), (4, 8, 512, 64, 1, 64, 64, False),
+               (2, 8, 2048, 64, 3, 64, 64, True), (2, 4, 2560, 64, 2, 32, 64, False),
+               (4, 8, 1280, 64, 1, 64, 64, True), (1, 4, 3000, 32, 3, 128, 32, True)]
+
+
+@pytest.mark.parametrize("case", PHASE_CASES, ids=lambda c: "B{}H{}L{}dk{}nu{}dv{}C{}".format(*c[:7]))
+def test_prepare_then_scan_equals_forward(case):
     """The two phases, enqueued one after the other, give exactly what the
-    one-call forward gives (same kernels, same arithmetic)."""
-    for (B, H, L, nu, w0) in [(2, 4, 200, 2, True), (4, 8, 512, 1, False)]:
-        d = to_dev(inputs.random_forward_inputs(B, H, L, 64, nu, 64, "bf16", 0.01 if w0 else None, seed=L))
-        y, Wf = fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=d["W0"], nu=nu, chunk=64)
-        need = fw.fw_delta_forward_workspace_size(B, H, L, 64, nu, 64, 64, torch.bfloat16)
-        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
-        y2 = torch.empty_like(y)
-        W2 = torch.empty_like(Wf)
-        fw.fw_delta_forward_prepare(d["q"], d["k"], d["v"], d["beta"], ws, nu=nu, chunk=64)
-        fw.fw_delta_forward_scan(ws, y2, W0=d["W0"], W_final=W2, nu=nu, chunk=64)
-        torch.cuda.synchronize()
-        assert torch.equal(y, y2) and torch.equal(Wf, W2)
+    one-call forward gives, whether that call runs them as the same two
+    kernels or as one launch (same arithmetic either way)."""
+    B, H, L, d_key, nu, d_v, C, w0 = case
+    launches = fw.fw_delta_forward_kernel_count(B, H, L, d_key, nu, d_v, C, torch.bfloat16)
+    assert launches == (2 if PHASE_CASES.index(case) < 2 else 1), launches
+    d = to_dev(inputs.random_forward_inputs(B, H, L, d_key, nu, d_v, "bf16", 0.01 if w0 else None, seed=L))
+    y, Wf = fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=d["W0"], nu=nu, chunk=C)
+    need = fw.fw_delta_forward_workspace_size(B, H, L, d_key, nu, d_v, C, torch.bfloat16)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    y2 = torch.empty_like(y)
+    W2 = torch.empty_like(Wf)
+    fw.fw_delta_forward_prepare(d["q"], d["k"], d["v"], d["beta"], ws, nu=nu, chunk=C)
+    fw.fw_delta_forward_scan(ws, y2, W0=d["W0"], W_final=W2, nu=nu, chunk=C)
+    torch.cuda.synchronize()
+    assert fw.fw_device_status() == fw.FW_OK
+    assert torch.equal(y, y2) and torch.equal(Wf, W2)
 
 
 # ---------------------------------------------------------------- K3 decode
