@@ -880,9 +880,11 @@ FW_DEV void scan_walk(const ScanArgs &g, uint8_t *smem, int vblk, int64_t bh, in
     // Thread 0's bookkeeping of the bulk loads: images issued and images
     // waited for (its own waits), and the ready flags acquired (FUSED).
     int a_issued = 0, a_waited = 0, k_issued = 0, k_waited = 0, acquired = 0;
-    // FUSED: the flag of chunk `acquired` is read one chunk ahead (an acquire
-    // load whose value is only looked at when the chunk is needed, so the
-    // round trip to L2 stays off the serial path); ahead_v = that value.
+    // FUSED: the flag of chunk `acquired` is read one chunk ahead, by an
+    // acquire load issued while thread 0 waits for its MMA3 anyway (an
+    // acquire holds back the thread's later memory accesses until it returns,
+    // so anywhere else it would stall the serial path); ahead_v = its value,
+    // looked at when the chunk is needed.
     unsigned ahead_v = 0;
     bool ahead = false;
     const unsigned *fl = FUSED ? g.flags + (size_t)bh * nch : nullptr;
@@ -890,6 +892,7 @@ FW_DEV void scan_walk(const ScanArgs &g, uint8_t *smem, int vblk, int64_t bh, in
         if constexpr (FUSED) {
             if (acquired < nch) {
                 ahead_v = flag_load(fl + acquired);
+                asm volatile("fence.proxy.async.global;" ::: "memory"); // later bulk copies after it
                 ahead = true;
             }
         }
@@ -899,7 +902,7 @@ FW_DEV void scan_walk(const ScanArgs &g, uint8_t *smem, int vblk, int64_t bh, in
         if constexpr (FUSED) {
             for (; acquired <= cc && acquired < nch; ++acquired) {
                 if (ahead && ahead_v != 0) {
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    // acquired (and proxy-fenced) when it was read
                 } else if (!flag_wait(fl + acquired, status)) {
                     return false;
                 }
@@ -1081,6 +1084,8 @@ FW_DEV void scan_walk(const ScanArgs &g, uint8_t *smem, int vblk, int64_t bh, in
                          desc_sw128(ut_s + (uint32_t)s * 2048u, 8192, 1024), idesc,
                          (s > 0 || c > 0 || has_w0) ? 1u : 0u);
             mma_commit(bar_m3);
+            if (tid == 0)
+                read_ahead(); // the flag needed after the next MMA1
         }
         ok = mbar_wait(bar_m3, m3_phase, status);
         m3_phase ^= 1;
@@ -1089,11 +1094,8 @@ FW_DEV void scan_walk(const ScanArgs &g, uint8_t *smem, int vblk, int64_t bh, in
             break;
         }
         tc_fence_after();
-        if (tid == 0) {
-            if (c + NKB < nch) // this K buffer is consumed: fetch a later chunk's
-                fetch_k(c + NKB);
-            read_ahead();      // the next chunk's flag, looked at after its MMA1
-        }
+        if (tid == 0 && c + NKB < nch) // this K buffer is consumed: fetch a later chunk's
+            fetch_k(c + NKB);
         for (int mb = 0; mb < MB; ++mb) {
             const int d = 128 * mb + row;
             float sv[CPT];
