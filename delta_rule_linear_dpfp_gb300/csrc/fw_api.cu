@@ -462,7 +462,7 @@ FW_API int fw_delta_forward_prepare(const void *q, const void *k, const void *v,
     if (device_info(&di) != cudaSuccess)
         return FW_ERR_CUDA;
     return cuda_status(fw::tc_prepare_launch(q, k, v, beta, workspace, B, H, L, d_key, nu, d_v, chunk, eps,
-                                             di.status, static_cast<cudaStream_t>(stream)));
+                                             di.num_sms, di.status, static_cast<cudaStream_t>(stream)));
 }
 
 FW_API int fw_delta_forward_scan(const void *workspace, size_t workspace_bytes, const float *W0,

@@ -680,6 +680,106 @@ teardown:
     return !__syncthreads_or(!ok);
 }
 
+// Ready flags of the single-launch forward: flag (b,h, c) is set once chunk
+// c's record of (b,h) is complete.  The writer orders every write of the
+// record (bulk copies included) before a release store; the reader's acquire
+// load orders every later read, bulk copies included, after it.
+FW_DEV void flag_set(unsigned *f) {
+    asm volatile("fence.proxy.async.global;" ::: "memory"); // bulk-copy writes before the release
+    __threadfence();
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
+}
+FW_DEV unsigned flag_load(const unsigned *f) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+// Bounded wait for a flag (false after kWaitLimitNs, with kStatusTimeout
+// recorded); on success later bulk copies observe what the writer released.
+FW_DEV bool flag_wait(const unsigned *f, unsigned *status) {
+    bool ok = flag_load(f) != 0;
+    if (!ok) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t i = 1;; ++i) {
+            __nanosleep(100);
+            if (flag_load(f) != 0) {
+                ok = true;
+                break;
+            }
+            if ((i & 31) == 0 && globaltimer_ns() - t0 > kWaitLimitNs)
+                break;
+        }
+    }
+    if (!ok) {
+        record_status(status, kStatusTimeout);
+        return false;
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
+// Pull chunk c of (b,h)'s q, k and v rows into L2 (a prefetch: no data
+// reaches the thread, and L2 is the point of coherence).
+template <int DK>
+FW_DEV void prep_prefetch(const PrepArgs &g, int c, int64_t bh) {
+    const int t0 = c * g.C, Lc = min(g.C, g.L - t0);
+    const size_t tok = (size_t)bh * g.L + t0;
+    l2_prefetch(g.k + tok * DK, (uint32_t)(Lc * DK * 2));
+    l2_prefetch(g.q + tok * DK, (uint32_t)(Lc * DK * 2));
+    if ((g.d_vr * 2) % 16 == 0)
+        l2_prefetch(g.v + tok * g.d_vr, (uint32_t)(Lc * g.d_vr * 2));
+}
+
+// A persistent prep CTA: chunks job0, job0 + stride, ... in chunk-major
+// order (job = c * BH + bh), each prepared as one chunk_prep_kernel CTA
+// prepares it, the next chunk's rows pulled into L2 while the current one is
+// worked out.  flags (or null): chunk c of (b,h)'s ready flag, set once its
+// record is complete.  False if a wait gave up.
+template <int DK, bool SUM>
+FW_DEV bool prep_jobs(const PrepArgs &g, const PrepSmem &m, int BH, int job0, int stride, unsigned *flags,
+                      int tid) {
+    const int jobs = BH * g.nch;
+    prep_init<SUM>(m, g.Dp, g.d_v, tid);
+    uint32_t parity = 0;
+    bool ok = true;
+    for (int job = job0; job < jobs; job += stride, parity ^= 1u) {
+        const int c = job / BH;
+        const int64_t bh = job % BH;
+        if (tid == 0 && job + stride < jobs)
+            prep_prefetch<DK>(g, (job + stride) / BH, (job + stride) % BH);
+        PrepRegs<DK> r;
+        prep_load<DK, SUM>(g, c, bh, tid, r);
+        if (!prep_compute<DK, SUM>(g, m, r, c, bh, parity, tid)) {
+            ok = false;
+            break;
+        }
+        if (flags && tid == 0)
+            flag_set(flags + (size_t)bh * g.nch + c);
+    }
+    if ((tid >> 5) == 0)
+        tmem_dealloc(*m.slot, prep_tmem_cols(g.Dp, g.d_v));
+    return ok;
+}
+
+// The prep as a persistent grid (where the chunks need more than one wave of
+// chunk_prep_kernel CTAs): CTA i prepares chunks i, i + gridDim.x, ...
+template <int DK, bool SUM>
+__global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_persistent_kernel(PrepArgs g, int BH) {
+    extern __shared__ uint8_t smem_raw[];
+    const PrepSmem m = prep_layout(align1024(smem_raw), g.Dp);
+    const int tid = threadIdx.x;
+    if (tid == 0 && (int)blockIdx.x < BH * g.nch) // the first chunk's rows while the preceding kernel finishes
+        prep_prefetch<DK>(g, (int)blockIdx.x / BH, (int)blockIdx.x % BH);
+    griddep_wait(); // the inputs may be, and the workspace may still be read by, the preceding kernel
+    PrepArgs a = g;
+    a.q = after_wait(a.q);
+    a.k = after_wait(a.k);
+    a.v = after_wait(a.v);
+    a.beta = after_wait(a.beta);
+    griddep_launch_dependents();
+    prep_jobs<DK, SUM>(a, m, BH, (int)blockIdx.x, (int)gridDim.x, nullptr, tid);
+}
+
 template <int DK, bool SUM>
 __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(PrepArgs g) {
     extern __shared__ uint8_t smem_raw[];
@@ -721,44 +821,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(PrepArgs g)
 // value channels (64-column blocks `blk` bytes apart).
 FW_DEV uint32_t vtile_chunk(int row, int j0, uint32_t blk) {
     return (uint32_t)(j0 >> 6) * blk + (uint32_t)row * 128u + ((uint32_t)(((j0 & 63) >> 3) ^ (row & 7)) << 4);
-}
-
-// Ready flags of the single-launch forward: flag (b,h, c) is set once chunk
-// c's record of (b,h) is complete.  The writer orders every write of the
-// record (bulk copies included) before a release store; the reader's acquire
-// load orders every later read, bulk copies included, after it.
-FW_DEV void flag_set(unsigned *f) {
-    asm volatile("fence.proxy.async.global;" ::: "memory"); // bulk-copy writes before the release
-    __threadfence();
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
-}
-FW_DEV unsigned flag_load(const unsigned *f) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
-    return v;
-}
-// Bounded wait for a flag (false after kWaitLimitNs, with kStatusTimeout
-// recorded); on success later bulk copies observe what the writer released.
-FW_DEV bool flag_wait(const unsigned *f, unsigned *status) {
-    bool ok = flag_load(f) != 0;
-    if (!ok) {
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t i = 1;; ++i) {
-            __nanosleep(100);
-            if (flag_load(f) != 0) {
-                ok = true;
-                break;
-            }
-            if ((i & 31) == 0 && globaltimer_ns() - t0 > kWaitLimitNs)
-                break;
-        }
-    }
-    if (!ok) {
-        record_status(status, kStatusTimeout);
-        return false;
-    }
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    return true;
 }
 
 struct ScanArgs {
@@ -1157,23 +1219,9 @@ __global__ void __launch_bounds__(NTH, 1) chunk_fused_kernel(PrepArgs pa, ScanAr
         scan_walk<DVB, NTH, NKB, NA, false, true>(sa, smem, (int)blockIdx.x % nvb, (int)blockIdx.x / nvb, tid);
         return;
     }
-    const PrepSmem m = prep_layout(smem, pa.Dp);
-    const int nprep = (int)gridDim.x - nscan, BH = nscan / nvb;
-    const int jobs = BH * pa.nch;
-    prep_init<false>(m, pa.Dp, pa.d_v, tid);
-    uint32_t parity = 0;
-    for (int job = (int)blockIdx.x - nscan; job < jobs; job += nprep, parity ^= 1u) {
-        const int c = job / BH;
-        const int64_t bh = job % BH;
-        PrepRegs<DK> r;
-        prep_load<DK, false>(pa, c, bh, tid, r);
-        if (!prep_compute<DK, false>(pa, m, r, c, bh, parity, tid))
-            break;
-        if (tid == 0)
-            flag_set(flags + (size_t)bh * pa.nch + c);
-    }
-    if ((tid >> 5) == 0)
-        tmem_dealloc(*m.slot, prep_tmem_cols(pa.Dp, pa.d_v));
+    const int BH = nscan / nvb;
+    prep_jobs<DK, false>(pa, prep_layout(smem, pa.Dp), BH, (int)blockIdx.x - nscan, (int)gridDim.x - nscan, flags,
+                         tid);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1199,6 +1247,25 @@ template <typename K> cudaError_t set_smem(K kern, size_t bytes) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     return e;
+}
+
+// Prep CTAs resident per SM: shared memory, tensor memory (512 columns per
+// SM) and registers (the kernel is built for two CTAs of 256 threads).
+// Counted here: the runtime's occupancy query reports one CTA per SM for
+// this kernel whatever its resources, while two do run at once.
+cudaError_t prep_ctas_per_sm(int Dp, int d_v, int *per_sm) {
+    int dev = 0, smem_sm = 0, rsv = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e != cudaSuccess)
+        return e;
+    const int by_smem = (int)((size_t)smem_sm / (prep_smem(Dp, d_v) + (size_t)rsv));
+    const int by_tmem = 512 / (int)prep_tmem_cols(Dp, d_v);
+    *per_sm = std::max(1, std::min(std::min(by_smem, by_tmem), 2));
+    return cudaSuccess;
 }
 
 bool fits(int Dp, int d_v, int dvb) {
@@ -1263,11 +1330,26 @@ ScanArgs scan_args(const float *W0, float *Wf, const float *z0, float *zf, void 
     return a;
 }
 
+// One CTA per chunk where every chunk's CTA is resident at once; otherwise
+// a persistent grid of as many CTAs as the GPU holds, each looping over
+// chunks (same arithmetic per chunk).
 template <int DK, bool SUM>
-cudaError_t launch_prep(const PrepArgs &a, int BH, cudaStream_t st) {
+cudaError_t launch_prep(const PrepArgs &a, int BH, int num_sms, cudaStream_t st) {
     const size_t smem = prep_smem(a.Dp, a.d_v);
+    int per_sm = 0;
+    cudaError_t e = prep_ctas_per_sm(a.Dp, a.d_v, &per_sm);
+    if (e != cudaSuccess)
+        return e;
+    const long long jobs = (long long)BH * a.nch, resident = (long long)per_sm * num_sms;
+    if (num_sms > 0 && jobs > resident) {
+        auto kern = chunk_prep_persistent_kernel<DK, SUM>;
+        e = set_smem(kern, smem);
+        if (e != cudaSuccess)
+            return e;
+        return launch_pdl(kern, dim3((unsigned)resident), dim3(kPrepThreads), smem, st, a, BH);
+    }
     auto kern = chunk_prep_kernel<DK, SUM>;
-    cudaError_t e = set_smem(kern, smem);
+    e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;
     return launch_pdl(kern, dim3((unsigned)a.nch, (unsigned)BH), dim3(kPrepThreads), smem, st, a);
@@ -1310,21 +1392,10 @@ cudaError_t fused_plan(int BH, int nch, int Dp, int d_v, int num_sms, int *grid,
         return cudaErrorNotSupported;
     const long long jobs = (long long)BH * nch;
     {
-        // prep CTAs per SM: shared memory, tensor memory (512 columns per SM)
-        // and registers (the kernel is built for two CTAs of 256 threads).
-        // Counted here: the runtime's occupancy query reports one CTA per SM
-        // for this kernel whatever its resources, while two do run at once.
-        int dev = 0, smem_sm = 0, rsv = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess)
-            e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-        if (e == cudaSuccess)
-            e = cudaDeviceGetAttribute(&rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        int prep_per_sm = 0;
+        const cudaError_t e = prep_ctas_per_sm(Dp, d_v, &prep_per_sm);
         if (e != cudaSuccess)
             return e;
-        const int by_smem = (int)((size_t)smem_sm / (prep_smem(Dp, d_v) + (size_t)rsv));
-        const int by_tmem = 512 / (int)prep_tmem_cols(Dp, d_v);
-        const int prep_per_sm = std::min(std::min(by_smem, by_tmem), 2);
         if (jobs <= (long long)prep_per_sm * num_sms)
             return cudaErrorNotSupported;
     }
@@ -1414,13 +1485,13 @@ size_t tc_forward_workspace_bytes(int B, int H, int L, int d_key, int nu, int d_
 namespace {
 
 template <bool SUM>
-cudaError_t prep_dispatch(const PrepArgs &a, int BH, int d_key, cudaStream_t st) {
+cudaError_t prep_dispatch(const PrepArgs &a, int BH, int d_key, int num_sms, cudaStream_t st) {
     switch (d_key) {
-    case 8: return launch_prep<8, SUM>(a, BH, st);
-    case 16: return launch_prep<16, SUM>(a, BH, st);
-    case 32: return launch_prep<32, SUM>(a, BH, st);
-    case 64: return launch_prep<64, SUM>(a, BH, st);
-    case 128: return launch_prep<128, SUM>(a, BH, st);
+    case 8: return launch_prep<8, SUM>(a, BH, num_sms, st);
+    case 16: return launch_prep<16, SUM>(a, BH, num_sms, st);
+    case 32: return launch_prep<32, SUM>(a, BH, num_sms, st);
+    case 64: return launch_prep<64, SUM>(a, BH, num_sms, st);
+    case 128: return launch_prep<128, SUM>(a, BH, num_sms, st);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -1461,12 +1532,12 @@ cudaError_t forward_plan(int B, int H, int L, int d_key, int nu, int d_v, int ch
 } // namespace
 
 cudaError_t tc_prepare_launch(const void *q, const void *k, const void *v, const void *beta, void *workspace,
-                              int B, int H, int L, int d_key, int nu, int d_v, int chunk, float eps,
+                              int B, int H, int L, int d_key, int nu, int d_v, int chunk, float eps, int num_sms,
                               unsigned *status, cudaStream_t st) {
     const int nch = (L + chunk - 1) / chunk;
     const PrepArgs a = prep_args(q, k, v, beta, static_cast<uint8_t *>(workspace), L, chunk, nch, nu,
                                  padded_ddot(2 * d_key * nu), d_v, d_v, eps, status);
-    return prep_dispatch<false>(a, B * H, d_key, st);
+    return prep_dispatch<false>(a, B * H, d_key, num_sms, st);
 }
 
 cudaError_t tc_scan_launch(const void *workspace, const float *W0, float *W_final, void *y, int B, int H, int L,
@@ -1515,7 +1586,7 @@ cudaError_t tc_forward_launch(const void *q, const void *k, const void *v, const
         if (e != cudaErrorNotSupported)
             return e;
     }
-    const cudaError_t e = prep_dispatch<false>(pa, BH, d_key, st);
+    const cudaError_t e = prep_dispatch<false>(pa, BH, d_key, num_sms, st);
     if (e != cudaSuccess)
         return e;
     const ScanArgs sa = scan_args(W0, W_final, nullptr, nullptr, y, ws, nullptr, L, chunk, nch, d_v, d_v, d_dot, Dp,
@@ -1555,7 +1626,7 @@ cudaError_t tc_linear_launch(const void *q, const void *k, const void *v, const 
     const int Dp = padded_ddot(d_dot);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const PrepArgs pa = prep_args(q, k, v, nullptr, ws, L, chunk, nch, nu, Dp, dv2, d_v, eps, status);
-    cudaError_t e = prep_dispatch<true>(pa, BH, d_key, st);
+    cudaError_t e = prep_dispatch<true>(pa, BH, d_key, num_sms, st);
     if (e != cudaSuccess)
         return e;
     if (normalize)

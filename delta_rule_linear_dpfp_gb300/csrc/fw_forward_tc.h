@@ -19,7 +19,7 @@ size_t tc_forward_workspace_bytes(int B, int H, int L, int d_key, int nu, int d_
 // The two phases of the bf16 forward (arguments validated by the caller):
 // per-chunk preparation into the workspace, then the serial state scan.
 cudaError_t tc_prepare_launch(const void *q, const void *k, const void *v, const void *beta, void *workspace,
-                              int B, int H, int L, int d_key, int nu, int d_v, int chunk, float eps,
+                              int B, int H, int L, int d_key, int nu, int d_v, int chunk, float eps, int num_sms,
                               unsigned *status, cudaStream_t st);
 cudaError_t tc_scan_launch(const void *workspace, const float *W0, float *W_final, void *y, int B, int H, int L,
                            int d_key, int nu, int d_v, int chunk, int num_sms, unsigned *status, cudaStream_t st);
