@@ -280,6 +280,18 @@ FW_API int fw_delta_forward_projected(const void *x, const void *W_all, int ldw,
     if (e != cudaSuccess)
         return FW_ERR_CUDA;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
+    // Where the forward runs as its two kernels, the projections are folded
+    // into the first (q, k, v and beta never reach global memory): two
+    // launches from x.  Otherwise the projection GEMM, then the forward.
+    if (fw::tc_prepare_x_supported(d_key, d_v) &&
+        fw::tc_forward_kernel_count(B, H, L, d_key, nu, d_v, chunk, di.num_sms) == 2) {
+        e = fw::tc_prepare_x_launch(x, W_all, ldw, ws + pl.fwd, B, H, L, d_model, d_key, nu, d_v, chunk, eps,
+                                    di.num_sms, di.status, st);
+        if (e != cudaSuccess)
+            return cuda_status(e);
+        return cuda_status(fw::tc_scan_launch(ws + pl.fwd, W0, W_final, y, B, H, L, d_key, nu, d_v, chunk,
+                                              di.num_sms, di.status, st));
+    }
     e = fw::launch_project(x, W_all, ldw, ws + pl.q, ws + pl.k, ws + pl.v, ws + pl.beta, B, L, H, d_key, d_v, d_model,
                            ws + pl.scratch, di.status, st);
     if (e != cudaSuccess)

@@ -285,9 +285,17 @@ struct PrepSmem {
     uint32_t *slot;  // TMEM base address
 };
 
+// The barriers and the TMEM slot take the first kPrepHead bytes (the
+// projection prologue of chunk_prep_x_kernel keeps its own barriers there
+// too, and streams its operands through the space after them).
+constexpr int kPrepHead = 1024;
 FW_DEV PrepSmem prep_layout(uint8_t *smem, int Dp) {
     PrepSmem m;
-    m.kq = smem;
+    m.bar_g = (uint64_t *)smem;
+    m.bar_i = m.bar_g + 1;
+    m.bar_f = m.bar_g + 2;
+    m.slot = (uint32_t *)(m.bar_g + 3);
+    m.kq = smem + kPrepHead;
     m.ip = m.kq + 256 * Dp;
     m.tt = m.ip + 16384;
     m.Am = (float *)(m.tt + 8192);
@@ -295,10 +303,6 @@ FW_DEV PrepSmem prep_layout(uint8_t *smem, int Dp) {
     m.Rm = m.Nm + 64 * LDS;
     m.bs = m.Rm + 16 * LDS;
     m.vt = (uint8_t *)m.Am;
-    m.bar_g = (uint64_t *)(m.bs + 64);
-    m.bar_i = m.bar_g + 1;
-    m.bar_f = m.bar_g + 2;
-    m.slot = (uint32_t *)(m.bar_g + 3);
     return m;
 }
 
@@ -816,6 +820,224 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(PrepArgs g)
 }
 
 // ---------------------------------------------------------------------------
+// The projection prologue folded into the prep (the attention module's
+// bias-free projections of the Fast Weights Transformer guide, section
+// "module structure": q, k, v = x W, beta = sigmoid(x w_beta)) for one chunk
+// of one head:
+//   P = x[the chunk's rows] [W_q | W_k | W_v | W_beta](head h's columns)
+// K (d_model) is walked in steps of 64 through a ring of NS stages of TMA copies
+// placed after the prep's barrier block (the prep's own tiles are not in use
+// yet): the chunk's 64 rows of x (K-major) and three 64 x 64 boxes of W_all
+// (MN-major), head h's q, k and v columns.  Warp 1 issues q | k and warp 2
+// v (N = 128 and 64, one accumulator each); the MMAs take M = 128 rows of x,
+// the 64 past the box being the stage's next bytes, whose products land in
+// accumulator lanes nobody reads.  Warps 4 and 5 meanwhile form beta's
+// pre-activation x w_beta on CUDA cores from the same x rows (one thread per
+// row, w_beta's column staged once).  P is rounded to bf16 (beta through the
+// sigmoid first), as launch_project rounds it, into a staging area in the
+// fp32 work space, from which the prep takes its inputs instead of global
+// memory; the prep then runs as in chunk_prep_kernel.
+constexpr int kXStage = 8192 + 3 * 8192; // one K step: the x box and three W boxes
+
+struct ProjCols {
+    int q, k, v, b; // first column of the q, k, v parts of W_all and of its beta columns
+    int ldw;        // row stride of W_all (elements)
+};
+
+// The staged bf16 rows (k and q [64][DK], v [64][d_vr]) keep each row's
+// 16-byte chunks in the order chunk ^ (row % chunks per row), so that the
+// 16-byte stores of eight consecutive rows (one row per thread) fall in
+// different banks.
+FW_DEV int staged_chunk(int row, int c8, int chunks) { return row * chunks + (c8 ^ (row & (chunks - 1))); }
+
+// prep_load's registers, from the staged bf16 rows and beta [64].
+template <int DK>
+FW_DEV void prep_load_staged(const __nv_bfloat16 *kst, const __nv_bfloat16 *qst, const __nv_bfloat16 *vst,
+                             const __nv_bfloat16 *bst, int Lc, int d_vr, int tid, PrepRegs<DK> &r) {
+    using R = PrepRegs<DK>;
+    static_assert(R::kHalfRows, "d_key <= 64");
+    const int warp = tid >> 5, lane = tid & 31;
+    const int hr = 16 * warp + ((lane & 7) | ((lane >> 4) << 3));
+    const int t = hr & 63;
+    const uint4 *src = reinterpret_cast<const uint4 *>(hr < 64 ? kst : qst);
+#pragma unroll
+    for (int c8 = 0; c8 < R::kRaw; ++c8)
+        r.raw[c8] = t < Lc ? src[staged_chunk(t, c8, R::kRaw)] : make_uint4(0, 0, 0, 0);
+    const int vcpr = d_vr / 8;
+#pragma unroll
+    for (int i = 0; i < R::kVChunks; ++i) {
+        const int idx = tid + i * kPrepThreads, tt = idx / vcpr, j8 = idx % vcpr;
+        r.vpre[i] = (idx < 64 * vcpr && tt < Lc) ? reinterpret_cast<const uint4 *>(vst)[staged_chunk(tt, j8, vcpr)]
+                                                 : make_uint4(0, 0, 0, 0);
+    }
+    r.beta_t = (tid < Lc && tid < 64) ? __bfloat162float(bst[tid]) : 0.f;
+}
+
+template <int DK, int NS>
+__global__ void __launch_bounds__(kPrepThreads, 2)
+    chunk_prep_x_kernel(PrepArgs g, const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw,
+                        int d_model, int H, ProjCols pc, const __nv_bfloat16 *W_all) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const PrepSmem m = prep_layout(smem, g.Dp);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + 32); // [NS] a stage's copies landed
+    uint64_t *empty = full + NS;                                // [NS] a stage is read (2 MMA issuers + 2 beta warps)
+    uint64_t *pdone = full + 2 * NS;                            // every projection MMA is done
+    uint8_t *ring = smem + kPrepHead;
+    float *wb = reinterpret_cast<float *>(ring + NS * kXStage); // w_beta's column of head h [d_model]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x;
+    const int64_t bh = blockIdx.y;
+    const int b = (int)(bh / H), h = (int)(bh % H);
+    const int t0 = c * g.C, Lc = min(g.C, g.L - t0);
+    const int nk = d_model / 64;
+
+    prep_init<false>(m, g.Dp, g.d_v, tid);
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 4);
+        }
+        mbar_init(pdone, 2);
+        fence_barrier_init();
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tx)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tw)) : "memory");
+    }
+    griddep_wait(); // x and W_all may be, and the workspace may still be read by, the preceding kernel
+    griddep_launch_dependents();
+    W_all = after_wait(W_all);
+    // the copies of K step i (thread 0: the ring's first stages go out before
+    // anything else, the rest as the stages free up)
+    const int row0 = b * g.L + t0; // x row of the chunk's first token
+    auto issue = [&](int i) {
+        const int s = i % NS;
+        uint8_t *st = ring + s * kXStage;
+        mbar_arrive_expect_tx(full + s, kXStage);
+        tma_load_2d(st, &tx, 64 * i, row0, full + s);
+        tma_load_2d(st + 8192, &tw, pc.q + h * DK, 64 * i, full + s);
+        tma_load_2d(st + 16384, &tw, pc.k + h * DK, 64 * i, full + s);
+        tma_load_2d(st + 24576, &tw, pc.v + h * g.d_vr, 64 * i, full + s);
+    };
+    if (tid == 0)
+        for (int i = 0; i < min(NS, nk); ++i)
+            issue(i);
+    for (int j = tid; j < d_model; j += kPrepThreads)
+        wb[j] = __bfloat162float(__ldcg(W_all + (size_t)j * pc.ldw + pc.b + h));
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *m.slot;
+
+    bool ok = true;
+    float zb = 0.f; // beta's pre-activation of this thread's row (warps 4 and 5)
+    if (warp == 0 && lane == 0) {          // producer: the rest of the copies
+        int issued = min(NS, nk);
+        for (int i = NS; i < nk; ++i) {
+            if (!mbar_wait(empty + i % NS, (uint32_t)((i / NS - 1) & 1), g.status)) {
+                ok = false;
+                break;
+            }
+            issue(i);
+            issued = i + 1;
+        }
+        // before the ring is reused or the CTA leaves, every copy issued has landed (bounded)
+        for (int i = max(0, issued - NS); i < issued; ++i)
+            mbar_wait(full + i % NS, (uint32_t)((i / NS) & 1), g.status);
+    } else if ((warp == 1 || warp == 2) && lane == 0) { // warp 1: q | k, warp 2: v
+        const uint32_t idesc = idesc_bf16(128, warp == 1 ? 128 : 64, 0, 1);
+        const uint32_t acc = tm + (uint32_t)(128 * (warp - 1));
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % NS;
+            if (!mbar_wait(full + s, (uint32_t)((i / NS) & 1), g.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a = smem_u32(ring + s * kXStage);
+            const uint32_t w = a + 8192u + (uint32_t)(warp - 1) * 16384u;
+#pragma unroll
+            for (int st = 0; st < 4; ++st)
+                mma_bf16(acc, desc_sw128(a + kmajor_step(st, 128), 16, 1024),
+                         desc_sw128(w + (uint32_t)st * 2048u, 8192, 1024), idesc, (i > 0 || st > 0) ? 1u : 0u);
+            mma_commit(empty + s);
+        }
+        mma_commit(pdone);
+    } else if (warp == 4 || warp == 5) {   // beta's pre-activation, one row of x per thread
+        const int row = tid - 128;
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % NS;
+            if (!mbar_wait(full + s, (uint32_t)((i / NS) & 1), g.status)) {
+                ok = false;
+                break;
+            }
+            const uint8_t *xr = ring + s * kXStage + row * 128; // the box's row: 8 swizzled 16-byte chunks
+            const float *w = wb + 64 * i;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float xv[8];
+                unpack8(*reinterpret_cast<const uint4 *>(xr + ((c8 ^ (row & 7)) << 4)), xv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    zb = fmaf(xv[e], w[8 * c8 + e], zb);
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(empty + s);
+        }
+    }
+    __syncwarp();
+    ok = mbar_wait(pdone, 0, g.status) && ok;
+    tc_fence_after();
+    if (__syncthreads_or(!ok)) {
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0)
+            tmem_dealloc(tm, prep_tmem_cols(g.Dp, g.d_v));
+        return;
+    }
+    // P (rows = the chunk's tokens, lanes 0..63) to the bf16 staging area:
+    // warps 0 and 1 the q | k columns, warps 4 and 5 the v | beta columns
+    __nv_bfloat16 *kst = reinterpret_cast<__nv_bfloat16 *>(m.Am);
+    __nv_bfloat16 *qst = kst + 64 * DK;
+    __nv_bfloat16 *vst = qst + 64 * DK;
+    __nv_bfloat16 *bst = vst + 64 * g.d_vr;
+    if ((warp & 3) < 2) {
+        const int row = 32 * (warp & 3) + lane, half = warp >> 2;
+        const uint32_t lb = tmem_lane_base(warp);
+        constexpr int KC = DK / 8;
+        const int vcpr = g.d_vr / 8;
+        if (half == 1)
+            bst[row] = __float2bfloat16_rn(1.0f / (1.0f + expf(-zb)));
+        for (int c0 = 0; c0 < (half ? 64 : 128); c0 += 64) { // four loads in flight, then one wait
+            float p[64];
+#pragma unroll
+            for (int j = 0; j < 64; j += 16)
+                tmem_ld16(tm + lb + (uint32_t)(128 * half + c0 + j), p + j);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e8 = 0; e8 < 64; e8 += 8) {
+                const int col = c0 + e8; // first of 8 columns
+                if (half == 0) {
+                    if (col < DK)
+                        reinterpret_cast<uint4 *>(qst)[staged_chunk(row, col / 8, KC)] = pack8(p + e8);
+                    else if (col >= 64 && col - 64 < DK)
+                        reinterpret_cast<uint4 *>(kst)[staged_chunk(row, (col - 64) / 8, KC)] = pack8(p + e8);
+                } else if (col < g.d_vr) {
+                    reinterpret_cast<uint4 *>(vst)[staged_chunk(row, col / 8, vcpr)] = pack8(p + e8);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    PrepRegs<DK> r;
+    prep_load_staged<DK>(kst, qst, vst, bst, Lc, g.d_vr, tid, r);
+    prep_compute<DK, false>(g, m, r, c, bh, 0, tid);
+    if (warp == 0)
+        tmem_dealloc(tm, prep_tmem_cols(g.Dp, g.d_v));
+}
+
+// ---------------------------------------------------------------------------
 // 16-byte chunk holding columns j0 .. j0+7 of row `row` of an MN-major SW128
 // operand tile whose rows are the contraction index and whose columns are
 // value channels (64-column blocks `blk` bytes apart).
@@ -1228,7 +1450,7 @@ __global__ void __launch_bounds__(NTH, 1) chunk_fused_kernel(PrepArgs pa, ScanAr
 size_t prep_smem(int Dp, int d_v) {
     const int VB = (d_v + 63) / 64;
     (void)VB; // the V tile (<= 16 KB) reuses the fp32 work space (37 KB)
-    return (size_t)256 * Dp + 16384 + 8192 + (2 * 64 + 16) * LDS * 4 + 64 * 4 + 32 + 1024;
+    return (size_t)kPrepHead + 256 * Dp + 16384 + 8192 + (2 * 64 + 16) * LDS * 4 + 64 * 4 + 1024;
 }
 
 size_t scan_smem(int Dp, int dvb, int nkb, int na) {
@@ -1592,6 +1814,63 @@ cudaError_t tc_forward_launch(const void *q, const void *k, const void *v, const
     const ScanArgs sa = scan_args(W0, W_final, nullptr, nullptr, y, ws, nullptr, L, chunk, nch, d_v, d_v, d_dot, Dp,
                                   status);
     return scan_dispatch(sa, BH, num_sms, false, st);
+}
+
+// ------------------------------------------------ the prep from x (projections folded in)
+bool tc_prepare_x_supported(int d_key, int d_v) { return d_key <= 64 && d_v <= 64; }
+
+namespace {
+
+template <int DK, int NS>
+cudaError_t launch_prep_x(const PrepArgs &a, const CUtensorMap &tx, const CUtensorMap &tw, int BH, int d_model,
+                          int H, ProjCols pc, const __nv_bfloat16 *W_all, cudaStream_t st) {
+    const size_t smem =
+        std::max(prep_smem(a.Dp, a.d_v), (size_t)kPrepHead + (size_t)NS * kXStage + 4 * (size_t)d_model + 1024);
+    auto kern = chunk_prep_x_kernel<DK, NS>;
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(kern, dim3((unsigned)a.nch, (unsigned)BH), dim3(kPrepThreads), smem, st, a, tx, tw, d_model,
+                      H, pc, W_all);
+}
+
+} // namespace
+
+template <int DK>
+cudaError_t launch_prep_x_stages(const PrepArgs &a, const CUtensorMap &tx, const CUtensorMap &tw, int BH,
+                                 int d_model, int H, ProjCols pc, const __nv_bfloat16 *W_all, int num_sms,
+                                 cudaStream_t st) {
+    // four stages in flight where every CTA has an SM to itself (the ring
+    // then costs the second CTA per SM nothing), else two
+    if ((long long)a.nch * BH <= num_sms)
+        return launch_prep_x<DK, 4>(a, tx, tw, BH, d_model, H, pc, W_all, st);
+    return launch_prep_x<DK, 2>(a, tx, tw, BH, d_model, H, pc, W_all, st);
+}
+
+cudaError_t tc_prepare_x_launch(const void *x, const void *W_all, int ldw, void *workspace, int B, int H, int L,
+                                int d_model, int d_key, int nu, int d_v, int chunk, float eps, int num_sms,
+                                unsigned *status, cudaStream_t st) {
+    if (!tc_prepare_x_supported(d_key, d_v))
+        return cudaErrorInvalidValue;
+    const int N = H * (2 * d_key + d_v + 1);
+    CUtensorMap tx, tw;
+    cudaError_t e = make_bf16_map(&tx, x, B * L, d_model, d_model, 64);
+    if (e == cudaSuccess)
+        e = make_bf16_map(&tw, W_all, d_model, N, ldw, 64);
+    if (e != cudaSuccess)
+        return e;
+    const int nch = (L + chunk - 1) / chunk;
+    const PrepArgs a = prep_args(nullptr, nullptr, nullptr, nullptr, static_cast<uint8_t *>(workspace), L, chunk, nch,
+                                 nu, padded_ddot(2 * d_key * nu), d_v, d_v, eps, status);
+    const ProjCols pc = {0, H * d_key, 2 * H * d_key, H * (2 * d_key + d_v), ldw};
+    const __nv_bfloat16 *w = static_cast<const __nv_bfloat16 *>(W_all);
+    switch (d_key) {
+    case 8: return launch_prep_x_stages<8>(a, tx, tw, B * H, d_model, H, pc, w, num_sms, st);
+    case 16: return launch_prep_x_stages<16>(a, tx, tw, B * H, d_model, H, pc, w, num_sms, st);
+    case 32: return launch_prep_x_stages<32>(a, tx, tw, B * H, d_model, H, pc, w, num_sms, st);
+    case 64: return launch_prep_x_stages<64>(a, tx, tw, B * H, d_model, H, pc, w, num_sms, st);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 // ------------------------------------------------ the sum rule (linear attention)

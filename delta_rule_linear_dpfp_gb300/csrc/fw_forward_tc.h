@@ -1,5 +1,6 @@
 // fw_forward_tc.h -- host interface of the bf16 chunked forward (tcgen05).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -35,6 +36,20 @@ cudaError_t tc_forward_launch(const void *q, const void *k, const void *v, const
                               const float *W0, float *W_final, void *y, void *workspace, int B,
                               int H, int L, int d_key, int nu, int d_v, int chunk, float eps,
                               int num_sms, unsigned *status, cudaStream_t st);
+
+// The prep with the projection prologue folded in: q, k, v and beta of each
+// chunk computed from x [B*L, d_model] and W_all [d_model, ldw] (the layout
+// launch_project reads) inside the prep kernel, then the records written as
+// tc_prepare_launch writes them.  d_key <= 64, d_v <= 64, d_model % 64 == 0;
+// x and W_all 16-byte aligned (arguments validated by the caller).
+bool tc_prepare_x_supported(int d_key, int d_v);
+cudaError_t tc_prepare_x_launch(const void *x, const void *W_all, int ldw, void *workspace, int B, int H, int L,
+                                int d_model, int d_key, int nu, int d_v, int chunk, float eps, int num_sms,
+                                unsigned *status, cudaStream_t st);
+
+// A 2-D TMA map of a row-major bf16 matrix [rows, cols] (row stride ld
+// elements) in boxes of box_rows x 64 columns, 128-byte swizzle.
+cudaError_t make_bf16_map(CUtensorMap *map, const void *base, int rows, int cols, int ld, int box_rows);
 
 // The sum rule (linear attention), bf16 I/O: W_i = W_{i-1} + v_i phi(k_i)^T,
 // y_i = W_i phi(q_i), divided by z_i . phi(q_i) (z_i = sum of phi(k)) when

@@ -138,14 +138,6 @@ FW_DEV void finish16(const GemmOut &o, const float *acc, int m, int n, int N) {
     }
 }
 
-// 2-D TMA tensor copy of one box into shared memory, completion counted on
-// `bar` in bytes.  x is the inner (contiguous) coordinate.
-FW_DEV void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-                 ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-                 : "memory");
-}
-
 // grid (M tiles, N tiles, K slices); K slice z covers K steps
 // [z * per, min(nk, (z + 1) * per)) of 64.  part: [slices][M tiles * 128][N
 // tiles * 128] fp32 partial tiles (used with slices > 1 only).
@@ -348,6 +340,10 @@ cudaError_t make_map(CUtensorMap *map, const void *base, int rows, int cols, int
 }
 
 } // namespace
+
+cudaError_t make_bf16_map(CUtensorMap *map, const void *base, int rows, int cols, int ld, int box_rows) {
+    return make_map(map, base, rows, cols, ld, box_rows);
+}
 
 int gemm_slices(int M, int N, int K) {
     const int tiles = ((M + 127) / 128) * ((N + 127) / 128), nk = K / 64;

@@ -76,6 +76,12 @@ FW_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *status) {
     return mbar_wait_ns(bar, parity, status, kWaitLimitNs);
 }
 
+// A plain arrival (release: this thread's earlier shared-memory accesses are
+// ordered before it).
+FW_DEV void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 FW_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
@@ -88,6 +94,16 @@ FW_DEV void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) 
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_u32(dst)),
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 2-D TMA tensor copy of one box into shared memory, completion counted on
+// `bar` in bytes.  x is the inner (contiguous) coordinate; x times the
+// element size must be a multiple of 16 bytes.  `map` is a CUtensorMap
+// (kernel parameter or global memory).
+FW_DEV void tma_load_2d(void *dst, const void *map, int x, int y, uint64_t *bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
                  : "memory");
 }
 

@@ -31,7 +31,16 @@ CASES = [  # B, H, L, d_model, d_key, d_v, nu, w0
     (2, 4, 200, 128, 32, 64, 2, True),       # ragged token count (400) and column count (516)
     (1, 2, 77, 64, 16, 16, 3, False),
     (3, 3, 50, 192, 64, 32, 1, True),
+    (1, 8, 4096, 512, 64, 64, 1, True),      # the forward as one launch: the separate projection GEMM first
+    (1, 2, 300, 256, 128, 64, 1, False),     # d_key 128: the separate projection GEMM first
 ]
+
+
+def test_projected_path_choice():
+    """The projections are folded into the prep where the forward runs as its
+    two kernels (d_key, d_v <= 64); otherwise they run as a GEMM first."""
+    assert fw.fw_delta_forward_kernel_count(1, 8, 1024, 64, 1, 64, 64, torch.bfloat16) == 2
+    assert fw.fw_delta_forward_kernel_count(1, 8, 4096, 64, 1, 64, 64, torch.bfloat16) == 1
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "b{}h{}l{}dm{}dk{}dv{}nu{}w{}".format(*c))
