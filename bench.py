@@ -608,7 +608,7 @@ def measure_rows(fw, inputs, dev, stream, pk):
     r = roofline("fw_linear_forward (prepare + scan)", flops, nbytes, ms, pk)
     r["tokens/s"] = B * L / (ms * 1e-3)
     rows["linear_b4h8_l512_normalised"] = r
-    # the projected workload from x: projection prologue (tcgen05 GEMM) + the chunked forward
+    # the projected workload from x: the projections folded into the prep, then the scan
     B, H, L, d_model, d_key, d_v, nu, C = 1, 8, 1024, 512, 64, 64, 1, 64
     d_dot = 2 * d_key * nu
     lx = inputs.layer_inputs(B, H, L, d_model, d_key, d_v)
@@ -622,7 +622,9 @@ def measure_rows(fw, inputs, dev, stream, pk):
     N = H * (2 * d_key + d_v + 1)
     flops = 2.0 * B * L * d_model * N + forward_flops_per_head_token(C, d_dot, d_v) * B * H * L
     nbytes = B * L * d_model * 2 + d_model * N * 2 + B * H * L * d_v * 2 + B * H * d_v * d_dot * 4
-    r = roofline("fw_delta_forward_projected (projection + prepare + scan)", flops, nbytes, ms, pk)
+    launches = fw.fw_delta_forward_kernel_count(B, H, L, d_key, nu, d_v, C, torch.bfloat16)
+    r = roofline("fw_delta_forward_projected (prep from x + scan)" if launches == 2 and d_key <= 64 and d_v <= 64
+                 else "fw_delta_forward_projected (projection GEMM + forward)", flops, nbytes, ms, pk)
     r["tokens/s"] = B * L / (ms * 1e-3)
     rows["projected_b1h8_l1024_dmodel512"] = r
     # the backward of the delta rule on the bench workload (dq, dk, dv, dbeta, dW0 from dy)

@@ -177,12 +177,19 @@ FW_API size_t fw_delta_forward_projected_workspace_size(int B, int L, int d_mode
  *              rounded up to 8 (the padding columns are read, not used)
  *   W0, W_final, y, chunk, eps : as for fw_delta_forward (y [B, H, L, d_v])
  *   workspace: device scratch of fw_delta_forward_projected_workspace_size()
- *              bytes: the projected q, k, v, beta, then the forward's
+ *              bytes: room for the projected q, k, v, beta, then the
+ *              forward's workspace
  * q, k, v and beta are rounded to bf16 once (fp32 accumulation).
  * Errors as for fw_delta_forward; FW_ERR_INVALID_ARG also for d_model not a
- * multiple of 64 or a bad ldw.  The projections' GEMM (with a reduction
- * kernel after it when B L is small and K is split across CTAs), then the
- * forward's two kernels, chained by programmatic dependent launch.
+ * multiple of 64 or a bad ldw.
+ * Kernels: where fw_delta_forward_kernel_count() of the shape is 2 and
+ * d_key, d_v <= 64, the projections run inside the forward's first kernel
+ * (each chunk's prep computes its own rows of q, k, v and beta from x with
+ * TMA-fed tensor-core MMAs; they never reach global memory), then the walk
+ * over the chunks: two launches from x.  Otherwise the projections' GEMM
+ * (with a reduction kernel after it when B L is small and K is split across
+ * CTAs) writes q, k, v, beta to the workspace and fw_delta_forward follows.
+ * Launches are chained by programmatic dependent launch.
  */
 FW_API int fw_delta_forward_projected(const void *x, const void *W_all, int ldw, const float *W0,
                                       float *W_final, void *y, void *workspace, size_t workspace_bytes,
