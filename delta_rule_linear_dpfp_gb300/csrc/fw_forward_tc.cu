@@ -116,15 +116,15 @@ __host__ __device__ inline uint32_t tmem_cols_pow2(int need) {
 // 128-byte rows, 16-byte chunks swizzled by k & 7).
 FW_DEV uint32_t ttile_chunk(int kk, int n) { return (uint32_t)kk * 128u + ((uint32_t)((n >> 3) ^ (kk & 7)) << 4); }
 
-// (I + A)^-1 for a strictly lower 64 x 64 A, by 16 x 16 blocks:
-//   diagonal blocks by forward substitution (one column per thread), then
-//   block row I: N_IJ = -N_II * sum_{K=J}^{I-1} A_IK N_KJ   (J < I).
-// A, N: [64][LDS]; R: [16][LDS] scratch; all 16-byte aligned.  Only the
-// blocks on and below the diagonal of N are written (the ones above are
-// zero and never read here).  As each block of N is final it also goes out,
-// times beta of its column, in bf16 to the T operand tile tt (T = N diag(beta));
-// the blocks above the diagonal are written as zeros.  NT threads (>= 256);
-// ends synchronised.
+// (I + A)^-1 for a strictly lower 64 x 64 A: the four 16 x 16 diagonal
+// blocks by forward substitution (one column per thread), then the blocks
+// below the diagonal by doubling (16 -> 32 -> 64, below).
+// A, N: [64][LDS]; R: [16][LDS] scratch (used as [32][32]); all 16-byte
+// aligned.  Only the blocks on and below the diagonal of N are written (the
+// ones above are zero and never read here).  As each block of N is final it
+// also goes out, times beta of its column, in bf16 to the T operand tile tt
+// (T = N diag(beta)); the blocks above the diagonal are written as zeros.
+// NT threads (>= 256); ends synchronised.
 template <int NT>
 FW_DEV void unit_lower_inverse(const float *A, float *N, float *R, const float *bs, uint8_t *tt, int tid) {
     if (tid < 64) {
@@ -153,57 +153,105 @@ FW_DEV void unit_lower_inverse(const float *A, float *N, float *R, const float *
         *reinterpret_cast<uint4 *>(tt + ttile_chunk(kk, n0)) = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
-    // off-diagonal blocks; each thread computes 4 adjacent outputs of a row
-    // from 16-byte loads, so every A (or N) element it loads feeds 4 FMAs
-    for (int I = 1; I < 4; ++I) {
-        for (int idx = tid; idx < 64 * I; idx += NT) {
-            const int J = idx >> 6, ii = (idx >> 2) & 15, j0 = 16 * J + 4 * (idx & 3);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int K = J; K < I; ++K) {
-                const float *ar = A + (16 * I + ii) * LDS + 16 * K;
+    // The blocks below the diagonal by doubling the block size: with
+    // P = (I + A_11)^-1 and Q = (I + A_22)^-1 known for the two diagonal
+    // blocks of a 2 x 2 partition, (I + A)^-1 = [P 0; -Q A_21 P  Q].  Level 1
+    // takes the two 32 x 32 diagonal blocks at once (16 x 16 halves), level 2
+    // the whole 64 x 64; each level is two products, R = A_21 P, then
+    // -Q R.  Each thread computes 4 adjacent outputs of a row from 16-byte
+    // loads, so every A (or N) element it loads feeds 4 FMAs.  R is used as
+    // [32][32].  Only blocks on and below the diagonal of N are read.
+    auto t_out = [&](int kk, int j0, float4 v) { // N row kk, columns j0..j0+3 -> N and the T tile
+        *reinterpret_cast<float4 *>(N + kk * LDS + j0) = v;
+        uint2 t4;
+        t4.x = pack_bf16x2(v.x * bs[j0], v.y * bs[j0 + 1]);
+        t4.y = pack_bf16x2(v.z * bs[j0 + 2], v.w * bs[j0 + 3]);
+        *reinterpret_cast<uint2 *>(tt + ttile_chunk(kk, j0) + 2 * (j0 & 7)) = t4;
+    };
+    // level 1: blocks b = 0, 1 of 32 rows; R_b = A_{2b+1,2b} N_{2b,2b} (16 x 16)
+    const int b1 = tid >> 6, i1 = (tid >> 2) & 15, j1 = 4 * (tid & 3);
+    if (tid < 128) {
+        const int c0 = 32 * b1, r0 = c0 + 16;
+        const float *ar = A + (r0 + i1) * LDS + c0;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int s4 = 0; s4 < 16; s4 += 4) {
-                    const float4 a = *reinterpret_cast<const float4 *>(ar + s4);
-                    const float av[4] = {a.x, a.y, a.z, a.w};
+        for (int s4 = 0; s4 < 16; s4 += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(ar + s4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float4 n = *reinterpret_cast<const float4 *>(N + (16 * K + s4 + e) * LDS + j0);
-                        acc.x = fmaf(av[e], n.x, acc.x);
-                        acc.y = fmaf(av[e], n.y, acc.y);
-                        acc.z = fmaf(av[e], n.z, acc.z);
-                        acc.w = fmaf(av[e], n.w, acc.w);
-                    }
-                }
+            for (int e = 0; e < 4; ++e) {
+                const float4 n = *reinterpret_cast<const float4 *>(N + (c0 + s4 + e) * LDS + c0 + j1);
+                acc.x = fmaf(av[e], n.x, acc.x);
+                acc.y = fmaf(av[e], n.y, acc.y);
+                acc.z = fmaf(av[e], n.z, acc.z);
+                acc.w = fmaf(av[e], n.w, acc.w);
             }
-            *reinterpret_cast<float4 *>(R + ii * LDS + j0) = acc;
         }
-        __syncthreads();
-        for (int idx = tid; idx < 64 * I; idx += NT) {
-            const int ii = (idx >> 2) & 15, j0 = 16 * (idx >> 6) + 4 * (idx & 3);
-            const float *nr = N + (16 * I + ii) * LDS + 16 * I;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int s4 = 0; s4 < 16; s4 += 4) {
-                const float4 nn = *reinterpret_cast<const float4 *>(nr + s4);
-                const float nv[4] = {nn.x, nn.y, nn.z, nn.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 r = *reinterpret_cast<const float4 *>(R + (s4 + e) * LDS + j0);
-                    acc.x = fmaf(nv[e], r.x, acc.x);
-                    acc.y = fmaf(nv[e], r.y, acc.y);
-                    acc.z = fmaf(nv[e], r.z, acc.z);
-                    acc.w = fmaf(nv[e], r.w, acc.w);
-                }
-            }
-            const int kk = 16 * I + ii;
-            *reinterpret_cast<float4 *>(N + kk * LDS + j0) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-            uint2 t4;
-            t4.x = pack_bf16x2(-acc.x * bs[j0], -acc.y * bs[j0 + 1]);
-            t4.y = pack_bf16x2(-acc.z * bs[j0 + 2], -acc.w * bs[j0 + 3]);
-            *reinterpret_cast<uint2 *>(tt + ttile_chunk(kk, j0) + 2 * (j0 & 7)) = t4;
-        }
-        __syncthreads();
+        *reinterpret_cast<float4 *>(R + (16 * b1 + i1) * 32 + j1) = acc;
     }
+    __syncthreads();
+    // N_{2b+1,2b} = -N_{2b+1,2b+1} R_b
+    if (tid < 128) {
+        const int c0 = 32 * b1, r0 = c0 + 16;
+        const float *nr = N + (r0 + i1) * LDS + r0;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s4 = 0; s4 < 16; s4 += 4) {
+            const float4 nn = *reinterpret_cast<const float4 *>(nr + s4);
+            const float nv[4] = {nn.x, nn.y, nn.z, nn.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 r = *reinterpret_cast<const float4 *>(R + (16 * b1 + s4 + e) * 32 + j1);
+                acc.x = fmaf(nv[e], r.x, acc.x);
+                acc.y = fmaf(nv[e], r.y, acc.y);
+                acc.z = fmaf(nv[e], r.z, acc.z);
+                acc.w = fmaf(nv[e], r.w, acc.w);
+            }
+        }
+        t_out(r0 + i1, c0 + j1, make_float4(-acc.x, -acc.y, -acc.z, -acc.w));
+    }
+    __syncthreads();
+    // level 2: R = A[32:64, 0:32] P with P = N[0:32, 0:32] (its block (0, 1)
+    // is above the diagonal: columns 16..31 sum over rows 16..31 only)
+    const int i2 = tid >> 3, j2 = 4 * (tid & 7);
+    if (tid < 256) {
+        const float *ar = A + (32 + i2) * LDS;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k4 = j2 >= 16 ? 16 : 0; k4 < 32; k4 += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(ar + k4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 n = *reinterpret_cast<const float4 *>(N + (k4 + e) * LDS + j2);
+                acc.x = fmaf(av[e], n.x, acc.x);
+                acc.y = fmaf(av[e], n.y, acc.y);
+                acc.z = fmaf(av[e], n.z, acc.z);
+                acc.w = fmaf(av[e], n.w, acc.w);
+            }
+        }
+        *reinterpret_cast<float4 *>(R + i2 * 32 + j2) = acc;
+    }
+    __syncthreads();
+    // N[32:64, 0:32] = -Q R with Q = N[32:64, 32:64] (rows 0..15 of Q sum
+    // over its columns 0..15 only)
+    if (tid < 256) {
+        const float *nr = N + (32 + i2) * LDS + 32;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k4 = 0; k4 < (i2 < 16 ? 16 : 32); k4 += 4) {
+            const float4 nn = *reinterpret_cast<const float4 *>(nr + k4);
+            const float nv[4] = {nn.x, nn.y, nn.z, nn.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 r = *reinterpret_cast<const float4 *>(R + (k4 + e) * 32 + j2);
+                acc.x = fmaf(nv[e], r.x, acc.x);
+                acc.y = fmaf(nv[e], r.y, acc.y);
+                acc.z = fmaf(nv[e], r.z, acc.z);
+                acc.w = fmaf(nv[e], r.w, acc.w);
+            }
+        }
+        t_out(32 + i2, j2, make_float4(-acc.x, -acc.y, -acc.z, -acc.w));
+    }
+    __syncthreads();
 }
 
 // ---------------------------------------------------------------------------
@@ -326,7 +374,7 @@ template <int DK> struct PrepRegs {
     static constexpr int kVChunks = 4; // 64 * 128 / 8 / kPrepThreads
     uint4 raw[kRaw];
     uint4 vpre[kVChunks];
-    float beta_t;
+    __nv_bfloat16 beta_raw; // converted only where it is stored, so its load's latency is not waited for early
 };
 
 // Global loads of chunk c of (b,h), all in flight before any is used.
@@ -362,9 +410,9 @@ FW_DEV void prep_load(const PrepArgs &g, int c, int64_t bh, int tid, PrepRegs<DK
         if (idx < 64 * vcpr && t < Lc)
             r.vpre[i] = __ldcg(reinterpret_cast<const uint4 *>(g.v + ((size_t)bh * g.L + t0 + t) * g.d_vr + j));
     }
-    r.beta_t = 0.f;
+    r.beta_raw = __float2bfloat16_rn(0.f);
     if (!SUM && tid < Lc && tid < 64)
-        r.beta_t = __bfloat162float(g.beta[bh * g.L + t0 + tid]);
+        r.beta_raw = g.beta[bh * g.L + t0 + tid];
 }
 
 // Barriers and tensor memory of a prep CTA (once per CTA; published by the
@@ -385,11 +433,12 @@ FW_DEV void prep_init(const PrepSmem &m, int Dp, int d_v, int tid) {
 
 // Chunk c of (b,h), from the DPFP to the record: [W'; Q'] and K images, U'
 // and Y'.  `parity` is the phase of this chunk on the CTA's three MMA
-// barriers (each completes once per chunk).  Ends with every bulk copy
-// complete and a CTA barrier; false if a wait gave up.
+// barriers (each completes once per chunk).  Ends with every bulk copy done
+// reading shared memory (and, with wait_writes, fully complete: before a
+// ready flag is set) and a CTA barrier; false if a wait gave up.
 template <int DK, bool SUM>
 FW_DEV bool prep_compute(const PrepArgs &g, const PrepSmem &m, const PrepRegs<DK> &regs, int c, int64_t bh,
-                         uint32_t parity, int tid) {
+                         uint32_t parity, int tid, bool wait_writes) {
     using R = PrepRegs<DK>;
     constexpr int G = R::G, RPW = R::RPW, N2 = 2 * DK;
     constexpr bool kHalfRows = R::kHalfRows;
@@ -399,7 +448,7 @@ FW_DEV bool prep_compute(const PrepArgs &g, const PrepSmem &m, const PrepRegs<DK
     uint64_t *bar_g = m.bar_g, *bar_i = m.bar_i, *bar_f = m.bar_f;
     const auto &raw = regs.raw;
     const auto &vpre = regs.vpre;
-    const float beta_t = regs.beta_t;
+
     const int nu = g.nu, Dp = g.Dp, d_v = g.d_v, d_vr = g.d_vr;
     const float eps = g.eps;
     unsigned *status = g.status;
@@ -445,7 +494,7 @@ FW_DEV bool prep_compute(const PrepArgs &g, const PrepSmem &m, const PrepRegs<DK
         }
     }
     if (tid < 64)
-        bs[tid] = beta_t; // 0 on padded rows
+        bs[tid] = __bfloat162float(regs.beta_raw); // 0 on padded rows
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -663,11 +712,16 @@ FW_DEV bool prep_compute(const PrepArgs &g, const PrepSmem &m, const PrepRegs<DK
         bulk_s2g(rec + rc.a, kq, 256u * (uint32_t)Dp);
         bulk_commit();
     }
-    // U' (rows < 64) and Y' (rows >= 64) go straight from registers to the
-    // record in fp32 as [d_v/4][64][4], so a warp's 16-byte stores are one
-    // contiguous run
+    // U' (rows < 64) and Y' (rows >= 64) in fp32 as the record's
+    // [d_v/4][64][4] blocks, U' then Y' (contiguous in the record): where they
+    // fit, staged in the fp32 work space (free once the last MMA has read V)
+    // and sent as one bulk copy; else stored from registers (16-byte stores,
+    // one contiguous run per warp)
     {
-        float *uy = reinterpret_cast<float *>(rec + (row < 64 ? rc.up : rc.yp)) + 4 * (row & 63);
+        const uint32_t uy_bytes = 512u * (uint32_t)d_v;
+        const bool staged = uy_bytes <= (uint32_t)((2 * 64 + 16) * LDS + 64) * 4u;
+        float *uy = staged ? Am + (row < 64 ? 0 : 64 * d_v) + 4 * (row & 63)
+                           : reinterpret_cast<float *>(rec + (row < 64 ? rc.up : rc.yp)) + 4 * (row & 63);
         for (int c0 = 16 * half; c0 < d_v; c0 += 32) {
             float w[16];
             tmem_ld16(tm + lb + (uint32_t)(Dp + c0), w);
@@ -676,10 +730,22 @@ FW_DEV bool prep_compute(const PrepArgs &g, const PrepSmem &m, const PrepRegs<DK
             for (int e = 0; e < 16; e += 4)
                 *reinterpret_cast<float4 *>(uy + 256 * ((c0 + e) >> 2)) = make_float4(w[e], w[e + 1], w[e + 2], w[e + 3]);
         }
+        if (staged) {
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                bulk_s2g(rec + rc.up, Am, uy_bytes);
+                bulk_commit();
+            }
+        }
     }
 teardown:
-    if (tid == 0)
-        bulk_wait_all(); // every bulk copy of the chunk is complete
+    if (tid == 0) {
+        if (wait_writes)
+            bulk_wait_all();  // every bulk copy of the chunk is complete
+        else
+            bulk_wait_read(); // the copies are done with shared memory (the writes land before the kernel ends)
+    }
     tc_fence_before();
     return !__syncthreads_or(!ok);
 }
@@ -753,7 +819,7 @@ FW_DEV bool prep_jobs(const PrepArgs &g, const PrepSmem &m, int BH, int job0, in
             prep_prefetch<DK>(g, (job + stride) / BH, (job + stride) % BH);
         PrepRegs<DK> r;
         prep_load<DK, SUM>(g, c, bh, tid, r);
-        if (!prep_compute<DK, SUM>(g, m, r, c, bh, parity, tid)) {
+        if (!prep_compute<DK, SUM>(g, m, r, c, bh, parity, tid, flags != nullptr)) {
             ok = false;
             break;
         }
@@ -814,7 +880,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(PrepArgs g)
     PrepRegs<DK> r;
     prep_load<DK, SUM>(a, c, bh, tid, r);
     prep_init<SUM>(m, a.Dp, a.d_v, tid);
-    prep_compute<DK, SUM>(a, m, r, c, bh, 0, tid);
+    prep_compute<DK, SUM>(a, m, r, c, bh, 0, tid, false);
     if ((tid >> 5) == 0)
         tmem_dealloc(*m.slot, prep_tmem_cols(a.Dp, a.d_v));
 }
@@ -870,7 +936,7 @@ FW_DEV void prep_load_staged(const __nv_bfloat16 *kst, const __nv_bfloat16 *qst,
         r.vpre[i] = (idx < 64 * vcpr && tt < Lc) ? reinterpret_cast<const uint4 *>(vst)[staged_chunk(tt, j8, vcpr)]
                                                  : make_uint4(0, 0, 0, 0);
     }
-    r.beta_t = (tid < Lc && tid < 64) ? __bfloat162float(bst[tid]) : 0.f;
+    r.beta_raw = (tid < Lc && tid < 64) ? bst[tid] : __float2bfloat16_rn(0.f);
 }
 
 template <int DK, int NS>
@@ -1032,7 +1098,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     __syncthreads();
     PrepRegs<DK> r;
     prep_load_staged<DK>(kst, qst, vst, bst, Lc, g.d_vr, tid, r);
-    prep_compute<DK, false>(g, m, r, c, bh, 0, tid);
+    prep_compute<DK, false>(g, m, r, c, bh, 0, tid, false);
     if (warp == 0)
         tmem_dealloc(tm, prep_tmem_cols(g.Dp, g.d_v));
 }
