@@ -55,6 +55,12 @@ def parse():
                    help="only run this many token steps of the 6-layer stack workload (for profilers), then exit")
     p.add_argument("--backward-steps", type=int, default=0,
                    help="only run this many backward calls on the b4h8_l512 workload (for profilers), then exit")
+    p.add_argument("--forward-steps", type=int, default=0,
+                   help="only run this many forward calls on --forward-workload (for profilers), then exit")
+    p.add_argument("--forward-workload", default="b4h8_l512", help="the workload of --forward-steps")
+    p.add_argument("--projected-steps", type=int, default=0,
+                   help="only run this many projected-forward calls on B1 H8 L1024 d_model 512 (for profilers), "
+                        "then exit")
     return p.parse_args()
 
 
@@ -734,6 +740,39 @@ def backward_only(steps):
     print(json.dumps({"backward_steps": steps, "launches_per_step": 6}))
 
 
+def forward_only(steps, name):
+    """`steps` fw_delta_forward calls on one of inputs.FORWARD_CONFIGS through
+    the public API, nothing else: the command the forward rows' profiles are
+    captured from."""
+    from delta_rule_linear_dpfp_gb300 import binding as fw, build, inputs
+    build.build()
+    fw.load()
+    c = inputs.FORWARD_CONFIGS[name]
+    B, H, L, d_key, nu, d_v, C = (c[n] for n in ("B", "H", "L", "d_key", "nu", "d_v", "chunk"))
+    d = {k: (None if v is None else v.cuda()) for k, v in inputs.forward_inputs(name).items()}
+    for _ in range(steps):
+        fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=d.get("W0"), nu=nu, chunk=C)
+    torch.cuda.synchronize()
+    print(json.dumps({"forward_steps": steps, "workload": name,
+                      "launches_per_step": fw.fw_delta_forward_kernel_count(B, H, L, d_key, nu, d_v, C,
+                                                                            torch.bfloat16)}))
+
+
+def projected_only(steps):
+    """`steps` fw_delta_forward_projected calls on B1 H8 L1024 d_model 512
+    through the public API, nothing else (the projected row's profile)."""
+    from delta_rule_linear_dpfp_gb300 import binding as fw, build, inputs
+    build.build()
+    fw.load()
+    B, H, L, d_model, d_key, d_v = 1, 8, 1024, 512, 64, 64
+    lx = inputs.layer_inputs(B, H, L, d_model, d_key, d_v)
+    x, W = lx["x"].cuda(), lx["W_all"].cuda()
+    for _ in range(steps):
+        fw.fw_delta_forward_projected(x, W, H, d_key, d_v)
+    torch.cuda.synchronize()
+    print(json.dumps({"projected_steps": steps}))
+
+
 # ------------------------------------------------------------ the oracle
 class OracleSample:
     """The fp64 CPU oracle on the host cores over a bounded sample of the
@@ -824,6 +863,12 @@ def main():
         return
     if args.backward_steps:
         backward_only(args.backward_steps)
+        return
+    if args.forward_steps:
+        forward_only(args.forward_steps, args.forward_workload)
+        return
+    if args.projected_steps:
+        projected_only(args.projected_steps)
         return
     if world > 1:
         torch.cuda.set_device(local_rank)
