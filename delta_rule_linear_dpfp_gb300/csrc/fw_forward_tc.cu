@@ -1167,6 +1167,7 @@ FW_DEV void scan_walk(const ScanArgs &g, uint8_t *smem, int vblk, int64_t bh, in
     uint64_t *bar_m1 = bar_a + 4;                     // MMA1 done (both issuers)
     uint64_t *bar_m3 = bar_a + 5;                     // MMA3 done (every block's issuer)
     uint32_t *slot = (uint32_t *)(bar_a + 6);
+    uint32_t *flag_ok = slot + 1;                     // FUSED: the acquiring thread's verdict
 
     const int warp = tid >> 5, row = tid & 127, col0 = (tid >> 7) * CPT;
     const int v0 = vblk * (ZN ? 16 : DVB);
@@ -1228,36 +1229,22 @@ FW_DEV void scan_walk(const ScanArgs &g, uint8_t *smem, int vblk, int64_t bh, in
     if (has_w0)
         tmem_st_wait();
     // Thread 0's bookkeeping of the bulk loads: images issued and images
-    // waited for (its own waits), and the ready flags acquired (FUSED).
-    int a_issued = 0, a_waited = 0, k_issued = 0, k_waited = 0, acquired = 0;
-    // FUSED: the flag of chunk `acquired` is read one chunk ahead, by an
-    // acquire load issued while thread 0 waits for its MMA3 anyway (an
-    // acquire holds back the thread's later memory accesses until it returns,
-    // so anywhere else it would stall the serial path); ahead_v = its value,
-    // looked at when the chunk is needed.
-    unsigned ahead_v = 0;
-    bool ahead = false;
+    // waited for (its own waits).
+    int a_issued = 0, a_waited = 0, k_issued = 0, k_waited = 0;
+    // FUSED: thread kAcq (lane 0 of warp 3, which issues no MMA) acquires the
+    // ready flags, while MMA1 runs: an acquire load holds back the thread's
+    // later memory accesses until it returns, and warp 3 only waits there.
+    // Its verdict goes to thread 0 through shared memory; the CTA barrier
+    // after MMA1 orders the acquire before thread 0's bulk copies (which a
+    // proxy fence then orders after it).
+    constexpr int kAcq = 96;
+    int acquired = 0; // thread kAcq: the flags of chunks 0 .. acquired - 1 are acquired
     const unsigned *fl = FUSED ? g.flags + (size_t)bh * nch : nullptr;
-    auto read_ahead = [&]() {
+    auto acquire_to = [&](int cc) -> bool { // thread kAcq
         if constexpr (FUSED) {
-            if (acquired < nch) {
-                ahead_v = flag_load(fl + acquired);
-                asm volatile("fence.proxy.async.global;" ::: "memory"); // later bulk copies after it
-                ahead = true;
-            }
-        }
-    };
-    // acquire the ready flags of chunks up to cc (thread 0)
-    auto acquire_to = [&](int cc) -> bool {
-        if constexpr (FUSED) {
-            for (; acquired <= cc && acquired < nch; ++acquired) {
-                if (ahead && ahead_v != 0) {
-                    // acquired (and proxy-fenced) when it was read
-                } else if (!flag_wait(fl + acquired, status)) {
+            for (; acquired <= cc && acquired < nch; ++acquired)
+                if (!flag_wait(fl + acquired, status))
                     return false;
-                }
-                ahead = false;
-            }
         }
         return true;
     };
@@ -1294,8 +1281,16 @@ FW_DEV void scan_walk(const ScanArgs &g, uint8_t *smem, int vblk, int64_t bh, in
         rec0 = wsr + (size_t)bh * nch * rc.bytes;
     }
     bool ok = true;
+    if constexpr (FUSED) { // the flags of the chunks the first loads read
+        if (tid == kAcq)
+            *flag_ok = acquire_to(NA == 2 || NKB == 2 ? 1 : 0) ? 1u : 0u;
+        __syncthreads();
+        if (tid == 0) {
+            ok = *flag_ok != 0;
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+    }
     if (tid == 0) { // chunk 0's [W'; Q'] and the first K image(s)
-        ok = acquire_to(NA == 2 || NKB == 2 ? 1 : 0);
         if (ok) {
             fetch_a(0);
             if (NA == 2 && nch > 1)
@@ -1345,6 +1340,9 @@ FW_DEV void scan_walk(const ScanArgs &g, uint8_t *smem, int vblk, int64_t bh, in
             break;
         }
 
+        // the flags of the chunks the loads after this MMA1 read (thread kAcq)
+        if (FUSED && tid == kAcq)
+            *flag_ok = acquire_to(c + (NA > NKB ? NA : NKB)) ? 1u : 0u;
         // MMA1: D1 = [W'; Q'] S^T, warp 0 over the first half of the
         // contraction into tD1, warp 1 over the second into tD1b
         if (lead && warp < 2) {
@@ -1363,11 +1361,16 @@ FW_DEV void scan_walk(const ScanArgs &g, uint8_t *smem, int vblk, int64_t bh, in
             break;
         }
         tc_fence_after();
-        // this [W'; Q'] buffer is consumed: fetch a later chunk's (thread 0,
-        // after the ready flags of the chunks the next loads read)
+        // this [W'; Q'] buffer is consumed: fetch a later chunk's at once
+        // (thread 0, once the ready flags of the chunks the next loads read
+        // are acquired): the image's load takes most of the time until the
+        // next MMA1
         bool ok_f = true;
         if (tid == 0) {
-            ok_f = acquire_to(c + (NA > NKB ? NA : NKB));
+            if constexpr (FUSED) {
+                ok_f = *flag_ok != 0;
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
             if (ok_f && c + NA < nch)
                 fetch_a(c + NA);
         }
@@ -1434,8 +1437,6 @@ FW_DEV void scan_walk(const ScanArgs &g, uint8_t *smem, int vblk, int64_t bh, in
                          desc_sw128(ut_s + (uint32_t)s * 2048u, 8192, 1024), idesc,
                          (s > 0 || c > 0 || has_w0) ? 1u : 0u);
             mma_commit(bar_m3);
-            if (tid == 0)
-                read_ahead(); // the flag needed after the next MMA1
         }
         ok = mbar_wait(bar_m3, m3_phase, status);
         m3_phase ^= 1;
