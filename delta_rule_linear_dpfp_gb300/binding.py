@@ -27,7 +27,8 @@ EXPORTS = ("fw_status_string", "fw_dpfp", "fw_delta_forward_workspace_size", "fw
            "fw_delta_forward_kernel_count",
            "fw_delta_decode_step", "fw_device_status", "fw_selftest_umma",
            "fw_delta_forward_noalloc", "fw_delta_forward_prepare", "fw_delta_forward_scan",
-           "fw_selftest_wait_timeout", "fw_linear_forward_workspace_size", "fw_linear_forward",
+           "fw_selftest_wait_timeout", "fw_selftest_flag_timeout", "fw_linear_forward_workspace_size",
+           "fw_linear_forward",
            "fw_delta_backward_workspace_size", "fw_delta_backward",
            "fw_delta_forward_projected_workspace_size", "fw_delta_forward_projected",
            "fw_decode_stack_workspace_size", "fw_decode_stack_step")
@@ -89,6 +90,8 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.fw_delta_forward_noalloc.argtypes = [vp] * 7 + [i32] * 8 + [f32, vp]
     lib.fw_selftest_wait_timeout.restype = i32
     lib.fw_selftest_wait_timeout.argtypes = [i32, vp]
+    lib.fw_selftest_flag_timeout.restype = i32
+    lib.fw_selftest_flag_timeout.argtypes = [i32, vp]
     lib.fw_linear_forward_workspace_size.restype = sz
     lib.fw_linear_forward_workspace_size.argtypes = [i32] * 9
     lib.fw_linear_forward.restype = i32
@@ -475,3 +478,8 @@ def fw_selftest_umma(A, B, a_mn: int = 0, b_mn: int = 0, swap_mn: int = 0, strea
 def fw_selftest_wait_timeout(limit_us: int = 2000, stream=None):
     """Run the bounded-wait failure path once (see include/fastweight_selftest.h)."""
     _check(load().fw_selftest_wait_timeout(int(limit_us), _stream(stream)), "fw_selftest_wait_timeout")
+
+
+def fw_selftest_flag_timeout(limit_us: int = 2000, stream=None):
+    """Run the ready-flag wait's failure path once (see include/fastweight_selftest.h)."""
+    _check(load().fw_selftest_flag_timeout(int(limit_us), _stream(stream)), "fw_selftest_flag_timeout")

@@ -750,44 +750,6 @@ teardown:
     return !__syncthreads_or(!ok);
 }
 
-// Ready flags of the single-launch forward: flag (b,h, c) is set once chunk
-// c's record of (b,h) is complete.  The writer orders every write of the
-// record (bulk copies included) before a release store; the reader's acquire
-// load orders every later read, bulk copies included, after it.
-FW_DEV void flag_set(unsigned *f) {
-    asm volatile("fence.proxy.async.global;" ::: "memory"); // bulk-copy writes before the release
-    __threadfence();
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
-}
-FW_DEV unsigned flag_load(const unsigned *f) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
-    return v;
-}
-// Bounded wait for a flag (false after kWaitLimitNs, with kStatusTimeout
-// recorded); on success later bulk copies observe what the writer released.
-FW_DEV bool flag_wait(const unsigned *f, unsigned *status) {
-    bool ok = flag_load(f) != 0;
-    if (!ok) {
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t i = 1;; ++i) {
-            __nanosleep(100);
-            if (flag_load(f) != 0) {
-                ok = true;
-                break;
-            }
-            if ((i & 31) == 0 && globaltimer_ns() - t0 > kWaitLimitNs)
-                break;
-        }
-    }
-    if (!ok) {
-        record_status(status, kStatusTimeout);
-        return false;
-    }
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    return true;
-}
-
 // Pull chunk c of (b,h)'s q, k and v rows into L2 (a prefetch: no data
 // reaches the thread, and L2 is the point of coherence).
 template <int DK>

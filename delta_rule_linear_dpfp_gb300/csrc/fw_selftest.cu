@@ -130,7 +130,26 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns, unsigned *status) {
     __syncthreads();
 }
 
+// A ready flag that nothing ever sets.
+__device__ unsigned g_selftest_flag;
+
+__global__ void flag_timeout_kernel(uint64_t limit_ns, unsigned *status) {
+    if (threadIdx.x == 0)
+        (void)flag_wait_ns(&g_selftest_flag, status, limit_ns);
+    __syncthreads();
+}
+
 } // namespace
+
+extern "C" FW_API int fw_selftest_flag_timeout(int limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > 100000)
+        return FW_ERR_INVALID_ARG;
+    unsigned *status = nullptr;
+    if (fw::status_word(&status) != cudaSuccess)
+        return FW_ERR_CUDA;
+    flag_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>((uint64_t)limit_us * 1000u, status);
+    return cudaGetLastError() == cudaSuccess ? FW_OK : FW_ERR_CUDA;
+}
 
 extern "C" FW_API int fw_selftest_wait_timeout(int limit_us, void *stream) {
     if (limit_us < 1 || limit_us > 100000)

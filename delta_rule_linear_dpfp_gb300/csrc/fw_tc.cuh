@@ -87,6 +87,47 @@ FW_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 
+// ------------------------------------------------------------ ready flags
+// A flag in global memory that one CTA sets once what it guards is complete
+// and another CTA of the same (cooperative) launch waits for.  The writer
+// orders every write it guards (bulk copies included) before a release
+// store; the reader's acquire load orders every later read, bulk copies
+// included, after it.
+FW_DEV void flag_set(unsigned *f) {
+    asm volatile("fence.proxy.async.global;" ::: "memory"); // bulk-copy writes before the release
+    __threadfence();
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
+}
+FW_DEV unsigned flag_load(const unsigned *f) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+// Bounded wait for a flag: false after limit_ns, with kStatusTimeout
+// recorded; on success later bulk copies observe what the writer released.
+FW_DEV bool flag_wait_ns(const unsigned *f, unsigned *status, uint64_t limit_ns) {
+    bool ok = flag_load(f) != 0;
+    if (!ok) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t i = 1;; ++i) {
+            __nanosleep(100);
+            if (flag_load(f) != 0) {
+                ok = true;
+                break;
+            }
+            if ((i & 31) == 0 && globaltimer_ns() - t0 > limit_ns)
+                break;
+        }
+    }
+    if (!ok) {
+        record_status(status, kStatusTimeout);
+        return false;
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+FW_DEV bool flag_wait(const unsigned *f, unsigned *status) { return flag_wait_ns(f, status, kWaitLimitNs); }
+
 // ------------------------------------------------ 1-D bulk copy (TMA engine)
 // global -> shared, completion counted on `bar` in bytes.  dst, src and
 // bytes must be multiples of 16.

@@ -44,6 +44,15 @@ FW_API int fw_selftest_umma(const float *A, const float *B, float *D, int N, int
  */
 FW_API int fw_selftest_wait_timeout(int limit_us, void *stream);
 
+/*
+ * fw_selftest_flag_timeout -- the same for the ready-flag waits of the
+ * single-launch forward (a CTA spinning, with sleeps, on a flag in global
+ * memory that another CTA sets): one CTA waits on a flag that nothing ever
+ * sets, gives up after limit_us microseconds (1 .. 100000), records
+ * FW_ERR_TIMEOUT in the device status word and exits normally.
+ */
+FW_API int fw_selftest_flag_timeout(int limit_us, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

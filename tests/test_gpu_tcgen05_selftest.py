@@ -64,3 +64,21 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     D = fw.fw_selftest_umma(A.cuda(), B.cuda())
     torch.cuda.synchronize()
     assert np.array_equal(D.cpu().double().numpy(), (A.double() @ B.double().T).numpy())
+
+
+def test_flag_wait_reports_timeout_and_context_survives():
+    """A wait on a ready flag nothing sets (the single-launch forward's hand-over
+    between CTAs) gives up after its bound, the status word reports
+    FW_ERR_TIMEOUT once, and the single-launch forward still runs correctly."""
+    assert fw.fw_device_status() == fw.FW_OK
+    fw.fw_selftest_flag_timeout(3000)
+    assert fw.fw_device_status() == fw.FW_ERR_TIMEOUT
+    assert fw.fw_device_status() == fw.FW_OK
+    from delta_rule_linear_dpfp_gb300 import inputs
+    assert fw.fw_delta_forward_kernel_count(2, 8, 2048, 64, 3, 64, 64, torch.bfloat16) == 1
+    d = {k: (None if v is None else v.cuda()) for k, v in inputs.forward_inputs("b2h8_l2048_nu3").items()}
+    y1, W1 = fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=d["W0"], nu=3)
+    y2, W2 = fw.fw_delta_forward(d["q"], d["k"], d["v"], d["beta"], W0=d["W0"], nu=3)
+    torch.cuda.synchronize()
+    assert fw.fw_device_status() == fw.FW_OK
+    assert torch.equal(y1, y2) and torch.equal(W1, W2)
