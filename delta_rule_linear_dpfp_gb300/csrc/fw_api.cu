@@ -215,7 +215,7 @@ namespace {
 // The projected q, k, v, beta inside the workspace, each 256-byte aligned,
 // then the forward's own workspace.
 struct ProjLayout {
-    size_t q, k, v, beta, scratch, fwd, bytes;
+    size_t q, k, v, beta, fwd, bytes;
 };
 ProjLayout proj_layout(int B, int L, int d_model, int H, int d_key, int d_v, size_t fwd_bytes) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -225,8 +225,7 @@ ProjLayout proj_layout(int B, int L, int d_model, int H, int d_key, int d_v, siz
     p.k = up(p.q + tok * d_key * 2);
     p.v = up(p.k + tok * d_key * 2);
     p.beta = up(p.v + tok * d_v * 2);
-    p.scratch = up(p.beta + tok * 2);
-    p.fwd = up(p.scratch + fw::gemm_scratch_bytes(B * L, H * (2 * d_key + d_v + 1), d_model));
+    p.fwd = up(p.beta + tok * 2);
     p.bytes = p.fwd + fwd_bytes;
     return p;
 }
@@ -293,7 +292,7 @@ FW_API int fw_delta_forward_projected(const void *x, const void *W_all, int ldw,
                                               di.num_sms, di.status, st));
     }
     e = fw::launch_project(x, W_all, ldw, ws + pl.q, ws + pl.k, ws + pl.v, ws + pl.beta, B, L, H, d_key, d_v, d_model,
-                           ws + pl.scratch, di.status, st);
+                           false, di.status, st);
     if (e != cudaSuccess)
         return cuda_status(e);
     e = fw::tc_forward_launch(ws + pl.q, ws + pl.k, ws + pl.v, ws + pl.beta, W0, W_final, y, ws + pl.fwd, B, H, L,

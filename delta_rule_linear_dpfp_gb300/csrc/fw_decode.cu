@@ -57,6 +57,13 @@ __global__ void __launch_bounds__(256)
     };
 
     griddep_launch_dependents();
+    // the CTA's rows into L2 while the preceding kernel still runs (a
+    // prefetch, so safe even if that kernel writes W: L2 is the point of
+    // coherence, and the loads below come after the wait)
+    if (tid == 0) {
+        const int nr = min(kRowsPerCta, d_v - r0);
+        l2_prefetch(W + (bh * d_v + r0) * (int64_t)d_dot, (uint32_t)(nr * d_dot * 4));
+    }
     griddep_wait(); // q, k, v, beta or W may be the preceding kernel's output: no load before this
     q = after_wait(q);
     k = after_wait(k);

@@ -89,29 +89,30 @@ cudaError_t launch_dpfp(const void *x, void *phi, int64_t rows, int d_key, int n
                         float eps, int num_sms, cudaStream_t st);
 
 // The dense layers run on one tcgen05 GEMM fed by TMA (fw_project.cu).  When
-// the output tiles alone would leave most SMs idle, K is split into slices
-// whose fp32 partial tiles a second kernel adds in slice order; that needs
-// gemm_scratch_bytes() of device scratch (0 when K is not split).
+// the output tiles alone would leave most SMs idle, K is split into up to 8
+// slices, each tile's slices one thread-block cluster whose CTAs add their
+// fp32 partial tiles in slice order through distributed shared memory.
 int gemm_slices(int M, int N, int K);
-size_t gemm_scratch_bytes(int M, int N, int K);
 size_t project_smem_bytes();
 
 // The projection prologue: q, k, v, beta (bf16, [B,H,L,*]) = x [B*L, d_model]
 // (bf16) times W_all = [W_q | W_k | W_v | W_beta] ([d_model, ldw], the first
 // N = H (2 d_key + d_v + 1) columns used; beta through the sigmoid).
 // d_model % 64 == 0, ldw % 8 == 0, ldw >= N rounded up to 8; x and W_all
-// 16-byte aligned.
+// 16-byte aligned.  w_early: the kernel may read the weights before the
+// preceding kernel on the stream has completed (only where that kernel is
+// one of this library's, which never write a weight).
 cudaError_t launch_project(const void *x, const void *Wall, int ldw, void *q, void *k, void *v, void *beta, int B,
-                           int L, int H, int d_key, int d_v, int d_model, void *scratch, unsigned *status,
+                           int L, int H, int d_key, int d_v, int d_model, bool w_early, unsigned *status,
                            cudaStream_t st);
 
 // A dense layer: P = A W + bias with A [M, K] bf16 and W [K, N] bf16
 // (row-major), then out = resid + P (fp32; resid may be NULL or equal to
 // out; out_bf16_copy, when not NULL, receives the same values in bf16) or,
 // with relu, out = bf16(max(P, 0)).  K % 64 == 0, N % 8 == 0; bias (fp32
-// [N]) may be NULL.
+// [N]) may be NULL.  w_early as for launch_project.
 cudaError_t launch_dense(const void *A, const void *W, int K, int M, int N, const float *bias, const float *resid,
-                         void *out, bool relu, void *out_bf16_copy, void *scratch, unsigned *status,
+                         void *out, bool relu, void *out_bf16_copy, bool w_early, unsigned *status,
                          cudaStream_t st);
 
 // Row-wise layer normalisation (biased variance): out[m] = (x[m] - mean) /

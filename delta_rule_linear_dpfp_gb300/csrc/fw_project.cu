@@ -26,11 +26,16 @@
 // tensor core works.  One thread issues the copies, another the MMAs
 // (tcgen05, fp32 accumulator in TMEM); the ring's full / empty mbarriers
 // order them.  The epilogue reads TMEM, one output row per thread: with one
-// slice it finishes the tile at once; with several, every CTA stores its
-// fp32 partial tile and a second kernel adds the partials in slice order
-// (the same sum on every run) and finishes them.  Finishing routes every 8 columns to their head
-// in q, k, v (16-byte stores) or beta (sigmoid), or adds the bias and then
-// the residual (fp32, optionally also a bf16 copy) or applies ReLU (bf16).
+// slice it finishes the tile at once.  With several, the slices of a tile
+// are one thread-block cluster: every CTA stages its fp32 partial tile in
+// its own shared memory and, after a cluster barrier, sends rows
+// [r R, r R + R) of it to cluster rank r with one bulk copy into r's shared
+// memory (distributed shared memory, completion counted on r's mbarrier);
+// CTA r then adds its rows of all the slices in slice order (the same sum on
+// every run) and finishes them.
+// Finishing routes every 8 columns to their head in q, k, v (16-byte
+// stores) or beta (sigmoid), or adds the bias and then the residual (fp32,
+// optionally also a bf16 copy) or applies ReLU (bf16).
 #include <cuda.h>
 
 #include <algorithm>
@@ -49,11 +54,17 @@ constexpr int kProjThreads = 128;
 constexpr int kStages = 4;
 constexpr int kStageBytes = 32768; // A 16 KB + B 16 KB
 // K is split when the output tiles alone would occupy fewer than half the
-// SMs, into slices that bring the grid to about kTargetCtas CTAs: measured
-// on the layer stack's GEMMs (M = 256), splitting every one of them, with
-// its extra reduction kernel, beat splitting only the long (K = 2048) one
-// by 13% per token (471 vs 540 us).
+// SMs, into slices that bring the grid to about kTargetCtas CTAs, at most
+// kMaxSlices (the portable cluster size): measured on the layer stack's
+// GEMMs (M = 256), splitting every one of them beat splitting only the long
+// (K = 2048) one by 13% per token (471 vs 540 us, with the slices then added
+// by a separate kernel).
 constexpr int kTargetCtas = 148;
+constexpr int kMaxSlices = 8;
+constexpr int kPartLd = 132; // fp32 row stride of a staged partial tile (16-byte stores 4-way at most)
+// the staged partial tile, then the rows received from the other slices
+constexpr int kTileBytes = 128 * kPartLd * 4;
+constexpr int kBarOff = kStages * kStageBytes > 2 * kTileBytes ? kStages * kStageBytes : 2 * kTileBytes;
 
 enum { kEpiHeads = 0, kEpiBiasResid = 1, kEpiBiasRelu = 2 };
 
@@ -138,22 +149,75 @@ FW_DEV void finish16(const GemmOut &o, const float *acc, int m, int n, int N) {
     }
 }
 
-// grid (M tiles, N tiles, K slices); K slice z covers K steps
-// [z * per, min(nk, (z + 1) * per)) of 64.  part: [slices][M tiles * 128][N
-// tiles * 128] fp32 partial tiles (used with slices > 1 only).
+FW_DEV void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The address of this CTA's shared location `saddr` in cluster rank `rank`.
+FW_DEV uint32_t cluster_addr(uint32_t saddr, uint32_t rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(saddr), "r"(rank));
+    return ra;
+}
+// Bulk copy of `bytes` (a multiple of 16, both ends 16-byte aligned) from
+// this CTA's shared memory to another CTA's of the cluster, completion
+// counted in bytes on that CTA's mbarrier (dst and bar: cluster addresses).
+FW_DEV void bulk_s2cluster(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// The finish of 8 columns n .. n + 7 of row m from the slices' sum, with
+// the bias (bz) and residual (rz) loaded beforehand: the same arithmetic as
+// bias_out.
 template <int EPI>
+FW_DEV void bias_finish(const GemmOut &o, const float *acc, const float (&bz)[8], const float (&rz)[8], int m, int n) {
+    float t8[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        t8[e] = acc[e] + bz[e];
+    const size_t off = (size_t)m * o.ldo + n;
+    if (EPI == kEpiBiasResid) {
+        if (o.resid) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                t8[e] += rz[e];
+        }
+        store8(o.out_f32 + off, t8);
+        if (o.out_bf16)
+            store8(o.out_bf16 + off, t8);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            t8[e] = fmaxf(t8[e], 0.f);
+        store8(o.out_bf16 + off, t8);
+    }
+}
+
+// grid (M tiles, N tiles, SL K slices); K slice z covers K steps
+// [z * per, min(nk, (z + 1) * per)) of 64 (none past nk: its partial tile is
+// zero).  With SL > 1 the launch groups a tile's slices into one cluster
+// (1, 1, SL), so slice z is the cluster's rank z.  w_early: the weights' copies
+// of the first stages are issued before the wait for the preceding kernel
+// (which then must not be one that writes W while this kernel may run: in
+// the layer stack it is always one of this library's kernels, none of which
+// writes a weight).
+template <int EPI, int SL>
 __global__ void __launch_bounds__(kProjThreads)
     gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, int K, int M, int N,
-                int per, GemmOut o, float *part, unsigned *status) {
+                int per, GemmOut o, int w_early, unsigned *status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t *full = (uint64_t *)(smem + kStages * kStageBytes); // [kStages] a stage's copies landed
-    uint64_t *empty = full + kStages;                            // [kStages] a stage's MMAs are done
-    uint64_t *done = empty + kStages;                            // every MMA is done
-    uint32_t *slot = (uint32_t *)(done + 1);
+    uint64_t *full = (uint64_t *)(smem + kBarOff); // [kStages] a stage's copies landed
+    uint64_t *empty = full + kStages;              // [kStages] a stage's MMAs are done
+    uint64_t *done = empty + kStages;              // every MMA is done
+    uint64_t *rx = done + 1;                       // SL > 1: the other slices' rows have landed
+    uint32_t *slot = (uint32_t *)(rx + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int m0 = blockIdx.x * 128, n0 = blockIdx.y * 128, z = blockIdx.z, slices = gridDim.z;
-    const int nk = K / 64, kb0 = z * per, nkl = min(nk, kb0 + per) - kb0;
+    const int m0 = blockIdx.x * 128, n0 = blockIdx.y * 128, z = blockIdx.z;
+    const int nk = K / 64, kb0 = z * per, nkl = max(0, min(nk, kb0 + per) - kb0);
+    constexpr uint32_t kRowsBytes = (uint32_t)(128 / SL) * kPartLd * 4; // one rank's rows of a partial tile
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -161,7 +225,10 @@ __global__ void __launch_bounds__(kProjThreads)
             mbar_init(empty + s, 1);
         }
         mbar_init(done, 1);
+        mbar_init(rx, 1);
         fence_barrier_init();
+        if (SL > 1) // armed before the cluster barrier that precedes any sender's copy
+            mbar_arrive_expect_tx(rx, (uint32_t)(SL - 1) * kRowsBytes);
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&ta)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tb)) : "memory");
     }
@@ -169,8 +236,18 @@ __global__ void __launch_bounds__(kProjThreads)
         tmem_alloc(slot, 128);
         tmem_relinquish();
     }
+    __syncthreads(); // the barriers are initialised
     griddep_launch_dependents();
-    griddep_wait(); // A and W may be the preceding kernel's output
+    const int npre = w_early ? min(kStages, nkl) : 0;
+    if (warp == 0 && lane == 0) // the weights of the first stages, before the wait
+        for (int i = 0; i < npre; ++i) {
+            uint8_t *b = smem + i * kStageBytes + 16384;
+            const int k0 = 64 * (kb0 + i);
+            mbar_arrive_expect_tx(full + i, kStageBytes);
+            tma_load_2d(b, &tb, n0, k0, full + i);
+            tma_load_2d(b + 8192, &tb, n0 + 64, k0, full + i);
+        }
+    griddep_wait(); // A (and, without w_early, W) may be the preceding kernel's output
     o.bias = after_wait(o.bias);
     o.resid = after_wait(o.resid);
     tc_fence_before();
@@ -189,10 +266,12 @@ __global__ void __launch_bounds__(kProjThreads)
             }
             uint8_t *a = smem + s * kStageBytes, *b = a + 16384;
             const int k0 = 64 * (kb0 + i);
-            mbar_arrive_expect_tx(full + s, kStageBytes);
+            if (i >= npre) {
+                mbar_arrive_expect_tx(full + s, kStageBytes);
+                tma_load_2d(b, &tb, n0, k0, full + s);
+                tma_load_2d(b + 8192, &tb, n0 + 64, k0, full + s);
+            }
             tma_load_2d(a, &ta, k0, m0, full + s);
-            tma_load_2d(b, &tb, n0, k0, full + s);
-            tma_load_2d(b + 8192, &tb, n0 + 64, k0, full + s);
             issued = i + 1;
         }
         // before the CTA can leave, every copy issued has landed (bounded)
@@ -219,88 +298,110 @@ __global__ void __launch_bounds__(kProjThreads)
     __syncwarp();
     ok = mbar_wait(done, 0, status) && ok;
     tc_fence_after();
-    if (__syncthreads_or(!ok)) {
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0)
-            tmem_dealloc(tm, 128);
-        return;
-    }
+    const bool bad = __syncthreads_or(!ok);
     const int m = m0 + tid;
     const uint32_t lane_base = tmem_lane_base(warp);
-    if (slices == 1) {
-        for (int c0 = 0; c0 < 128; c0 += 16) {
-            float acc[16];
-            tmem_ld16(tm + lane_base + (uint32_t)c0, acc);
-            tmem_ld_wait();
-            if (m < M && n0 + c0 < N)
-                finish16<EPI>(o, acc, m, n0 + c0, N);
-        }
-    } else { // this slice's fp32 partial tile; splitk_reduce_kernel adds the slices
-        const size_t ldp = (size_t)gridDim.y * 128, rows = (size_t)gridDim.x * 128;
-        float *mine = part + ((size_t)z * rows + m) * ldp + n0;
-        for (int c0 = 0; c0 < 128; c0 += 16) {
-            float acc[16];
-            tmem_ld16(tm + lane_base + (uint32_t)c0, acc);
-            tmem_ld_wait();
+    if constexpr (SL == 1) {
+        if (!bad)
+            for (int c0 = 0; c0 < 128; c0 += 16) {
+                float acc[16];
+                tmem_ld16(tm + lane_base + (uint32_t)c0, acc);
+                tmem_ld_wait();
+                if (m < M && n0 + c0 < N)
+                    finish16<EPI>(o, acc, m, n0 + c0, N);
+            }
+    } else {
+        // Rank z finishes rows [z R, z R + R) of the tile; this thread the
+        // 8-column group cg of rows z R + rr + 8 j, j < UPT.  Its bias and
+        // residual are loaded first, to arrive while the partials are staged.
+        constexpr int R = 128 / SL, UPT = R / 8;
+        const int cg = tid & 15, rr = tid >> 4, n = n0 + 8 * cg;
+        float bz[8], rz[UPT][8];
 #pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                __stcg(reinterpret_cast<float4 *>(mine + c0 + j), make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]));
+        for (int e = 0; e < 8; ++e)
+            bz[e] = 0.f;
+        if (EPI != kEpiHeads && o.bias && n < N)
+            load8(o.bias + n, bz);
+#pragma unroll
+        for (int j = 0; j < UPT; ++j) {
+            const int mm = m0 + z * R + rr + 8 * j;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                rz[j][e] = 0.f;
+            if (EPI == kEpiBiasResid && o.resid && mm < M && n < N)
+                load8(o.resid + (size_t)mm * o.ldo + n, rz[j]);
         }
+        // this slice's partial tile into shared memory, over the ring (every
+        // copy has landed and every MMA is done; zero for a slice past K); a
+        // CTA whose wait gave up still sends its rows and takes part in both
+        // cluster barriers (the status word then reports the timeout)
+        float *pt = reinterpret_cast<float *>(smem), *rxb = pt + 128 * kPartLd;
+        if (!bad)
+            for (int c0 = 0; c0 < 128; c0 += 16) {
+                float acc[16];
+                if (nkl > 0) {
+                    tmem_ld16(tm + lane_base + (uint32_t)c0, acc);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        acc[j] = 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                    *reinterpret_cast<float4 *>(pt + tid * kPartLd + c0 + j) =
+                        make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+            }
+        fence_async_smem(); // the staged tile, for the bulk copies that read it
+        cluster_sync();     // every slice has staged its tile (and armed its receiver)
+        // rows [r R, r R + R) of the staged tile to rank r, into its receive
+        // buffer's slot z (R rows at stride kPartLd are one contiguous run)
+        if (tid == 0) {
+            const uint32_t rx_s = smem_u32(rx), slot_s = smem_u32(rxb + (size_t)z * R * kPartLd);
+            for (int r = 0; r < SL; ++r)
+                if (r != z)
+                    bulk_s2cluster(cluster_addr(slot_s, (uint32_t)r), pt + (size_t)r * R * kPartLd, kRowsBytes,
+                                   cluster_addr(rx_s, (uint32_t)r));
+        }
+        (void)mbar_wait(rx, 0, status); // the other slices' rows of this rank have landed
+        // the sums in slice order: slice z's rows from the staged tile, the
+        // others' from the receive buffer
+#pragma unroll
+        for (int j = 0; j < UPT; ++j) {
+            const int row = rr + 8 * j; // within this rank's R rows
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[e] = 0.f;
+#pragma unroll
+            for (int zz = 0; zz < SL; ++zz) {
+                const float *src = zz == z ? pt + (size_t)(z * R + row) * kPartLd + 8 * cg
+                                           : rxb + (size_t)(zz * R + row) * kPartLd + 8 * cg;
+                const float4 a = *reinterpret_cast<const float4 *>(src);
+                const float4 b = *reinterpret_cast<const float4 *>(src + 4);
+                acc[0] += a.x;
+                acc[1] += a.y;
+                acc[2] += a.z;
+                acc[3] += a.w;
+                acc[4] += b.x;
+                acc[5] += b.y;
+                acc[6] += b.z;
+                acc[7] += b.w;
+            }
+            const int mm = m0 + z * R + rr + 8 * j;
+            if (mm < M && n < N) {
+                if (EPI == kEpiHeads)
+                    heads_out(o, acc, mm, n, N);
+                else
+                    bias_finish<EPI>(o, acc, bz, rz[j], mm, n);
+            }
+        }
+        cluster_sync(); // every copy has landed (each rank waited for its rows): no source is in use
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0)
         tmem_dealloc(tm, 128);
-}
-
-// The slices of a split-K GEMM added in slice order (so the sum does not
-// depend on which CTA finished first), then finished like a one-slice tile.
-// One thread per 8 columns of a row; the loads of up to 8 slices are issued
-// before any is added.  part: [slices][Mp][ldp] fp32.
-template <int EPI>
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *part, int slices, int Mp, int ldp, int M, int N,
-                                                            GemmOut o) {
-    griddep_launch_dependents();
-    griddep_wait(); // the partial tiles are the preceding kernel's
-    part = after_wait(part);
-    o.bias = after_wait(o.bias);
-    o.resid = after_wait(o.resid);
-    const int g8 = (N + 7) / 8;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)M * g8;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int m = (int)(i / g8), n = 8 * (int)(i % g8);
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            acc[e] = 0.f;
-        for (int z0 = 0; z0 < slices; z0 += 8) {
-            float4 f[8][2];
-#pragma unroll
-            for (int zz = 0; zz < 8; ++zz)
-                if (z0 + zz < slices) {
-                    const float4 *src = reinterpret_cast<const float4 *>(part + ((size_t)(z0 + zz) * Mp + m) * ldp + n);
-                    f[zz][0] = __ldcg(src);
-                    f[zz][1] = __ldcg(src + 1);
-                }
-#pragma unroll
-            for (int zz = 0; zz < 8; ++zz)
-                if (z0 + zz < slices) {
-                    acc[0] += f[zz][0].x;
-                    acc[1] += f[zz][0].y;
-                    acc[2] += f[zz][0].z;
-                    acc[3] += f[zz][0].w;
-                    acc[4] += f[zz][1].x;
-                    acc[5] += f[zz][1].y;
-                    acc[6] += f[zz][1].z;
-                    acc[7] += f[zz][1].w;
-                }
-        }
-        if (EPI == kEpiHeads)
-            heads_out(o, acc, m, n, N);
-        else
-            bias_out<EPI>(o, acc, m, n);
-    }
 }
 
 // ------------------------------------------------------------ tensor maps
@@ -349,51 +450,61 @@ int gemm_slices(int M, int N, int K) {
     const int tiles = ((M + 127) / 128) * ((N + 127) / 128), nk = K / 64;
     if (tiles >= kTargetCtas / 2 || nk <= 1)
         return 1;
-    const int want = std::min(nk, (kTargetCtas + tiles - 1) / tiles);
-    const int per = (nk + want - 1) / want;
-    return (nk + per - 1) / per;
+    const int want = std::min(std::min(nk, kMaxSlices), (kTargetCtas + tiles - 1) / tiles);
+    int sl = 1; // a power of two (the reduction's shape is compiled per slice count)
+    while (2 * sl <= want)
+        sl *= 2;
+    return sl;
 }
 
-size_t gemm_scratch_bytes(int M, int N, int K) {
-    const int sl = gemm_slices(M, N, K);
-    if (sl == 1)
-        return 0;
-    const size_t tm = (M + 127) / 128, tn = (N + 127) / 128;
-    return (size_t)sl * tm * 128 * tn * 128 * 4;
-}
+size_t project_smem_bytes() { return (size_t)kBarOff + (2 * kStages + 2) * 8 + 16 + 1024; }
 
-size_t project_smem_bytes() { return (size_t)kStages * kStageBytes + (2 * kStages + 1) * 8 + 16 + 1024; }
+template <int EPI, int SL>
+cudaError_t launch_gemm_sl(const CUtensorMap &ta, const CUtensorMap &tb, int K, int M, int N, const GemmOut &o,
+                           bool w_early, unsigned *status, cudaStream_t st) {
+    const size_t smem = project_smem_bytes();
+    auto kern = gemm_kernel<EPI, SL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    const int nk = K / 64, per = (nk + SL - 1) / SL;
+    // programmatic dependent launch, and the slices of a tile as one cluster
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((M + 127) / 128), (unsigned)((N + 127) / 128), (unsigned)SL);
+    cfg.blockDim = dim3(kProjThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = (unsigned)SL;
+    cfg.attrs = attr;
+    cfg.numAttrs = SL > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, K, M, N, per, o, w_early ? 1 : 0, status);
+}
 
 template <int EPI>
-cudaError_t launch_gemm_t(const void *A, const void *W, int ldw, int K, int M, int N, const GemmOut &o, void *scratch,
-                          unsigned *status, cudaStream_t st) {
+cudaError_t launch_gemm_t(const void *A, const void *W, int ldw, int K, int M, int N, const GemmOut &o,
+                          bool w_early, unsigned *status, cudaStream_t st) {
     CUtensorMap ta, tb;
     cudaError_t e = make_map(&ta, A, M, K, K, 128);
     if (e == cudaSuccess)
         e = make_map(&tb, W, K, N, ldw, 64);
     if (e != cudaSuccess)
         return e;
-    const size_t smem = project_smem_bytes();
-    auto kern = gemm_kernel<EPI>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess)
-        return e;
-    const int sl = gemm_slices(M, N, K), nk = K / 64, per = (nk + sl - 1) / sl;
-    const int tm = (M + 127) / 128, tn = (N + 127) / 128;
-    if (sl > 1 && !scratch)
-        return cudaErrorInvalidValue;
-    float *part = static_cast<float *>(scratch);
-    const dim3 grid((unsigned)tm, (unsigned)tn, (unsigned)sl);
-    e = launch_pdl(kern, grid, dim3(kProjThreads), smem, st, ta, tb, K, M, N, per, o, part, status);
-    if (e != cudaSuccess || sl == 1)
-        return e;
-    const int64_t work = (int64_t)M * ((N + 7) / 8);
-    return launch_pdl(splitk_reduce_kernel<EPI>, dim3((unsigned)std::min<int64_t>((work + 255) / 256, 1184)),
-                      dim3(256), 0, st, (const float *)part, sl, tm * 128, tn * 128, M, N, o);
+    switch (gemm_slices(M, N, K)) {
+    case 1: return launch_gemm_sl<EPI, 1>(ta, tb, K, M, N, o, w_early, status, st);
+    case 2: return launch_gemm_sl<EPI, 2>(ta, tb, K, M, N, o, w_early, status, st);
+    case 4: return launch_gemm_sl<EPI, 4>(ta, tb, K, M, N, o, w_early, status, st);
+    default: return launch_gemm_sl<EPI, 8>(ta, tb, K, M, N, o, w_early, status, st);
+    }
 }
 
 cudaError_t launch_project(const void *x, const void *Wall, int ldw, void *q, void *k, void *v, void *beta, int B,
-                           int L, int H, int d_key, int d_v, int d_model, void *scratch, unsigned *status,
+                           int L, int H, int d_key, int d_v, int d_model, bool w_early, unsigned *status,
                            cudaStream_t st) {
     GemmOut o = {};
     o.q = static_cast<__nv_bfloat16 *>(q);
@@ -405,11 +516,11 @@ cudaError_t launch_project(const void *x, const void *Wall, int ldw, void *q, vo
     o.d_key = d_key;
     o.d_v = d_v;
     const int M = B * L, N = H * (2 * d_key + d_v + 1);
-    return launch_gemm_t<kEpiHeads>(x, Wall, ldw, d_model, M, N, o, scratch, status, st);
+    return launch_gemm_t<kEpiHeads>(x, Wall, ldw, d_model, M, N, o, w_early, status, st);
 }
 
 cudaError_t launch_dense(const void *A, const void *W, int K, int M, int N, const float *bias, const float *resid,
-                         void *out, bool relu, void *out_bf16_copy, void *scratch, unsigned *status,
+                         void *out, bool relu, void *out_bf16_copy, bool w_early, unsigned *status,
                          cudaStream_t st) {
     GemmOut o = {};
     o.bias = bias;
@@ -417,11 +528,11 @@ cudaError_t launch_dense(const void *A, const void *W, int K, int M, int N, cons
     o.ldo = N;
     if (relu) {
         o.out_bf16 = static_cast<__nv_bfloat16 *>(out);
-        return launch_gemm_t<kEpiBiasRelu>(A, W, N, K, M, N, o, scratch, status, st);
+        return launch_gemm_t<kEpiBiasRelu>(A, W, N, K, M, N, o, w_early, status, st);
     }
     o.out_f32 = static_cast<float *>(out);
     o.out_bf16 = static_cast<__nv_bfloat16 *>(out_bf16_copy);
-    return launch_gemm_t<kEpiBiasResid>(A, W, N, K, M, N, o, scratch, status, st);
+    return launch_gemm_t<kEpiBiasResid>(A, W, N, K, M, N, o, w_early, status, st);
 }
 
 } // namespace fw

@@ -107,15 +107,6 @@ __global__ void __launch_bounds__(256) to_bf16_kernel(const float *__restrict__ 
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
-size_t stack_scratch(int B, int H, int d_key, int d_v, int d_model, int d_ff) {
-    const int N = H * (2 * d_key + d_v + 1);
-    size_t m = gemm_scratch_bytes(B, N, d_model);
-    m = std::max(m, gemm_scratch_bytes(B, d_model, H * d_v));
-    m = std::max(m, gemm_scratch_bytes(B, d_ff, d_model));
-    m = std::max(m, gemm_scratch_bytes(B, d_model, d_ff));
-    return m;
-}
-
 } // namespace
 
 cudaError_t launch_layernorm(const float *x, const float *gamma, const float *beta, void *out, bool out_bf16, int M,
@@ -140,8 +131,7 @@ StackLayout stack_layout(int B, int H, int d_key, int d_v, int d_model, int d_ff
     p.h = up256(p.z + (size_t)B * d_model * 2);
     p.x = up256(p.h + (size_t)B * d_ff * 2);
     p.x16 = up256(p.x + (size_t)B * d_model * 4);
-    p.scratch = up256(p.x16 + (size_t)B * d_model * 2);
-    p.bytes = up256(p.scratch + stack_scratch(B, H, d_key, d_v, d_model, d_ff));
+    p.bytes = up256(p.x16 + (size_t)B * d_model * 2);
     return p;
 }
 
@@ -152,7 +142,7 @@ cudaError_t stack_step_launch(const fw_stack_layer *layers, int n_layers, const 
     const StackLayout pl = stack_layout(B, H, d_key, d_v, d_model, d_ff);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *xr = reinterpret_cast<float *>(ws + pl.x);
-    void *x16 = ws + pl.x16, *scratch = ws + pl.scratch;
+    void *x16 = ws + pl.x16;
     cudaError_t e = cudaSuccess;
     if (n_layers > 0) {
         const int64_t n8 = (int64_t)B * d_model / 8;
@@ -163,20 +153,20 @@ cudaError_t stack_step_launch(const fw_stack_layer *layers, int n_layers, const 
         const fw_stack_layer &ly = layers[l];
         const float *xin = l == 0 ? x : xr;
         e = launch_project(x16, ly.W_in, ldw_in, ws + pl.q, ws + pl.k, ws + pl.v, ws + pl.beta, B, 1, H, d_key, d_v,
-                           d_model, scratch, status, st);
+                           d_model, true, status, st);
         if (e == cudaSuccess)
             e = launch_decode(ws + pl.q, ws + pl.k, ws + pl.v, ws + pl.beta, ly.W, ws + pl.y, B * H, d_key, nu, d_v,
                               1, eps, num_sms, st);
         if (e == cudaSuccess) // x <- x + y W_o + b_o
-            e = launch_dense(ws + pl.y, ly.W_o, H * d_v, B, d_model, ly.b_o, xin, xr, false, nullptr, scratch, status,
+            e = launch_dense(ws + pl.y, ly.W_o, H * d_v, B, d_model, ly.b_o, xin, xr, false, nullptr, true, status,
                              st);
         if (e == cudaSuccess)
             e = launch_layernorm(xr, ly.ln_gamma, ly.ln_beta, ws + pl.z, true, B, d_model, ln_eps, st);
         if (e == cudaSuccess) // hidden = relu(LN(x) W_1 + b_1)
-            e = launch_dense(ws + pl.z, ly.W_1, d_model, B, d_ff, ly.b_1, nullptr, ws + pl.h, true, nullptr, scratch,
+            e = launch_dense(ws + pl.z, ly.W_1, d_model, B, d_ff, ly.b_1, nullptr, ws + pl.h, true, nullptr, true,
                              status, st);
         if (e == cudaSuccess) // x <- x + hidden W_2 + b_2, and its bf16 copy for the next projection
-            e = launch_dense(ws + pl.h, ly.W_2, d_ff, B, d_model, ly.b_2, xr, xr, false, x16, scratch, status, st);
+            e = launch_dense(ws + pl.h, ly.W_2, d_ff, B, d_model, ly.b_2, xr, xr, false, x16, true, status, st);
     }
     if (e == cudaSuccess)
         e = launch_layernorm(n_layers ? xr : x, ln_gamma, ln_beta, out, false, B, d_model, ln_eps, st);
