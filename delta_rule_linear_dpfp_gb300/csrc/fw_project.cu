@@ -28,11 +28,13 @@
 // order them.  The epilogue reads TMEM, one output row per thread: with one
 // slice it finishes the tile at once.  With several, the slices of a tile
 // are one thread-block cluster: every CTA stages its fp32 partial tile in
-// its own shared memory and, after a cluster barrier, sends rows
-// [r R, r R + R) of it to cluster rank r with one bulk copy into r's shared
-// memory (distributed shared memory, completion counted on r's mbarrier);
-// CTA r then adds its rows of all the slices in slice order (the same sum on
-// every run) and finishes them.
+// its own shared memory and sends rows [r R, r R + R) of it to cluster rank
+// r with one bulk copy into r's receive buffer (distributed shared memory,
+// completion counted on r's mbarrier); CTA r then adds its rows of all the
+// slices in slice order (the same sum on every run) and finishes them.  The
+// receive buffers lie outside the TMA ring, so a slice sends as soon as its
+// own tile is staged; the one cluster barrier (every CTA's mbarriers are
+// initialised) comes before the wait for the preceding kernel.
 // Finishing routes every 8 columns to their head in q, k, v (16-byte
 // stores) or beta (sigmoid), or adds the bias and then the residual (fp32,
 // optionally also a bf16 copy) or applies ReLU (bf16).
@@ -62,9 +64,12 @@ constexpr int kStageBytes = 32768; // A 16 KB + B 16 KB
 constexpr int kTargetCtas = 148;
 constexpr int kMaxSlices = 8;
 constexpr int kPartLd = 132; // fp32 row stride of a staged partial tile (16-byte stores 4-way at most)
-// the staged partial tile, then the rows received from the other slices
+// the staged partial tile over the ring (once it is drained), the rows
+// received from the other slices after it, then the mbarriers
 constexpr int kTileBytes = 128 * kPartLd * 4;
-constexpr int kBarOff = kStages * kStageBytes > 2 * kTileBytes ? kStages * kStageBytes : 2 * kTileBytes;
+static_assert(kTileBytes <= kStages * kStageBytes, "the staged tile fits in the ring");
+constexpr int kRxOff = kStages * kStageBytes;
+constexpr int kBarOff = kRxOff + kTileBytes;
 
 enum { kEpiHeads = 0, kEpiBiasResid = 1, kEpiBiasRelu = 2 };
 
@@ -213,7 +218,8 @@ __global__ void __launch_bounds__(kProjThreads)
     uint64_t *empty = full + kStages;              // [kStages] a stage's MMAs are done
     uint64_t *done = empty + kStages;              // every MMA is done
     uint64_t *rx = done + 1;                       // SL > 1: the other slices' rows have landed
-    uint32_t *slot = (uint32_t *)(rx + 1);
+    uint64_t *sent = rx + 1;                       // SL > 1: every rank has received this slice's rows
+    uint32_t *slot = (uint32_t *)(sent + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int m0 = blockIdx.x * 128, n0 = blockIdx.y * 128, z = blockIdx.z;
     const int nk = K / 64, kb0 = z * per, nkl = max(0, min(nk, kb0 + per) - kb0);
@@ -226,6 +232,7 @@ __global__ void __launch_bounds__(kProjThreads)
         }
         mbar_init(done, 1);
         mbar_init(rx, 1);
+        mbar_init(sent, SL > 1 ? SL - 1 : 1);
         fence_barrier_init();
         if (SL > 1) // armed before the cluster barrier that precedes any sender's copy
             mbar_arrive_expect_tx(rx, (uint32_t)(SL - 1) * kRowsBytes);
@@ -237,6 +244,8 @@ __global__ void __launch_bounds__(kProjThreads)
         tmem_relinquish();
     }
     __syncthreads(); // the barriers are initialised
+    if (SL > 1)
+        cluster_sync(); // ... in every CTA of the cluster, before any copy or arrival reaches them
     griddep_launch_dependents();
     const int npre = w_early ? min(kStages, nkl) : 0;
     if (warp == 0 && lane == 0) // the weights of the first stages, before the wait
@@ -335,7 +344,7 @@ __global__ void __launch_bounds__(kProjThreads)
         // copy has landed and every MMA is done; zero for a slice past K); a
         // CTA whose wait gave up still sends its rows and takes part in both
         // cluster barriers (the status word then reports the timeout)
-        float *pt = reinterpret_cast<float *>(smem), *rxb = pt + 128 * kPartLd;
+        float *pt = reinterpret_cast<float *>(smem), *rxb = reinterpret_cast<float *>(smem + kRxOff);
         if (!bad)
             for (int c0 = 0; c0 < 128; c0 += 16) {
                 float acc[16];
@@ -353,7 +362,7 @@ __global__ void __launch_bounds__(kProjThreads)
                         make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
             }
         fence_async_smem(); // the staged tile, for the bulk copies that read it
-        cluster_sync();     // every slice has staged its tile (and armed its receiver)
+        __syncthreads();
         // rows [r R, r R + R) of the staged tile to rank r, into its receive
         // buffer's slot z (R rows at stride kPartLd are one contiguous run)
         if (tid == 0) {
@@ -364,6 +373,13 @@ __global__ void __launch_bounds__(kProjThreads)
                                    cluster_addr(rx_s, (uint32_t)r));
         }
         (void)mbar_wait(rx, 0, status); // the other slices' rows of this rank have landed
+        // ... so their copies are done with the senders' tiles: tell each
+        // sender (a relaxed arrival: it publishes no data, and a release
+        // would hold the warp at a cluster-scope fence for about a microsecond)
+        if (tid < SL && tid != z)
+            asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                             cluster_addr(smem_u32(sent), (uint32_t)tid))
+                         : "memory");
         // the sums in slice order: slice z's rows from the staged tile, the
         // others' from the receive buffer
 #pragma unroll
@@ -396,7 +412,7 @@ __global__ void __launch_bounds__(kProjThreads)
                     bias_finish<EPI>(o, acc, bz, rz[j], mm, n);
             }
         }
-        cluster_sync(); // every copy has landed (each rank waited for its rows): no source is in use
+        (void)mbar_wait(sent, 0, status); // every rank has this slice's rows: the staged tile is free
     }
     tc_fence_before();
     __syncthreads();
@@ -457,7 +473,7 @@ int gemm_slices(int M, int N, int K) {
     return sl;
 }
 
-size_t project_smem_bytes() { return (size_t)kBarOff + (2 * kStages + 2) * 8 + 16 + 1024; }
+size_t project_smem_bytes() { return (size_t)kBarOff + (2 * kStages + 3) * 8 + 16 + 1024; }
 
 template <int EPI, int SL>
 cudaError_t launch_gemm_sl(const CUtensorMap &ta, const CUtensorMap &tb, int K, int M, int N, const GemmOut &o,
