@@ -93,9 +93,12 @@ FW_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
 // orders every write it guards (bulk copies included) before a release
 // store; the reader's acquire load orders every later read, bulk copies
 // included, after it.
+// The writer has waited for its bulk copies to complete (their writes are
+// then visible to it); the proxy fence orders those async-proxy writes
+// before its later generic accesses, and the release store orders every
+// earlier access of the thread before the flag.
 FW_DEV void flag_set(unsigned *f) {
-    asm volatile("fence.proxy.async.global;" ::: "memory"); // bulk-copy writes before the release
-    __threadfence();
+    asm volatile("fence.proxy.async.global;" ::: "memory");
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
 }
 FW_DEV unsigned flag_load(const unsigned *f) {
