@@ -673,7 +673,7 @@ def measure_rows(fw, inputs, dev, stream, pk):
     wbytes = (d_model * sl[0]["W_in"].shape[1] + H * d_v * d_model + 2 * d_model * d_ff) * 2
     nbytes = nl * (2 * B * H * d_v * d_dot * 4 + wbytes) + 2 * B * d_model * 4
     flops = nl * (2.0 * B * (d_model * N + H * d_v * d_model + 2 * d_model * d_ff) + 6.0 * B * H * d_v * d_dot)
-    r = roofline("fw_decode_stack_step (6 layers, 38 launches)", flops, nbytes, ms, pk)
+    r = roofline("fw_decode_stack_step (6 layers, 32 launches)", flops, nbytes, ms, pk)
     r["tokens/s"] = B / (ms * 1e-3)
     # the same token step captured once as a CUDA graph and replayed (8 tokens per timing)
     gs = torch.cuda.Stream()
@@ -701,7 +701,7 @@ def measure_rows(fw, inputs, dev, stream, pk):
 
 def stack_only(steps):
     """`steps` token steps of the stack_b256_l6 workload through the public API
-    (38 launches each), nothing else: the command the stack's launch list is
+    (32 launches each), nothing else: the command the stack's launch list is
     captured from."""
     from delta_rule_linear_dpfp_gb300 import binding as fw, build, inputs
     build.build()
@@ -718,7 +718,7 @@ def stack_only(steps):
     for i in range(steps):
         fw.fw_decode_stack_step(sx[i % 4], sl, H, d_key, d_v, nu=nu, ln_gamma=sg, ln_beta=sb, out=out, workspace=ws)
     torch.cuda.synchronize()
-    print(json.dumps({"stack_steps": steps, "launches_per_step": 6 * nl + 2}))
+    print(json.dumps({"stack_steps": steps, "launches_per_step": 5 * nl + 2}))
 
 
 def backward_only(steps):

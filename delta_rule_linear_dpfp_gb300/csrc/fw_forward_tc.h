@@ -106,14 +106,34 @@ cudaError_t launch_project(const void *x, const void *Wall, int ldw, void *q, vo
                            int L, int H, int d_key, int d_v, int d_model, bool w_early, unsigned *status,
                            cudaStream_t st);
 
+// A dense layer's A operand as the LayerNorm of fp32 rows x [M, K]
+// (biased variance over K; gamma, beta fp32 [K] or null for 1 and 0),
+// rounded to bf16, from the per-row statistics of x that the dense layer
+// which wrote x left in `stats`: (mean, sum of squared deviations) of each
+// 128-column part, [M][parts], parts = K / 128.
+struct DenseLn {
+    const float *x;
+    const float2 *stats;
+    const float *gamma, *beta;
+    float eps;
+    int parts;
+};
+// Whether launch_dense can take its A as a DenseLn for these sizes: K a
+// multiple of 128, and at most two K steps of 64 per K slice (x's fp32 tiles
+// are staged in the two ring stages those steps leave free).
+bool dense_ln_supported(int M, int N, int K);
+
 // A dense layer: P = A W + bias with A [M, K] bf16 and W [K, N] bf16
 // (row-major), then out = resid + P (fp32; resid may be NULL or equal to
 // out; out_bf16_copy, when not NULL, receives the same values in bf16) or,
 // with relu, out = bf16(max(P, 0)).  K % 64 == 0, N % 8 == 0; bias (fp32
-// [N]) may be NULL.  w_early as for launch_project.
+// [N]) may be NULL.  w_early as for launch_project.  stats (fp32 output
+// only, N % 128 == 0; or null): the output rows' statistics for a DenseLn
+// of a later layer.  ln (or null): A is that LayerNorm instead, computed in
+// the kernel (A then only sizes the unused tensor map).
 cudaError_t launch_dense(const void *A, const void *W, int K, int M, int N, const float *bias, const float *resid,
-                         void *out, bool relu, void *out_bf16_copy, bool w_early, unsigned *status,
-                         cudaStream_t st);
+                         void *out, bool relu, void *out_bf16_copy, bool w_early, float2 *stats, const DenseLn *ln,
+                         unsigned *status, cudaStream_t st);
 
 // Row-wise layer normalisation (biased variance): out[m] = (x[m] - mean) /
 // sqrt(var + eps) * gamma + beta over D columns; x fp32 [M, D]; out bf16

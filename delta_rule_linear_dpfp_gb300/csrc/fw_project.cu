@@ -70,6 +70,7 @@ constexpr int kTileBytes = 128 * kPartLd * 4;
 static_assert(kTileBytes <= kStages * kStageBytes, "the staged tile fits in the ring");
 constexpr int kRxOff = kStages * kStageBytes;
 constexpr int kBarOff = kRxOff + kTileBytes;
+constexpr int kLnOff = kBarOff + 256; // the rows' LayerNorm statistics (a DenseLn A), 1 KB
 
 enum { kEpiHeads = 0, kEpiBiasResid = 1, kEpiBiasRelu = 2 };
 
@@ -83,7 +84,31 @@ struct GemmOut {
     float *out_f32;
     __nv_bfloat16 *out_bf16;
     int ldo;
+    // kEpiBiasResid (or null): per output row and 128-column tile n0 / 128,
+    // the (mean, sum of squared deviations) of the finished values, at
+    // stats[m * (ldo / 128) + n0 / 128]: a later LayerNorm's statistics
+    float2 *stats;
 };
+
+// Chan's combination of group a's (mean, M2) with group b's, of na and nb
+// values: the statistics of the union.
+FW_DEV void chan_combine(float &mean, float &m2, float na, float mb, float m2b, float nb) {
+    const float d = mb - mean, n = na + nb;
+    mean = mean + d * (nb / n);
+    m2 = m2 + m2b + d * d * (na * nb / n);
+}
+// (mean, M2) of 8 values, two passes.
+FW_DEV void stats8(const float (&v)[8], float &mean, float &m2) {
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        s += v[e];
+    mean = s * 0.125f;
+    m2 = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        m2 = fmaf(v[e] - mean, v[e] - mean, m2);
+}
 
 // 8 columns n .. n + 7 of row m of P routed to their head in q, k, v, or
 // to beta through the sigmoid (one head per column).
@@ -116,8 +141,7 @@ FW_DEV void heads_out(const GemmOut &o, const float *acc, int m, int n, int N) {
 // residual row (fp32 out, and its bf16 copy when asked; the residual may be
 // the output itself) or passed through ReLU (bf16 out).
 template <int EPI>
-FW_DEV void bias_out(const GemmOut &o, const float *acc, int m, int n) {
-    float t8[8];
+FW_DEV void bias_out(const GemmOut &o, const float *acc, int m, int n, float (&t8)[8]) {
 #pragma unroll
     for (int e = 0; e < 8; ++e)
         t8[e] = acc[e] + (o.bias ? __ldcg(o.bias + n + e) : 0.f);
@@ -141,18 +165,34 @@ FW_DEV void bias_out(const GemmOut &o, const float *acc, int m, int n) {
     }
 }
 
+// 16 columns of row m; with o.stats, the 8-column groups' statistics are
+// folded into the row's running (mean, M2) over `cnt` values.
 template <int EPI>
-FW_DEV void finish16(const GemmOut &o, const float *acc, int m, int n, int N) {
+FW_DEV void finish16(const GemmOut &o, const float *acc, int m, int n, int N, float &mean, float &m2, float &cnt) {
 #pragma unroll
     for (int h8 = 0; h8 < 16; h8 += 8) {
         if (n + h8 >= N)
             break;
-        if (EPI == kEpiHeads)
+        if (EPI == kEpiHeads) {
             heads_out(o, acc + h8, m, n + h8, N);
-        else
-            bias_out<EPI>(o, acc + h8, m, n + h8);
+        } else {
+            float t8[8];
+            bias_out<EPI>(o, acc + h8, m, n + h8, t8);
+            if (EPI == kEpiBiasResid && o.stats) {
+                float mb, m2b;
+                stats8(t8, mb, m2b);
+                if (cnt == 0.f) {
+                    mean = mb;
+                    m2 = m2b;
+                } else {
+                    chan_combine(mean, m2, cnt, mb, m2b, 8.f);
+                }
+                cnt += 8.f;
+            }
+        }
     }
 }
+
 
 FW_DEV void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -177,8 +217,8 @@ FW_DEV void bulk_s2cluster(uint32_t dst, const void *src, uint32_t bytes, uint32
 // the bias (bz) and residual (rz) loaded beforehand: the same arithmetic as
 // bias_out.
 template <int EPI>
-FW_DEV void bias_finish(const GemmOut &o, const float *acc, const float (&bz)[8], const float (&rz)[8], int m, int n) {
-    float t8[8];
+FW_DEV void bias_finish(const GemmOut &o, const float *acc, const float (&bz)[8], const float (&rz)[8], int m, int n,
+                        float (&t8)[8]) {
 #pragma unroll
     for (int e = 0; e < 8; ++e)
         t8[e] = acc[e] + bz[e];
@@ -207,11 +247,14 @@ FW_DEV void bias_finish(const GemmOut &o, const float *acc, const float (&bz)[8]
 // of the first stages are issued before the wait for the preceding kernel
 // (which then must not be one that writes W while this kernel may run: in
 // the layer stack it is always one of this library's kernels, none of which
-// writes a weight).
+// writes a weight).  ln.x (or null): A is LayerNorm(x), formed by the CTA's
+// threads (every K step of the slice staged at once: per <= 2), in place of
+// A's TMA copies; tx: x's fp32 tensor map (128-row x 64-column boxes).
 template <int EPI, int SL>
 __global__ void __launch_bounds__(kProjThreads)
-    gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, int K, int M, int N,
-                int per, GemmOut o, int w_early, unsigned *status) {
+    gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+                const __grid_constant__ CUtensorMap tx, int K, int M, int N, int per, GemmOut o, DenseLn ln,
+                int w_early, unsigned *status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = (uint64_t *)(smem + kBarOff); // [kStages] a stage's copies landed
@@ -219,20 +262,25 @@ __global__ void __launch_bounds__(kProjThreads)
     uint64_t *done = empty + kStages;              // every MMA is done
     uint64_t *rx = done + 1;                       // SL > 1: the other slices' rows have landed
     uint64_t *sent = rx + 1;                       // SL > 1: every rank has received this slice's rows
-    uint32_t *slot = (uint32_t *)(sent + 1);
+    uint64_t *xbar = sent + 1;                     // ln.x: x's tiles have landed
+    uint32_t *slot = (uint32_t *)(xbar + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int m0 = blockIdx.x * 128, n0 = blockIdx.y * 128, z = blockIdx.z;
     const int nk = K / 64, kb0 = z * per, nkl = max(0, min(nk, kb0 + per) - kb0);
     constexpr uint32_t kRowsBytes = (uint32_t)(128 / SL) * kPartLd * 4; // one rank's rows of a partial tile
 
+    // a stage is full once its copies have landed and, where A is formed
+    // here, every thread has stored its row of A
+    const uint32_t stage_tx = ln.x ? 16384u : (uint32_t)kStageBytes;
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(full + s, 1);
+            mbar_init(full + s, ln.x ? 1u + kProjThreads : 1u);
             mbar_init(empty + s, 1);
         }
         mbar_init(done, 1);
         mbar_init(rx, 1);
         mbar_init(sent, SL > 1 ? SL - 1 : 1);
+        mbar_init(xbar, 1);
         fence_barrier_init();
         if (SL > 1) // armed before the cluster barrier that precedes any sender's copy
             mbar_arrive_expect_tx(rx, (uint32_t)(SL - 1) * kRowsBytes);
@@ -252,7 +300,7 @@ __global__ void __launch_bounds__(kProjThreads)
         for (int i = 0; i < npre; ++i) {
             uint8_t *b = smem + i * kStageBytes + 16384;
             const int k0 = 64 * (kb0 + i);
-            mbar_arrive_expect_tx(full + i, kStageBytes);
+            mbar_arrive_expect_tx(full + i, stage_tx);
             tma_load_2d(b, &tb, n0, k0, full + i);
             tma_load_2d(b + 8192, &tb, n0 + 64, k0, full + i);
         }
@@ -263,6 +311,66 @@ __global__ void __launch_bounds__(kProjThreads)
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *slot;
+    if (ln.x) {
+        // A = LN(x) for every stage (at most two: per <= 2).  x's fp32 tile of
+        // each stage (128 rows x 64 columns, 32 KB, unswizzled) comes by TMA
+        // into the ring's stages 2 and 3, which two K steps leave free, while
+        // each row's mean and 1 / sqrt(var + eps) are combined from its
+        // 128-column parts (thread = row) into shared memory.  Then two rows
+        // per warp instruction (16 lanes x 16 bytes each) are normalised and
+        // stored in bf16 into the stage's K-major 128-byte-swizzled layout.
+        const float2 *stats = after_wait(ln.stats);
+        float *mst = reinterpret_cast<float *>(smem + kLnOff); // [128] means, then [128] 1 / sigma
+        if (tid == 0) {
+            mbar_arrive_expect_tx(xbar, (uint32_t)nkl * 32768u);
+            for (int i = 0; i < nkl; ++i)
+                tma_load_2d(smem + (2 + i) * kStageBytes, &tx, 64 * (kb0 + i), m0, xbar);
+        }
+        {
+            const int m = m0 + tid;
+            float mean = 0.f, rstd = 0.f;
+            if (m < M) {
+                const float2 s0 = __ldcg(stats + (size_t)m * ln.parts);
+                mean = s0.x;
+                float m2 = s0.y;
+                for (int p = 1; p < ln.parts; ++p) {
+                    const float2 sp = __ldcg(stats + (size_t)m * ln.parts + p);
+                    chan_combine(mean, m2, 128.f * p, sp.x, sp.y, 128.f);
+                }
+                rstd = rsqrtf(m2 / (128.f * ln.parts) + ln.eps);
+            }
+            mst[tid] = mean;
+            mst[128 + tid] = rstd;
+        }
+        const bool xin = mbar_wait(xbar, 0, status); // (a timeout leaves A as it is: the status reports it)
+        __syncthreads();
+        const int cq = lane & 15, rsel = lane >> 4; // the lane's 4 columns of a stage; which of the 2 rows
+        for (int i = 0; i < nkl; ++i) {
+            uint8_t *a = smem + i * kStageBytes;
+            const float *xs = reinterpret_cast<const float *>(smem + (2 + i) * kStageBytes); // [128][64]
+            const int k = 64 * (kb0 + i) + 4 * cq;
+            float4 g = make_float4(1.f, 1.f, 1.f, 1.f), bb = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (ln.gamma)
+                g = __ldg(reinterpret_cast<const float4 *>(ln.gamma + k));
+            if (ln.beta)
+                bb = __ldg(reinterpret_cast<const float4 *>(ln.beta + k));
+#pragma unroll 4
+            for (int r = 0; r < 16; ++r) {
+                const int row = 32 * warp + 2 * r + rsel;
+                const float mu = mst[row], rs = mst[128 + row];
+                const bool live = xin && m0 + row < M;
+                const float4 xr = *reinterpret_cast<const float4 *>(xs + row * 64 + 4 * cq);
+                const float v0 = live ? (xr.x - mu) * rs * g.x + bb.x : 0.f;
+                const float v1 = live ? (xr.y - mu) * rs * g.y + bb.y : 0.f;
+                const float v2 = live ? (xr.z - mu) * rs * g.z + bb.z : 0.f;
+                const float v3 = live ? (xr.w - mu) * rs * g.w + bb.w : 0.f;
+                *reinterpret_cast<uint2 *>(a + (uint32_t)row * 128u + ((uint32_t)((cq >> 1) ^ (row & 7)) << 4) +
+                                           (uint32_t)(cq & 1) * 8u) = make_uint2(pack_bf16x2(v0, v1), pack_bf16x2(v2, v3));
+            }
+            fence_async_smem();
+            mbar_arrive(full + i);
+        }
+    }
 
     bool ok = true;
     if (warp == 0 && lane == 0) {          // producer: the TMA copies of each K step
@@ -276,11 +384,12 @@ __global__ void __launch_bounds__(kProjThreads)
             uint8_t *a = smem + s * kStageBytes, *b = a + 16384;
             const int k0 = 64 * (kb0 + i);
             if (i >= npre) {
-                mbar_arrive_expect_tx(full + s, kStageBytes);
+                mbar_arrive_expect_tx(full + s, stage_tx);
                 tma_load_2d(b, &tb, n0, k0, full + s);
                 tma_load_2d(b + 8192, &tb, n0 + 64, k0, full + s);
             }
-            tma_load_2d(a, &ta, k0, m0, full + s);
+            if (!ln.x)
+                tma_load_2d(a, &ta, k0, m0, full + s);
             issued = i + 1;
         }
         // before the CTA can leave, every copy issued has landed (bounded)
@@ -311,14 +420,18 @@ __global__ void __launch_bounds__(kProjThreads)
     const int m = m0 + tid;
     const uint32_t lane_base = tmem_lane_base(warp);
     if constexpr (SL == 1) {
-        if (!bad)
+        float mu = 0.f, m2 = 0.f, cnt = 0.f; // the row's statistics (o.stats)
+        if (!bad) {
             for (int c0 = 0; c0 < 128; c0 += 16) {
                 float acc[16];
                 tmem_ld16(tm + lane_base + (uint32_t)c0, acc);
                 tmem_ld_wait();
                 if (m < M && n0 + c0 < N)
-                    finish16<EPI>(o, acc, m, n0 + c0, N);
+                    finish16<EPI>(o, acc, m, n0 + c0, N, mu, m2, cnt);
             }
+            if (EPI == kEpiBiasResid && o.stats && m < M)
+                o.stats[(size_t)m * (o.ldo / 128) + n0 / 128] = make_float2(mu, m2);
+        }
     } else {
         // Rank z finishes rows [z R, z R + R) of the tile; this thread the
         // 8-column group cg of rows z R + rr + 8 j, j < UPT.  Its bias and
@@ -405,11 +518,27 @@ __global__ void __launch_bounds__(kProjThreads)
                 acc[7] += b.w;
             }
             const int mm = m0 + z * R + rr + 8 * j;
+            float t8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (mm < M && n < N) {
                 if (EPI == kEpiHeads)
                     heads_out(o, acc, mm, n, N);
                 else
-                    bias_finish<EPI>(o, acc, bz, rz[j], mm, n);
+                    bias_finish<EPI>(o, acc, bz, rz[j], mm, n, t8);
+            }
+            if (EPI == kEpiBiasResid && o.stats) {
+                // the row's 128 columns lie with the 16 lanes of this
+                // half-warp: their groups combined pairwise, lane cg = 0's
+                // result stored
+                float mu, m2;
+                stats8(t8, mu, m2);
+#pragma unroll
+                for (int off = 1; off < 16; off <<= 1) {
+                    const float mb = __shfl_xor_sync(0xffffffffu, mu, off);
+                    const float m2b = __shfl_xor_sync(0xffffffffu, m2, off);
+                    chan_combine(mu, m2, 8.f * off, mb, m2b, 8.f * off);
+                }
+                if (cg == 0 && mm < M)
+                    o.stats[(size_t)mm * (o.ldo / 128) + n0 / 128] = make_float2(mu, m2);
             }
         }
         (void)mbar_wait(sent, 0, status); // every rank has this slice's rows: the staged tile is free
@@ -456,6 +585,23 @@ cudaError_t make_map(CUtensorMap *map, const void *base, int rows, int cols, int
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// A row-major fp32 matrix [rows, cols] with row stride ld (elements) seen as
+// unswizzled boxes of box_rows x 64 columns (256-byte rows); out-of-range
+// elements read as zero.
+cudaError_t make_f32_map(CUtensorMap *map, const void *base, int rows, int cols, int ld, int box_rows) {
+    EncodeTiled fn = encoder();
+    if (!fn)
+        return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 } // namespace
 
 cudaError_t make_bf16_map(CUtensorMap *map, const void *base, int rows, int cols, int ld, int box_rows) {
@@ -473,11 +619,16 @@ int gemm_slices(int M, int N, int K) {
     return sl;
 }
 
-size_t project_smem_bytes() { return (size_t)kBarOff + (2 * kStages + 3) * 8 + 16 + 1024; }
+size_t project_smem_bytes() { return (size_t)kLnOff + 1024 + 1024; }
+
+bool dense_ln_supported(int M, int N, int K) {
+    const int nk = K / 64, sl = gemm_slices(M, N, K);
+    return K % 128 == 0 && (nk + sl - 1) / sl <= 2; // x's tiles fill the ring's stages 2 and 3
+}
 
 template <int EPI, int SL>
-cudaError_t launch_gemm_sl(const CUtensorMap &ta, const CUtensorMap &tb, int K, int M, int N, const GemmOut &o,
-                           bool w_early, unsigned *status, cudaStream_t st) {
+cudaError_t launch_gemm_sl(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tx, int K, int M, int N,
+                           const GemmOut &o, const DenseLn &ln, bool w_early, unsigned *status, cudaStream_t st) {
     const size_t smem = project_smem_bytes();
     auto kern = gemm_kernel<EPI, SL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -499,23 +650,32 @@ cudaError_t launch_gemm_sl(const CUtensorMap &ta, const CUtensorMap &tb, int K, 
     attr[1].val.clusterDim.z = (unsigned)SL;
     cfg.attrs = attr;
     cfg.numAttrs = SL > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, K, M, N, per, o, w_early ? 1 : 0, status);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tx, K, M, N, per, o, ln, w_early ? 1 : 0, status);
 }
 
 template <int EPI>
 cudaError_t launch_gemm_t(const void *A, const void *W, int ldw, int K, int M, int N, const GemmOut &o,
-                          bool w_early, unsigned *status, cudaStream_t st) {
-    CUtensorMap ta, tb;
+                          const DenseLn &ln, bool w_early, unsigned *status, cudaStream_t st) {
+    if (ln.x && !dense_ln_supported(M, N, K))
+        return cudaErrorInvalidValue;
+    if (o.stats && N % 128)
+        return cudaErrorInvalidValue;
+    CUtensorMap ta, tb, tx;
+    // (with ln.x, A's map is encoded but never read; without, x's map is A's)
     cudaError_t e = make_map(&ta, A, M, K, K, 128);
     if (e == cudaSuccess)
         e = make_map(&tb, W, K, N, ldw, 64);
+    if (e == cudaSuccess)
+        e = ln.x ? make_f32_map(&tx, ln.x, M, K, K, 128) : cudaSuccess;
     if (e != cudaSuccess)
         return e;
+    if (!ln.x)
+        tx = ta;
     switch (gemm_slices(M, N, K)) {
-    case 1: return launch_gemm_sl<EPI, 1>(ta, tb, K, M, N, o, w_early, status, st);
-    case 2: return launch_gemm_sl<EPI, 2>(ta, tb, K, M, N, o, w_early, status, st);
-    case 4: return launch_gemm_sl<EPI, 4>(ta, tb, K, M, N, o, w_early, status, st);
-    default: return launch_gemm_sl<EPI, 8>(ta, tb, K, M, N, o, w_early, status, st);
+    case 1: return launch_gemm_sl<EPI, 1>(ta, tb, tx, K, M, N, o, ln, w_early, status, st);
+    case 2: return launch_gemm_sl<EPI, 2>(ta, tb, tx, K, M, N, o, ln, w_early, status, st);
+    case 4: return launch_gemm_sl<EPI, 4>(ta, tb, tx, K, M, N, o, ln, w_early, status, st);
+    default: return launch_gemm_sl<EPI, 8>(ta, tb, tx, K, M, N, o, ln, w_early, status, st);
     }
 }
 
@@ -532,23 +692,25 @@ cudaError_t launch_project(const void *x, const void *Wall, int ldw, void *q, vo
     o.d_key = d_key;
     o.d_v = d_v;
     const int M = B * L, N = H * (2 * d_key + d_v + 1);
-    return launch_gemm_t<kEpiHeads>(x, Wall, ldw, d_model, M, N, o, w_early, status, st);
+    return launch_gemm_t<kEpiHeads>(x, Wall, ldw, d_model, M, N, o, DenseLn{}, w_early, status, st);
 }
 
 cudaError_t launch_dense(const void *A, const void *W, int K, int M, int N, const float *bias, const float *resid,
-                         void *out, bool relu, void *out_bf16_copy, bool w_early, unsigned *status,
-                         cudaStream_t st) {
+                         void *out, bool relu, void *out_bf16_copy, bool w_early, float2 *stats, const DenseLn *ln,
+                         unsigned *status, cudaStream_t st) {
     GemmOut o = {};
     o.bias = bias;
     o.resid = resid;
     o.ldo = N;
+    const DenseLn lnv = ln ? *ln : DenseLn{};
     if (relu) {
         o.out_bf16 = static_cast<__nv_bfloat16 *>(out);
-        return launch_gemm_t<kEpiBiasRelu>(A, W, N, K, M, N, o, w_early, status, st);
+        return launch_gemm_t<kEpiBiasRelu>(A, W, N, K, M, N, o, lnv, w_early, status, st);
     }
     o.out_f32 = static_cast<float *>(out);
     o.out_bf16 = static_cast<__nv_bfloat16 *>(out_bf16_copy);
-    return launch_gemm_t<kEpiBiasResid>(A, W, N, K, M, N, o, w_early, status, st);
+    o.stats = stats;
+    return launch_gemm_t<kEpiBiasResid>(A, W, N, K, M, N, o, lnv, w_early, status, st);
 }
 
 } // namespace fw

@@ -131,7 +131,8 @@ StackLayout stack_layout(int B, int H, int d_key, int d_v, int d_model, int d_ff
     p.h = up256(p.z + (size_t)B * d_model * 2);
     p.x = up256(p.h + (size_t)B * d_ff * 2);
     p.x16 = up256(p.x + (size_t)B * d_model * 4);
-    p.bytes = up256(p.x16 + (size_t)B * d_model * 2);
+    p.stats = up256(p.x16 + (size_t)B * d_model * 2);
+    p.bytes = up256(p.stats + (size_t)B * (d_model / 128 + 1) * 8);
     return p;
 }
 
@@ -143,6 +144,11 @@ cudaError_t stack_step_launch(const fw_stack_layer *layers, int n_layers, const 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *xr = reinterpret_cast<float *>(ws + pl.x);
     void *x16 = ws + pl.x16;
+    // each layer's norm folded into its first feed-forward map: the output
+    // map leaves the statistics of x's rows, and the feed-forward GEMM forms
+    // its A = LN(x) itself (else a LayerNorm kernel between the two)
+    const bool ln_fused = d_model % 128 == 0 && dense_ln_supported(B, d_ff, d_model);
+    float2 *stats = reinterpret_cast<float2 *>(ws + pl.stats);
     cudaError_t e = cudaSuccess;
     if (n_layers > 0) {
         const int64_t n8 = (int64_t)B * d_model / 8;
@@ -158,15 +164,18 @@ cudaError_t stack_step_launch(const fw_stack_layer *layers, int n_layers, const 
             e = launch_decode(ws + pl.q, ws + pl.k, ws + pl.v, ws + pl.beta, ly.W, ws + pl.y, B * H, d_key, nu, d_v,
                               1, eps, num_sms, st);
         if (e == cudaSuccess) // x <- x + y W_o + b_o
-            e = launch_dense(ws + pl.y, ly.W_o, H * d_v, B, d_model, ly.b_o, xin, xr, false, nullptr, true, status,
-                             st);
-        if (e == cudaSuccess)
+            e = launch_dense(ws + pl.y, ly.W_o, H * d_v, B, d_model, ly.b_o, xin, xr, false, nullptr, true,
+                             ln_fused ? stats : nullptr, nullptr, status, st);
+        if (e == cudaSuccess && !ln_fused)
             e = launch_layernorm(xr, ly.ln_gamma, ly.ln_beta, ws + pl.z, true, B, d_model, ln_eps, st);
-        if (e == cudaSuccess) // hidden = relu(LN(x) W_1 + b_1)
+        if (e == cudaSuccess) { // hidden = relu(LN(x) W_1 + b_1)
+            const DenseLn ln = {xr, stats, ly.ln_gamma, ly.ln_beta, ln_eps, d_model / 128};
             e = launch_dense(ws + pl.z, ly.W_1, d_model, B, d_ff, ly.b_1, nullptr, ws + pl.h, true, nullptr, true,
-                             status, st);
+                             nullptr, ln_fused ? &ln : nullptr, status, st);
+        }
         if (e == cudaSuccess) // x <- x + hidden W_2 + b_2, and its bf16 copy for the next projection
-            e = launch_dense(ws + pl.h, ly.W_2, d_ff, B, d_model, ly.b_2, xr, xr, false, x16, true, status, st);
+            e = launch_dense(ws + pl.h, ly.W_2, d_ff, B, d_model, ly.b_2, xr, xr, false, x16, true, nullptr, nullptr,
+                             status, st);
     }
     if (e == cudaSuccess)
         e = launch_layernorm(n_layers ? xr : x, ln_gamma, ln_beta, out, false, B, d_model, ln_eps, st);
