@@ -262,8 +262,8 @@ __global__ void __launch_bounds__(kProjThreads)
     uint64_t *done = empty + kStages;              // every MMA is done
     uint64_t *rx = done + 1;                       // SL > 1: the other slices' rows have landed
     uint64_t *sent = rx + 1;                       // SL > 1: every rank has received this slice's rows
-    uint64_t *xbar = sent + 1;                     // ln.x: x's tiles have landed
-    uint32_t *slot = (uint32_t *)(xbar + 1);
+    uint64_t *xbar = sent + 1;                     // [2] ln.x: x's tile of stage i has landed
+    uint32_t *slot = (uint32_t *)(xbar + 2);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int m0 = blockIdx.x * 128, n0 = blockIdx.y * 128, z = blockIdx.z;
     const int nk = K / 64, kb0 = z * per, nkl = max(0, min(nk, kb0 + per) - kb0);
@@ -281,6 +281,7 @@ __global__ void __launch_bounds__(kProjThreads)
         mbar_init(rx, 1);
         mbar_init(sent, SL > 1 ? SL - 1 : 1);
         mbar_init(xbar, 1);
+        mbar_init(xbar + 1, 1);
         fence_barrier_init();
         if (SL > 1) // armed before the cluster barrier that precedes any sender's copy
             mbar_arrive_expect_tx(rx, (uint32_t)(SL - 1) * kRowsBytes);
@@ -321,11 +322,11 @@ __global__ void __launch_bounds__(kProjThreads)
         // stored in bf16 into the stage's K-major 128-byte-swizzled layout.
         const float2 *stats = after_wait(ln.stats);
         float *mst = reinterpret_cast<float *>(smem + kLnOff); // [128] means, then [128] 1 / sigma
-        if (tid == 0) {
-            mbar_arrive_expect_tx(xbar, (uint32_t)nkl * 32768u);
-            for (int i = 0; i < nkl; ++i)
-                tma_load_2d(smem + (2 + i) * kStageBytes, &tx, 64 * (kb0 + i), m0, xbar);
-        }
+        if (tid == 0)
+            for (int i = 0; i < nkl; ++i) {
+                mbar_arrive_expect_tx(xbar + i, 32768u);
+                tma_load_2d(smem + (2 + i) * kStageBytes, &tx, 64 * (kb0 + i), m0, xbar + i);
+            }
         {
             const int m = m0 + tid;
             float mean = 0.f, rstd = 0.f;
@@ -342,10 +343,11 @@ __global__ void __launch_bounds__(kProjThreads)
             mst[tid] = mean;
             mst[128 + tid] = rstd;
         }
-        const bool xin = mbar_wait(xbar, 0, status); // (a timeout leaves A as it is: the status reports it)
         __syncthreads();
         const int cq = lane & 15, rsel = lane >> 4; // the lane's 4 columns of a stage; which of the 2 rows
         for (int i = 0; i < nkl; ++i) {
+            // (a timeout leaves this stage's A zero: the status word reports it)
+            const bool xin = mbar_wait(xbar + i, 0, status);
             uint8_t *a = smem + i * kStageBytes;
             const float *xs = reinterpret_cast<const float *>(smem + (2 + i) * kStageBytes); // [128][64]
             const int k = 64 * (kb0 + i) + 4 * cq;
