@@ -187,8 +187,9 @@ FW_API size_t fw_delta_forward_projected_workspace_size(int B, int L, int d_mode
  * (each chunk's prep computes its own rows of q, k, v and beta from x with
  * TMA-fed tensor-core MMAs; they never reach global memory), then the walk
  * over the chunks: two launches from x.  Otherwise the projections' GEMM
- * (with a reduction kernel after it when B L is small and K is split across
- * CTAs) writes q, k, v, beta to the workspace and fw_delta_forward follows.
+ * (when B L is small, K is split across the CTAs of a thread-block cluster,
+ * which add their partial tiles in the same kernel) writes q, k, v, beta to
+ * the workspace and fw_delta_forward follows.
  * Launches are chained by programmatic dependent launch.
  */
 FW_API int fw_delta_forward_projected(const void *x, const void *W_all, int ldw, const float *W0,
@@ -413,10 +414,13 @@ FW_API size_t fw_decode_stack_workspace_size(int B, int H, int d_key, int d_v, i
  * x += relu(LN(x) W_1 + b_1) W_2 + b_2.  The residual stream x is fp32;
  * what the tensor cores read (x, y, LN(x), the hidden layer) is rounded to
  * bf16 and every product accumulates in fp32.  Six operations per layer
- * plus a cast and the final norm, each one kernel, or two when a dense
- * layer's K is split across CTAs (a reduction kernel follows): 10 n_layers
- * + 2 kernels at the 256-sequence, d_model 512 shape; all on `stream`,
- * chained by programmatic dependent launch (capturable in one CUDA graph).
+ * plus a cast and the final norm.  A dense layer whose K is split across
+ * CTAs adds the slices inside its kernel, and where the first feed-forward
+ * map's K slices are at most two steps of 64 (as at the 256-sequence,
+ * d_model 512 shape), that GEMM forms LN(x) itself from statistics the
+ * output map leaves: 5 n_layers + 2 kernels there, else 6 n_layers + 2; all
+ * on `stream`, chained by programmatic dependent launch (capturable in one
+ * CUDA graph).
  * Errors: FW_ERR_INVALID_ARG for bad sizes, NULL or unaligned pointers, a
  * small workspace; FW_ERR_UNSUPPORTED for d_key outside {8, 16, 32, 64, 128},
  * d_dot > 1024, d_model not a multiple of 128 or above 1024, H d_v or d_ff
