@@ -330,14 +330,17 @@ __global__ void __launch_bounds__(kProjThreads)
         {
             const int m = m0 + tid;
             float mean = 0.f, rstd = 0.f;
-            if (m < M) {
-                const float2 s0 = __ldcg(stats + (size_t)m * ln.parts);
-                mean = s0.x;
-                float m2 = s0.y;
-                for (int p = 1; p < ln.parts; ++p) {
-                    const float2 sp = __ldcg(stats + (size_t)m * ln.parts + p);
-                    chan_combine(mean, m2, 128.f * p, sp.x, sp.y, 128.f);
-                }
+            if (m < M) { // every part's load in flight first (parts <= 8: K <= 1024)
+                float2 sp[8];
+#pragma unroll
+                for (int p = 0; p < 8; ++p)
+                    sp[p] = p < ln.parts ? __ldcg(stats + (size_t)m * ln.parts + p) : make_float2(0.f, 0.f);
+                mean = sp[0].x;
+                float m2 = sp[0].y;
+#pragma unroll
+                for (int p = 1; p < 8; ++p)
+                    if (p < ln.parts)
+                        chan_combine(mean, m2, 128.f * p, sp[p].x, sp[p].y, 128.f);
                 rstd = rsqrtf(m2 / (128.f * ln.parts) + ln.eps);
             }
             mst[tid] = mean;
@@ -625,7 +628,8 @@ size_t project_smem_bytes() { return (size_t)kLnOff + 1024 + 1024; }
 
 bool dense_ln_supported(int M, int N, int K) {
     const int nk = K / 64, sl = gemm_slices(M, N, K);
-    return K % 128 == 0 && (nk + sl - 1) / sl <= 2; // x's tiles fill the ring's stages 2 and 3
+    // x's tiles fill the ring's stages 2 and 3; a row has at most 8 parts
+    return K % 128 == 0 && K <= 1024 && (nk + sl - 1) / sl <= 2;
 }
 
 template <int EPI, int SL>
