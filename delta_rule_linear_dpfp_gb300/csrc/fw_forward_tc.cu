@@ -1749,10 +1749,16 @@ cudaError_t prep_dispatch(const PrepArgs &a, int BH, int d_key, int num_sms, cud
 
 // The scan of the delta rule or of the unnormalised sum rule: 16 channels
 // per CTA (128 threads) where those CTAs fit on the GPU at once, else 32
-// (256 threads: half as many CTAs for the same per-chunk time).  `wide`
-// forces 32, as the single-launch forward uses, so that the standalone
-// phases of a shape that forward takes give the same bits.
+// (256 threads: half as many CTAs for the same per-chunk time), and 64 (256
+// threads, each with 32 columns) where even the 32-channel CTAs would take
+// more than one wave: a chunk step's MMAs cost about the same for N = 64 and
+// the read-outs double, so one wave of 64-channel CTAs beats two of 32
+// (b16h8_l2048_nu3: 156 -> 118 us).  `wide` forces 32, as the single-launch
+// forward uses, so that the standalone phases of a shape that forward takes
+// give the same bits.
 cudaError_t scan_dispatch(const ScanArgs &a, int BH, int num_sms, bool wide, cudaStream_t st) {
+    if (!wide && a.d_v % 64 == 0 && (long long)BH * (a.d_v / 32) > num_sms)
+        return launch_scan_bufs<64, 256, false>(a, BH, st);
     if (wide_scan(a.d_v) && (wide || (long long)BH * (a.d_v / 16) > num_sms))
         return launch_scan_bufs<32, 256, false>(a, BH, st);
     return launch_scan_bufs<16, 128, false>(a, BH, st);

@@ -105,6 +105,7 @@ EDGE = [
     (1, 2, 150, 64, 3, 128, 64, "bf16", True),    # bf16 at the largest padded d_dot + d_v (384 + 128)
     (2, 2, 90, 128, 1, 128, 64, "bf16", False),   # d_key 128, d_v 128
     (3, 1, 64, 8, 1, 16, 16, "bf16", True),       # the smallest d_key and d_v, exactly one chunk
+    (20, 8, 200, 64, 1, 128, 64, "bf16", True),   # 64-channel walks (32-channel ones would outnumber the SMs), ragged
 ]
 
 
