@@ -358,9 +358,11 @@ def run_ours(args, rank, world, local_rank):
     # CUDA graph that is then replayed (the copy streams fork from and join
     # the capture stream; every replay still copies in, computes and copies
     # out each of its steps), which takes the host's Python out of the loop.
-    E2E_GRAPH = 8
-    # as many end-to-end steps as timed steps (rounded up to whole graphs)
-    e2e_steps = max(E2E_GRAPH, (args.steps + E2E_GRAPH - 1) // E2E_GRAPH * E2E_GRAPH)
+    E2E_GRAPH = 32  # steps per replayed graph: the copy-in and copy-out at a replay boundary overlap nothing
+    # as many end-to-end steps as timed steps; the graph form replays whole
+    # graphs, so it covers that many rounded up to whole graphs
+    e2e_steps = args.steps
+    e2e_graph_steps = max(E2E_GRAPH, (args.steps + E2E_GRAPH - 1) // E2E_GRAPH * E2E_GRAPH)
     for i in range(4):                          # warm up
         e2e_step(i, stream)
     barrier()
@@ -394,12 +396,12 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(e2e_steps // E2E_GRAPH):
+    for _ in range(e2e_graph_steps // E2E_GRAPH):
         graph.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_graph_steps, world, dev)
     clk = clocks.stop()
     # the last step's results came back intact
     y_back = views(h_out[(E2E_GRAPH - 1) & 1], out_offs, out_sd)[0]
@@ -449,7 +451,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": {"value": tokens_per_step * world / (e2e_eager_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_eager_ms,
-                "steps": e2e_steps,
+                "steps": e2e_steps, "graph_steps": e2e_graph_steps,
                 "graph_value": tokens_per_step * world / (e2e_ms * 1e-3), "graph_ms_per_step": e2e_ms,
                 "how": f"pinned host buffers (rotating over {E2E_HOST_SETS} distinct input sets); per step one "
                        f"packed copy in ({', '.join(names)}), fw_delta_forward through the C ABI, one packed "
