@@ -217,7 +217,7 @@ namespace {
 struct ProjLayout {
     size_t q, k, v, beta, fwd, bytes;
 };
-ProjLayout proj_layout(int B, int L, int d_model, int H, int d_key, int d_v, size_t fwd_bytes) {
+ProjLayout proj_layout(int B, int L, int H, int d_key, int d_v, size_t fwd_bytes) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t tok = (size_t)B * H * L;
     ProjLayout p;
@@ -237,7 +237,7 @@ FW_API size_t fw_delta_forward_projected_workspace_size(int B, int L, int d_mode
     if (d_model <= 0 || d_model % 64 || H <= 0 || check_forward_shape(B, H, L, d_key, nu, d_v, chunk,
                                                                       FW_DTYPE_BF16) != FW_OK)
         return 0;
-    return proj_layout(B, L, d_model, H, d_key, d_v, fw::tc_forward_workspace_bytes(B, H, L, d_key, nu, d_v, chunk))
+    return proj_layout(B, L, H, d_key, d_v, fw::tc_forward_workspace_bytes(B, H, L, d_key, nu, d_v, chunk))
         .bytes;
 }
 
@@ -271,7 +271,7 @@ FW_API int fw_delta_forward_projected(const void *x, const void *W_all, int ldw,
     if (!x || !W_all || !y || !aligned16(x) || !aligned16(W_all) || !aligned16(y))
         return FW_ERR_INVALID_ARG;
     const ProjLayout pl =
-        proj_layout(B, L, d_model, H, d_key, d_v, fw::tc_forward_workspace_bytes(B, H, L, d_key, nu, d_v, chunk));
+        proj_layout(B, L, H, d_key, d_v, fw::tc_forward_workspace_bytes(B, H, L, d_key, nu, d_v, chunk));
     if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes)
         return FW_ERR_INVALID_ARG;
     DeviceInfo di;
