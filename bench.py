@@ -441,9 +441,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: B{B} H{H} L{L} d_key{d_key} nu{nu} (d_dot {d_dot}) d_v{d_v} "
-                               f"bf16 I/O, fp32 state, chunk {C}, "
-                               f"{'W0 ~ N(0, 0.01) in' if has_w0 else 'W0 = 0'}, y and W_final out",
+        "config": {"workload": workload_name(inputs.FORWARD_CONFIGS[WORKLOAD]),
+                   "io": "bf16 in and out, fp32 state",
                    "global_batch": B * world, "seq_len": L,
                    "parallelism": "replicas" if world == 1 else f"replicas x{world}",
                    "l2": f"inputs rotate over {nsets} sets ({nsets * set_bytes / 2**20:.0f} MiB "
@@ -775,19 +774,27 @@ def projected_only(steps):
     print(json.dumps({"projected_steps": steps}))
 
 
+def workload_name(cfg):
+    """The bench workload as both arms name it in their config."""
+    d_dot = 2 * cfg["d_key"] * cfg["nu"]
+    w0 = f"W0 ~ N(0, {cfg['w0_var']}) in" if cfg.get("w0_var") else "W0 = 0"
+    return (f"{WORKLOAD}: B{cfg['B']} H{cfg['H']} L{cfg['L']} d_key{cfg['d_key']} nu{cfg['nu']} "
+            f"(d_dot {d_dot}) d_v{cfg['d_v']}, chunk {cfg['chunk']}, {w0}, y and W_final out")
+
+
 # ------------------------------------------------------------ the oracle
 class OracleSample:
     """The fp64 CPU oracle on the host cores over a bounded sample of the
     workload: whole (b,h) sequences when the time budget allows several, else
     the first tokens of one sequence.  Inputs are drawn and widened once."""
 
-    def __init__(self, B, H, L, d_key, nu, d_v, io, seed=0):
+    def __init__(self, B, H, L, d_key, nu, d_v, io, w0_var=None, seed=0):
         import numpy as np
 
         import oracle
         from delta_rule_linear_dpfp_gb300 import inputs
         self.oracle, self.np = oracle, np
-        d = inputs.random_forward_inputs(B, H, L, d_key, nu, d_v, io, None, seed)
+        d = inputs.random_forward_inputs(B, H, L, d_key, nu, d_v, io, w0_var, seed)
         flat = lambda t: np.ascontiguousarray(
             t.float().double().numpy().reshape((1, B * H) + tuple(t.shape[2:])))
         self.f = {k: flat(v) for k, v in d.items() if v is not None}
@@ -800,7 +807,8 @@ class OracleSample:
     def _run(self, pairs, tokens, threads):
         f = self.f
         sl = lambda a: self.np.ascontiguousarray(a[:, :pairs, :tokens])
-        self.oracle.delta_forward(sl(f["q"]), sl(f["k"]), sl(f["v"]), sl(f["beta"]), None, self.nu,
+        W0 = self.np.ascontiguousarray(f["W0"][:, :pairs]) if "W0" in f else None
+        self.oracle.delta_forward(sl(f["q"]), sl(f["k"]), sl(f["v"]), sl(f["beta"]), W0, self.nu,
                                   1e-6, threads)
 
     def plan(self, budget_s, threads):
@@ -828,7 +836,7 @@ def run_reference(args, rank, world):
     cfg = inputs.FORWARD_CONFIGS[WORKLOAD]
     B, H, L, d_key, nu, d_v = (cfg[n] for n in ("B", "H", "L", "d_key", "nu", "d_v"))
     budget = max(0.002, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
-    orc = OracleSample(B, H, L, d_key, nu, d_v, cfg["io"])
+    orc = OracleSample(B, H, L, d_key, nu, d_v, cfg["io"], cfg.get("w0_var"))
     for _ in range(args.warmup):
         orc.measure(budget)
     tok, secs = 0.0, 0.0
@@ -842,7 +850,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: B{B} H{H} L{L} d_key{d_key} nu{nu} d_v{d_v}",
+        "config": {"workload": workload_name(cfg), "io": "fp64 throughout (the oracle)",
                    "global_batch": B, "seq_len": L, "parallelism": "host cores"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
@@ -881,7 +889,7 @@ def main():
             from delta_rule_linear_dpfp_gb300 import inputs
             cfg = inputs.FORWARD_CONFIGS[WORKLOAD]
             orc = OracleSample(cfg["B"], cfg["H"], cfg["L"], cfg["d_key"], cfg["nu"], cfg["d_v"],
-                               cfg["io"])
+                               cfg["io"], cfg.get("w0_var"))
             v, cores, sample, _ = orc.measure(12.0)
             v1, _, sample1, _ = orc.measure(6.0, max_threads=1)
             res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
