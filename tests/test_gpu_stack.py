@@ -67,6 +67,11 @@ SMALL = [  # B, H, d_key, nu, d_v, d_model, d_ff, n_layers
     (5, 2, 16, 2, 32, 128, 192, 3),      # a ragged row tile (5 of 128 rows), d_dot 64
     (130, 4, 32, 1, 16, 256, 320, 2),    # two row tiles, the second ragged; d_ff not a multiple of 128
     (3, 1, 64, 3, 64, 128, 64, 1),       # nu 3 (d_dot 384)
+    # The cases above fold the LayerNorm into the first feed-forward map.  Below, a CTA of that map
+    # would hold 4 K steps of 64 (more than its ring leaves room for beside the fp32 rows of x), so
+    # the norm runs as its own kernel between the output map and the feed-forward block:
+    (640, 2, 32, 1, 64, 256, 2048, 1),   # 80 output tiles: K not split
+    (256, 4, 64, 1, 64, 1024, 2432, 1),  # d_model 1024, 38 output tiles: K in 4 slices of 4 steps
 ]
 
 
