@@ -54,6 +54,20 @@ MUTANTS = {
     "backward_normaliser_term_dropped": ("const double gp = gphi[m] / (s + eps) - gp_dot_p / ((s + eps) * (s + eps));",
                                          "const double gp = gphi[m] / (s + eps);"),
     "backward_roll_partner_dropped": ("            gx[src] += gp * x[j];\n", "\n"),
+    "backward_roll_partner_wrong": ("gx[j] += gp * x[src];", "gx[j] += gp * x[j];"),
+    "backward_beta_grad_drops_retrieve": ("gb += gu[r] * (v[t * d_v + r] - a[t * d_v + r]);",
+                                          "gb += gu[r] * v[t * d_v + r];"),
+    "backward_value_grad_drops_beta": ("gv[t * d_v + r] = beta[t] * gu[r];", "gv[t * d_v + r] = gu[r];"),
+    "backward_readout_grad_with_key": ("gW[(size_t)r * d_dot + m] += gy[t * d_v + r] * pqt[m];",
+                                       "gW[(size_t)r * d_dot + m] += gy[t * d_v + r] * pkt[m];"),
+    "backward_final_state_grad_ignored": ("gW[e] = gWL ? gWL[e] : 0.0;", "gW[e] = 0.0;"),
+    "backward_minus_k_branch_sign": ("gk[j] = (k[j] > 0.0 ? gx[j] : 0.0) - (-k[j] > 0.0 ? gx[d_key + j] : 0.0);",
+                                     "gk[j] = (k[j] > 0.0 ? gx[j] : 0.0) + (-k[j] > 0.0 ? gx[d_key + j] : 0.0);"),
+    "backward_key_grad_with_new_state": ("- Wp[(size_t)r * d_dot + m] * beta[t] * gu[r];",
+                                         "- Wn[(size_t)r * d_dot + m] * beta[t] * gu[r];"),
+    # the DPFP map: the shift off by one (block 1 = x * x), the normaliser over block 1 only
+    "dpfp_shift_off_by_one": ("int src = ((j - i) % n + n) % n;", "int src = ((j - i + 1) % n + n) % n;"),
+    "dpfp_sum_over_first_block": ("            s += p;\n", "            s += (i == 1) ? p : 0.0;\n"),
 }
 
 
