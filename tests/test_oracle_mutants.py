@@ -97,3 +97,46 @@ def test_mutant_is_caught(tmp_path, name):
         except (AssertionError, ValueError, FloatingPointError):
             failed.append(getattr(pin, "__name__", "chunked"))
     assert failed, f"no pin caught the planted mistake '{name}'"
+
+
+# The projections (oracle.project, numpy): each mutant is the function's own
+# source with one textual change, executed in the oracle module's namespace
+# and put in its place for the projection pin.
+PROJECTION_MUTANTS = {
+    "beta_sigmoid_sign": ("np.exp(-P[", "np.exp(P["),
+    "heads_split_feature_major": ("a.reshape(B, L, H, d).transpose(0, 2, 1, 3)",
+                                  "a.reshape(B, L, d, H).transpose(0, 3, 1, 2)"),
+    "query_and_key_swapped": ("q = heads(P[..., :nq], d_key)\n    k = heads(P[..., nq:2 * nq], d_key)",
+                              "k = heads(P[..., :nq], d_key)\n    q = heads(P[..., nq:2 * nq], d_key)"),
+    "value_from_the_key_block": ("v = heads(P[..., 2 * nq:2 * nq + nv], d_v)", "v = heads(P[..., nq:nq + nv], d_v)"),
+    "beta_from_the_first_columns": ("P[..., 2 * nq + nv:2 * nq + nv + H]", "P[..., 0:H]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PROJECTION_MUTANTS))
+def test_projection_mutant_is_caught(monkeypatch, name):
+    import inspect
+    import textwrap
+
+    import oracle
+    old, new = PROJECTION_MUTANTS[name]
+    src = textwrap.dedent(inspect.getsource(oracle.project))
+    assert src.count(old) == 1, f"mutation anchor for {name} not found in oracle.project"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), "<mutant>", "exec"), ns)
+    monkeypatch.setattr(oracle, "project", ns["project"])
+    with pytest.raises((AssertionError, ValueError, IndexError)):
+        oracle_pins.pin_projection_selection(None)
+
+
+def test_projection_copy_without_mutation_passes(monkeypatch):
+    """The control for the cases above: the unchanged source, put in place the
+    same way, passes the pin."""
+    import inspect
+    import textwrap
+
+    import oracle
+    ns = dict(vars(oracle))
+    exec(compile(textwrap.dedent(inspect.getsource(oracle.project)), "<copy>", "exec"), ns)
+    monkeypatch.setattr(oracle, "project", ns["project"])
+    oracle_pins.pin_projection_selection(None)
