@@ -35,6 +35,12 @@ MUTANTS = {
                            'return x, x, new_states'),
     "norm_before_attention": ('q, k, v, beta = project(x[:, None, :]',
                               'q, k, v, beta = project(layer_norm(x, None, None, ln_eps)[:, None, :]'),
+    "norm_gamma_dropped": ('        out = out * _f64(gamma)\n', '        out = out * 1.0\n'),
+    "norm_mean_not_subtracted": ('out = (x - mean) / np.sqrt(var + eps)', 'out = x / np.sqrt(var + eps)'),
+    "norm_parameters_swapped": ('layer_norm(x, ly.get("ln_gamma"), ly.get("ln_beta"), ln_eps)',
+                                'layer_norm(x, ly.get("ln_beta"), ly.get("ln_gamma"), ln_eps)'),
+    "hidden_bias_dropped": (' + _bias(ly.get("b_1"))', ''),
+    "second_feed_forward_bias_dropped": (' + _bias(ly.get("b_2"))', ''),
 }
 
 
