@@ -332,8 +332,7 @@ FW_API int fw_delta_forward_scan(const void *workspace, size_t workspace_bytes, 
  *   - The array's device address is looked up (cudaGetSymbolAddress) the
  *     first time this function runs in a context on a device, with that
  *     device current, and kept for that context; a new context on the device
- *     (after cudaDeviceReset, for instance) is looked up afresh.  Make the
- *     first call in a context before any stream capture on the device.
+ *     (after cudaDeviceReset, for instance) is looked up afresh.
  *   - Every call on a device shares the one array, and its contents from the
  *     previous call are left in place (nothing needs them to be zero).  Calls
  *     that may run at the same time on the GPU (different streams without an
