@@ -37,7 +37,7 @@ def test_reference_arm_prints_one_contract_line():
 
 
 def test_reference_arm_under_torchrun_prints_once():
-    """Launched as the driver launches N > 1 (torchrun, two ranks): rank 0
+    """Launched as a run on N > 1 GPUs is launched (torchrun, two ranks): rank 0
     alone runs the oracle and prints the line, the other rank exits 0."""
     import socket
     with socket.socket() as s:
