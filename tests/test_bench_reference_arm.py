@@ -52,3 +52,18 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1, r.stdout
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
+def test_recorded_traffic_belongs_to_the_current_sources():
+    """The DRAM traffic bench.py reports for the headline kernel comes from an
+    ncu capture tied to a hash of the forward's sources; any change to them
+    (a comment included) needs a new capture, else the line reports null."""
+    sys.path.insert(0, ROOT)
+    try:
+        import bench
+        rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+        entry = rec[f"chunk_fused_kernel@{bench.WORKLOAD}"]
+        assert entry["source_hash"] == bench.source_hash(bench.FORWARD_SOURCES)
+        assert entry["dram_bytes_per_launch"] == entry["read"] + entry["write"] > 0
+    finally:
+        sys.path.remove(ROOT)
